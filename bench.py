@@ -1,0 +1,448 @@
+#!/usr/bin/env python3
+"""Benchmark of the decode-FFN weight stream on GB300 (one JSON line on stdout).
+
+Default workload (--workload stack52_m1): one decode token through a 52-layer
+FFN stack of the Muser book's model shape (hidden 6656, FFN 19968).  Per layer:
+input RMSNorm (layer 0 only) -> Q4_K gate/up 19968x6656 with SiLU gating ->
+Q6_K down 6656x19968 with the dual-eps fused tail.  A step streams the 52
+layers' 13.44 GB of distinct weights (far larger than the 129 MB L2).
+`--workload stack52_m16` runs the same stack at M = 16 (speculative verify).
+
+Arms:
+  --impl native     libmuser (CUDA, sm_103a) through its C ABI.
+  --impl reference  the fp64 CPU oracle on the host cores (a bounded row
+                    sample of the same workload per step) -- the only other
+                    place this script runs oracle/ besides the cpu_baseline leg.
+
+Multi-GPU (torchrun): replicas only -- every rank runs the whole workload on
+its own GPU; the value is the sum over ranks, timed by the slowest rank.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import shutil
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+H, F, NL = synth.HIDDEN, synth.FFN, synth.N_LAYERS
+Q4K_MAT = H * (F // 256) * 144          # 74,760,192 B (gate or up; same count as Q4_K down)
+Q6K_MAT = H * (F // 256) * 210          # 109,025,280 B
+LAYER_W = 2 * Q4K_MAT + Q6K_MAT         # 258,545,664 B
+METRIC = "weight-stream GB/s (% of GB300 HBM peak); decode FFN tokens/sec, 1 GPU"
+
+# ncu DRAM traffic of the dominant kernel, per launch, with the source hash it
+# was captured on (profiles/ summary); reported as null once the kernel changed.
+NCU_TRAFFIC = {"kernel": "mv1_kernel<Q4_K,2,silu>", "bytes_per_launch": None, "source_sha256": None,
+               "profile": None}
+
+
+def _env_int(k, d):
+    try:
+        return int(os.environ.get(k, d))
+    except ValueError:
+        return d
+
+
+def algorithmic_bytes(M: int):
+    """Per layer and per kernel: weights read + activations read/written (f32)."""
+    gate_up = 2 * Q4K_MAT + 4 * M * H + 4 * M * F           # Wg, Wu, x in, mid out
+    down_tail = Q6K_MAT + 4 * M * F + 4 * M * H * 5 + 4 * 2 * H  # Wd, mid, proj w, p r, r r/w, out w, w1/w2
+    entry = 4 * M * H * 2 + 4 * H
+    return gate_up, down_tail, entry
+
+
+def read_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as fh:
+            d = json.load(fh)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def source_sha():
+    h = hashlib.sha256()
+    for f in sorted(os.listdir(os.path.join(ROOT, "quantized_weight_streaming_q4_gb300", "csrc"))):
+        with open(os.path.join(ROOT, "quantized_weight_streaming_q4_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str | None):
+        self.proc = None
+        self.gpu_id = gpu_id
+        self.path = None
+
+    def start(self):
+        exe = shutil.which("nvidia-smi")
+        if not exe:
+            return
+        os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+        cmd = [exe, f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100"]
+        if self.gpu_id:
+            cmd += ["-i", self.gpu_id]
+        self.fh = open(self.path, "w")
+        self.proc = subprocess.Popen(cmd, stdout=self.fh, stderr=subprocess.DEVNULL)
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------- native
+class NativeStack:
+    """The workload on the GPU, driven through libmuser's C ABI."""
+
+    def __init__(self, M: int, n_layers: int, seed: int = 0):
+        import torch
+        import quantized_weight_streaming_q4_gb300 as mu
+        self.torch, self.mu, self.M, self.nl = torch, mu, M, n_layers
+        self.L = mu.lib()
+        wl = 4
+        self.layers = []
+        self.structs = []
+        t0 = time.time()
+        for l in range(n_layers):
+            Ld = synth.ffn_layer(l, H, F, seed=seed, workload=wl)
+            w_next = synth.input_norm_weight(l + 1, H, seed=seed, workload=wl)
+            d = {k: torch.from_numpy(v).cuda() for k, v in Ld.items()}
+            d["w_next"] = torch.from_numpy(w_next).cuda()
+            self.layers.append(d)
+            self.structs.append(mu.FfnLayer(d["Wg"].data_ptr(), d["Wu"].data_ptr(), d["Wd"].data_ptr(),
+                                            d["w1"].data_ptr(), d["w_next"].data_ptr(), mu.MUSER_Q4_K,
+                                            mu.MUSER_Q6_K))
+        self.gen_s = time.time() - t0
+        self.w_in = torch.from_numpy(synth.input_norm_weight(0, H, seed=seed, workload=wl)).cuda()
+        self.r0 = synth.residual_rows(M, H, seed=seed, workload=wl)
+        self.resid = torch.from_numpy(self.r0).cuda()
+        self.out = torch.empty(M, H, dtype=torch.float32, device="cuda")
+        self.x = [torch.empty(M, H, dtype=torch.float32, device="cuda") for _ in range(2)]
+        self.mid = torch.empty(M, F, dtype=torch.float32, device="cuda")
+        self.proj = torch.empty(M, H, dtype=torch.float32, device="cuda")
+        self.scratch = torch.zeros(64, dtype=torch.float32, device="cuda")
+        wsb = mu.muser_ffn_workspace_bytes(H, F, M)
+        self.ws = torch.zeros(wsb // 4 + 64, dtype=torch.float32, device="cuda")
+        self.wsb = wsb
+        self.stream = torch.cuda.current_stream()
+        self.sh = self.stream.cuda_stream
+        self.arr = (mu.FfnLayer * n_layers)(*self.structs)
+        self.launches_per_step = 1 + 2 * n_layers
+
+    def _rc(self, name, rc):
+        if rc != 0:
+            raise RuntimeError(f"{name}: {self.mu.muser_last_error()}")
+
+    def step(self, events=None):
+        """One token (M rows) through every layer, per-layer calls; `events`
+        brackets each gate/up launch (the dominant kernel)."""
+        L, M, sh = self.L, self.M, self.sh
+        self._rc("rms_norm", L.muser_rms_norm(self.resid.data_ptr(), self.w_in.data_ptr(),
+                                              self.x[0].data_ptr(), H, M, 1e-5, sh))
+        x, xn = self.x[0], self.x[1]
+        for l, d in enumerate(self.layers):
+            if events is not None:
+                events[l][0].record(self.stream)
+            self._rc("gate_up", L.muser_ffn_gate_up_silu(12, d["Wg"].data_ptr(), d["Wu"].data_ptr(), F, H,
+                                                         x.data_ptr(), M, self.mid.data_ptr(), sh))
+            if events is not None:
+                events[l][1].record(self.stream)
+            dst = self.out if l == self.nl - 1 else xn
+            self._rc("down_tail", L.muser_qmatvec_residual_dual_rmsnorm(
+                14, d["Wd"].data_ptr(), H, F, self.mid.data_ptr(), M, self.proj.data_ptr(),
+                self.resid.data_ptr(), dst.data_ptr(), d["w1"].data_ptr(), d["w_next"].data_ptr(),
+                1e-8, 1e-5, self.scratch.data_ptr(), 256, sh))
+            if events is not None:
+                events[l][2].record(self.stream)
+            x, xn = xn, x
+
+    def step_public(self):
+        """The same token through the one-call public entry point."""
+        self._rc("ffn_stack", self.L.muser_ffn_stack(
+            self.arr, self.nl, self.w_in.data_ptr(), H, F, self.M, self.resid.data_ptr(),
+            self.out.data_ptr(), 1e-5, 1e-8, self.ws.data_ptr(), self.wsb, self.sh))
+
+
+def run_native(args, rank, world):
+    import torch
+    import quantized_weight_streaming_q4_gb300 as mu
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(_env_int("LOCAL_RANK", 0))
+        dist.init_process_group("nccl")
+    mu.build()
+    M = 16 if args.workload == "stack52_m16" else 1
+    nl = args.layers
+    S = NativeStack(M, nl)
+    gu_bytes, dt_bytes, entry_bytes = algorithmic_bytes(M)
+    step_bytes = nl * (gu_bytes + dt_bytes) + entry_bytes
+    weight_bytes = nl * LAYER_W
+
+    def barrier():
+        torch.cuda.synchronize()
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    # warm-up
+    for _ in range(args.warmup):
+        S.step()
+    barrier()
+
+    uuid = None
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(torch.cuda.current_device()).uuid)
+    except Exception:
+        pass
+    clocks = ClockSampler(uuid)
+    clocks.start()
+    time.sleep(0.3)
+    # one event triple per layer and step, read after the timed region
+    events = [[[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(nl)]
+              for _ in range(args.steps)]
+    barrier()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(S.stream)
+    for k in range(args.steps):
+        S.step(events[k])
+    t_end.record(S.stream)
+    barrier()
+    total_ms = t_start.elapsed_time(t_end)
+    clock = clocks.stop()
+    gu_ms = [ev[l][0].elapsed_time(ev[l][1]) for ev in events for l in range(nl)]
+    dt_ms = [ev[l][1].elapsed_time(ev[l][2]) for ev in events for l in range(nl)]
+    ms = total_ms / args.steps
+    if dist is not None:
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+
+    # e2e: host residual in (pinned), the public call, host output out
+    h_in = torch.from_numpy(S.r0.copy()).pin_memory()
+    h_out = torch.empty(M, H, dtype=torch.float32).pin_memory()
+    for _ in range(max(1, min(3, args.warmup))):
+        S.resid.copy_(h_in, non_blocking=True)
+        S.step_public()
+        h_out.copy_(S.out, non_blocking=True)
+    barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e_steps = args.steps
+    e0.record(S.stream)
+    for _ in range(e_steps):
+        S.resid.copy_(h_in, non_blocking=True)
+        S.step_public()
+        h_out.copy_(S.out, non_blocking=True)
+    e1.record(S.stream)
+    barrier()
+    e2e_ms = e0.elapsed_time(e1) / e_steps
+    if dist is not None:
+        t = torch.tensor([e2e_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    assert np.isfinite(h_out.numpy()).all()
+    status = mu.muser_device_status()
+
+    peak, peak_kind = read_peaks()
+    gu_mean = statistics.mean(gu_ms)
+    dt_mean = statistics.mean(dt_ms)
+    achieved = gu_bytes / (gu_mean * 1e-3) / 1e9
+    traffic = None
+    if NCU_TRAFFIC["bytes_per_launch"] and NCU_TRAFFIC["source_sha256"] == source_sha():
+        traffic = NCU_TRAFFIC["bytes_per_launch"]
+    gbs = world * weight_bytes / (ms * 1e-3) / 1e9
+    result = {
+        "metric": METRIC,
+        "value": round(gbs, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic (seeded; Q4_K/Q6_K fields and activations drawn per the workload recipe)",
+        "config": {
+            "workload": f"decode-FFN stack: {nl} layers x [rms_norm(layer 0) -> Q4_K gate/up {F}x{H} + SiLU "
+                        f"-> Q6_K down {H}x{F} + dual-eps tail], M={M}",
+            "layers": nl, "hidden": H, "ffn": F, "M": M,
+            "weight_bytes_per_step": weight_bytes,
+            "algorithmic_bytes_per_step": step_bytes,
+            "l2": f"inputs larger than L2: {weight_bytes / 1e9:.2f} GB of distinct weights per step vs 129 MB L2",
+            "parallelism": "replicas" if world > 1 else "single GPU",
+        },
+        "tokens_per_s": round(world * M / (ms * 1e-3), 3),
+        "hbm_frac_of_" + peak_kind: round(gbs / world / peak, 4),
+        "roofline": {
+            "bound": "hbm",
+            "kernel": "muser_ffn_gate_up_silu (mv1 Q4_K gate+up, SiLU epilogue)",
+            "achieved": round(achieved, 1),
+            "peak": peak,
+            "peak_kind": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else "fallback 6.8 TB/s",
+            "unit": "GB/s",
+            "frac": round(achieved / peak, 4),
+            "traffic": traffic,
+            "algorithmic_bytes_per_launch": gu_bytes,
+            "mean_launch_us": round(gu_mean * 1e3, 2),
+            "second_kernel": {"name": "muser_qmatvec_residual_dual_rmsnorm (mv1 Q6_K + tail)",
+                              "achieved_gbs": round(dt_bytes / (dt_mean * 1e-3) / 1e9, 1),
+                              "mean_launch_us": round(dt_mean * 1e3, 2),
+                              "algorithmic_bytes_per_launch": dt_bytes},
+        },
+        "e2e": {"value": round(world * weight_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+                "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": 4 * M * H,
+                "d2h_bytes_per_step": 4 * M * H,
+                "api": "muser_ffn_stack (one C call per token) with pinned host residual in / output out"},
+        "gpu_launches": args.steps * S.launches_per_step,
+        "clocks": clock,
+        "device_status": status,
+        "weights_generation_s": round(S.gen_s, 1),
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
+    return result
+
+
+# ------------------------------------------------------------- CPU oracle
+def _oracle_layer_sample(frac_rows: float, seed=0):
+    """A bounded sample of one layer: the first rows of gate/up/down."""
+    wl = 4
+    rg = max(8, int(F * frac_rows))
+    rd = max(8, int(H * frac_rows))
+    Wg = synth.q4k_matrix(F, H, seed=seed, workload=wl, layer=0, tensor=synth.T_GATE)[:rg]
+    Wu = synth.q4k_matrix(F, H, seed=seed, workload=wl, layer=0, tensor=synth.T_UP)[:rg]
+    Wd = synth.q6k_matrix(H, F, seed=seed, workload=wl, layer=0, tensor=synth.T_DOWN)[:rd]
+    return np.ascontiguousarray(Wg), np.ascontiguousarray(Wu), np.ascontiguousarray(Wd), rg, rd
+
+
+def _oracle_step(oracle, Wg, Wu, Wd, rg, rd, x, mid_full):
+    g = oracle.qmatvec("q4_k", Wg, rg, H, x)
+    u = oracle.qmatvec("q4_k", Wu, rg, H, x)
+    oracle.silu_mul(g, u)
+    oracle.qmatvec("q6_k", Wd, rd, F, mid_full)
+    return Wg.nbytes + Wu.nbytes + Wd.nbytes
+
+
+def cpu_baseline(seconds: float, frac_rows: float = 0.125):
+    import oracle
+    Wg, Wu, Wd, rg, rd = _oracle_layer_sample(frac_rows)
+    x = synth.normal((1, H), seed=1)
+    mid = synth.normal((1, F), seed=2)
+    nbytes, t_tot, reps = 0, 0.0, 0
+    while t_tot < seconds or reps < 1:
+        t0 = time.perf_counter()
+        nbytes += _oracle_step(oracle, Wg, Wu, Wd, rg, rd, x, mid)
+        t_tot += time.perf_counter() - t0
+        reps += 1
+    gbs = nbytes / t_tot / 1e9
+    return {"value": round(gbs, 4), "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",
+            "tokens_per_s": round(gbs * 1e9 / (NL * LAYER_W), 6),
+            "sample": f"{reps} passes of the fp64 oracle over the first {frac_rows:.3f} of the rows of "
+                      f"one layer's gate/up/down ({(Wg.nbytes + Wu.nbytes + Wd.nbytes) / 1e6:.1f} MB of "
+                      f"weights), {t_tot:.1f} s"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    import oracle
+    Wg, Wu, Wd, rg, rd = _oracle_layer_sample(args.ref_frac)
+    x = synth.normal((1, H), seed=1)
+    mid = synth.normal((1, F), seed=2)
+    for _ in range(args.warmup):
+        _oracle_step(oracle, Wg, Wu, Wd, rg, rd, x, mid)
+    t0 = time.perf_counter()
+    nbytes = 0
+    for _ in range(args.steps):
+        nbytes += _oracle_step(oracle, Wg, Wu, Wd, rg, rd, x, mid)
+    dt = time.perf_counter() - t0
+    gbs = nbytes / dt / 1e9
+    M = 16 if args.workload == "stack52_m16" else 1
+    sample = (f"each step: fp64 oracle over the first {args.ref_frac:.3f} of the rows of one layer's "
+              f"gate/up/down, {nbytes / args.steps / 1e6:.1f} MB of weights, M=1")
+    return {
+        "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "impl": "reference",
+        "config": {"workload": f"decode-FFN stack: {args.layers} layers, M={M} (bounded row sample per step)",
+                   "layers": args.layers, "hidden": H, "ffn": F, "M": M},
+        "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "kind": "oracle",
+                         "cores": oracle.num_threads(), "sample": sample},
+        "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["native", "reference"], default="native")
+    ap.add_argument("--workload", choices=["stack52_m1", "stack52_m16"], default="stack52_m1")
+    ap.add_argument("--layers", type=int, default=NL)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--ref-frac", type=float, default=0.0625)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    rank, world = _env_int("RANK", 0), _env_int("WORLD_SIZE", 1)
+    if args.impl == "reference":
+        res = run_reference(args, rank, world)
+    else:
+        res = run_native(args, rank, world)
+    if rank == 0 and res is not None:
+        print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    main()

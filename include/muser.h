@@ -1,0 +1,267 @@
+/*
+ * muser.h -- C ABI of libmuser, the GB300 (sm_103a) decode-FFN weight-streaming
+ * library.
+ *
+ * The operations are those of the Muser engine's decode hot path as the book
+ * "How to Write an Inference Engine -- the Muser book" describes it: the
+ * one-token quantized matvec over ggml-style Q4_K / Q6_K super-blocks
+ * (Ch 19 §19.3, §19.5), the FFN gate/up/SiLU step (Ch 10 Figure 10.1 box 11,
+ * §10.3 (d)), the dual-epsilon fused residual tail (Ch 19 §19.4; Ch 10 §10.4
+ * Figure 10.2) and the f16 K/V ring store (Ch 15 §15.4-§15.5).
+ *
+ * Conventions shared by every entry point:
+ *  - Ownership: the caller owns every buffer.  No entry point allocates or
+ *    frees device memory.  Pointers marked "device" must point to memory of
+ *    the current CUDA device; "host" pointers to ordinary host memory.
+ *  - Streams: `stream` is a cudaStream_t (NULL = the legacy default stream).
+ *    Work is enqueued asynchronously on it; nothing synchronises the host
+ *    except muser_sync().
+ *  - Errors: every entry point returns a muser_status.  Arguments are checked
+ *    on the host before anything is launched; on any error nothing is
+ *    launched and no output buffer is touched (the book's fail-closed rule,
+ *    Ch 4 §4.4 and Ch 10 §10.9).  muser_last_error() returns a description of
+ *    the calling thread's most recent error.
+ *  - Types: activations and norm weights are binary32 ("f32"), row-major.
+ *    A quantized matrix W with `rows` outputs and `cols` inputs is stored as
+ *    rows of cols/256 consecutive super-blocks: rows*(cols/256)*block_bytes
+ *    bytes, block_bytes = 144 (Q4_K) or 210 (Q6_K).
+ *  - Alignment: f32 pointers and quantized matrices 16-byte aligned (any
+ *    cudaMalloc/torch allocation is).  Misaligned pointers return
+ *    MUSER_ERR_MISALIGNED.
+ *  - Activation rows: M is the number of activation rows (1 for one-token
+ *    decode, up to MUSER_MAX_M = 16 for the speculative-verify shape,
+ *    Ch 10 §10.1 MAX_DFLASH_BLOCK).
+ */
+#ifndef MUSER_H
+#define MUSER_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MUSER_ABI_VERSION 1
+#define MUSER_MAX_M 16
+
+/* ggml type ids, informational */
+typedef enum { MUSER_Q4_K = 12, MUSER_Q6_K = 14 } muser_qtype;
+
+typedef enum {
+    MUSER_OK = 0,
+    MUSER_ERR_INVALID_ARG = -1,        /* a size, count or pointer is invalid */
+    MUSER_ERR_UNSUPPORTED = -2,        /* quant type or shape the library does not handle */
+    MUSER_ERR_MISALIGNED = -3,         /* a pointer breaks the alignment rule above */
+    MUSER_ERR_CACHE_DISCONTINUITY = -4,/* KV append at a position other than origin_logical+len */
+    MUSER_ERR_CUDA = -5,               /* a CUDA runtime call or launch failed */
+    MUSER_ERR_TIMEOUT = -6             /* muser_sync gave up before the stream drained */
+} muser_status;
+
+/* ABI version (MUSER_ABI_VERSION of the built library). */
+int muser_version(void);
+
+/* Description of the calling thread's last error ("" if none).  The string
+ * stays valid until the next failing call on the same thread. */
+const char* muser_last_error(void);
+
+/* Bytes of one super-block of `qtype` (144, 210; 0 if unknown). */
+size_t muser_block_bytes(int qtype);
+
+/* Bytes of a rows x cols matrix of `qtype` (0 if cols % 256 != 0 or the type
+ * is unknown). */
+size_t muser_matrix_bytes(int qtype, int64_t rows, int64_t cols);
+
+/*
+ * muser_dequantize -- out[r*cols + k] = the binary32 value of weight (r, k).
+ *   Q4_K: d*scale_j*q - dmin*min_j of sub-block j = k%256/32; Q6_K:
+ *   d*scale_s*(q-32) of sub-block s = k%256/16 (block layouts: Ch 19 §19.3,
+ *   ggml super-block bit positions).  Each value is the exactly rounded
+ *   binary32 of that expression; this is the bit-exact test hook of the
+ *   path (the matvec kernels never materialise these values).
+ *   W: device, rows x cols matrix; out: device f32 [rows*cols].
+ */
+int muser_dequantize(int qtype, const void* W, int64_t rows, int64_t cols, float* out,
+                     void* stream);
+
+/*
+ * muser_qmatvec -- y[m*rows + r] = sum_k w(r,k) * x[m*cols + k], m < M
+ *   (Ch 19 §19.1 operation 1; the decode projection of Ch 1).  Weights are
+ *   dequantised in registers straight from HBM; sums are binary32.
+ *   W: device matrix; x: device f32 [M*cols]; y: device f32 [M*rows].
+ *   1 <= M <= 16, cols % 256 == 0, rows >= 1.  x and y must not overlap.
+ */
+int muser_qmatvec(int qtype, const void* W, int64_t rows, int64_t cols, const float* x, int M,
+                  float* y, void* stream);
+
+/*
+ * muser_rms_norm -- out[m*n+i] = w[i] * x[m*n+i] / sqrt(mean_i(x[m*n+i]^2) + eps)
+ *   (Ch 2 §2.6 rms_norm_batch; the layer-0 input norm of Ch 10 Figure 10.1).
+ *   x, out: device f32 [M*n] (may alias); w: device f32 [n].  n % 4 == 0,
+ *   eps > 0, 1 <= M.
+ */
+int muser_rms_norm(const float* x, const float* w, float* out, int n, int M, float eps,
+                   void* stream);
+
+/*
+ * muser_silu_mul -- out[i] = silu(a[i]) * b[i], silu(z) = z/(1+exp(-z))
+ *   (muser_silu_mul_inplace, Ch 10 Figure 10.1 box 11).  Device f32 arrays of
+ *   n elements; out may alias a or b.
+ */
+int muser_silu_mul(const float* a, const float* b, float* out, int64_t n, void* stream);
+
+/*
+ * muser_ffn_gate_up_silu -- mid[m*ffn + r] = silu(g) * u with
+ *   g = sum_k wg(r,k) x[m*hidden+k] and u = sum_k wu(r,k) x[m*hidden+k]
+ *   (both binary32), computed in one pass that streams both matrices
+ *   (the book's opt-in ffn_q4k_gate_up_silu fusion, Ch 10 §10.3 (d)).
+ *   Wg, Wu: device matrices [ffn x hidden] of `qtype`; x: device f32
+ *   [M*hidden]; mid: device f32 [M*ffn].
+ */
+int muser_ffn_gate_up_silu(int qtype, const void* Wg, const void* Wu, int64_t ffn,
+                           int64_t hidden, const float* x, int M, float* mid, void* stream);
+
+/*
+ * muser_fused_residual_dual_rmsnorm -- the dual-eps tail (Ch 19 §19.4,
+ *   muser_fused_norm_residual_rms_norm_32sg; Ch 10 Figure 10.2), per row m:
+ *     residual += w1 * src / sqrt(mean(src^2) + eps1)      (in place)
+ *     out       = w2 * residual / sqrt(mean(residual^2) + eps2)
+ *   The updated residual is stored as binary32 and the second norm reads the
+ *   stored value (the book's device-memory rounding point, §19.7).
+ *   residual: device f32 [M*n] in/out; src, out: device f32 [M*n]; w1, w2:
+ *   device f32 [n].  n % 4 == 0; eps1, eps2 > 0; out must not alias
+ *   residual or src.
+ */
+int muser_fused_residual_dual_rmsnorm(float* residual, const float* src, float* out,
+                                      const float* w1, const float* w2, int n, int M, float eps1,
+                                      float eps2, void* stream);
+
+/* Scratch bytes muser_qmatvec_residual_dual_rmsnorm needs (a small constant). */
+size_t muser_scratch_bytes(int64_t hidden, int M);
+
+/*
+ * muser_qmatvec_residual_dual_rmsnorm -- the layer exit of Ch 19 §19.5 in one
+ *   call: projected = W_down . mid (binary32, written to `projected`), then
+ *   the dual-eps tail above with src = projected.
+ *   Wdown: device matrix [hidden x ffn]; mid: device f32 [M*ffn];
+ *   projected: device f32 [M*hidden] (output); residual: device f32
+ *   [M*hidden] in/out; out: device f32 [M*hidden]; w1, w2: device f32
+ *   [hidden].
+ *   scratch: device memory of at least muser_scratch_bytes(hidden, M) bytes,
+ *   16-byte aligned, owned by the caller, zero-filled before its first use;
+ *   every successful call leaves it zero-filled again.  One scratch buffer
+ *   must not be used by two calls that can run at the same time.
+ */
+int muser_qmatvec_residual_dual_rmsnorm(int qtype, const void* Wdown, int64_t hidden, int64_t ffn,
+                                        const float* mid, int M, float* projected,
+                                        float* residual, float* out, const float* w1,
+                                        const float* w2, float eps1, float eps2, void* scratch,
+                                        size_t scratch_bytes, void* stream);
+
+/*
+ * One decode-FFN layer's parameters (Ch 10 Figure 10.1 boxes 11-13): gate and
+ * up [ffn x hidden], down [hidden x ffn], the post-FFN norm weight (w1, eps1)
+ * and the next norm's weight (w2, eps2): the next layer's input norm, or the
+ * output norm after the last layer (§10.3 (c)).  All pointers are device
+ * pointers; the struct itself is host memory.
+ */
+typedef struct {
+    const void* w_gate;
+    const void* w_up;
+    const void* w_down;
+    const float* post_norm;
+    const float* next_norm;
+    int32_t gate_up_qtype;
+    int32_t down_qtype;
+} muser_ffn_layer;
+
+/* Bytes of workspace muser_ffn_block / muser_ffn_stack need: two normed-input
+ * buffers, the FFN intermediate, the projected buffer and the tail scratch. */
+size_t muser_ffn_workspace_bytes(int64_t hidden, int64_t ffn, int M);
+
+/*
+ * muser_ffn_stack -- `n_layers` decode-FFN layers over M residual rows
+ *   (Ch 10 §10.3-§10.4): the entry RMSNorm (weight entry_norm, eps_norm) runs
+ *   once; then per layer l: mid = silu(Wg.x) * (Wu.x); projected = Wd.mid;
+ *   residual += post_norm * rms_norm(projected, eps_post); x = next_norm *
+ *   rms_norm(residual, eps_norm).  `out` receives the last layer's x.
+ *   layers: host array of n_layers structs; entry_norm: device f32 [hidden];
+ *   residual: device f32 [M*hidden] in/out; out: device f32 [M*hidden];
+ *   workspace: device memory of muser_ffn_workspace_bytes(hidden, ffn, M)
+ *   bytes, 16-byte aligned, zero-filled before its first use.
+ *   n_layers == 1 is one decode-FFN block.
+ */
+int muser_ffn_stack(const muser_ffn_layer* layers, int n_layers, const float* entry_norm,
+                    int64_t hidden, int64_t ffn, int M, float* residual, float* out,
+                    float eps_norm, float eps_post, void* workspace, size_t workspace_bytes,
+                    void* stream);
+
+/*
+ * K/V plane metadata (Ch 15 §15.2 MetalKvPlane).  key/value are device
+ * binary16 planes of capacity*kv_dim halves.  Token-major index:
+ * physical*kv_dim + e; head-major: (e/head_dim*capacity + physical)*head_dim
+ * + e%head_dim (§15.3 Figure 15.1).  The struct is host memory; the library
+ * updates len/origin_* on success only.
+ */
+typedef struct {
+    uint16_t* key;
+    uint16_t* value;
+    int64_t capacity;
+    int64_t len;
+    int64_t origin_logical;
+    int64_t origin_physical;
+    int32_t kv_dim;
+    int32_t head_dim;
+    int32_t head_major;
+    int32_t reserved;
+} muser_kv_plane;
+
+/*
+ * muser_kv_ring_write -- append `count` token rows at logical positions
+ *   position..position+count-1 (Ch 15 §15.5 append / append_batch): the
+ *   physical row comes from the plane's explicit origins, never from the
+ *   absolute position; K and V are stored as binary16 rounded to nearest
+ *   even.  position != origin_logical + len returns
+ *   MUSER_ERR_CACHE_DISCONTINUITY and leaves the plane and its metadata
+ *   untouched.  When count > capacity only the last `capacity` rows survive,
+ *   as with sequential appends.
+ *   plane: host struct (updated on success); k, v: device f32
+ *   [count*kv_dim]; first_physical: host, receives the physical row of
+ *   `position` (may be NULL).
+ */
+int muser_kv_ring_write(muser_kv_plane* plane, const float* k, const float* v, int64_t position,
+                        int64_t count, int64_t* first_physical, void* stream);
+
+/*
+ * muser_sync -- wait until all work enqueued on `stream` has finished, for at
+ *   most timeout_ms milliseconds (the book's bounded wait_for_completion,
+ *   Ch 2 §2.10).  Returns MUSER_OK, MUSER_ERR_TIMEOUT (the work keeps
+ *   running) or MUSER_ERR_CUDA.  timeout_ms < 0 waits without a limit.
+ */
+int muser_sync(void* stream, int timeout_ms);
+
+/*
+ * muser_debug_spin -- enqueue a kernel that busy-waits `microseconds` on the
+ *   GPU's global timer and then returns (bounded by construction, at most
+ *   10 s).  Exists to exercise muser_sync's timeout path without stalling the
+ *   GPU.
+ */
+int muser_debug_spin(int64_t microseconds, void* stream);
+
+/* Number of SMs of the current device (for reports); -1 on error. */
+int muser_device_sm_count(void);
+
+/*
+ * muser_device_status -- the library's device status word (0 = clean).  Bit 1:
+ *   a kernel gave up a bounded wait on a weight-tile transfer and returned
+ *   without finishing its outputs; bit 2: its clean-up wait also gave up.
+ *   Synchronous (reads device memory); reset != 0 clears the word afterwards.
+ *   Returns 0xFFFFFFFF if the word cannot be read.
+ */
+unsigned muser_device_status(int reset);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MUSER_H */

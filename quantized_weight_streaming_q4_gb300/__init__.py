@@ -1,0 +1,250 @@
+"""Python binding of libmuser, the GB300 decode-FFN weight-streaming library.
+
+Argument marshalling only: every step of the path runs in libmuser's CUDA
+kernels (``csrc/``), reached through the C ABI declared in ``include/muser.h``.
+PyTorch supplies device memory and streams.  There is no CPU fallback: if the
+library is not built, every call raises.
+
+The functions carry the C names.  Tensor arguments are torch tensors on the
+current CUDA device (contiguous, the dtype the C ABI states); ``stream``
+defaults to torch's current stream.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+__all__ = [
+    "MUSER_Q4_K", "MUSER_Q6_K", "QTYPES", "MuserError", "build", "library_path", "lib",
+    "muser_version", "muser_last_error", "muser_block_bytes", "muser_matrix_bytes",
+    "muser_dequantize", "muser_qmatvec", "muser_rms_norm", "muser_silu_mul",
+    "muser_ffn_gate_up_silu", "muser_fused_residual_dual_rmsnorm", "muser_scratch_bytes",
+    "muser_qmatvec_residual_dual_rmsnorm", "FfnLayer", "muser_ffn_workspace_bytes",
+    "muser_ffn_stack", "KvPlane", "muser_kv_ring_write", "muser_sync", "muser_debug_spin",
+    "muser_device_sm_count", "muser_device_status",
+]
+
+MUSER_Q4_K = 12
+MUSER_Q6_K = 14
+QTYPES = {"q4_k": MUSER_Q4_K, "q6_k": MUSER_Q6_K}
+BLOCK_BYTES = {MUSER_Q4_K: 144, MUSER_Q6_K: 210}
+STATUS = {0: "MUSER_OK", -1: "MUSER_ERR_INVALID_ARG", -2: "MUSER_ERR_UNSUPPORTED",
+          -3: "MUSER_ERR_MISALIGNED", -4: "MUSER_ERR_CACHE_DISCONTINUITY", -5: "MUSER_ERR_CUDA",
+          -6: "MUSER_ERR_TIMEOUT"}
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_LIB = os.path.join(_PKG, "_build", "libmuser.so")
+_lock = threading.Lock()
+_lib = None
+
+
+class MuserError(RuntimeError):
+    def __init__(self, fn: str, status: int, message: str):
+        super().__init__(f"{fn} -> {STATUS.get(status, status)}: {message}")
+        self.status = status
+
+
+def build(force: bool = False, verbose: bool = False) -> str:
+    from . import buildlib as _b
+    return _b.build(force=force, verbose=verbose)
+
+
+def library_path() -> str:
+    return _LIB
+
+
+class FfnLayer(ctypes.Structure):
+    _fields_ = [("w_gate", ctypes.c_void_p), ("w_up", ctypes.c_void_p), ("w_down", ctypes.c_void_p),
+                ("post_norm", ctypes.c_void_p), ("next_norm", ctypes.c_void_p),
+                ("gate_up_qtype", ctypes.c_int32), ("down_qtype", ctypes.c_int32)]
+
+
+class KvPlane(ctypes.Structure):
+    _fields_ = [("key", ctypes.c_void_p), ("value", ctypes.c_void_p), ("capacity", ctypes.c_int64),
+                ("len", ctypes.c_int64), ("origin_logical", ctypes.c_int64),
+                ("origin_physical", ctypes.c_int64), ("kv_dim", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("head_major", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
+
+
+def lib():
+    """The loaded libmuser (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(_LIB):
+            raise RuntimeError(f"libmuser is not built ({_LIB} missing); call "
+                               "quantized_weight_streaming_q4_gb300.build() first")
+        L = ctypes.CDLL(_LIB)
+        P, I, I64, F, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+        sig = {
+            "muser_version": (I, []),
+            "muser_last_error": (ctypes.c_char_p, []),
+            "muser_block_bytes": (SZ, [I]),
+            "muser_matrix_bytes": (SZ, [I, I64, I64]),
+            "muser_dequantize": (I, [I, P, I64, I64, P, P]),
+            "muser_qmatvec": (I, [I, P, I64, I64, P, I, P, P]),
+            "muser_rms_norm": (I, [P, P, P, I, I, F, P]),
+            "muser_silu_mul": (I, [P, P, P, I64, P]),
+            "muser_ffn_gate_up_silu": (I, [I, P, P, I64, I64, P, I, P, P]),
+            "muser_fused_residual_dual_rmsnorm": (I, [P, P, P, P, P, I, I, F, F, P]),
+            "muser_scratch_bytes": (SZ, [I64, I]),
+            "muser_qmatvec_residual_dual_rmsnorm": (I, [I, P, I64, I64, P, I, P, P, P, P, P, F, F, P,
+                                                        SZ, P]),
+            "muser_ffn_workspace_bytes": (SZ, [I64, I64, I]),
+            "muser_ffn_stack": (I, [ctypes.POINTER(FfnLayer), I, P, I64, I64, I, P, P, F, F, P, SZ,
+                                    P]),
+            "muser_kv_ring_write": (I, [ctypes.POINTER(KvPlane), P, P, I64, I64,
+                                        ctypes.POINTER(I64), P]),
+            "muser_sync": (I, [P, I]),
+            "muser_debug_spin": (I, [I64, P]),
+            "muser_device_sm_count": (I, []),
+            "muser_device_status": (ctypes.c_uint, [I]),
+        }
+        for name, (res, args) in sig.items():
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = L
+        return _lib
+
+
+# ------------------------------------------------------------------ helpers
+def _qt(qtype) -> int:
+    return QTYPES[qtype] if isinstance(qtype, str) else int(qtype)
+
+
+def _ptr(t) -> int | None:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(fn: str, rc: int) -> int:
+    if rc != 0:
+        msg = lib().muser_last_error()
+        raise MuserError(fn, rc, msg.decode() if msg else "")
+    return rc
+
+
+# --------------------------------------------------------------- entry points
+def muser_version() -> int:
+    return lib().muser_version()
+
+
+def muser_last_error() -> str:
+    m = lib().muser_last_error()
+    return m.decode() if m else ""
+
+
+def muser_block_bytes(qtype) -> int:
+    return lib().muser_block_bytes(_qt(qtype))
+
+
+def muser_matrix_bytes(qtype, rows: int, cols: int) -> int:
+    return lib().muser_matrix_bytes(_qt(qtype), rows, cols)
+
+
+def muser_dequantize(qtype, W, rows: int, cols: int, out, stream=None) -> None:
+    _check("muser_dequantize", lib().muser_dequantize(_qt(qtype), _ptr(W), rows, cols, _ptr(out),
+                                                      _stream(stream)))
+
+
+def muser_qmatvec(qtype, W, rows: int, cols: int, x, M: int, y, stream=None) -> None:
+    _check("muser_qmatvec", lib().muser_qmatvec(_qt(qtype), _ptr(W), rows, cols, _ptr(x), M,
+                                                _ptr(y), _stream(stream)))
+
+
+def muser_rms_norm(x, w, out, n: int, M: int, eps: float, stream=None) -> None:
+    _check("muser_rms_norm", lib().muser_rms_norm(_ptr(x), _ptr(w), _ptr(out), n, M, eps,
+                                                  _stream(stream)))
+
+
+def muser_silu_mul(a, b, out, n: int, stream=None) -> None:
+    _check("muser_silu_mul", lib().muser_silu_mul(_ptr(a), _ptr(b), _ptr(out), n, _stream(stream)))
+
+
+def muser_ffn_gate_up_silu(qtype, Wg, Wu, ffn: int, hidden: int, x, M: int, mid, stream=None) -> None:
+    _check("muser_ffn_gate_up_silu",
+           lib().muser_ffn_gate_up_silu(_qt(qtype), _ptr(Wg), _ptr(Wu), ffn, hidden, _ptr(x), M,
+                                        _ptr(mid), _stream(stream)))
+
+
+def muser_fused_residual_dual_rmsnorm(residual, src, out, w1, w2, n: int, M: int, eps1: float,
+                                      eps2: float, stream=None) -> None:
+    _check("muser_fused_residual_dual_rmsnorm",
+           lib().muser_fused_residual_dual_rmsnorm(_ptr(residual), _ptr(src), _ptr(out), _ptr(w1),
+                                                   _ptr(w2), n, M, eps1, eps2, _stream(stream)))
+
+
+def muser_scratch_bytes(hidden: int, M: int) -> int:
+    return lib().muser_scratch_bytes(hidden, M)
+
+
+def muser_qmatvec_residual_dual_rmsnorm(qtype, Wdown, hidden: int, ffn: int, mid, M: int,
+                                        projected, residual, out, w1, w2, eps1: float,
+                                        eps2: float, scratch, scratch_bytes: int,
+                                        stream=None) -> None:
+    _check("muser_qmatvec_residual_dual_rmsnorm",
+           lib().muser_qmatvec_residual_dual_rmsnorm(
+               _qt(qtype), _ptr(Wdown), hidden, ffn, _ptr(mid), M, _ptr(projected),
+               _ptr(residual), _ptr(out), _ptr(w1), _ptr(w2), eps1, eps2, _ptr(scratch),
+               scratch_bytes, _stream(stream)))
+
+
+def muser_ffn_workspace_bytes(hidden: int, ffn: int, M: int) -> int:
+    return lib().muser_ffn_workspace_bytes(hidden, ffn, M)
+
+
+def muser_ffn_stack(layers, entry_norm, hidden: int, ffn: int, M: int, residual, out,
+                    eps_norm: float, eps_post: float, workspace, workspace_bytes: int,
+                    stream=None) -> None:
+    """layers: a ctypes array of FfnLayer (host memory) or a list of FfnLayer."""
+    if not isinstance(layers, ctypes.Array):
+        layers = (FfnLayer * len(layers))(*layers)
+    _check("muser_ffn_stack",
+           lib().muser_ffn_stack(layers, len(layers), _ptr(entry_norm), hidden, ffn, M,
+                                 _ptr(residual), _ptr(out), eps_norm, eps_post, _ptr(workspace),
+                                 workspace_bytes, _stream(stream)))
+
+
+def muser_kv_ring_write(plane: KvPlane, k, v, position: int, count: int, stream=None) -> int:
+    """Appends `count` rows; returns the physical row of `position`."""
+    first = ctypes.c_int64(-1)
+    _check("muser_kv_ring_write",
+           lib().muser_kv_ring_write(ctypes.byref(plane), _ptr(k), _ptr(v), position, count,
+                                     ctypes.byref(first), _stream(stream)))
+    return first.value
+
+
+def muser_sync(stream=None, timeout_ms: int = -1) -> int:
+    """Returns 0 or raises (MUSER_ERR_TIMEOUT is returned, not raised)."""
+    rc = lib().muser_sync(_stream(stream), timeout_ms)
+    if rc == -6:
+        return rc
+    return _check("muser_sync", rc)
+
+
+def muser_debug_spin(microseconds: int, stream=None) -> None:
+    _check("muser_debug_spin", lib().muser_debug_spin(microseconds, _stream(stream)))
+
+
+def muser_device_sm_count() -> int:
+    return lib().muser_device_sm_count()
+
+
+def muser_device_status(reset: bool = False) -> int:
+    return lib().muser_device_status(1 if reset else 0)

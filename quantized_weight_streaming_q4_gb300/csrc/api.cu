@@ -1,0 +1,468 @@
+// api.cu -- the C ABI of libmuser (declared in include/muser.h): argument
+// validation on the host, then launches on the caller's stream.  Nothing here
+// allocates device memory.
+#include <time.h>
+
+#include <algorithm>
+#include <cstdarg>
+#include <cstdio>
+#include <mutex>
+
+#include "common.cuh"
+#include "kernels.cuh"
+
+namespace muser {
+
+static thread_local char g_err[512];
+
+int set_error(int status, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof g_err, fmt, ap);
+    va_end(ap);
+    return status;
+}
+void clear_error() { g_err[0] = 0; }
+int cuda_fail(cudaError_t e, const char* what) {
+    return set_error(MUSER_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+int check_launch(const char* what) {
+    const cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? MUSER_OK : cuda_fail(e, what);
+}
+
+namespace {
+constexpr int kMaxDev = 64;
+std::mutex g_attr_mu;
+int g_sm[kMaxDev] = {0};
+int g_smem[kMaxDev] = {0};
+
+int device_attr(int* cache, cudaDeviceAttr attr) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return -1;
+    std::lock_guard<std::mutex> lk(g_attr_mu);
+    if (cache[dev] == 0) {
+        int v = 0;
+        if (cudaDeviceGetAttribute(&v, attr, dev) != cudaSuccess) return -1;
+        cache[dev] = v;
+    }
+    return cache[dev];
+}
+
+bool known_qtype(int q) { return q == MUSER_Q4_K || q == MUSER_Q6_K; }
+size_t block_bytes_of(int q) {
+    return q == MUSER_Q4_K ? static_cast<size_t>(kQ4KBytes)
+                           : (q == MUSER_Q6_K ? static_cast<size_t>(kQ6KBytes) : 0);
+}
+
+// Shared checks of a quantized matrix operand.
+int check_matrix(const char* fn, int qtype, const void* W, int64_t rows, int64_t cols) {
+    if (!known_qtype(qtype))
+        return set_error(MUSER_ERR_UNSUPPORTED, "%s: unsupported quant type %d (Q4_K=12, Q6_K=14)", fn, qtype);
+    if (W == nullptr) return set_error(MUSER_ERR_INVALID_ARG, "%s: weight pointer is NULL", fn);
+    if (rows < 1 || rows > (int64_t{1} << 31))
+        return set_error(MUSER_ERR_INVALID_ARG, "%s: rows = %lld out of range", fn, (long long)rows);
+    if (cols < kQK || cols % kQK != 0 || cols > (int64_t{1} << 28))
+        return set_error(MUSER_ERR_INVALID_ARG, "%s: cols = %lld must be a positive multiple of 256", fn, (long long)cols);
+    if (!is_aligned(W, 16))
+        return set_error(MUSER_ERR_MISALIGNED, "%s: weight pointer not 16-byte aligned", fn);
+    return MUSER_OK;
+}
+
+int check_f32(const char* fn, const char* name, const void* p) {
+    if (p == nullptr) return set_error(MUSER_ERR_INVALID_ARG, "%s: %s is NULL", fn, name);
+    if (!is_aligned(p, 16)) return set_error(MUSER_ERR_MISALIGNED, "%s: %s not 16-byte aligned", fn, name);
+    return MUSER_OK;
+}
+
+int check_M(const char* fn, int M) {
+    if (M < 1 || M > MUSER_MAX_M)
+        return set_error(MUSER_ERR_INVALID_ARG, "%s: M = %d outside 1..%d", fn, M, MUSER_MAX_M);
+    return MUSER_OK;
+}
+
+#define MUSER_TRY(expr)                  \
+    do {                                 \
+        const int _rc = (expr);          \
+        if (_rc != MUSER_OK) return _rc; \
+    } while (0)
+
+constexpr size_t kScratchBytes = 256;
+
+size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+struct Workspace {
+    float* xa;
+    float* xb;
+    float* mid;
+    float* proj;
+    void* scratch;
+    size_t total;
+};
+Workspace carve(void* base, int64_t hidden, int64_t ffn, int M) {
+    Workspace w{};
+    uint8_t* p = static_cast<uint8_t*>(base);
+    size_t off = 0;
+    const size_t hb = round_up(sizeof(float) * static_cast<size_t>(hidden) * M, 256);
+    const size_t fb = round_up(sizeof(float) * static_cast<size_t>(ffn) * M, 256);
+    w.xa = reinterpret_cast<float*>(p + off);
+    off += hb;
+    w.xb = reinterpret_cast<float*>(p + off);
+    off += hb;
+    w.mid = reinterpret_cast<float*>(p + off);
+    off += fb;
+    w.proj = reinterpret_cast<float*>(p + off);
+    off += hb;
+    w.scratch = p + off;
+    off += kScratchBytes;
+    w.total = off;
+    return w;
+}
+
+// Launch the matvec + tail on validated arguments.
+int down_tail_launch(int qtype, const void* Wdown, int64_t hidden, int64_t ffn, const float* mid,
+                     int M, float* projected, float* residual, float* out, const float* w1,
+                     const float* w2, float eps1, float eps2, void* scratch, cudaStream_t s) {
+    if (M == 1 && mv1_supported(qtype, ffn)) {
+        Mv1Args a{};
+        a.W[0] = static_cast<const uint8_t*>(Wdown);
+        a.W[1] = a.W[0];
+        a.rows = hidden;
+        a.nsb = static_cast<int>(ffn / kQK);
+        a.x = mid;
+        a.y0 = projected;
+        a.resid = residual;
+        a.out = out;
+        a.w1 = w1;
+        a.w2 = w2;
+        a.eps1 = eps1;
+        a.eps2 = eps2;
+        a.ticket = static_cast<unsigned*>(scratch);
+        return launch_mv1(qtype, 1, kEpiTail, a, s);
+    }
+    MvMArgs a{};
+    a.W[0] = static_cast<const uint8_t*>(Wdown);
+    a.W[1] = a.W[0];
+    a.rows = hidden;
+    a.nsb = static_cast<int>(ffn / kQK);
+    a.x = mid;
+    a.M = M;
+    a.y0 = projected;
+    MUSER_TRY(launch_mvM(qtype, 1, kEpiStore, a, s));
+    return launch_dual_tail(residual, projected, out, w1, w2, static_cast<int>(hidden), M, eps1,
+                            eps2, s);
+}
+
+int gate_up_launch(int qtype, const void* Wg, const void* Wu, int64_t ffn, int64_t hidden,
+                   const float* x, int M, float* mid, cudaStream_t s) {
+    if (M == 1 && mv1_supported(qtype, hidden)) {
+        Mv1Args a{};
+        a.W[0] = static_cast<const uint8_t*>(Wg);
+        a.W[1] = static_cast<const uint8_t*>(Wu);
+        a.rows = ffn;
+        a.nsb = static_cast<int>(hidden / kQK);
+        a.x = x;
+        a.y0 = mid;
+        return launch_mv1(qtype, 2, kEpiSiluMul, a, s);
+    }
+    MvMArgs a{};
+    a.W[0] = static_cast<const uint8_t*>(Wg);
+    a.W[1] = static_cast<const uint8_t*>(Wu);
+    a.rows = ffn;
+    a.nsb = static_cast<int>(hidden / kQK);
+    a.x = x;
+    a.M = M;
+    a.y0 = mid;
+    return launch_mvM(qtype, 2, kEpiSiluMul, a, s);
+}
+
+}  // namespace
+
+int sm_count() { return device_attr(g_sm, cudaDevAttrMultiProcessorCount); }
+int max_smem_optin() { return device_attr(g_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin); }
+
+}  // namespace muser
+
+using namespace muser;
+
+extern "C" {
+
+int muser_version(void) { return MUSER_ABI_VERSION; }
+
+const char* muser_last_error(void) { return g_err; }
+
+size_t muser_block_bytes(int qtype) { return block_bytes_of(qtype); }
+
+size_t muser_matrix_bytes(int qtype, int64_t rows, int64_t cols) {
+    if (!known_qtype(qtype) || rows < 0 || cols < 0 || cols % kQK) return 0;
+    return static_cast<size_t>(rows) * static_cast<size_t>(cols / kQK) * block_bytes_of(qtype);
+}
+
+int muser_dequantize(int qtype, const void* W, int64_t rows, int64_t cols, float* out,
+                     void* stream) {
+    clear_error();
+    MUSER_TRY(check_matrix("muser_dequantize", qtype, W, rows, cols));
+    MUSER_TRY(check_f32("muser_dequantize", "out", out));
+    return launch_dequantize(qtype, static_cast<const uint8_t*>(W), rows, cols, out,
+                             as_stream(stream));
+}
+
+int muser_qmatvec(int qtype, const void* W, int64_t rows, int64_t cols, const float* x, int M,
+                  float* y, void* stream) {
+    clear_error();
+    const char* fn = "muser_qmatvec";
+    MUSER_TRY(check_matrix(fn, qtype, W, rows, cols));
+    MUSER_TRY(check_M(fn, M));
+    MUSER_TRY(check_f32(fn, "x", x));
+    MUSER_TRY(check_f32(fn, "y", y));
+    if (M == 1 && mv1_supported(qtype, cols)) {
+        Mv1Args a{};
+        a.W[0] = static_cast<const uint8_t*>(W);
+        a.W[1] = a.W[0];
+        a.rows = rows;
+        a.nsb = static_cast<int>(cols / kQK);
+        a.x = x;
+        a.y0 = y;
+        return launch_mv1(qtype, 1, kEpiStore, a, as_stream(stream));
+    }
+    MvMArgs a{};
+    a.W[0] = static_cast<const uint8_t*>(W);
+    a.W[1] = a.W[0];
+    a.rows = rows;
+    a.nsb = static_cast<int>(cols / kQK);
+    a.x = x;
+    a.M = M;
+    a.y0 = y;
+    return launch_mvM(qtype, 1, kEpiStore, a, as_stream(stream));
+}
+
+int muser_rms_norm(const float* x, const float* w, float* out, int n, int M, float eps,
+                   void* stream) {
+    clear_error();
+    const char* fn = "muser_rms_norm";
+    MUSER_TRY(check_f32(fn, "x", x));
+    MUSER_TRY(check_f32(fn, "w", w));
+    MUSER_TRY(check_f32(fn, "out", out));
+    if (n < 4 || n % 4) return set_error(MUSER_ERR_INVALID_ARG, "%s: n = %d must be a positive multiple of 4", fn, n);
+    if (M < 1 || M > 65535) return set_error(MUSER_ERR_INVALID_ARG, "%s: M = %d out of range", fn, M);
+    if (!(eps > 0.0f)) return set_error(MUSER_ERR_INVALID_ARG, "%s: eps must be > 0", fn);
+    return launch_rms_norm(x, w, out, n, M, eps, as_stream(stream));
+}
+
+int muser_silu_mul(const float* a, const float* b, float* out, int64_t n, void* stream) {
+    clear_error();
+    const char* fn = "muser_silu_mul";
+    if (n < 0) return set_error(MUSER_ERR_INVALID_ARG, "%s: n < 0", fn);
+    if (n == 0) return MUSER_OK;
+    if (!a || !b || !out) return set_error(MUSER_ERR_INVALID_ARG, "%s: NULL pointer", fn);
+    if (!is_aligned(a, 4) || !is_aligned(b, 4) || !is_aligned(out, 4))
+        return set_error(MUSER_ERR_MISALIGNED, "%s: pointers must be 4-byte aligned", fn);
+    return launch_silu_mul(a, b, out, n, as_stream(stream));
+}
+
+int muser_ffn_gate_up_silu(int qtype, const void* Wg, const void* Wu, int64_t ffn,
+                           int64_t hidden, const float* x, int M, float* mid, void* stream) {
+    clear_error();
+    const char* fn = "muser_ffn_gate_up_silu";
+    MUSER_TRY(check_matrix(fn, qtype, Wg, ffn, hidden));
+    MUSER_TRY(check_matrix(fn, qtype, Wu, ffn, hidden));
+    MUSER_TRY(check_M(fn, M));
+    MUSER_TRY(check_f32(fn, "x", x));
+    MUSER_TRY(check_f32(fn, "mid", mid));
+    return gate_up_launch(qtype, Wg, Wu, ffn, hidden, x, M, mid, as_stream(stream));
+}
+
+int muser_fused_residual_dual_rmsnorm(float* residual, const float* src, float* out,
+                                      const float* w1, const float* w2, int n, int M, float eps1,
+                                      float eps2, void* stream) {
+    clear_error();
+    const char* fn = "muser_fused_residual_dual_rmsnorm";
+    MUSER_TRY(check_f32(fn, "residual", residual));
+    MUSER_TRY(check_f32(fn, "src", src));
+    MUSER_TRY(check_f32(fn, "out", out));
+    MUSER_TRY(check_f32(fn, "w1", w1));
+    MUSER_TRY(check_f32(fn, "w2", w2));
+    if (n < 4 || n % 4) return set_error(MUSER_ERR_INVALID_ARG, "%s: n = %d must be a positive multiple of 4", fn, n);
+    if (M < 1 || M > 65535) return set_error(MUSER_ERR_INVALID_ARG, "%s: M = %d out of range", fn, M);
+    if (!(eps1 > 0.0f) || !(eps2 > 0.0f)) return set_error(MUSER_ERR_INVALID_ARG, "%s: eps must be > 0", fn);
+    if (out == residual || out == src)
+        return set_error(MUSER_ERR_INVALID_ARG, "%s: out must not alias residual or src", fn);
+    return launch_dual_tail(residual, src, out, w1, w2, n, M, eps1, eps2, as_stream(stream));
+}
+
+size_t muser_scratch_bytes(int64_t hidden, int M) {
+    (void)hidden;
+    (void)M;
+    return kScratchBytes;
+}
+
+int muser_qmatvec_residual_dual_rmsnorm(int qtype, const void* Wdown, int64_t hidden, int64_t ffn,
+                                        const float* mid, int M, float* projected,
+                                        float* residual, float* out, const float* w1,
+                                        const float* w2, float eps1, float eps2, void* scratch,
+                                        size_t scratch_bytes, void* stream) {
+    clear_error();
+    const char* fn = "muser_qmatvec_residual_dual_rmsnorm";
+    MUSER_TRY(check_matrix(fn, qtype, Wdown, hidden, ffn));
+    MUSER_TRY(check_M(fn, M));
+    MUSER_TRY(check_f32(fn, "mid", mid));
+    MUSER_TRY(check_f32(fn, "projected", projected));
+    MUSER_TRY(check_f32(fn, "residual", residual));
+    MUSER_TRY(check_f32(fn, "out", out));
+    MUSER_TRY(check_f32(fn, "w1", w1));
+    MUSER_TRY(check_f32(fn, "w2", w2));
+    MUSER_TRY(check_f32(fn, "scratch", scratch));
+    if (hidden % 4) return set_error(MUSER_ERR_INVALID_ARG, "%s: hidden must be a multiple of 4", fn);
+    if (scratch_bytes < kScratchBytes)
+        return set_error(MUSER_ERR_INVALID_ARG, "%s: scratch_bytes %zu < %zu", fn, scratch_bytes, kScratchBytes);
+    if (!(eps1 > 0.0f) || !(eps2 > 0.0f)) return set_error(MUSER_ERR_INVALID_ARG, "%s: eps must be > 0", fn);
+    if (out == residual || out == projected || projected == residual)
+        return set_error(MUSER_ERR_INVALID_ARG, "%s: projected, residual and out must be distinct", fn);
+    return down_tail_launch(qtype, Wdown, hidden, ffn, mid, M, projected, residual, out, w1, w2,
+                            eps1, eps2, scratch, as_stream(stream));
+}
+
+size_t muser_ffn_workspace_bytes(int64_t hidden, int64_t ffn, int M) {
+    if (hidden < 1 || ffn < 1 || M < 1) return 0;
+    return carve(nullptr, hidden, ffn, M).total;
+}
+
+int muser_ffn_stack(const muser_ffn_layer* layers, int n_layers, const float* entry_norm,
+                    int64_t hidden, int64_t ffn, int M, float* residual, float* out,
+                    float eps_norm, float eps_post, void* workspace, size_t workspace_bytes,
+                    void* stream) {
+    clear_error();
+    const char* fn = "muser_ffn_stack";
+    if (layers == nullptr || n_layers < 1)
+        return set_error(MUSER_ERR_INVALID_ARG, "%s: need at least one layer", fn);
+    MUSER_TRY(check_M(fn, M));
+    MUSER_TRY(check_f32(fn, "entry_norm", entry_norm));
+    MUSER_TRY(check_f32(fn, "residual", residual));
+    MUSER_TRY(check_f32(fn, "out", out));
+    MUSER_TRY(check_f32(fn, "workspace", workspace));
+    if (out == residual) return set_error(MUSER_ERR_INVALID_ARG, "%s: out must not alias residual", fn);
+    if (hidden % 4 || hidden > (int64_t{1} << 30))
+        return set_error(MUSER_ERR_INVALID_ARG, "%s: hidden must be a multiple of 4", fn);
+    if (!(eps_norm > 0.0f) || !(eps_post > 0.0f)) return set_error(MUSER_ERR_INVALID_ARG, "%s: eps must be > 0", fn);
+    const Workspace ws = carve(workspace, hidden, ffn, M);
+    if (workspace_bytes < ws.total)
+        return set_error(MUSER_ERR_INVALID_ARG, "%s: workspace_bytes %zu < %zu", fn, workspace_bytes, ws.total);
+    for (int l = 0; l < n_layers; ++l) {
+        const muser_ffn_layer& L = layers[l];
+        MUSER_TRY(check_matrix(fn, L.gate_up_qtype, L.w_gate, ffn, hidden));
+        MUSER_TRY(check_matrix(fn, L.gate_up_qtype, L.w_up, ffn, hidden));
+        MUSER_TRY(check_matrix(fn, L.down_qtype, L.w_down, hidden, ffn));
+        MUSER_TRY(check_f32(fn, "post_norm", L.post_norm));
+        MUSER_TRY(check_f32(fn, "next_norm", L.next_norm));
+    }
+    cudaStream_t s = as_stream(stream);
+    MUSER_TRY(launch_rms_norm(residual, entry_norm, ws.xa, static_cast<int>(hidden), M, eps_norm, s));
+    float* x = ws.xa;
+    float* xnext = ws.xb;
+    for (int l = 0; l < n_layers; ++l) {
+        const muser_ffn_layer& L = layers[l];
+        MUSER_TRY(gate_up_launch(L.gate_up_qtype, L.w_gate, L.w_up, ffn, hidden, x, M, ws.mid, s));
+        float* dst = (l == n_layers - 1) ? out : xnext;
+        MUSER_TRY(down_tail_launch(L.down_qtype, L.w_down, hidden, ffn, ws.mid, M, ws.proj,
+                                   residual, dst, L.post_norm, L.next_norm, eps_post, eps_norm,
+                                   ws.scratch, s));
+        std::swap(x, xnext);
+    }
+    return MUSER_OK;
+}
+
+int muser_kv_ring_write(muser_kv_plane* plane, const float* k, const float* v, int64_t position,
+                        int64_t count, int64_t* first_physical, void* stream) {
+    clear_error();
+    const char* fn = "muser_kv_ring_write";
+    if (plane == nullptr) return set_error(MUSER_ERR_INVALID_ARG, "%s: plane is NULL", fn);
+    muser_kv_plane& P = *plane;
+    if (P.key == nullptr || P.value == nullptr)
+        return set_error(MUSER_ERR_INVALID_ARG, "%s: plane buffers are NULL", fn);
+    if (!is_aligned(P.key, 2) || !is_aligned(P.value, 2))
+        return set_error(MUSER_ERR_MISALIGNED, "%s: plane buffers must be 2-byte aligned", fn);
+    if (P.capacity < 1 || P.len < 0 || P.len > P.capacity || P.origin_logical < 0 ||
+        P.origin_physical < 0 || P.origin_physical >= P.capacity)
+        return set_error(MUSER_ERR_INVALID_ARG, "%s: inconsistent ring metadata", fn);
+    if (P.kv_dim < 1 || (P.head_major && (P.head_dim < 1 || P.kv_dim % P.head_dim != 0)))
+        return set_error(MUSER_ERR_INVALID_ARG, "%s: bad kv_dim/head_dim", fn);
+    if (count < 0) return set_error(MUSER_ERR_INVALID_ARG, "%s: count < 0", fn);
+    const int64_t expected = P.origin_logical + P.len;
+    if (position != expected)
+        return set_error(MUSER_ERR_CACHE_DISCONTINUITY,
+                         "%s: cache discontinuity: expected position %lld, got %lld", fn,
+                         (long long)expected, (long long)position);
+    const int64_t phys_first = (P.origin_physical + P.len) % P.capacity;
+    if (count == 0) {
+        if (first_physical) *first_physical = phys_first;
+        return MUSER_OK;
+    }
+    if (!k || !v) return set_error(MUSER_ERR_INVALID_ARG, "%s: k/v NULL", fn);
+    if (!is_aligned(k, 4) || !is_aligned(v, 4))
+        return set_error(MUSER_ERR_MISALIGNED, "%s: k/v must be 4-byte aligned", fn);
+    // Sequential appends: only the last `capacity` rows of the batch survive.
+    const int64_t src_first = std::max<int64_t>(0, count - P.capacity);
+    MUSER_TRY(launch_kv_store(P.key, P.value, k, v, P.kv_dim, P.head_dim, P.head_major,
+                              P.capacity, phys_first, src_first, count - src_first,
+                              as_stream(stream)));
+    const int64_t total = P.len + count;
+    if (total <= P.capacity) {
+        P.len = total;
+    } else {
+        const int64_t advance = total - P.capacity;
+        P.len = P.capacity;
+        P.origin_logical += advance;
+        P.origin_physical = (P.origin_physical + advance) % P.capacity;
+    }
+    if (first_physical) *first_physical = phys_first;
+    return MUSER_OK;
+}
+
+int muser_sync(void* stream, int timeout_ms) {
+    clear_error();
+    cudaEvent_t ev;
+    cudaError_t e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);
+    if (e != cudaSuccess) return cuda_fail(e, "muser_sync: cudaEventCreate");
+    e = cudaEventRecord(ev, as_stream(stream));
+    if (e != cudaSuccess) {
+        cudaEventDestroy(ev);
+        return cuda_fail(e, "muser_sync: cudaEventRecord");
+    }
+    timespec t0;
+    clock_gettime(CLOCK_MONOTONIC, &t0);
+    int rc = MUSER_OK;
+    for (;;) {
+        e = cudaEventQuery(ev);
+        if (e == cudaSuccess) break;
+        if (e != cudaErrorNotReady) {
+            rc = cuda_fail(e, "muser_sync: cudaEventQuery");
+            break;
+        }
+        if (timeout_ms >= 0) {
+            timespec t;
+            clock_gettime(CLOCK_MONOTONIC, &t);
+            const double ms = (t.tv_sec - t0.tv_sec) * 1e3 + (t.tv_nsec - t0.tv_nsec) * 1e-6;
+            if (ms >= timeout_ms) {
+                rc = set_error(MUSER_ERR_TIMEOUT, "muser_sync: stream still busy after %d ms", timeout_ms);
+                break;
+            }
+        }
+        const timespec nap{0, 20000};
+        nanosleep(&nap, nullptr);
+    }
+    cudaEventDestroy(ev);
+    return rc;
+}
+
+int muser_debug_spin(int64_t microseconds, void* stream) {
+    clear_error();
+    if (microseconds < 0 || microseconds > 10 * 1000 * 1000)
+        return set_error(MUSER_ERR_INVALID_ARG, "muser_debug_spin: 0..10 s only");
+    return launch_spin(microseconds, as_stream(stream));
+}
+
+int muser_device_sm_count(void) { return sm_count(); }
+
+unsigned muser_device_status(int reset) { return read_device_status(reset != 0); }
+
+}  // extern "C"

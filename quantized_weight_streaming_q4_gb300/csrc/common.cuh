@@ -1,0 +1,226 @@
+// common.cuh -- host error plumbing and device helpers shared by libmuser's
+// translation units (CUDA, sm_103a).
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+#include "muser.h"
+
+namespace muser {
+
+// ------------------------------------------------------------------- host
+// Records a printf-style message for muser_last_error() on this thread and
+// returns `status`.
+int set_error(int status, const char* fmt, ...);
+void clear_error();
+// Maps a CUDA error to MUSER_ERR_CUDA with a message naming `what`.
+int cuda_fail(cudaError_t e, const char* what);
+// Checks cudaGetLastError() after a launch.
+int check_launch(const char* what);
+// SM count of the current device (cached per device).
+int sm_count();
+// Max dynamic shared memory per block of the current device (opt-in limit).
+int max_smem_optin();
+
+inline bool is_aligned(const void* p, size_t a) {
+    return (reinterpret_cast<uintptr_t>(p) % a) == 0;
+}
+inline cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
+
+// Device-side status word: kernels that give up a bounded wait set a bit
+// here instead of hanging; the host can read and clear it.
+enum : unsigned { kDevStatusWaitTimeout = 1u, kDevStatusTxTimeout = 2u };
+unsigned read_device_status(bool reset);
+
+// ------------------------------------------------------------------ device
+constexpr int kQK = 256;          // weights per super-block
+constexpr int kQ4KBytes = 144;    // Q4_K super-block bytes
+constexpr int kQ6KBytes = 210;    // Q6_K super-block bytes
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// Deterministic block-wide sum: per-warp shuffle trees, then thread 0 adds
+// the warp partials in warp order.  `red` needs 33 floats of shared memory.
+// Every thread of the block must call it; all get the same value.
+__device__ __forceinline__ float block_sum(float v, float* red) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int nwarps = (blockDim.x + 31) >> 5;
+    v = warp_sum(v);
+    if (lane == 0) red[warp] = v;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float t = 0.0f;
+        for (int w = 0; w < nwarps; ++w) t += red[w];
+        red[32] = t;
+    }
+    __syncthreads();
+    const float t = red[32];
+    __syncthreads();
+    return t;
+}
+
+// Read-only global loads.  *_stream bypasses L1 allocation (weights are read
+// once); plain nc loads keep L1 allocation.
+__device__ __forceinline__ uint4 ldg_stream16(const void* p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+__device__ __forceinline__ uint32_t ldg_u32(const void* p) {
+    uint32_t v;
+    asm volatile("ld.global.nc.u32 %0, [%1];" : "=r"(v) : "l"(p));
+    return v;
+}
+__device__ __forceinline__ uint32_t ldg_u16(const void* p) {
+    unsigned short v;
+    asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(v) : "l"(p));
+    return v;
+}
+__device__ __forceinline__ uint32_t ldg_u8(const void* p) {
+    unsigned short v;
+    asm volatile("ld.global.nc.u8 %0, [%1];" : "=h"(v) : "l"(p));
+    return v & 0xffu;
+}
+
+// Binary16 bits -> binary32 (exact).
+__device__ __forceinline__ float h2f(uint32_t bits16) {
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(bits16 & 0xffffu)));
+}
+
+// The float whose bit pattern is `bits`.  With only the low 23 bits set it is
+// a subnormal: bits * 2^-149, exactly.
+__device__ __forceinline__ float bits_f(uint32_t bits) { return __uint_as_float(bits); }
+
+// Small unsigned byte -> float through the 2^23 magic exponent: the float
+// with bits 0x4B0000XX is 2^23 + XX, exactly.
+__device__ __forceinline__ float byte_to_f(uint32_t word, uint32_t sel_with_magic) {
+    return __uint_as_float(__byte_perm(word, 0x4B000000u, sel_with_magic)) - 8388608.0f;
+}
+
+// ---------------------------------------------------------- TMA / mbarrier
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
+}
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+// 1-D bulk copy global -> shared, completion counted on `bar` (bytes).
+// dst, src 16-byte aligned; bytes a multiple of 16.
+__device__ __forceinline__ void tma_load_1d(void* dst, const void* src, uint32_t bytes,
+                                            uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+            "r"(smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Bounded wait on an mbarrier phase.  Returns false (and sets `flag` in the
+// device status word *status) if the phase did not complete within about
+// `max_polls` polls (~1 s with the default).
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, unsigned* status,
+                                                  unsigned flag, uint32_t max_polls = (1u << 24)) {
+    for (uint32_t i = 0; i < max_polls; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (i > 64) __nanosleep(64);
+    }
+    atomicOr(status, flag);
+    return false;
+}
+
+// Programmatic dependent launch controls (no-ops without the launch attribute).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ----------------------------------------------------------- dual-eps tail
+// One row of the dual-eps tail (Muser book Ch 19 §19.4): three passes over
+// the row by the whole block, float4 strides, deterministic reductions.
+//   pass 1: inv1 = 1/sqrt(mean(src^2) + eps1)
+//   pass 2: resid = resid + (src*inv1)*w1, stored; accumulate resid^2
+//   pass 3: out = (resid*inv2)*w2 with inv2 = 1/sqrt(mean(resid^2) + eps2)
+// `src` may have been written by other blocks of the same grid (read with
+// .cg loads that bypass L1).  `red` needs 33 floats of shared memory.
+__device__ __forceinline__ void block_dual_tail_row(float* resid, const float* src, float* out,
+                                                    const float* w1, const float* w2, int n,
+                                                    float eps1, float eps2, float* red) {
+    const int n4 = n >> 2;
+    const float4* s4 = reinterpret_cast<const float4*>(src);
+    float4* r4 = reinterpret_cast<float4*>(resid);
+    float4* o4 = reinterpret_cast<float4*>(out);
+    const float4* a4 = reinterpret_cast<const float4*>(w1);
+    const float4* b4 = reinterpret_cast<const float4*>(w2);
+    float ss = 0.0f;
+    for (int i = threadIdx.x; i < n4; i += blockDim.x) {
+        const float4 v = __ldcg(s4 + i);
+        ss = fmaf(v.x, v.x, ss);
+        ss = fmaf(v.y, v.y, ss);
+        ss = fmaf(v.z, v.z, ss);
+        ss = fmaf(v.w, v.w, ss);
+    }
+    ss = block_sum(ss, red);
+    const float inv1 = 1.0f / sqrtf(ss / static_cast<float>(n) + eps1);
+    float sh = 0.0f;
+    for (int i = threadIdx.x; i < n4; i += blockDim.x) {
+        const float4 v = __ldcg(s4 + i);
+        const float4 r = __ldcg(r4 + i);
+        const float4 w = __ldg(a4 + i);
+        float4 h;
+        h.x = fmaf(v.x * inv1, w.x, r.x);
+        h.y = fmaf(v.y * inv1, w.y, r.y);
+        h.z = fmaf(v.z * inv1, w.z, r.z);
+        h.w = fmaf(v.w * inv1, w.w, r.w);
+        r4[i] = h;
+        sh = fmaf(h.x, h.x, sh);
+        sh = fmaf(h.y, h.y, sh);
+        sh = fmaf(h.z, h.z, sh);
+        sh = fmaf(h.w, h.w, sh);
+    }
+    sh = block_sum(sh, red);
+    const float inv2 = 1.0f / sqrtf(sh / static_cast<float>(n) + eps2);
+    for (int i = threadIdx.x; i < n4; i += blockDim.x) {
+        const float4 h = r4[i];  // this thread's own pass-2 stores
+        const float4 w = __ldg(b4 + i);
+        o4[i] = make_float4((h.x * inv2) * w.x, (h.y * inv2) * w.y, (h.z * inv2) * w.z,
+                            (h.w * inv2) * w.w);
+    }
+}
+
+// SiLU(g) * u in binary32 (z/(1+exp(-z)) with CUDA's expf and IEEE division).
+__device__ __forceinline__ float silu_mul_f(float g, float u) {
+    return (g / (1.0f + expf(-g))) * u;
+}
+
+}  // namespace muser

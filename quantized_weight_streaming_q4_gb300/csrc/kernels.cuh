@@ -1,0 +1,58 @@
+// kernels.cuh -- launch interfaces between libmuser's translation units.
+#pragma once
+
+#include "common.cuh"
+
+namespace muser {
+
+enum EpiKind { kEpiStore = 0, kEpiSiluMul = 1, kEpiTail = 2 };
+
+// One-token matvec (mv1.cu).  W[0..NMAT-1] share rows x (nsb*256) and x.
+struct Mv1Args {
+    const uint8_t* W[2];
+    int64_t rows;
+    int nsb;
+    const float* x;
+    float* y0;  // store: y of W[0]; silu: mid; tail: projected
+    float* y1;  // store with two matrices: y of W[1]
+    // tail epilogue
+    float* resid;
+    float* out;
+    const float* w1;
+    const float* w2;
+    float eps1, eps2;
+    unsigned* ticket;
+    // geometry, filled by the launcher
+    int G, RS, ns;
+    uint32_t stage_bytes;
+    int part_off, stage_off;
+};
+bool mv1_supported(int qtype, int64_t cols);
+int launch_mv1(int qtype, int nmat, int epi, const Mv1Args& a, cudaStream_t s);
+
+// Multi-row matvec (mvM.cu): y[m*rows + r], m < M <= 16.
+struct MvMArgs {
+    const uint8_t* W[2];
+    int64_t rows;
+    int nsb;
+    const float* x;
+    int M;
+    float* y0;
+    float* y1;
+};
+int launch_mvM(int qtype, int nmat, int epi, const MvMArgs& a, cudaStream_t s);
+
+// misc.cu
+int launch_dequantize(int qtype, const uint8_t* W, int64_t rows, int64_t cols, float* out,
+                      cudaStream_t s);
+int launch_rms_norm(const float* x, const float* w, float* out, int n, int M, float eps,
+                    cudaStream_t s);
+int launch_silu_mul(const float* a, const float* b, float* out, int64_t n, cudaStream_t s);
+int launch_dual_tail(float* resid, const float* src, float* out, const float* w1,
+                     const float* w2, int n, int M, float eps1, float eps2, cudaStream_t s);
+int launch_kv_store(uint16_t* key, uint16_t* value, const float* k, const float* v,
+                    int64_t kv_dim, int64_t head_dim, int head_major, int64_t capacity,
+                    int64_t phys_of_first, int64_t src_first, int64_t nrows, cudaStream_t s);
+int launch_spin(int64_t microseconds, cudaStream_t s);
+
+}  // namespace muser

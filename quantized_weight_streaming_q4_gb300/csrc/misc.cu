@@ -1,0 +1,197 @@
+// misc.cu -- the small kernels of the path: exact dequantisation (the
+// bit-exact test hook), RMSNorm, SiLU gating, the standalone dual-eps tail,
+// the f16 K/V ring store, and a bounded spin used to test muser_sync.
+#include "common.cuh"
+#include "kernels.cuh"
+
+namespace muser {
+
+namespace {
+
+// ----------------------------------------------------------- dequantize
+// One thread per 32-weight sub-block slot (see mvM.cu for the same slot
+// arithmetic): value = the exactly rounded binary32 of the block formula.
+__global__ void dequant_q4k_kernel(const uint8_t* __restrict__ W, int64_t nblocks,
+                                   float* __restrict__ out) {
+    const int64_t gid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (gid >= nblocks * 8) return;
+    const int64_t blkno = gid >> 3;
+    const int j = static_cast<int>(gid & 7);
+    const uint8_t* blk = W + blkno * kQ4KBytes;
+    const uint4 hd = *reinterpret_cast<const uint4*>(blk);
+    const int c = j >> 1;
+    const uint4 qa = *reinterpret_cast<const uint4*>(blk + 16 + 32 * c);
+    const uint4 qb = *reinterpret_cast<const uint4*>(blk + 32 + 32 * c);
+    uint32_t sc, mn;
+    if (j < 4) {
+        sc = (hd.y >> (8 * j)) & 63u;
+        mn = (hd.z >> (8 * j)) & 63u;
+    } else {
+        const int jj = j - 4;
+        sc = ((hd.w >> (8 * jj)) & 0x0Fu) | (((hd.y >> (8 * jj + 6)) & 3u) << 4);
+        mn = ((hd.w >> (8 * jj + 4)) & 0x0Fu) | (((hd.z >> (8 * jj + 6)) & 3u) << 4);
+    }
+    const float dsc = __fmul_rn(h2f(hd.x), static_cast<float>(sc));
+    const float ndm = -__fmul_rn(h2f(hd.x >> 16), static_cast<float>(mn));
+    const uint32_t words[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
+    const int sh = (j & 1) ? 4 : 0;
+    float* o = out + blkno * kQK + 32 * j;
+#pragma unroll
+    for (int t = 0; t < 8; ++t) {
+        const uint32_t q4 = (words[t] >> sh) & 0x0F0F0F0Fu;
+        float4 v;
+        v.x = __fmaf_rn(dsc, static_cast<float>(q4 & 0xFFu), ndm);
+        v.y = __fmaf_rn(dsc, static_cast<float>((q4 >> 8) & 0xFFu), ndm);
+        v.z = __fmaf_rn(dsc, static_cast<float>((q4 >> 16) & 0xFFu), ndm);
+        v.w = __fmaf_rn(dsc, static_cast<float>(q4 >> 24), ndm);
+        reinterpret_cast<float4*>(o)[t] = v;
+    }
+}
+
+__global__ void dequant_q6k_kernel(const uint8_t* __restrict__ W, int64_t nblocks,
+                                   float* __restrict__ out) {
+    const int64_t gid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (gid >= nblocks * 8) return;
+    const int64_t blkno = gid >> 3;
+    const int j8 = static_cast<int>(gid & 7);
+    const int h = j8 >> 2, g = j8 & 3;
+    const uint8_t* blk = W + blkno * kQ6KBytes;
+    const float d = h2f(ldg_u16(blk + 208));
+    const float dsc0 = __fmul_rn(d, static_cast<float>(static_cast<int8_t>(ldg_u8(blk + 192 + 8 * h + 2 * g))));
+    const float dsc1 = __fmul_rn(d, static_cast<float>(static_cast<int8_t>(ldg_u8(blk + 193 + 8 * h + 2 * g))));
+    const uint8_t* ql = blk + 64 * h + 32 * (g & 1);
+    const uint8_t* qh = blk + 128 + 32 * h;
+    float* o = out + blkno * kQK + 128 * h + 32 * g;
+    for (int l = 0; l < 32; ++l) {
+        const uint32_t lb = ldg_u8(ql + l), hb = ldg_u8(qh + l);
+        const uint32_t q = ((g & 2) ? (lb >> 4) : (lb & 0x0Fu)) | (((hb >> (2 * g)) & 3u) << 4);
+        o[l] = __fmul_rn(l < 16 ? dsc0 : dsc1, static_cast<float>(static_cast<int>(q) - 32));
+    }
+}
+
+// ------------------------------------------------------------ RMSNorm
+// One block per row (Muser book Ch 2 §2.6 rms_norm_batch):
+// out = (x * inv) * w, inv = 1/sqrt(mean(x^2) + eps).
+__global__ void rms_norm_kernel(const float* x, const float* __restrict__ w, float* out, int n,
+                                float eps) {
+    __shared__ float red[33];
+    const float4* x4 = reinterpret_cast<const float4*>(x + static_cast<int64_t>(blockIdx.x) * n);
+    float4* o4 = reinterpret_cast<float4*>(out + static_cast<int64_t>(blockIdx.x) * n);
+    const float4* w4 = reinterpret_cast<const float4*>(w);
+    const int n4 = n >> 2;
+    float ss = 0.0f;
+    for (int i = threadIdx.x; i < n4; i += blockDim.x) {
+        const float4 v = x4[i];
+        ss = fmaf(v.x, v.x, ss);
+        ss = fmaf(v.y, v.y, ss);
+        ss = fmaf(v.z, v.z, ss);
+        ss = fmaf(v.w, v.w, ss);
+    }
+    ss = block_sum(ss, red);
+    const float inv = 1.0f / sqrtf(ss / static_cast<float>(n) + eps);
+    for (int i = threadIdx.x; i < n4; i += blockDim.x) {
+        const float4 v = x4[i];
+        const float4 ww = __ldg(w4 + i);
+        o4[i] = make_float4((v.x * inv) * ww.x, (v.y * inv) * ww.y, (v.z * inv) * ww.z,
+                            (v.w * inv) * ww.w);
+    }
+}
+
+__global__ void silu_mul_kernel(const float* a, const float* b, float* out, int64_t n) {
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+        out[i] = silu_mul_f(a[i], b[i]);
+}
+
+// One block per row; the page's kernel uses one 1,024-thread group per row.
+__global__ void dual_tail_kernel(float* resid, const float* src, float* out, const float* w1,
+                                 const float* w2, int n, float eps1, float eps2) {
+    __shared__ float red[33];
+    const int64_t off = static_cast<int64_t>(blockIdx.x) * n;
+    block_dual_tail_row(resid + off, src + off, out + off, w1, w2, n, eps1, eps2, red);
+}
+
+// -------------------------------------------------------------- KV store
+// Muser book Ch 15 §15.4 (muser_kv_store_batch_f16): source row t of the batch
+// (t >= src_first) lands in physical row (phys_of_first + t) % capacity; the
+// binary32 -> binary16 conversion rounds to nearest even.
+__global__ void kv_store_kernel(uint16_t* key, uint16_t* value, const float* k, const float* v,
+                                int64_t kv_dim, int64_t head_dim, int head_major,
+                                int64_t capacity, int64_t phys_of_first, int64_t src_first,
+                                int64_t nrows) {
+    const int64_t total = nrows * kv_dim;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t t = src_first + i / kv_dim;
+        const int64_t e = i % kv_dim;
+        const int64_t phys = (phys_of_first + t) % capacity;
+        int64_t dst = phys * kv_dim + e;
+        if (head_major) dst = ((e / head_dim) * capacity + phys) * head_dim + e % head_dim;
+        const int64_t s = t * kv_dim + e;
+        key[dst] = __half_as_ushort(__float2half_rn(k[s]));
+        value[dst] = __half_as_ushort(__float2half_rn(v[s]));
+    }
+}
+
+// Busy-waits on the global nanosecond timer; returns after `ns` (bounded).
+__global__ void spin_kernel(uint64_t ns) {
+    uint64_t t0, t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
+    do {
+        __nanosleep(1000);
+        asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    } while (t - t0 < ns);
+}
+
+}  // namespace
+
+int launch_dequantize(int qtype, const uint8_t* W, int64_t rows, int64_t cols, float* out,
+                      cudaStream_t s) {
+    const int64_t nblocks = rows * (cols / kQK);
+    const int64_t threads = nblocks * 8;
+    if (threads == 0) return MUSER_OK;
+    const int bs = 256;
+    const int64_t grid = (threads + bs - 1) / bs;
+    if (qtype == MUSER_Q4_K) dequant_q4k_kernel<<<static_cast<unsigned>(grid), bs, 0, s>>>(W, nblocks, out);
+    else dequant_q6k_kernel<<<static_cast<unsigned>(grid), bs, 0, s>>>(W, nblocks, out);
+    return check_launch("dequantize");
+}
+
+int launch_rms_norm(const float* x, const float* w, float* out, int n, int M, float eps,
+                    cudaStream_t s) {
+    rms_norm_kernel<<<M, 1024, 0, s>>>(x, w, out, n, eps);
+    return check_launch("rms_norm");
+}
+
+int launch_silu_mul(const float* a, const float* b, float* out, int64_t n, cudaStream_t s) {
+    if (n == 0) return MUSER_OK;
+    const int bs = 256;
+    const int64_t grid = std::min<int64_t>((n + bs - 1) / bs, static_cast<int64_t>(sm_count()) * 16);
+    silu_mul_kernel<<<static_cast<unsigned>(grid), bs, 0, s>>>(a, b, out, n);
+    return check_launch("silu_mul");
+}
+
+int launch_dual_tail(float* resid, const float* src, float* out, const float* w1,
+                     const float* w2, int n, int M, float eps1, float eps2, cudaStream_t s) {
+    dual_tail_kernel<<<M, 1024, 0, s>>>(resid, src, out, w1, w2, n, eps1, eps2);
+    return check_launch("dual_tail");
+}
+
+int launch_kv_store(uint16_t* key, uint16_t* value, const float* k, const float* v,
+                    int64_t kv_dim, int64_t head_dim, int head_major, int64_t capacity,
+                    int64_t phys_of_first, int64_t src_first, int64_t nrows, cudaStream_t s) {
+    const int64_t total = nrows * kv_dim;
+    if (total == 0) return MUSER_OK;
+    const int bs = 256;
+    const int64_t grid = std::min<int64_t>((total + bs - 1) / bs, static_cast<int64_t>(sm_count()) * 8);
+    kv_store_kernel<<<static_cast<unsigned>(grid), bs, 0, s>>>(
+        key, value, k, v, kv_dim, head_dim, head_major, capacity, phys_of_first, src_first, nrows);
+    return check_launch("kv_store");
+}
+
+int launch_spin(int64_t microseconds, cudaStream_t s) {
+    spin_kernel<<<1, 1, 0, s>>>(static_cast<uint64_t>(microseconds) * 1000ull);
+    return check_launch("spin");
+}
+
+}  // namespace muser

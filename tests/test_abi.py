@@ -1,0 +1,125 @@
+"""The C ABI without a GPU: libmuser builds for sm_103a, loads, exports every
+function include/muser.h declares, and its host-side argument checks fail
+closed (no CUDA call is reached on these paths)."""
+import ctypes
+import os
+import re
+import shutil
+
+import pytest
+
+import quantized_weight_streaming_q4_gb300 as mu
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "muser.h")
+
+needs_nvcc = pytest.mark.skipif(shutil.which("nvcc") is None and not os.path.exists("/usr/local/cuda/bin/nvcc"),
+                                reason="nvcc not available")
+
+
+@pytest.fixture(scope="module")
+def L():
+    mu.build()
+    return mu.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(muser_[a-z0-9_]+)\s*\(", text)))
+
+
+@needs_nvcc
+def test_every_declared_symbol_is_exported(L):
+    names = declared_functions()
+    assert len(names) >= 15
+    missing = [n for n in names if not hasattr(L, n)]
+    assert not missing, missing
+
+
+@needs_nvcc
+def test_sizes_and_version(L):
+    assert mu.muser_version() == 1
+    assert mu.muser_block_bytes("q4_k") == 144 and mu.muser_block_bytes("q6_k") == 210
+    assert mu.muser_block_bytes(7) == 0
+    assert mu.muser_matrix_bytes("q4_k", 6656, 19968) == 74760192
+    assert mu.muser_matrix_bytes("q6_k", 6656, 19968) == 109025280
+    assert mu.muser_matrix_bytes("q4_k", 1, 300) == 0
+    assert mu.muser_scratch_bytes(6656, 1) >= 16
+    assert mu.muser_ffn_workspace_bytes(6656, 19968, 16) >= 4 * (2 * 16 * 6656 + 16 * 19968 + 16 * 6656)
+
+
+FAKE = 1 << 20  # an aligned, never-dereferenced pointer value
+
+
+@needs_nvcc
+@pytest.mark.parametrize("args,status", [
+    ((99, FAKE, 8, 256, FAKE, 1, FAKE), -2),         # unknown quant type
+    ((12, None, 8, 256, FAKE, 1, FAKE), -1),         # NULL weights
+    ((12, FAKE, 8, 300, FAKE, 1, FAKE), -1),         # cols not a multiple of 256
+    ((12, FAKE, 0, 256, FAKE, 1, FAKE), -1),         # no rows
+    ((12, FAKE + 4, 8, 256, FAKE, 1, FAKE), -3),     # misaligned weights
+    ((12, FAKE, 8, 256, FAKE + 8, 1, FAKE), -3),     # misaligned x
+    ((12, FAKE, 8, 256, FAKE, 0, FAKE), -1),         # M = 0
+    ((14, FAKE, 8, 256, FAKE, 17, FAKE), -1),        # M = 17
+])
+def test_qmatvec_rejects_bad_arguments(L, args, status):
+    rc = L.muser_qmatvec(*args, None)
+    assert rc == status
+    assert mu.muser_last_error()
+
+
+@needs_nvcc
+def test_tail_and_fused_reject_bad_arguments(L):
+    assert L.muser_fused_residual_dual_rmsnorm(FAKE, FAKE, FAKE, FAKE, FAKE, 6, 1, 1e-8, 1e-5, None) == -1
+    assert L.muser_fused_residual_dual_rmsnorm(FAKE, FAKE, FAKE, FAKE, FAKE, 8, 1, 0.0, 1e-5, None) == -1
+    assert L.muser_fused_residual_dual_rmsnorm(FAKE, FAKE, FAKE, FAKE, FAKE, 8, 1, 1e-8, 1e-5, None) == -1  # out aliases residual
+    rc = L.muser_qmatvec_residual_dual_rmsnorm(12, FAKE, 6656, 19968, FAKE, 1, FAKE, FAKE + 256, FAKE + 512,
+                                               FAKE, FAKE, 1e-8, 1e-5, FAKE, 8, None)
+    assert rc == -1 and "scratch" in mu.muser_last_error()
+    # every call below fails validation before any launch (fake pointers are never used)
+    assert L.muser_ffn_gate_up_silu(14, FAKE, FAKE, 100, 6600, FAKE, 1, FAKE, None) == -1
+
+
+@needs_nvcc
+def test_stack_rejects_bad_layers(L):
+    layer = mu.FfnLayer(FAKE, FAKE, FAKE + 4, FAKE, FAKE, 12, 14)   # misaligned down matrix
+    arr = (mu.FfnLayer * 1)(layer)
+    ws = mu.muser_ffn_workspace_bytes(512, 1024, 1)
+    rc = L.muser_ffn_stack(arr, 1, FAKE, 512, 1024, 1, FAKE, FAKE * 2, 1e-5, 1e-8, FAKE * 4, ws, None)
+    assert rc == -3
+    rc = L.muser_ffn_stack(arr, 0, FAKE, 512, 1024, 1, FAKE, FAKE * 2, 1e-5, 1e-8, FAKE * 4, ws, None)
+    assert rc == -1
+    good = (mu.FfnLayer * 1)(mu.FfnLayer(FAKE, FAKE, FAKE, FAKE, FAKE, 12, 14))
+    rc = L.muser_ffn_stack(good, 1, FAKE, 512, 1024, 1, FAKE, FAKE * 2, 1e-5, 1e-8, FAKE * 4, ws - 16, None)
+    assert rc == -1 and "workspace" in mu.muser_last_error()
+
+
+@needs_nvcc
+def test_kv_ring_discontinuity_fails_closed_without_touching_the_plane(L):
+    plane = mu.KvPlane(FAKE, FAKE * 2, 2048, 2048, 5, 5, 256, 128, 0, 0)
+    first = ctypes.c_int64(-7)
+    for bad in (2052, 2054, 0):
+        rc = L.muser_kv_ring_write(ctypes.byref(plane), FAKE, FAKE, bad, 1, ctypes.byref(first), None)
+        assert rc == -4
+        assert "discontinuity" in mu.muser_last_error()
+        assert (plane.len, plane.origin_logical, plane.origin_physical) == (2048, 5, 5)
+        assert first.value == -7
+    # zero rows at the right position is a no-op that reports the write row
+    rc = L.muser_kv_ring_write(ctypes.byref(plane), None, None, 2053, 0, ctypes.byref(first), None)
+    assert rc == 0 and first.value == 5
+    # inconsistent metadata is rejected
+    bad_plane = mu.KvPlane(FAKE, FAKE, 32, 40, 0, 0, 256, 128, 0, 0)
+    assert L.muser_kv_ring_write(ctypes.byref(bad_plane), FAKE, FAKE, 40, 1, None, None) == -1
+
+
+@needs_nvcc
+def test_debug_spin_bound(L):
+    assert L.muser_debug_spin(11 * 1000 * 1000, None) == -1
+
+
+def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
+    monkeypatch.setattr(mu, "_lib", None)
+    monkeypatch.setattr(mu, "_LIB", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="not built"):
+        mu.lib()

@@ -1,0 +1,273 @@
+"""GPU parity of every libmuser entry point against the fp64 oracle, through
+the C ABI, on seeded inputs that span several tiles and ragged tails.
+
+Bit-exact: dequantised weights, one-hot matvec columns, K/V planes and ring
+metadata.  Floating point: the path's bound (tests/gpu_util.py)."""
+import ctypes
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from tests.gpu_util import assert_close, check_canary, dev, host, nan_like
+from tests.kquant_pack import pack_q4k, pack_q6k
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+import quantized_weight_streaming_q4_gb300 as mu  # noqa: E402
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    mu.build()
+    mu.lib()
+    torch.cuda.init()
+    yield
+    torch.cuda.synchronize()
+
+
+def _qmatvec(qtype, W, rows, cols, x, canary=64):
+    M = x.shape[0]
+    Wd, xd = dev(W), dev(x)
+    y = nan_like((M, rows), extra=canary)
+    mu.muser_qmatvec(qtype, Wd, rows, cols, xd, M, y)
+    out = host(y[:M * rows]).reshape(M, rows)
+    check_canary(y, M * rows)
+    return out
+
+
+# ------------------------------------------------------------ dequantize
+@pytest.mark.parametrize("qtype", ["q4_k", "q6_k"])
+@pytest.mark.parametrize("rows,cols", [(1, 256), (37, 768), (512, 2048), (300, 6656)])
+def test_dequantize_bit_exact(qtype, rows, cols):
+    W = synth.qmatrix(qtype, rows, cols, seed=rows + cols)
+    out = nan_like((rows, cols), extra=16)
+    mu.muser_dequantize(qtype, dev(W), rows, cols, out)
+    got = host(out[:rows * cols]).reshape(rows, cols)
+    check_canary(out, rows * cols)
+    ref = oracle.dequantize(qtype, W, rows, cols)
+    assert np.array_equal(got.view(np.uint32), ref.view(np.uint32))
+
+
+def test_dequantize_extreme_blocks_bit_exact():
+    rng = np.random.default_rng(0)
+    blocks4 = [pack_q4k(65504.0, 2.0 ** -24, [63] * 8, [63] * 8, list(range(16)) * 16),
+               pack_q4k(2.0 ** -24, 65504.0, [63] * 8, [0] * 8, [15] * 256),
+               pack_q4k(6.1e-5, 3.0e-7, rng.integers(0, 64, 8), rng.integers(0, 64, 8), rng.integers(0, 16, 256)),
+               pack_q4k(0.0, 0.0, [5] * 8, [5] * 8, [7] * 256)]
+    W4 = np.concatenate(blocks4).reshape(1, -1)
+    out = nan_like((1, 1024))
+    mu.muser_dequantize("q4_k", dev(W4), 1, 1024, out)
+    assert np.array_equal(host(out).view(np.uint32), oracle.dequantize("q4_k", W4, 1, 1024).ravel().view(np.uint32))
+    blocks6 = [pack_q6k(65504.0, [127] * 8 + [-128] * 8, list(range(64)) * 4),
+               pack_q6k(2.0 ** -24, rng.integers(-128, 128, 16), rng.integers(0, 64, 256)),
+               pack_q6k(1.0, [-128] * 16, [0] * 256)]
+    W6 = np.concatenate(blocks6 + [blocks6[0]]).reshape(1, -1)
+    out = nan_like((1, 1024))
+    mu.muser_dequantize("q6_k", dev(W6), 1, 1024, out)
+    assert np.array_equal(host(out).view(np.uint32), oracle.dequantize("q6_k", W6, 1, 1024).ravel().view(np.uint32))
+
+
+# ---------------------------------------------------------------- matvec
+@pytest.mark.parametrize("qtype", ["q4_k", "q6_k"])
+@pytest.mark.parametrize("rows,cols", [(512, 2048), (37, 768), (5, 256), (1, 512), (997, 6656),
+                                       (300, 19968)])
+def test_qmatvec_m1(qtype, rows, cols):
+    W = synth.qmatrix(qtype, rows, cols, seed=3 * rows + cols)
+    x = synth.normal((1, cols), seed=rows, tensor=synth.T_X)
+    got = _qmatvec(qtype, W, rows, cols, x)
+    ref = oracle.qmatvec(qtype, W, rows, cols, x)
+    assert_close(got, ref, f"{qtype} {rows}x{cols} M=1", scaled=True)
+
+
+@pytest.mark.parametrize("qtype", ["q4_k", "q6_k"])
+@pytest.mark.parametrize("M", [2, 3, 5, 8, 16])
+@pytest.mark.parametrize("rows,cols", [(100, 768), (37, 2048)])
+def test_qmatvec_multirow(qtype, M, rows, cols):
+    W = synth.qmatrix(qtype, rows, cols, seed=M + rows)
+    x = synth.normal((M, cols), seed=M, tensor=synth.T_X)
+    got = _qmatvec(qtype, W, rows, cols, x)
+    ref = oracle.qmatvec(qtype, W, rows, cols, x)
+    assert_close(got, ref, f"{qtype} {rows}x{cols} M={M}", scaled=True)
+
+
+@pytest.mark.parametrize("qtype", ["q4_k", "q6_k"])
+def test_qmatvec_one_hot_columns_bit_exact(qtype):
+    # x = e_j picks column j of the dequantised matrix exactly (one product by
+    # 1.0, every other term an exact zero), so every code and scale position
+    # of the kernels' layout arithmetic is pinned against the oracle.
+    rows, cols = 64, 768
+    W = synth.qmatrix(qtype, rows, cols, seed=77)
+    dense = oracle.dequantize(qtype, W, rows, cols)
+    Wd = dev(W)
+    y = nan_like((16, rows))
+    js = list(range(0, cols, 5)) + [cols - 1]
+    for j in js:  # M = 1 path
+        x = np.zeros((1, cols), np.float32)
+        x[0, j] = 1.0
+        mu.muser_qmatvec(qtype, Wd, rows, cols, dev(x), 1, y)
+        got = host(y[:rows])
+        assert np.array_equal(got.view(np.uint32) & 0x7FFFFFFF, dense[:, j].view(np.uint32) & 0x7FFFFFFF), j
+    for base in range(0, cols, 16):  # M = 16 path: sixteen one-hot rows at once
+        x = np.zeros((16, cols), np.float32)
+        for m in range(16):
+            x[m, base + m] = 1.0
+        mu.muser_qmatvec(qtype, Wd, rows, cols, dev(x), 16, y)
+        got = host(y).reshape(16, rows)
+        ref = dense[:, base:base + 16].T
+        assert np.array_equal(got.view(np.uint32) & 0x7FFFFFFF, ref.view(np.uint32) & 0x7FFFFFFF), base
+
+
+# ------------------------------------------------------- gate / up / SiLU
+@pytest.mark.parametrize("M", [1, 4, 16])
+def test_ffn_gate_up_silu(M):
+    ffn, hidden = 2000 + M, 6656
+    Wg = synth.q4k_matrix(ffn, hidden, seed=M, tensor=synth.T_GATE)
+    Wu = synth.q4k_matrix(ffn, hidden, seed=M, tensor=synth.T_UP)
+    x = oracle.rms_norm(synth.normal((M, hidden), seed=M), synth.norm_weight(hidden, seed=M), 1e-5)
+    mid = nan_like((M, ffn), extra=32)
+    mu.muser_ffn_gate_up_silu("q4_k", dev(Wg), dev(Wu), ffn, hidden, dev(x), M, mid)
+    got = host(mid[:M * ffn]).reshape(M, ffn)
+    check_canary(mid, M * ffn)
+    ref = oracle.gate_up_silu("q4_k", Wg, Wu, ffn, hidden, x)
+    assert_close(got, ref, f"gate_up_silu M={M}", scaled=True)
+
+
+def test_silu_mul_and_rms_norm():
+    a, b = synth.ffn_mid_factors(19968, 3, seed=9)
+    out = nan_like((3, 19968))
+    mu.muser_silu_mul(dev(a), dev(b), out, a.size)
+    assert_close(host(out).reshape(3, -1), oracle.silu_mul(a, b), "silu_mul")
+    x = synth.normal((5, 6656), seed=10) * np.float32(7.0)
+    w = synth.norm_weight(6656, seed=10)
+    o = nan_like((5, 6656))
+    mu.muser_rms_norm(dev(x), dev(w), o, 6656, 5, 1e-5)
+    assert_close(host(o).reshape(5, -1), oracle.rms_norm(x, w, 1e-5), "rms_norm")
+
+
+# ------------------------------------------------------------- dual tail
+def test_tail_worked_example_from_book():
+    r = dev(np.array([[1, 2, 3, 4]], np.float32))
+    p = dev(np.array([[4, 0, 0, 0]], np.float32))
+    ones = dev(np.ones(4, np.float32))
+    out = nan_like((1, 4))
+    mu.muser_fused_residual_dual_rmsnorm(r, p, out, ones, ones, 4, 1, 1e-8, 1e-5)
+    np.testing.assert_allclose(host(r)[0], [3, 2, 3, 4], atol=1e-6)
+    np.testing.assert_allclose(host(out), [0.973, 0.649, 0.973, 1.297], atol=1e-3)
+
+
+@pytest.mark.parametrize("M,n", [(1, 6656), (16, 6656), (3, 4100)])
+def test_fused_residual_dual_rmsnorm(M, n):
+    r = synth.normal((M, n), seed=n + M, tensor=synth.T_RESID)
+    p = synth.normal((M, n), seed=n + M, tensor=synth.T_X) * np.float32(2.5e6)
+    w1 = synth.norm_weight(n, seed=M, tensor=synth.T_W1)
+    w2 = synth.norm_weight(n, seed=M, tensor=synth.T_W2)
+    rd, out = dev(r), nan_like((M, n))
+    mu.muser_fused_residual_dual_rmsnorm(rd, dev(p), out, dev(w1), dev(w2), n, M, 1e-8, 1e-5)
+    r_ref, out_ref = oracle.dual_tail(r, p, w1, w2, 1e-8, 1e-5)
+    assert_close(host(rd), r_ref, "tail residual")
+    assert_close(host(out).reshape(M, n), out_ref, "tail out")
+
+
+def test_tail_zero_projection_keeps_residual_bit_exact():
+    n = 6656
+    r = synth.normal((2, n), seed=1, tensor=synth.T_RESID)
+    rd = dev(r)
+    out = nan_like((2, n))
+    w = dev(synth.norm_weight(n, seed=1))
+    mu.muser_fused_residual_dual_rmsnorm(rd, dev(np.zeros_like(r)), out, w, w, n, 2, 1e-8, 1e-5)
+    assert np.array_equal(host(rd), r)
+
+
+@pytest.mark.parametrize("qtype", ["q4_k", "q6_k"])
+@pytest.mark.parametrize("M", [1, 16])
+def test_down_projection_with_fused_tail(qtype, M):
+    hidden, ffn = 6656, 19968 if M == 1 else 2048
+    case = synth.down_tail_case(qtype, hidden, ffn, M, seed=5)
+    a, b = case["a"], case["b"]
+    mid_d = nan_like((M, ffn))
+    mu.muser_silu_mul(dev(a), dev(b), mid_d, a.size)
+    mid_ref = oracle.silu_mul(a, b)
+    Wd, w1, w2 = dev(case["W"]), dev(case["w1"]), dev(case["w2"])
+    resid = dev(case["resid"])
+    proj, out = nan_like((M, hidden)), nan_like((M, hidden))
+    nscr = mu.muser_scratch_bytes(hidden, M)
+    scratch = torch.zeros(nscr // 4 + 4, dtype=torch.float32, device="cuda")
+    p_ref, r_ref, o_ref = oracle.down_tail(qtype, case["W"], hidden, ffn, mid_ref, case["resid"],
+                                           case["w1"], case["w2"])
+    mu.muser_qmatvec_residual_dual_rmsnorm(qtype, Wd, hidden, ffn, mid_d, M, proj, resid, out, w1,
+                                           w2, 1e-8, 1e-5, scratch, nscr)
+    assert_close(host(proj).reshape(M, hidden), p_ref, "projected", scaled=True)
+    assert_close(host(resid), r_ref, "residual")
+    assert_close(host(out).reshape(M, hidden), o_ref, "next-norm output")
+    assert not host(scratch).any(), "scratch must be left zeroed"
+    # a second call on the updated residual (scratch reuse) matches the oracle too
+    _, r_ref2, o_ref2 = oracle.down_tail(qtype, case["W"], hidden, ffn, mid_ref, r_ref,
+                                         case["w1"], case["w2"])
+    mu.muser_qmatvec_residual_dual_rmsnorm(qtype, Wd, hidden, ffn, mid_d, M, proj, resid, out, w1,
+                                           w2, 1e-8, 1e-5, scratch, nscr)
+    assert_close(host(resid), r_ref2, "residual (second call)")
+    assert_close(host(out).reshape(M, hidden), o_ref2, "output (second call)")
+    assert mu.muser_device_status() == 0
+
+
+# ---------------------------------------------------------------- KV ring
+def _plane_pair(cap, kv_dim, head_dim, head_major):
+    key = torch.full((cap * kv_dim,), 0xDEAD, dtype=torch.int32, device="cuda").to(torch.int16)
+    val = key.clone()
+    plane = mu.KvPlane(key.data_ptr(), val.data_ptr(), cap, 0, 0, 0, kv_dim, head_dim,
+                       1 if head_major else 0, 0)
+    ring = oracle.Ring(cap, 0, 0, 0)
+    okey = np.full(cap * kv_dim, 0xDEAD, np.uint16)
+    oval = okey.copy()
+    return key, val, plane, ring, okey, oval
+
+
+@pytest.mark.parametrize("head_major", [False, True])
+@pytest.mark.parametrize("cap", [32, 2048])
+def test_kv_ring_write_bit_exact(head_major, cap):
+    kv_dim, head_dim = 256, 128
+    key, val, plane, ring, okey, oval = _plane_pair(cap, kv_dim, head_dim, head_major)
+    pos = 0
+    counts = [1, 1, 30, 1, 1, 5, cap + 3, 1, 2]   # crosses the wrap, and one batch > capacity
+    for step, count in enumerate(counts):
+        k, v = synth.kv_rows(count, kv_dim, seed=step, step=step)
+        k[0, :3] = [70000.0, -1e-9, 65519.0]  # overflow, underflow, tie cases
+        first = mu.muser_kv_ring_write(plane, dev(k), dev(v), pos, count)
+        rc, ofirst = oracle.kv_write(ring, okey, oval, kv_dim, head_dim, head_major, k, v, pos)
+        assert rc == 0 and first == ofirst
+        assert (plane.len, plane.origin_logical, plane.origin_physical) == (
+            ring.len, ring.origin_logical, ring.origin_physical)
+        pos += count
+    assert np.array_equal(host(key).view(np.uint16), okey)
+    assert np.array_equal(host(val).view(np.uint16), oval)
+
+
+def test_kv_ring_discontinuity_leaves_planes_untouched():
+    key, val, plane, ring, okey, oval = _plane_pair(32, 256, 128, False)
+    k, v = synth.kv_rows(40, 256, seed=1)
+    mu.muser_kv_ring_write(plane, dev(k), dev(v), 0, 40)
+    before = (host(key).copy(), host(val).copy(), plane.len, plane.origin_logical, plane.origin_physical)
+    for bad in (39, 41, 0):
+        with pytest.raises(mu.MuserError) as ei:
+            mu.muser_kv_ring_write(plane, dev(k[:1]), dev(v[:1]), bad, 1)
+        assert ei.value.status == -4
+    after = (host(key), host(val), plane.len, plane.origin_logical, plane.origin_physical)
+    assert np.array_equal(before[0], after[0]) and np.array_equal(before[1], after[1])
+    assert before[2:] == after[2:]
+
+
+# ----------------------------------------------------------------- sync
+def test_sync_bounded_wait_times_out_then_completes():
+    s = torch.cuda.Stream()
+    mu.muser_debug_spin(300_000, s)   # a bounded 0.3 s kernel
+    assert mu.muser_sync(s, 20) == -6
+    assert mu.muser_sync(s, -1) == 0
+    assert mu.muser_sync(s, 1000) == 0
+
+
+def test_device_status_clean():
+    torch.cuda.synchronize()
+    assert mu.muser_device_status() == 0

@@ -1,0 +1,137 @@
+"""The five workloads at their full sizes, on the GPU, against the oracle.
+
+0: Q4_K 512x2048 matvec; 1/2: Q4_K / Q6_K W_down 6656x19968 + dual-eps tail;
+3: one decode-FFN block (M = 1, gate/up Q4_K, down Q6_K); 4: 52 layers at
+M = 16 (the oracle follows two of the sixteen independent rows through every
+layer; a 3-layer slice is checked on all sixteen rows)."""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from tests.gpu_util import assert_close, dev, host, nan_like
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+import quantized_weight_streaming_q4_gb300 as mu  # noqa: E402
+
+H, F = synth.HIDDEN, synth.FFN
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    mu.build()
+    mu.lib()
+    torch.cuda.init()
+
+
+def test_workload0_q4k_matvec_512x2048():
+    W, x = synth.matvec_case(512, 2048, 1, "q4_k", seed=0, workload=0)
+    y = nan_like((1, 512))
+    mu.muser_qmatvec("q4_k", dev(W), 512, 2048, dev(x), 1, y)
+    assert_close(host(y).reshape(1, 512), oracle.qmatvec("q4_k", W, 512, 2048, x), "workload 0", scaled=True)
+
+
+@pytest.mark.parametrize("qtype,wl", [("q4_k", 1), ("q6_k", 2)])
+def test_workloads_1_2_down_projection_and_tail(qtype, wl):
+    case = synth.down_tail_case(qtype, H, F, 1, seed=0, workload=wl)
+    mid = nan_like((1, F))
+    mu.muser_silu_mul(dev(case["a"]), dev(case["b"]), mid, F)
+    mid_ref = oracle.silu_mul(case["a"], case["b"])
+    assert_close(host(mid).reshape(1, F), mid_ref, "ffn_mid", scaled=True)
+    resid = dev(case["resid"])
+    proj, out = nan_like((1, H)), nan_like((1, H))
+    nscr = mu.muser_scratch_bytes(H, 1)
+    scratch = torch.zeros(64, dtype=torch.float32, device="cuda")
+    mu.muser_qmatvec_residual_dual_rmsnorm(qtype, dev(case["W"]), H, F, mid, 1, proj, resid, out,
+                                           dev(case["w1"]), dev(case["w2"]), 1e-8, 1e-5, scratch,
+                                           nscr)
+    p_ref, r_ref, o_ref = oracle.down_tail(qtype, case["W"], H, F, mid_ref, case["resid"],
+                                           case["w1"], case["w2"])
+    assert_close(host(proj).reshape(1, H), p_ref, f"workload {wl} projected", scaled=True)
+    assert_close(host(resid), r_ref, f"workload {wl} residual")
+    assert_close(host(out).reshape(1, H), o_ref, f"workload {wl} output")
+
+
+def _layer_dev(L, w_next):
+    d = {k: dev(v) for k, v in L.items()}
+    d["w_next"] = dev(w_next)
+    return d
+
+
+def _ffn_layer_struct(d, down_qtype="q6_k"):
+    return mu.FfnLayer(d["Wg"].data_ptr(), d["Wu"].data_ptr(), d["Wd"].data_ptr(),
+                       d["w1"].data_ptr(), d["w_next"].data_ptr(), mu.MUSER_Q4_K,
+                       mu.QTYPES[down_qtype])
+
+
+def test_workload3_ffn_block_m1():
+    L = synth.ffn_layer(0, H, F, seed=0, workload=3)
+    w_in = synth.input_norm_weight(0, H, seed=0, workload=3)
+    w_next = synth.input_norm_weight(1, H, seed=0, workload=3)
+    r = synth.residual_rows(1, H, seed=0, workload=3)
+    x_ref, mid_ref, p_ref, r_ref, o_ref = oracle.ffn_block(r, w_in, L, w_next, H, F)
+    d = _layer_dev(L, w_next)
+    # the public one-call path
+    ws_bytes = mu.muser_ffn_workspace_bytes(H, F, 1)
+    ws = torch.zeros(ws_bytes // 4, dtype=torch.float32, device="cuda")
+    resid, out = dev(r), nan_like((1, H))
+    mu.muser_ffn_stack([_ffn_layer_struct(d)], dev(w_in), H, F, 1, resid, out, 1e-5, 1e-8, ws,
+                       ws_bytes)
+    assert_close(host(resid), r_ref, "block residual")
+    assert_close(host(out).reshape(1, H), o_ref, "block output")
+    # the same block step by step, every intermediate against the oracle
+    resid2, x, mid = dev(r), nan_like((1, H)), nan_like((1, F))
+    proj, out2 = nan_like((1, H)), nan_like((1, H))
+    mu.muser_rms_norm(resid2, dev(w_in), x, H, 1, 1e-5)
+    assert_close(host(x).reshape(1, H), x_ref, "normed input")
+    mu.muser_ffn_gate_up_silu("q4_k", d["Wg"], d["Wu"], F, H, x, 1, mid)
+    assert_close(host(mid).reshape(1, F), mid_ref, "ffn_mid", scaled=True)
+    scratch = torch.zeros(64, dtype=torch.float32, device="cuda")
+    mu.muser_qmatvec_residual_dual_rmsnorm("q6_k", d["Wd"], H, F, mid, 1, proj, resid2, out2,
+                                           d["w1"], d["w_next"], 1e-8, 1e-5, scratch, 256)
+    assert_close(host(proj).reshape(1, H), p_ref, "projected", scaled=True)
+    assert_close(host(resid2), r_ref, "residual")
+    assert_close(host(out2).reshape(1, H), o_ref, "output")
+
+
+def _stack(n_layers, M, rows_checked, seed=0):
+    wl = 4
+    w_in0 = synth.input_norm_weight(0, H, seed=seed, workload=wl)
+    r = synth.residual_rows(M, H, seed=seed, workload=wl)
+    x_ref = oracle.rms_norm(r[rows_checked], w_in0, 1e-5)
+    r_ref = r[rows_checked].copy()
+    keep, structs = [], []
+    for l in range(n_layers):
+        L = synth.ffn_layer(l, H, F, seed=seed, workload=wl)
+        w_next = synth.input_norm_weight(l + 1, H, seed=seed, workload=wl)
+        d = _layer_dev(L, w_next)
+        keep.append(d)
+        structs.append(_ffn_layer_struct(d))
+        r_ref, x_ref, _, _ = oracle.ffn_layer(x_ref, r_ref, L, w_next, H, F)
+        del L
+    ws_bytes = mu.muser_ffn_workspace_bytes(H, F, M)
+    ws = torch.zeros(ws_bytes // 4, dtype=torch.float32, device="cuda")
+    resid, out = dev(r), nan_like((M, H))
+    mu.muser_ffn_stack(structs, dev(w_in0), H, F, M, resid, out, 1e-5, 1e-8, ws, ws_bytes)
+    got_r = host(resid)
+    got_o = host(out).reshape(M, H)
+    assert np.isfinite(got_r).all() and np.isfinite(got_o).all()
+    del keep
+    return got_r[rows_checked], got_o[rows_checked], r_ref, x_ref
+
+
+def test_workload4_stack_slice_all_rows():
+    rows = np.arange(16)
+    gr, go, rr, orf = _stack(3, 16, rows)
+    assert_close(gr, rr, "3-layer stack residual (16 rows)")
+    assert_close(go, orf, "3-layer stack output (16 rows)")
+
+
+def test_workload4_full_52_layers_sampled_rows():
+    rows = np.array([0, 13])
+    gr, go, rr, orf = _stack(synth.N_LAYERS, 16, rows)
+    assert_close(gr, rr, "52-layer residual (rows 0, 13)")
+    assert_close(go, orf, "52-layer output (rows 0, 13)")
+    torch.cuda.empty_cache()
