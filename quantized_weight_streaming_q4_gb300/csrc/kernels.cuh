@@ -23,7 +23,9 @@ struct Mv1Args {
     float eps1, eps2;
     unsigned* ticket;
     // geometry, filled by the launcher
-    int G, RS, ns;
+    int G, RS, ns, nconsumer_warps;
+    int TG;  // consumer threads per row group
+    int HP;  // Q6_K parity split: first thread of the odd-block half
     uint32_t stage_bytes;
     int part_off, stage_off;
 };

@@ -35,166 +35,263 @@ namespace {
 
 constexpr float kTwo96 = 79228162514264337593543950336.0f;  // 2^96
 
-// ------------------------------------------------------ shared-memory reads
-// 16 bytes at a 2-byte-aligned shared address (five word loads, byte permute).
-__device__ __forceinline__ uint4 lds16_a2(const uint8_t* p) {
-    const uintptr_t a = reinterpret_cast<uintptr_t>(p);
-    const uint32_t* w = reinterpret_cast<const uint32_t*>(a & ~static_cast<uintptr_t>(3));
-    const uint32_t sel = (a & 2) ? 0x5432u : 0x3210u;
-    const uint32_t w0 = w[0], w1 = w[1], w2 = w[2], w3 = w[3], w4 = w[4];
-    return make_uint4(__byte_perm(w0, w1, sel), __byte_perm(w1, w2, sel), __byte_perm(w2, w3, sel),
-                      __byte_perm(w3, w4, sel));
-}
-__device__ __forceinline__ uint2 lds8_a2(const uint8_t* p) {
-    const uintptr_t a = reinterpret_cast<uintptr_t>(p);
-    const uint32_t* w = reinterpret_cast<const uint32_t*>(a & ~static_cast<uintptr_t>(3));
-    const uint32_t sel = (a & 2) ? 0x5432u : 0x3210u;
-    const uint32_t w0 = w[0], w1 = w[1], w2 = w[2];
-    return make_uint2(__byte_perm(w0, w1, sel), __byte_perm(w1, w2, sel));
-}
-
 // --------------------------------------------------- per-thread input slice
+// Arithmetic on register pairs.  Two consecutive 32-bit code words form one
+// 64-bit value; masking it with a 64-bit constant (the same mask in both
+// halves) yields two subnormal-float operands in one register pair, which
+// fma.rn.f32x2 consumes directly.  A 64-bit right shift moves the top of the
+// high word into the top of the low word; every mask applied after a shift
+// clears those bit positions, so the shift acts per half.
+typedef unsigned long long u64;
+
+__device__ __forceinline__ u64 f2_bits(float a, float b) {
+    return (static_cast<u64>(__float_as_uint(b)) << 32) | __float_as_uint(a);
+}
+__device__ __forceinline__ u64 fma2(u64 a, u64 b, u64 c) {
+    u64 d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ float lo_f(u64 v) { return __uint_as_float(static_cast<uint32_t>(v)); }
+__device__ __forceinline__ float hi_f(u64 v) { return __uint_as_float(static_cast<uint32_t>(v >> 32)); }
+
+constexpr u64 rep(uint32_t m) { return (static_cast<u64>(m) << 32) | m; }
+
 // Q4_K slice (b, c): weights 64c + l of super-block b, l = 0..63.  Code byte
 // 32c + 4t + j holds weight 64c + 4t + j (low nibble) and 64c + 32 + 4t + j
-// (high nibble).  Inside the 32-bit word t the nibbles are used at bit
-// positions lo: 0, 8, 16, 12 and hi: 4, 12, 8, 16 (bytes 0..3; the top three
-// nibbles after a 12-bit shift), so the slice stores x * 2^(53 - p).
+// (high nibble).  Words t = 2k, 2k+1 form pair k.  Nibble position i of a
+// word (0..7: bytes 0,0,1,1,2 low/high at bits 0,4,8,12,16; then bytes 2,3,3
+// after a 12-bit shift at bits 8,12,16) is used in place, so the slice holds
+// x * 2^(53 - p_i) for p = 0,4,8,12,16,8,12,16: a code masked at bit p is the
+// subnormal code * 2^(p-149) and the product is exactly code * x * 2^-96.
 struct SliceQ4 {
-    float xr[64];
+    u64 xp[4][8];      // [pair k][position i] = (x' of word 2k, x' of word 2k+1)
     float s_lo, s_hi;  // sums of x over sub-blocks 2c and 2c+1 (unscaled)
 };
 
 __device__ __forceinline__ void load_slice_q4(SliceQ4& s, const float* x, int b, int c) {
     const float* xb = x + b * kQK + 64 * c;
+    constexpr float sc[8] = {0x1p53f, 0x1p49f, 0x1p45f, 0x1p41f, 0x1p37f, 0x1p45f, 0x1p41f, 0x1p37f};
+    // weight offset of word t, position i (lo: 4t + byte; hi: 32 + 4t + byte)
     float slo = 0.0f, shi = 0.0f;
 #pragma unroll
-    for (int t = 0; t < 8; ++t) {
-        const float4 lo = __ldg(reinterpret_cast<const float4*>(xb + 4 * t));
-        const float4 hi = __ldg(reinterpret_cast<const float4*>(xb + 32 + 4 * t));
-        s.xr[8 * t + 0] = lo.x * 0x1p53f;
-        s.xr[8 * t + 1] = lo.y * 0x1p45f;
-        s.xr[8 * t + 2] = lo.z * 0x1p37f;
-        s.xr[8 * t + 3] = lo.w * 0x1p41f;
-        s.xr[8 * t + 4] = hi.x * 0x1p49f;
-        s.xr[8 * t + 5] = hi.y * 0x1p41f;
-        s.xr[8 * t + 6] = hi.z * 0x1p45f;
-        s.xr[8 * t + 7] = hi.w * 0x1p37f;
-        slo += (lo.x + lo.y) + (lo.z + lo.w);
-        shi += (hi.x + hi.y) + (hi.z + hi.w);
+    for (int k = 0; k < 4; ++k) {
+        // positions of word t: lo byte0, hi byte0, lo byte1, hi byte1, ... (lo at 4t + j, hi at 32 + 4t + j)
+        const float4 l0 = __ldg(reinterpret_cast<const float4*>(xb + 8 * k));
+        const float4 h0 = __ldg(reinterpret_cast<const float4*>(xb + 32 + 8 * k));
+        const float4 l1 = __ldg(reinterpret_cast<const float4*>(xb + 8 * k + 4));
+        const float4 h1 = __ldg(reinterpret_cast<const float4*>(xb + 32 + 8 * k + 4));
+        const float v0[8] = {l0.x, h0.x, l0.y, h0.y, l0.z, h0.z, l0.w, h0.w};
+        const float v1[8] = {l1.x, h1.x, l1.y, h1.y, l1.z, h1.z, l1.w, h1.w};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) s.xp[k][i] = f2_bits(v0[i] * sc[i], v1[i] * sc[i]);
+        slo += ((v0[0] + v0[2]) + (v0[4] + v0[6])) + ((v1[0] + v1[2]) + (v1[4] + v1[6]));
+        shi += ((v0[1] + v0[3]) + (v0[5] + v0[7])) + ((v1[1] + v1[3]) + (v1[5] + v1[7]));
     }
     s.s_lo = slo;
     s.s_hi = shi;
 }
 
 // Q6_K slice (b, c = 2h + j): weights 128h + 32g + 16j + l, g = 0..3,
-// l = 0..15 (sub-blocks 8h + 2g + j).  Six-bit codes are rebuilt four to a
-// word (bytes at bit 0, 8, 16 and, after a 16-bit shift, 8), so the slice
-// stores x * 2^(53 - p) with p = 0, 8, 16, 8.
+// l = 0..15 (sub-blocks 8h + 2g + j); word i of a code field covers
+// l = 4i..4i+3, words 2k, 2k+1 form pair k.  Six-bit codes are rebuilt four to
+// a word and used at bits 0, 8, 16 and (after a 16-bit shift) 8, so the slice
+// holds x * 2^(53 - p) with p = 0, 8, 16, 8.
 struct SliceQ6 {
-    float xr[64];      // [(i*4 + g)*4 + jj] for l = 4i + jj
+    u64 xp[2][4][4];   // [pair k][group g][byte jj]
     float s_neg32[4];  // -32 * sum of x over sub-block 8h + 2g + j
 };
 
-__device__ __forceinline__ void load_slice_q6(SliceQ6& s, const float* x, int b, int c) {
+// rot: the thread's blocks start 2 bytes past a word boundary.  Their code
+// fields are read as aligned words W0..W4 around the field; W1..W3 hold field
+// bytes 2..13 and one byte permute folds W4 (bytes 14, 15) and W0 (bytes 0, 1)
+// into the first word, so word i of the field holds bytes lmap[i][0..3].
+__device__ __forceinline__ int q6_lmap(bool rot, int i, int jj) {
+    if (!rot) return 4 * i + jj;
+    if (i == 0) return jj < 2 ? 14 + jj : jj - 2;
+    return 4 * i - 2 + jj;
+}
+
+__device__ __forceinline__ void load_slice_q6(SliceQ6& s, const float* x, int b, int c, bool rot) {
     const int h = c >> 1, j = c & 1;
+    constexpr float sc[4] = {0x1p53f, 0x1p45f, 0x1p37f, 0x1p45f};
 #pragma unroll
     for (int g = 0; g < 4; ++g) {
         const float* xg = x + b * kQK + 128 * h + 32 * g + 16 * j;
+        float v[16];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const float4 f = __ldg(reinterpret_cast<const float4*>(xg + 4 * q));
+            v[4 * q + 0] = f.x;
+            v[4 * q + 1] = f.y;
+            v[4 * q + 2] = f.z;
+            v[4 * q + 3] = f.w;
+        }
         float sum = 0.0f;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const float4 v = __ldg(reinterpret_cast<const float4*>(xg + 4 * i));
-            s.xr[(i * 4 + g) * 4 + 0] = v.x * 0x1p53f;
-            s.xr[(i * 4 + g) * 4 + 1] = v.y * 0x1p45f;
-            s.xr[(i * 4 + g) * 4 + 2] = v.z * 0x1p37f;
-            s.xr[(i * 4 + g) * 4 + 3] = v.w * 0x1p45f;
-            sum += (v.x + v.y) + (v.z + v.w);
-        }
+        for (int l = 0; l < 16; ++l) sum += v[l];
         s.s_neg32[g] = -32.0f * sum;
+#pragma unroll
+        for (int k = 0; k < 2; ++k)
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj)
+                s.xp[k][g][jj] = f2_bits(v[q6_lmap(rot, 2 * k, jj)] * sc[jj], v[q6_lmap(rot, 2 * k + 1, jj)] * sc[jj]);
     }
 }
 
-// ------------------------------------------------ one row x one slice (dot)
-// Q4_K: sum over the slice's 64 weights of w * x, with
+// ------------------------------------------------ rows x one slice (dot)
+// NR independent weight rows (two matrices, or two rows of one) against the
+// same input slice: the streams are interleaved so each warp has 2*NR
+// independent accumulator chains in flight.
+
+// Q4_K: out[r] = sum over the slice's 64 weights of w * x, with
 // w = d*sc_j*q - dmin*m_j (j = 2c, 2c+1).
-__device__ __forceinline__ float dot_q4(const SliceQ4& s, const uint8_t* blk, int c,
-                                        uint32_t sel_lo, uint32_t sel_hi) {
-    const uint4 hd = *reinterpret_cast<const uint4*>(blk);
-    const uint4 qa = *reinterpret_cast<const uint4*>(blk + 16 + 32 * c);
-    const uint4 qb = *reinterpret_cast<const uint4*>(blk + 32 + 32 * c);
-    const uint32_t words[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
-    float2 A = make_float2(0.0f, 0.0f), B = make_float2(0.0f, 0.0f);
+template <int NR>
+__device__ __forceinline__ void dot_q4(const SliceQ4& s, const uint8_t* const* blk, int c,
+                                       uint32_t sel_lo, uint32_t sel_hi, float* out) {
+    uint4 hd[NR];
+    u64 P4[NR][4];
 #pragma unroll
-    for (int t = 0; t < 8; ++t) {
-        const uint32_t w = words[t];
-        const uint32_t v = w >> 12;
-        A = __ffma2_rn(make_float2(bits_f(w & 0xFu), bits_f(w & 0xF00u)),
-                       make_float2(s.xr[8 * t + 0], s.xr[8 * t + 1]), A);
-        A = __ffma2_rn(make_float2(bits_f(w & 0xF0000u), bits_f(v & 0xF000u)),
-                       make_float2(s.xr[8 * t + 2], s.xr[8 * t + 3]), A);
-        B = __ffma2_rn(make_float2(bits_f(w & 0xF0u), bits_f(w & 0xF000u)),
-                       make_float2(s.xr[8 * t + 4], s.xr[8 * t + 5]), B);
-        B = __ffma2_rn(make_float2(bits_f(v & 0xF00u), bits_f(v & 0xF0000u)),
-                       make_float2(s.xr[8 * t + 6], s.xr[8 * t + 7]), B);
+    for (int r = 0; r < NR; ++r) {
+        hd[r] = *reinterpret_cast<const uint4*>(blk[r]);
+        const ulonglong2 qa = *reinterpret_cast<const ulonglong2*>(blk[r] + 16 + 32 * c);
+        const ulonglong2 qb = *reinterpret_cast<const ulonglong2*>(blk[r] + 32 + 32 * c);
+        P4[r][0] = qa.x;
+        P4[r][1] = qa.y;
+        P4[r][2] = qb.x;
+        P4[r][3] = qb.y;
     }
-    // six-bit scales/mins of sub-blocks 0..3 (low bits) and 4..7 (split)
-    const uint32_t scw = (c < 2) ? (hd.y & 0x3F3F3F3Fu)
-                                 : ((hd.w & 0x0F0F0F0Fu) | ((hd.y >> 2) & 0x30303030u));
-    const uint32_t mnw = (c < 2) ? (hd.z & 0x3F3F3F3Fu)
-                                 : (((hd.w >> 4) & 0x0F0F0F0Fu) | ((hd.z >> 2) & 0x30303030u));
-    const float2 scm_lo = make_float2(byte_to_f(scw, sel_lo), byte_to_f(mnw, sel_lo));
-    const float2 scm_hi = make_float2(byte_to_f(scw, sel_hi), byte_to_f(mnw, sel_hi));
-    const float d = h2f(hd.x), dmin = h2f(hd.x >> 16);
-    float2 T = __fmul2_rn(scm_lo, make_float2(A.x + A.y, s.s_lo));
-    T = __ffma2_rn(scm_hi, make_float2(B.x + B.y, s.s_hi), T);
-    return fmaf(d * kTwo96, T.x, -(dmin * T.y));
+    u64 A[NR], B[NR];  // pairs: sub-block 2c (low nibbles), 2c+1 (high nibbles)
+#pragma unroll
+    for (int r = 0; r < NR; ++r) A[r] = B[r] = 0;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+#pragma unroll
+        for (int r = 0; r < NR; ++r) {
+            const u64 P = P4[r][k];
+            const u64 V = P >> 12;
+            A[r] = fma2(P & rep(0xFu), s.xp[k][0], A[r]);
+            B[r] = fma2(P & rep(0xF0u), s.xp[k][1], B[r]);
+            A[r] = fma2(P & rep(0xF00u), s.xp[k][2], A[r]);
+            B[r] = fma2(P & rep(0xF000u), s.xp[k][3], B[r]);
+            A[r] = fma2(P & rep(0xF0000u), s.xp[k][4], A[r]);
+            B[r] = fma2(V & rep(0xF00u), s.xp[k][5], B[r]);
+            A[r] = fma2(V & rep(0xF000u), s.xp[k][6], A[r]);
+            B[r] = fma2(V & rep(0xF0000u), s.xp[k][7], B[r]);
+        }
+    }
+#pragma unroll
+    for (int r = 0; r < NR; ++r) {
+        // six-bit scales/mins of sub-blocks 0..3 (low bits) and 4..7 (split)
+        const uint32_t scw = (c < 2) ? (hd[r].y & 0x3F3F3F3Fu)
+                                     : ((hd[r].w & 0x0F0F0F0Fu) | ((hd[r].y >> 2) & 0x30303030u));
+        const uint32_t mnw = (c < 2) ? (hd[r].z & 0x3F3F3F3Fu)
+                                     : (((hd[r].w >> 4) & 0x0F0F0F0Fu) | ((hd[r].z >> 2) & 0x30303030u));
+        const float2 scm_lo = make_float2(byte_to_f(scw, sel_lo), byte_to_f(mnw, sel_lo));
+        const float2 scm_hi = make_float2(byte_to_f(scw, sel_hi), byte_to_f(mnw, sel_hi));
+        const float d = h2f(hd[r].x), dmin = h2f(hd[r].x >> 16);
+        float2 T = __fmul2_rn(scm_lo, make_float2(lo_f(A[r]) + hi_f(A[r]), s.s_lo));
+        T = __ffma2_rn(scm_hi, make_float2(lo_f(B[r]) + hi_f(B[r]), s.s_hi), T);
+        out[r] = fmaf(d * kTwo96, T.x, -(dmin * T.y));
+    }
 }
 
-// Q6_K: sum over the slice of d*sc_s*(q-32) * x.
-__device__ __forceinline__ float dot_q6(const SliceQ6& s, const uint8_t* blk, int c,
-                                        uint32_t sel_sc) {
+// Code-field loads.  kMode 0: the field is 4-byte aligned, words 2k, 2k+1
+// as one 64-bit pair.  kMode 1: the field sits 2 bytes past a word boundary
+// and the thread's input slice is rotated to match (see q6_lmap): pair 0 =
+// (bytes 14,15,0,1 ; W1), pair 1 = (W2 ; W3) of the aligned words W0..W4 from
+// p - 2.  kMode 2: 2 bytes past a boundary, words realigned by byte permutes
+// (rows whose alignment alternates).
+constexpr int kAlign = 0, kRotated = 1, kRealign = 2;
+
+template <int kMode>
+__device__ __forceinline__ u64 lds_pair(const uint8_t* p, int k) {
+    if constexpr (kMode == kAlign) {
+        const uint32_t* w = reinterpret_cast<const uint32_t*>(p) + 2 * k;
+        return (static_cast<u64>(w[1]) << 32) | w[0];
+    } else if constexpr (kMode == kRotated) {
+        const uint32_t* w = reinterpret_cast<const uint32_t*>(p - 2);
+        if (k == 0) {
+            const uint32_t c0 = __byte_perm(w[4], w[0], 0x7610u);
+            return (static_cast<u64>(w[1]) << 32) | c0;
+        }
+        return (static_cast<u64>(w[3]) << 32) | w[2];
+    } else {
+        const uint32_t* w = reinterpret_cast<const uint32_t*>(p - 2) + 2 * k;
+        const uint32_t w0 = w[0], w1 = w[1], w2 = w[2];
+        return (static_cast<u64>(__byte_perm(w1, w2, 0x5432u)) << 32) | __byte_perm(w0, w1, 0x5432u);
+    }
+}
+// 8 bytes (two words) at shared address p, aligned as above.
+template <bool kAligned>
+__device__ __forceinline__ uint2 lds_w2(const uint8_t* p) {
+    if constexpr (kAligned) {
+        const uint32_t* w = reinterpret_cast<const uint32_t*>(p);
+        return make_uint2(w[0], w[1]);
+    } else {
+        const uint32_t* w = reinterpret_cast<const uint32_t*>(p - 2);
+        const uint32_t w0 = w[0], w1 = w[1], w2 = w[2];
+        return make_uint2(__byte_perm(w0, w1, 0x5432u), __byte_perm(w1, w2, 0x5432u));
+    }
+}
+
+// Q6_K: out[r] = sum over the slice of d*sc_s*(q-32) * x.  With rows of a
+// multiple of 4 bytes, even blocks start 4-byte aligned in the stage and odd
+// ones 2 bytes past a boundary (210-byte blocks).
+template <int NR, int kMode>
+__device__ __forceinline__ void dot_q6(const SliceQ6& s, const uint8_t* const* blk, int c,
+                                       uint32_t sel_sc, float* out) {
     const int h = c >> 1, j = c & 1;
-    const uint4 ql0 = lds16_a2(blk + 64 * h + 16 * j);
-    const uint4 ql1 = lds16_a2(blk + 64 * h + 32 + 16 * j);
-    const uint4 qh = lds16_a2(blk + 128 + 32 * h + 16 * j);
-    const uint2 sc8 = lds8_a2(blk + 192 + 8 * h);
-    const uint32_t dbits = *reinterpret_cast<const uint16_t*>(blk + 208);
-    const uint32_t A4[4] = {ql0.x, ql0.y, ql0.z, ql0.w};
-    const uint32_t B4[4] = {ql1.x, ql1.y, ql1.z, ql1.w};
-    const uint32_t H4[4] = {qh.x, qh.y, qh.z, qh.w};
-    float2 acc[4];
+    u64 acc[NR][4];
 #pragma unroll
-    for (int g = 0; g < 4; ++g) acc[g] = make_float2(0.0f, 0.0f);
+    for (int r = 0; r < NR; ++r)
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const uint32_t A = A4[i], B = B4[i], H = H4[i];
-        uint32_t Q[4];
-        Q[0] = (A & 0x0F0F0F0Fu) | ((H & 0x03030303u) << 4);
-        Q[1] = (B & 0x0F0F0F0Fu) | ((H & 0x0C0C0C0Cu) << 2);
-        Q[2] = ((A >> 4) & 0x0F0F0F0Fu) | (H & 0x30303030u);
-        Q[3] = ((B >> 4) & 0x0F0F0F0Fu) | ((H >> 2) & 0x30303030u);
+        for (int g = 0; g < 4; ++g) acc[r][g] = 0;
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+#pragma unroll
+        for (int r = 0; r < NR; ++r) {
+            const u64 A = lds_pair<kMode>(blk[r] + 64 * h + 16 * j, k);
+            const u64 B = lds_pair<kMode>(blk[r] + 64 * h + 32 + 16 * j, k);
+            const u64 H = lds_pair<kMode>(blk[r] + 128 + 32 * h + 16 * j, k);
+            u64 Q[4];
+            Q[0] = (A & rep(0x0F0F0F0Fu)) | ((H & rep(0x03030303u)) << 4);
+            Q[1] = (B & rep(0x0F0F0F0Fu)) | ((H & rep(0x0C0C0C0Cu)) << 2);
+            Q[2] = ((A >> 4) & rep(0x0F0F0F0Fu)) | (H & rep(0x30303030u));
+            Q[3] = ((B >> 4) & rep(0x0F0F0F0Fu)) | ((H >> 2) & rep(0x30303030u));
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+                acc[r][g] = fma2(Q[g] & rep(0x3Fu), s.xp[k][g][0], acc[r][g]);
+                acc[r][g] = fma2(Q[g] & rep(0x3F00u), s.xp[k][g][1], acc[r][g]);
+                acc[r][g] = fma2(Q[g] & rep(0x3F0000u), s.xp[k][g][2], acc[r][g]);
+                acc[r][g] = fma2((Q[g] >> 16) & rep(0x3F00u), s.xp[k][g][3], acc[r][g]);
+            }
+        }
+    }
+#pragma unroll
+    for (int r = 0; r < NR; ++r) {
+        const uint2 sc8 = lds_w2<kMode == kAlign>(blk[r] + 192 + 8 * h);
+        const uint32_t dbits = *reinterpret_cast<const uint16_t*>(blk[r] + 208);
+        // int8 scales of sub-blocks 8h + 2g + j -> floats (offset-binary via 2^23 magic)
+        const uint32_t sc4 = __byte_perm(sc8.x, sc8.y, sel_sc) ^ 0x80808080u;
+        float sum = 0.0f;
 #pragma unroll
         for (int g = 0; g < 4; ++g) {
-            const float* xq = &s.xr[(i * 4 + g) * 4];
-            acc[g] = __ffma2_rn(make_float2(bits_f(Q[g] & 0x3Fu), bits_f(Q[g] & 0x3F00u)),
-                                make_float2(xq[0], xq[1]), acc[g]);
-            acc[g] = __ffma2_rn(make_float2(bits_f(Q[g] & 0x3F0000u), bits_f((Q[g] >> 16) & 0x3F00u)),
-                                make_float2(xq[2], xq[3]), acc[g]);
+            const float scg = byte_to_f(sc4, 0x7540u | g) - 128.0f;
+            const float tg = fmaf(lo_f(acc[r][g]) + hi_f(acc[r][g]), kTwo96, s.s_neg32[g]);
+            sum = fmaf(scg, tg, sum);
         }
+        out[r] = h2f(dbits) * sum;
     }
-    // int8 scales of sub-blocks 8h + 2g + j -> floats (offset-binary via 2^23 magic)
-    const uint32_t sc4 = __byte_perm(sc8.x, sc8.y, sel_sc) ^ 0x80808080u;
-    float sum = 0.0f;
-#pragma unroll
-    for (int g = 0; g < 4; ++g) {
-        const float scg = byte_to_f(sc4, 0x7540u | g) - 128.0f;
-        const float tg = fmaf(acc[g].x + acc[g].y, kTwo96, s.s_neg32[g]);
-        sum = fmaf(scg, tg, sum);
-    }
-    return h2f(dbits) * sum;
 }
 
 // -------------------------------------------------------------- the kernel
+// Warp roles: warps 0..nconsumer-1 compute (each thread one input slice and a
+// row group); the last warp produces (TMA issue, per-stage row reduction and
+// output).  Stage buffer s has a "full" mbarrier (producer arrival + TMA
+// transaction bytes) and an "empty" mbarrier (one arrival per consumer warp
+// once it has read the stage and stored its partials).  No block-wide barrier
+// runs per stage.
 template <int QT, int NMAT, int EPI>
 __global__ void __launch_bounds__(512, 1) mv1_kernel(const Mv1Args p) {
     extern __shared__ __align__(128) uint8_t smem[];
@@ -202,149 +299,292 @@ __global__ void __launch_bounds__(512, 1) mv1_kernel(const Mv1Args p) {
     const int nsb = p.nsb;
     const int nbc = nsb * 4;
     const int G = p.G, RS = p.RS, NS = p.ns;
-    const int64_t rowbytes = static_cast<int64_t>(nsb) * kBlk;
+    const int ncw = p.nconsumer_warps;
+    const uint32_t rowbytes = static_cast<uint32_t>(nsb) * kBlk;
     const int64_t r0 = p.rows * blockIdx.x / gridDim.x;
     const int64_t r1 = p.rows * (blockIdx.x + 1) / gridDim.x;
     const int nloc = static_cast<int>(r1 - r0);
     const int nstages = (nloc + RS - 1) / RS;
 
-    // shared layout: [bars NS x 8 B][red 64 floats][flag][partials 2*NMAT*RS*nbc][stages]
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
-    float* red = reinterpret_cast<float*>(smem + 8 * 16);
-    int* flag = reinterpret_cast<int*>(smem + 8 * 16 + 64 * 4);
+    // shared layout: barriers [full 8][empty 8][pfull 16][reduced 16] | red 64 | flag |
+    // partial slots (2*NS) | stage buffers (NS)
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem);
+    uint64_t* empty = full + 8;
+    uint64_t* pfull = full + 16;
+    uint64_t* reduced = full + 32;
+    uint64_t* xready = full + 48;
+    float* red = reinterpret_cast<float*>(smem + 512);
+    int* flag = reinterpret_cast<int*>(smem + 512 + 64 * 4);
     float* part = reinterpret_cast<float*>(smem + p.part_off);
     uint8_t* stage_base = smem + p.stage_off;
     const uint32_t stage_bytes = p.stage_bytes;  // per matrix
+    const int part_stride = NMAT * RS * nbc;
+    int L = 32;
+    while (L > 1 && L * RS * NMAT > 32) L >>= 1;
 
     const int tid = threadIdx.x;
     const int lane = tid & 31, warp = tid >> 5;
-    const int nwarps = blockDim.x >> 5;
-    const int g = tid / nbc;
-    const int bc = tid - g * nbc;
-    const int b = bc >> 2, c = bc & 3;
-    const bool active = g < G;
-
-    // Issue the bulk copies of stage k (all matrices) into buffer k % NS.
-    auto issue = [&](int k) {
-        const int buf = k % NS;
-        const int64_t lr0 = static_cast<int64_t>(k) * RS;
-        const int64_t lr1 = min(static_cast<int64_t>(nloc), lr0 + RS);
-        uint32_t total = 0;
-        uint32_t sizes[NMAT];
-        const uint8_t* srcs[NMAT];
-        for (int m = 0; m < NMAT; ++m) {
-            const uint8_t* start = p.W[m] + (r0 + lr0) * rowbytes;
-            const uint8_t* end = p.W[m] + (r0 + lr1) * rowbytes;
-            const uint8_t* matend = p.W[m] + p.rows * rowbytes;
-            const uint8_t* s16 = reinterpret_cast<const uint8_t*>(
-                reinterpret_cast<uintptr_t>(start) & ~static_cast<uintptr_t>(15));
-            uintptr_t e16 = (reinterpret_cast<uintptr_t>(end) + 15) & ~static_cast<uintptr_t>(15);
-            const uintptr_t mend16 = reinterpret_cast<uintptr_t>(matend) & ~static_cast<uintptr_t>(15);
-            if (e16 > mend16) e16 = mend16;  // never read past the matrix
-            uint8_t* dst = stage_base + (static_cast<size_t>(buf) * NMAT + m) * stage_bytes;
-            // bytes in [e16, end) (only at the matrix end) are copied by hand
-            for (const uint8_t* q = reinterpret_cast<const uint8_t*>(e16); q < end; ++q)
-                dst[q - s16] = static_cast<uint8_t>(ldg_u8(q));
-            sizes[m] = static_cast<uint32_t>(e16 - reinterpret_cast<uintptr_t>(s16));
-            srcs[m] = s16;
-            total += sizes[m];
-        }
-        mbar_arrive_expect_tx(&bars[buf], total);
-        for (int m = 0; m < NMAT; ++m) {
-            if (sizes[m] == 0) continue;
-            uint8_t* dst = stage_base + (static_cast<size_t>(buf) * NMAT + m) * stage_bytes;
-            tma_load_1d(dst, srcs[m], sizes[m], &bars[buf]);
-        }
-    };
+    const int NP = 2 * NS;  // partial slots
 
     if (tid == 0) {
-        for (int i = 0; i < NS; ++i) mbar_init(&bars[i], 1);
+        for (int i = 0; i < NS; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], static_cast<uint32_t>(ncw));
+        }
+        for (int i = 0; i < NP; ++i) {
+            mbar_init(&pfull[i], static_cast<uint32_t>(ncw));
+            mbar_init(&reduced[i], 1);
+        }
+        mbar_init(xready, static_cast<uint32_t>(ncw));
         fence_mbar_init();
     }
     __syncthreads();
-    if (tid == 0) {
-        for (int k = 0; k < min(NS, nstages); ++k) issue(k);
-    }
-
-    // This thread's input slice, in registers for the whole kernel.
-    using Slice = typename std::conditional<QT == MUSER_Q4_K, SliceQ4, SliceQ6>::type;
-    Slice sl;
-    if (active) {
-        if constexpr (QT == MUSER_Q4_K) load_slice_q4(sl, p.x, b, c);
-        else load_slice_q6(sl, p.x, b, c);
-    }
-    const uint32_t sel_lo = 0x7540u | static_cast<uint32_t>(2 * (c & 1));
-    const uint32_t sel_hi = 0x7540u | static_cast<uint32_t>(2 * (c & 1) + 1);
-    const uint32_t jq = static_cast<uint32_t>(c & 1);
-    const uint32_t sel_sc = jq | ((jq + 2) << 4) | ((jq + 4) << 8) | ((jq + 6) << 12);
-    __syncthreads();  // hand-copied stage tails (matrix end) are visible
 
     bool ok = true;
-    const int part_stride = NMAT * RS * nbc;
-    for (int k = 0; k < nstages; ++k) {
-        const int buf = k % NS;
-        const int64_t lr0 = static_cast<int64_t>(k) * RS;
-        const int rows_here = static_cast<int>(min(static_cast<int64_t>(RS), nloc - lr0));
-        if (ok) ok = mbar_wait_bounded(&bars[buf], static_cast<uint32_t>((k / NS) & 1),
-                                       &g_device_status, kDevStatusWaitTimeout);
-        float* pk = part + (k & 1) * part_stride;
-        if (active && ok) {
+    if (warp == ncw) {
+        // ---------------------------------------------------------- TMA warp
+        // Bulk copies of stage k (all matrices) into buffer k % NS.
+        auto issue = [&](int k) {
+            const int buf = k % NS;
+            const int64_t lr0 = static_cast<int64_t>(k) * RS;
+            const int64_t lr1 = min(static_cast<int64_t>(nloc), lr0 + RS);
+            uint32_t total = 0;
+            uint32_t sizes[NMAT];
+            const uint8_t* srcs[NMAT];
 #pragma unroll
             for (int m = 0; m < NMAT; ++m) {
-                const uint8_t* sbuf = stage_base + (static_cast<size_t>(buf) * NMAT + m) * stage_bytes;
                 const uint8_t* start = p.W[m] + (r0 + lr0) * rowbytes;
-                const int delta = static_cast<int>(reinterpret_cast<uintptr_t>(start) & 15);
-                for (int rs = g; rs < rows_here; rs += G) {
-                    const uint8_t* blk = sbuf + delta + rs * rowbytes + static_cast<int64_t>(b) * kBlk;
-                    float v;
-                    if constexpr (QT == MUSER_Q4_K) v = dot_q4(sl, blk, c, sel_lo, sel_hi);
-                    else v = dot_q6(sl, blk, c, sel_sc);
-                    pk[(m * RS + rs) * nbc + bc] = v;
-                }
+                const uint8_t* end = p.W[m] + (r0 + lr1) * rowbytes;
+                const uint8_t* matend = p.W[m] + p.rows * rowbytes;
+                const uint8_t* s16 = reinterpret_cast<const uint8_t*>(
+                    reinterpret_cast<uintptr_t>(start) & ~static_cast<uintptr_t>(15));
+                uintptr_t e16 = (reinterpret_cast<uintptr_t>(end) + 15) & ~static_cast<uintptr_t>(15);
+                const uintptr_t mend16 = reinterpret_cast<uintptr_t>(matend) & ~static_cast<uintptr_t>(15);
+                if (e16 > mend16) e16 = mend16;  // never read past the matrix
+                uint8_t* dst = stage_base + (static_cast<size_t>(buf) * NMAT + m) * stage_bytes;
+                // bytes in [e16, end) (only at the matrix end) are copied by hand
+                for (const uint8_t* q = reinterpret_cast<const uint8_t*>(e16); q < end; ++q)
+                    dst[q - s16] = static_cast<uint8_t>(ldg_u8(q));
+                sizes[m] = static_cast<uint32_t>(e16 - reinterpret_cast<uintptr_t>(s16));
+                srcs[m] = s16;
+                total += sizes[m];
             }
-        }
-        ok = __syncthreads_and(ok);  // stage k consumed; partials of stage k complete
-        if (tid == 0 && ok && k + NS < nstages) {
-            fence_proxy_async_smem();
-            issue(k + NS);
-        }
-        // One warp per row adds the slice partials in a fixed order.
-        for (int rs = warp; rs < rows_here; rs += nwarps) {
-            float v[NMAT];
+            mbar_arrive_expect_tx(&full[buf], total);
 #pragma unroll
             for (int m = 0; m < NMAT; ++m) {
-                const float* pr = pk + (m * RS + rs) * nbc;
-                float s = 0.0f;
-                for (int i = lane; i < nbc; i += 32) s += pr[i];
-                v[m] = warp_sum(s);
+                if (sizes[m] == 0) continue;
+                uint8_t* dst = stage_base + (static_cast<size_t>(buf) * NMAT + m) * stage_bytes;
+                tma_load_1d(dst, srcs[m], sizes[m], &full[buf]);
             }
-            if (lane == 0) {
-                const int64_t row = r0 + lr0 + rs;
-                if constexpr (EPI == kEpiSiluMul) {
-                    p.y0[row] = silu_mul_f(v[0], v[NMAT - 1]);
-                } else {
-                    p.y0[row] = v[0];
-                    if constexpr (NMAT == 2) p.y1[row] = v[NMAT - 1];
+        };
+        // The weight copies start only once every consumer warp holds its
+        // input slice: x must not queue behind a burst of weight traffic.
+        pdl_launch_dependents();
+        pdl_wait();
+        ok = mbar_wait_bounded(xready, 0, &g_device_status, kDevStatusWaitTimeout);
+        if (ok && lane == 0)
+            for (int k = 0; k < min(NS, nstages); ++k) issue(k);
+        __syncwarp();
+        for (int k = 0; k + NS < nstages && ok; ++k) {
+            // buffer k % NS is free once every consumer warp has read stage k;
+            // the partial slot of stage k + NS once stage k - NS is reduced
+            ok = mbar_wait_bounded(&empty[k % NS], static_cast<uint32_t>((k / NS) & 1),
+                                   &g_device_status, kDevStatusWaitTimeout);
+            const int kp = k + NS;
+            if (ok && kp >= NP)
+                ok = mbar_wait_bounded(&reduced[kp % NP], static_cast<uint32_t>(((kp - NP) / NP) & 1),
+                                       &g_device_status, kDevStatusWaitTimeout);
+            if (ok && lane == 0) issue(kp);
+            __syncwarp();
+        }
+    } else if (warp == ncw + 1) {
+        // ------------------------------------------------------ reducer warp
+        pdl_launch_dependents();
+        pdl_wait();  // outputs of the previous kernel are complete before ours are written
+        const int n4 = nbc / 4;
+        for (int k = 0; k < nstages; ++k) {
+            const int slot = k % NP;
+            if (ok) ok = mbar_wait_bounded(&pfull[slot], static_cast<uint32_t>((k / NP) & 1),
+                                           &g_device_status, kDevStatusWaitTimeout);
+            if (!ok) break;
+            const int64_t lr0 = static_cast<int64_t>(k) * RS;
+            const int rows_here = static_cast<int>(min(static_cast<int64_t>(RS), nloc - lr0));
+            const float* pk = part + slot * part_stride;
+            // Output o = rs*NMAT + m owns lanes [o*L, o*L + L); each lane adds
+            // a fixed strided set of float4 partials (loads issued first), then
+            // a shuffle tree inside the lane group finishes the sum.
+            for (int o0 = 0; o0 < rows_here * NMAT; o0 += 32 / L) {
+                const int o = o0 + lane / L;
+                const int sub = lane % L;
+                const int rs = o / NMAT, m = o % NMAT;
+                float acc = 0.0f;
+                if (rs < rows_here) {
+                    const float4* pr = reinterpret_cast<const float4*>(pk + (m * RS + rs) * nbc);
+                    for (int j0 = sub; j0 < n4; j0 += 8 * L) {
+                        float4 q[8];
+#pragma unroll
+                        for (int u = 0; u < 8; ++u) {
+                            const int j = j0 + u * L;
+                            q[u] = j < n4 ? pr[j] : make_float4(0.f, 0.f, 0.f, 0.f);
+                        }
+#pragma unroll
+                        for (int u = 0; u < 8; ++u) acc += (q[u].x + q[u].y) + (q[u].z + q[u].w);
+                    }
                 }
-                if constexpr (EPI == kEpiTail) __threadfence();
+                for (int off = L / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+                float other = 0.0f;
+                if constexpr (NMAT == 2) other = __shfl_down_sync(0xffffffffu, acc, L);
+                if (sub == 0 && rs < rows_here && m == 0) {
+                    const int64_t row = r0 + lr0 + rs;
+                    if constexpr (EPI == kEpiSiluMul) {
+                        p.y0[row] = silu_mul_f(acc, other);
+                    } else {
+                        p.y0[row] = acc;
+                        if constexpr (NMAT == 2) p.y1[row] = other;
+                    }
+                    if constexpr (EPI == kEpiTail) __threadfence();
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&reduced[slot]);
+        }
+    } else {
+        // Thread -> (row group g, slice (b, c)).  Q6_K with an even number of
+        // super-blocks per row: the first half of a row group's slices take the
+        // even super-blocks, the second half the odd ones, so whole warps share
+        // one block alignment (even blocks start 4-byte aligned in the stage,
+        // odd ones 2 bytes past a boundary).
+        // A row group spans p.TG threads; with the split, the odd half starts
+        // at thread p.HP of the group (a warp boundary when it fits), and
+        // threads in the padding between the halves idle.
+        const int g = tid / p.TG;
+        const int idx = tid - g * p.TG;
+        int b, c;
+        bool active = g < G;
+        const bool parity_split = (QT == MUSER_Q6_K) && (nsb % 2 == 0);
+        if (parity_split) {
+            const int half = nbc / 2;
+            const bool odd = idx >= p.HP;
+            const int i2 = odd ? idx - p.HP : idx;
+            if (i2 >= half) active = false;
+            b = 2 * (i2 >> 2) + (odd ? 1 : 0);
+            c = i2 & 3;
+            if (!active) b = c = 0;
+        } else {
+            b = idx >> 2;
+            c = idx & 3;
+        }
+        const int bc = b * 4 + c;  // partial slot of this slice
+        pdl_launch_dependents();
+        pdl_wait();  // x is the previous kernel's output
+        using Slice = typename std::conditional<QT == MUSER_Q4_K, SliceQ4, SliceQ6>::type;
+        Slice sl;
+        if (active) {
+            if constexpr (QT == MUSER_Q4_K) load_slice_q4(sl, p.x, b, c);
+            else load_slice_q6(sl, p.x, b, c, parity_split && (b & 1));
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(xready);
+        const uint32_t sel_lo = 0x7540u | static_cast<uint32_t>(2 * (c & 1));
+        const uint32_t sel_hi = 0x7540u | static_cast<uint32_t>(2 * (c & 1) + 1);
+        const uint32_t jq = static_cast<uint32_t>(c & 1);
+        const uint32_t sel_sc = jq | ((jq + 2) << 4) | ((jq + 4) << 8) | ((jq + 6) << 12);
+        const uint32_t slice_off = static_cast<uint32_t>(b) * kBlk;
+
+        // One stage's rows for this thread; kAl selects the Q6_K load path.
+        auto stage = [&](auto al_tag, const uint8_t* const* sb, int rows_here, float* pk) {
+            constexpr bool kAl = decltype(al_tag)::value;
+            auto dots = [&](auto nr_tag, const uint8_t* const* blk, float* out) {
+                constexpr int NR = decltype(nr_tag)::value;
+                if constexpr (QT == MUSER_Q4_K) dot_q4<NR>(sl, blk, c, sel_lo, sel_hi, out);
+                else dot_q6<NR, kAl ? kAlign : kRotated>(sl, blk, c, sel_sc, out);
+            };
+            using One = std::integral_constant<int, 1>;
+            using Two = std::integral_constant<int, 2>;
+            if constexpr (NMAT == 2) {
+                // the gate and up rows of row rs, interleaved
+                for (int rs = g; rs < rows_here; rs += G) {
+                    const uint8_t* blk[2] = {sb[0] + rs * rowbytes, sb[1] + rs * rowbytes};
+                    float v[2];
+                    dots(Two{}, blk, v);
+                    pk[rs * nbc + bc] = v[0];
+                    pk[(RS + rs) * nbc + bc] = v[1];
+                }
+            } else {
+                // rows rs and rs + G, interleaved
+                for (int rs = g; rs < rows_here; rs += 2 * G) {
+                    const uint8_t* blk[2] = {sb[0] + rs * rowbytes, sb[0] + (rs + G) * rowbytes};
+                    float v[2];
+                    if (rs + G < rows_here) {
+                        dots(Two{}, blk, v);
+                        pk[rs * nbc + bc] = v[0];
+                        pk[(rs + G) * nbc + bc] = v[1];
+                    } else {
+                        dots(One{}, blk, v);
+                        pk[rs * nbc + bc] = v[0];
+                    }
+                }
+            }
+        };
+        // Q6_K rows whose byte length is not a multiple of 4: alignment
+        // alternates by row, so each row picks its path (one row at a time).
+        auto stage_any = [&](const uint8_t* const* sb, int rows_here, float* pk) {
+            for (int m = 0; m < NMAT; ++m)
+                for (int rs = g; rs < rows_here; rs += G) {
+                    const uint8_t* blk[1] = {sb[m] + rs * rowbytes};
+                    float v[1];
+                    if constexpr (QT == MUSER_Q4_K) {
+                        dot_q4<1>(sl, blk, c, sel_lo, sel_hi, v);
+                    } else {
+                        if ((reinterpret_cast<uintptr_t>(blk[0]) & 2) == 0) dot_q6<1, kAlign>(sl, blk, c, sel_sc, v);
+                        else dot_q6<1, kRealign>(sl, blk, c, sel_sc, v);
+                    }
+                    pk[(m * RS + rs) * nbc + bc] = v[0];
+                }
+        };
+        const bool rows4 = (rowbytes & 3u) == 0;
+        const bool aligned = (b % 2 == 0);
+        for (int k = 0; k < nstages; ++k) {
+            const int buf = k % NS;
+            const int64_t lr0 = static_cast<int64_t>(k) * RS;
+            const int rows_here = static_cast<int>(min(static_cast<int64_t>(RS), nloc - lr0));
+            if (ok) ok = mbar_wait_bounded(&full[buf], static_cast<uint32_t>((k / NS) & 1),
+                                           &g_device_status, kDevStatusWaitTimeout);
+            float* pk = part + (k % NP) * part_stride;
+            if (active && ok) {
+                const uint8_t* sb[NMAT];
+#pragma unroll
+                for (int m = 0; m < NMAT; ++m) {
+                    const uint8_t* start = p.W[m] + (r0 + lr0) * static_cast<int64_t>(rowbytes);
+                    const uint32_t delta = static_cast<uint32_t>(reinterpret_cast<uintptr_t>(start) & 15);
+                    sb[m] = stage_base + (static_cast<uint32_t>(buf) * NMAT + m) * stage_bytes + delta + slice_off;
+                }
+                if (QT == MUSER_Q6_K && !rows4) stage_any(sb, rows_here, pk);
+                else if (QT == MUSER_Q4_K || aligned) stage(std::true_type{}, sb, rows_here, pk);
+                else stage(std::false_type{}, sb, rows_here, pk);
+            }
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&empty[buf]);
+                mbar_arrive(&pfull[k % NP]);
             }
         }
     }
+    ok = __syncthreads_and(ok);
     if (!ok) {
         // A bounded wait gave up (status word set).  Give the copies still in
         // flight a bounded chance to land before the block's shared memory is
         // released, then leave without writing the tail.
         if (tid == 0) {
             for (int k = max(0, nstages - NS); k < nstages; ++k)
-                (void)mbar_wait_bounded(&bars[k % NS], static_cast<uint32_t>((k / NS) & 1),
-                                        &g_device_status, kDevStatusTxTimeout, 1u << 20);
+                (void)mbar_wait_bounded(&full[k % NS], static_cast<uint32_t>((k / NS) & 1),
+                                        &g_device_status, kDevStatusTxTimeout, 20);
         }
         return;
     }
 
     if constexpr (EPI == kEpiTail) {
         // Last CTA to finish runs the dual-eps tail over the whole row.
-        __syncthreads();
         if (tid == 0) {
             __threadfence();
             const unsigned t = atomicAdd(p.ticket, 1u);
@@ -374,10 +614,12 @@ unsigned read_device_status(bool reset) {
 }
 
 // ------------------------------------------------------------------ launch
+constexpr int kMaxConsumerThreads = 448;  // + the TMA and reducer warps = 512 threads
+
 bool mv1_supported(int qtype, int64_t cols) {
     (void)qtype;
     const int64_t nbc = (cols / kQK) * 4;
-    return cols % kQK == 0 && nbc >= 1 && nbc <= 512;
+    return cols % kQK == 0 && nbc >= 1 && nbc <= kMaxConsumerThreads;
 }
 
 template <int QT, int NMAT, int EPI>
@@ -386,32 +628,59 @@ static int launch_mv1_t(Mv1Args a, cudaStream_t stream) {
     const int nbc = a.nsb * 4;
     const int64_t rowbytes = static_cast<int64_t>(a.nsb) * kBlk;
     const int sms = sm_count();
-    int grid = static_cast<int>(std::min<int64_t>(sms, a.rows));
-    a.G = std::max(1, 512 / nbc);
-    const int threads = ((nbc * a.G + 31) / 32) * 32;
+    if (sms <= 0) return set_error(MUSER_ERR_CUDA, "mv1: cannot query the SM count");
+    const int grid = static_cast<int>(std::min<int64_t>(sms, a.rows));
+    // Q6_K rows of an even number of super-blocks split their slices by block
+    // parity; each half is padded to whole warps when that still fits.
+    a.TG = nbc;
+    a.HP = nbc / 2;
+    if (QT == MUSER_Q6_K && a.nsb % 2 == 0) {
+        const int hp = (nbc / 2 + 31) / 32 * 32;
+        if (2 * hp <= kMaxConsumerThreads) {
+            a.HP = hp;
+            a.TG = 2 * hp;
+        }
+    }
+    a.G = std::max(1, kMaxConsumerThreads / a.TG);
+    a.nconsumer_warps = (a.TG * a.G + 31) / 32;
+    const int threads = (a.nconsumer_warps + 2) * 32;
     // rows per stage: a multiple of G, stage near 32 KB over all matrices
     const int64_t per_row = rowbytes * NMAT;
-    int64_t rs = std::max<int64_t>(1, (32 * 1024) / (per_row * a.G)) * a.G;
+    const int64_t unit = static_cast<int64_t>(a.G) * (NMAT == 1 ? 2 : 1);  // one matrix: rows go in pairs
+    int64_t rs = std::max<int64_t>(1, (32 * 1024) / (per_row * unit)) * unit;
     const int64_t rows_per_cta = (a.rows + grid - 1) / grid;
-    rs = std::min<int64_t>(rs, ((rows_per_cta + a.G - 1) / a.G) * a.G);
+    rs = std::min<int64_t>(rs, ((rows_per_cta + unit - 1) / unit) * unit);
     a.RS = static_cast<int>(rs);
     a.stage_bytes = static_cast<uint32_t>(((rs * rowbytes + 32) + 127) / 128 * 128);
-    const int head = 8 * 16 + 64 * 4 + 64;  // bars, red, flag
+    const int head = 512 + 64 * 4 + 64;  // barriers, red, flag
     a.part_off = (head + 127) / 128 * 128;
-    const int64_t part_bytes = static_cast<int64_t>(2) * NMAT * a.RS * nbc * 4;
-    a.stage_off = static_cast<int>((a.part_off + part_bytes + 127) / 128 * 128);
     const int64_t budget = max_smem_optin();
     const int64_t per_stage = static_cast<int64_t>(a.stage_bytes) * NMAT;
-    int ns = static_cast<int>((budget - a.stage_off) / per_stage);
+    const int64_t part_per_stage = static_cast<int64_t>(NMAT) * a.RS * nbc * 4;
+    int ns = static_cast<int>((budget - a.part_off - 256) / (per_stage + 2 * part_per_stage));
     ns = std::min(ns, 8);
-    if (ns < 2) return set_error(MUSER_ERR_UNSUPPORTED, "mv1: shape needs %lld B of shared memory per stage", (long long)per_stage);
+    if (ns < 2)
+        return set_error(MUSER_ERR_UNSUPPORTED, "mv1: shape needs %lld B of shared memory per stage",
+                         (long long)per_stage);
     a.ns = ns;
+    a.stage_off = static_cast<int>((a.part_off + 2 * ns * part_per_stage + 127) / 128 * 128);
     const size_t smem = static_cast<size_t>(a.stage_off + ns * per_stage);
     auto kern = mv1_kernel<QT, NMAT, EPI>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return cuda_fail(e, "mv1: cudaFuncSetAttribute");
-    kern<<<grid, threads, smem, stream>>>(a);
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(threads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kern, a);
+    if (e != cudaSuccess) return cuda_fail(e, "mv1: cudaLaunchKernelEx");
     return check_launch("mv1_kernel");
 }
 

@@ -2,8 +2,9 @@
 
 0: Q4_K 512x2048 matvec; 1/2: Q4_K / Q6_K W_down 6656x19968 + dual-eps tail;
 3: one decode-FFN block (M = 1, gate/up Q4_K, down Q6_K); 4: 52 layers at
-M = 16 (the oracle follows two of the sixteen independent rows through every
-layer; a 3-layer slice is checked on all sixteen rows)."""
+M = 16 (and M = 1, the benchmark's stack): every layer teacher-forced on the
+oracle's own layer input, plus the end-to-end stack (a 3-layer slice end to
+end at the per-layer bound)."""
 import numpy as np
 import pytest
 
@@ -129,9 +130,79 @@ def test_workload4_stack_slice_all_rows():
     assert_close(go, orf, "3-layer stack output (16 rows)")
 
 
-def test_workload4_full_52_layers_sampled_rows():
-    rows = np.array([0, 13])
-    gr, go, rr, orf = _stack(synth.N_LAYERS, 16, rows)
-    assert_close(gr, rr, "52-layer residual (rows 0, 13)")
-    assert_close(go, orf, "52-layer output (rows 0, 13)")
+# The 52-layer stack amplifies rounding chaotically on some rows: one-ulp
+# binary32 nudges on the input of the fp64 oracle itself move its layer-51
+# residual by up to ~6e-3 of the row's RMS (rows whose gates sit deep in
+# SiLU's exponential tail), while other rows do not amplify at all (~5e-7).
+# So (1) every layer is held to the path's bound teacher-forced -- the GPU
+# layer runs on the oracle's own input of that layer -- at M = 16 and M = 1;
+# (2) a second oracle trajectory from nudged inputs classifies each row from
+# the oracle alone; stable rows are held to the path's bound end to end,
+# chaotic rows to finiteness and their RMS (error reported).
+STABLE = 1e-5        # oracle self-sensitivity (max |dr| / rms) below which a row is stable
+CHAOTIC_RMS = 0.05   # chaotic rows: |rms(gpu) - rms(oracle)| / rms(oracle)
+
+
+def _nudge(r):
+    r2 = r.copy()
+    r2.view(np.int32)[:, ::7] += 1
+    return r2
+
+
+def test_workload4_52_layers_teacher_forced_and_end_to_end():
+    """M = 16 (workload 4) and M = 1 (the benchmark's stack) through 52 layers."""
+    wl, M = 4, 16
+    w_in0 = synth.input_norm_weight(0, H, seed=0, workload=wl)
+    r0 = synth.residual_rows(M, H, seed=0, workload=wl)
+    rr = np.concatenate([r0, _nudge(r0)])           # oracle: true and nudged trajectories
+    xx = oracle.rms_norm(rr, w_in0, 1e-5)
+    keep, structs = [], []
+    mid16, proj16, out16 = nan_like((16, F)), nan_like((16, H)), nan_like((16, H))
+    mid1, proj1, out1 = nan_like((1, F)), nan_like((1, H)), nan_like((1, H))
+    scratch = torch.zeros(64, dtype=torch.float32, device="cuda")
+    for l in range(synth.N_LAYERS):
+        L = synth.ffn_layer(l, H, F, seed=0, workload=wl)
+        w_next = synth.input_norm_weight(l + 1, H, seed=0, workload=wl)
+        d = _layer_dev(L, w_next)
+        keep.append(d)
+        structs.append(_ffn_layer_struct(d))
+        r_next, x_next, mid_o, p_o = oracle.ffn_layer(xx, rr, L, w_next, H, F)
+        # teacher-forced GPU layer at M = 16 and M = 1 on the oracle's input
+        for Mt, mid, proj, out in ((16, mid16, proj16, out16), (1, mid1, proj1, out1)):
+            xg, rg = dev(xx[:Mt]), dev(rr[:Mt])
+            mu.muser_ffn_gate_up_silu("q4_k", d["Wg"], d["Wu"], F, H, xg, Mt, mid)
+            assert_close(host(mid).reshape(-1, F)[:Mt], mid_o[:Mt], f"layer {l} mid M={Mt}", scaled=True)
+            mu.muser_qmatvec_residual_dual_rmsnorm("q6_k", d["Wd"], H, F, mid, Mt, proj, rg, out,
+                                                   d["w1"], d["w_next"], 1e-8, 1e-5, scratch, 256)
+            assert_close(host(proj).reshape(-1, H)[:Mt], p_o[:Mt], f"layer {l} projected M={Mt}", scaled=True)
+            assert_close(host(rg), r_next[:Mt], f"layer {l} residual M={Mt}")
+            assert_close(host(out).reshape(-1, H)[:Mt], x_next[:Mt], f"layer {l} output M={Mt}")
+        rr, xx = r_next, x_next
+        del L
+    assert not host(scratch).any()
+    r_ref, x_ref = rr[:M], xx[:M]
+    rms = np.sqrt(np.mean(r_ref.astype(np.float64) ** 2, axis=1))
+    sens = np.abs(rr[M:].astype(np.float64) - r_ref).max(axis=1) / rms
+    stable = sens < STABLE
+    assert stable.sum() >= 4 and (~stable).sum() >= 1
+    ws_bytes = mu.muser_ffn_workspace_bytes(H, F, M)
+    ws = torch.zeros(ws_bytes // 4, dtype=torch.float32, device="cuda")
+    for Mt, rows in ((16, np.arange(16)), (1, np.array([int(np.argmax(stable))])),
+                     (1, np.array([int(np.argmin(stable))]))):
+        resid, out = dev(r0[rows]), nan_like((Mt, H))
+        ws.zero_()
+        mu.muser_ffn_stack(structs, dev(w_in0), H, F, Mt, resid, out, 1e-5, 1e-8, ws, ws_bytes)
+        gr, go = host(resid), host(out).reshape(Mt, H)
+        assert np.isfinite(gr).all() and np.isfinite(go).all()
+        for i, row in enumerate(rows):
+            err = np.abs(gr[i].astype(np.float64) - r_ref[row]).max() / rms[row]
+            print(f"52-layer M={Mt} row {row}: oracle self-sensitivity {sens[row]:.1e}, "
+                  f"gpu max |err|/rms {err:.1e} ({'stable' if stable[row] else 'chaotic'})")
+            if stable[row]:
+                assert_close(gr[i:i + 1], r_ref[row:row + 1], f"52-layer residual row {row} M={Mt}")
+                assert_close(go[i:i + 1], x_ref[row:row + 1], f"52-layer output row {row} M={Mt}")
+            else:
+                g_rms = np.sqrt(np.mean(gr[i].astype(np.float64) ** 2))
+                assert abs(g_rms - rms[row]) / rms[row] < CHAOTIC_RMS
+    del keep
     torch.cuda.empty_cache()
