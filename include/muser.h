@@ -158,6 +158,48 @@ int muser_qmatvec_residual_dual_rmsnorm(int qtype, const void* Wdown, int64_t hi
                                         const float* w2, float eps1, float eps2, void* scratch,
                                         size_t scratch_bytes, void* stream);
 
+/* Size of the library's own scratch array (1 MiB), see the call below. */
+#define MUSER_STATIC_SCRATCH_BYTES (1u << 20)
+
+/*
+ * muser_qmatvec_residual_dual_rmsnorm_static -- the same down projection and
+ *   dual-eps tail as muser_qmatvec_residual_dual_rmsnorm, for callers that
+ *   cannot hand the library any device memory of their own.  The Muser book
+ *   has no counterpart to this call; it is a convenience of this library.
+ *
+ *   Who needs it: a host that embeds the library but owns no allocator (its
+ *   device memory was carved up front into weights, KV cache and activations
+ *   by someone else, and nothing is left to lend), and a token loop that must
+ *   not call cudaMalloc or cudaFree between tokens, because those calls can
+ *   wait for the whole device and so stall the stream it is feeding.
+ *
+ *   Instead of `projected` and `scratch`, the call uses an array that is
+ *   compiled into the library: MUSER_STATIC_SCRATCH_BYTES bytes of device
+ *   memory on every GPU that loads the library, held until the process
+ *   exits.  Its first 256 bytes hold the tail's completion counter and the
+ *   rest holds the projected rows, so M * hidden * 4 + 256 must not exceed
+ *   MUSER_STATIC_SCRATCH_BYTES (M * hidden <= 262080); larger sizes fail
+ *   with MUSER_ERR_INVALID_ARG and a message naming the limit.  The call
+ *   never calls cudaMalloc, cudaFree or any routine that allocates.
+ *
+ *   The first call on each device looks up the array's device address, with
+ *   that device current, and keeps it; make that first call before starting
+ *   any stream capture.  Every call clears the completion counter on
+ *   `stream` before its kernels run; the projected rows are overwritten.
+ *
+ *   All calls in the process share the one array of their device, and it
+ *   keeps whatever the last call left in it.  Calls whose work can overlap
+ *   on the GPU (on streams with no ordering between them) race on it and
+ *   give wrong results: issue them on one stream, or order them with events.
+ *
+ *   Other arguments, alignment and errors as muser_qmatvec_residual_dual_rmsnorm.
+ */
+int muser_qmatvec_residual_dual_rmsnorm_static(int qtype, const void* Wdown, int64_t hidden,
+                                               int64_t ffn, const float* mid, int M,
+                                               float* residual, float* out, const float* w1,
+                                               const float* w2, float eps1, float eps2,
+                                               void* stream);
+
 /*
  * One decode-FFN layer's parameters (Ch 10 Figure 10.1 boxes 11-13): gate and
  * up [ffn x hidden], down [hidden x ffn], the post-FFN norm weight (w1, eps1)

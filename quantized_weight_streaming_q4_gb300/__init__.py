@@ -20,7 +20,8 @@ __all__ = [
     "muser_version", "muser_last_error", "muser_block_bytes", "muser_matrix_bytes",
     "muser_dequantize", "muser_qmatvec", "muser_rms_norm", "muser_silu_mul",
     "muser_ffn_gate_up_silu", "muser_fused_residual_dual_rmsnorm", "muser_scratch_bytes",
-    "muser_qmatvec_residual_dual_rmsnorm", "FfnLayer", "muser_ffn_workspace_bytes",
+    "muser_qmatvec_residual_dual_rmsnorm", "muser_qmatvec_residual_dual_rmsnorm_static",
+    "MUSER_STATIC_SCRATCH_BYTES", "FfnLayer", "muser_ffn_workspace_bytes",
     "muser_ffn_stack", "KvPlane", "muser_kv_ring_write", "muser_sync", "muser_debug_spin",
     "muser_device_sm_count", "muser_device_status",
 ]
@@ -28,6 +29,7 @@ __all__ = [
 MUSER_Q4_K = 12
 MUSER_Q6_K = 14
 QTYPES = {"q4_k": MUSER_Q4_K, "q6_k": MUSER_Q6_K}
+MUSER_STATIC_SCRATCH_BYTES = 1 << 20
 BLOCK_BYTES = {MUSER_Q4_K: 144, MUSER_Q6_K: 210}
 STATUS = {0: "MUSER_OK", -1: "MUSER_ERR_INVALID_ARG", -2: "MUSER_ERR_UNSUPPORTED",
           -3: "MUSER_ERR_MISALIGNED", -4: "MUSER_ERR_CACHE_DISCONTINUITY", -5: "MUSER_ERR_CUDA",
@@ -93,6 +95,8 @@ def lib():
             "muser_scratch_bytes": (SZ, [I64, I]),
             "muser_qmatvec_residual_dual_rmsnorm": (I, [I, P, I64, I64, P, I, P, P, P, P, P, F, F, P,
                                                         SZ, P]),
+            "muser_qmatvec_residual_dual_rmsnorm_static": (I, [I, P, I64, I64, P, I, P, P, P, P, F,
+                                                               F, P]),
             "muser_ffn_workspace_bytes": (SZ, [I64, I64, I]),
             "muser_ffn_stack": (I, [ctypes.POINTER(FfnLayer), I, P, I64, I64, I, P, P, F, F, P, SZ,
                                     P]),
@@ -203,6 +207,17 @@ def muser_qmatvec_residual_dual_rmsnorm(qtype, Wdown, hidden: int, ffn: int, mid
                _qt(qtype), _ptr(Wdown), hidden, ffn, _ptr(mid), M, _ptr(projected),
                _ptr(residual), _ptr(out), _ptr(w1), _ptr(w2), eps1, eps2, _ptr(scratch),
                scratch_bytes, _stream(stream)))
+
+
+def muser_qmatvec_residual_dual_rmsnorm_static(qtype, Wdown, hidden: int, ffn: int, mid, M: int,
+                                               residual, out, w1, w2, eps1: float, eps2: float,
+                                               stream=None) -> None:
+    """As muser_qmatvec_residual_dual_rmsnorm, with the library's own fixed
+    scratch in place of `projected` and `scratch` (see include/muser.h)."""
+    _check("muser_qmatvec_residual_dual_rmsnorm_static",
+           lib().muser_qmatvec_residual_dual_rmsnorm_static(
+               _qt(qtype), _ptr(Wdown), hidden, ffn, _ptr(mid), M, _ptr(residual), _ptr(out),
+               _ptr(w1), _ptr(w2), eps1, eps2, _stream(stream)))
 
 
 def muser_ffn_workspace_bytes(hidden: int, ffn: int, M: int) -> int:

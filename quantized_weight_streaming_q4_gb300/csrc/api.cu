@@ -181,6 +181,38 @@ int gate_up_launch(int qtype, const void* Wg, const void* Wu, int64_t ffn, int64
 int sm_count() { return device_attr(g_sm, cudaDevAttrMultiProcessorCount); }
 int max_smem_optin() { return device_attr(g_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin); }
 
+// Scratch of muser_qmatvec_residual_dual_rmsnorm_static: the tail's
+// completion counter in the first kStaticCounterBytes, then the projected
+// rows.  It is part of the library image, so every GPU that loads the library
+// holds it until the process exits.
+static __device__ __align__(256) unsigned char g_static_scratch[MUSER_STATIC_SCRATCH_BYTES];
+
+namespace {
+constexpr size_t kStaticCounterBytes = 256;
+std::mutex g_static_mu;
+void* g_static_ptr[kMaxDev] = {nullptr};
+
+// Device address of g_static_scratch on the current device.  The lookup
+// runs once per device, with that device current; later calls reuse it.
+int static_scratch(const char* fn, unsigned char** ptr) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDev)
+        return set_error(MUSER_ERR_UNSUPPORTED, "%s: device %d beyond the library's %d", fn, dev, kMaxDev);
+    std::lock_guard<std::mutex> lk(g_static_mu);
+    if (g_static_ptr[dev] == nullptr) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_static_scratch);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(static scratch)");
+        if (p == nullptr) return set_error(MUSER_ERR_CUDA, "%s: static scratch has no device address", fn);
+        g_static_ptr[dev] = p;
+    }
+    *ptr = static_cast<unsigned char*>(g_static_ptr[dev]);
+    return MUSER_OK;
+}
+}  // namespace
+
 }  // namespace muser
 
 using namespace muser;
@@ -320,6 +352,43 @@ int muser_qmatvec_residual_dual_rmsnorm(int qtype, const void* Wdown, int64_t hi
         return set_error(MUSER_ERR_INVALID_ARG, "%s: projected, residual and out must be distinct", fn);
     return down_tail_launch(qtype, Wdown, hidden, ffn, mid, M, projected, residual, out, w1, w2,
                             eps1, eps2, scratch, as_stream(stream));
+}
+
+int muser_qmatvec_residual_dual_rmsnorm_static(int qtype, const void* Wdown, int64_t hidden,
+                                               int64_t ffn, const float* mid, int M,
+                                               float* residual, float* out, const float* w1,
+                                               const float* w2, float eps1, float eps2,
+                                               void* stream) {
+    clear_error();
+    const char* fn = "muser_qmatvec_residual_dual_rmsnorm_static";
+    MUSER_TRY(check_matrix(fn, qtype, Wdown, hidden, ffn));
+    MUSER_TRY(check_M(fn, M));
+    MUSER_TRY(check_f32(fn, "mid", mid));
+    MUSER_TRY(check_f32(fn, "residual", residual));
+    MUSER_TRY(check_f32(fn, "out", out));
+    MUSER_TRY(check_f32(fn, "w1", w1));
+    MUSER_TRY(check_f32(fn, "w2", w2));
+    if (hidden % 4) return set_error(MUSER_ERR_INVALID_ARG, "%s: hidden must be a multiple of 4", fn);
+    const size_t need = kStaticCounterBytes + sizeof(float) * static_cast<size_t>(hidden) * M;
+    if (need > MUSER_STATIC_SCRATCH_BYTES)
+        return set_error(MUSER_ERR_INVALID_ARG,
+                         "%s: M * hidden = %lld needs %zu bytes of scratch, more than the library's "
+                         "fixed %zu (M * hidden <= %zu)",
+                         fn, static_cast<long long>(hidden) * M, need,
+                         static_cast<size_t>(MUSER_STATIC_SCRATCH_BYTES),
+                         (static_cast<size_t>(MUSER_STATIC_SCRATCH_BYTES) - kStaticCounterBytes) / sizeof(float));
+    if (!(eps1 > 0.0f) || !(eps2 > 0.0f)) return set_error(MUSER_ERR_INVALID_ARG, "%s: eps must be > 0", fn);
+    if (out == residual) return set_error(MUSER_ERR_INVALID_ARG, "%s: out must not alias residual", fn);
+    unsigned char* base = nullptr;
+    MUSER_TRY(static_scratch(fn, &base));
+    const cudaStream_t s = as_stream(stream);
+    // The array keeps the last call's bytes: the completion counter must read
+    // zero when this call's kernels start, whatever an earlier call left.
+    const cudaError_t e = cudaMemsetAsync(base, 0, kStaticCounterBytes, s);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(static scratch counter)");
+    float* projected = reinterpret_cast<float*>(base + kStaticCounterBytes);
+    return down_tail_launch(qtype, Wdown, hidden, ffn, mid, M, projected, residual, out, w1, w2,
+                            eps1, eps2, base, s);
 }
 
 size_t muser_ffn_workspace_bytes(int64_t hidden, int64_t ffn, int M) {

@@ -123,3 +123,13 @@ def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
     monkeypatch.setattr(mu, "_LIB", str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="not built"):
         mu.lib()
+
+
+@needs_nvcc
+def test_static_scratch_entry_rejects_oversize_before_any_cuda_call(L):
+    # 16 x 16384 floats of projected rows exceed the library's fixed scratch
+    rc = L.muser_qmatvec_residual_dual_rmsnorm_static(12, FAKE, 16384, 256, FAKE, 16, FAKE, FAKE * 2,
+                                                      FAKE, FAKE, 1e-8, 1e-5, None)
+    assert rc == -1 and "262080" in mu.muser_last_error()
+    assert L.muser_qmatvec_residual_dual_rmsnorm_static(12, FAKE, 6656, 19968, FAKE, 1, FAKE, FAKE,
+                                                        FAKE, FAKE, 1e-8, 1e-5, None) == -1  # out aliases residual
