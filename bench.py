@@ -40,12 +40,14 @@ H, F, NL = synth.HIDDEN, synth.FFN, synth.N_LAYERS
 Q4K_MAT = H * (F // 256) * 144          # 74,760,192 B (gate or up; same count as Q4_K down)
 Q6K_MAT = H * (F // 256) * 210          # 109,025,280 B
 LAYER_W = 2 * Q4K_MAT + Q6K_MAT         # 258,545,664 B
+PROBES = 4                              # layers per step whose two launches are event-timed
 METRIC = "weight-stream GB/s (% of GB300 HBM peak); decode FFN tokens/sec, 1 GPU"
 
 # ncu DRAM traffic of the dominant kernel, per launch, with the source hash it
 # was captured on (profiles/ summary); reported as null once the kernel changed.
-NCU_TRAFFIC = {"kernel": "mv1_kernel<Q4_K,2,silu>", "bytes_per_launch": None, "source_sha256": None,
-               "profile": None}
+NCU_TRAFFIC = {"kernel": "mv1_kernel<Q4_K,2,silu>", "bytes_per_launch": 153062912,
+               "source_sha256": "bd36400e0de4348ce62a4aeb04edfc78e76f3072d0a14c1be50fa8c048ffde81",
+               "profile": "profiles/mv1_gate_up_q4k_and_down_q6k_tail.md"}
 
 
 def _env_int(k, d):
@@ -178,26 +180,28 @@ class NativeStack:
             raise RuntimeError(f"{name}: {self.mu.muser_last_error()}")
 
     def step(self, events=None):
-        """One token (M rows) through every layer, per-layer calls; `events`
-        brackets each gate/up launch (the dominant kernel)."""
+        """One token (M rows) through every layer, per-layer calls.  `events`
+        maps a few layers to an event triple that brackets their gate/up and
+        down launches (the others run back to back, overlapped by PDL)."""
         L, M, sh = self.L, self.M, self.sh
         self._rc("rms_norm", L.muser_rms_norm(self.resid.data_ptr(), self.w_in.data_ptr(),
                                               self.x[0].data_ptr(), H, M, 1e-5, sh))
         x, xn = self.x[0], self.x[1]
         for l, d in enumerate(self.layers):
-            if events is not None:
-                events[l][0].record(self.stream)
+            ev = events.get(l) if events is not None else None
+            if ev is not None:
+                ev[0].record(self.stream)
             self._rc("gate_up", L.muser_ffn_gate_up_silu(12, d["Wg"].data_ptr(), d["Wu"].data_ptr(), F, H,
                                                          x.data_ptr(), M, self.mid.data_ptr(), sh))
-            if events is not None:
-                events[l][1].record(self.stream)
+            if ev is not None:
+                ev[1].record(self.stream)
             dst = self.out if l == self.nl - 1 else xn
             self._rc("down_tail", L.muser_qmatvec_residual_dual_rmsnorm(
                 14, d["Wd"].data_ptr(), H, F, self.mid.data_ptr(), M, self.proj.data_ptr(),
                 self.resid.data_ptr(), dst.data_ptr(), d["w1"].data_ptr(), d["w_next"].data_ptr(),
                 1e-8, 1e-5, self.scratch.data_ptr(), 256, sh))
-            if events is not None:
-                events[l][2].record(self.stream)
+            if ev is not None:
+                ev[2].record(self.stream)
             x, xn = xn, x
 
     def step_public(self):
@@ -242,9 +246,14 @@ def run_native(args, rank, world):
     clocks = ClockSampler(uuid)
     clocks.start()
     time.sleep(0.3)
-    # one event triple per layer and step, read after the timed region
-    events = [[[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(nl)]
-              for _ in range(args.steps)]
+    # Per-kernel durations: each step brackets PROBES layers spread over the
+    # stack (a different set every step) with event triples, read after the
+    # timed region.  Events stop PDL overlap only at the bracketed launches.
+    probes = min(PROBES, nl)
+    events = []
+    for k in range(args.steps):
+        ls = sorted({(k + j * max(1, nl // probes)) % nl for j in range(probes)})
+        events.append({l: [torch.cuda.Event(enable_timing=True) for _ in range(3)] for l in ls})
     barrier()
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
@@ -255,8 +264,8 @@ def run_native(args, rank, world):
     barrier()
     total_ms = t_start.elapsed_time(t_end)
     clock = clocks.stop()
-    gu_ms = [ev[l][0].elapsed_time(ev[l][1]) for ev in events for l in range(nl)]
-    dt_ms = [ev[l][1].elapsed_time(ev[l][2]) for ev in events for l in range(nl)]
+    gu_ms = [t[0].elapsed_time(t[1]) for ev in events for t in ev.values()]
+    dt_ms = [t[1].elapsed_time(t[2]) for ev in events for t in ev.values()]
     ms = total_ms / args.steps
     if dist is not None:
         t = torch.tensor([ms], device="cuda")
@@ -294,9 +303,10 @@ def run_native(args, rank, world):
     dt_mean = statistics.mean(dt_ms)
     achieved = gu_bytes / (gu_mean * 1e-3) / 1e9
     traffic = None
-    if NCU_TRAFFIC["bytes_per_launch"] and NCU_TRAFFIC["source_sha256"] == source_sha():
+    if M == 1 and NCU_TRAFFIC["bytes_per_launch"] and NCU_TRAFFIC["source_sha256"] == source_sha():
         traffic = NCU_TRAFFIC["bytes_per_launch"]
     gbs = world * weight_bytes / (ms * 1e-3) / 1e9
+    kname = "mv1" if M == 1 else "mvM"
     result = {
         "metric": METRIC,
         "value": round(gbs, 2),
@@ -323,7 +333,7 @@ def run_native(args, rank, world):
         "hbm_frac_of_" + peak_kind: round(gbs / world / peak, 4),
         "roofline": {
             "bound": "hbm",
-            "kernel": "muser_ffn_gate_up_silu (mv1 Q4_K gate+up, SiLU epilogue)",
+            "kernel": f"muser_ffn_gate_up_silu ({kname} Q4_K gate+up, SiLU epilogue)",
             "achieved": round(achieved, 1),
             "peak": peak,
             "peak_kind": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else "fallback 6.8 TB/s",
@@ -332,7 +342,7 @@ def run_native(args, rank, world):
             "traffic": traffic,
             "algorithmic_bytes_per_launch": gu_bytes,
             "mean_launch_us": round(gu_mean * 1e3, 2),
-            "second_kernel": {"name": "muser_qmatvec_residual_dual_rmsnorm (mv1 Q6_K + tail)",
+            "second_kernel": {"name": f"muser_qmatvec_residual_dual_rmsnorm ({kname} Q6_K + tail)",
                               "achieved_gbs": round(dt_bytes / (dt_mean * 1e-3) / 1e9, 1),
                               "mean_launch_us": round(dt_mean * 1e3, 2),
                               "algorithmic_bytes_per_launch": dt_bytes},

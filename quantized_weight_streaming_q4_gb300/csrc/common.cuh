@@ -151,13 +151,24 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity, ui
         : "memory");
     return ok != 0;
 }
-// Bounded wait on an mbarrier phase: `max_tries` suspended attempts of at most
-// 10 ms each (about 1 s with the default).  Returns false and sets `flag` in
-// the device status word *status if the phase did not complete.
+// Nanoseconds of the GPU's global timer.
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+// Bounded wait on an mbarrier phase: suspended attempts until the phase
+// completes or `limit_ns` of global time (1 s by default) have passed; the
+// bound is in time, so it holds however early an attempt returns.  Returns
+// false and sets `flag` in the device status word *status on giving up.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, unsigned* status,
-                                                  unsigned flag, uint32_t max_tries = 100) {
-    for (uint32_t i = 0; i < max_tries; ++i)
-        if (mbar_try_wait(bar, parity, 10000000u)) return true;
+                                                  unsigned flag, uint64_t limit_ns = 1000000000ull) {
+    if (mbar_try_wait(bar, parity, 1000000u)) return true;
+    const uint64_t t0 = global_ns();
+    for (;;) {
+        if (mbar_try_wait(bar, parity, 1000000u)) return true;
+        if (global_ns() - t0 > limit_ns) break;
+    }
     atomicOr(status, flag);
     return false;
 }

@@ -578,7 +578,7 @@ __global__ void __launch_bounds__(512, 1) mv1_kernel(const Mv1Args p) {
         if (tid == 0) {
             for (int k = max(0, nstages - NS); k < nstages; ++k)
                 (void)mbar_wait_bounded(&full[k % NS], static_cast<uint32_t>((k / NS) & 1),
-                                        &g_device_status, kDevStatusTxTimeout, 20);
+                                        &g_device_status, kDevStatusTxTimeout, 200000000ull);
         }
         return;
     }
