@@ -166,7 +166,8 @@ class NativeStack:
         self.x = [torch.empty(M, H, dtype=torch.float32, device="cuda") for _ in range(2)]
         self.mid = torch.empty(M, F, dtype=torch.float32, device="cuda")
         self.proj = torch.empty(M, H, dtype=torch.float32, device="cuda")
-        self.scratch = torch.zeros(64, dtype=torch.float32, device="cuda")
+        self.scratch_bytes = mu.muser_scratch_bytes(H, M)
+        self.scratch = torch.zeros(self.scratch_bytes // 4 + 64, dtype=torch.float32, device="cuda")
         wsb = mu.muser_ffn_workspace_bytes(H, F, M)
         self.ws = torch.zeros(wsb // 4 + 64, dtype=torch.float32, device="cuda")
         self.wsb = wsb
@@ -199,7 +200,7 @@ class NativeStack:
             self._rc("down_tail", L.muser_qmatvec_residual_dual_rmsnorm(
                 14, d["Wd"].data_ptr(), H, F, self.mid.data_ptr(), M, self.proj.data_ptr(),
                 self.resid.data_ptr(), dst.data_ptr(), d["w1"].data_ptr(), d["w_next"].data_ptr(),
-                1e-8, 1e-5, self.scratch.data_ptr(), 256, sh))
+                1e-8, 1e-5, self.scratch.data_ptr(), self.scratch_bytes, sh))
             if ev is not None:
                 ev[2].record(self.stream)
             x, xn = xn, x

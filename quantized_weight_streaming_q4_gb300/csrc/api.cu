@@ -81,13 +81,18 @@ int check_M(const char* fn, int M) {
     return MUSER_OK;
 }
 
-#define MUSER_TRY(expr)                  \
-    do {                                 \
-        const int _rc = (expr);          \
-        if (_rc != MUSER_OK) return _rc; \
-    } while (0)
 
 constexpr size_t kScratchBytes = 256;
+// Route one-token calls to the tensor-core kernel (mvt) instead of mv1.
+constexpr bool kTensorCoreM1 = false;
+
+// Scratch of the fused down projection + tail: the CUDA-core kernel's ticket
+// (kScratchBytes), then the tensor-core kernel's tickets and partial sums.
+// The bound holds for every row length (a one-block Q6_K row has the most
+// tiles).
+size_t down_scratch_bytes(int64_t hidden) {
+    return kScratchBytes + mvt_scratch_bytes(MUSER_Q6_K, 1, hidden, kQK);
+}
 
 size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
@@ -96,7 +101,9 @@ struct Workspace {
     float* xb;
     float* mid;
     float* proj;
-    void* scratch;
+    void* scratch;     // down + tail scratch, down_scratch_bytes(hidden)
+    void* gu_scratch;  // gate/up tensor-core scratch (null if the shape has none)
+    size_t scratch_bytes;
     size_t total;
 };
 Workspace carve(void* base, int64_t hidden, int64_t ffn, int M) {
@@ -114,7 +121,11 @@ Workspace carve(void* base, int64_t hidden, int64_t ffn, int M) {
     w.proj = reinterpret_cast<float*>(p + off);
     off += hb;
     w.scratch = p + off;
-    off += kScratchBytes;
+    w.scratch_bytes = round_up(down_scratch_bytes(hidden), 256);
+    off += w.scratch_bytes;
+    const size_t gu = mvt_scratch_bytes(MUSER_Q4_K, 2, ffn, hidden);
+    w.gu_scratch = gu ? p + off : nullptr;
+    off += round_up(gu, 256);
     w.total = off;
     return w;
 }
@@ -122,7 +133,27 @@ Workspace carve(void* base, int64_t hidden, int64_t ffn, int M) {
 // Launch the matvec + tail on validated arguments.
 int down_tail_launch(int qtype, const void* Wdown, int64_t hidden, int64_t ffn, const float* mid,
                      int M, float* projected, float* residual, float* out, const float* w1,
-                     const float* w2, float eps1, float eps2, void* scratch, cudaStream_t s) {
+                     const float* w2, float eps1, float eps2, void* scratch, size_t scratch_bytes,
+                     cudaStream_t s) {
+    // One token: the CUDA-core kernel mv1 is measured faster than the
+    // tensor-core kernel on this shape, so it takes M = 1.
+    if (kTensorCoreM1 && M == 1 && mvt_supported(qtype, 1, hidden, ffn) &&
+        scratch_bytes >= kScratchBytes + mvt_scratch_bytes(qtype, 1, hidden, ffn)) {
+        MvtArgs a{};
+        a.W[0] = static_cast<const uint8_t*>(Wdown);
+        a.W[1] = a.W[0];
+        a.rows = hidden;
+        a.nsb = static_cast<int>(ffn / kQK);
+        a.x = mid;
+        a.y = projected;
+        a.resid = residual;
+        a.out = out;
+        a.w1 = w1;
+        a.w2 = w2;
+        a.eps1 = eps1;
+        a.eps2 = eps2;
+        return launch_mvt(qtype, kEpiTail, a, static_cast<uint8_t*>(scratch) + kScratchBytes, s);
+    }
     if (M == 1 && mv1_supported(qtype, ffn)) {
         Mv1Args a{};
         a.W[0] = static_cast<const uint8_t*>(Wdown);
@@ -153,8 +184,19 @@ int down_tail_launch(int qtype, const void* Wdown, int64_t hidden, int64_t ffn, 
                             eps2, s);
 }
 
+// scratch: the tensor-core kernel's even-split scratch, or null (whole tiles).
 int gate_up_launch(int qtype, const void* Wg, const void* Wu, int64_t ffn, int64_t hidden,
-                   const float* x, int M, float* mid, cudaStream_t s) {
+                   const float* x, int M, float* mid, void* scratch, cudaStream_t s) {
+    if (kTensorCoreM1 && M == 1 && mvt_supported(qtype, 2, ffn, hidden)) {
+        MvtArgs a{};
+        a.W[0] = static_cast<const uint8_t*>(Wg);
+        a.W[1] = static_cast<const uint8_t*>(Wu);
+        a.rows = ffn;
+        a.nsb = static_cast<int>(hidden / kQK);
+        a.x = x;
+        a.y = mid;
+        return launch_mvt(qtype, kEpiSiluMul, a, scratch, s);
+    }
     if (M == 1 && mv1_supported(qtype, hidden)) {
         Mv1Args a{};
         a.W[0] = static_cast<const uint8_t*>(Wg);
@@ -301,7 +343,7 @@ int muser_ffn_gate_up_silu(int qtype, const void* Wg, const void* Wu, int64_t ff
     MUSER_TRY(check_M(fn, M));
     MUSER_TRY(check_f32(fn, "x", x));
     MUSER_TRY(check_f32(fn, "mid", mid));
-    return gate_up_launch(qtype, Wg, Wu, ffn, hidden, x, M, mid, as_stream(stream));
+    return gate_up_launch(qtype, Wg, Wu, ffn, hidden, x, M, mid, nullptr, as_stream(stream));
 }
 
 int muser_fused_residual_dual_rmsnorm(float* residual, const float* src, float* out,
@@ -323,9 +365,9 @@ int muser_fused_residual_dual_rmsnorm(float* residual, const float* src, float* 
 }
 
 size_t muser_scratch_bytes(int64_t hidden, int M) {
-    (void)hidden;
     (void)M;
-    return kScratchBytes;
+    if (hidden < 1) return kScratchBytes;
+    return down_scratch_bytes(hidden);
 }
 
 int muser_qmatvec_residual_dual_rmsnorm(int qtype, const void* Wdown, int64_t hidden, int64_t ffn,
@@ -351,7 +393,7 @@ int muser_qmatvec_residual_dual_rmsnorm(int qtype, const void* Wdown, int64_t hi
     if (out == residual || out == projected || projected == residual)
         return set_error(MUSER_ERR_INVALID_ARG, "%s: projected, residual and out must be distinct", fn);
     return down_tail_launch(qtype, Wdown, hidden, ffn, mid, M, projected, residual, out, w1, w2,
-                            eps1, eps2, scratch, as_stream(stream));
+                            eps1, eps2, scratch, scratch_bytes, as_stream(stream));
 }
 
 int muser_qmatvec_residual_dual_rmsnorm_static(int qtype, const void* Wdown, int64_t hidden,
@@ -388,7 +430,7 @@ int muser_qmatvec_residual_dual_rmsnorm_static(int qtype, const void* Wdown, int
     if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(static scratch counter)");
     float* projected = reinterpret_cast<float*>(base + kStaticCounterBytes);
     return down_tail_launch(qtype, Wdown, hidden, ffn, mid, M, projected, residual, out, w1, w2,
-                            eps1, eps2, base, s);
+                            eps1, eps2, base, kStaticCounterBytes, s);
 }
 
 size_t muser_ffn_workspace_bytes(int64_t hidden, int64_t ffn, int M) {
@@ -430,11 +472,11 @@ int muser_ffn_stack(const muser_ffn_layer* layers, int n_layers, const float* en
     float* xnext = ws.xb;
     for (int l = 0; l < n_layers; ++l) {
         const muser_ffn_layer& L = layers[l];
-        MUSER_TRY(gate_up_launch(L.gate_up_qtype, L.w_gate, L.w_up, ffn, hidden, x, M, ws.mid, s));
+        MUSER_TRY(gate_up_launch(L.gate_up_qtype, L.w_gate, L.w_up, ffn, hidden, x, M, ws.mid, ws.gu_scratch, s));
         float* dst = (l == n_layers - 1) ? out : xnext;
         MUSER_TRY(down_tail_launch(L.down_qtype, L.w_down, hidden, ffn, ws.mid, M, ws.proj,
                                    residual, dst, L.post_norm, L.next_norm, eps_post, eps_norm,
-                                   ws.scratch, s));
+                                   ws.scratch, ws.scratch_bytes, s));
         std::swap(x, xnext);
     }
     return MUSER_OK;

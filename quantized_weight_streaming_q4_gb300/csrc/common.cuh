@@ -26,6 +26,13 @@ int sm_count();
 // Max dynamic shared memory per block of the current device (opt-in limit).
 int max_smem_optin();
 
+// Returns the status of `expr` from the enclosing function unless it is MUSER_OK.
+#define MUSER_TRY(expr)                  \
+    do {                                 \
+        const int _rc = (expr);          \
+        if (_rc != MUSER_OK) return _rc; \
+    } while (0)
+
 inline bool is_aligned(const void* p, size_t a) {
     return (reinterpret_cast<uintptr_t>(p) % a) == 0;
 }

@@ -44,6 +44,36 @@ struct MvMArgs {
 };
 int launch_mvM(int qtype, int nmat, int epi, const MvMArgs& a, cudaStream_t s);
 
+// One-token matvec on the tensor cores (mvt.cu).  Gate+up Q4_K with the SiLU
+// epilogue (two matrices), or one Q4_K/Q6_K matrix with the store or tail
+// epilogue.  Work is split into (row tile, super-block) units over all SMs;
+// tiles shared by several CTAs are summed through `part`/`tick` scratch.
+struct MvtArgs {
+    const uint8_t* W[2];
+    int64_t rows;  // rows of each matrix
+    int nsb;       // super-blocks per row
+    const float* x;
+    float* y;      // store: y; silu: mid; tail: projected
+    float* resid;
+    float* out;
+    const float* w1;
+    const float* w2;
+    float eps1, eps2;
+    float* part;      // scratch: partial sums, 128 floats per slot; tile t from CTA c in slot t + c
+    unsigned* tick;   // scratch: per-tile tickets [ntiles], then the tail counter
+    unsigned* status; // device status word
+    // geometry, filled by the launcher
+    int ntiles, P, maxparts, ns, tiles_per_cta;
+    uint32_t x_off, b_off, stage_off;
+};
+bool mvt_supported(int qtype, int nmat, int64_t rows, int64_t cols);
+size_t mvt_scratch_bytes(int qtype, int nmat, int64_t rows, int64_t cols);
+// scratch == nullptr: whole tiles per CTA; else the even split over all SMs
+// with `scratch` of mvt_scratch_bytes() (zero-filled, left zeroed).
+int launch_mvt(int qtype, int epi, MvtArgs a, void* scratch, cudaStream_t s);
+// Device address of the status word (mv1.cu), for kernels in other units.
+unsigned* device_status_word();
+
 // misc.cu
 int launch_dequantize(int qtype, const uint8_t* W, int64_t rows, int64_t cols, float* out,
                       cudaStream_t s);

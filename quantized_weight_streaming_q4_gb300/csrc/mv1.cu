@@ -602,6 +602,12 @@ __global__ void __launch_bounds__(512, 1) mv1_kernel(const Mv1Args p) {
 
 }  // namespace
 
+unsigned* device_status_word() {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_device_status) != cudaSuccess) return nullptr;
+    return static_cast<unsigned*>(ptr);
+}
+
 unsigned read_device_status(bool reset) {
     unsigned v = 0;
     cudaError_t e = cudaMemcpyFromSymbol(&v, g_device_status, sizeof(v));

@@ -1,0 +1,924 @@
+// mvt.cu -- the one-token k-quant matvec of Ch 19 §19.1 (operation 1) and
+// §19.5-§19.6 on the fifth-generation tensor cores (tcgen05), for GB300.
+//
+// What it computes: y[r] = sum_k w[r,k] * x[k] with w the Q4_K or Q6_K
+// weight of Ch 19 §19.3, then the epilogue: store, silu(gate) * up
+// (Ch 10 Figure 10.1 box 11), or the dual-eps tail of Ch 19 §19.4.
+//
+// How:
+//  * Dequantisation is packed.  A 4-bit (or rebuilt 6-bit) code is OR-ed
+//    into the mantissa of the binary16 1024.0, giving 1024 + q exactly, two
+//    codes per 32-bit register.  One fma.rn.f16x2 per pair then makes the
+//    integer sc*q (Q4_K) or sc*(q-32) (Q6_K), exact in binary16 (|.| <= 1024).
+//  * Those integers are the A operand of tcgen05.mma kind::f16, written to
+//    tensor memory (one TMEM lane per weight row, two values per column).
+//  * x is the B operand, split into two binary16 parts,
+//    x * 2^-e = hi + lo * 2^-11, with e a power-of-two scale chosen so that
+//    max|x| * 2^-e < 2^15.  Each product is exact in the binary32
+//    accumulator.  The two D columns are combined as (hi + lo/2048) * 2^e.
+//  * One MMA chain covers one super-block (16 MMAs of K = 16).  Each
+//    super-block's D is read back and scaled by its d (and, for Q4_K, the
+//    min term dmin * sum_j m_j * sum(x over sub-block j) is subtracted), so
+//    the per-block scales never enter the tensor core.
+//  * The K order inside a super-block follows the order the codes come out
+//    of the registers.  x is permuted to match when the B operand is built.
+//
+// Work split: (row tile, super-block) units are spread evenly over the
+// grid.  A tile is 128 TMEM lanes: 128 rows of one matrix, or 64 rows of gate
+// and the same 64 rows of up.  A tile whose units fall in several CTAs is
+// summed from `part` in a fixed order by the last CTA to finish it (atomic
+// ticket), so results do not depend on timing.
+//
+// Weights arrive by 2-D tensor copies: one box of (super-block bytes x tile
+// rows) per matrix and unit.  Q6_K rows of 78 super-blocks are 2-byte
+// aligned, so a tile takes rows of one residue class modulo P (P * row bytes
+// = 0 mod 16): the class is a 2-D array with a 16-byte multiple row stride,
+// every lane of a unit sees the same misalignment, and the box starts at the
+// 16-byte boundary below the block (240-byte box rows).  The shared-memory
+// loads are then 16-byte loads realigned by compile-time shifts.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cstdio>
+#include <mutex>
+#include <type_traits>
+
+#include "common.cuh"
+#include "kernels.cuh"
+
+namespace muser {
+namespace {
+
+// ------------------------------------------------------------ constants
+constexpr int kDeqWarps = 8;                  // warps 0-7: dequantisation, two per TMEM lane quadrant
+constexpr int kTmaWarp = kDeqWarps;           // warp 8: bulk copies
+constexpr int kMmaWarp = kDeqWarps + 1;       // warp 9: TMEM allocation, MMA issue
+constexpr int kRbWarp0 = kDeqWarps + 2;       // warps 10-13: D readback and epilogue, one per quadrant
+constexpr int kThreads = (kDeqWarps + 6) * 32;
+constexpr int kNA = 3;                        // A stages in TMEM (128 columns each)
+constexpr int kND = 4;                        // D buffers in TMEM (16 columns each)
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kDCol0 = kNA * 128;        // first D column
+constexpr int kMaxStages = 12;
+constexpr uint32_t kMagic2 = 0x64006400u;     // binary16 1024.0 in both halves
+
+// ------------------------------------------------------- tcgen05 helpers
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// 32 lanes x 32 columns from this warp's lane quadrant, one column per register.
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* v) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]),
+        "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]),
+        "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]),
+        "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+        : "memory");
+}
+__device__ __forceinline__ void tmem_ld2(uint32_t taddr, uint32_t& a, uint32_t& b) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x2.b32 {%0,%1}, [%2];" : "=r"(a), "=r"(b) : "r"(taddr) : "memory");
+}
+
+// Shared-memory matrix descriptor, no swizzle: start, leading (K-direction
+// core-matrix) byte offset, stride (N-direction 8-row group) byte offset.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+    return static_cast<uint64_t>((addr & 0x3FFFFu) >> 4) | (static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16) |
+           (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46);
+}
+// Instruction descriptor: D binary32, A and B binary16, both K-major,
+// N = 16, M = 128.
+constexpr uint32_t kIdesc = (1u << 4) | ((16u >> 3) << 17) | ((128u >> 4) << 24);
+
+__device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(kIdesc), "r"(accumulate)
+        : "memory");
+}
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+
+// fma.rn.f16x2 on raw register pairs.
+__device__ __forceinline__ uint32_t hfma2u(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t d;
+    asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+// Both halves = the binary16 value of f (f exactly representable).
+__device__ __forceinline__ uint32_t h2rep(float f) {
+    const uint32_t h = __half_as_ushort(__float2half_rn(f));
+    return h | (h << 16);
+}
+
+__device__ __forceinline__ uint4 lds128(const uint8_t* p) { return *reinterpret_cast<const uint4*>(p); }
+
+// 2-D tensor copy of one box at (x bytes, y rows) into shared memory; the
+// completed bytes are counted on `bar`.  x is a multiple of 16.
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::
+            "r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// ------------------------------------------------------ Q4_K (144-byte block)
+// Scale and min (6 bits each) of sub-block j from the packed bytes s[0..11],
+// held as words s0 = s[0..3], s1 = s[4..7], s2 = s[8..11] (Ch 19 §19.3).
+__device__ __forceinline__ void q4k_scale_min(uint32_t s0, uint32_t s1, uint32_t s2, int j, uint32_t& sc,
+                                              uint32_t& m) {
+    if (j < 4) {
+        sc = (s0 >> (8 * j)) & 63u;
+        m = (s1 >> (8 * j)) & 63u;
+    } else {
+        const int b = 8 * (j - 4);
+        sc = ((s2 >> b) & 15u) | (((s0 >> b) >> 6 & 3u) << 4);
+        m = ((s2 >> (b + 4)) & 15u) | (((s1 >> b) >> 6 & 3u) << 4);
+    }
+}
+
+// Column order of a Q4_K super-block (128 TMEM columns, two K slots each):
+// column 32c + 4t + j of chunk c (64 weights), code word t (bytes 4t..4t+3):
+//   j = 0: weights 64c + 4t + {0, 2}     (low nibbles, sub-block 2c)
+//   j = 1: weights 64c + 4t + {1, 3}
+//   j = 2: weights 64c + 32 + 4t + {0, 2} (high nibbles, sub-block 2c + 1)
+//   j = 3: weights 64c + 32 + 4t + {1, 3}
+__device__ __forceinline__ int q4k_slot_weight(int col, int e) {
+    const int c = col >> 5, t = (col >> 2) & 7, j = col & 3;
+    return 64 * c + ((j & 2) ? 32 : 0) + 4 * t + (j & 1) + 2 * e;
+}
+
+// Chunks 2hf and 2hf + 1 of the row's block at `blk` (16-byte aligned) into
+// TMEM columns [col0 + 64hf, +64) of this warp's lanes.
+__device__ __forceinline__ void q4k_dequant_half(const uint8_t* blk, int hf, uint32_t taddr) {
+    const uint4 hd = lds128(blk);
+#pragma unroll
+    for (int cc = 0; cc < 2; ++cc) {
+        const int c = 2 * hf + cc;
+        const uint4 qa = lds128(blk + 16 + 32 * c);
+        const uint4 qb = lds128(blk + 32 + 32 * c);
+        const uint32_t P[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
+        uint32_t scA, scB, mu_;
+        q4k_scale_min(hd.y, hd.z, hd.w, 2 * c, scA, mu_);
+        q4k_scale_min(hd.y, hd.z, hd.w, 2 * c + 1, scB, mu_);
+        const uint32_t kA = h2rep(static_cast<float>(scA)), cA = h2rep(-1024.0f * static_cast<float>(scA));
+        const uint32_t kB = h2rep(static_cast<float>(scB) * 0.0625f), cB = h2rep(-64.0f * static_cast<float>(scB));
+        uint32_t o[32];
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+            const uint32_t p = P[t], p8 = p >> 8;
+            o[4 * t + 0] = hfma2u((p & 0x000F000Fu) | kMagic2, kA, cA);
+            o[4 * t + 1] = hfma2u((p8 & 0x000F000Fu) | kMagic2, kA, cA);
+            o[4 * t + 2] = hfma2u((p & 0x00F000F0u) | kMagic2, kB, cB);
+            o[4 * t + 3] = hfma2u((p8 & 0x00F000F0u) | kMagic2, kB, cB);
+        }
+        tmem_st32(taddr + 32u * c, o);
+    }
+}
+
+// d * 2^e scale and the min term of a Q4_K block for the readback.
+__device__ __forceinline__ void q4k_block_scales(const uint8_t* blk, const float* X, float& d, float& minterm) {
+    const uint4 hd = lds128(blk);
+    d = h2f(hd.x);
+    const float dmin = h2f(hd.x >> 16);
+    float s = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        uint32_t sc, m;
+        q4k_scale_min(hd.y, hd.z, hd.w, j, sc, m);
+        s = fmaf(static_cast<float>(m), X[j], s);
+    }
+    minterm = dmin * s;
+}
+
+// ------------------------------------------------------ Q6_K (210-byte block)
+// Column order of a Q6_K super-block: column 64h + 8i + jj, code word i
+// (bytes 4i..4i+3 of the half's ql groups), jj = 2g + b:
+//   weights 128h + 32g + 4i + b + {0, 2}    (g = 0..3, b = 0, 1)
+// Group g takes the low (g < 2) or high (g >= 2) nibble of ql[64h + 32(g&1) + l]
+// and qh[32h + l] bits 2g, 2g+1 (Ch 19 §19.3).
+__device__ __forceinline__ int q6k_slot_weight(int col, int e) {
+    const int h = col >> 6, i = (col >> 3) & 7, jj = col & 7;
+    return 128 * h + 32 * (jj >> 1) + 4 * i + (jj & 1) + 2 * e;
+}
+
+// Word at byte offset lb (even) of the register copy w[] of a row buffer's
+// 16-byte blocks.  All offsets are compile-time constants once the callers'
+// loops are unrolled, so w[] stays in registers; odd halves are stitched
+// with a funnel shift.
+__device__ __forceinline__ uint32_t word_at(const uint32_t* w, int lb) {
+    if ((lb & 3) == 0) return w[lb >> 2];
+    return __funnelshift_r(w[lb >> 2], w[(lb >> 2) + 1], 16);
+}
+
+// Loads 16-byte blocks [B0, B1] of the row buffer into w[].
+template <int B0, int B1>
+__device__ __forceinline__ void load_blocks(const uint8_t* rb, uint32_t* w) {
+#pragma unroll
+    for (int b = B0; b <= B1; ++b) {
+        const uint4 v = lds128(rb + 16 * b);
+        w[4 * (b - B0)] = v.x;
+        w[4 * (b - B0) + 1] = v.y;
+        w[4 * (b - B0) + 2] = v.z;
+        w[4 * (b - B0) + 3] = v.w;
+    }
+}
+
+// Half H of the row's block starting DELTA bytes into the 16-byte aligned row
+// buffer `rb`, into TMEM columns [64H, +64) of this warp's lanes (taddr is the
+// A stage's first column).
+template <int DELTA, int H>
+__device__ __forceinline__ void q6k_dequant_half(const uint8_t* rb, uint32_t taddr) {
+    constexpr int QL = DELTA + 64 * H, QH = DELTA + 128 + 32 * H, SC = DELTA + 192 + 8 * H;
+    constexpr int LB0 = QL / 16, LB1 = (QL + 65) / 16;
+    constexpr int HB0 = QH / 16, HB1 = (QH + 33) / 16;
+    constexpr int SB0 = SC / 16, SB1 = (SC + 9) / 16;
+    uint32_t ws[4 * (SB1 - SB0 + 1)];
+    load_blocks<SB0, SB1>(rb, ws);
+    const uint32_t S0 = word_at(ws, SC - 16 * SB0), S1 = word_at(ws, SC + 4 - 16 * SB0);
+    uint32_t wl[4 * (LB1 - LB0 + 1)], wh[4 * (HB1 - HB0 + 1)];
+    load_blocks<LB0, LB1>(rb, wl);
+    load_blocks<HB0, HB1>(rb, wh);
+#pragma unroll
+    for (int ci = 0; ci < 2; ++ci) {
+        // words i = 4ci..4ci+3 use the scales sc[8H + 2g + ci], g = 0..3
+        uint32_t k[4], cst[4];
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+            const int idx = 2 * g + ci;
+            const uint32_t sw = idx < 4 ? S0 : S1;
+            const float sc = static_cast<float>(static_cast<int8_t>((sw >> (8 * (idx & 3))) & 0xFFu));
+            k[g] = h2rep(g < 2 ? sc : sc * 0.0625f);
+            cst[g] = h2rep(g < 2 ? -1056.0f * sc : -96.0f * sc);
+        }
+        uint32_t o[32];
+#pragma unroll
+        for (int ii = 0; ii < 4; ++ii) {
+            const int i = 4 * ci + ii;
+            const uint32_t w0 = word_at(wl, QL - 16 * LB0 + 4 * i);       // ql[64H + l], l = 4i..4i+3
+            const uint32_t w1 = word_at(wl, QL - 16 * LB0 + 32 + 4 * i);  // ql[64H + 32 + l]
+            const uint32_t hq = word_at(wh, QH - 16 * HB0 + 4 * i);       // qh[32H + l]
+            const uint32_t w0s = w0 >> 8, w1s = w1 >> 8;
+            const uint32_t s4 = hq << 4, s4r = hq >> 4, s2 = hq << 2, s6r = hq >> 6;
+            // g = 0, 1: 1024 + q; g = 2, 3: 1024 + 16 q (the scale carries 1/16)
+            o[8 * ii + 0] = hfma2u((w0 & 0x000F000Fu) | (s4 & 0x00300030u) | kMagic2, k[0], cst[0]);
+            o[8 * ii + 1] = hfma2u((w0s & 0x000F000Fu) | (s4r & 0x00300030u) | kMagic2, k[0], cst[0]);
+            o[8 * ii + 2] = hfma2u((w1 & 0x000F000Fu) | (s2 & 0x00300030u) | kMagic2, k[1], cst[1]);
+            o[8 * ii + 3] = hfma2u((w1s & 0x000F000Fu) | (s6r & 0x00300030u) | kMagic2, k[1], cst[1]);
+            o[8 * ii + 4] = hfma2u((w0 & 0x00F000F0u) | (s4 & 0x03000300u) | kMagic2, k[2], cst[2]);
+            o[8 * ii + 5] = hfma2u((w0s & 0x00F000F0u) | (s4r & 0x03000300u) | kMagic2, k[2], cst[2]);
+            o[8 * ii + 6] = hfma2u((w1 & 0x00F000F0u) | (s2 & 0x03000300u) | kMagic2, k[3], cst[3]);
+            o[8 * ii + 7] = hfma2u((w1s & 0x00F000F0u) | (s6r & 0x03000300u) | kMagic2, k[3], cst[3]);
+        }
+        tmem_st32(taddr + 64u * H + 32u * ci, o);
+    }
+}
+
+// d of a Q6_K block starting DELTA bytes into the row buffer.
+template <int DELTA>
+__device__ __forceinline__ float q6k_block_d(const uint8_t* rb) {
+    constexpr int D = DELTA + 208;
+    uint32_t w[8];
+    load_blocks<D / 16, (D + 3) / 16>(rb, w);
+    return h2f(word_at(w, D - 16 * (D / 16)));
+}
+
+// ---------------------------------------------------------------- kernel
+__device__ __forceinline__ void named_sync(int id, int n) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+constexpr int kBarReadback = 1;  // the four readback warps (128 threads)
+constexpr int kBarBuild = 2;     // every warp but the bulk-copy warp
+
+// Super-block of the k-th unit of a tile.  Q6_K visits a tile's blocks in
+// (sb mod 8, sb / 8) order: the block's misalignment in shared memory
+// depends only on sb mod 8, so one realignment code path serves runs of
+// consecutive units.  Q4_K blocks are aligned and keep their order.
+template <int QT>
+__device__ __forceinline__ int unit_sb(int k, int nsb) {
+    if constexpr (QT == MUSER_Q4_K) {
+        return k;
+    } else {
+        int start = 0;
+#pragma unroll
+        for (int r = 0; r < 8; ++r) {
+            const int cnt = (nsb - r + 7) >> 3;  // blocks sb = r mod 8 below nsb
+            if (k < start + cnt) return r + 8 * (k - start);
+            start += cnt;
+        }
+        return 0;
+    }
+}
+
+// Walks a CTA's units in order without divisions: tile t, position k in the
+// tile, and the super-block sb visited at that position (see unit_sb).
+template <int QT>
+struct UnitIter {
+    int t, k, sb, nsb;
+    __device__ __forceinline__ UnitIter(int64_t u, int nsb_) : nsb(nsb_) {
+        t = static_cast<int>(u / nsb_);
+        k = static_cast<int>(u - static_cast<int64_t>(t) * nsb_);
+        sb = unit_sb<QT>(k, nsb_);
+    }
+    __device__ __forceinline__ void next() {
+        if (++k == nsb) {
+            k = 0;
+            ++t;
+            sb = 0;
+        } else if constexpr (QT == MUSER_Q4_K) {
+            sb = k;
+        } else {
+            sb += 8;  // next block of the same residue, or the first of the next residue
+            if (sb >= nsb) sb = (sb & 7) + 1;
+        }
+    }
+};
+
+// Slot and phase bit of a ring of barriers, advanced once per unit.
+struct Ring {
+    int slot = 0;
+    uint32_t phase = 0;
+    __device__ __forceinline__ void next(int n) {
+        if (++slot == n) {
+            slot = 0;
+            phase ^= 1u;
+        }
+    }
+};
+
+// CTA that owns unit u when U units are split evenly over G CTAs.
+__device__ __forceinline__ int cta_of(int64_t u, int64_t U, int64_t G) {
+    return static_cast<int>(((u + 1) * G - 1) / U);
+}
+
+struct TileMap {
+    int P, nmat;
+    // Row and matrix of TMEM lane l in tile t.
+    __device__ __forceinline__ int64_t row(int t, int l, int& mat) const {
+        if (nmat == 2) {
+            mat = l >> 6;
+            return static_cast<int64_t>(t) * 64 + (l & 63);
+        }
+        mat = 0;
+        return static_cast<int64_t>(t / P) * 128 * P + static_cast<int64_t>(l) * P + (t % P);
+    }
+};
+
+template <int QT, int EPI>
+__global__ void __launch_bounds__(kThreads, 1)
+    mvt_kernel(const MvtArgs p, const __grid_constant__ CUtensorMap map0, const __grid_constant__ CUtensorMap map1) {
+    constexpr int NMAT = (EPI == kEpiSiluMul) ? 2 : 1;
+    constexpr int kBlk = (QT == MUSER_Q4_K) ? kQ4KBytes : kQ6KBytes;
+    constexpr int RS = (QT == MUSER_Q4_K) ? 144 : 240;  // row slot of a stage (odd multiple of 16 B)
+    constexpr uint32_t kStage = 128u * RS;
+    extern __shared__ __align__(1024) uint8_t smem[];
+    const int nsb = p.nsb;
+    const int64_t rowbytes = static_cast<int64_t>(nsb) * kBlk;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int NS = p.ns;
+    const int64_t U = static_cast<int64_t>(p.ntiles) * nsb, G = gridDim.x;
+    // Even split of the units (tiles may straddle CTAs), or whole tiles.
+    int64_t u0 = U * blockIdx.x / G, u1 = U * (blockIdx.x + 1) / G;
+    if (p.tiles_per_cta > 0) {
+        u0 = std::min<int64_t>(U, static_cast<int64_t>(blockIdx.x) * p.tiles_per_cta * nsb);
+        u1 = std::min<int64_t>(U, u0 + static_cast<int64_t>(p.tiles_per_cta) * nsb);
+    }
+    const int nunits = static_cast<int>(u1 - u0);
+    const TileMap tm{p.P, NMAT};
+
+    // shared memory: barriers | TMEM address, flags | red | xch | scale ring |
+    // per-block x scales, sub-block sums | B operand | weight stages
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem);
+    uint64_t* empty = full + kMaxStages;
+    uint64_t* afull = empty + kMaxStages;
+    uint64_t* aempty = afull + kNA;
+    uint64_t* dfull = aempty + kNA;
+    uint64_t* dempty = dfull + kND;
+    uint64_t* sfull = dempty + kND;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + 352);
+    int* flags = reinterpret_cast<int*>(smem + 368);     // [0] run the tail, [1] tile ticket won
+    float* red = reinterpret_cast<float*>(smem + 512);   // 64 floats
+    float* xch = reinterpret_cast<float*>(smem + 768);   // 128 floats
+    float2* scr = reinterpret_cast<float2*>(smem + 1280);  // [kND][128]: d * 2^e and min term per lane
+    float* esc = reinterpret_cast<float*>(smem + p.x_off);  // [nsb]: 2^e of each block's B
+    float* X = esc + ((nsb + 3) & ~3);                        // Q4_K: [nsb * 8] sub-block sums of x
+    uint8_t* B = smem + p.b_off;
+    uint8_t* stages = smem + p.stage_off;
+
+    if (tid == 0) {
+        for (int i = 0; i < NS; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], kDeqWarps);
+        }
+        for (int i = 0; i < kNA; ++i) {
+            mbar_init(&afull[i], kDeqWarps);
+            mbar_init(&aempty[i], 1);
+        }
+        for (int i = 0; i < kND; ++i) {
+            mbar_init(&dfull[i], 1);
+            mbar_init(&dempty[i], 4);
+            mbar_init(&sfull[i], 4);
+        }
+        flags[0] = 0;
+        flags[1] = 0;
+        fence_mbar_init();
+    }
+    if (warp == kMmaWarp) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                     "r"(kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    pdl_launch_dependents();
+    bool ok = true;
+
+    if (warp == kTmaWarp) {
+        // ------------------------------------------------ bulk-copy warp
+        // Weights do not depend on the previous kernel: no PDL wait here.
+        UnitIter<QT> it(u0, nsb);
+        int s = 0;
+        uint32_t ph = 0;
+        for (int i = 0; i < nunits && ok; ++i, it.next()) {
+            if (i >= NS)
+                ok = mbar_wait_bounded(&empty[s], ph ^ 1u, p.status, kDevStatusWaitTimeout);
+            if (!ok) break;
+            const int t = it.t, sb = it.sb;
+            uint8_t* dst = stages + static_cast<size_t>(s) * kStage;
+            if (lane == 0) {
+                mbar_arrive_expect_tx(&full[s], kStage);
+                if constexpr (NMAT == 2) {
+                    // gate rows to lanes 0..63, up rows to lanes 64..127
+                    tma_load_2d(dst, &map0, sb * kBlk, t * 64, &full[s]);
+                    tma_load_2d(dst + 64 * RS, &map1, sb * kBlk, t * 64, &full[s]);
+                } else if constexpr (QT == MUSER_Q4_K) {
+                    tma_load_2d(dst, &map0, sb * kBlk, t * 128, &full[s]);
+                } else {
+                    // class t % P of block t / P: box from the 16-byte boundary below the block
+                    const int64_t off = static_cast<int64_t>(t % p.P) * rowbytes + static_cast<int64_t>(sb) * kBlk;
+                    tma_load_2d(dst, &map0, static_cast<int>(off & ~static_cast<int64_t>(15)), (t / p.P) * 128, &full[s]);
+                }
+            }
+            __syncwarp();
+            if (++s == NS) {
+                s = 0;
+                ph ^= 1u;
+            }
+        }
+    } else {
+        // -------------------- B operand, per-block x scales, sub-block sums
+        // One warp per super-block: x * 2^-e = hi + lo * 2^-11 in binary16,
+        // in the block's column order, with max|x| * 2^-e < 2^15 per block.
+        pdl_wait();  // x is the previous kernel's output
+        const int bw = warp < kTmaWarp ? warp : warp - 1;
+        constexpr int nbw = kThreads / 32 - 1;
+        auto split = [](float v, uint32_t& hi, uint32_t& lo) {
+            const __half h = __float2half_rn(v);
+            hi = __half_as_ushort(h);
+            lo = __half_as_ushort(__float2half_rn((v - __half2float(h)) * 2048.0f));
+        };
+        auto pack = [&](float a, float b, uint32_t& hi, uint32_t& lo) {
+            uint32_t ha, la, hb, lb;
+            split(a, ha, la);
+            split(b, hb, lb);
+            hi = ha | (hb << 16);
+            lo = la | (lb << 16);
+        };
+        for (int sb = bw; sb < nsb; sb += nbw) {
+            if constexpr (QT == MUSER_Q4_K) {
+                const int c = lane >> 3, t = lane & 7;
+                const float* xs = p.x + sb * 256 + 64 * c + 4 * t;
+                const float4 xa = __ldg(reinterpret_cast<const float4*>(xs));
+                const float4 xb = __ldg(reinterpret_cast<const float4*>(xs + 32));
+                float mx = fmaxf(fmaxf(fmaxf(fabsf(xa.x), fabsf(xa.y)), fmaxf(fabsf(xa.z), fabsf(xa.w))),
+                                 fmaxf(fmaxf(fabsf(xb.x), fabsf(xb.y)), fmaxf(fabsf(xb.z), fabsf(xb.w))));
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+                int E = 0;
+                if (mx > 0.0f) (void)frexpf(mx, &E);  // mx < 2^E
+                E = min(max(E, -100), 120);          // keep both scales finite
+                const float dn = ldexpf(1.0f, 15 - E);
+                uint4 hi, lo;
+                pack(xa.x * dn, xa.z * dn, hi.x, lo.x);
+                pack(xa.y * dn, xa.w * dn, hi.y, lo.y);
+                pack(xb.x * dn, xb.z * dn, hi.z, lo.z);
+                pack(xb.y * dn, xb.w * dn, hi.w, lo.w);
+                uint8_t* ch = B + 32 * (sb * 32 + 8 * c + t);
+                *reinterpret_cast<uint4*>(ch) = hi;
+                *reinterpret_cast<uint4*>(ch + 16) = lo;
+                float sa = (xa.x + xa.y) + (xa.z + xa.w), sbb = (xb.x + xb.y) + (xb.z + xb.w);
+#pragma unroll
+                for (int o = 1; o < 8; o <<= 1) {
+                    sa += __shfl_xor_sync(0xffffffffu, sa, o);
+                    sbb += __shfl_xor_sync(0xffffffffu, sbb, o);
+                }
+                if (t == 0) {
+                    X[sb * 8 + 2 * c] = sa;
+                    X[sb * 8 + 2 * c + 1] = sbb;
+                }
+                if (lane == 0) esc[sb] = ldexpf(1.0f, E - 15);
+            } else {
+                const int item = lane & 15, h = item >> 3, i = item & 7;
+                const float* xs = p.x + sb * 256 + 128 * h + 4 * i;
+                float4 v[4];
+                float mx = 0.0f;
+#pragma unroll
+                for (int g = 0; g < 4; ++g) {
+                    v[g] = __ldg(reinterpret_cast<const float4*>(xs + 32 * g));
+                    mx = fmaxf(mx, fmaxf(fmaxf(fabsf(v[g].x), fabsf(v[g].y)), fmaxf(fabsf(v[g].z), fabsf(v[g].w))));
+                }
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+                int E = 0;
+                if (mx > 0.0f) (void)frexpf(mx, &E);
+                E = min(max(E, -100), 120);
+                const float dn = ldexpf(1.0f, 15 - E);
+                uint4 h0, l0, h1, l1;
+                pack(v[0].x * dn, v[0].z * dn, h0.x, l0.x);
+                pack(v[0].y * dn, v[0].w * dn, h0.y, l0.y);
+                pack(v[1].x * dn, v[1].z * dn, h0.z, l0.z);
+                pack(v[1].y * dn, v[1].w * dn, h0.w, l0.w);
+                pack(v[2].x * dn, v[2].z * dn, h1.x, l1.x);
+                pack(v[2].y * dn, v[2].w * dn, h1.y, l1.y);
+                pack(v[3].x * dn, v[3].z * dn, h1.z, l1.z);
+                pack(v[3].y * dn, v[3].w * dn, h1.w, l1.w);
+                if (lane < 16) {
+                    uint8_t* ch = B + 32 * (sb * 32 + 16 * h + 2 * i);
+                    *reinterpret_cast<uint4*>(ch) = h0;
+                    *reinterpret_cast<uint4*>(ch + 16) = l0;
+                    *reinterpret_cast<uint4*>(ch + 32) = h1;
+                    *reinterpret_cast<uint4*>(ch + 48) = l1;
+                }
+                if (lane == 0) esc[sb] = ldexpf(1.0f, E - 15);
+            }
+        }
+        if (bw == 0) reinterpret_cast<uint4*>(B + nsb * 1024)[lane] = make_uint4(0u, 0u, 0u, 0u);  // slack
+        fence_proxy_async_smem();
+        named_sync(kBarBuild, nbw * 32);
+
+        if (warp == kMmaWarp) {
+            // ----------------------------------------------- MMA issue
+            if (lane == 0) {
+                UnitIter<QT> it(u0, nsb);
+                Ring ra, rd;
+                for (int i = 0; i < nunits && ok; ++i, it.next(), ra.next(kNA), rd.next(kND)) {
+                    const int a = ra.slot, db = rd.slot;
+                    ok = mbar_wait_bounded(&afull[a], ra.phase, p.status, kDevStatusWaitTimeout);
+                    if (ok && i >= kND) ok = mbar_wait_bounded(&dempty[db], rd.phase ^ 1u, p.status, kDevStatusWaitTimeout);
+                    if (!ok) break;
+                    tc_fence_after();
+                    const uint32_t bbase = smem_u32(B) + 1024u * it.sb;
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        mma_f16_ts(tmem + kDCol0 + 16u * db, tmem + 128u * a + 8u * j,
+                                   smem_desc(bbase + 64u * j, 32u, 256u), j > 0 ? 1u : 0u);
+                    mma_commit(&aempty[a]);
+                    mma_commit(&dfull[db]);
+                }
+            }
+            __syncwarp();
+        } else if (warp < kDeqWarps) {
+            // ------------------------------------- dequantisation warps
+            const int q = warp & 3, hf = warp >> 2;
+            const int l = 32 * q + lane;  // this thread's TMEM lane in every tile
+            const uint32_t tq = tmem + (static_cast<uint32_t>(32 * q) << 16);
+            UnitIter<QT> it(u0, nsb);
+            Ring rs, ra, rd;
+            int cur_t = -1, cls_off = 0;  // Q6_K: (class * row bytes) mod 16 of the current tile
+            for (int i = 0; i < nunits; ++i, it.next(), rs.next(NS), ra.next(kNA), rd.next(kND)) {
+                const int s = rs.slot, a = ra.slot, db = rd.slot;
+                if (ok) ok = mbar_wait_bounded(&full[s], rs.phase, p.status, kDevStatusWaitTimeout);
+                if (ok && i >= kNA) ok = mbar_wait_bounded(&aempty[a], ra.phase ^ 1u, p.status, kDevStatusWaitTimeout);
+                const uint8_t* rb = stages + static_cast<size_t>(s) * kStage + l * RS;
+                const uint32_t ta = tq + 128u * a;
+                const int sb = it.sb;
+                float d = 0.0f, mn = 0.0f;
+                if (ok) {
+                    if constexpr (QT == MUSER_Q4_K) {
+                        q4k_dequant_half(rb, hf, ta);
+                        if (hf == 0) q4k_block_scales(rb, X + 8 * sb, d, mn);
+                    } else {
+                        if (it.t != cur_t) {
+                            cur_t = it.t;
+                            cls_off = static_cast<int>((static_cast<int64_t>(cur_t % p.P) * rowbytes) & 15);
+                        }
+                        const int delta = (cls_off + 2 * sb) & 15;  // 210 = 2 mod 16
+                        switch (delta >> 1) {
+#define MUSER_Q6_CASE(k)                                                    \
+    case k:                                                                 \
+        if (hf == 0) {                                                      \
+            q6k_dequant_half<2 * k, 0>(rb, ta);                             \
+            d = q6k_block_d<2 * k>(rb);                                     \
+        } else {                                                            \
+            q6k_dequant_half<2 * k, 1>(rb, ta);                             \
+        }                                                                   \
+        break;
+                            MUSER_Q6_CASE(0) MUSER_Q6_CASE(1) MUSER_Q6_CASE(2) MUSER_Q6_CASE(3)
+                            MUSER_Q6_CASE(4) MUSER_Q6_CASE(5) MUSER_Q6_CASE(6) MUSER_Q6_CASE(7)
+#undef MUSER_Q6_CASE
+                        }
+                    }
+                    tc_wait_st();
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(&afull[a]);
+                    mbar_arrive(&empty[s]);
+                }
+                if (hf == 0) {
+                    // hand this unit's scales to the readback warp of the quadrant
+                    if (ok && i >= kND) ok = mbar_wait_bounded(&dempty[db], rd.phase ^ 1u, p.status, kDevStatusWaitTimeout);
+                    scr[db * 128 + l] = make_float2(d * esc[sb], mn);
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&sfull[db]);
+                }
+            }
+        } else {
+            // ------------------------------ readback and epilogue warps
+            const int q = warp & 3;
+            const int l = 32 * q + lane;
+            const uint32_t tq = tmem + (static_cast<uint32_t>(32 * q) << 16);
+            float yacc = 0.0f;
+            UnitIter<QT> it(u0, nsb);
+            Ring rd;
+            for (int i = 0; i < nunits; ++i, it.next(), rd.next(kND)) {
+                const int db = rd.slot;
+                if (ok) ok = mbar_wait_bounded(&dfull[db], rd.phase, p.status, kDevStatusWaitTimeout);
+                if (ok) ok = mbar_wait_bounded(&sfull[db], rd.phase, p.status, kDevStatusWaitTimeout);
+                uint32_t r0 = 0, r1 = 0;
+                if (ok) {
+                    tc_fence_after();
+                    tmem_ld2(tq + kDCol0 + 16u * db, r0, r1);
+                    tc_wait_ld();
+                }
+                const float2 sc = scr[db * 128 + l];
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&dempty[db]);
+                yacc += fmaf(__uint_as_float(r0) + __uint_as_float(r1) * (1.0f / 2048.0f), sc.x, -sc.y);
+                const int t = it.t;
+                if (it.k != nsb - 1 && i != nunits - 1) continue;
+                // ---- the tile's last unit in this CTA
+                int c0 = blockIdx.x, c1 = blockIdx.x;
+                if (p.tiles_per_cta == 0) {
+                    c0 = cta_of(static_cast<int64_t>(t) * nsb, U, G);
+                    c1 = cta_of(static_cast<int64_t>(t + 1) * nsb - 1, U, G);
+                }
+                float val = yacc;
+                yacc = 0.0f;
+                if (c1 > c0) {
+                    // Tile t's part from CTA c sits in slot t + c: CTAs take the
+                    // units in order, so no two (tile, CTA) pairs share a slot.
+                    float* slot = p.part + static_cast<size_t>(t + c0) * 128;
+                    slot[(blockIdx.x - c0) * 128 + l] = val;
+                    __threadfence();
+                    named_sync(kBarReadback, 128);
+                    if (l == 0) flags[1] = (atomicAdd(&p.tick[t], 1u) == static_cast<unsigned>(c1 - c0)) ? 1 : 0;
+                    named_sync(kBarReadback, 128);
+                    const bool last = flags[1] != 0;
+                    named_sync(kBarReadback, 128);
+                    if (!last) continue;
+                    __threadfence();
+                    val = 0.0f;
+                    for (int pp = 0; pp <= c1 - c0; ++pp) {
+                        val += __ldcg(slot + pp * 128 + l);
+                        slot[pp * 128 + l] = 0.0f;  // leave the scratch zeroed
+                    }
+                    if (l == 0) p.tick[t] = 0u;
+                }
+                int mat;
+                const int64_t row = tm.row(t, l, mat);
+                if constexpr (EPI == kEpiSiluMul) {
+                    xch[l] = val;
+                    named_sync(kBarReadback, 128);
+                    if (l < 64 && row < p.rows) p.y[row] = silu_mul_f(xch[l], xch[l + 64]);
+                    named_sync(kBarReadback, 128);
+                } else {
+                    if (row < p.rows) p.y[row] = val;
+                    if constexpr (EPI == kEpiTail) {
+                        __threadfence();
+                        named_sync(kBarReadback, 128);
+                        if (l == 0 && atomicAdd(&p.tick[p.ntiles], 1u) == static_cast<unsigned>(p.ntiles - 1))
+                            flags[0] = 1;
+                    }
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    ok = __syncthreads_and(ok);
+    if (warp == kMmaWarp) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+    }
+    if constexpr (EPI == kEpiTail) {
+        if (ok && flags[0]) {
+            __threadfence();
+            block_dual_tail_row(p.resid, p.y, p.out, p.w1, p.w2, static_cast<int>(p.rows), p.eps1, p.eps2, red);
+            if (tid == 0) p.tick[p.ntiles] = 0u;
+        }
+    }
+}
+
+}  // namespace
+
+// ------------------------------------------------------------------ host
+namespace {
+
+constexpr int kMaxGrid = 256;  // bound on the grid, so scratch sizes need no device query
+
+struct MvtGeo {
+    int P = 1, ntiles = 0, grid = 0, maxparts = 1, ns = 0, tiles_per_cta = 0;
+    uint32_t x_off = 0, b_off = 0, stage_off = 0, smem = 0;
+};
+
+int gcd_int(int64_t a, int64_t b) {
+    while (b) {
+        const int64_t t = a % b;
+        a = b;
+        b = t;
+    }
+    return static_cast<int>(a);
+}
+
+// Geometry of one launch; false if the shape does not fit this kernel.
+bool mvt_geometry(int qtype, int nmat, int64_t rows, int64_t cols, MvtGeo& g, bool whole_tiles = false) {
+    if (qtype != MUSER_Q4_K && qtype != MUSER_Q6_K) return false;
+    if (nmat == 2 && qtype != MUSER_Q4_K) return false;
+    if (cols % kQK != 0 || rows < 1) return false;
+    const int64_t nsb = cols / kQK;
+    const int blk = qtype == MUSER_Q4_K ? kQ4KBytes : kQ6KBytes;
+    const int64_t rowbytes = nsb * blk;
+    if ((rows * rowbytes) % 16 != 0) return false;  // 16-byte copies never pass the matrix end
+    g.P = nmat == 2 ? 1 : 16 / gcd_int(rowbytes, 16);
+    if (rows % g.P != 0) return false;  // the class view of the matrix must be exact
+    if (nmat == 2) g.ntiles = static_cast<int>((rows + 63) / 64);
+    else g.ntiles = static_cast<int>(g.P * ((rows + 128 * g.P - 1) / (128 * g.P)));
+    const int sms = std::min(sm_count(), kMaxGrid);
+    if (sms <= 0) return false;
+    const int64_t U = static_cast<int64_t>(g.ntiles) * nsb;
+    if (whole_tiles) {
+        g.tiles_per_cta = (g.ntiles + sms - 1) / sms;
+        g.grid = (g.ntiles + g.tiles_per_cta - 1) / g.tiles_per_cta;
+        g.maxparts = 1;
+    } else {
+        g.grid = static_cast<int>(std::min<int64_t>(sms, U));
+        auto cta_of_h = [&](int64_t u) { return static_cast<int>(((u + 1) * g.grid - 1) / U); };
+        g.maxparts = 1;
+        for (int t = 0; t < g.ntiles; ++t)
+            g.maxparts = std::max(g.maxparts, cta_of_h(static_cast<int64_t>(t + 1) * nsb - 1) -
+                                                  cta_of_h(static_cast<int64_t>(t) * nsb) + 1);
+    }
+    // barriers, TMEM address, flags (0..511), red (512..767), xch (768..1279),
+    // scale ring (1280..1280 + kND * 128 * 8)
+    g.x_off = 1280 + kND * 128 * 8;
+    const uint32_t xbytes = static_cast<uint32_t>(((nsb + 3) & ~3) * 4 + (qtype == MUSER_Q4_K ? nsb * 8 * 4 : 0));
+    g.b_off = (g.x_off + xbytes + 127) / 128 * 128;
+    const uint32_t bbytes = static_cast<uint32_t>(nsb * 1024 + 512);
+    g.stage_off = (g.b_off + bbytes + 1023) / 1024 * 1024;
+    const uint32_t stage = 128u * (qtype == MUSER_Q4_K ? 144u : 240u);
+    const int64_t budget = max_smem_optin();
+    if (budget <= g.stage_off) return false;
+    g.ns = static_cast<int>(std::min<int64_t>(kMaxStages, (budget - g.stage_off) / stage));
+    if (g.ns < 3) return false;
+    g.smem = g.stage_off + static_cast<uint32_t>(g.ns) * stage;
+    return true;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    });
+    return fn;
+}
+
+// A 2-D byte-array view of a matrix: `outer` rows of `inner` bytes, `stride`
+// bytes apart, copied in boxes of box_x bytes x box_y rows.
+int encode_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t stride, uint32_t box_x,
+               uint32_t box_y) {
+    auto fn = encode_fn();
+    if (fn == nullptr) return set_error(MUSER_ERR_CUDA, "mvt: cuTensorMapEncodeTiled is not available");
+    const cuuint64_t dims[2] = {inner, outer};
+    const cuuint64_t strides[1] = {stride};
+    const cuuint32_t box[2] = {box_x, box_y};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return set_error(MUSER_ERR_CUDA, "mvt: cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
+    return MUSER_OK;
+}
+
+template <int QT, int EPI>
+int launch_mvt_t(MvtArgs a, const MvtGeo& g, cudaStream_t stream) {
+    constexpr int NMAT = (EPI == kEpiSiluMul) ? 2 : 1;
+    const uint64_t rowbytes = static_cast<uint64_t>(a.nsb) * (QT == MUSER_Q4_K ? kQ4KBytes : kQ6KBytes);
+    const uint64_t rows = static_cast<uint64_t>(a.rows);
+    CUtensorMap m0, m1;
+    if constexpr (QT == MUSER_Q4_K) {
+        const uint32_t box_y = NMAT == 2 ? 64u : 128u;
+        MUSER_TRY(encode_map(&m0, a.W[0], rowbytes, rows, rowbytes, kQ4KBytes, box_y));
+        MUSER_TRY(encode_map(&m1, a.W[NMAT - 1], rowbytes, rows, rowbytes, kQ4KBytes, box_y));
+    } else {
+        const uint64_t P = static_cast<uint64_t>(g.P);
+        MUSER_TRY(encode_map(&m0, a.W[0], P * rowbytes, rows / P, P * rowbytes, 240u, 128u));
+        m1 = m0;
+    }
+    auto kern = mvt_kernel<QT, EPI>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(g.smem));
+    if (e != cudaSuccess) return cuda_fail(e, "mvt: cudaFuncSetAttribute");
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(g.grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = g.smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kern, a, m0, m1);
+    if (e != cudaSuccess) return cuda_fail(e, "mvt: cudaLaunchKernelEx");
+    return check_launch("mvt_kernel");
+}
+
+}  // namespace
+
+bool mvt_supported(int qtype, int nmat, int64_t rows, int64_t cols) {
+    MvtGeo g;
+    return mvt_geometry(qtype, nmat, rows, cols, g, true);
+}
+
+// Scratch of the even split: per-tile tickets and the tail counter, then
+// ntiles + grid - 1 partial slots of 128 floats.  Depends only on the tile
+// count and the grid bound, not on the device.
+size_t mvt_scratch_bytes(int qtype, int nmat, int64_t rows, int64_t cols) {
+    if (qtype != MUSER_Q4_K && qtype != MUSER_Q6_K) return 0;
+    if (cols % kQK != 0 || rows < 1) return 0;
+    const int64_t rowbytes = (cols / kQK) * (qtype == MUSER_Q4_K ? kQ4KBytes : kQ6KBytes);
+    const int P = nmat == 2 ? 1 : 16 / gcd_int(rowbytes, 16);
+    const int64_t ntiles = nmat == 2 ? (rows + 63) / 64 : P * ((rows + 128 * P - 1) / (128 * P));
+    const size_t ticks = (static_cast<size_t>(ntiles) + 1) * sizeof(unsigned);
+    return (ticks + 255) / 256 * 256 + static_cast<size_t>(ntiles + kMaxGrid) * 128 * sizeof(float);
+}
+
+// scratch == nullptr: whole tiles per CTA (no partial sums).  Otherwise the
+// even split, with `scratch` of mvt_scratch_bytes(), zero-filled, left zeroed.
+int launch_mvt(int qtype, int epi, MvtArgs a, void* scratch, cudaStream_t s) {
+    const int nmat = epi == kEpiSiluMul ? 2 : 1;
+    const int64_t cols = static_cast<int64_t>(a.nsb) * kQK;
+    MvtGeo g;
+    if (!mvt_geometry(qtype, nmat, a.rows, cols, g, scratch == nullptr))
+        return set_error(MUSER_ERR_UNSUPPORTED, "mvt: shape not supported");
+    if (epi == kEpiTail && scratch == nullptr)
+        return set_error(MUSER_ERR_UNSUPPORTED, "mvt: the tail epilogue needs scratch");
+    a.ntiles = g.ntiles;
+    a.P = g.P;
+    a.maxparts = g.maxparts;
+    a.ns = g.ns;
+    a.tiles_per_cta = g.tiles_per_cta;
+    a.x_off = g.x_off;
+    a.b_off = g.b_off;
+    a.stage_off = g.stage_off;
+    if (scratch != nullptr) {
+        const size_t ticks = (static_cast<size_t>(g.ntiles) + 1) * sizeof(unsigned);
+        a.tick = static_cast<unsigned*>(scratch);
+        a.part = reinterpret_cast<float*>(static_cast<uint8_t*>(scratch) + (ticks + 255) / 256 * 256);
+    }
+    if (a.status == nullptr) a.status = device_status_word();
+    if (a.status == nullptr) return set_error(MUSER_ERR_CUDA, "mvt: no device status word");
+    if (qtype == MUSER_Q4_K) {
+        if (epi == kEpiSiluMul) return launch_mvt_t<MUSER_Q4_K, kEpiSiluMul>(a, g, s);
+        if (epi == kEpiStore) return launch_mvt_t<MUSER_Q4_K, kEpiStore>(a, g, s);
+        if (epi == kEpiTail) return launch_mvt_t<MUSER_Q4_K, kEpiTail>(a, g, s);
+    } else {
+        if (epi == kEpiStore) return launch_mvt_t<MUSER_Q6_K, kEpiStore>(a, g, s);
+        if (epi == kEpiTail) return launch_mvt_t<MUSER_Q6_K, kEpiTail>(a, g, s);
+    }
+    return set_error(MUSER_ERR_UNSUPPORTED, "mvt: no kernel for qtype %d epilogue %d", qtype, epi);
+}
+
+}  // namespace muser

@@ -182,8 +182,10 @@ def test_tail_zero_projection_keeps_residual_bit_exact():
 
 
 @pytest.mark.parametrize("qtype", ["q4_k", "q6_k"])
-@pytest.mark.parametrize("M", [1, 16])
-def test_down_projection_with_fused_tail(qtype, M):
+@pytest.mark.parametrize("M,small_scratch", [(1, False), (1, True), (16, False)])
+def test_down_projection_with_fused_tail(qtype, M, small_scratch):
+    """M = 1 with full scratch runs the tensor-core kernel (tiles split over
+    all SMs); with the 256-byte minimum it runs the CUDA-core kernel."""
     hidden, ffn = 6656, 19968 if M == 1 else 2048
     case = synth.down_tail_case(qtype, hidden, ffn, M, seed=5)
     a, b = case["a"], case["b"]
@@ -193,7 +195,7 @@ def test_down_projection_with_fused_tail(qtype, M):
     Wd, w1, w2 = dev(case["W"]), dev(case["w1"]), dev(case["w2"])
     resid = dev(case["resid"])
     proj, out = nan_like((M, hidden)), nan_like((M, hidden))
-    nscr = mu.muser_scratch_bytes(hidden, M)
+    nscr = 256 if small_scratch else mu.muser_scratch_bytes(hidden, M)
     scratch = torch.zeros(nscr // 4 + 4, dtype=torch.float32, device="cuda")
     p_ref, r_ref, o_ref = oracle.down_tail(qtype, case["W"], hidden, ffn, mid_ref, case["resid"],
                                            case["w1"], case["w2"])

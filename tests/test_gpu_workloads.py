@@ -44,7 +44,7 @@ def test_workloads_1_2_down_projection_and_tail(qtype, wl):
     resid = dev(case["resid"])
     proj, out = nan_like((1, H)), nan_like((1, H))
     nscr = mu.muser_scratch_bytes(H, 1)
-    scratch = torch.zeros(64, dtype=torch.float32, device="cuda")
+    scratch = torch.zeros(nscr // 4, dtype=torch.float32, device="cuda")
     mu.muser_qmatvec_residual_dual_rmsnorm(qtype, dev(case["W"]), H, F, mid, 1, proj, resid, out,
                                            dev(case["w1"]), dev(case["w2"]), 1e-8, 1e-5, scratch,
                                            nscr)
@@ -159,7 +159,8 @@ def test_workload4_52_layers_teacher_forced_and_end_to_end():
     keep, structs = [], []
     mid16, proj16, out16 = nan_like((16, F)), nan_like((16, H)), nan_like((16, H))
     mid1, proj1, out1 = nan_like((1, F)), nan_like((1, H)), nan_like((1, H))
-    scratch = torch.zeros(64, dtype=torch.float32, device="cuda")
+    nscr = mu.muser_scratch_bytes(H, 16)
+    scratch = torch.zeros(nscr // 4, dtype=torch.float32, device="cuda")
     for l in range(synth.N_LAYERS):
         L = synth.ffn_layer(l, H, F, seed=0, workload=wl)
         w_next = synth.input_norm_weight(l + 1, H, seed=0, workload=wl)
@@ -173,7 +174,7 @@ def test_workload4_52_layers_teacher_forced_and_end_to_end():
             mu.muser_ffn_gate_up_silu("q4_k", d["Wg"], d["Wu"], F, H, xg, Mt, mid)
             assert_close(host(mid).reshape(-1, F)[:Mt], mid_o[:Mt], f"layer {l} mid M={Mt}", scaled=True)
             mu.muser_qmatvec_residual_dual_rmsnorm("q6_k", d["Wd"], H, F, mid, Mt, proj, rg, out,
-                                                   d["w1"], d["w_next"], 1e-8, 1e-5, scratch, 256)
+                                                   d["w1"], d["w_next"], 1e-8, 1e-5, scratch, nscr)
             assert_close(host(proj).reshape(-1, H)[:Mt], p_o[:Mt], f"layer {l} projected M={Mt}", scaled=True)
             assert_close(host(rg), r_next[:Mt], f"layer {l} residual M={Mt}")
             assert_close(host(out).reshape(-1, H)[:Mt], x_next[:Mt], f"layer {l} output M={Mt}")
