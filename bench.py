@@ -307,7 +307,7 @@ def run_native(args, rank, world):
     if M == 1 and NCU_TRAFFIC["bytes_per_launch"] and NCU_TRAFFIC["source_sha256"] == source_sha():
         traffic = NCU_TRAFFIC["bytes_per_launch"]
     gbs = world * weight_bytes / (ms * 1e-3) / 1e9
-    kname = "mv1" if M == 1 else "mvM"
+    kname = "mv1" if M == 1 else "mvt"
     result = {
         "metric": METRIC,
         "value": round(gbs, 2),

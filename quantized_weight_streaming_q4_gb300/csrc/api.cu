@@ -90,8 +90,8 @@ constexpr bool kTensorCoreM1 = false;
 // (kScratchBytes), then the tensor-core kernel's tickets and partial sums.
 // The bound holds for every row length (a one-block Q6_K row has the most
 // tiles).
-size_t down_scratch_bytes(int64_t hidden) {
-    return kScratchBytes + mvt_scratch_bytes(MUSER_Q6_K, 1, hidden, kQK);
+size_t down_scratch_bytes(int64_t hidden, int M) {
+    return kScratchBytes + mvt_scratch_bytes(MUSER_Q6_K, 1, hidden, kQK, M);
 }
 
 size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
@@ -121,9 +121,9 @@ Workspace carve(void* base, int64_t hidden, int64_t ffn, int M) {
     w.proj = reinterpret_cast<float*>(p + off);
     off += hb;
     w.scratch = p + off;
-    w.scratch_bytes = round_up(down_scratch_bytes(hidden), 256);
+    w.scratch_bytes = round_up(down_scratch_bytes(hidden, M), 256);
     off += w.scratch_bytes;
-    const size_t gu = mvt_scratch_bytes(MUSER_Q4_K, 2, ffn, hidden);
+    const size_t gu = mvt_scratch_bytes(MUSER_Q4_K, 2, ffn, hidden, M);
     w.gu_scratch = gu ? p + off : nullptr;
     off += round_up(gu, 256);
     w.total = off;
@@ -137,8 +137,22 @@ int down_tail_launch(int qtype, const void* Wdown, int64_t hidden, int64_t ffn, 
                      cudaStream_t s) {
     // One token: the CUDA-core kernel mv1 is measured faster than the
     // tensor-core kernel on this shape, so it takes M = 1.
-    if (kTensorCoreM1 && M == 1 && mvt_supported(qtype, 1, hidden, ffn) &&
-        scratch_bytes >= kScratchBytes + mvt_scratch_bytes(qtype, 1, hidden, ffn)) {
+    const bool tc_fits = mvt_supported(qtype, 1, hidden, ffn, M) &&
+                         scratch_bytes >= kScratchBytes + mvt_scratch_bytes(qtype, 1, hidden, ffn, M);
+    if (M > 1 && tc_fits) {
+        // several rows: the tensor-core matvec into `projected`, then the tail per row
+        MvtArgs a{};
+        a.W[0] = static_cast<const uint8_t*>(Wdown);
+        a.W[1] = a.W[0];
+        a.rows = hidden;
+        a.nsb = static_cast<int>(ffn / kQK);
+        a.x = mid;
+        a.M = M;
+        a.y = projected;
+        MUSER_TRY(launch_mvt(qtype, kEpiStore, a, static_cast<uint8_t*>(scratch) + kScratchBytes, s));
+        return launch_dual_tail(residual, projected, out, w1, w2, static_cast<int>(hidden), M, eps1, eps2, s);
+    }
+    if (kTensorCoreM1 && M == 1 && tc_fits) {
         MvtArgs a{};
         a.W[0] = static_cast<const uint8_t*>(Wdown);
         a.W[1] = a.W[0];
@@ -152,6 +166,7 @@ int down_tail_launch(int qtype, const void* Wdown, int64_t hidden, int64_t ffn, 
         a.w2 = w2;
         a.eps1 = eps1;
         a.eps2 = eps2;
+        a.M = 1;
         return launch_mvt(qtype, kEpiTail, a, static_cast<uint8_t*>(scratch) + kScratchBytes, s);
     }
     if (M == 1 && mv1_supported(qtype, ffn)) {
@@ -187,13 +202,14 @@ int down_tail_launch(int qtype, const void* Wdown, int64_t hidden, int64_t ffn, 
 // scratch: the tensor-core kernel's even-split scratch, or null (whole tiles).
 int gate_up_launch(int qtype, const void* Wg, const void* Wu, int64_t ffn, int64_t hidden,
                    const float* x, int M, float* mid, void* scratch, cudaStream_t s) {
-    if (kTensorCoreM1 && M == 1 && mvt_supported(qtype, 2, ffn, hidden)) {
+    if ((M > 1 || kTensorCoreM1) && mvt_supported(qtype, 2, ffn, hidden, M)) {
         MvtArgs a{};
         a.W[0] = static_cast<const uint8_t*>(Wg);
         a.W[1] = static_cast<const uint8_t*>(Wu);
         a.rows = ffn;
         a.nsb = static_cast<int>(hidden / kQK);
         a.x = x;
+        a.M = M;
         a.y = mid;
         return launch_mvt(qtype, kEpiSiluMul, a, scratch, s);
     }
@@ -366,8 +382,8 @@ int muser_fused_residual_dual_rmsnorm(float* residual, const float* src, float* 
 
 size_t muser_scratch_bytes(int64_t hidden, int M) {
     (void)M;
-    if (hidden < 1) return kScratchBytes;
-    return down_scratch_bytes(hidden);
+    if (hidden < 1 || M < 1 || M > MUSER_MAX_M) return kScratchBytes;
+    return down_scratch_bytes(hidden, M);
 }
 
 int muser_qmatvec_residual_dual_rmsnorm(int qtype, const void* Wdown, int64_t hidden, int64_t ffn,

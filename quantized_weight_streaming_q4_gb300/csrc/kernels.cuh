@@ -52,8 +52,9 @@ struct MvtArgs {
     const uint8_t* W[2];
     int64_t rows;  // rows of each matrix
     int nsb;       // super-blocks per row
-    const float* x;
-    float* y;      // store: y; silu: mid; tail: projected
+    const float* x;  // [M][nsb*256]
+    int M;           // rows of x (1..16)
+    float* y;        // [M][rows]; store: y; silu: mid; tail: projected
     float* resid;
     float* out;
     const float* w1;
@@ -64,10 +65,10 @@ struct MvtArgs {
     unsigned* status; // device status word
     // geometry, filled by the launcher
     int ntiles, P, maxparts, ns, tiles_per_cta;
-    uint32_t x_off, b_off, stage_off;
+    uint32_t x_off, b_off, stage_off, xch_off;
 };
-bool mvt_supported(int qtype, int nmat, int64_t rows, int64_t cols);
-size_t mvt_scratch_bytes(int qtype, int nmat, int64_t rows, int64_t cols);
+bool mvt_supported(int qtype, int nmat, int64_t rows, int64_t cols, int M);
+size_t mvt_scratch_bytes(int qtype, int nmat, int64_t rows, int64_t cols, int M);
 // scratch == nullptr: whole tiles per CTA; else the even split over all SMs
 // with `scratch` of mvt_scratch_bytes() (zero-filled, left zeroed).
 int launch_mvt(int qtype, int epi, MvtArgs a, void* scratch, cudaStream_t s);

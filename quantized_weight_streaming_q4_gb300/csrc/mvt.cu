@@ -55,9 +55,12 @@ constexpr int kDeqWarps = 8;                  // warps 0-7: dequantisation, two 
 constexpr int kTmaWarp = kDeqWarps;           // warp 8: bulk copies
 constexpr int kMmaWarp = kDeqWarps + 1;       // warp 9: TMEM allocation, MMA issue
 constexpr int kRbWarp0 = kDeqWarps + 2;       // warps 10-13: D readback and epilogue, one per quadrant
-constexpr int kThreads = (kDeqWarps + 6) * 32;
+constexpr int kBldWarp0 = kDeqWarps + 6;      // warps 14-15 (several rows of x): per-unit B operand
+constexpr int kNB = 3;                        // B slabs in shared memory (several rows of x)
 constexpr int kNA = 3;                        // A stages in TMEM (128 columns each)
-constexpr int kND = 4;                        // D buffers in TMEM (16 columns each)
+constexpr int kND = 4;                        // D buffers in TMEM (16 columns, 32 for several rows)
+// Threads of a CTA: one row of x, or several (two more warps build B).
+__host__ __device__ constexpr int mvt_threads(bool multi) { return (kDeqWarps + (multi ? 8 : 6)) * 32; }
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kDCol0 = kNA * 128;        // first D column
 constexpr int kMaxStages = 12;
@@ -87,6 +90,17 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* v) {
 __device__ __forceinline__ void tmem_ld2(uint32_t taddr, uint32_t& a, uint32_t& b) {
     asm volatile("tcgen05.ld.sync.aligned.32x32b.x2.b32 {%0,%1}, [%2];" : "=r"(a), "=r"(b) : "r"(taddr) : "memory");
 }
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t* v) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,"
+        "%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]), "=r"(v[8]),
+          "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]), "=r"(v[16]),
+          "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]),
+          "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+        : "r"(taddr)
+        : "memory");
+}
 
 // Shared-memory matrix descriptor, no swizzle: start, leading (K-direction
 // core-matrix) byte offset, stride (N-direction 8-row group) byte offset.
@@ -95,14 +109,15 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint3
            (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46);
 }
 // Instruction descriptor: D binary32, A and B binary16, both K-major,
-// N = 16, M = 128.
-constexpr uint32_t kIdesc = (1u << 4) | ((16u >> 3) << 17) | ((128u >> 4) << 24);
+// M = 128, N = 16 (one row of x) or 32 (up to 16 rows, hi and lo each).
+constexpr uint32_t idesc_n(uint32_t n) { return (1u << 4) | ((n >> 3) << 17) | ((128u >> 4) << 24); }
 
-__device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t accumulate) {
+__device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                           uint32_t accumulate) {
     asm volatile(
         "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b_desc), "r"(kIdesc), "r"(accumulate)
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
@@ -155,10 +170,6 @@ __device__ __forceinline__ void q4k_scale_min(uint32_t s0, uint32_t s1, uint32_t
 //   j = 1: weights 64c + 4t + {1, 3}
 //   j = 2: weights 64c + 32 + 4t + {0, 2} (high nibbles, sub-block 2c + 1)
 //   j = 3: weights 64c + 32 + 4t + {1, 3}
-__device__ __forceinline__ int q4k_slot_weight(int col, int e) {
-    const int c = col >> 5, t = (col >> 2) & 7, j = col & 3;
-    return 64 * c + ((j & 2) ? 32 : 0) + 4 * t + (j & 1) + 2 * e;
-}
 
 // Chunks 2hf and 2hf + 1 of the row's block at `blk` (16-byte aligned) into
 // TMEM columns [col0 + 64hf, +64) of this warp's lanes.
@@ -203,16 +214,23 @@ __device__ __forceinline__ void q4k_block_scales(const uint8_t* blk, const float
     minterm = dmin * s;
 }
 
+// d, dmin and the eight 6-bit mins of a Q4_K block, one min per byte
+// (sub-blocks 0-3 in m03, 4-7 in m47), for several rows of x.
+__device__ __forceinline__ void q4k_block_dmins(const uint8_t* blk, float& d, float& dmin, uint32_t& m03,
+                                                uint32_t& m47) {
+    const uint4 hd = lds128(blk);
+    d = h2f(hd.x);
+    dmin = h2f(hd.x >> 16);
+    m03 = hd.z & 0x3F3F3F3Fu;
+    m47 = ((hd.w >> 4) & 0x0F0F0F0Fu) | ((hd.z >> 2) & 0x30303030u);
+}
+
 // ------------------------------------------------------ Q6_K (210-byte block)
 // Column order of a Q6_K super-block: column 64h + 8i + jj, code word i
 // (bytes 4i..4i+3 of the half's ql groups), jj = 2g + b:
 //   weights 128h + 32g + 4i + b + {0, 2}    (g = 0..3, b = 0, 1)
 // Group g takes the low (g < 2) or high (g >= 2) nibble of ql[64h + 32(g&1) + l]
 // and qh[32h + l] bits 2g, 2g+1 (Ch 19 §19.3).
-__device__ __forceinline__ int q6k_slot_weight(int col, int e) {
-    const int h = col >> 6, i = (col >> 3) & 7, jj = col & 7;
-    return 128 * h + 32 * (jj >> 1) + 4 * i + (jj & 1) + 2 * e;
-}
 
 // Word at byte offset lb (even) of the register copy w[] of a row buffer's
 // 16-byte blocks.  All offsets are compile-time constants once the callers'
@@ -300,7 +318,7 @@ __device__ __forceinline__ void named_sync(int id, int n) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
 constexpr int kBarReadback = 1;  // the four readback warps (128 threads)
-constexpr int kBarBuild = 2;     // every warp but the bulk-copy warp
+constexpr int kBarBuild = 2;     // one row of x: every warp but the bulk-copy warp
 
 // Super-block of the k-th unit of a tile.  Q6_K visits a tile's blocks in
 // (sb mod 8, sb / 8) order: the block's misalignment in shared memory
@@ -376,15 +394,115 @@ struct TileMap {
     }
 };
 
-template <int QT, int EPI>
-__global__ void __launch_bounds__(kThreads, 1)
-    mvt_kernel(const MvtArgs p, const __grid_constant__ CUtensorMap map0, const __grid_constant__ CUtensorMap map1) {
+// Splits v into binary16 hi and lo with v = hi + lo * 2^-11 (to binary16 precision).
+__device__ __forceinline__ void split_hl(float v, uint32_t& hi, uint32_t& lo) {
+    const __half h = __float2half_rn(v);
+    hi = __half_as_ushort(h);
+    lo = __half_as_ushort(__float2half_rn((v - __half2float(h)) * 2048.0f));
+}
+__device__ __forceinline__ void pack_hl(float a, float b, uint32_t& hi, uint32_t& lo) {
+    uint32_t ha, la, hb, lb;
+    split_hl(a, ha, la);
+    split_hl(b, hb, lb);
+    hi = ha | (hb << 16);
+    lo = la | (lb << 16);
+}
+// Exponent E with max|x| < 2^E, kept in a range where both 2^(15-E) and
+// 2^(E-15) are finite normal floats.
+__device__ __forceinline__ int scale_exp(float mx) {
+    int E = 0;
+    if (mx > 0.0f) (void)frexpf(mx, &E);
+    return min(max(E, -100), 120);
+}
+
+// One row of x for one super-block, by one warp: binary16 hi/lo words of the
+// block's 128 columns (four per lane for Q4_K: words hi[0..3], lo[0..3] of
+// chunk 8c + t; eight for Q6_K lanes 0-15: chunks 16h + 2i and + 1), the
+// block's power-of-two scale 2^e (max|x| * 2^-e < 2^15) and, for Q4_K, the
+// sub-block sums of x (valid in lanes t == 0: sub-blocks 2c and 2c + 1).
+template <int QT>
+struct BlockX {
+    uint4 hi0, lo0, hi1, lo1;
+    float esc, sa, sb;
+};
+template <int QT, bool kShared = false>
+__device__ __forceinline__ BlockX<QT> block_x(const float* xb, int lane) {
+    auto ld4 = [](const float* a) {
+        if constexpr (kShared) return *reinterpret_cast<const float4*>(a);
+        else return __ldg(reinterpret_cast<const float4*>(a));
+    };
+    BlockX<QT> r;
+    if constexpr (QT == MUSER_Q4_K) {
+        const int c = lane >> 3, t = lane & 7;
+        const float* xs = xb + 64 * c + 4 * t;
+        const float4 xa = ld4(xs);
+        const float4 xc = ld4(xs + 32);
+        float mx = fmaxf(fmaxf(fmaxf(fabsf(xa.x), fabsf(xa.y)), fmaxf(fabsf(xa.z), fabsf(xa.w))),
+                         fmaxf(fmaxf(fabsf(xc.x), fabsf(xc.y)), fmaxf(fabsf(xc.z), fabsf(xc.w))));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        const int E = scale_exp(mx);
+        const float dn = ldexpf(1.0f, 15 - E);
+        pack_hl(xa.x * dn, xa.z * dn, r.hi0.x, r.lo0.x);
+        pack_hl(xa.y * dn, xa.w * dn, r.hi0.y, r.lo0.y);
+        pack_hl(xc.x * dn, xc.z * dn, r.hi0.z, r.lo0.z);
+        pack_hl(xc.y * dn, xc.w * dn, r.hi0.w, r.lo0.w);
+        float sa = (xa.x + xa.y) + (xa.z + xa.w), sc = (xc.x + xc.y) + (xc.z + xc.w);
+#pragma unroll
+        for (int o = 1; o < 8; o <<= 1) {
+            sa += __shfl_xor_sync(0xffffffffu, sa, o);
+            sc += __shfl_xor_sync(0xffffffffu, sc, o);
+        }
+        r.sa = sa;
+        r.sb = sc;
+        r.esc = ldexpf(1.0f, E - 15);
+    } else {
+        const int item = lane & 15, h = item >> 3, i = item & 7;
+        const float* xs = xb + 128 * h + 4 * i;
+        float4 v[4];
+        float mx = 0.0f;
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+            v[g] = ld4(xs + 32 * g);
+            mx = fmaxf(mx, fmaxf(fmaxf(fabsf(v[g].x), fabsf(v[g].y)), fmaxf(fabsf(v[g].z), fabsf(v[g].w))));
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        const int E = scale_exp(mx);
+        const float dn = ldexpf(1.0f, 15 - E);
+        pack_hl(v[0].x * dn, v[0].z * dn, r.hi0.x, r.lo0.x);
+        pack_hl(v[0].y * dn, v[0].w * dn, r.hi0.y, r.lo0.y);
+        pack_hl(v[1].x * dn, v[1].z * dn, r.hi0.z, r.lo0.z);
+        pack_hl(v[1].y * dn, v[1].w * dn, r.hi0.w, r.lo0.w);
+        pack_hl(v[2].x * dn, v[2].z * dn, r.hi1.x, r.lo1.x);
+        pack_hl(v[2].y * dn, v[2].w * dn, r.hi1.y, r.lo1.y);
+        pack_hl(v[3].x * dn, v[3].z * dn, r.hi1.z, r.lo1.z);
+        pack_hl(v[3].y * dn, v[3].w * dn, r.hi1.w, r.lo1.w);
+        r.sa = r.sb = 0.0f;
+        r.esc = ldexpf(1.0f, E - 15);
+    }
+    return r;
+}
+
+template <int QT, int EPI, bool MULTI>
+__global__ void __launch_bounds__(mvt_threads(MULTI), 1)
+    mvt_kernel(const MvtArgs p, const __grid_constant__ CUtensorMap map0, const __grid_constant__ CUtensorMap map1,
+               const __grid_constant__ CUtensorMap mapx) {
     constexpr int NMAT = (EPI == kEpiSiluMul) ? 2 : 1;
     constexpr int kBlk = (QT == MUSER_Q4_K) ? kQ4KBytes : kQ6KBytes;
     constexpr int RS = (QT == MUSER_Q4_K) ? 144 : 240;  // row slot of a stage (odd multiple of 16 B)
     constexpr uint32_t kStage = 128u * RS;
+    constexpr int kThr = mvt_threads(MULTI);
+    constexpr uint32_t kXSlot = 8 * 256 * 4;             // eight rows of x for one block
+    constexpr int MB = MULTI ? 16 : 1;                   // rows of x a lane accumulates
+    constexpr uint32_t kDCols = MULTI ? 32u : 16u;       // D columns per buffer
+    constexpr uint32_t kIdesc = idesc_n(kDCols);
+    constexpr uint32_t kSlab = 16384;                    // B slab of one unit (several rows of x)
+    constexpr int kXr = MB * 8 + MB;                     // per-unit x sums (Q4_K) and scales, floats
     extern __shared__ __align__(1024) uint8_t smem[];
     const int nsb = p.nsb;
+    const int K = nsb * 256;
+    const int M = MULTI ? p.M : 1;
     const int64_t rowbytes = static_cast<int64_t>(nsb) * kBlk;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int NS = p.ns;
@@ -398,8 +516,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int nunits = static_cast<int>(u1 - u0);
     const TileMap tm{p.P, NMAT};
 
-    // shared memory: barriers | TMEM address, flags | red | xch | scale ring |
-    // per-block x scales, sub-block sums | B operand | weight stages
+    // shared memory: barriers | TMEM address, flags | red | scale ring | xch |
+    // x scales and sums | B operand | weight stages
     uint64_t* full = reinterpret_cast<uint64_t*>(smem);
     uint64_t* empty = full + kMaxStages;
     uint64_t* afull = empty + kMaxStages;
@@ -407,14 +525,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* dfull = aempty + kNA;
     uint64_t* dempty = dfull + kND;
     uint64_t* sfull = dempty + kND;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + 352);
-    int* flags = reinterpret_cast<int*>(smem + 368);     // [0] run the tail, [1] tile ticket won
-    float* red = reinterpret_cast<float*>(smem + 512);   // 64 floats
-    float* xch = reinterpret_cast<float*>(smem + 768);   // 128 floats
-    float2* scr = reinterpret_cast<float2*>(smem + 1280);  // [kND][128]: d * 2^e and min term per lane
-    float* esc = reinterpret_cast<float*>(smem + p.x_off);  // [nsb]: 2^e of each block's B
-    float* X = esc + ((nsb + 3) & ~3);                        // Q4_K: [nsb * 8] sub-block sums of x
+    uint64_t* bfull = sfull + kND;
+    uint64_t* bempty = bfull + kNB;
+    uint64_t* xfull = bempty + kNB;  // [2 builder warps][kNB]
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + 448);
+    int* flags = reinterpret_cast<int*>(smem + 464);       // [0] run the tail, [1] tile ticket won
+    float* red = reinterpret_cast<float*>(smem + 512);     // 64 floats
+    float4* scr = reinterpret_cast<float4*>(smem + 1280);  // [kND][128] block scales per lane
+    float* xch = reinterpret_cast<float*>(smem + p.xch_off);  // [MB][128] tile values
+    // one row of x: esc[nsb] 2^e per block, X[nsb * 8] sub-block sums;
+    // several rows: a ring [kND][kXr] of X[m][8] and esc[m] per unit
+    float* esc = reinterpret_cast<float*>(smem + p.x_off);
+    float* X = esc + ((nsb + 3) & ~3);
+    float* xr = reinterpret_cast<float*>(smem + p.x_off);
     uint8_t* B = smem + p.b_off;
+    uint8_t* xring = B + kNB * kSlab;  // several rows: [2 builder warps][kNB] slots of 8 rows of x
     uint8_t* stages = smem + p.stage_off;
 
     if (tid == 0) {
@@ -429,7 +554,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < kND; ++i) {
             mbar_init(&dfull[i], 1);
             mbar_init(&dempty[i], 4);
-            mbar_init(&sfull[i], 4);
+            mbar_init(&sfull[i], MULTI ? 6 : 4);  // dequant warps of half 0 (+ the builders)
+        }
+        for (int i = 0; i < kNB; ++i) {
+            mbar_init(&bfull[i], 2);
+            mbar_init(&bempty[i], 1);
+            mbar_init(&xfull[i], 1);
+            mbar_init(&xfull[kNB + i], 1);
         }
         flags[0] = 0;
         flags[1] = 0;
@@ -452,11 +583,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------ bulk-copy warp
         // Weights do not depend on the previous kernel: no PDL wait here.
         UnitIter<QT> it(u0, nsb);
-        int s = 0;
-        uint32_t ph = 0;
-        for (int i = 0; i < nunits && ok; ++i, it.next()) {
-            if (i >= NS)
-                ok = mbar_wait_bounded(&empty[s], ph ^ 1u, p.status, kDevStatusWaitTimeout);
+        Ring rs;
+        for (int i = 0; i < nunits && ok; ++i, it.next(), rs.next(NS)) {
+            const int s = rs.slot;
+            if (i >= NS) ok = mbar_wait_bounded(&empty[s], rs.phase ^ 1u, p.status, kDevStatusWaitTimeout);
             if (!ok) break;
             const int t = it.t, sb = it.sb;
             uint8_t* dst = stages + static_cast<size_t>(s) * kStage;
@@ -475,118 +605,66 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             __syncwarp();
-            if (++s == NS) {
-                s = 0;
-                ph ^= 1u;
-            }
         }
     } else {
-        // -------------------- B operand, per-block x scales, sub-block sums
-        // One warp per super-block: x * 2^-e = hi + lo * 2^-11 in binary16,
-        // in the block's column order, with max|x| * 2^-e < 2^15 per block.
-        pdl_wait();  // x is the previous kernel's output
-        const int bw = warp < kTmaWarp ? warp : warp - 1;
-        constexpr int nbw = kThreads / 32 - 1;
-        auto split = [](float v, uint32_t& hi, uint32_t& lo) {
-            const __half h = __float2half_rn(v);
-            hi = __half_as_ushort(h);
-            lo = __half_as_ushort(__float2half_rn((v - __half2float(h)) * 2048.0f));
-        };
-        auto pack = [&](float a, float b, uint32_t& hi, uint32_t& lo) {
-            uint32_t ha, la, hb, lb;
-            split(a, ha, la);
-            split(b, hb, lb);
-            hi = ha | (hb << 16);
-            lo = la | (lb << 16);
-        };
-        for (int sb = bw; sb < nsb; sb += nbw) {
-            if constexpr (QT == MUSER_Q4_K) {
-                const int c = lane >> 3, t = lane & 7;
-                const float* xs = p.x + sb * 256 + 64 * c + 4 * t;
-                const float4 xa = __ldg(reinterpret_cast<const float4*>(xs));
-                const float4 xb = __ldg(reinterpret_cast<const float4*>(xs + 32));
-                float mx = fmaxf(fmaxf(fmaxf(fabsf(xa.x), fabsf(xa.y)), fmaxf(fabsf(xa.z), fabsf(xa.w))),
-                                 fmaxf(fmaxf(fabsf(xb.x), fabsf(xb.y)), fmaxf(fabsf(xb.z), fabsf(xb.w))));
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-                int E = 0;
-                if (mx > 0.0f) (void)frexpf(mx, &E);  // mx < 2^E
-                E = min(max(E, -100), 120);          // keep both scales finite
-                const float dn = ldexpf(1.0f, 15 - E);
-                uint4 hi, lo;
-                pack(xa.x * dn, xa.z * dn, hi.x, lo.x);
-                pack(xa.y * dn, xa.w * dn, hi.y, lo.y);
-                pack(xb.x * dn, xb.z * dn, hi.z, lo.z);
-                pack(xb.y * dn, xb.w * dn, hi.w, lo.w);
-                uint8_t* ch = B + 32 * (sb * 32 + 8 * c + t);
-                *reinterpret_cast<uint4*>(ch) = hi;
-                *reinterpret_cast<uint4*>(ch + 16) = lo;
-                float sa = (xa.x + xa.y) + (xa.z + xa.w), sbb = (xb.x + xb.y) + (xb.z + xb.w);
-#pragma unroll
-                for (int o = 1; o < 8; o <<= 1) {
-                    sa += __shfl_xor_sync(0xffffffffu, sa, o);
-                    sbb += __shfl_xor_sync(0xffffffffu, sbb, o);
-                }
-                if (t == 0) {
-                    X[sb * 8 + 2 * c] = sa;
-                    X[sb * 8 + 2 * c + 1] = sbb;
-                }
-                if (lane == 0) esc[sb] = ldexpf(1.0f, E - 15);
-            } else {
-                const int item = lane & 15, h = item >> 3, i = item & 7;
-                const float* xs = p.x + sb * 256 + 128 * h + 4 * i;
-                float4 v[4];
-                float mx = 0.0f;
-#pragma unroll
-                for (int g = 0; g < 4; ++g) {
-                    v[g] = __ldg(reinterpret_cast<const float4*>(xs + 32 * g));
-                    mx = fmaxf(mx, fmaxf(fmaxf(fabsf(v[g].x), fabsf(v[g].y)), fmaxf(fabsf(v[g].z), fabsf(v[g].w))));
-                }
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-                int E = 0;
-                if (mx > 0.0f) (void)frexpf(mx, &E);
-                E = min(max(E, -100), 120);
-                const float dn = ldexpf(1.0f, 15 - E);
-                uint4 h0, l0, h1, l1;
-                pack(v[0].x * dn, v[0].z * dn, h0.x, l0.x);
-                pack(v[0].y * dn, v[0].w * dn, h0.y, l0.y);
-                pack(v[1].x * dn, v[1].z * dn, h0.z, l0.z);
-                pack(v[1].y * dn, v[1].w * dn, h0.w, l0.w);
-                pack(v[2].x * dn, v[2].z * dn, h1.x, l1.x);
-                pack(v[2].y * dn, v[2].w * dn, h1.y, l1.y);
-                pack(v[3].x * dn, v[3].z * dn, h1.z, l1.z);
-                pack(v[3].y * dn, v[3].w * dn, h1.w, l1.w);
-                if (lane < 16) {
+        pdl_wait();  // x is the previous kernel's output; outputs are written after it
+        if constexpr (!MULTI) {
+            // ---------- one row of x: the whole B operand, one warp per block
+            const int bw = warp < kTmaWarp ? warp : warp - 1;
+            constexpr int nbw = kThr / 32 - 1;
+            for (int sb = bw; sb < nsb; sb += nbw) {
+                const BlockX<QT> bx = block_x<QT>(p.x + sb * 256, lane);
+                if constexpr (QT == MUSER_Q4_K) {
+                    const int c = lane >> 3, t = lane & 7;
+                    uint8_t* ch = B + 32 * (sb * 32 + 8 * c + t);
+                    *reinterpret_cast<uint4*>(ch) = bx.hi0;
+                    *reinterpret_cast<uint4*>(ch + 16) = bx.lo0;
+                    if (t == 0) {
+                        X[sb * 8 + 2 * c] = bx.sa;
+                        X[sb * 8 + 2 * c + 1] = bx.sb;
+                    }
+                } else if (lane < 16) {
+                    const int h = lane >> 3, i = lane & 7;
                     uint8_t* ch = B + 32 * (sb * 32 + 16 * h + 2 * i);
-                    *reinterpret_cast<uint4*>(ch) = h0;
-                    *reinterpret_cast<uint4*>(ch + 16) = l0;
-                    *reinterpret_cast<uint4*>(ch + 32) = h1;
-                    *reinterpret_cast<uint4*>(ch + 48) = l1;
+                    *reinterpret_cast<uint4*>(ch) = bx.hi0;
+                    *reinterpret_cast<uint4*>(ch + 16) = bx.lo0;
+                    *reinterpret_cast<uint4*>(ch + 32) = bx.hi1;
+                    *reinterpret_cast<uint4*>(ch + 48) = bx.lo1;
                 }
-                if (lane == 0) esc[sb] = ldexpf(1.0f, E - 15);
+                if (lane == 0) esc[sb] = bx.esc;
             }
+            if (bw == 0) reinterpret_cast<uint4*>(B + nsb * 1024)[lane] = make_uint4(0u, 0u, 0u, 0u);  // slack
+            fence_proxy_async_smem();
+            named_sync(kBarBuild, nbw * 32);
         }
-        if (bw == 0) reinterpret_cast<uint4*>(B + nsb * 1024)[lane] = make_uint4(0u, 0u, 0u, 0u);  // slack
-        fence_proxy_async_smem();
-        named_sync(kBarBuild, nbw * 32);
 
         if (warp == kMmaWarp) {
             // ----------------------------------------------- MMA issue
             if (lane == 0) {
                 UnitIter<QT> it(u0, nsb);
-                Ring ra, rd;
-                for (int i = 0; i < nunits && ok; ++i, it.next(), ra.next(kNA), rd.next(kND)) {
+                Ring ra, rd, rb;
+                for (int i = 0; i < nunits && ok; ++i, it.next(), ra.next(kNA), rd.next(kND), rb.next(kNB)) {
                     const int a = ra.slot, db = rd.slot;
                     ok = mbar_wait_bounded(&afull[a], ra.phase, p.status, kDevStatusWaitTimeout);
+                    if (MULTI && ok) ok = mbar_wait_bounded(&bfull[rb.slot], rb.phase, p.status, kDevStatusWaitTimeout);
                     if (ok && i >= kND) ok = mbar_wait_bounded(&dempty[db], rd.phase ^ 1u, p.status, kDevStatusWaitTimeout);
                     if (!ok) break;
                     tc_fence_after();
-                    const uint32_t bbase = smem_u32(B) + 1024u * it.sb;
+                    const uint32_t dcol = tmem + kDCol0 + kDCols * db, acol = tmem + 128u * a;
+                    if constexpr (MULTI) {
+                        // slab: K chunk stride 512 B, N-group stride 128 B
+                        const uint32_t bbase = smem_u32(B) + kSlab * rb.slot;
 #pragma unroll
-                    for (int j = 0; j < 16; ++j)
-                        mma_f16_ts(tmem + kDCol0 + 16u * db, tmem + 128u * a + 8u * j,
-                                   smem_desc(bbase + 64u * j, 32u, 256u), j > 0 ? 1u : 0u);
+                        for (int j = 0; j < 16; ++j)
+                            mma_f16_ts(dcol, acol + 8u * j, smem_desc(bbase + 1024u * j, 512u, 128u), kIdesc, j > 0 ? 1u : 0u);
+                        mma_commit(&bempty[rb.slot]);
+                    } else {
+                        // compact: two rows per 32-byte chunk, chunks overlap
+                        const uint32_t bbase = smem_u32(B) + 1024u * it.sb;
+#pragma unroll
+                        for (int j = 0; j < 16; ++j)
+                            mma_f16_ts(dcol, acol + 8u * j, smem_desc(bbase + 64u * j, 32u, 256u), kIdesc, j > 0 ? 1u : 0u);
+                    }
                     mma_commit(&aempty[a]);
                     mma_commit(&dfull[db]);
                 }
@@ -604,34 +682,46 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int s = rs.slot, a = ra.slot, db = rd.slot;
                 if (ok) ok = mbar_wait_bounded(&full[s], rs.phase, p.status, kDevStatusWaitTimeout);
                 if (ok && i >= kNA) ok = mbar_wait_bounded(&aempty[a], ra.phase ^ 1u, p.status, kDevStatusWaitTimeout);
-                const uint8_t* rb = stages + static_cast<size_t>(s) * kStage + l * RS;
+                const uint8_t* rbuf = stages + static_cast<size_t>(s) * kStage + l * RS;
                 const uint32_t ta = tq + 128u * a;
                 const int sb = it.sb;
-                float d = 0.0f, mn = 0.0f;
+                float4 sc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
                 if (ok) {
                     if constexpr (QT == MUSER_Q4_K) {
-                        q4k_dequant_half(rb, hf, ta);
-                        if (hf == 0) q4k_block_scales(rb, X + 8 * sb, d, mn);
+                        q4k_dequant_half(rbuf, hf, ta);
+                        if (hf == 0) {
+                            if constexpr (MULTI) {
+                                uint32_t m03, m47;
+                                q4k_block_dmins(rbuf, sc.x, sc.y, m03, m47);
+                                sc.z = __uint_as_float(m03);
+                                sc.w = __uint_as_float(m47);
+                            } else {
+                                q4k_block_scales(rbuf, X + 8 * sb, sc.x, sc.y);
+                                sc.x *= esc[sb];
+                            }
+                        }
                     } else {
                         if (it.t != cur_t) {
                             cur_t = it.t;
                             cls_off = static_cast<int>((static_cast<int64_t>(cur_t % p.P) * rowbytes) & 15);
                         }
                         const int delta = (cls_off + 2 * sb) & 15;  // 210 = 2 mod 16
+                        float d = 0.0f;
                         switch (delta >> 1) {
 #define MUSER_Q6_CASE(k)                                                    \
     case k:                                                                 \
         if (hf == 0) {                                                      \
-            q6k_dequant_half<2 * k, 0>(rb, ta);                             \
-            d = q6k_block_d<2 * k>(rb);                                     \
+            q6k_dequant_half<2 * k, 0>(rbuf, ta);                           \
+            d = q6k_block_d<2 * k>(rbuf);                                   \
         } else {                                                            \
-            q6k_dequant_half<2 * k, 1>(rb, ta);                             \
+            q6k_dequant_half<2 * k, 1>(rbuf, ta);                           \
         }                                                                   \
         break;
                             MUSER_Q6_CASE(0) MUSER_Q6_CASE(1) MUSER_Q6_CASE(2) MUSER_Q6_CASE(3)
                             MUSER_Q6_CASE(4) MUSER_Q6_CASE(5) MUSER_Q6_CASE(6) MUSER_Q6_CASE(7)
 #undef MUSER_Q6_CASE
                         }
+                        sc.x = MULTI ? d : d * esc[sb];
                     }
                     tc_wait_st();
                 }
@@ -642,36 +732,131 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mbar_arrive(&empty[s]);
                 }
                 if (hf == 0) {
-                    // hand this unit's scales to the readback warp of the quadrant
+                    // hand this unit's block scales to the readback warp of the quadrant
                     if (ok && i >= kND) ok = mbar_wait_bounded(&dempty[db], rd.phase ^ 1u, p.status, kDevStatusWaitTimeout);
-                    scr[db * 128 + l] = make_float2(d * esc[sb], mn);
+                    scr[db * 128 + l] = sc;
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&sfull[db]);
                 }
             }
-        } else {
+        } else if (MULTI && warp >= kBldWarp0) {
+            // -------- several rows of x: per-unit B slabs, scales and sums
+            // Builder warp bw owns rows 8bw..8bw+7 of x; its slots of x are
+            // filled by 2-D tensor copies (rows past M read as zero), kNB
+            // units ahead.
+            const int bw = warp - kBldWarp0;
+            const int mlo = 8 * bw, mhi = min(M, mlo + 8);
+            uint64_t* xf = xfull + kNB * bw;
+            uint8_t* xs0 = xring + static_cast<size_t>(bw) * kNB * kXSlot;
+            auto load_x = [&](int slot, int sb) {
+                mbar_arrive_expect_tx(&xf[slot], kXSlot);
+                tma_load_2d(xs0 + slot * kXSlot, &mapx, sb * 256, mlo, &xf[slot]);
+            };
+            if (lane == 0 && mlo < M) {
+                UnitIter<QT> ahead(u0, nsb);
+                for (int j = 0; j < kNB && j < nunits; ++j, ahead.next()) load_x(j, ahead.sb);
+            }
+            UnitIter<QT> it(u0, nsb), ahead(u0, nsb);
+            for (int j = 0; j < kNB; ++j) ahead.next();
+            Ring rb, rd;
+            for (int i = 0; i < nunits; ++i, it.next(), ahead.next(), rb.next(kNB), rd.next(kND)) {
+                if (ok && i >= kNB) ok = mbar_wait_bounded(&bempty[rb.slot], rb.phase ^ 1u, p.status, kDevStatusWaitTimeout);
+                if (ok && i >= kND) ok = mbar_wait_bounded(&dempty[rd.slot], rd.phase ^ 1u, p.status, kDevStatusWaitTimeout);
+                if (ok && mlo < M) ok = mbar_wait_bounded(&xf[rb.slot], rb.phase, p.status, kDevStatusWaitTimeout);
+                uint8_t* slab = B + kSlab * rb.slot;
+                float* xu = xr + kXr * rd.slot;
+                const float* xs = reinterpret_cast<const float*>(xs0 + rb.slot * kXSlot);
+                for (int m = mlo; m < mhi && ok; ++m) {
+                    const BlockX<QT> bx = block_x<QT, true>(xs + (m - mlo) * 256, lane);
+                    // rows 2m (hi) and 2m + 1 (lo) of the slab's N-group m / 4
+                    const uint32_t rowoff = (m >> 2) * 128 + (2 * m & 7) * 16;
+                    if constexpr (QT == MUSER_Q4_K) {
+                        const int c = lane >> 3, t = lane & 7;
+                        uint8_t* ch = slab + (8 * c + t) * 512 + rowoff;
+                        *reinterpret_cast<uint4*>(ch) = bx.hi0;
+                        *reinterpret_cast<uint4*>(ch + 16) = bx.lo0;
+                        if (t == 0) {
+                            xu[8 * m + 2 * c] = bx.sa;
+                            xu[8 * m + 2 * c + 1] = bx.sb;
+                        }
+                    } else if (lane < 16) {
+                        const int h = lane >> 3, ii = lane & 7;
+                        uint8_t* ch = slab + (16 * h + 2 * ii) * 512 + rowoff;
+                        *reinterpret_cast<uint4*>(ch) = bx.hi0;
+                        *reinterpret_cast<uint4*>(ch + 16) = bx.lo0;
+                        *reinterpret_cast<uint4*>(ch + 512) = bx.hi1;
+                        *reinterpret_cast<uint4*>(ch + 512 + 16) = bx.lo1;
+                    }
+                    if (lane == 0) xu[8 * MB + m] = bx.esc;
+                }
+                fence_proxy_async_smem();  // slab for the MMA; x slot for the next copy
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(&bfull[rb.slot]);
+                    mbar_arrive(&sfull[rd.slot]);
+                    if (mlo < M && i + kNB < nunits) load_x(rb.slot, ahead.sb);
+                }
+            }
+        } else if (warp >= kRbWarp0 && warp < kRbWarp0 + 4) {
             // ------------------------------ readback and epilogue warps
             const int q = warp & 3;
             const int l = 32 * q + lane;
             const uint32_t tq = tmem + (static_cast<uint32_t>(32 * q) << 16);
-            float yacc = 0.0f;
+            float yacc[MB];
+#pragma unroll
+            for (int m = 0; m < MB; ++m) yacc[m] = 0.0f;
             UnitIter<QT> it(u0, nsb);
             Ring rd;
             for (int i = 0; i < nunits; ++i, it.next(), rd.next(kND)) {
                 const int db = rd.slot;
                 if (ok) ok = mbar_wait_bounded(&dfull[db], rd.phase, p.status, kDevStatusWaitTimeout);
                 if (ok) ok = mbar_wait_bounded(&sfull[db], rd.phase, p.status, kDevStatusWaitTimeout);
-                uint32_t r0 = 0, r1 = 0;
-                if (ok) {
-                    tc_fence_after();
-                    tmem_ld2(tq + kDCol0 + 16u * db, r0, r1);
-                    tc_wait_ld();
+                const float4 sc = scr[db * 128 + l];
+                if constexpr (MULTI) {
+                    uint32_t dv[32];
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) dv[j] = 0u;
+                    if (ok) {
+                        tc_fence_after();
+                        tmem_ld32(tq + kDCol0 + kDCols * db, dv);
+                        tc_wait_ld();
+                    }
+                    const float* xu = xr + kXr * db;
+                    float mins[8];
+                    if constexpr (QT == MUSER_Q4_K) {
+                        const uint32_t m03 = __float_as_uint(sc.z), m47 = __float_as_uint(sc.w);
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            mins[j] = static_cast<float>((m03 >> (8 * j)) & 0xFFu);
+                            mins[j + 4] = static_cast<float>((m47 >> (8 * j)) & 0xFFu);
+                        }
+                    }
+#pragma unroll
+                    for (int m = 0; m < MB; ++m) {
+                        if (m < M) {
+                            const float dd = __uint_as_float(dv[2 * m]) + __uint_as_float(dv[2 * m + 1]) * (1.0f / 2048.0f);
+                            float v = dd * (sc.x * xu[8 * MB + m]);
+                            if constexpr (QT == MUSER_Q4_K) {
+                                float s = 0.0f;
+#pragma unroll
+                                for (int j = 0; j < 8; ++j) s = fmaf(mins[j], xu[8 * m + j], s);
+                                v = fmaf(-sc.y, s, v);
+                            }
+                            yacc[m] += v;
+                        }
+                    }
+                } else {
+                    uint32_t r0 = 0, r1 = 0;
+                    if (ok) {
+                        tc_fence_after();
+                        tmem_ld2(tq + kDCol0 + kDCols * db, r0, r1);
+                        tc_wait_ld();
+                    }
+                    yacc[0] += fmaf(__uint_as_float(r0) + __uint_as_float(r1) * (1.0f / 2048.0f), sc.x, -sc.y);
                 }
-                const float2 sc = scr[db * 128 + l];
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&dempty[db]);
-                yacc += fmaf(__uint_as_float(r0) + __uint_as_float(r1) * (1.0f / 2048.0f), sc.x, -sc.y);
                 const int t = it.t;
                 if (it.k != nsb - 1 && i != nunits - 1) continue;
                 // ---- the tile's last unit in this CTA
@@ -680,13 +865,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                     c0 = cta_of(static_cast<int64_t>(t) * nsb, U, G);
                     c1 = cta_of(static_cast<int64_t>(t + 1) * nsb - 1, U, G);
                 }
-                float val = yacc;
-                yacc = 0.0f;
+                float val[MB];
+#pragma unroll
+                for (int m = 0; m < MB; ++m) {
+                    val[m] = yacc[m];
+                    yacc[m] = 0.0f;
+                }
                 if (c1 > c0) {
-                    // Tile t's part from CTA c sits in slot t + c: CTAs take the
-                    // units in order, so no two (tile, CTA) pairs share a slot.
-                    float* slot = p.part + static_cast<size_t>(t + c0) * 128;
-                    slot[(blockIdx.x - c0) * 128 + l] = val;
+                    // Tile t's part from CTA c sits in slot t + c (MB x 128 floats):
+                    // CTAs take the units in order, so no two (tile, CTA) pairs share a slot.
+                    float* own = p.part + static_cast<size_t>(t + blockIdx.x) * MB * 128;
+#pragma unroll
+                    for (int m = 0; m < MB; ++m)
+                        if (m < M) own[m * 128 + l] = val[m];
                     __threadfence();
                     named_sync(kBarReadback, 128);
                     if (l == 0) flags[1] = (atomicAdd(&p.tick[t], 1u) == static_cast<unsigned>(c1 - c0)) ? 1 : 0;
@@ -695,22 +886,37 @@ __global__ void __launch_bounds__(kThreads, 1)
                     named_sync(kBarReadback, 128);
                     if (!last) continue;
                     __threadfence();
-                    val = 0.0f;
+#pragma unroll
+                    for (int m = 0; m < MB; ++m) val[m] = 0.0f;
                     for (int pp = 0; pp <= c1 - c0; ++pp) {
-                        val += __ldcg(slot + pp * 128 + l);
-                        slot[pp * 128 + l] = 0.0f;  // leave the scratch zeroed
+                        float* slot = p.part + static_cast<size_t>(t + c0 + pp) * MB * 128;
+#pragma unroll
+                        for (int m = 0; m < MB; ++m)
+                            if (m < M) {
+                                val[m] += __ldcg(slot + m * 128 + l);
+                                slot[m * 128 + l] = 0.0f;  // leave the scratch zeroed
+                            }
                     }
                     if (l == 0) p.tick[t] = 0u;
                 }
                 int mat;
                 const int64_t row = tm.row(t, l, mat);
                 if constexpr (EPI == kEpiSiluMul) {
-                    xch[l] = val;
+#pragma unroll
+                    for (int m = 0; m < MB; ++m)
+                        if (m < M) xch[m * 128 + l] = val[m];
                     named_sync(kBarReadback, 128);
-                    if (l < 64 && row < p.rows) p.y[row] = silu_mul_f(xch[l], xch[l + 64]);
+                    if (l < 64 && row < p.rows) {
+                        for (int m = 0; m < M; ++m)
+                            p.y[static_cast<int64_t>(m) * p.rows + row] = silu_mul_f(xch[m * 128 + l], xch[m * 128 + l + 64]);
+                    }
                     named_sync(kBarReadback, 128);
                 } else {
-                    if (row < p.rows) p.y[row] = val;
+                    if (row < p.rows) {
+#pragma unroll
+                        for (int m = 0; m < MB; ++m)
+                            if (m < M) p.y[static_cast<int64_t>(m) * p.rows + row] = val[m];
+                    }
                     if constexpr (EPI == kEpiTail) {
                         __threadfence();
                         named_sync(kBarReadback, 128);
@@ -727,7 +933,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
     }
-    if constexpr (EPI == kEpiTail) {
+    if constexpr (EPI == kEpiTail && !MULTI) {
         if (ok && flags[0]) {
             __threadfence();
             block_dual_tail_row(p.resid, p.y, p.out, p.w1, p.w2, static_cast<int>(p.rows), p.eps1, p.eps2, red);
@@ -745,7 +951,7 @@ constexpr int kMaxGrid = 256;  // bound on the grid, so scratch sizes need no de
 
 struct MvtGeo {
     int P = 1, ntiles = 0, grid = 0, maxparts = 1, ns = 0, tiles_per_cta = 0;
-    uint32_t x_off = 0, b_off = 0, stage_off = 0, smem = 0;
+    uint32_t x_off = 0, b_off = 0, stage_off = 0, xch_off = 0, smem = 0;
 };
 
 int gcd_int(int64_t a, int64_t b) {
@@ -757,19 +963,23 @@ int gcd_int(int64_t a, int64_t b) {
     return static_cast<int>(a);
 }
 
+int tile_count(int nmat, int64_t rows, int P) {
+    return nmat == 2 ? static_cast<int>((rows + 63) / 64) : static_cast<int>(P * ((rows + 128 * P - 1) / (128 * P)));
+}
+
 // Geometry of one launch; false if the shape does not fit this kernel.
-bool mvt_geometry(int qtype, int nmat, int64_t rows, int64_t cols, MvtGeo& g, bool whole_tiles = false) {
+bool mvt_geometry(int qtype, int nmat, int64_t rows, int64_t cols, int M, MvtGeo& g, bool whole_tiles) {
     if (qtype != MUSER_Q4_K && qtype != MUSER_Q6_K) return false;
     if (nmat == 2 && qtype != MUSER_Q4_K) return false;
-    if (cols % kQK != 0 || rows < 1) return false;
+    if (cols % kQK != 0 || rows < 1 || M < 1 || M > 16) return false;
+    const bool multi = M > 1;
     const int64_t nsb = cols / kQK;
     const int blk = qtype == MUSER_Q4_K ? kQ4KBytes : kQ6KBytes;
     const int64_t rowbytes = nsb * blk;
     if ((rows * rowbytes) % 16 != 0) return false;  // 16-byte copies never pass the matrix end
     g.P = nmat == 2 ? 1 : 16 / gcd_int(rowbytes, 16);
     if (rows % g.P != 0) return false;  // the class view of the matrix must be exact
-    if (nmat == 2) g.ntiles = static_cast<int>((rows + 63) / 64);
-    else g.ntiles = static_cast<int>(g.P * ((rows + 128 * g.P - 1) / (128 * g.P)));
+    g.ntiles = tile_count(nmat, rows, g.P);
     const int sms = std::min(sm_count(), kMaxGrid);
     if (sms <= 0) return false;
     const int64_t U = static_cast<int64_t>(g.ntiles) * nsb;
@@ -785,12 +995,17 @@ bool mvt_geometry(int qtype, int nmat, int64_t rows, int64_t cols, MvtGeo& g, bo
             g.maxparts = std::max(g.maxparts, cta_of_h(static_cast<int64_t>(t + 1) * nsb - 1) -
                                                   cta_of_h(static_cast<int64_t>(t) * nsb) + 1);
     }
-    // barriers, TMEM address, flags (0..511), red (512..767), xch (768..1279),
-    // scale ring (1280..1280 + kND * 128 * 8)
-    g.x_off = 1280 + kND * 128 * 8;
-    const uint32_t xbytes = static_cast<uint32_t>(((nsb + 3) & ~3) * 4 + (qtype == MUSER_Q4_K ? nsb * 8 * 4 : 0));
+    // barriers, TMEM address, flags (0..511), red (512..767), scale ring
+    // (1280 + kND * 128 * 16), tile exchange, x scales and sums, B, stages
+    const int MB = multi ? 16 : 1;
+    g.xch_off = 1280 + kND * 128 * 16;
+    g.x_off = g.xch_off + MB * 128 * 4;
+    const uint32_t xbytes = multi ? static_cast<uint32_t>(kND * (MB * 8 + MB) * 4)
+                                  : static_cast<uint32_t>(((nsb + 3) & ~3) * 4 + (qtype == MUSER_Q4_K ? nsb * 8 * 4 : 0));
     g.b_off = (g.x_off + xbytes + 127) / 128 * 128;
-    const uint32_t bbytes = static_cast<uint32_t>(nsb * 1024 + 512);
+    // several rows: kNB B slabs, then two builder warps' kNB slots of 8 rows of x
+    const uint32_t bbytes = multi ? static_cast<uint32_t>(kNB * 16384 + 2 * kNB * 8192)
+                                  : static_cast<uint32_t>(nsb * 1024 + 512);
     g.stage_off = (g.b_off + bbytes + 1023) / 1024 * 1024;
     const uint32_t stage = 128u * (qtype == MUSER_Q4_K ? 144u : 240u);
     const int64_t budget = max_smem_optin();
@@ -832,7 +1047,23 @@ int encode_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
     return MUSER_OK;
 }
 
-template <int QT, int EPI>
+// A row-major binary32 matrix of `outer` rows of `inner` elements.
+int encode_map_f32(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t stride_bytes,
+                   uint32_t box_x, uint32_t box_y) {
+    auto fn = encode_fn();
+    if (fn == nullptr) return set_error(MUSER_ERR_CUDA, "mvt: cuTensorMapEncodeTiled is not available");
+    const cuuint64_t dims[2] = {inner, outer};
+    const cuuint64_t strides[1] = {stride_bytes};
+    const cuuint32_t box[2] = {box_x, box_y};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return set_error(MUSER_ERR_CUDA, "mvt: cuTensorMapEncodeTiled (x) failed (%d)", static_cast<int>(r));
+    return MUSER_OK;
+}
+
+template <int QT, int EPI, bool MULTI>
 int launch_mvt_t(MvtArgs a, const MvtGeo& g, cudaStream_t stream) {
     constexpr int NMAT = (EPI == kEpiSiluMul) ? 2 : 1;
     const uint64_t rowbytes = static_cast<uint64_t>(a.nsb) * (QT == MUSER_Q4_K ? kQ4KBytes : kQ6KBytes);
@@ -847,12 +1078,18 @@ int launch_mvt_t(MvtArgs a, const MvtGeo& g, cudaStream_t stream) {
         MUSER_TRY(encode_map(&m0, a.W[0], P * rowbytes, rows / P, P * rowbytes, 240u, 128u));
         m1 = m0;
     }
-    auto kern = mvt_kernel<QT, EPI>;
+    CUtensorMap mx = m0;
+    if constexpr (MULTI) {
+        // x as M rows of K floats, copied in boxes of one block x eight rows
+        const uint64_t K = static_cast<uint64_t>(a.nsb) * kQK;
+        MUSER_TRY(encode_map_f32(&mx, a.x, K, static_cast<uint64_t>(a.M), K * 4, 256u, 8u));
+    }
+    auto kern = mvt_kernel<QT, EPI, MULTI>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(g.smem));
     if (e != cudaSuccess) return cuda_fail(e, "mvt: cudaFuncSetAttribute");
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(g.grid);
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(mvt_threads(MULTI));
     cfg.dynamicSmemBytes = g.smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
@@ -860,41 +1097,43 @@ int launch_mvt_t(MvtArgs a, const MvtGeo& g, cudaStream_t stream) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, kern, a, m0, m1);
+    e = cudaLaunchKernelEx(&cfg, kern, a, m0, m1, mx);
     if (e != cudaSuccess) return cuda_fail(e, "mvt: cudaLaunchKernelEx");
     return check_launch("mvt_kernel");
 }
 
 }  // namespace
 
-bool mvt_supported(int qtype, int nmat, int64_t rows, int64_t cols) {
+bool mvt_supported(int qtype, int nmat, int64_t rows, int64_t cols, int M) {
     MvtGeo g;
-    return mvt_geometry(qtype, nmat, rows, cols, g, true);
+    return mvt_geometry(qtype, nmat, rows, cols, M, g, true);
 }
 
 // Scratch of the even split: per-tile tickets and the tail counter, then
-// ntiles + grid - 1 partial slots of 128 floats.  Depends only on the tile
-// count and the grid bound, not on the device.
-size_t mvt_scratch_bytes(int qtype, int nmat, int64_t rows, int64_t cols) {
+// ntiles + grid - 1 partial slots of 128 floats per row of x.  Depends only
+// on the tile count and the grid bound, not on the device.
+size_t mvt_scratch_bytes(int qtype, int nmat, int64_t rows, int64_t cols, int M) {
     if (qtype != MUSER_Q4_K && qtype != MUSER_Q6_K) return 0;
-    if (cols % kQK != 0 || rows < 1) return 0;
+    if (cols % kQK != 0 || rows < 1 || M < 1 || M > 16) return 0;
     const int64_t rowbytes = (cols / kQK) * (qtype == MUSER_Q4_K ? kQ4KBytes : kQ6KBytes);
     const int P = nmat == 2 ? 1 : 16 / gcd_int(rowbytes, 16);
-    const int64_t ntiles = nmat == 2 ? (rows + 63) / 64 : P * ((rows + 128 * P - 1) / (128 * P));
+    const int64_t ntiles = tile_count(nmat, rows, P);
     const size_t ticks = (static_cast<size_t>(ntiles) + 1) * sizeof(unsigned);
-    return (ticks + 255) / 256 * 256 + static_cast<size_t>(ntiles + kMaxGrid) * 128 * sizeof(float);
+    const int MB = M > 1 ? 16 : 1;
+    return (ticks + 255) / 256 * 256 + static_cast<size_t>(ntiles + kMaxGrid) * MB * 128 * sizeof(float);
 }
 
 // scratch == nullptr: whole tiles per CTA (no partial sums).  Otherwise the
 // even split, with `scratch` of mvt_scratch_bytes(), zero-filled, left zeroed.
+// The tail epilogue is for one row of x and needs scratch.
 int launch_mvt(int qtype, int epi, MvtArgs a, void* scratch, cudaStream_t s) {
     const int nmat = epi == kEpiSiluMul ? 2 : 1;
     const int64_t cols = static_cast<int64_t>(a.nsb) * kQK;
     MvtGeo g;
-    if (!mvt_geometry(qtype, nmat, a.rows, cols, g, scratch == nullptr))
+    if (!mvt_geometry(qtype, nmat, a.rows, cols, a.M, g, scratch == nullptr))
         return set_error(MUSER_ERR_UNSUPPORTED, "mvt: shape not supported");
-    if (epi == kEpiTail && scratch == nullptr)
-        return set_error(MUSER_ERR_UNSUPPORTED, "mvt: the tail epilogue needs scratch");
+    if (epi == kEpiTail && (scratch == nullptr || a.M != 1))
+        return set_error(MUSER_ERR_UNSUPPORTED, "mvt: the tail epilogue needs scratch and one row of x");
     a.ntiles = g.ntiles;
     a.P = g.P;
     a.maxparts = g.maxparts;
@@ -903,6 +1142,7 @@ int launch_mvt(int qtype, int epi, MvtArgs a, void* scratch, cudaStream_t s) {
     a.x_off = g.x_off;
     a.b_off = g.b_off;
     a.stage_off = g.stage_off;
+    a.xch_off = g.xch_off;
     if (scratch != nullptr) {
         const size_t ticks = (static_cast<size_t>(g.ntiles) + 1) * sizeof(unsigned);
         a.tick = static_cast<unsigned*>(scratch);
@@ -910,13 +1150,17 @@ int launch_mvt(int qtype, int epi, MvtArgs a, void* scratch, cudaStream_t s) {
     }
     if (a.status == nullptr) a.status = device_status_word();
     if (a.status == nullptr) return set_error(MUSER_ERR_CUDA, "mvt: no device status word");
+    const bool multi = a.M > 1;
     if (qtype == MUSER_Q4_K) {
-        if (epi == kEpiSiluMul) return launch_mvt_t<MUSER_Q4_K, kEpiSiluMul>(a, g, s);
-        if (epi == kEpiStore) return launch_mvt_t<MUSER_Q4_K, kEpiStore>(a, g, s);
-        if (epi == kEpiTail) return launch_mvt_t<MUSER_Q4_K, kEpiTail>(a, g, s);
+        if (epi == kEpiSiluMul)
+            return multi ? launch_mvt_t<MUSER_Q4_K, kEpiSiluMul, true>(a, g, s) : launch_mvt_t<MUSER_Q4_K, kEpiSiluMul, false>(a, g, s);
+        if (epi == kEpiStore)
+            return multi ? launch_mvt_t<MUSER_Q4_K, kEpiStore, true>(a, g, s) : launch_mvt_t<MUSER_Q4_K, kEpiStore, false>(a, g, s);
+        if (epi == kEpiTail) return launch_mvt_t<MUSER_Q4_K, kEpiTail, false>(a, g, s);
     } else {
-        if (epi == kEpiStore) return launch_mvt_t<MUSER_Q6_K, kEpiStore>(a, g, s);
-        if (epi == kEpiTail) return launch_mvt_t<MUSER_Q6_K, kEpiTail>(a, g, s);
+        if (epi == kEpiStore)
+            return multi ? launch_mvt_t<MUSER_Q6_K, kEpiStore, true>(a, g, s) : launch_mvt_t<MUSER_Q6_K, kEpiStore, false>(a, g, s);
+        if (epi == kEpiTail) return launch_mvt_t<MUSER_Q6_K, kEpiTail, false>(a, g, s);
     }
     return set_error(MUSER_ERR_UNSUPPORTED, "mvt: no kernel for qtype %d epilogue %d", qtype, epi);
 }

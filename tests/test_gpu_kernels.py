@@ -182,10 +182,10 @@ def test_tail_zero_projection_keeps_residual_bit_exact():
 
 
 @pytest.mark.parametrize("qtype", ["q4_k", "q6_k"])
-@pytest.mark.parametrize("M,small_scratch", [(1, False), (1, True), (16, False)])
+@pytest.mark.parametrize("M,small_scratch", [(1, False), (1, True), (3, False), (16, False)])
 def test_down_projection_with_fused_tail(qtype, M, small_scratch):
-    """M = 1 with full scratch runs the tensor-core kernel (tiles split over
-    all SMs); with the 256-byte minimum it runs the CUDA-core kernel."""
+    """M > 1 with full scratch runs the tensor-core kernel (tiles split over
+    all SMs); M = 1, or the 256-byte minimum, the CUDA-core kernels."""
     hidden, ffn = 6656, 19968 if M == 1 else 2048
     case = synth.down_tail_case(qtype, hidden, ffn, M, seed=5)
     a, b = case["a"], case["b"]

@@ -123,6 +123,34 @@ def _stack(n_layers, M, rows_checked, seed=0):
     return got_r[rows_checked], got_o[rows_checked], r_ref, x_ref
 
 
+@pytest.mark.parametrize("M", [3, 16])
+def test_small_stack_several_rows(M):
+    """Two layers at hidden 512, ffn 1280 through muser_ffn_stack: partial
+    gate/up tiles split over CTAs, Q6_K down rows of 5 blocks (1050 bytes, the
+    worst row alignment), several rows of x."""
+    hidden, ffn, wl = 512, 1280, 3
+    w_in0 = synth.input_norm_weight(0, hidden, seed=7, workload=wl)
+    r = synth.residual_rows(M, hidden, seed=7, workload=wl)
+    x_ref, r_ref = oracle.rms_norm(r, w_in0, 1e-5), r.copy()
+    keep, structs = [], []
+    for l in range(2):
+        L = synth.ffn_layer(l, hidden, ffn, seed=7, workload=wl)
+        w_next = synth.input_norm_weight(l + 1, hidden, seed=7, workload=wl)
+        d = _layer_dev(L, w_next)
+        keep.append(d)
+        structs.append(_ffn_layer_struct(d))
+        r_ref, x_ref, _, _ = oracle.ffn_layer(x_ref, r_ref, L, w_next, hidden, ffn)
+    ws_bytes = mu.muser_ffn_workspace_bytes(hidden, ffn, M)
+    ws = torch.zeros(ws_bytes // 4, dtype=torch.float32, device="cuda")
+    resid, out = dev(r), nan_like((M, hidden))
+    mu.muser_ffn_stack(structs, dev(w_in0), hidden, ffn, M, resid, out, 1e-5, 1e-8, ws, ws_bytes)
+    assert_close(host(resid).reshape(M, hidden), r_ref, f"2-layer residual M={M}")
+    assert_close(host(out).reshape(M, hidden), x_ref, f"2-layer output M={M}")
+    assert not host(ws).reshape(-1)[-(mu.muser_scratch_bytes(hidden, M) // 4):].any(), "scratch left zeroed"
+    assert mu.muser_device_status() == 0
+    del keep
+
+
 def test_workload4_stack_slice_all_rows():
     rows = np.arange(16)
     gr, go, rr, orf = _stack(3, 16, rows)
