@@ -394,18 +394,21 @@ struct TileMap {
     }
 };
 
-// Splits v into binary16 hi and lo with v = hi + lo * 2^-11 (to binary16 precision).
-__device__ __forceinline__ void split_hl(float v, uint32_t& hi, uint32_t& lo) {
-    const __half h = __float2half_rn(v);
-    hi = __half_as_ushort(h);
-    lo = __half_as_ushort(__float2half_rn((v - __half2float(h)) * 2048.0f));
+// Splits a pair of scaled values (|a| < 2^15) into binary16 hi and lo with
+// a = hi + lo * 2^-11: hi is a rounded to a multiple of 16 (the 1.5 * 2^27
+// add/subtract rounds at that grid), exact in binary16; lo = (a - hi) * 2^11,
+// |lo| <= 2^14, rounded once.  The error is at most 2^-8 in units of a, that
+// is 2^-22 of the block maximum.
+__device__ __forceinline__ void pack_hl(float2 a, uint32_t& hi, uint32_t& lo) {
+    const float2 c = make_float2(201326592.0f, 201326592.0f);
+    const float2 h = __fadd2_rn(__fadd2_rn(a, c), make_float2(-c.x, -c.y));
+    const float2 r = __fmul2_rn(__fadd2_rn(a, make_float2(-h.x, -h.y)), make_float2(2048.0f, 2048.0f));
+    const __half2 hh = __float22half2_rn(h), hl = __float22half2_rn(r);
+    hi = *reinterpret_cast<const uint32_t*>(&hh);
+    lo = *reinterpret_cast<const uint32_t*>(&hl);
 }
 __device__ __forceinline__ void pack_hl(float a, float b, uint32_t& hi, uint32_t& lo) {
-    uint32_t ha, la, hb, lb;
-    split_hl(a, ha, la);
-    split_hl(b, hb, lb);
-    hi = ha | (hb << 16);
-    lo = la | (lb << 16);
+    pack_hl(make_float2(a, b), hi, lo);
 }
 // Exponent E with max|x| < 2^E, kept in a range where both 2^(15-E) and
 // 2^(E-15) are finite normal floats.
@@ -484,6 +487,87 @@ __device__ __forceinline__ BlockX<QT> block_x(const float* xb, int lane) {
     return r;
 }
 
+// Several rows of x: lane (m, q) of a builder warp converts a quarter of
+// row m's block (64 values) straight into the B slab.  The quarter is the
+// set of 16-byte x chunks j with j = q mod 4, which keeps the shared-memory
+// reads of a warp at most 2-way conflicted; the row's block maximum and the
+// Q4_K sub-block sums need only the 4 lanes of the row.  Returns 2^e, the
+// row's block scale; the sums of sub-blocks 0..7 are valid in lane q == 0.
+template <int QT>
+__device__ __forceinline__ float build_row_quarter(const float* xrow, int q, uint8_t* slab, uint32_t rowoff,
+                                                   float* xsum8) {
+    float4 v[16];
+    if constexpr (QT == MUSER_Q4_K) {
+        // B chunk 8c + t (t = q, q + 4): x chunks 16c + t and 16c + 8 + t
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int t = q + 4 * h;
+                v[4 * c + 2 * h] = *reinterpret_cast<const float4*>(xrow + 64 * c + 4 * t);
+                v[4 * c + 2 * h + 1] = *reinterpret_cast<const float4*>(xrow + 64 * c + 32 + 4 * t);
+            }
+    } else {
+        // item (h, i), i = q + 4e: x chunks 32h + 8g + i, g = 0..3
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+            for (int e = 0; e < 2; ++e)
+#pragma unroll
+                for (int g = 0; g < 4; ++g)
+                    v[8 * h + 4 * e + g] = *reinterpret_cast<const float4*>(xrow + 128 * h + 32 * g + 4 * (q + 4 * e));
+    }
+    float mx = 0.0f;
+#pragma unroll
+    for (int k = 0; k < 16; ++k)
+        mx = fmaxf(mx, fmaxf(fmaxf(fabsf(v[k].x), fabsf(v[k].y)), fmaxf(fabsf(v[k].z), fabsf(v[k].w))));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+    const int E = scale_exp(mx);
+    const float dn = ldexpf(1.0f, 15 - E);
+    auto store = [&](int chunk, const float4& a, const float4& b) {
+        // columns (a.x,a.z) (a.y,a.w) (b.x,b.z) (b.y,b.w) of the chunk
+        uint4 hi, lo;
+        const float2 d2 = make_float2(dn, dn);
+        pack_hl(__fmul2_rn(make_float2(a.x, a.z), d2), hi.x, lo.x);
+        pack_hl(__fmul2_rn(make_float2(a.y, a.w), d2), hi.y, lo.y);
+        pack_hl(__fmul2_rn(make_float2(b.x, b.z), d2), hi.z, lo.z);
+        pack_hl(__fmul2_rn(make_float2(b.y, b.w), d2), hi.w, lo.w);
+        uint8_t* ch = slab + chunk * 512 + rowoff;
+        *reinterpret_cast<uint4*>(ch) = hi;
+        *reinterpret_cast<uint4*>(ch + 16) = lo;
+    };
+    if constexpr (QT == MUSER_Q4_K) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            float sa = 0.0f, sb = 0.0f;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const float4 a = v[4 * c + 2 * h], b = v[4 * c + 2 * h + 1];
+                store(8 * c + q + 4 * h, a, b);
+                sa += (a.x + a.y) + (a.z + a.w);
+                sb += (b.x + b.y) + (b.z + b.w);
+            }
+            sa += __shfl_xor_sync(0xffffffffu, sa, 1);
+            sa += __shfl_xor_sync(0xffffffffu, sa, 2);
+            sb += __shfl_xor_sync(0xffffffffu, sb, 1);
+            sb += __shfl_xor_sync(0xffffffffu, sb, 2);
+            xsum8[2 * c] = sa;
+            xsum8[2 * c + 1] = sb;
+        }
+    } else {
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int i = q + 4 * e;
+                store(16 * h + 2 * i, v[8 * h + 4 * e], v[8 * h + 4 * e + 1]);
+                store(16 * h + 2 * i + 1, v[8 * h + 4 * e + 2], v[8 * h + 4 * e + 3]);
+            }
+    }
+    return ldexpf(1.0f, E - 15);
+}
+
 template <int QT, int EPI, bool MULTI>
 __global__ void __launch_bounds__(mvt_threads(MULTI), 1)
     mvt_kernel(const MvtArgs p, const __grid_constant__ CUtensorMap map0, const __grid_constant__ CUtensorMap map1,
@@ -501,7 +585,6 @@ __global__ void __launch_bounds__(mvt_threads(MULTI), 1)
     constexpr int kXr = MB * 8 + MB;                     // per-unit x sums (Q4_K) and scales, floats
     extern __shared__ __align__(1024) uint8_t smem[];
     const int nsb = p.nsb;
-    const int K = nsb * 256;
     const int M = MULTI ? p.M : 1;
     const int64_t rowbytes = static_cast<int64_t>(nsb) * kBlk;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -766,28 +849,19 @@ __global__ void __launch_bounds__(mvt_threads(MULTI), 1)
                 uint8_t* slab = B + kSlab * rb.slot;
                 float* xu = xr + kXr * rd.slot;
                 const float* xs = reinterpret_cast<const float*>(xs0 + rb.slot * kXSlot);
-                for (int m = mlo; m < mhi && ok; ++m) {
-                    const BlockX<QT> bx = block_x<QT, true>(xs + (m - mlo) * 256, lane);
-                    // rows 2m (hi) and 2m + 1 (lo) of the slab's N-group m / 4
-                    const uint32_t rowoff = (m >> 2) * 128 + (2 * m & 7) * 16;
-                    if constexpr (QT == MUSER_Q4_K) {
-                        const int c = lane >> 3, t = lane & 7;
-                        uint8_t* ch = slab + (8 * c + t) * 512 + rowoff;
-                        *reinterpret_cast<uint4*>(ch) = bx.hi0;
-                        *reinterpret_cast<uint4*>(ch + 16) = bx.lo0;
-                        if (t == 0) {
-                            xu[8 * m + 2 * c] = bx.sa;
-                            xu[8 * m + 2 * c + 1] = bx.sb;
+                if (ok && mlo < M) {
+                    // lane (m, q): row m = mlo + lane / 4, quarter q = lane % 4
+                    const int ml = lane >> 2, q = lane & 3, m = mlo + ml;
+                    float xs8[8];
+                    const float e2 = build_row_quarter<QT>(xs + ml * 256, q, slab,
+                                                           (m >> 2) * 128 + (2 * m & 7) * 16, xs8);
+                    if (m < mhi && q == 0) {
+                        xu[8 * MB + m] = e2;
+                        if constexpr (QT == MUSER_Q4_K) {
+                            *reinterpret_cast<float4*>(xu + 8 * m) = make_float4(xs8[0], xs8[1], xs8[2], xs8[3]);
+                            *reinterpret_cast<float4*>(xu + 8 * m + 4) = make_float4(xs8[4], xs8[5], xs8[6], xs8[7]);
                         }
-                    } else if (lane < 16) {
-                        const int h = lane >> 3, ii = lane & 7;
-                        uint8_t* ch = slab + (16 * h + 2 * ii) * 512 + rowoff;
-                        *reinterpret_cast<uint4*>(ch) = bx.hi0;
-                        *reinterpret_cast<uint4*>(ch + 16) = bx.lo0;
-                        *reinterpret_cast<uint4*>(ch + 512) = bx.hi1;
-                        *reinterpret_cast<uint4*>(ch + 512 + 16) = bx.lo1;
                     }
-                    if (lane == 0) xu[8 * MB + m] = bx.esc;
                 }
                 fence_proxy_async_smem();  // slab for the MMA; x slot for the next copy
                 __syncwarp();
@@ -832,17 +906,29 @@ __global__ void __launch_bounds__(mvt_threads(MULTI), 1)
                         }
                     }
 #pragma unroll
-                    for (int m = 0; m < MB; ++m) {
-                        if (m < M) {
-                            const float dd = __uint_as_float(dv[2 * m]) + __uint_as_float(dv[2 * m + 1]) * (1.0f / 2048.0f);
-                            float v = dd * (sc.x * xu[8 * MB + m]);
-                            if constexpr (QT == MUSER_Q4_K) {
-                                float s = 0.0f;
+                    for (int m4 = 0; m4 < MB; m4 += 4) {
+                        if (m4 >= M) break;
+                        const float4 e4 = *reinterpret_cast<const float4*>(xu + 8 * MB + m4);
+                        const float ev[4] = {e4.x, e4.y, e4.z, e4.w};
 #pragma unroll
-                                for (int j = 0; j < 8; ++j) s = fmaf(mins[j], xu[8 * m + j], s);
+                        for (int mm = 0; mm < 4; ++mm) {
+                            const int m = m4 + mm;
+                            const float dd = __uint_as_float(dv[2 * m]) + __uint_as_float(dv[2 * m + 1]) * (1.0f / 2048.0f);
+                            float v = dd * (sc.x * ev[mm]);
+                            if constexpr (QT == MUSER_Q4_K) {
+                                const float4 xa = *reinterpret_cast<const float4*>(xu + 8 * m);
+                                const float4 xb = *reinterpret_cast<const float4*>(xu + 8 * m + 4);
+                                float s = mins[0] * xa.x;
+                                s = fmaf(mins[1], xa.y, s);
+                                s = fmaf(mins[2], xa.z, s);
+                                s = fmaf(mins[3], xa.w, s);
+                                s = fmaf(mins[4], xb.x, s);
+                                s = fmaf(mins[5], xb.y, s);
+                                s = fmaf(mins[6], xb.z, s);
+                                s = fmaf(mins[7], xb.w, s);
                                 v = fmaf(-sc.y, s, v);
                             }
-                            yacc[m] += v;
+                            yacc[m] += v;  // rows m >= M stay zero-weighted and are never stored
                         }
                     }
                 } else {
