@@ -232,15 +232,6 @@ __device__ __forceinline__ void q4k_block_dmins(const uint8_t* blk, float& d, fl
 // Group g takes the low (g < 2) or high (g >= 2) nibble of ql[64h + 32(g&1) + l]
 // and qh[32h + l] bits 2g, 2g+1 (Ch 19 §19.3).
 
-// Word at byte offset lb (even) of the register copy w[] of a row buffer's
-// 16-byte blocks.  All offsets are compile-time constants once the callers'
-// loops are unrolled, so w[] stays in registers; odd halves are stitched
-// with a funnel shift.
-__device__ __forceinline__ uint32_t word_at(const uint32_t* w, int lb) {
-    if ((lb & 3) == 0) return w[lb >> 2];
-    return __funnelshift_r(w[lb >> 2], w[(lb >> 2) + 1], 16);
-}
-
 // Loads 16-byte blocks [B0, B1] of the row buffer into w[].
 template <int B0, int B1>
 __device__ __forceinline__ void load_blocks(const uint8_t* rb, uint32_t* w) {
@@ -254,21 +245,45 @@ __device__ __forceinline__ void load_blocks(const uint8_t* rb, uint32_t* w) {
     }
 }
 
-// Half H of the row's block starting DELTA bytes into the 16-byte aligned row
-// buffer `rb`, into TMEM columns [64H, +64) of this warp's lanes (taddr is the
-// A stage's first column).
-template <int DELTA, int H>
-__device__ __forceinline__ void q6k_dequant_half(const uint8_t* rb, uint32_t taddr) {
-    constexpr int QL = DELTA + 64 * H, QH = DELTA + 128 + 32 * H, SC = DELTA + 192 + 8 * H;
-    constexpr int LB0 = QL / 16, LB1 = (QL + 65) / 16;
-    constexpr int HB0 = QH / 16, HB1 = (QH + 33) / 16;
-    constexpr int SB0 = SC / 16, SB1 = (SC + 9) / 16;
-    uint32_t ws[4 * (SB1 - SB0 + 1)];
-    load_blocks<SB0, SB1>(rb, ws);
-    const uint32_t S0 = word_at(ws, SC - 16 * SB0), S1 = word_at(ws, SC + 4 - 16 * SB0);
-    uint32_t wl[4 * (LB1 - LB0 + 1)], wh[4 * (HB1 - HB0 + 1)];
-    load_blocks<LB0, LB1>(rb, wl);
-    load_blocks<HB0, HB1>(rb, wh);
+// Half H of the row's block starting `delta` bytes into the 16-byte aligned
+// row buffer `rb` (delta even, 0..14, the same for every lane of a unit),
+// into TMEM columns [64H, +64) of this warp's lanes (taddr is the A stage's
+// first column).  Sets d (the block's scale) for H == 0.  The fields' 16-byte
+// blocks are loaded at fixed offsets; a uniform switch moves the words by
+// delta / 4 and a uniform funnel shift handles the 2-byte remainder, so one
+// code body serves every misalignment.
+template <int H>
+__device__ __forceinline__ void q6k_dequant_half(const uint8_t* rb, int delta, uint32_t taddr, float& d) {
+    constexpr int QL = 64 * H, QH = 128 + 32 * H;
+    uint32_t wl[20], wh[12], ws[12];
+    load_blocks<QL / 16, QL / 16 + 4>(rb, wl);  // ql: bytes QL .. QL + 79
+    load_blocks<QH / 16, QH / 16 + 2>(rb, wh);  // qh: bytes QH .. QH + 47
+    load_blocks<12, 14>(rb, ws);                // scales and d: bytes 192 .. 239
+    uint32_t l[17], h[9], s[7];                 // words from delta (before the 2-byte shift)
+    auto take = [&](int k) {
+#pragma unroll
+        for (int i = 0; i < 17; ++i) l[i] = wl[i + k];
+#pragma unroll
+        for (int i = 0; i < 9; ++i) h[i] = wh[i + k];
+#pragma unroll
+        for (int i = 0; i < 7; ++i) s[i] = ws[i + k];  // s[0..3] scales, s[4..5] d
+    };
+    switch (delta >> 2) {
+        case 0: take(0); break;
+        case 1: take(1); break;
+        case 2: take(2); break;
+        default: take(3); break;
+    }
+    if (delta & 2) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) l[i] = __funnelshift_r(l[i], l[i + 1], 16);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) h[i] = __funnelshift_r(h[i], h[i + 1], 16);
+#pragma unroll
+        for (int i = 0; i < 6; ++i) s[i] = __funnelshift_r(s[i], s[i + 1], 16);
+    }
+    if (H == 0) d = h2f(s[4]);
+    const uint32_t S0 = s[2 * H], S1 = s[2 * H + 1];  // sc[8H .. 8H + 7]
 #pragma unroll
     for (int ci = 0; ci < 2; ++ci) {
         // words i = 4ci..4ci+3 use the scales sc[8H + 2g + ci], g = 0..3
@@ -285,9 +300,9 @@ __device__ __forceinline__ void q6k_dequant_half(const uint8_t* rb, uint32_t tad
 #pragma unroll
         for (int ii = 0; ii < 4; ++ii) {
             const int i = 4 * ci + ii;
-            const uint32_t w0 = word_at(wl, QL - 16 * LB0 + 4 * i);       // ql[64H + l], l = 4i..4i+3
-            const uint32_t w1 = word_at(wl, QL - 16 * LB0 + 32 + 4 * i);  // ql[64H + 32 + l]
-            const uint32_t hq = word_at(wh, QH - 16 * HB0 + 4 * i);       // qh[32H + l]
+            const uint32_t w0 = l[i];       // ql[64H + l], l = 4i..4i+3
+            const uint32_t w1 = l[8 + i];   // ql[64H + 32 + l]
+            const uint32_t hq = h[i];       // qh[32H + l]
             const uint32_t w0s = w0 >> 8, w1s = w1 >> 8;
             const uint32_t s4 = hq << 4, s4r = hq >> 4, s2 = hq << 2, s6r = hq >> 6;
             // g = 0, 1: 1024 + q; g = 2, 3: 1024 + 16 q (the scale carries 1/16)
@@ -302,15 +317,6 @@ __device__ __forceinline__ void q6k_dequant_half(const uint8_t* rb, uint32_t tad
         }
         tmem_st32(taddr + 64u * H + 32u * ci, o);
     }
-}
-
-// d of a Q6_K block starting DELTA bytes into the row buffer.
-template <int DELTA>
-__device__ __forceinline__ float q6k_block_d(const uint8_t* rb) {
-    constexpr int D = DELTA + 208;
-    uint32_t w[8];
-    load_blocks<D / 16, (D + 3) / 16>(rb, w);
-    return h2f(word_at(w, D - 16 * (D / 16)));
 }
 
 // ---------------------------------------------------------------- kernel
@@ -790,20 +796,8 @@ __global__ void __launch_bounds__(mvt_threads(MULTI), 1)
                         }
                         const int delta = (cls_off + 2 * sb) & 15;  // 210 = 2 mod 16
                         float d = 0.0f;
-                        switch (delta >> 1) {
-#define MUSER_Q6_CASE(k)                                                    \
-    case k:                                                                 \
-        if (hf == 0) {                                                      \
-            q6k_dequant_half<2 * k, 0>(rbuf, ta);                           \
-            d = q6k_block_d<2 * k>(rbuf);                                   \
-        } else {                                                            \
-            q6k_dequant_half<2 * k, 1>(rbuf, ta);                           \
-        }                                                                   \
-        break;
-                            MUSER_Q6_CASE(0) MUSER_Q6_CASE(1) MUSER_Q6_CASE(2) MUSER_Q6_CASE(3)
-                            MUSER_Q6_CASE(4) MUSER_Q6_CASE(5) MUSER_Q6_CASE(6) MUSER_Q6_CASE(7)
-#undef MUSER_Q6_CASE
-                        }
+                        if (hf == 0) q6k_dequant_half<0>(rbuf, delta, ta, d);
+                        else q6k_dequant_half<1>(rbuf, delta, ta, d);
                         sc.x = MULTI ? d : d * esc[sb];
                     }
                     tc_wait_st();
