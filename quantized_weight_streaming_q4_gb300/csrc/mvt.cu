@@ -58,7 +58,11 @@ constexpr int kRbWarp0 = kDeqWarps + 2;       // warps 10-13: D readback and epi
 constexpr int kBldWarp0 = kDeqWarps + 6;      // warps 14-15 (several rows of x): per-unit B operand
 constexpr int kNB = 3;                        // B slabs in shared memory (several rows of x)
 constexpr int kNA = 3;                        // A stages in TMEM (128 columns each)
-constexpr int kND = 4;                        // D buffers in TMEM (16 columns, 32 for several rows)
+constexpr int kND = 3;                        // D buffers in TMEM (16 columns, 32 for several rows)
+// One MMA commit per unit releases its A stage and B slab and publishes its
+// D buffer (a commit drains the MMA pipe, so there is only one), which needs
+// the three per-unit rings to have the same length.
+static_assert(kNA == kND && kNB == kND, "per-unit rings share one completion barrier");
 // Threads of a CTA: one row of x, or several (two more warps build B).
 __host__ __device__ constexpr int mvt_threads(bool multi) { return (kDeqWarps + (multi ? 8 : 6)) * 32; }
 constexpr uint32_t kTmemCols = 512;
@@ -434,18 +438,26 @@ struct BlockX {
     uint4 hi0, lo0, hi1, lo1;
     float esc, sa, sb;
 };
-template <int QT, bool kShared = false>
-__device__ __forceinline__ BlockX<QT> block_x(const float* xb, int lane) {
-    auto ld4 = [](const float* a) {
-        if constexpr (kShared) return *reinterpret_cast<const float4*>(a);
-        else return __ldg(reinterpret_cast<const float4*>(a));
-    };
-    BlockX<QT> r;
+// The lane's x values of a block: Q4_K v[0] = x[64c + 4t ..], v[1] = x[64c +
+// 32 + 4t ..]; Q6_K v[g] = x[128h + 32g + 4i ..] (g = 0..3).
+template <int QT>
+__device__ __forceinline__ void block_x_load(const float* xb, int lane, float4* v) {
     if constexpr (QT == MUSER_Q4_K) {
         const int c = lane >> 3, t = lane & 7;
-        const float* xs = xb + 64 * c + 4 * t;
-        const float4 xa = ld4(xs);
-        const float4 xc = ld4(xs + 32);
+        v[0] = __ldg(reinterpret_cast<const float4*>(xb + 64 * c + 4 * t));
+        v[1] = __ldg(reinterpret_cast<const float4*>(xb + 64 * c + 32 + 4 * t));
+    } else {
+        const int item = lane & 15, h = item >> 3, i = item & 7;
+#pragma unroll
+        for (int g = 0; g < 4; ++g) v[g] = __ldg(reinterpret_cast<const float4*>(xb + 128 * h + 32 * g + 4 * i));
+    }
+}
+template <int QT>
+__device__ __forceinline__ BlockX<QT> block_x(const float4* pv, int lane) {
+    BlockX<QT> r;
+    if constexpr (QT == MUSER_Q4_K) {
+        const float4 xa = pv[0];
+        const float4 xc = pv[1];
         float mx = fmaxf(fmaxf(fmaxf(fabsf(xa.x), fabsf(xa.y)), fmaxf(fabsf(xa.z), fabsf(xa.w))),
                          fmaxf(fmaxf(fabsf(xc.x), fabsf(xc.y)), fmaxf(fabsf(xc.z), fabsf(xc.w))));
 #pragma unroll
@@ -466,15 +478,11 @@ __device__ __forceinline__ BlockX<QT> block_x(const float* xb, int lane) {
         r.sb = sc;
         r.esc = ldexpf(1.0f, E - 15);
     } else {
-        const int item = lane & 15, h = item >> 3, i = item & 7;
-        const float* xs = xb + 128 * h + 4 * i;
-        float4 v[4];
+        const float4* v = pv;
         float mx = 0.0f;
 #pragma unroll
-        for (int g = 0; g < 4; ++g) {
-            v[g] = ld4(xs + 32 * g);
+        for (int g = 0; g < 4; ++g)
             mx = fmaxf(mx, fmaxf(fmaxf(fabsf(v[g].x), fabsf(v[g].y)), fmaxf(fabsf(v[g].z), fabsf(v[g].w))));
-        }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
         const int E = scale_exp(mx);
@@ -610,13 +618,11 @@ __global__ void __launch_bounds__(mvt_threads(MULTI), 1)
     uint64_t* full = reinterpret_cast<uint64_t*>(smem);
     uint64_t* empty = full + kMaxStages;
     uint64_t* afull = empty + kMaxStages;
-    uint64_t* aempty = afull + kNA;
-    uint64_t* dfull = aempty + kNA;
+    uint64_t* dfull = afull + kNA;   // MMA of the slot's unit done: A stage and B slab free, D ready
     uint64_t* dempty = dfull + kND;
     uint64_t* sfull = dempty + kND;
     uint64_t* bfull = sfull + kND;
-    uint64_t* bempty = bfull + kNB;
-    uint64_t* xfull = bempty + kNB;  // [2 builder warps][kNB]
+    uint64_t* xfull = bfull + kNB;   // [2 builder warps][kNB]
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + 448);
     int* flags = reinterpret_cast<int*>(smem + 464);       // [0] run the tail, [1] tile ticket won
     float* red = reinterpret_cast<float*>(smem + 512);     // 64 floats
@@ -638,7 +644,6 @@ __global__ void __launch_bounds__(mvt_threads(MULTI), 1)
         }
         for (int i = 0; i < kNA; ++i) {
             mbar_init(&afull[i], kDeqWarps);
-            mbar_init(&aempty[i], 1);
         }
         for (int i = 0; i < kND; ++i) {
             mbar_init(&dfull[i], 1);
@@ -647,7 +652,6 @@ __global__ void __launch_bounds__(mvt_threads(MULTI), 1)
         }
         for (int i = 0; i < kNB; ++i) {
             mbar_init(&bfull[i], 2);
-            mbar_init(&bempty[i], 1);
             mbar_init(&xfull[i], 1);
             mbar_init(&xfull[kNB + i], 1);
         }
@@ -701,8 +705,18 @@ __global__ void __launch_bounds__(mvt_threads(MULTI), 1)
             // ---------- one row of x: the whole B operand, one warp per block
             const int bw = warp < kTmaWarp ? warp : warp - 1;
             constexpr int nbw = kThr / 32 - 1;
-            for (int sb = bw; sb < nsb; sb += nbw) {
-                const BlockX<QT> bx = block_x<QT>(p.x + sb * 256, lane);
+            constexpr int kG = 4;                          // blocks a warp loads before converting
+            constexpr int kV = QT == MUSER_Q4_K ? 2 : 4;   // float4 per lane and block
+            for (int sb0 = bw; sb0 < nsb; sb0 += kG * nbw) {
+                float4 raw[kG][kV];
+#pragma unroll
+                for (int j = 0; j < kG; ++j)
+                    if (sb0 + j * nbw < nsb) block_x_load<QT>(p.x + (sb0 + j * nbw) * 256, lane, raw[j]);
+#pragma unroll
+                for (int j = 0; j < kG; ++j) {
+                const int sb = sb0 + j * nbw;
+                if (sb >= nsb) break;
+                const BlockX<QT> bx = block_x<QT>(raw[j], lane);
                 if constexpr (QT == MUSER_Q4_K) {
                     const int c = lane >> 3, t = lane & 7;
                     uint8_t* ch = B + 32 * (sb * 32 + 8 * c + t);
@@ -721,6 +735,7 @@ __global__ void __launch_bounds__(mvt_threads(MULTI), 1)
                     *reinterpret_cast<uint4*>(ch + 48) = bx.lo1;
                 }
                 if (lane == 0) esc[sb] = bx.esc;
+                }
             }
             if (bw == 0) reinterpret_cast<uint4*>(B + nsb * 1024)[lane] = make_uint4(0u, 0u, 0u, 0u);  // slack
             fence_proxy_async_smem();
@@ -746,7 +761,6 @@ __global__ void __launch_bounds__(mvt_threads(MULTI), 1)
 #pragma unroll
                         for (int j = 0; j < 16; ++j)
                             mma_f16_ts(dcol, acol + 8u * j, smem_desc(bbase + 1024u * j, 512u, 128u), kIdesc, j > 0 ? 1u : 0u);
-                        mma_commit(&bempty[rb.slot]);
                     } else {
                         // compact: two rows per 32-byte chunk, chunks overlap
                         const uint32_t bbase = smem_u32(B) + 1024u * it.sb;
@@ -754,7 +768,6 @@ __global__ void __launch_bounds__(mvt_threads(MULTI), 1)
                         for (int j = 0; j < 16; ++j)
                             mma_f16_ts(dcol, acol + 8u * j, smem_desc(bbase + 64u * j, 32u, 256u), kIdesc, j > 0 ? 1u : 0u);
                     }
-                    mma_commit(&aempty[a]);
                     mma_commit(&dfull[db]);
                 }
             }
@@ -770,7 +783,7 @@ __global__ void __launch_bounds__(mvt_threads(MULTI), 1)
             for (int i = 0; i < nunits; ++i, it.next(), rs.next(NS), ra.next(kNA), rd.next(kND)) {
                 const int s = rs.slot, a = ra.slot, db = rd.slot;
                 if (ok) ok = mbar_wait_bounded(&full[s], rs.phase, p.status, kDevStatusWaitTimeout);
-                if (ok && i >= kNA) ok = mbar_wait_bounded(&aempty[a], ra.phase ^ 1u, p.status, kDevStatusWaitTimeout);
+                if (ok && i >= kNA) ok = mbar_wait_bounded(&dfull[a], ra.phase ^ 1u, p.status, kDevStatusWaitTimeout);
                 const uint8_t* rbuf = stages + static_cast<size_t>(s) * kStage + l * RS;
                 const uint32_t ta = tq + 128u * a;
                 const int sb = it.sb;
@@ -837,7 +850,7 @@ __global__ void __launch_bounds__(mvt_threads(MULTI), 1)
             for (int j = 0; j < kNB; ++j) ahead.next();
             Ring rb, rd;
             for (int i = 0; i < nunits; ++i, it.next(), ahead.next(), rb.next(kNB), rd.next(kND)) {
-                if (ok && i >= kNB) ok = mbar_wait_bounded(&bempty[rb.slot], rb.phase ^ 1u, p.status, kDevStatusWaitTimeout);
+                if (ok && i >= kNB) ok = mbar_wait_bounded(&dfull[rb.slot], rb.phase ^ 1u, p.status, kDevStatusWaitTimeout);
                 if (ok && i >= kND) ok = mbar_wait_bounded(&dempty[rd.slot], rd.phase ^ 1u, p.status, kDevStatusWaitTimeout);
                 if (ok && mlo < M) ok = mbar_wait_bounded(&xf[rb.slot], rb.phase, p.status, kDevStatusWaitTimeout);
                 uint8_t* slab = B + kSlab * rb.slot;
