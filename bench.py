@@ -45,8 +45,8 @@ METRIC = "weight-stream GB/s (% of GB300 HBM peak); decode FFN tokens/sec, 1 GPU
 
 # ncu DRAM traffic of the dominant kernel, per launch, with the source hash it
 # was captured on (profiles/ summary); reported as null once the kernel changed.
-NCU_TRAFFIC = {"kernel": "mv1_kernel<Q4_K,2,silu>", "bytes_per_launch": 153062912,
-               "source_sha256": "bd36400e0de4348ce62a4aeb04edfc78e76f3072d0a14c1be50fa8c048ffde81",
+NCU_TRAFFIC = {"kernel": "mv1_kernel<Q4_K,2,silu>", "bytes_per_launch": 152660480,
+               "source_sha256": "9f98676aa555252a8f6dc452556bb4317824063669020f834850e26f9060c4ce",
                "profile": "profiles/mv1_gate_up_q4k_and_down_q6k_tail.md"}
 
 
@@ -75,9 +75,14 @@ def read_peaks():
         return 6800.0, "fallback"
 
 
+# Sources that define the one-token gate/up kernel (mv1): a change to any of
+# them makes the recorded DRAM traffic stale.
+MV1_SOURCES = ("common.cuh", "kernels.cuh", "mv1.cu")
+
+
 def source_sha():
     h = hashlib.sha256()
-    for f in sorted(os.listdir(os.path.join(ROOT, "quantized_weight_streaming_q4_gb300", "csrc"))):
+    for f in MV1_SOURCES:
         with open(os.path.join(ROOT, "quantized_weight_streaming_q4_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()

@@ -255,13 +255,11 @@ __device__ __forceinline__ void load_blocks(const uint8_t* rb, uint32_t* w) {
 // first column).  Sets d (the block's scale) for H == 0.  The fields' 16-byte
 // blocks are loaded at fixed offsets; a uniform switch moves the words by
 // delta / 4 and a uniform funnel shift handles the 2-byte remainder, so one
-// code body serves every misalignment.
-template <int H>
-__device__ __forceinline__ void q6k_dequant_half(const uint8_t* rb, int delta, uint32_t taddr, float& d) {
-    constexpr int QL = 64 * H, QH = 128 + 32 * H;
+// code body serves every misalignment and both halves.
+__device__ __forceinline__ void q6k_dequant_half(const uint8_t* rb, int H, int delta, uint32_t taddr, float& d) {
     uint32_t wl[20], wh[12], ws[12];
-    load_blocks<QL / 16, QL / 16 + 4>(rb, wl);  // ql: bytes QL .. QL + 79
-    load_blocks<QH / 16, QH / 16 + 2>(rb, wh);  // qh: bytes QH .. QH + 47
+    load_blocks<0, 4>(rb + 64 * H, wl);         // ql: bytes 64H .. 64H + 79
+    load_blocks<0, 2>(rb + 128 + 32 * H, wh);   // qh: bytes 128 + 32H .. + 47
     load_blocks<12, 14>(rb, ws);                // scales and d: bytes 192 .. 239
     uint32_t l[17], h[9], s[7];                 // words from delta (before the 2-byte shift)
     auto take = [&](int k) {
@@ -287,7 +285,7 @@ __device__ __forceinline__ void q6k_dequant_half(const uint8_t* rb, int delta, u
         for (int i = 0; i < 6; ++i) s[i] = __funnelshift_r(s[i], s[i + 1], 16);
     }
     if (H == 0) d = h2f(s[4]);
-    const uint32_t S0 = s[2 * H], S1 = s[2 * H + 1];  // sc[8H .. 8H + 7]
+    const uint32_t S0 = H ? s[2] : s[0], S1 = H ? s[3] : s[1];  // sc[8H .. 8H + 7]
 #pragma unroll
     for (int ci = 0; ci < 2; ++ci) {
         // words i = 4ci..4ci+3 use the scales sc[8H + 2g + ci], g = 0..3
@@ -809,8 +807,7 @@ __global__ void __launch_bounds__(mvt_threads(MULTI), 1)
                         }
                         const int delta = (cls_off + 2 * sb) & 15;  // 210 = 2 mod 16
                         float d = 0.0f;
-                        if (hf == 0) q6k_dequant_half<0>(rbuf, delta, ta, d);
-                        else q6k_dequant_half<1>(rbuf, delta, ta, d);
+                        q6k_dequant_half(rbuf, hf, delta, ta, d);
                         sc.x = MULTI ? d : d * esc[sb];
                     }
                     tc_wait_st();
