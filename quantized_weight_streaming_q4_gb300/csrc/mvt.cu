@@ -141,7 +141,17 @@ __device__ __forceinline__ uint32_t h2rep(float f) {
     return h | (h << 16);
 }
 
-__device__ __forceinline__ uint4 lds128(const uint8_t* p) { return *reinterpret_cast<const uint4*>(p); }
+// Shared-memory loads through the shared window (the pointers are generic).
+__device__ __forceinline__ uint4 lds128(const void* p) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(smem_u32(p)));
+    return v;
+}
+__device__ __forceinline__ float4 lds_f4(const void* p) {
+    float4 v;
+    asm volatile("ld.shared.v4.f32 {%0,%1,%2,%3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(smem_u32(p)));
+    return v;
+}
 
 // 2-D tensor copy of one box at (x bytes, y rows) into shared memory; the
 // completed bytes are counted on `bar`.  x is a multiple of 16.
@@ -516,8 +526,8 @@ __device__ __forceinline__ float build_row_quarter(const float* xrow, int q, uin
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 const int t = q + 4 * h;
-                v[4 * c + 2 * h] = *reinterpret_cast<const float4*>(xrow + 64 * c + 4 * t);
-                v[4 * c + 2 * h + 1] = *reinterpret_cast<const float4*>(xrow + 64 * c + 32 + 4 * t);
+                v[4 * c + 2 * h] = lds_f4(xrow + 64 * c + 4 * t);
+                v[4 * c + 2 * h + 1] = lds_f4(xrow + 64 * c + 32 + 4 * t);
             }
     } else {
         // item (h, i), i = q + 4e: x chunks 32h + 8g + i, g = 0..3
@@ -527,7 +537,7 @@ __device__ __forceinline__ float build_row_quarter(const float* xrow, int q, uin
             for (int e = 0; e < 2; ++e)
 #pragma unroll
                 for (int g = 0; g < 4; ++g)
-                    v[8 * h + 4 * e + g] = *reinterpret_cast<const float4*>(xrow + 128 * h + 32 * g + 4 * (q + 4 * e));
+                    v[8 * h + 4 * e + g] = lds_f4(xrow + 128 * h + 32 * g + 4 * (q + 4 * e));
     }
     float mx = 0.0f;
 #pragma unroll
@@ -889,7 +899,7 @@ __global__ void __launch_bounds__(mvt_threads(MULTI), 1)
                 const int db = rd.slot;
                 if (ok) ok = mbar_wait_bounded(&dfull[db], rd.phase, p.status, kDevStatusWaitTimeout);
                 if (ok) ok = mbar_wait_bounded(&sfull[db], rd.phase, p.status, kDevStatusWaitTimeout);
-                const float4 sc = scr[db * 128 + l];
+                const float4 sc = lds_f4(&scr[db * 128 + l]);
                 if constexpr (MULTI) {
                     uint32_t dv[32];
 #pragma unroll
@@ -912,7 +922,7 @@ __global__ void __launch_bounds__(mvt_threads(MULTI), 1)
 #pragma unroll
                     for (int m4 = 0; m4 < MB; m4 += 4) {
                         if (m4 >= M) break;
-                        const float4 e4 = *reinterpret_cast<const float4*>(xu + 8 * MB + m4);
+                        const float4 e4 = lds_f4(xu + 8 * MB + m4);
                         const float ev[4] = {e4.x, e4.y, e4.z, e4.w};
 #pragma unroll
                         for (int mm = 0; mm < 4; ++mm) {
@@ -920,8 +930,8 @@ __global__ void __launch_bounds__(mvt_threads(MULTI), 1)
                             const float dd = __uint_as_float(dv[2 * m]) + __uint_as_float(dv[2 * m + 1]) * (1.0f / 2048.0f);
                             float v = dd * (sc.x * ev[mm]);
                             if constexpr (QT == MUSER_Q4_K) {
-                                const float4 xa = *reinterpret_cast<const float4*>(xu + 8 * m);
-                                const float4 xb = *reinterpret_cast<const float4*>(xu + 8 * m + 4);
+                                const float4 xa = lds_f4(xu + 8 * m);
+                                const float4 xb = lds_f4(xu + 8 * m + 4);
                                 float s = mins[0] * xa.x;
                                 s = fmaf(mins[1], xa.y, s);
                                 s = fmaf(mins[2], xa.z, s);
