@@ -171,6 +171,8 @@ class NativeStack:
         self.x = [torch.empty(M, H, dtype=torch.float32, device="cuda") for _ in range(2)]
         self.mid = torch.empty(M, F, dtype=torch.float32, device="cuda")
         self.proj = torch.empty(M, H, dtype=torch.float32, device="cuda")
+        self.gu_scratch_bytes = mu.muser_gate_up_scratch_bytes(mu.MUSER_Q4_K, F, H, M)
+        self.gu_scratch = torch.zeros(max(self.gu_scratch_bytes, 16) // 4, dtype=torch.float32, device="cuda")
         self.scratch_bytes = mu.muser_scratch_bytes(H, M)
         self.scratch = torch.zeros(self.scratch_bytes // 4 + 64, dtype=torch.float32, device="cuda")
         wsb = mu.muser_ffn_workspace_bytes(H, F, M)
@@ -197,8 +199,9 @@ class NativeStack:
             ev = events.get(l) if events is not None else None
             if ev is not None:
                 ev[0].record(self.stream)
-            self._rc("gate_up", L.muser_ffn_gate_up_silu(12, d["Wg"].data_ptr(), d["Wu"].data_ptr(), F, H,
-                                                         x.data_ptr(), M, self.mid.data_ptr(), sh))
+            self._rc("gate_up", L.muser_ffn_gate_up_silu_scratch(
+                12, d["Wg"].data_ptr(), d["Wu"].data_ptr(), F, H, x.data_ptr(), M, self.mid.data_ptr(),
+                self.gu_scratch.data_ptr(), self.gu_scratch_bytes, sh))
             if ev is not None:
                 ev[1].record(self.stream)
             dst = self.out if l == self.nl - 1 else xn

@@ -121,6 +121,25 @@ int muser_silu_mul(const float* a, const float* b, float* out, int64_t n, void* 
 int muser_ffn_gate_up_silu(int qtype, const void* Wg, const void* Wu, int64_t ffn,
                            int64_t hidden, const float* x, int M, float* mid, void* stream);
 
+/* Scratch bytes muser_ffn_gate_up_silu_scratch needs (0: the call needs none). */
+size_t muser_gate_up_scratch_bytes(int qtype, int64_t ffn, int64_t hidden, int M);
+
+/*
+ * muser_ffn_gate_up_silu_scratch -- the same result as muser_ffn_gate_up_silu.
+ *   With caller scratch the tensor-core kernel (2..16 rows of x) can split a
+ *   row tile's super-blocks over several SMs and sum the parts in a fixed
+ *   order; without it each SM takes whole tiles, which leaves SMs idle when
+ *   the tile count is not a multiple of the SM count.
+ *   scratch: device memory of at least muser_gate_up_scratch_bytes(...) bytes,
+ *   16-byte aligned, owned by the caller, zero-filled before its first use;
+ *   every successful call leaves it zero-filled again.  Calls that can run at
+ *   the same time must not share it.  Other arguments as
+ *   muser_ffn_gate_up_silu.
+ */
+int muser_ffn_gate_up_silu_scratch(int qtype, const void* Wg, const void* Wu, int64_t ffn,
+                                   int64_t hidden, const float* x, int M, float* mid, void* scratch,
+                                   size_t scratch_bytes, void* stream);
+
 /*
  * muser_fused_residual_dual_rmsnorm -- the dual-eps tail (Ch 19 §19.4,
  *   muser_fused_norm_residual_rms_norm_32sg; Ch 10 Figure 10.2), per row m:

@@ -19,7 +19,8 @@ __all__ = [
     "MUSER_Q4_K", "MUSER_Q6_K", "QTYPES", "MuserError", "build", "library_path", "lib",
     "muser_version", "muser_last_error", "muser_block_bytes", "muser_matrix_bytes",
     "muser_dequantize", "muser_qmatvec", "muser_rms_norm", "muser_silu_mul",
-    "muser_ffn_gate_up_silu", "muser_fused_residual_dual_rmsnorm", "muser_scratch_bytes",
+    "muser_ffn_gate_up_silu", "muser_gate_up_scratch_bytes", "muser_ffn_gate_up_silu_scratch",
+    "muser_fused_residual_dual_rmsnorm", "muser_scratch_bytes",
     "muser_qmatvec_residual_dual_rmsnorm", "muser_qmatvec_residual_dual_rmsnorm_static",
     "MUSER_STATIC_SCRATCH_BYTES", "FfnLayer", "muser_ffn_workspace_bytes",
     "muser_ffn_stack", "KvPlane", "muser_kv_ring_write", "muser_sync", "muser_debug_spin",
@@ -91,6 +92,8 @@ def lib():
             "muser_rms_norm": (I, [P, P, P, I, I, F, P]),
             "muser_silu_mul": (I, [P, P, P, I64, P]),
             "muser_ffn_gate_up_silu": (I, [I, P, P, I64, I64, P, I, P, P]),
+            "muser_gate_up_scratch_bytes": (SZ, [I, I64, I64, I]),
+            "muser_ffn_gate_up_silu_scratch": (I, [I, P, P, I64, I64, P, I, P, P, SZ, P]),
             "muser_fused_residual_dual_rmsnorm": (I, [P, P, P, P, P, I, I, F, F, P]),
             "muser_scratch_bytes": (SZ, [I64, I]),
             "muser_qmatvec_residual_dual_rmsnorm": (I, [I, P, I64, I64, P, I, P, P, P, P, P, F, F, P,
@@ -185,6 +188,17 @@ def muser_ffn_gate_up_silu(qtype, Wg, Wu, ffn: int, hidden: int, x, M: int, mid,
     _check("muser_ffn_gate_up_silu",
            lib().muser_ffn_gate_up_silu(_qt(qtype), _ptr(Wg), _ptr(Wu), ffn, hidden, _ptr(x), M,
                                         _ptr(mid), _stream(stream)))
+
+
+def muser_gate_up_scratch_bytes(qtype, ffn: int, hidden: int, M: int) -> int:
+    return lib().muser_gate_up_scratch_bytes(_qt(qtype), ffn, hidden, M)
+
+
+def muser_ffn_gate_up_silu_scratch(qtype, Wg, Wu, ffn: int, hidden: int, x, M: int, mid, scratch,
+                                   scratch_bytes: int, stream=None) -> None:
+    _check("muser_ffn_gate_up_silu_scratch",
+           lib().muser_ffn_gate_up_silu_scratch(_qt(qtype), _ptr(Wg), _ptr(Wu), ffn, hidden, _ptr(x), M,
+                                                _ptr(mid), _ptr(scratch), scratch_bytes, _stream(stream)))
 
 
 def muser_fused_residual_dual_rmsnorm(residual, src, out, w1, w2, n: int, M: int, eps1: float,

@@ -362,6 +362,30 @@ int muser_ffn_gate_up_silu(int qtype, const void* Wg, const void* Wu, int64_t ff
     return gate_up_launch(qtype, Wg, Wu, ffn, hidden, x, M, mid, nullptr, as_stream(stream));
 }
 
+size_t muser_gate_up_scratch_bytes(int qtype, int64_t ffn, int64_t hidden, int M) {
+    if (M < 1 || M > MUSER_MAX_M) return 0;
+    return mvt_scratch_bytes(qtype, 2, ffn, hidden, M);
+}
+
+int muser_ffn_gate_up_silu_scratch(int qtype, const void* Wg, const void* Wu, int64_t ffn,
+                                   int64_t hidden, const float* x, int M, float* mid, void* scratch,
+                                   size_t scratch_bytes, void* stream) {
+    clear_error();
+    const char* fn = "muser_ffn_gate_up_silu_scratch";
+    MUSER_TRY(check_matrix(fn, qtype, Wg, ffn, hidden));
+    MUSER_TRY(check_matrix(fn, qtype, Wu, ffn, hidden));
+    MUSER_TRY(check_M(fn, M));
+    MUSER_TRY(check_f32(fn, "x", x));
+    MUSER_TRY(check_f32(fn, "mid", mid));
+    const size_t need = mvt_scratch_bytes(qtype, 2, ffn, hidden, M);
+    if (need > 0) {
+        MUSER_TRY(check_f32(fn, "scratch", scratch));
+        if (scratch_bytes < need)
+            return set_error(MUSER_ERR_INVALID_ARG, "%s: scratch_bytes %zu < %zu", fn, scratch_bytes, need);
+    }
+    return gate_up_launch(qtype, Wg, Wu, ffn, hidden, x, M, mid, need > 0 ? scratch : nullptr, as_stream(stream));
+}
+
 int muser_fused_residual_dual_rmsnorm(float* residual, const float* src, float* out,
                                       const float* w1, const float* w2, int n, int M, float eps1,
                                       float eps2, void* stream) {

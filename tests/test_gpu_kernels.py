@@ -122,13 +122,22 @@ def test_qmatvec_one_hot_columns_bit_exact(qtype):
 
 # ------------------------------------------------------- gate / up / SiLU
 @pytest.mark.parametrize("M", [1, 4, 16])
-def test_ffn_gate_up_silu(M):
+@pytest.mark.parametrize("with_scratch", [False, True])
+def test_ffn_gate_up_silu(M, with_scratch):
+    """Without scratch the tensor-core kernel (M > 1) takes whole row tiles;
+    with it the tiles' super-blocks split over SMs (ragged ffn in both)."""
     ffn, hidden = 2000 + M, 6656
     Wg = synth.q4k_matrix(ffn, hidden, seed=M, tensor=synth.T_GATE)
     Wu = synth.q4k_matrix(ffn, hidden, seed=M, tensor=synth.T_UP)
     x = oracle.rms_norm(synth.normal((M, hidden), seed=M), synth.norm_weight(hidden, seed=M), 1e-5)
     mid = nan_like((M, ffn), extra=32)
-    mu.muser_ffn_gate_up_silu("q4_k", dev(Wg), dev(Wu), ffn, hidden, dev(x), M, mid)
+    if with_scratch:
+        nscr = mu.muser_gate_up_scratch_bytes("q4_k", ffn, hidden, M)
+        scratch = torch.zeros(max(nscr, 16) // 4, dtype=torch.float32, device="cuda")
+        mu.muser_ffn_gate_up_silu_scratch("q4_k", dev(Wg), dev(Wu), ffn, hidden, dev(x), M, mid, scratch, nscr)
+        assert not host(scratch).any(), "scratch must be left zeroed"
+    else:
+        mu.muser_ffn_gate_up_silu("q4_k", dev(Wg), dev(Wu), ffn, hidden, dev(x), M, mid)
     got = host(mid[:M * ffn]).reshape(M, ffn)
     check_canary(mid, M * ffn)
     ref = oracle.gate_up_silu("q4_k", Wg, Wu, ffn, hidden, x)
