@@ -84,6 +84,7 @@ int check_M(const char* fn, int M) {
 
 constexpr size_t kScratchBytes = 256;
 // Route one-token calls to the tensor-core kernel (mvt) instead of mv1.
+// mv1 measures faster for one row of x (one launch and inside the stack).
 constexpr bool kTensorCoreM1 = false;
 
 // Scratch of the fused down projection + tail: the CUDA-core kernel's ticket

@@ -116,12 +116,34 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint3
 // M = 128, N = 16 (one row of x) or 32 (up to 16 rows, hi and lo each).
 constexpr uint32_t idesc_n(uint32_t n) { return (1u << 4) | ((n >> 3) << 17) | ((128u >> 4) << 24); }
 
-__device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                                           uint32_t accumulate) {
+// One super-block's MMA chain: 16 MMAs of K = 16 into D (the first one
+// overwrites, the rest accumulate), A columns a_tmem + 8j, B descriptors
+// b_desc + j * b_step.  One asm block, so the predicates and the operand
+// advances cost one instruction each.
+__device__ __forceinline__ void mma_chain16(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                            uint64_t b_step) {
     asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        "{\n\t.reg .pred pf, pt;\n\t.reg .b32 ra;\n\t.reg .b64 rd;\n\t"
+        "setp.ne.b32 pf, %0, %0;\n\tsetp.eq.b32 pt, %0, %0;\n\t"
+        "mov.b32 ra, %1;\n\tmov.b64 rd, %2;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [ra], rd, %3, pf;\n\t"
+        "add.u32 ra, ra, 8;\n\tadd.u64 rd, rd, %4;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [ra], rd, %3, pt;\n\t"
+        "add.u32 ra, ra, 8;\n\tadd.u64 rd, rd, %4;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [ra], rd, %3, pt;\n\t"
+        "add.u32 ra, ra, 8;\n\tadd.u64 rd, rd, %4;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [ra], rd, %3, pt;\n\t"
+        "add.u32 ra, ra, 8;\n\tadd.u64 rd, rd, %4;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [ra], rd, %3, pt;\n\t"
+        "add.u32 ra, ra, 8;\n\tadd.u64 rd, rd, %4;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [ra], rd, %3, pt;\n\t"
+        "add.u32 ra, ra, 8;\n\tadd.u64 rd, rd, %4;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [ra], rd, %3, pt;\n\t"
+        "add.u32 ra, ra, 8;\n\tadd.u64 rd, rd, %4;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [ra], rd, %3, pt;\n\t"
+        "add.u32 ra, ra, 8;\n\tadd.u64 rd, rd, %4;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [ra], rd, %3, pt;\n\t"
+        "add.u32 ra, ra, 8;\n\tadd.u64 rd, rd, %4;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [ra], rd, %3, pt;\n\t"
+        "add.u32 ra, ra, 8;\n\tadd.u64 rd, rd, %4;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [ra], rd, %3, pt;\n\t"
+        "add.u32 ra, ra, 8;\n\tadd.u64 rd, rd, %4;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [ra], rd, %3, pt;\n\t"
+        "add.u32 ra, ra, 8;\n\tadd.u64 rd, rd, %4;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [ra], rd, %3, pt;\n\t"
+        "add.u32 ra, ra, 8;\n\tadd.u64 rd, rd, %4;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [ra], rd, %3, pt;\n\t"
+        "add.u32 ra, ra, 8;\n\tadd.u64 rd, rd, %4;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [ra], rd, %3, pt;\n\t"
+        "add.u32 ra, ra, 8;\n\tadd.u64 rd, rd, %4;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [ra], rd, %3, pt;\n\t"
+        "}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "l"(b_step)
         : "memory");
 }
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
@@ -766,15 +788,11 @@ __global__ void __launch_bounds__(mvt_threads(MULTI), 1)
                     if constexpr (MULTI) {
                         // slab: K chunk stride 512 B, N-group stride 128 B
                         const uint32_t bbase = smem_u32(B) + kSlab * rb.slot;
-#pragma unroll
-                        for (int j = 0; j < 16; ++j)
-                            mma_f16_ts(dcol, acol + 8u * j, smem_desc(bbase + 1024u * j, 512u, 128u), kIdesc, j > 0 ? 1u : 0u);
+                        mma_chain16(dcol, acol, smem_desc(bbase, 512u, 128u), kIdesc, 1024u >> 4);
                     } else {
                         // compact: two rows per 32-byte chunk, chunks overlap
                         const uint32_t bbase = smem_u32(B) + 1024u * it.sb;
-#pragma unroll
-                        for (int j = 0; j < 16; ++j)
-                            mma_f16_ts(dcol, acol + 8u * j, smem_desc(bbase + 64u * j, 32u, 256u), kIdesc, j > 0 ? 1u : 0u);
+                        mma_chain16(dcol, acol, smem_desc(bbase, 32u, 256u), kIdesc, 64u >> 4);
                     }
                     mma_commit(&dfull[db]);
                 }
