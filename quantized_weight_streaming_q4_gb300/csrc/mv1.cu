@@ -8,12 +8,11 @@
 //    blocks are only 2-byte aligned, so staging whole row spans is what keeps
 //    the global traffic in 16-byte-aligned bulk transfers.
 //  * Each thread owns a fixed 64-weight slice (super-block b, chunk c) of the
-//    input vector for the whole kernel and keeps it in registers, pre-scaled
-//    by powers of two so that a 4- or 6-bit code masked in place inside its
-//    32-bit word -- a subnormal float equal to code * 2^(p-149) -- times the
-//    scaled input is exactly code * x * 2^-96.  One AND per weight turns a
-//    code into an exact float operand; products go through packed
-//    fma.rn.f32x2.  Scales are applied once per sub-block.
+//    input vector for the whole kernel and keeps it in registers, held as
+//    the three bytes of a 24-bit fixed-point copy (one power of two per
+//    slice).  Codes are masked in place, four to a 32-bit word, and dp4a
+//    adds four code * digit products per instruction into exact int32
+//    per-digit sub-block sums.  Scales are applied once per sub-block.
 //  * Per stage, the slice partials of every row land in shared memory and
 //    one warp per row adds them in a fixed order (deterministic results).
 //  * Epilogues: store y; SiLU-gate two matrices (gate/up, Ch 10 §10.3 (d));
@@ -33,193 +32,264 @@ __device__ unsigned g_device_status = 0u;
 
 namespace {
 
-constexpr float kTwo96 = 79228162514264337593543950336.0f;  // 2^96
-
 // --------------------------------------------------- per-thread input slice
-// Arithmetic on register pairs.  Two consecutive 32-bit code words form one
-// 64-bit value; masking it with a 64-bit constant (the same mask in both
-// halves) yields two subnormal-float operands in one register pair, which
-// fma.rn.f32x2 consumes directly.  A 64-bit right shift moves the top of the
-// high word into the top of the low word; every mask applied after a shift
-// clears those bit positions, so the shift acts per half.
-typedef unsigned long long u64;
+// The input slice is held as integers.  With one power of two 2^e per slice
+// (max |x| * 2^e in [2^22, 2^23)), X = rint(x * 2^e) is a 24-bit two's
+// complement integer, split into bytes X = D2*65536 + D1*256 + D0 (D0, D1
+// unsigned, D2 signed), each digit packed four to a register in the byte
+// order of the code words.  A code word masked to its nibbles (or rebuilt
+// Q6_K codes) is four unsigned bytes; one dp4a per digit adds four
+// code * digit products into an int32, so the per-digit sub-block sums are
+// exact integers.  The roundings are X itself (at most 2^-23 of the slice's
+// largest |x|) and the binary32 combination of the three digit sums.
 
-__device__ __forceinline__ u64 f2_bits(float a, float b) {
-    return (static_cast<u64>(__float_as_uint(b)) << 32) | __float_as_uint(a);
+// Exponent e of a slice with largest magnitude m (0 for m == 0): m * 2^e is
+// in [2^21, 2^23 - 1.5], so rint(x * 2^e) is in [-2^23 + 1, 2^23 - 1] for
+// every |x| <= m.  Reading the binade of m * (1 + 2^-23) moves the m whose
+// significand is within two units of 2 to the next binade (one bit less
+// precision for those slices, never an overflow).
+__device__ __forceinline__ int slice_exponent(float m) {
+    if (!(m > 0.0f)) return 0;
+    const float mu = m * 1.00000012f;
+    const int E = static_cast<int>((__float_as_uint(mu) >> 23) & 0xFFu) - 127;
+    return min(22 - E, 126);
 }
-__device__ __forceinline__ u64 fma2(u64 a, u64 b, u64 c) {
-    u64 d;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+// 2^e as a float, e in [-126, 127].
+__device__ __forceinline__ float pow2f(int e) { return __uint_as_float(static_cast<uint32_t>(e + 127) << 23); }
+
+// Bytes 0, 1 and 2 (the digits) of four 24-bit integers, each packed in order.
+__device__ __forceinline__ void pack_digits(int X0, int X1, int X2, int X3, uint32_t* w3) {
+    const uint32_t a = static_cast<uint32_t>(X0), b = static_cast<uint32_t>(X1);
+    const uint32_t c = static_cast<uint32_t>(X2), d = static_cast<uint32_t>(X3);
+    const uint32_t p01 = __byte_perm(a, b, 0x5140u), p23 = __byte_perm(c, d, 0x5140u);
+    w3[0] = __byte_perm(p01, p23, 0x5410u);
+    w3[1] = __byte_perm(p01, p23, 0x7632u);
+    w3[2] = __byte_perm(__byte_perm(a, b, 0x0062u), __byte_perm(c, d, 0x0062u), 0x5410u);
+}
+
+// Four-way byte dot products with int32 accumulation: unsigned codes times
+// the unsigned low digits, and times the signed top digit.
+__device__ __forceinline__ int dp4a_uu(uint32_t a, uint32_t b, int c) {
+    int d;
+    asm("dp4a.u32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
     return d;
 }
-__device__ __forceinline__ float lo_f(u64 v) { return __uint_as_float(static_cast<uint32_t>(v)); }
-__device__ __forceinline__ float hi_f(u64 v) { return __uint_as_float(static_cast<uint32_t>(v >> 32)); }
+__device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
+    int d;
+    asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+// D2*65536 + D1*256 + D0 from the three digit sums: T = D2*256 + D1 is an
+// exact int32 for every code range here (|T| < 2^28); the rest in binary32.
+__device__ __forceinline__ float combine3(int a0, int a1, int a2) {
+    return fmaf(static_cast<float>(a2 * 256 + a1), 256.0f, static_cast<float>(a0));
+}
 
-constexpr u64 rep(uint32_t m) { return (static_cast<u64>(m) << 32) | m; }
+// Small unsigned byte / 16 -> float through the 2^19 magic exponent: the
+// float with bits 0x490000XX is 2^19 + XX/16, exactly.
+__device__ __forceinline__ float byte_to_f16th(uint32_t word, uint32_t sel_with_magic) {
+    return __uint_as_float(__byte_perm(word, 0x49000000u, sel_with_magic)) - 524288.0f;
+}
 
 // Q4_K slice (b, c): weights 64c + l of super-block b, l = 0..63.  Code byte
-// 32c + 4t + j holds weight 64c + 4t + j (low nibble) and 64c + 32 + 4t + j
-// (high nibble).  Words t = 2k, 2k+1 form pair k.  Nibble position i of a
-// word (0..7: bytes 0,0,1,1,2 low/high at bits 0,4,8,12,16; then bytes 2,3,3
-// after a 12-bit shift at bits 8,12,16) is used in place, so the slice holds
-// x * 2^(53 - p_i) for p = 0,4,8,12,16,8,12,16: a code masked at bit p is the
-// subnormal code * 2^(p-149) and the product is exactly code * x * 2^-96.
+// 32c + 4t + i holds weight 64c + 4t + i in its low nibble (sub-block 2c) and
+// 64c + 32 + 4t + i in its high nibble (sub-block 2c+1).
 struct SliceQ4 {
-    u64 xp[4][8];      // [pair k][position i] = (x' of word 2k, x' of word 2k+1)
-    float s_lo, s_hi;  // sums of x over sub-blocks 2c and 2c+1 (unscaled)
+    uint32_t lo[3][8];  // [digit][word t]: digits of X at weights 64c + 4t + i, byte i
+    uint32_t hi[3][8];  // the same for weights 64c + 32 + 4t + i
+    float s_lo, s_hi;   // sums of x over sub-blocks 2c and 2c+1 (unscaled)
+    float inv;          // 2^-e
 };
 
 __device__ __forceinline__ void load_slice_q4(SliceQ4& s, const float* x, int b, int c) {
     const float* xb = x + b * kQK + 64 * c;
-    constexpr float sc[8] = {0x1p53f, 0x1p49f, 0x1p45f, 0x1p41f, 0x1p37f, 0x1p45f, 0x1p41f, 0x1p37f};
-    // weight offset of word t, position i (lo: 4t + byte; hi: 32 + 4t + byte)
-    float slo = 0.0f, shi = 0.0f;
+    float v[64];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        // positions of word t: lo byte0, hi byte0, lo byte1, hi byte1, ... (lo at 4t + j, hi at 32 + 4t + j)
-        const float4 l0 = __ldg(reinterpret_cast<const float4*>(xb + 8 * k));
-        const float4 h0 = __ldg(reinterpret_cast<const float4*>(xb + 32 + 8 * k));
-        const float4 l1 = __ldg(reinterpret_cast<const float4*>(xb + 8 * k + 4));
-        const float4 h1 = __ldg(reinterpret_cast<const float4*>(xb + 32 + 8 * k + 4));
-        const float v0[8] = {l0.x, h0.x, l0.y, h0.y, l0.z, h0.z, l0.w, h0.w};
-        const float v1[8] = {l1.x, h1.x, l1.y, h1.y, l1.z, h1.z, l1.w, h1.w};
-#pragma unroll
-        for (int i = 0; i < 8; ++i) s.xp[k][i] = f2_bits(v0[i] * sc[i], v1[i] * sc[i]);
-        slo += ((v0[0] + v0[2]) + (v0[4] + v0[6])) + ((v1[0] + v1[2]) + (v1[4] + v1[6]));
-        shi += ((v0[1] + v0[3]) + (v0[5] + v0[7])) + ((v1[1] + v1[3]) + (v1[5] + v1[7]));
+    for (int q = 0; q < 16; ++q) {
+        const float4 f = __ldg(reinterpret_cast<const float4*>(xb + 4 * q));
+        v[4 * q + 0] = f.x;
+        v[4 * q + 1] = f.y;
+        v[4 * q + 2] = f.z;
+        v[4 * q + 3] = f.w;
     }
+    float m = 0.0f, slo = 0.0f, shi = 0.0f;
+#pragma unroll
+    for (int l = 0; l < 32; ++l) {
+        m = fmaxf(m, fmaxf(fabsf(v[l]), fabsf(v[32 + l])));
+        slo += v[l];
+        shi += v[32 + l];
+    }
+    const int e = slice_exponent(m);
+    const float p2e = pow2f(e);
+    s.inv = pow2f(-e);
     s.s_lo = slo;
     s.s_hi = shi;
+#pragma unroll
+    for (int t = 0; t < 8; ++t) {
+        int XL[4], XH[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            XL[i] = __float2int_rn(v[4 * t + i] * p2e);
+            XH[i] = __float2int_rn(v[32 + 4 * t + i] * p2e);
+        }
+        uint32_t wl[3], wh[3];
+        pack_digits(XL[0], XL[1], XL[2], XL[3], wl);
+        pack_digits(XH[0], XH[1], XH[2], XH[3], wh);
+#pragma unroll
+        for (int k = 0; k < 3; ++k) {
+            s.lo[k][t] = wl[k];
+            s.hi[k][t] = wh[k];
+        }
+    }
 }
 
 // Q6_K slice (b, c = 2h + j): weights 128h + 32g + 16j + l, g = 0..3,
 // l = 0..15 (sub-blocks 8h + 2g + j); word i of a code field covers
-// l = 4i..4i+3, words 2k, 2k+1 form pair k.  Six-bit codes are rebuilt four to
-// a word and used at bits 0, 8, 16 and (after a 16-bit shift) 8, so the slice
-// holds x * 2^(53 - p) with p = 0, 8, 16, 8.
+// l = 4i..4i+3, or l = 4i-2..4i+1 (mod 16) when the block is rotated.
 struct SliceQ6 {
-    u64 xp[2][4][4];   // [pair k][group g][byte jj]
-    float s_neg32[4];  // -32 * sum of x over sub-block 8h + 2g + j
+    uint32_t x[4][3][4];  // [group g][digit][word i]
+    int neg32[4][3];      // -32 * sum of digit k of X over sub-block 8h + 2g + j
+    float inv;            // 2^-e
 };
 
 // rot: the thread's blocks start 2 bytes past a word boundary.  Their code
 // fields are read as aligned words W0..W4 around the field; W1..W3 hold field
 // bytes 2..13 and one byte permute folds W4 (bytes 14, 15) and W0 (bytes 0, 1)
-// into the first word, so word i of the field holds bytes lmap[i][0..3].
-__device__ __forceinline__ int q6_lmap(bool rot, int i, int jj) {
-    if (!rot) return 4 * i + jj;
-    if (i == 0) return jj < 2 ? 14 + jj : jj - 2;
-    return 4 * i - 2 + jj;
-}
-
+// into the first word, so word i of the field holds bytes 4i-2..4i+1 (mod 16)
+// and the slice's digit words are rotated the same way.
 __device__ __forceinline__ void load_slice_q6(SliceQ6& s, const float* x, int b, int c, bool rot) {
     const int h = c >> 1, j = c & 1;
-    constexpr float sc[4] = {0x1p53f, 0x1p45f, 0x1p37f, 0x1p45f};
+    float v[4][16];
+    float m = 0.0f;
 #pragma unroll
     for (int g = 0; g < 4; ++g) {
         const float* xg = x + b * kQK + 128 * h + 32 * g + 16 * j;
-        float v[16];
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
             const float4 f = __ldg(reinterpret_cast<const float4*>(xg + 4 * q));
-            v[4 * q + 0] = f.x;
-            v[4 * q + 1] = f.y;
-            v[4 * q + 2] = f.z;
-            v[4 * q + 3] = f.w;
+            v[g][4 * q + 0] = f.x;
+            v[g][4 * q + 1] = f.y;
+            v[g][4 * q + 2] = f.z;
+            v[g][4 * q + 3] = f.w;
         }
-        float sum = 0.0f;
 #pragma unroll
-        for (int l = 0; l < 16; ++l) sum += v[l];
-        s.s_neg32[g] = -32.0f * sum;
+        for (int l = 0; l < 16; ++l) m = fmaxf(m, fabsf(v[g][l]));
+    }
+    const int e = slice_exponent(m);
+    const float p2e = pow2f(e);
+    s.inv = pow2f(-e);
+    // a rotated word i holds bytes 4i - 2 .. 4i + 1 (mod 16) of the field
+    const uint32_t rsel = rot ? 0x5432u : 0x7654u;
 #pragma unroll
-        for (int k = 0; k < 2; ++k)
+    for (int g = 0; g < 4; ++g) {
+        uint32_t D[4][3];
 #pragma unroll
-            for (int jj = 0; jj < 4; ++jj)
-                s.xp[k][g][jj] = f2_bits(v[q6_lmap(rot, 2 * k, jj)] * sc[jj], v[q6_lmap(rot, 2 * k + 1, jj)] * sc[jj]);
+        for (int i = 0; i < 4; ++i)
+            pack_digits(__float2int_rn(v[g][4 * i] * p2e), __float2int_rn(v[g][4 * i + 1] * p2e),
+                        __float2int_rn(v[g][4 * i + 2] * p2e), __float2int_rn(v[g][4 * i + 3] * p2e), D[i]);
+        int sum[3] = {0, 0, 0};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            sum[0] = dp4a_uu(D[i][0], 0x01010101u, sum[0]);
+            sum[1] = dp4a_uu(D[i][1], 0x01010101u, sum[1]);
+            sum[2] = dp4a_us(0x01010101u, D[i][2], sum[2]);
+        }
+#pragma unroll
+        for (int k = 0; k < 3; ++k) {
+            s.neg32[g][k] = -32 * sum[k];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) s.x[g][k][i] = __byte_perm(D[(i + 3) & 3][k], D[i][k], rsel);
+        }
     }
 }
 
 // ------------------------------------------------ rows x one slice (dot)
 // NR independent weight rows (two matrices, or two rows of one) against the
-// same input slice: the streams are interleaved so each warp has 2*NR
-// independent accumulator chains in flight.
+// same input slice, interleaved so each warp has several independent dp4a
+// chains in flight.
 
 // Q4_K: out[r] = sum over the slice's 64 weights of w * x, with
-// w = d*sc_j*q - dmin*m_j (j = 2c, 2c+1).
+// w = d*sc_j*q - dmin*m_j (j = 2c, 2c+1).  Low nibbles are masked in place
+// as the bytes q; high nibbles are masked in place too, as the bytes 16q,
+// and their scale carries the 1/16.
 template <int NR>
 __device__ __forceinline__ void dot_q4(const SliceQ4& s, const uint8_t* const* blk, int c,
                                        uint32_t sel_lo, uint32_t sel_hi, float* out) {
     uint4 hd[NR];
-    u64 P4[NR][4];
+    uint32_t W[NR][8];
 #pragma unroll
     for (int r = 0; r < NR; ++r) {
         hd[r] = *reinterpret_cast<const uint4*>(blk[r]);
-        const ulonglong2 qa = *reinterpret_cast<const ulonglong2*>(blk[r] + 16 + 32 * c);
-        const ulonglong2 qb = *reinterpret_cast<const ulonglong2*>(blk[r] + 32 + 32 * c);
-        P4[r][0] = qa.x;
-        P4[r][1] = qa.y;
-        P4[r][2] = qb.x;
-        P4[r][3] = qb.y;
+        const uint4 qa = *reinterpret_cast<const uint4*>(blk[r] + 16 + 32 * c);
+        const uint4 qb = *reinterpret_cast<const uint4*>(blk[r] + 32 + 32 * c);
+        W[r][0] = qa.x; W[r][1] = qa.y; W[r][2] = qa.z; W[r][3] = qa.w;
+        W[r][4] = qb.x; W[r][5] = qb.y; W[r][6] = qb.z; W[r][7] = qb.w;
     }
-    u64 A[NR], B[NR];  // pairs: sub-block 2c (low nibbles), 2c+1 (high nibbles)
+    int acc[NR][6];
 #pragma unroll
-    for (int r = 0; r < NR; ++r) A[r] = B[r] = 0;
+    for (int r = 0; r < NR; ++r)
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
+        for (int k = 0; k < 6; ++k) acc[r][k] = 0;
+#pragma unroll
+    for (int t = 0; t < 8; ++t) {
 #pragma unroll
         for (int r = 0; r < NR; ++r) {
-            const u64 P = P4[r][k];
-            const u64 V = P >> 12;
-            A[r] = fma2(P & rep(0xFu), s.xp[k][0], A[r]);
-            B[r] = fma2(P & rep(0xF0u), s.xp[k][1], B[r]);
-            A[r] = fma2(P & rep(0xF00u), s.xp[k][2], A[r]);
-            B[r] = fma2(P & rep(0xF000u), s.xp[k][3], B[r]);
-            A[r] = fma2(P & rep(0xF0000u), s.xp[k][4], A[r]);
-            B[r] = fma2(V & rep(0xF00u), s.xp[k][5], B[r]);
-            A[r] = fma2(V & rep(0xF000u), s.xp[k][6], A[r]);
-            B[r] = fma2(V & rep(0xF0000u), s.xp[k][7], B[r]);
+            const uint32_t ql = W[r][t] & 0x0F0F0F0Fu;
+            const uint32_t qh = W[r][t] & 0xF0F0F0F0u;
+            acc[r][0] = dp4a_uu(ql, s.lo[0][t], acc[r][0]);
+            acc[r][1] = dp4a_uu(ql, s.lo[1][t], acc[r][1]);
+            acc[r][2] = dp4a_us(ql, s.lo[2][t], acc[r][2]);
+            acc[r][3] = dp4a_uu(qh, s.hi[0][t], acc[r][3]);
+            acc[r][4] = dp4a_uu(qh, s.hi[1][t], acc[r][4]);
+            acc[r][5] = dp4a_us(qh, s.hi[2][t], acc[r][5]);
         }
     }
 #pragma unroll
     for (int r = 0; r < NR; ++r) {
+        // sum(q * X) over sub-block 2c, and 16 * sum(q * X) over sub-block 2c+1
+        const float flo = combine3(acc[r][0], acc[r][1], acc[r][2]);
+        const float fhi = combine3(acc[r][3], acc[r][4], acc[r][5]);
         // six-bit scales/mins of sub-blocks 0..3 (low bits) and 4..7 (split)
         const uint32_t scw = (c < 2) ? (hd[r].y & 0x3F3F3F3Fu)
                                      : ((hd[r].w & 0x0F0F0F0Fu) | ((hd[r].y >> 2) & 0x30303030u));
         const uint32_t mnw = (c < 2) ? (hd[r].z & 0x3F3F3F3Fu)
                                      : (((hd[r].w >> 4) & 0x0F0F0F0Fu) | ((hd[r].z >> 2) & 0x30303030u));
-        const float2 scm_lo = make_float2(byte_to_f(scw, sel_lo), byte_to_f(mnw, sel_lo));
-        const float2 scm_hi = make_float2(byte_to_f(scw, sel_hi), byte_to_f(mnw, sel_hi));
+        const float sc_lo = byte_to_f(scw, sel_lo);
+        const float sc_hi = byte_to_f16th(scw, sel_hi);  // sc / 16
+        const float2 mins = make_float2(byte_to_f(mnw, sel_lo), byte_to_f(mnw, sel_hi));
         const float d = h2f(hd[r].x), dmin = h2f(hd[r].x >> 16);
-        float2 T = __fmul2_rn(scm_lo, make_float2(lo_f(A[r]) + hi_f(A[r]), s.s_lo));
-        T = __ffma2_rn(scm_hi, make_float2(lo_f(B[r]) + hi_f(B[r]), s.s_hi), T);
-        out[r] = fmaf(d * kTwo96, T.x, -(dmin * T.y));
+        const float dot = fmaf(sc_lo, flo, sc_hi * fhi);
+        const float msum = fmaf(mins.x, s.s_lo, mins.y * s.s_hi);
+        out[r] = fmaf(d * s.inv, dot, -(dmin * msum));
     }
 }
 
-// Code-field loads.  kMode 0: the field is 4-byte aligned, words 2k, 2k+1
-// as one 64-bit pair.  kMode 1: the field sits 2 bytes past a word boundary
-// and the thread's input slice is rotated to match (see q6_lmap): pair 0 =
-// (bytes 14,15,0,1 ; W1), pair 1 = (W2 ; W3) of the aligned words W0..W4 from
-// p - 2.  kMode 2: 2 bytes past a boundary, words realigned by byte permutes
-// (rows whose alignment alternates).
+// Code-field loads.  kAlign: the field is 4-byte aligned.  kRotated: the
+// field sits 2 bytes past a word boundary and the thread's input slice is
+// rotated to match (load_slice_q6): word 0 = (bytes 14,15,0,1), words 1..3 =
+// the aligned words W1..W3 from p - 2.  kRealign: 2 bytes past a boundary,
+// words realigned by byte permutes (rows whose alignment alternates).
 constexpr int kAlign = 0, kRotated = 1, kRealign = 2;
 
 template <int kMode>
-__device__ __forceinline__ u64 lds_pair(const uint8_t* p, int k) {
+__device__ __forceinline__ void lds_field(const uint8_t* p, uint32_t* w4) {
     if constexpr (kMode == kAlign) {
-        const uint32_t* w = reinterpret_cast<const uint32_t*>(p) + 2 * k;
-        return (static_cast<u64>(w[1]) << 32) | w[0];
+        const uint32_t* w = reinterpret_cast<const uint32_t*>(p);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) w4[i] = w[i];
     } else if constexpr (kMode == kRotated) {
         const uint32_t* w = reinterpret_cast<const uint32_t*>(p - 2);
-        if (k == 0) {
-            const uint32_t c0 = __byte_perm(w[4], w[0], 0x7610u);
-            return (static_cast<u64>(w[1]) << 32) | c0;
-        }
-        return (static_cast<u64>(w[3]) << 32) | w[2];
+        w4[0] = __byte_perm(w[4], w[0], 0x7610u);
+        w4[1] = w[1];
+        w4[2] = w[2];
+        w4[3] = w[3];
     } else {
-        const uint32_t* w = reinterpret_cast<const uint32_t*>(p - 2) + 2 * k;
-        const uint32_t w0 = w[0], w1 = w[1], w2 = w[2];
-        return (static_cast<u64>(__byte_perm(w1, w2, 0x5432u)) << 32) | __byte_perm(w0, w1, 0x5432u);
+        const uint32_t* w = reinterpret_cast<const uint32_t*>(p - 2);
+        uint32_t a[5];
+#pragma unroll
+        for (int i = 0; i < 5; ++i) a[i] = w[i];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) w4[i] = __byte_perm(a[i], a[i + 1], 0x5432u);
     }
 }
 // 8 bytes (two words) at shared address p, aligned as above.
@@ -235,36 +305,44 @@ __device__ __forceinline__ uint2 lds_w2(const uint8_t* p) {
     }
 }
 
-// Q6_K: out[r] = sum over the slice of d*sc_s*(q-32) * x.  With rows of a
+// Q6_K: out[r] = sum over the slice of d*sc_s*(q-32) * x.  The six-bit codes
+// are rebuilt four to a word as the bytes q; the -32 offset enters as each
+// digit accumulator's start, -32 * (sum of that digit).  With rows of a
 // multiple of 4 bytes, even blocks start 4-byte aligned in the stage and odd
 // ones 2 bytes past a boundary (210-byte blocks).
 template <int NR, int kMode>
 __device__ __forceinline__ void dot_q6(const SliceQ6& s, const uint8_t* const* blk, int c,
                                        uint32_t sel_sc, float* out) {
     const int h = c >> 1, j = c & 1;
-    u64 acc[NR][4];
+    int acc[NR][4][3];
 #pragma unroll
     for (int r = 0; r < NR; ++r)
 #pragma unroll
-        for (int g = 0; g < 4; ++g) acc[r][g] = 0;
+        for (int g = 0; g < 4; ++g)
 #pragma unroll
-    for (int k = 0; k < 2; ++k) {
+            for (int k = 0; k < 3; ++k) acc[r][g][k] = s.neg32[g][k];
+    uint32_t A[NR][4], B[NR][4], H[NR][4];
+#pragma unroll
+    for (int r = 0; r < NR; ++r) {
+        lds_field<kMode>(blk[r] + 64 * h + 16 * j, A[r]);
+        lds_field<kMode>(blk[r] + 64 * h + 32 + 16 * j, B[r]);
+        lds_field<kMode>(blk[r] + 128 + 32 * h + 16 * j, H[r]);
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
 #pragma unroll
         for (int r = 0; r < NR; ++r) {
-            const u64 A = lds_pair<kMode>(blk[r] + 64 * h + 16 * j, k);
-            const u64 B = lds_pair<kMode>(blk[r] + 64 * h + 32 + 16 * j, k);
-            const u64 H = lds_pair<kMode>(blk[r] + 128 + 32 * h + 16 * j, k);
-            u64 Q[4];
-            Q[0] = (A & rep(0x0F0F0F0Fu)) | ((H & rep(0x03030303u)) << 4);
-            Q[1] = (B & rep(0x0F0F0F0Fu)) | ((H & rep(0x0C0C0C0Cu)) << 2);
-            Q[2] = ((A >> 4) & rep(0x0F0F0F0Fu)) | (H & rep(0x30303030u));
-            Q[3] = ((B >> 4) & rep(0x0F0F0F0Fu)) | ((H >> 2) & rep(0x30303030u));
+            const uint32_t a = A[r][i], bq = B[r][i], hq = H[r][i];
+            uint32_t Q[4];
+            Q[0] = (a & 0x0F0F0F0Fu) | ((hq & 0x03030303u) << 4);
+            Q[1] = (bq & 0x0F0F0F0Fu) | ((hq & 0x0C0C0C0Cu) << 2);
+            Q[2] = ((a >> 4) & 0x0F0F0F0Fu) | (hq & 0x30303030u);
+            Q[3] = ((bq >> 4) & 0x0F0F0F0Fu) | ((hq >> 2) & 0x30303030u);
 #pragma unroll
             for (int g = 0; g < 4; ++g) {
-                acc[r][g] = fma2(Q[g] & rep(0x3Fu), s.xp[k][g][0], acc[r][g]);
-                acc[r][g] = fma2(Q[g] & rep(0x3F00u), s.xp[k][g][1], acc[r][g]);
-                acc[r][g] = fma2(Q[g] & rep(0x3F0000u), s.xp[k][g][2], acc[r][g]);
-                acc[r][g] = fma2((Q[g] >> 16) & rep(0x3F00u), s.xp[k][g][3], acc[r][g]);
+                acc[r][g][0] = dp4a_uu(Q[g], s.x[g][0][i], acc[r][g][0]);
+                acc[r][g][1] = dp4a_uu(Q[g], s.x[g][1][i], acc[r][g][1]);
+                acc[r][g][2] = dp4a_us(Q[g], s.x[g][2][i], acc[r][g][2]);
             }
         }
     }
@@ -278,17 +356,18 @@ __device__ __forceinline__ void dot_q6(const SliceQ6& s, const uint8_t* const* b
 #pragma unroll
         for (int g = 0; g < 4; ++g) {
             const float scg = byte_to_f(sc4, 0x7540u | g) - 128.0f;
-            const float tg = fmaf(lo_f(acc[r][g]) + hi_f(acc[r][g]), kTwo96, s.s_neg32[g]);
-            sum = fmaf(scg, tg, sum);
+            // sum((q - 32) * X) over the sub-block
+            sum = fmaf(scg, combine3(acc[r][g][0], acc[r][g][1], acc[r][g][2]), sum);
         }
-        out[r] = h2f(dbits) * sum;
+        out[r] = (h2f(dbits) * s.inv) * sum;
     }
 }
 
 // -------------------------------------------------------------- the kernel
 // Warp roles: warps 0..nconsumer-1 compute (each thread one input slice and a
-// row group); the last warp produces (TMA issue, per-stage row reduction and
-// output).  Stage buffer s has a "full" mbarrier (producer arrival + TMA
+// row group); the next warp issues the bulk copies; the last two reduce the
+// partials of alternate stages per row and write the outputs (epilogue).
+// Stage buffer s has a "full" mbarrier (producer arrival + TMA
 // transaction bytes) and an "empty" mbarrier (one arrival per consumer warp
 // once it has read the stage and stored its partials).  No block-wide barrier
 // runs per stage.
@@ -312,7 +391,6 @@ __global__ void __launch_bounds__(512, 1) mv1_kernel(const Mv1Args p) {
     uint64_t* empty = full + 8;
     uint64_t* pfull = full + 16;
     uint64_t* reduced = full + 32;
-    uint64_t* xready = full + 48;
     float* red = reinterpret_cast<float*>(smem + 512);
     int* flag = reinterpret_cast<int*>(smem + 512 + 64 * 4);
     float* part = reinterpret_cast<float*>(smem + p.part_off);
@@ -335,7 +413,6 @@ __global__ void __launch_bounds__(512, 1) mv1_kernel(const Mv1Args p) {
             mbar_init(&pfull[i], static_cast<uint32_t>(ncw));
             mbar_init(&reduced[i], 1);
         }
-        mbar_init(xready, static_cast<uint32_t>(ncw));
         fence_mbar_init();
     }
     __syncthreads();
@@ -343,7 +420,9 @@ __global__ void __launch_bounds__(512, 1) mv1_kernel(const Mv1Args p) {
     bool ok = true;
     if (warp == ncw) {
         // ---------------------------------------------------------- TMA warp
-        // Bulk copies of stage k (all matrices) into buffer k % NS.
+        // Bulk copies of stage k (all matrices) into buffer k % NS.  Each
+        // weight byte is read once per call: evict-first in L2.
+        const uint64_t wpol = l2_policy_evict_first();
         auto issue = [&](int k) {
             const int buf = k % NS;
             const int64_t lr0 = static_cast<int64_t>(k) * RS;
@@ -374,17 +453,16 @@ __global__ void __launch_bounds__(512, 1) mv1_kernel(const Mv1Args p) {
             for (int m = 0; m < NMAT; ++m) {
                 if (sizes[m] == 0) continue;
                 uint8_t* dst = stage_base + (static_cast<size_t>(buf) * NMAT + m) * stage_bytes;
-                tma_load_1d(dst, srcs[m], sizes[m], &full[buf]);
+                tma_load_1d_hint(dst, srcs[m], sizes[m], &full[buf], wpol);
             }
         };
-        // The weight copies start only once every consumer warp holds its
-        // input slice: x must not queue behind a burst of weight traffic.
-        pdl_launch_dependents();
-        pdl_wait();
-        ok = mbar_wait_bounded(xready, 0, &g_device_status, kDevStatusWaitTimeout);
-        if (ok && lane == 0)
+        // The weights do not depend on the previous kernel: the first NS
+        // stages are requested at once, so the stream overlaps the previous
+        // kernel's tail and this block's own input-slice set-up.
+        if (lane == 0)
             for (int k = 0; k < min(NS, nstages); ++k) issue(k);
         __syncwarp();
+        pdl_launch_dependents();
         for (int k = 0; k + NS < nstages && ok; ++k) {
             // buffer k % NS is free once every consumer warp has read stage k;
             // the partial slot of stage k + NS once stage k - NS is reduced
@@ -397,12 +475,14 @@ __global__ void __launch_bounds__(512, 1) mv1_kernel(const Mv1Args p) {
             if (ok && lane == 0) issue(kp);
             __syncwarp();
         }
-    } else if (warp == ncw + 1) {
-        // ------------------------------------------------------ reducer warp
+    } else if (warp > ncw) {
+        // ----------------------------------------------------- reducer warps
+        // Two warps take alternate stages (the 2*NS partial slots alternate
+        // with them, so each slot has one reducer).
         pdl_launch_dependents();
         pdl_wait();  // outputs of the previous kernel are complete before ours are written
         const int n4 = nbc / 4;
-        for (int k = 0; k < nstages; ++k) {
+        for (int k = warp - ncw - 1; k < nstages; k += 2) {
             const int slot = k % NP;
             if (ok) ok = mbar_wait_bounded(&pfull[slot], static_cast<uint32_t>((k / NP) & 1),
                                            &g_device_status, kDevStatusWaitTimeout);
@@ -483,8 +563,6 @@ __global__ void __launch_bounds__(512, 1) mv1_kernel(const Mv1Args p) {
             if constexpr (QT == MUSER_Q4_K) load_slice_q4(sl, p.x, b, c);
             else load_slice_q6(sl, p.x, b, c, parity_split && (b & 1));
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(xready);
         const uint32_t sel_lo = 0x7540u | static_cast<uint32_t>(2 * (c & 1));
         const uint32_t sel_hi = 0x7540u | static_cast<uint32_t>(2 * (c & 1) + 1);
         const uint32_t jq = static_cast<uint32_t>(c & 1);
@@ -620,7 +698,7 @@ unsigned read_device_status(bool reset) {
 }
 
 // ------------------------------------------------------------------ launch
-constexpr int kMaxConsumerThreads = 448;  // + the TMA and reducer warps = 512 threads
+constexpr int kMaxConsumerThreads = 416;  // + the TMA warp and two reducer warps = 512 threads
 
 bool mv1_supported(int qtype, int64_t cols) {
     (void)qtype;
@@ -649,7 +727,7 @@ static int launch_mv1_t(Mv1Args a, cudaStream_t stream) {
     }
     a.G = std::max(1, kMaxConsumerThreads / a.TG);
     a.nconsumer_warps = (a.TG * a.G + 31) / 32;
-    const int threads = (a.nconsumer_warps + 2) * 32;
+    const int threads = (a.nconsumer_warps + 3) * 32;
     // rows per stage: a multiple of G, stage near 32 KB over all matrices
     const int64_t per_row = rowbytes * NMAT;
     const int64_t unit = static_cast<int64_t>(a.G) * (NMAT == 1 ? 2 : 1);  // one matrix: rows go in pairs

@@ -184,6 +184,15 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
         "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
         : "memory");
 }
+// The same with an L2 cache policy (the weight stream: evict-first).
+__device__ __forceinline__ void tma_load_2d_hint(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar,
+                                                 uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
 
 // ------------------------------------------------------ Q4_K (144-byte block)
 // Scale and min (6 bits each) of sub-block j from the packed bytes s[0..11],
@@ -705,6 +714,8 @@ __global__ void __launch_bounds__(mvt_threads(MULTI), 1)
     if (warp == kTmaWarp) {
         // ------------------------------------------------ bulk-copy warp
         // Weights do not depend on the previous kernel: no PDL wait here.
+        // Each weight byte is read once per call: evict-first in L2.
+        const uint64_t wpol = l2_policy_evict_first();
         UnitIter<QT> it(u0, nsb);
         Ring rs;
         for (int i = 0; i < nunits && ok; ++i, it.next(), rs.next(NS)) {
@@ -717,14 +728,15 @@ __global__ void __launch_bounds__(mvt_threads(MULTI), 1)
                 mbar_arrive_expect_tx(&full[s], kStage);
                 if constexpr (NMAT == 2) {
                     // gate rows to lanes 0..63, up rows to lanes 64..127
-                    tma_load_2d(dst, &map0, sb * kBlk, t * 64, &full[s]);
-                    tma_load_2d(dst + 64 * RS, &map1, sb * kBlk, t * 64, &full[s]);
+                    tma_load_2d_hint(dst, &map0, sb * kBlk, t * 64, &full[s], wpol);
+                    tma_load_2d_hint(dst + 64 * RS, &map1, sb * kBlk, t * 64, &full[s], wpol);
                 } else if constexpr (QT == MUSER_Q4_K) {
-                    tma_load_2d(dst, &map0, sb * kBlk, t * 128, &full[s]);
+                    tma_load_2d_hint(dst, &map0, sb * kBlk, t * 128, &full[s], wpol);
                 } else {
                     // class t % P of block t / P: box from the 16-byte boundary below the block
                     const int64_t off = static_cast<int64_t>(t % p.P) * rowbytes + static_cast<int64_t>(sb) * kBlk;
-                    tma_load_2d(dst, &map0, static_cast<int>(off & ~static_cast<int64_t>(15)), (t / p.P) * 128, &full[s]);
+                    tma_load_2d_hint(dst, &map0, static_cast<int>(off & ~static_cast<int64_t>(15)), (t / p.P) * 128,
+                                     &full[s], wpol);
                 }
             }
             __syncwarp();
