@@ -114,9 +114,29 @@ __device__ __forceinline__ float byte_to_f(uint32_t word, uint32_t sel_with_magi
     return __uint_as_float(__byte_perm(word, 0x4B000000u, sel_with_magic)) - 8388608.0f;
 }
 
+// 16-byte shared-memory store (p 16-byte aligned, in shared memory).
+__device__ __forceinline__ void sts_float4(void* p, float4 v) {
+    asm volatile("st.shared.v4.f32 [%0], {%1,%2,%3,%4};" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(p))),
+                 "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w)
+                 : "memory");
+}
+// Barrier `id` (1..15) over the first `nthreads` threads of the block (a
+// multiple of 32; every warp taking part calls it).
+__device__ __forceinline__ void named_barrier_sync(int id, int nthreads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
 // ---------------------------------------------------------- TMA / mbarrier
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+// 16-byte shared-memory load (p 16-byte aligned, in shared memory).
+__device__ __forceinline__ float4 lds_float4(const void* p) {
+    float4 v;
+    asm volatile("ld.shared.v4.f32 {%0,%1,%2,%3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(smem_u32(p)));
+    return v;
 }
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));

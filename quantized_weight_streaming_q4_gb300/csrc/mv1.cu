@@ -101,12 +101,12 @@ struct SliceQ4 {
     float inv;          // 2^-e
 };
 
-__device__ __forceinline__ void load_slice_q4(SliceQ4& s, const float* x, int b, int c) {
-    const float* xb = x + b * kQK + 64 * c;
+// xs: the slice's 64 inputs in shared memory (its slot, see XSlots).
+__device__ __forceinline__ void load_slice_q4(SliceQ4& s, const float* xs) {
     float v[64];
 #pragma unroll
     for (int q = 0; q < 16; ++q) {
-        const float4 f = __ldg(reinterpret_cast<const float4*>(xb + 4 * q));
+        const float4 f = lds_float4(xs + 4 * q);
         v[4 * q + 0] = f.x;
         v[4 * q + 1] = f.y;
         v[4 * q + 2] = f.z;
@@ -157,16 +157,15 @@ struct SliceQ6 {
 // bytes 2..13 and one byte permute folds W4 (bytes 14, 15) and W0 (bytes 0, 1)
 // into the first word, so word i of the field holds bytes 4i-2..4i+1 (mod 16)
 // and the slice's digit words are rotated the same way.
-__device__ __forceinline__ void load_slice_q6(SliceQ6& s, const float* x, int b, int c, bool rot) {
-    const int h = c >> 1, j = c & 1;
+// xs: the slice's four 16-input groups in shared memory, group g at 16g.
+__device__ __forceinline__ void load_slice_q6(SliceQ6& s, const float* xs, bool rot) {
     float v[4][16];
     float m = 0.0f;
 #pragma unroll
     for (int g = 0; g < 4; ++g) {
-        const float* xg = x + b * kQK + 128 * h + 32 * g + 16 * j;
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-            const float4 f = __ldg(reinterpret_cast<const float4*>(xg + 4 * q));
+            const float4 f = lds_float4(xs + 16 * g + 4 * q);
             v[g][4 * q + 0] = f.x;
             v[g][4 * q + 1] = f.y;
             v[g][4 * q + 2] = f.z;
@@ -363,6 +362,41 @@ __device__ __forceinline__ void dot_q6(const SliceQ6& s, const uint8_t* const* b
     }
 }
 
+// ---------------------------------------------------------- input slots
+// Row-group thread idx owns slice (b, c).  Q6_K with an even number of
+// super-blocks per row: the first half of a row group's slices take the even
+// super-blocks, the second half (from thread HP) the odd ones, so whole warps
+// share one block alignment (even blocks start 4-byte aligned in the stage,
+// odd ones 2 bytes past a boundary); threads in the padding idle.  Returns
+// whether idx owns a slice.
+__device__ __forceinline__ bool slice_of(int idx, int nbc, bool parity_split, int HP, int& b, int& c) {
+    if (parity_split) {
+        const bool odd = idx >= HP;
+        const int i2 = odd ? idx - HP : idx;
+        b = 2 * (i2 >> 2) + (odd ? 1 : 0);
+        c = i2 & 3;
+        return i2 < nbc / 2;
+    }
+    b = idx >> 2;
+    c = idx & 3;
+    return idx < nbc;
+}
+// The consumer warps copy x into shared memory with coalesced float4 loads,
+// each slice's 64 inputs into a slot of its own (slot idx at idx * kXSlot
+// bytes; Q6_K groups g at 64g).  The 16-byte pad makes a quarter warp's float4
+// reads of consecutive slots fall in distinct banks.  (Read straight from
+// global memory, every warp-wide load of a slice touched 32 lines.)
+constexpr int kXSlot = 272;
+// Byte offset in the slots of x's float4 number i.
+__device__ __forceinline__ int xslot_offset(int i, bool q4, bool parity_split, int HP) {
+    if (q4) return (i >> 4) * kXSlot + (i & 15) * 16;  // slot 4b + c, chunk q
+    const int b = i >> 6, f = (i & 63) * 4;              // float f of super-block b
+    const int h = f >> 7, g = (f >> 5) & 3, j = (f >> 4) & 1, l4 = (f >> 2) & 3;
+    const int c = 2 * h + j;
+    const int idx = parity_split ? ((b & 1) ? HP : 0) + 4 * (b >> 1) + c : 4 * b + c;
+    return idx * kXSlot + 64 * g + 16 * l4;
+}
+
 // -------------------------------------------------------------- the kernel
 // Warp roles: warps 0..nconsumer-1 compute (each thread one input slice and a
 // row group); the next warp issues the bulk copies; the last two reduce the
@@ -385,15 +419,20 @@ __global__ void __launch_bounds__(512, 1) mv1_kernel(const Mv1Args p) {
     const int nloc = static_cast<int>(r1 - r0);
     const int nstages = (nloc + RS - 1) / RS;
 
-    // shared layout: barriers [full 8][empty 8][pfull 16][reduced 16] | red 64 | flag |
-    // partial slots (2*NS) | stage buffers (NS)
+    // shared layout: barriers [full 8][empty 8][pfull 16][reduced 16][-][xready] |
+    // red 64 | flag | partial slots (2*NS) | stage buffers (NS); the input
+    // slots overlay the top of the stage buffers (from p.x_off) until every
+    // consumer holds its slice.
     uint64_t* full = reinterpret_cast<uint64_t*>(smem);
     uint64_t* empty = full + 8;
     uint64_t* pfull = full + 16;
     uint64_t* reduced = full + 32;
+    uint64_t* xready = full + 49;  // every consumer warp holds its slice
     float* red = reinterpret_cast<float*>(smem + 512);
     int* flag = reinterpret_cast<int*>(smem + 512 + 64 * 4);
     float* part = reinterpret_cast<float*>(smem + p.part_off);
+    uint8_t* xslots = smem + p.x_off;
+    const bool parity_split = (QT == MUSER_Q6_K) && (nsb % 2 == 0);
     uint8_t* stage_base = smem + p.stage_off;
     const uint32_t stage_bytes = p.stage_bytes;  // per matrix
     const int part_stride = NMAT * RS * nbc;
@@ -413,6 +452,7 @@ __global__ void __launch_bounds__(512, 1) mv1_kernel(const Mv1Args p) {
             mbar_init(&pfull[i], static_cast<uint32_t>(ncw));
             mbar_init(&reduced[i], 1);
         }
+        mbar_init(xready, static_cast<uint32_t>(ncw));
         fence_mbar_init();
     }
     __syncthreads();
@@ -456,13 +496,20 @@ __global__ void __launch_bounds__(512, 1) mv1_kernel(const Mv1Args p) {
                 tma_load_1d_hint(dst, srcs[m], sizes[m], &full[buf], wpol);
             }
         };
-        // The weights do not depend on the previous kernel: the first NS
-        // stages are requested at once, so the stream overlaps the previous
-        // kernel's tail and this block's own input-slice set-up.
+        // The weights do not depend on the previous kernel: the stages whose
+        // buffers lie below the input slots are requested at once, so the
+        // stream overlaps the previous kernel's tail and the slice set-up.
+        const int nfirst = min(NS, nstages);
+        const int early = min(p.early_stages, nfirst);
         if (lane == 0)
-            for (int k = 0; k < min(NS, nstages); ++k) issue(k);
+            for (int k = 0; k < early; ++k) issue(k);
         __syncwarp();
         pdl_launch_dependents();
+        // The rest of the first NS stages once the slots are free again.
+        ok = mbar_wait_bounded(xready, 0, &g_device_status, kDevStatusWaitTimeout);
+        if (ok && lane == 0)
+            for (int k = early; k < nfirst; ++k) issue(k);
+        __syncwarp();
         for (int k = 0; k + NS < nstages && ok; ++k) {
             // buffer k % NS is free once every consumer warp has read stage k;
             // the partial slot of stage k + NS once stage k - NS is reduced
@@ -529,40 +576,32 @@ __global__ void __launch_bounds__(512, 1) mv1_kernel(const Mv1Args p) {
             if (lane == 0) mbar_arrive(&reduced[slot]);
         }
     } else {
-        // Thread -> (row group g, slice (b, c)).  Q6_K with an even number of
-        // super-blocks per row: the first half of a row group's slices take the
-        // even super-blocks, the second half the odd ones, so whole warps share
-        // one block alignment (even blocks start 4-byte aligned in the stage,
-        // odd ones 2 bytes past a boundary).
-        // A row group spans p.TG threads; with the split, the odd half starts
-        // at thread p.HP of the group (a warp boundary when it fits), and
-        // threads in the padding between the halves idle.
+        // Thread -> (row group g, slice (b, c) of slice_of); a row group spans
+        // p.TG threads.
         const int g = tid / p.TG;
         const int idx = tid - g * p.TG;
         int b, c;
-        bool active = g < G;
-        const bool parity_split = (QT == MUSER_Q6_K) && (nsb % 2 == 0);
-        if (parity_split) {
-            const int half = nbc / 2;
-            const bool odd = idx >= p.HP;
-            const int i2 = odd ? idx - p.HP : idx;
-            if (i2 >= half) active = false;
-            b = 2 * (i2 >> 2) + (odd ? 1 : 0);
-            c = i2 & 3;
-            if (!active) b = c = 0;
-        } else {
-            b = idx >> 2;
-            c = idx & 3;
-        }
+        bool active = slice_of(idx, nbc, parity_split, p.HP, b, c) && g < G;
+        if (!active) b = c = 0;
         const int bc = b * 4 + c;  // partial slot of this slice
         pdl_launch_dependents();
-        pdl_wait();  // x is the previous kernel's output
         using Slice = typename std::conditional<QT == MUSER_Q4_K, SliceQ4, SliceQ6>::type;
         Slice sl;
-        if (active) {
-            if constexpr (QT == MUSER_Q4_K) load_slice_q4(sl, p.x, b, c);
-            else load_slice_q6(sl, p.x, b, c, parity_split && (b & 1));
+        pdl_wait();  // x is the previous kernel's output
+        {
+            const float4* x4 = reinterpret_cast<const float4*>(p.x);
+            const int n4 = nbc * 16;
+            for (int i = tid; i < n4; i += ncw * 32)
+                sts_float4(xslots + xslot_offset(i, QT == MUSER_Q4_K, parity_split, p.HP), __ldg(x4 + i));
         }
+        named_barrier_sync(1, ncw * 32);  // the consumer warps only
+        if (active) {
+            const float* xs = reinterpret_cast<const float*>(xslots + idx * kXSlot);
+            if constexpr (QT == MUSER_Q4_K) load_slice_q4(sl, xs);
+            else load_slice_q6(sl, xs, parity_split && (b & 1));
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(xready);
         const uint32_t sel_lo = 0x7540u | static_cast<uint32_t>(2 * (c & 1));
         const uint32_t sel_hi = 0x7540u | static_cast<uint32_t>(2 * (c & 1) + 1);
         const uint32_t jq = static_cast<uint32_t>(c & 1);
@@ -749,6 +788,14 @@ static int launch_mv1_t(Mv1Args a, cudaStream_t stream) {
     a.ns = ns;
     a.stage_off = static_cast<int>((a.part_off + 2 * ns * part_per_stage + 127) / 128 * 128);
     const size_t smem = static_cast<size_t>(a.stage_off + ns * per_stage);
+    // input slots at the top of the stage buffers; the buffers below them
+    // take the first weight copies
+    const int64_t xbytes = (static_cast<int64_t>(a.TG) * kXSlot + 127) / 128 * 128;
+    if (xbytes > ns * per_stage)
+        return set_error(MUSER_ERR_UNSUPPORTED, "mv1: input slots (%lld B) exceed the stage buffers",
+                         (long long)xbytes);
+    a.x_off = static_cast<int>(static_cast<int64_t>(smem) - xbytes);
+    a.early_stages = static_cast<int>((a.x_off - a.stage_off) / per_stage);
     auto kern = mv1_kernel<QT, NMAT, EPI>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
