@@ -661,21 +661,30 @@ __global__ void __launch_bounds__(512, 1) mv1_kernel(const Mv1Args p) {
         };
         const bool rows4 = (rowbytes & 3u) == 0;
         const bool aligned = (b % 2 == 0);
+        // Ring positions advance by counters (no division per stage).  A
+        // stage's copy starts at the 16-byte boundary below its first row, so
+        // the rows sit `delta` bytes into the buffer; delta advances by
+        // RS * rowbytes mod 16 per stage.
+        int buf = 0, slot = 0, rows_left = nloc;
+        uint32_t phase = 0;
+        uint32_t delta[NMAT];
+        const uint8_t* sbase[NMAT];
+        const uint32_t dstep = (static_cast<uint32_t>(RS) * rowbytes) & 15u;
+#pragma unroll
+        for (int m = 0; m < NMAT; ++m) {
+            delta[m] = static_cast<uint32_t>((reinterpret_cast<uintptr_t>(p.W[m]) +
+                                              static_cast<uint64_t>(r0) * rowbytes) & 15u);
+            sbase[m] = stage_base + m * stage_bytes + slice_off;
+        }
+        const uint32_t buf_stride = NMAT * stage_bytes;
         for (int k = 0; k < nstages; ++k) {
-            const int buf = k % NS;
-            const int64_t lr0 = static_cast<int64_t>(k) * RS;
-            const int rows_here = static_cast<int>(min(static_cast<int64_t>(RS), nloc - lr0));
-            if (ok) ok = mbar_wait_bounded(&full[buf], static_cast<uint32_t>((k / NS) & 1),
-                                           &g_device_status, kDevStatusWaitTimeout);
-            float* pk = part + (k % NP) * part_stride;
+            const int rows_here = min(RS, rows_left);
+            if (ok) ok = mbar_wait_bounded(&full[buf], phase, &g_device_status, kDevStatusWaitTimeout);
+            float* pk = part + slot * part_stride;
             if (active && ok) {
                 const uint8_t* sb[NMAT];
 #pragma unroll
-                for (int m = 0; m < NMAT; ++m) {
-                    const uint8_t* start = p.W[m] + (r0 + lr0) * static_cast<int64_t>(rowbytes);
-                    const uint32_t delta = static_cast<uint32_t>(reinterpret_cast<uintptr_t>(start) & 15);
-                    sb[m] = stage_base + (static_cast<uint32_t>(buf) * NMAT + m) * stage_bytes + delta + slice_off;
-                }
+                for (int m = 0; m < NMAT; ++m) sb[m] = sbase[m] + buf * buf_stride + delta[m];
                 if (QT == MUSER_Q6_K && !rows4) stage_any(sb, rows_here, pk);
                 else if (QT == MUSER_Q4_K || aligned) stage(std::true_type{}, sb, rows_here, pk);
                 else stage(std::false_type{}, sb, rows_here, pk);
@@ -683,8 +692,16 @@ __global__ void __launch_bounds__(512, 1) mv1_kernel(const Mv1Args p) {
             __syncwarp();
             if (lane == 0) {
                 mbar_arrive(&empty[buf]);
-                mbar_arrive(&pfull[k % NP]);
+                mbar_arrive(&pfull[slot]);
             }
+#pragma unroll
+            for (int m = 0; m < NMAT; ++m) delta[m] = (delta[m] + dstep) & 15u;
+            rows_left -= RS;
+            if (++buf == NS) {
+                buf = 0;
+                phase ^= 1u;
+            }
+            if (++slot == NP) slot = 0;
         }
     }
     ok = __syncthreads_and(ok);
