@@ -460,11 +460,10 @@ __global__ void __launch_bounds__(512, 1) mv1_kernel(const Mv1Args p) {
     bool ok = true;
     if (warp == ncw) {
         // ---------------------------------------------------------- TMA warp
-        // Bulk copies of stage k (all matrices) into buffer k % NS.  Each
-        // weight byte is read once per call: evict-first in L2.
+        // Bulk copies of stage k (all matrices) into buffer buf = k % NS.
+        // Each weight byte is read once per call: evict-first in L2.
         const uint64_t wpol = l2_policy_evict_first();
-        auto issue = [&](int k) {
-            const int buf = k % NS;
+        auto issue = [&](int k, int buf) {
             const int64_t lr0 = static_cast<int64_t>(k) * RS;
             const int64_t lr1 = min(static_cast<int64_t>(nloc), lr0 + RS);
             uint32_t total = 0;
@@ -502,25 +501,32 @@ __global__ void __launch_bounds__(512, 1) mv1_kernel(const Mv1Args p) {
         const int nfirst = min(NS, nstages);
         const int early = min(p.early_stages, nfirst);
         if (lane == 0)
-            for (int k = 0; k < early; ++k) issue(k);
+            for (int k = 0; k < early; ++k) issue(k, k);
         __syncwarp();
         pdl_launch_dependents();
         // The rest of the first NS stages once the slots are free again.
         ok = mbar_wait_bounded(xready, 0, &g_device_status, kDevStatusWaitTimeout);
         if (ok && lane == 0)
-            for (int k = early; k < nfirst; ++k) issue(k);
+            for (int k = early; k < nfirst; ++k) issue(k, k);
         __syncwarp();
+        // Buffer k % NS is free once every consumer warp has read stage k;
+        // the partial slot of stage k + NS once stage k - NS is reduced.
+        // Ring positions advance by counters.
+        int ebuf = 0, rslot = NS;
+        uint32_t ephase = 0, rphase = 0;
         for (int k = 0; k + NS < nstages && ok; ++k) {
-            // buffer k % NS is free once every consumer warp has read stage k;
-            // the partial slot of stage k + NS once stage k - NS is reduced
-            ok = mbar_wait_bounded(&empty[k % NS], static_cast<uint32_t>((k / NS) & 1),
-                                   &g_device_status, kDevStatusWaitTimeout);
+            ok = mbar_wait_bounded(&empty[ebuf], ephase, &g_device_status, kDevStatusWaitTimeout);
             const int kp = k + NS;
             if (ok && kp >= NP)
-                ok = mbar_wait_bounded(&reduced[kp % NP], static_cast<uint32_t>(((kp - NP) / NP) & 1),
-                                       &g_device_status, kDevStatusWaitTimeout);
-            if (ok && lane == 0) issue(kp);
+                ok = mbar_wait_bounded(&reduced[rslot], rphase, &g_device_status, kDevStatusWaitTimeout);
+            if (ok && lane == 0) issue(kp, ebuf);
             __syncwarp();
+            if (++ebuf == NS) {
+                ebuf = 0;
+                ephase ^= 1u;
+            }
+            if (++rslot == NP) rslot = 0;
+            if (kp >= NP && rslot == 0) rphase ^= 1u;
         }
     } else if (warp > ncw) {
         // ----------------------------------------------------- reducer warps
@@ -529,10 +535,10 @@ __global__ void __launch_bounds__(512, 1) mv1_kernel(const Mv1Args p) {
         pdl_launch_dependents();
         pdl_wait();  // outputs of the previous kernel are complete before ours are written
         const int n4 = nbc / 4;
+        int slot = warp - ncw - 1;  // k % NP (NP is even)
+        uint32_t sphase = 0;        // (k / NP) & 1
         for (int k = warp - ncw - 1; k < nstages; k += 2) {
-            const int slot = k % NP;
-            if (ok) ok = mbar_wait_bounded(&pfull[slot], static_cast<uint32_t>((k / NP) & 1),
-                                           &g_device_status, kDevStatusWaitTimeout);
+            if (ok) ok = mbar_wait_bounded(&pfull[slot], sphase, &g_device_status, kDevStatusWaitTimeout);
             if (!ok) break;
             const int64_t lr0 = static_cast<int64_t>(k) * RS;
             const int rows_here = static_cast<int>(min(static_cast<int64_t>(RS), nloc - lr0));
@@ -574,6 +580,11 @@ __global__ void __launch_bounds__(512, 1) mv1_kernel(const Mv1Args p) {
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&reduced[slot]);
+            slot += 2;
+            if (slot >= NP) {
+                slot -= NP;
+                sphase ^= 1u;
+            }
         }
     } else {
         // Thread -> (row group g, slice (b, c) of slice_of); a row group spans
