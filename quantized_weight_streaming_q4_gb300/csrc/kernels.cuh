@@ -28,8 +28,9 @@ struct Mv1Args {
     int HP;  // Q6_K parity split: first thread of the odd-block half
     uint32_t stage_bytes;
     int part_off, stage_off;
-    int x_off;         // input slots (shared memory offset)
-    int early_stages;  // stage buffers below the input slots
+    int x_off;  // input slots (shared memory offset)
+    int rot;    // stage buffers under the input slots; stage k uses buffer (k + rot) % ns
+    int lead;   // stages requested before the loads of x
 };
 bool mv1_supported(int qtype, int64_t cols);
 int launch_mv1(int qtype, int nmat, int epi, const Mv1Args& a, cudaStream_t s);

@@ -419,15 +419,18 @@ __global__ void __launch_bounds__(512, 1) mv1_kernel(const Mv1Args p) {
     const int nloc = static_cast<int>(r1 - r0);
     const int nstages = (nloc + RS - 1) / RS;
 
-    // shared layout: barriers [full 8][empty 8][pfull 16][reduced 16][-][xready] |
-    // red 64 | flag | partial slots (2*NS) | stage buffers (NS); the input
-    // slots overlay the top of the stage buffers (from p.x_off) until every
-    // consumer holds its slice.
+    // shared layout: barriers [full 8][empty 8][pfull 16][reduced 16][xissued][xready] |
+    // red 64 | flag | partial slots (2*NS) | stage buffers (NS).  The input
+    // slots overlay the partial slots and, when larger, the first p.rot stage
+    // buffers, until every consumer holds its slice; stage k therefore uses
+    // buffer (k + rot) % NS, so that the first NS - rot stages can be
+    // requested before the slots are free.
     uint64_t* full = reinterpret_cast<uint64_t*>(smem);
     uint64_t* empty = full + 8;
     uint64_t* pfull = full + 16;
     uint64_t* reduced = full + 32;
-    uint64_t* xready = full + 49;  // every consumer warp holds its slice
+    uint64_t* xissued = full + 48;  // every consumer warp has issued its loads of x
+    uint64_t* xready = full + 49;   // every consumer warp holds its slice
     float* red = reinterpret_cast<float*>(smem + 512);
     int* flag = reinterpret_cast<int*>(smem + 512 + 64 * 4);
     float* part = reinterpret_cast<float*>(smem + p.part_off);
@@ -452,6 +455,7 @@ __global__ void __launch_bounds__(512, 1) mv1_kernel(const Mv1Args p) {
             mbar_init(&pfull[i], static_cast<uint32_t>(ncw));
             mbar_init(&reduced[i], 1);
         }
+        mbar_init(xissued, static_cast<uint32_t>(ncw));
         mbar_init(xready, static_cast<uint32_t>(ncw));
         fence_mbar_init();
     }
@@ -498,21 +502,29 @@ __global__ void __launch_bounds__(512, 1) mv1_kernel(const Mv1Args p) {
         // The weights do not depend on the previous kernel: the stages whose
         // buffers lie below the input slots are requested at once, so the
         // stream overlaps the previous kernel's tail and the slice set-up.
+        // Requests queue in order: only p.lead stages go ahead of the loads
+        // of x, the rest of the free buffers follow them.
         const int nfirst = min(NS, nstages);
-        const int early = min(p.early_stages, nfirst);
+        const int rot = p.rot;
+        const int early = min(NS - rot, nfirst);
+        const int lead = min(p.lead, early);
         if (lane == 0)
-            for (int k = 0; k < early; ++k) issue(k, k);
+            for (int k = 0; k < lead; ++k) issue(k, k + rot);
         __syncwarp();
         pdl_launch_dependents();
-        // The rest of the first NS stages once the slots are free again.
-        ok = mbar_wait_bounded(xready, 0, &g_device_status, kDevStatusWaitTimeout);
+        ok = mbar_wait_bounded(xissued, 0, &g_device_status, kDevStatusWaitTimeout);
         if (ok && lane == 0)
-            for (int k = early; k < nfirst; ++k) issue(k, k);
+            for (int k = lead; k < early; ++k) issue(k, k + rot);
+        __syncwarp();
+        // The rest of the first NS stages once the slots are free again.
+        if (ok) ok = mbar_wait_bounded(xready, 0, &g_device_status, kDevStatusWaitTimeout);
+        if (ok && lane == 0)
+            for (int k = early; k < nfirst; ++k) issue(k, k + rot - NS);
         __syncwarp();
         // Buffer k % NS is free once every consumer warp has read stage k;
         // the partial slot of stage k + NS once stage k - NS is reduced.
         // Ring positions advance by counters.
-        int ebuf = 0, rslot = NS;
+        int ebuf = rot, elap = 0, rslot = NS;
         uint32_t ephase = 0, rphase = 0;
         for (int k = 0; k + NS < nstages && ok; ++k) {
             ok = mbar_wait_bounded(&empty[ebuf], ephase, &g_device_status, kDevStatusWaitTimeout);
@@ -521,8 +533,9 @@ __global__ void __launch_bounds__(512, 1) mv1_kernel(const Mv1Args p) {
                 ok = mbar_wait_bounded(&reduced[rslot], rphase, &g_device_status, kDevStatusWaitTimeout);
             if (ok && lane == 0) issue(kp, ebuf);
             __syncwarp();
-            if (++ebuf == NS) {
-                ebuf = 0;
+            if (++ebuf == NS) ebuf = 0;
+            if (++elap == NS) {
+                elap = 0;
                 ephase ^= 1u;
             }
             if (++rslot == NP) rslot = 0;
@@ -600,10 +613,21 @@ __global__ void __launch_bounds__(512, 1) mv1_kernel(const Mv1Args p) {
         Slice sl;
         pdl_wait();  // x is the previous kernel's output
         {
+            // All of a thread's loads (at most 16: x holds 16 float4 per slice
+            // and there are at least as many consumer threads as slices) are
+            // in flight before the copy warp queues more weight requests.
             const float4* x4 = reinterpret_cast<const float4*>(p.x);
-            const int n4 = nbc * 16;
-            for (int i = tid; i < n4; i += ncw * 32)
-                sts_float4(xslots + xslot_offset(i, QT == MUSER_Q4_K, parity_split, p.HP), __ldg(x4 + i));
+            const int n4 = nbc * 16, nthr = ncw * 32;
+            float4 v[16];
+#pragma unroll
+            for (int u = 0; u < 16; ++u)
+                if (tid + u * nthr < n4) v[u] = __ldg(x4 + tid + u * nthr);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(xissued);
+#pragma unroll
+            for (int u = 0; u < 16; ++u)
+                if (tid + u * nthr < n4)
+                    sts_float4(xslots + xslot_offset(tid + u * nthr, QT == MUSER_Q4_K, parity_split, p.HP), v[u]);
         }
         named_barrier_sync(1, ncw * 32);  // the consumer warps only
         if (active) {
@@ -613,6 +637,8 @@ __global__ void __launch_bounds__(512, 1) mv1_kernel(const Mv1Args p) {
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(xready);
+        // the slots overlay the partial slots: every slice is read first
+        ok = mbar_wait_bounded(xready, 0, &g_device_status, kDevStatusWaitTimeout);
         const uint32_t sel_lo = 0x7540u | static_cast<uint32_t>(2 * (c & 1));
         const uint32_t sel_hi = 0x7540u | static_cast<uint32_t>(2 * (c & 1) + 1);
         const uint32_t jq = static_cast<uint32_t>(c & 1);
@@ -676,7 +702,7 @@ __global__ void __launch_bounds__(512, 1) mv1_kernel(const Mv1Args p) {
         // stage's copy starts at the 16-byte boundary below its first row, so
         // the rows sit `delta` bytes into the buffer; delta advances by
         // RS * rowbytes mod 16 per stage.
-        int buf = 0, slot = 0, rows_left = nloc;
+        int buf = p.rot, lap = 0, slot = 0, rows_left = nloc;
         uint32_t phase = 0;
         uint32_t delta[NMAT];
         const uint8_t* sbase[NMAT];
@@ -708,8 +734,9 @@ __global__ void __launch_bounds__(512, 1) mv1_kernel(const Mv1Args p) {
 #pragma unroll
             for (int m = 0; m < NMAT; ++m) delta[m] = (delta[m] + dstep) & 15u;
             rows_left -= RS;
-            if (++buf == NS) {
-                buf = 0;
+            if (++buf == NS) buf = 0;
+            if (++lap == NS) {
+                lap = 0;
                 phase ^= 1u;
             }
             if (++slot == NP) slot = 0;
@@ -722,7 +749,7 @@ __global__ void __launch_bounds__(512, 1) mv1_kernel(const Mv1Args p) {
         // released, then leave without writing the tail.
         if (tid == 0) {
             for (int k = max(0, nstages - NS); k < nstages; ++k)
-                (void)mbar_wait_bounded(&full[k % NS], static_cast<uint32_t>((k / NS) & 1),
+                (void)mbar_wait_bounded(&full[(k + p.rot) % NS], static_cast<uint32_t>((k / NS) & 1),
                                         &g_device_status, kDevStatusTxTimeout, 200000000ull);
         }
         return;
@@ -816,14 +843,16 @@ static int launch_mv1_t(Mv1Args a, cudaStream_t stream) {
     a.ns = ns;
     a.stage_off = static_cast<int>((a.part_off + 2 * ns * part_per_stage + 127) / 128 * 128);
     const size_t smem = static_cast<size_t>(a.stage_off + ns * per_stage);
-    // input slots at the top of the stage buffers; the buffers below them
-    // take the first weight copies
+    // input slots over the partial slots and, when larger, the first stage
+    // buffers; the other buffers take the first weight copies
     const int64_t xbytes = (static_cast<int64_t>(a.TG) * kXSlot + 127) / 128 * 128;
-    if (xbytes > ns * per_stage)
+    if (a.part_off + xbytes > static_cast<int64_t>(smem))
         return set_error(MUSER_ERR_UNSUPPORTED, "mv1: input slots (%lld B) exceed the stage buffers",
                          (long long)xbytes);
-    a.x_off = static_cast<int>(static_cast<int64_t>(smem) - xbytes);
-    a.early_stages = static_cast<int>((a.x_off - a.stage_off) / per_stage);
+    a.x_off = a.part_off;
+    const int64_t over = a.part_off + xbytes - a.stage_off;
+    a.rot = over > 0 ? static_cast<int>((over + per_stage - 1) / per_stage) : 0;
+    a.lead = 2;
     auto kern = mv1_kernel<QT, NMAT, EPI>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
