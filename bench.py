@@ -58,7 +58,17 @@ def _env_int(k, d):
 
 
 def algorithmic_bytes(M: int):
-    """Per layer and per kernel: weights read + activations read/written (f32)."""
+    """Per layer and per kernel: weights read + activations read/written (f32).
+
+    M = 1 runs each layer's tail inside the next layer's gate/up kernel:
+    (gate/up with the previous tail, plain down projection) per layer, and
+    the entry norm plus the last tail once per step.  M = 16 runs (gate/up,
+    down + tail) per layer and the entry norm once."""
+    if M == 1:
+        gate_up = 2 * Q4K_MAT + 4 * H * 6 + 4 * F  # Wg, Wu; p, r in/out, w1, w2, x out; mid out
+        down = Q6K_MAT + 4 * F + 4 * H             # Wd, mid in, proj out
+        entry = 4 * H * 3 + 4 * H * 6              # rms_norm (r, w, x); the last tail (p, r r/w, w1, w2, out)
+        return gate_up, down, entry
     gate_up = 2 * Q4K_MAT + 4 * M * H + 4 * M * F           # Wg, Wu, x in, mid out
     down_tail = Q6K_MAT + 4 * M * F + 4 * M * H * 5 + 4 * 2 * H  # Wd, mid, proj w, p r, r r/w, out w, w1/w2
     entry = 4 * M * H * 2 + 4 * H
@@ -181,7 +191,7 @@ class NativeStack:
         self.stream = torch.cuda.current_stream()
         self.sh = self.stream.cuda_stream
         self.arr = (mu.FfnLayer * n_layers)(*self.structs)
-        self.launches_per_step = 1 + 2 * n_layers
+        self.launches_per_step = 1 + 2 * n_layers + (1 if M == 1 else 0)
 
     def _rc(self, name, rc):
         if rc != 0:
@@ -191,6 +201,8 @@ class NativeStack:
         """One token (M rows) through every layer, per-layer calls.  `events`
         maps a few layers to an event triple that brackets their gate/up and
         down launches (the others run back to back, overlapped by PDL)."""
+        if self.M == 1:
+            return self._step_m1(events)
         L, M, sh = self.L, self.M, self.sh
         self._rc("rms_norm", L.muser_rms_norm(self.resid.data_ptr(), self.w_in.data_ptr(),
                                               self.x[0].data_ptr(), H, M, 1e-5, sh))
@@ -212,6 +224,39 @@ class NativeStack:
             if ev is not None:
                 ev[2].record(self.stream)
             x, xn = xn, x
+
+    def _step_m1(self, events=None):
+        """One row of x, the composition muser_ffn_stack uses for it: the
+        entry norm, then per layer gate/up (with the previous layer's tail
+        fused in, from layer 1) and the plain down projection, then the last
+        layer's tail."""
+        L, M, sh = self.L, self.M, self.sh
+        self._rc("rms_norm", L.muser_rms_norm(self.resid.data_ptr(), self.w_in.data_ptr(),
+                                              self.x[0].data_ptr(), H, M, 1e-5, sh))
+        prev = None
+        for l, d in enumerate(self.layers):
+            ev = events.get(l) if events is not None else None
+            if ev is not None:
+                ev[0].record(self.stream)
+            if prev is None:
+                self._rc("gate_up", L.muser_ffn_gate_up_silu(
+                    12, d["Wg"].data_ptr(), d["Wu"].data_ptr(), F, H, self.x[0].data_ptr(), M,
+                    self.mid.data_ptr(), sh))
+            else:
+                self._rc("gate_up_tail", L.muser_ffn_gate_up_silu_tail(
+                    12, d["Wg"].data_ptr(), d["Wu"].data_ptr(), F, H, self.proj.data_ptr(),
+                    self.resid.data_ptr(), prev["w1"].data_ptr(), prev["w_next"].data_ptr(), 1e-8, 1e-5,
+                    self.x[1].data_ptr(), M, self.mid.data_ptr(), sh))
+            if ev is not None:
+                ev[1].record(self.stream)
+            self._rc("down", L.muser_qmatvec(14, d["Wd"].data_ptr(), H, F, self.mid.data_ptr(), M,
+                                             self.proj.data_ptr(), sh))
+            if ev is not None:
+                ev[2].record(self.stream)
+            prev = d
+        self._rc("tail", L.muser_fused_residual_dual_rmsnorm(
+            self.resid.data_ptr(), self.proj.data_ptr(), self.out.data_ptr(), prev["w1"].data_ptr(),
+            prev["w_next"].data_ptr(), H, M, 1e-8, 1e-5, sh))
 
     def step_public(self):
         """The same token through the one-call public entry point."""
@@ -332,6 +377,9 @@ def run_native(args, rank, world):
         "config": {
             "workload": f"decode-FFN stack: {nl} layers x [rms_norm(layer 0) -> Q4_K gate/up {F}x{H} + SiLU "
                         f"-> Q6_K down {H}x{F} + dual-eps tail], M={M}",
+            "composition": ("per layer: gate/up kernel with the previous layer's tail in its prologue, "
+                            "down projection; entry norm and last tail once per step" if M == 1 else
+                            "per layer: gate/up kernel, down projection + tail kernel"),
             "layers": nl, "hidden": H, "ffn": F, "M": M,
             "weight_bytes_per_step": weight_bytes,
             "algorithmic_bytes_per_step": step_bytes,
@@ -342,7 +390,9 @@ def run_native(args, rank, world):
         "hbm_frac_of_" + peak_kind: round(gbs / world / peak, 4),
         "roofline": {
             "bound": "hbm",
-            "kernel": f"muser_ffn_gate_up_silu ({kname} Q4_K gate+up, SiLU epilogue)",
+            "kernel": (f"muser_ffn_gate_up_silu_tail ({kname} Q4_K gate+up, previous layer's dual-eps tail in "
+                       f"the prologue, SiLU epilogue)" if M == 1 else
+                       f"muser_ffn_gate_up_silu ({kname} Q4_K gate+up, SiLU epilogue)"),
             "achieved": round(achieved, 1),
             "peak": peak,
             "peak_kind": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else "fallback 6.8 TB/s",
@@ -351,7 +401,8 @@ def run_native(args, rank, world):
             "traffic": traffic,
             "algorithmic_bytes_per_launch": gu_bytes,
             "mean_launch_us": round(gu_mean * 1e3, 2),
-            "second_kernel": {"name": f"muser_qmatvec_residual_dual_rmsnorm ({kname} Q6_K + tail)",
+            "second_kernel": {"name": (f"muser_qmatvec ({kname} Q6_K down projection)" if M == 1 else
+                                       f"muser_qmatvec_residual_dual_rmsnorm ({kname} Q6_K + tail)"),
                               "achieved_gbs": round(dt_bytes / (dt_mean * 1e-3) / 1e9, 1),
                               "mean_launch_us": round(dt_mean * 1e3, 2),
                               "algorithmic_bytes_per_launch": dt_bytes},

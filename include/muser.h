@@ -155,6 +155,31 @@ int muser_fused_residual_dual_rmsnorm(float* residual, const float* src, float* 
                                       const float* w1, const float* w2, int n, int M, float eps1,
                                       float eps2, void* stream);
 
+/*
+ * muser_ffn_gate_up_silu_tail -- the boundary between two decode layers in
+ *   one call: the previous layer's dual-eps tail (Ch 19 §19.4, as
+ *   muser_fused_residual_dual_rmsnorm with src = projected, out = x_out),
+ *   then this layer's gate/up/SiLU on its output (Ch 10 §10.3 (d), as
+ *   muser_ffn_gate_up_silu with x = x_out).  Per row m:
+ *     residual += w1 * projected / sqrt(mean(projected^2) + eps1)  (in place)
+ *     x_out     = w2 * residual / sqrt(mean(residual^2) + eps2)
+ *     mid       = silu(Wg . x_out) * (Wu . x_out)
+ *   w2 is the next norm of the previous layer, i.e. this layer's input norm
+ *   (Ch 10 §10.4).  The rounding points are those of the two calls: the
+ *   residual and x_out are binary32 values.  For one row of x with a short
+ *   enough row (hidden <= 6656 for Q4_K gate/up) the tail runs inside the
+ *   gate/up kernel, so the layer boundary costs no separate launch; other
+ *   shapes run the two calls.
+ *   projected, residual, x_out: device f32 [M*hidden] (residual in/out,
+ *   x_out output; the three must be distinct); w1, w2: device f32 [hidden];
+ *   Wg, Wu: device matrices [ffn x hidden]; mid: device f32 [M*ffn].
+ *   hidden % 4 == 0; eps1, eps2 > 0.  Fail-closed like the two calls.
+ */
+int muser_ffn_gate_up_silu_tail(int qtype, const void* Wg, const void* Wu, int64_t ffn,
+                                int64_t hidden, const float* projected, float* residual,
+                                const float* w1, const float* w2, float eps1, float eps2,
+                                float* x_out, int M, float* mid, void* stream);
+
 /* Scratch bytes muser_qmatvec_residual_dual_rmsnorm needs (a small constant). */
 size_t muser_scratch_bytes(int64_t hidden, int M);
 

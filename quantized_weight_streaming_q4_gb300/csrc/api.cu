@@ -82,13 +82,17 @@ int check_M(const char* fn, int M) {
 }
 
 
-constexpr size_t kScratchBytes = 256;
+// Scratch of the one-token down + tail kernel: its ticket, then (from byte
+// kTailPartOffset) the blocks' sums of projected^2.
+constexpr size_t kTailPartOffset = 256;
+constexpr size_t kScratchBytes = kTailPartOffset + sizeof(float) * kMv1TailParts;
 // Route one-token calls to the tensor-core kernel (mvt) instead of mv1.
 // mv1 measures faster for one row of x (one launch and inside the stack).
 constexpr bool kTensorCoreM1 = false;
 
 // Scratch of the fused down projection + tail: the CUDA-core kernel's ticket
-// (kScratchBytes), then the tensor-core kernel's tickets and partial sums.
+// and per-block sums (kScratchBytes), then the tensor-core kernel's tickets
+// and partial sums.
 // The bound holds for every row length (a one-block Q6_K row has the most
 // tiles).
 size_t down_scratch_bytes(int64_t hidden, int M) {
@@ -185,6 +189,10 @@ int down_tail_launch(int qtype, const void* Wdown, int64_t hidden, int64_t ffn, 
         a.eps1 = eps1;
         a.eps2 = eps2;
         a.ticket = static_cast<unsigned*>(scratch);
+        // with room for the blocks' sums the tail skips its first pass
+        a.tail_part = scratch_bytes >= kScratchBytes
+                          ? reinterpret_cast<float*>(static_cast<uint8_t*>(scratch) + kTailPartOffset)
+                          : nullptr;
         return launch_mv1(qtype, 1, kEpiTail, a, s);
     }
     MvMArgs a{};
@@ -198,6 +206,38 @@ int down_tail_launch(int qtype, const void* Wdown, int64_t hidden, int64_t ffn, 
     MUSER_TRY(launch_mvM(qtype, 1, kEpiStore, a, s));
     return launch_dual_tail(residual, projected, out, w1, w2, static_cast<int>(hidden), M, eps1,
                             eps2, s);
+}
+
+// The tail of the previous layer fused into this layer's gate/up kernel.
+bool gate_up_tail_fused(int qtype, int64_t hidden, int M) {
+    return M == 1 && mv1_tail_prologue_supported(qtype, hidden);
+}
+
+int gate_up_launch(int qtype, const void* Wg, const void* Wu, int64_t ffn, int64_t hidden,
+                   const float* x, int M, float* mid, void* scratch, cudaStream_t s);
+
+// The layer boundary (previous tail, then gate/up) on validated arguments.
+int gate_up_tail_launch(int qtype, const void* Wg, const void* Wu, int64_t ffn, int64_t hidden,
+                        const float* projected, float* residual, const float* w1, const float* w2,
+                        float eps1, float eps2, float* x_out, int M, float* mid, cudaStream_t s) {
+    if (gate_up_tail_fused(qtype, hidden, M)) {
+        Mv1Args a{};
+        a.W[0] = static_cast<const uint8_t*>(Wg);
+        a.W[1] = static_cast<const uint8_t*>(Wu);
+        a.rows = ffn;
+        a.nsb = static_cast<int>(hidden / kQK);
+        a.x = projected;
+        a.y0 = mid;
+        a.resid = residual;
+        a.out = x_out;
+        a.w1 = w1;
+        a.w2 = w2;
+        a.eps1 = eps1;
+        a.eps2 = eps2;
+        return launch_mv1(qtype, 2, kEpiSiluMul, a, s, kXTail);
+    }
+    MUSER_TRY(launch_dual_tail(residual, projected, x_out, w1, w2, static_cast<int>(hidden), M, eps1, eps2, s));
+    return gate_up_launch(qtype, Wg, Wu, ffn, hidden, x_out, M, mid, nullptr, s);
 }
 
 // scratch: the tensor-core kernel's even-split scratch, or null (whole tiles).
@@ -387,6 +427,29 @@ int muser_ffn_gate_up_silu_scratch(int qtype, const void* Wg, const void* Wu, in
     return gate_up_launch(qtype, Wg, Wu, ffn, hidden, x, M, mid, need > 0 ? scratch : nullptr, as_stream(stream));
 }
 
+int muser_ffn_gate_up_silu_tail(int qtype, const void* Wg, const void* Wu, int64_t ffn,
+                                int64_t hidden, const float* projected, float* residual,
+                                const float* w1, const float* w2, float eps1, float eps2,
+                                float* x_out, int M, float* mid, void* stream) {
+    clear_error();
+    const char* fn = "muser_ffn_gate_up_silu_tail";
+    MUSER_TRY(check_matrix(fn, qtype, Wg, ffn, hidden));
+    MUSER_TRY(check_matrix(fn, qtype, Wu, ffn, hidden));
+    MUSER_TRY(check_M(fn, M));
+    MUSER_TRY(check_f32(fn, "projected", projected));
+    MUSER_TRY(check_f32(fn, "residual", residual));
+    MUSER_TRY(check_f32(fn, "w1", w1));
+    MUSER_TRY(check_f32(fn, "w2", w2));
+    MUSER_TRY(check_f32(fn, "x_out", x_out));
+    MUSER_TRY(check_f32(fn, "mid", mid));
+    if (hidden % 4) return set_error(MUSER_ERR_INVALID_ARG, "%s: hidden must be a multiple of 4", fn);
+    if (!(eps1 > 0.0f) || !(eps2 > 0.0f)) return set_error(MUSER_ERR_INVALID_ARG, "%s: eps must be > 0", fn);
+    if (x_out == residual || x_out == projected || projected == residual)
+        return set_error(MUSER_ERR_INVALID_ARG, "%s: projected, residual and x_out must be distinct", fn);
+    return gate_up_tail_launch(qtype, Wg, Wu, ffn, hidden, projected, residual, w1, w2, eps1, eps2,
+                               x_out, M, mid, as_stream(stream));
+}
+
 int muser_fused_residual_dual_rmsnorm(float* residual, const float* src, float* out,
                                       const float* w1, const float* w2, int n, int M, float eps1,
                                       float eps2, void* stream) {
@@ -428,8 +491,10 @@ int muser_qmatvec_residual_dual_rmsnorm(int qtype, const void* Wdown, int64_t hi
     MUSER_TRY(check_f32(fn, "w2", w2));
     MUSER_TRY(check_f32(fn, "scratch", scratch));
     if (hidden % 4) return set_error(MUSER_ERR_INVALID_ARG, "%s: hidden must be a multiple of 4", fn);
-    if (scratch_bytes < kScratchBytes)
-        return set_error(MUSER_ERR_INVALID_ARG, "%s: scratch_bytes %zu < %zu", fn, scratch_bytes, kScratchBytes);
+    // 256 bytes (the ticket) suffice; muser_scratch_bytes() also leaves room
+    // for the blocks' sums (a shorter tail) and the tensor-core kernel
+    if (scratch_bytes < kTailPartOffset)
+        return set_error(MUSER_ERR_INVALID_ARG, "%s: scratch_bytes %zu < %zu", fn, scratch_bytes, kTailPartOffset);
     if (!(eps1 > 0.0f) || !(eps2 > 0.0f)) return set_error(MUSER_ERR_INVALID_ARG, "%s: eps must be > 0", fn);
     if (out == residual || out == projected || projected == residual)
         return set_error(MUSER_ERR_INVALID_ARG, "%s: projected, residual and out must be distinct", fn);
@@ -509,6 +574,35 @@ int muser_ffn_stack(const muser_ffn_layer* layers, int n_layers, const float* en
     }
     cudaStream_t s = as_stream(stream);
     MUSER_TRY(launch_rms_norm(residual, entry_norm, ws.xa, static_cast<int>(hidden), M, eps_norm, s));
+    // One row of x: each layer's tail runs in the next layer's gate/up kernel
+    // and the down projection only stores `projected`; the last tail runs on
+    // its own.
+    bool fused = true;
+    for (int l = 0; l < n_layers && fused; ++l)
+        fused = gate_up_tail_fused(layers[l].gate_up_qtype, hidden, M) && mv1_supported(layers[l].down_qtype, ffn);
+    if (fused) {
+        for (int l = 0; l < n_layers; ++l) {
+            const muser_ffn_layer& L = layers[l];
+            if (l == 0) {
+                MUSER_TRY(gate_up_launch(L.gate_up_qtype, L.w_gate, L.w_up, ffn, hidden, ws.xa, M, ws.mid, nullptr, s));
+            } else {
+                const muser_ffn_layer& P = layers[l - 1];
+                MUSER_TRY(gate_up_tail_launch(L.gate_up_qtype, L.w_gate, L.w_up, ffn, hidden, ws.proj, residual,
+                                              P.post_norm, P.next_norm, eps_post, eps_norm, ws.xb, M, ws.mid, s));
+            }
+            Mv1Args d{};
+            d.W[0] = static_cast<const uint8_t*>(L.w_down);
+            d.W[1] = d.W[0];
+            d.rows = hidden;
+            d.nsb = static_cast<int>(ffn / kQK);
+            d.x = ws.mid;
+            d.y0 = ws.proj;
+            MUSER_TRY(launch_mv1(L.down_qtype, 1, kEpiStore, d, s));
+        }
+        const muser_ffn_layer& Z = layers[n_layers - 1];
+        return launch_dual_tail(residual, ws.proj, out, Z.post_norm, Z.next_norm, static_cast<int>(hidden), M,
+                                eps_post, eps_norm, s);
+    }
     float* x = ws.xa;
     float* xnext = ws.xb;
     for (int l = 0; l < n_layers; ++l) {

@@ -276,6 +276,66 @@ __device__ __forceinline__ void block_dual_tail_row(float* resid, const float* s
     }
 }
 
+// The same row of the dual-eps tail when every block of the grid has left
+// its share of sum(src^2) in parts[0..nparts) (the block that wrote those
+// rows of src summed their squares): the first pass is a sum of nparts
+// values, and the row (at most 4 float4 of each vector per thread) stays in
+// registers between the two remaining steps.  Needs n / 4 <= 4 * blockDim.x.
+__device__ __forceinline__ void block_dual_tail_row_parts(float* resid, const float* src, float* out,
+                                                          const float* w1, const float* w2, int n,
+                                                          float eps1, float eps2, const float* parts,
+                                                          int nparts, float* red) {
+    constexpr int V = 4;
+    const int n4 = n >> 2;
+    const float4* s4 = reinterpret_cast<const float4*>(src);
+    float4* r4 = reinterpret_cast<float4*>(resid);
+    float4* o4 = reinterpret_cast<float4*>(out);
+    const float4* a4 = reinterpret_cast<const float4*>(w1);
+    const float4* b4 = reinterpret_cast<const float4*>(w2);
+    float ss = 0.0f;
+    for (int i = threadIdx.x; i < nparts; i += blockDim.x) ss += __ldcg(parts + i);
+    float4 pv[V], rv[V], av[V], bv[V];
+#pragma unroll
+    for (int u = 0; u < V; ++u) {
+        const int i = threadIdx.x + u * blockDim.x;
+        if (i < n4) {
+            pv[u] = __ldcg(s4 + i);
+            rv[u] = __ldcg(r4 + i);
+            av[u] = __ldg(a4 + i);
+            bv[u] = __ldg(b4 + i);
+        }
+    }
+    ss = block_sum(ss, red);
+    const float inv1 = 1.0f / sqrtf(ss / static_cast<float>(n) + eps1);
+    float sh = 0.0f;
+#pragma unroll
+    for (int u = 0; u < V; ++u) {
+        const int i = threadIdx.x + u * blockDim.x;
+        if (i < n4) {
+            float4 h;
+            h.x = fmaf(pv[u].x * inv1, av[u].x, rv[u].x);
+            h.y = fmaf(pv[u].y * inv1, av[u].y, rv[u].y);
+            h.z = fmaf(pv[u].z * inv1, av[u].z, rv[u].z);
+            h.w = fmaf(pv[u].w * inv1, av[u].w, rv[u].w);
+            r4[i] = h;
+            sh = fmaf(h.x, h.x, sh);
+            sh = fmaf(h.y, h.y, sh);
+            sh = fmaf(h.z, h.z, sh);
+            sh = fmaf(h.w, h.w, sh);
+            rv[u] = h;
+        }
+    }
+    sh = block_sum(sh, red);
+    const float inv2 = 1.0f / sqrtf(sh / static_cast<float>(n) + eps2);
+#pragma unroll
+    for (int u = 0; u < V; ++u) {
+        const int i = threadIdx.x + u * blockDim.x;
+        if (i < n4)
+            o4[i] = make_float4((rv[u].x * inv2) * bv[u].x, (rv[u].y * inv2) * bv[u].y,
+                                (rv[u].z * inv2) * bv[u].z, (rv[u].w * inv2) * bv[u].w);
+    }
+}
+
 // SiLU(g) * u in binary32 (z/(1+exp(-z)) with CUDA's expf and IEEE division).
 __device__ __forceinline__ float silu_mul_f(float g, float u) {
     return (g / (1.0f + expf(-g))) * u;

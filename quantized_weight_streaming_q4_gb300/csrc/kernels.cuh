@@ -6,6 +6,9 @@
 namespace muser {
 
 enum EpiKind { kEpiStore = 0, kEpiSiluMul = 1, kEpiTail = 2 };
+// Where the one-token kernel's x comes from: memory, or the previous layer's
+// dual-eps tail computed in its prologue (x = p.x is then `projected`).
+enum XSource { kXMemory = 0, kXTail = 1 };
 
 // One-token matvec (mv1.cu).  W[0..NMAT-1] share rows x (nsb*256) and x.
 struct Mv1Args {
@@ -22,6 +25,7 @@ struct Mv1Args {
     const float* w2;
     float eps1, eps2;
     unsigned* ticket;
+    float* tail_part;  // per-block sums of projected^2 (kMv1TailParts floats), or null
     // geometry, filled by the launcher
     int G, RS, ns, nconsumer_warps;
     int TG;  // consumer threads per row group
@@ -32,8 +36,11 @@ struct Mv1Args {
     int rot;    // stage buffers under the input slots; stage k uses buffer (k + rot) % ns
     int lead;   // stages requested before the loads of x
 };
+// Blocks whose share of the tail's first sum fits in Mv1Args::tail_part.
+constexpr int kMv1TailParts = 192;
 bool mv1_supported(int qtype, int64_t cols);
-int launch_mv1(int qtype, int nmat, int epi, const Mv1Args& a, cudaStream_t s);
+bool mv1_tail_prologue_supported(int qtype, int64_t cols);
+int launch_mv1(int qtype, int nmat, int epi, const Mv1Args& a, cudaStream_t s, int xs = kXMemory);
 
 // Multi-row matvec (mvM.cu): y[m*rows + r], m < M <= 16.
 struct MvMArgs {

@@ -397,6 +397,20 @@ __device__ __forceinline__ int xslot_offset(int i, bool q4, bool parity_split, i
     return idx * kXSlot + 64 * g + 16 * l4;
 }
 
+// Sum of v over the first nwarps warps of the block (all of them call it):
+// warp trees, then every thread adds the warp sums in warp order, so every
+// thread gets the same value.  red needs nwarps floats; named barrier 1.
+__device__ __forceinline__ float warps_sum(float v, float* red, int nwarps) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    v = warp_sum(v);
+    if (lane == 0) red[warp] = v;
+    named_barrier_sync(1, nwarps * 32);
+    float t = 0.0f;
+    for (int w = 0; w < nwarps; ++w) t += red[w];
+    named_barrier_sync(1, nwarps * 32);
+    return t;
+}
+
 // -------------------------------------------------------------- the kernel
 // Warp roles: warps 0..nconsumer-1 compute (each thread one input slice and a
 // row group); the next warp issues the bulk copies; the last two reduce the
@@ -405,7 +419,11 @@ __device__ __forceinline__ int xslot_offset(int i, bool q4, bool parity_split, i
 // transaction bytes) and an "empty" mbarrier (one arrival per consumer warp
 // once it has read the stage and stored its partials).  No block-wide barrier
 // runs per stage.
-template <int QT, int NMAT, int EPI>
+// XS: where x comes from.  kXMemory: x is p.x.  kXTail: x is the next-norm
+// output of the previous layer's dual-eps tail (Ch 19 §19.4), computed here
+// by every block from p.x (= projected), p.resid, p.w1, p.w2: block 0 writes
+// the updated residual (and x to p.out when that is set).
+template <int QT, int NMAT, int EPI, int XS>
 __global__ void __launch_bounds__(512, 1) mv1_kernel(const Mv1Args p) {
     extern __shared__ __align__(128) uint8_t smem[];
     constexpr int kBlk = (QT == MUSER_Q4_K) ? kQ4KBytes : kQ6KBytes;
@@ -550,6 +568,7 @@ __global__ void __launch_bounds__(512, 1) mv1_kernel(const Mv1Args p) {
         const int n4 = nbc / 4;
         int slot = warp - ncw - 1;  // k % NP (NP is even)
         uint32_t sphase = 0;        // (k / NP) & 1
+        float tss = 0.0f;           // tail: sum of this warp's projected^2
         for (int k = warp - ncw - 1; k < nstages; k += 2) {
             if (ok) ok = mbar_wait_bounded(&pfull[slot], sphase, &g_device_status, kDevStatusWaitTimeout);
             if (!ok) break;
@@ -588,7 +607,10 @@ __global__ void __launch_bounds__(512, 1) mv1_kernel(const Mv1Args p) {
                         p.y0[row] = acc;
                         if constexpr (NMAT == 2) p.y1[row] = other;
                     }
-                    if constexpr (EPI == kEpiTail) __threadfence();
+                    if constexpr (EPI == kEpiTail) {
+                        tss = fmaf(acc, acc, tss);
+                        __threadfence();
+                    }
                 }
             }
             __syncwarp();
@@ -598,6 +620,10 @@ __global__ void __launch_bounds__(512, 1) mv1_kernel(const Mv1Args p) {
                 slot -= NP;
                 sphase ^= 1u;
             }
+        }
+        if constexpr (EPI == kEpiTail) {
+            tss = warp_sum(tss);
+            if (lane == 0) red[40 + warp - ncw - 1] = tss;
         }
     } else {
         // Thread -> (row group g, slice (b, c) of slice_of); a row group spans
@@ -612,7 +638,70 @@ __global__ void __launch_bounds__(512, 1) mv1_kernel(const Mv1Args p) {
         using Slice = typename std::conditional<QT == MUSER_Q4_K, SliceQ4, SliceQ6>::type;
         Slice sl;
         pdl_wait();  // x is the previous kernel's output
-        {
+        if constexpr (XS == kXTail) {
+            // The tail of the previous layer, at most 4 float4 of each vector
+            // per thread (the launcher checks), in registers.
+            const int n4 = nbc * 16, nthr = ncw * 32;
+            const float n = static_cast<float>(nbc * 64);
+            const float4* p4 = reinterpret_cast<const float4*>(p.x);
+            const float4* r4 = reinterpret_cast<const float4*>(p.resid);
+            const float4* a4 = reinterpret_cast<const float4*>(p.w1);
+            const float4* b4 = reinterpret_cast<const float4*>(p.w2);
+            float4 pv[4], rv[4], av[4], bv[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int i = tid + u * nthr;
+                if (i < n4) {
+                    pv[u] = __ldcg(p4 + i);
+                    rv[u] = __ldcg(r4 + i);
+                    av[u] = __ldg(a4 + i);
+                    bv[u] = __ldg(b4 + i);
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(xissued);
+            float ss = 0.0f;
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                if (tid + u * nthr < n4) {
+                    ss = fmaf(pv[u].x, pv[u].x, ss);
+                    ss = fmaf(pv[u].y, pv[u].y, ss);
+                    ss = fmaf(pv[u].z, pv[u].z, ss);
+                    ss = fmaf(pv[u].w, pv[u].w, ss);
+                }
+            ss = warps_sum(ss, red, ncw);
+            const float inv1 = 1.0f / sqrtf(ss / n + p.eps1);
+            float sh = 0.0f;
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                if (tid + u * nthr < n4) {
+                    float4 h;
+                    h.x = fmaf(pv[u].x * inv1, av[u].x, rv[u].x);
+                    h.y = fmaf(pv[u].y * inv1, av[u].y, rv[u].y);
+                    h.z = fmaf(pv[u].z * inv1, av[u].z, rv[u].z);
+                    h.w = fmaf(pv[u].w * inv1, av[u].w, rv[u].w);
+                    sh = fmaf(h.x, h.x, sh);
+                    sh = fmaf(h.y, h.y, sh);
+                    sh = fmaf(h.z, h.z, sh);
+                    sh = fmaf(h.w, h.w, sh);
+                    rv[u] = h;
+                }
+            sh = warps_sum(sh, red, ncw);
+            const float inv2 = 1.0f / sqrtf(sh / n + p.eps2);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int i = tid + u * nthr;
+                if (i < n4) {
+                    const float4 xv = make_float4((rv[u].x * inv2) * bv[u].x, (rv[u].y * inv2) * bv[u].y,
+                                                  (rv[u].z * inv2) * bv[u].z, (rv[u].w * inv2) * bv[u].w);
+                    sts_float4(xslots + xslot_offset(i, QT == MUSER_Q4_K, parity_split, p.HP), xv);
+                    if (blockIdx.x == 0) {
+                        reinterpret_cast<float4*>(p.resid)[i] = rv[u];
+                        if (p.out) reinterpret_cast<float4*>(p.out)[i] = xv;
+                    }
+                }
+            }
+        } else {
             // All of a thread's loads (at most 16: x holds 16 float4 per slice
             // and there are at least as many consumer threads as slices) are
             // in flight before the copy warp queues more weight requests.
@@ -756,8 +845,11 @@ __global__ void __launch_bounds__(512, 1) mv1_kernel(const Mv1Args p) {
     }
 
     if constexpr (EPI == kEpiTail) {
-        // Last CTA to finish runs the dual-eps tail over the whole row.
+        // Last CTA to finish runs the dual-eps tail over the whole row.  With
+        // p.tail_part, every CTA first leaves the sum of its rows' squares
+        // there (its two reducers' sums, in order).
         if (tid == 0) {
+            if (p.tail_part) p.tail_part[blockIdx.x] = red[40] + red[41];
             __threadfence();
             const unsigned t = atomicAdd(p.ticket, 1u);
             *flag = (t == gridDim.x - 1) ? 1 : 0;
@@ -765,9 +857,17 @@ __global__ void __launch_bounds__(512, 1) mv1_kernel(const Mv1Args p) {
         __syncthreads();
         if (*flag) {
             __threadfence();
-            block_dual_tail_row(p.resid, p.y0, p.out, p.w1, p.w2, static_cast<int>(p.rows), p.eps1,
-                                p.eps2, red);
-            if (tid == 0) *p.ticket = 0u;  // leave the scratch zeroed for the next call
+            const int n = static_cast<int>(p.rows);
+            if (p.tail_part && (n >> 2) <= 4 * static_cast<int>(blockDim.x))
+                block_dual_tail_row_parts(p.resid, p.y0, p.out, p.w1, p.w2, n, p.eps1, p.eps2, p.tail_part,
+                                          static_cast<int>(gridDim.x), red);
+            else
+                block_dual_tail_row(p.resid, p.y0, p.out, p.w1, p.w2, n, p.eps1, p.eps2, red);
+            // leave the scratch zeroed for the next call (the partials were
+            // read before the tail's block-wide sums)
+            if (p.tail_part)
+                for (int i = tid; i < static_cast<int>(gridDim.x); i += blockDim.x) p.tail_part[i] = 0.0f;
+            if (tid == 0) *p.ticket = 0u;
         }
     }
 }
@@ -800,7 +900,34 @@ bool mv1_supported(int qtype, int64_t cols) {
     return cols % kQK == 0 && nbc >= 1 && nbc <= kMaxConsumerThreads;
 }
 
-template <int QT, int NMAT, int EPI>
+// Consumer geometry of a row of `cols` inputs: threads per row group (TG),
+// the odd-half start (HP), row groups (G) and consumer warps.
+struct Mv1Geom {
+    int TG, HP, G, ncw;
+};
+static Mv1Geom mv1_geom(int qtype, int nsb) {
+    const int nbc = nsb * 4;
+    Mv1Geom g{nbc, nbc / 2, 1, 1};
+    if (qtype == MUSER_Q6_K && nsb % 2 == 0) {
+        const int hp = (nbc / 2 + 31) / 32 * 32;
+        if (2 * hp <= kMaxConsumerThreads) {
+            g.HP = hp;
+            g.TG = 2 * hp;
+        }
+    }
+    g.G = std::max(1, kMaxConsumerThreads / g.TG);
+    g.ncw = (g.TG * g.G + 31) / 32;
+    return g;
+}
+
+bool mv1_tail_prologue_supported(int qtype, int64_t cols) {
+    if (!mv1_supported(qtype, cols)) return false;
+    const int nsb = static_cast<int>(cols / kQK);
+    // the tail keeps at most 4 float4 of each vector per consumer thread
+    return nsb * 4 * 16 <= 4 * 32 * mv1_geom(qtype, nsb).ncw;
+}
+
+template <int QT, int NMAT, int EPI, int XS>
 static int launch_mv1_t(Mv1Args a, cudaStream_t stream) {
     constexpr int kBlk = (QT == MUSER_Q4_K) ? kQ4KBytes : kQ6KBytes;
     const int nbc = a.nsb * 4;
@@ -808,19 +935,16 @@ static int launch_mv1_t(Mv1Args a, cudaStream_t stream) {
     const int sms = sm_count();
     if (sms <= 0) return set_error(MUSER_ERR_CUDA, "mv1: cannot query the SM count");
     const int grid = static_cast<int>(std::min<int64_t>(sms, a.rows));
+    if (EPI == kEpiTail && grid > kMv1TailParts) a.tail_part = nullptr;
     // Q6_K rows of an even number of super-blocks split their slices by block
     // parity; each half is padded to whole warps when that still fits.
-    a.TG = nbc;
-    a.HP = nbc / 2;
-    if (QT == MUSER_Q6_K && a.nsb % 2 == 0) {
-        const int hp = (nbc / 2 + 31) / 32 * 32;
-        if (2 * hp <= kMaxConsumerThreads) {
-            a.HP = hp;
-            a.TG = 2 * hp;
-        }
-    }
-    a.G = std::max(1, kMaxConsumerThreads / a.TG);
-    a.nconsumer_warps = (a.TG * a.G + 31) / 32;
+    const Mv1Geom geo = mv1_geom(QT, a.nsb);
+    a.TG = geo.TG;
+    a.HP = geo.HP;
+    a.G = geo.G;
+    a.nconsumer_warps = geo.ncw;
+    if (XS == kXTail && !(nbc * 16 <= 4 * 32 * geo.ncw))
+        return set_error(MUSER_ERR_UNSUPPORTED, "mv1: %d inputs exceed the fused tail's registers", nbc * 64);
     const int threads = (a.nconsumer_warps + 3) * 32;
     // rows per stage: a multiple of G, stage near 32 KB over all matrices
     const int64_t per_row = rowbytes * NMAT;
@@ -853,7 +977,7 @@ static int launch_mv1_t(Mv1Args a, cudaStream_t stream) {
     const int64_t over = a.part_off + xbytes - a.stage_off;
     a.rot = over > 0 ? static_cast<int>((over + per_stage - 1) / per_stage) : 0;
     a.lead = 2;
-    auto kern = mv1_kernel<QT, NMAT, EPI>;
+    auto kern = mv1_kernel<QT, NMAT, EPI, XS>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return cuda_fail(e, "mv1: cudaFuncSetAttribute");
@@ -872,15 +996,20 @@ static int launch_mv1_t(Mv1Args a, cudaStream_t stream) {
     return check_launch("mv1_kernel");
 }
 
-int launch_mv1(int qtype, int nmat, int epi, const Mv1Args& a, cudaStream_t s) {
-    if (qtype == MUSER_Q4_K) {
-        if (nmat == 1 && epi == kEpiStore) return launch_mv1_t<MUSER_Q4_K, 1, kEpiStore>(a, s);
-        if (nmat == 1 && epi == kEpiTail) return launch_mv1_t<MUSER_Q4_K, 1, kEpiTail>(a, s);
-        if (nmat == 2 && epi == kEpiSiluMul) return launch_mv1_t<MUSER_Q4_K, 2, kEpiSiluMul>(a, s);
+int launch_mv1(int qtype, int nmat, int epi, const Mv1Args& a, cudaStream_t s, int xs) {
+    if (xs == kXTail) {
+        if (qtype == MUSER_Q4_K && nmat == 2 && epi == kEpiSiluMul)
+            return launch_mv1_t<MUSER_Q4_K, 2, kEpiSiluMul, kXTail>(a, s);
+        if (qtype == MUSER_Q6_K && nmat == 2 && epi == kEpiSiluMul)
+            return launch_mv1_t<MUSER_Q6_K, 2, kEpiSiluMul, kXTail>(a, s);
+    } else if (qtype == MUSER_Q4_K) {
+        if (nmat == 1 && epi == kEpiStore) return launch_mv1_t<MUSER_Q4_K, 1, kEpiStore, kXMemory>(a, s);
+        if (nmat == 1 && epi == kEpiTail) return launch_mv1_t<MUSER_Q4_K, 1, kEpiTail, kXMemory>(a, s);
+        if (nmat == 2 && epi == kEpiSiluMul) return launch_mv1_t<MUSER_Q4_K, 2, kEpiSiluMul, kXMemory>(a, s);
     } else if (qtype == MUSER_Q6_K) {
-        if (nmat == 1 && epi == kEpiStore) return launch_mv1_t<MUSER_Q6_K, 1, kEpiStore>(a, s);
-        if (nmat == 1 && epi == kEpiTail) return launch_mv1_t<MUSER_Q6_K, 1, kEpiTail>(a, s);
-        if (nmat == 2 && epi == kEpiSiluMul) return launch_mv1_t<MUSER_Q6_K, 2, kEpiSiluMul>(a, s);
+        if (nmat == 1 && epi == kEpiStore) return launch_mv1_t<MUSER_Q6_K, 1, kEpiStore, kXMemory>(a, s);
+        if (nmat == 1 && epi == kEpiTail) return launch_mv1_t<MUSER_Q6_K, 1, kEpiTail, kXMemory>(a, s);
+        if (nmat == 2 && epi == kEpiSiluMul) return launch_mv1_t<MUSER_Q6_K, 2, kEpiSiluMul, kXMemory>(a, s);
     }
     return set_error(MUSER_ERR_UNSUPPORTED, "mv1: no kernel for qtype %d nmat %d epilogue %d", qtype, nmat, epi);
 }

@@ -144,6 +144,31 @@ def test_ffn_gate_up_silu(M, with_scratch):
     assert_close(got, ref, f"gate_up_silu M={M}", scaled=True)
 
 
+@pytest.mark.parametrize("M,ffn", [(1, 19968), (1, 2001), (3, 2003)])
+def test_ffn_gate_up_silu_tail(M, ffn):
+    """The layer boundary: the previous tail then gate/up/SiLU.  One row of x
+    runs the tail inside the gate/up kernel (every block computes x, block 0
+    writes residual and x_out); M = 3 runs the two calls."""
+    hidden = 6656
+    Wg = synth.q4k_matrix(ffn, hidden, seed=40 + M, tensor=synth.T_GATE)
+    Wu = synth.q4k_matrix(ffn, hidden, seed=40 + M, tensor=synth.T_UP)
+    r = synth.normal((M, hidden), seed=41, tensor=synth.T_RESID)
+    p = synth.normal((M, hidden), seed=41, tensor=synth.T_X) * np.float32(2.5e6)
+    w1 = synth.norm_weight(hidden, seed=42, tensor=synth.T_W1)
+    w2 = synth.norm_weight(hidden, seed=42, tensor=synth.T_W2)
+    rd, x_out, mid = dev(r), nan_like((M, hidden), extra=32), nan_like((M, ffn), extra=32)
+    mu.muser_ffn_gate_up_silu_tail("q4_k", dev(Wg), dev(Wu), ffn, hidden, dev(p), rd, dev(w1), dev(w2),
+                                   1e-8, 1e-5, x_out, M, mid)
+    r_ref, x_ref = oracle.dual_tail(r, p, w1, w2, 1e-8, 1e-5)
+    mid_ref = oracle.gate_up_silu("q4_k", Wg, Wu, ffn, hidden, x_ref)
+    assert_close(host(rd).reshape(M, hidden), r_ref, "tail residual")
+    assert_close(host(x_out[:M * hidden]).reshape(M, hidden), x_ref, "tail x_out")
+    assert_close(host(mid[:M * ffn]).reshape(M, ffn), mid_ref, f"gate_up_silu after the tail M={M}", scaled=True)
+    check_canary(x_out, M * hidden)
+    check_canary(mid, M * ffn)
+    assert mu.muser_device_status() == 0
+
+
 def test_silu_mul_and_rms_norm():
     a, b = synth.ffn_mid_factors(19968, 3, seed=9)
     out = nan_like((3, 19968))
