@@ -114,12 +114,33 @@ __device__ __forceinline__ float byte_to_f(uint32_t word, uint32_t sel_with_magi
     return __uint_as_float(__byte_perm(word, 0x4B000000u, sel_with_magic)) - 8388608.0f;
 }
 
+__device__ __forceinline__ uint4 lds_uint4(const void* p) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(static_cast<uint32_t>(__cvta_generic_to_shared(p))));
+    return v;
+}
+__device__ __forceinline__ void sts_uint4(void* p, uint4 v) {
+    asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(p))),
+                 "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                 : "memory");
+}
 // 16-byte shared-memory store (p 16-byte aligned, in shared memory).
 __device__ __forceinline__ void sts_float4(void* p, float4 v) {
     asm volatile("st.shared.v4.f32 [%0], {%1,%2,%3,%4};" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(p))),
                  "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w)
                  : "memory");
 }
+// 16-byte asynchronous copy global -> shared (both 16-byte aligned), and
+// the waits on this thread's copies.
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(dst))),
+                 "l"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 // Barrier `id` (1..15) over the first `nthreads` threads of the block (a
 // multiple of 32; every warp taking part calls it).
 __device__ __forceinline__ void named_barrier_sync(int id, int nthreads) {

@@ -101,48 +101,6 @@ struct SliceQ4 {
     float inv;          // 2^-e
 };
 
-// xs: the slice's 64 inputs in shared memory (its slot, see XSlots).
-__device__ __forceinline__ void load_slice_q4(SliceQ4& s, const float* xs) {
-    float v[64];
-#pragma unroll
-    for (int q = 0; q < 16; ++q) {
-        const float4 f = lds_float4(xs + 4 * q);
-        v[4 * q + 0] = f.x;
-        v[4 * q + 1] = f.y;
-        v[4 * q + 2] = f.z;
-        v[4 * q + 3] = f.w;
-    }
-    float m = 0.0f, slo = 0.0f, shi = 0.0f;
-#pragma unroll
-    for (int l = 0; l < 32; ++l) {
-        m = fmaxf(m, fmaxf(fabsf(v[l]), fabsf(v[32 + l])));
-        slo += v[l];
-        shi += v[32 + l];
-    }
-    const int e = slice_exponent(m);
-    const float p2e = pow2f(e);
-    s.inv = pow2f(-e);
-    s.s_lo = slo;
-    s.s_hi = shi;
-#pragma unroll
-    for (int t = 0; t < 8; ++t) {
-        int XL[4], XH[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            XL[i] = __float2int_rn(v[4 * t + i] * p2e);
-            XH[i] = __float2int_rn(v[32 + 4 * t + i] * p2e);
-        }
-        uint32_t wl[3], wh[3];
-        pack_digits(XL[0], XL[1], XL[2], XL[3], wl);
-        pack_digits(XH[0], XH[1], XH[2], XH[3], wh);
-#pragma unroll
-        for (int k = 0; k < 3; ++k) {
-            s.lo[k][t] = wl[k];
-            s.hi[k][t] = wh[k];
-        }
-    }
-}
-
 // Q6_K slice (b, c = 2h + j): weights 128h + 32g + 16j + l, g = 0..3,
 // l = 0..15 (sub-blocks 8h + 2g + j); word i of a code field covers
 // l = 4i..4i+3, or l = 4i-2..4i+1 (mod 16) when the block is rotated.
@@ -157,7 +115,86 @@ struct SliceQ6 {
 // bytes 2..13 and one byte permute folds W4 (bytes 14, 15) and W0 (bytes 0, 1)
 // into the first word, so word i of the field holds bytes 4i-2..4i+1 (mod 16)
 // and the slice's digit words are rotated the same way.
-// xs: the slice's four 16-input groups in shared memory, group g at 16g.
+// ------------------------------------------------ slice conversion
+// The consumer threads convert the slices in quarters: quarter k of slot s
+// holds 16 of its 64 inputs (Q4_K: words 4(k&1)..4(k&1)+3 of the low half
+// for k < 2, of the high half for k >= 2; Q6_K: group k).  The four quarters
+// of a slot sit in four neighbouring lanes, which agree on the slot's
+// exponent with two shuffles.  The digit words and the slot's scalars then
+// overwrite the slot's inputs, and every thread loads the record of its own
+// slot.  Record layouts (32-bit words):
+//   Q4_K: lo[d][t] at 8d + t, hi[d][t] at 24 + 8d + t; inv, s_lo, s_hi at 48..50.
+//   Q6_K: x[g][d][i] at 12g + 4d + i; neg32[g][d] at 48 + 3g + d; inv at 60.
+// All 32 lanes of a warp call it (shuffles); a lane with !valid converts
+// zeros and stores nothing.
+template <int QT>
+__device__ __forceinline__ void convert_quarter(uint8_t* slot, int k, bool valid, bool rot) {
+    float v[16];
+    const float* xs = reinterpret_cast<const float*>(slot) + 16 * k;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const float4 f = valid ? lds_float4(xs + 4 * q) : make_float4(0.f, 0.f, 0.f, 0.f);
+        v[4 * q + 0] = f.x;
+        v[4 * q + 1] = f.y;
+        v[4 * q + 2] = f.z;
+        v[4 * q + 3] = f.w;
+    }
+    float m = 0.0f;
+#pragma unroll
+    for (int l = 0; l < 16; ++l) m = fmaxf(m, fabsf(v[l]));
+    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+    const int e = slice_exponent(m);
+    const float p2e = pow2f(e);
+    const float inv = pow2f(-e);
+    uint32_t D[4][3];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        pack_digits(__float2int_rn(v[4 * i] * p2e), __float2int_rn(v[4 * i + 1] * p2e),
+                    __float2int_rn(v[4 * i + 2] * p2e), __float2int_rn(v[4 * i + 3] * p2e), D[i]);
+    uint32_t* rec = reinterpret_cast<uint32_t*>(slot);
+    if constexpr (QT == MUSER_Q4_K) {
+        float sum = 0.0f;
+#pragma unroll
+        for (int l = 0; l < 16; ++l) sum += v[l];
+        sum += __shfl_xor_sync(0xffffffffu, sum, 1);  // the half's sum (quarters 2j, 2j + 1)
+        __syncwarp();
+        if (valid) {
+            const int base = (k >= 2 ? 24 : 0) + 4 * (k & 1);
+#pragma unroll
+            for (int d = 0; d < 3; ++d) sts_uint4(rec + base + 8 * d, make_uint4(D[0][d], D[1][d], D[2][d], D[3][d]));
+            if (k == 0) {
+                rec[48] = __float_as_uint(inv);
+                rec[49] = __float_as_uint(sum);
+            }
+            if (k == 2) rec[50] = __float_as_uint(sum);
+        }
+    } else {
+        int sums[3] = {0, 0, 0};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            sums[0] = dp4a_uu(D[i][0], 0x01010101u, sums[0]);
+            sums[1] = dp4a_uu(D[i][1], 0x01010101u, sums[1]);
+            sums[2] = dp4a_us(0x01010101u, D[i][2], sums[2]);
+        }
+        // a rotated word i holds bytes 4i - 2 .. 4i + 1 (mod 16) of the field
+        const uint32_t rsel = rot ? 0x5432u : 0x7654u;
+        __syncwarp();
+        if (valid) {
+#pragma unroll
+            for (int d = 0; d < 3; ++d)
+                sts_uint4(rec + 12 * k + 4 * d,
+                          make_uint4(__byte_perm(D[3][d], D[0][d], rsel), __byte_perm(D[0][d], D[1][d], rsel),
+                                     __byte_perm(D[1][d], D[2][d], rsel), __byte_perm(D[2][d], D[3][d], rsel)));
+#pragma unroll
+            for (int d = 0; d < 3; ++d) rec[48 + 3 * k + d] = static_cast<uint32_t>(-32 * sums[d]);
+            if (k == 0) rec[60] = __float_as_uint(inv);
+        }
+    }
+}
+
+// One thread converts a whole Q6_K slot (four 16-input groups, group g at xs
+// + 16g) into its own slice.
 __device__ __forceinline__ void load_slice_q6(SliceQ6& s, const float* xs, bool rot) {
     float v[4][16];
     float m = 0.0f;
@@ -200,6 +237,40 @@ __device__ __forceinline__ void load_slice_q6(SliceQ6& s, const float* xs, bool 
             for (int i = 0; i < 4; ++i) s.x[g][k][i] = __byte_perm(D[(i + 3) & 3][k], D[i][k], rsel);
         }
     }
+}
+
+__device__ __forceinline__ void load_record(SliceQ4& s, const uint8_t* slot) {
+    const uint32_t* rec = reinterpret_cast<const uint32_t*>(slot);
+#pragma unroll
+    for (int d = 0; d < 3; ++d)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const uint4 a = lds_uint4(rec + 8 * d + 4 * h), b = lds_uint4(rec + 24 + 8 * d + 4 * h);
+            s.lo[d][4 * h + 0] = a.x; s.lo[d][4 * h + 1] = a.y; s.lo[d][4 * h + 2] = a.z; s.lo[d][4 * h + 3] = a.w;
+            s.hi[d][4 * h + 0] = b.x; s.hi[d][4 * h + 1] = b.y; s.hi[d][4 * h + 2] = b.z; s.hi[d][4 * h + 3] = b.w;
+        }
+    const uint4 t = lds_uint4(rec + 48);
+    s.inv = __uint_as_float(t.x);
+    s.s_lo = __uint_as_float(t.y);
+    s.s_hi = __uint_as_float(t.z);
+}
+__device__ __forceinline__ void load_record(SliceQ6& s, const uint8_t* slot) {
+    const uint32_t* rec = reinterpret_cast<const uint32_t*>(slot);
+#pragma unroll
+    for (int g = 0; g < 4; ++g)
+#pragma unroll
+        for (int d = 0; d < 3; ++d) {
+            const uint4 a = lds_uint4(rec + 12 * g + 4 * d);
+            s.x[g][d][0] = a.x; s.x[g][d][1] = a.y; s.x[g][d][2] = a.z; s.x[g][d][3] = a.w;
+        }
+#pragma unroll
+    for (int q = 0; q < 3; ++q) {
+        const uint4 a = lds_uint4(rec + 48 + 4 * q);
+        const uint32_t w[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+        for (int u = 0; u < 4; ++u) s.neg32[(4 * q + u) / 3][(4 * q + u) % 3] = static_cast<int>(w[u]);
+    }
+    s.inv = __uint_as_float(rec[60]);
 }
 
 // ------------------------------------------------ rows x one slice (dot)
@@ -265,7 +336,7 @@ __device__ __forceinline__ void dot_q4(const SliceQ4& s, const uint8_t* const* b
 
 // Code-field loads.  kAlign: the field is 4-byte aligned.  kRotated: the
 // field sits 2 bytes past a word boundary and the thread's input slice is
-// rotated to match (load_slice_q6): word 0 = (bytes 14,15,0,1), words 1..3 =
+// rotated to match (convert_quarter): word 0 = (bytes 14,15,0,1), words 1..3 =
 // the aligned words W1..W3 from p - 2.  kRealign: 2 bytes past a boundary,
 // words realigned by byte permutes (rows whose alignment alternates).
 constexpr int kAlign = 0, kRotated = 1, kRealign = 2;
@@ -637,11 +708,16 @@ __global__ void __launch_bounds__(512, 1) mv1_kernel(const Mv1Args p) {
         pdl_launch_dependents();
         using Slice = typename std::conditional<QT == MUSER_Q4_K, SliceQ4, SliceQ6>::type;
         Slice sl;
-        pdl_wait();  // x is the previous kernel's output
+        // Every block reads all of x: block b starts its loads at float4 number
+        // b * n4 / grid (then wraps), so the blocks do not all ask for the
+        // same lines of L2 at the same time.
+        const int n4 = nbc * 16, nthr = ncw * 32;
+        const int x0 = static_cast<int>((static_cast<int64_t>(blockIdx.x) * n4) / gridDim.x);
+        auto xi = [&](int j) { return j + x0 < n4 ? j + x0 : j + x0 - n4; };
         if constexpr (XS == kXTail) {
             // The tail of the previous layer, at most 4 float4 of each vector
-            // per thread (the launcher checks), in registers.
-            const int n4 = nbc * 16, nthr = ncw * 32;
+            // per thread (the launcher checks), in registers.  The norm
+            // weights do not depend on the previous kernel.
             const float n = static_cast<float>(nbc * 64);
             const float4* p4 = reinterpret_cast<const float4*>(p.x);
             const float4* r4 = reinterpret_cast<const float4*>(p.resid);
@@ -650,12 +726,19 @@ __global__ void __launch_bounds__(512, 1) mv1_kernel(const Mv1Args p) {
             float4 pv[4], rv[4], av[4], bv[4];
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
-                const int i = tid + u * nthr;
-                if (i < n4) {
-                    pv[u] = __ldcg(p4 + i);
-                    rv[u] = __ldcg(r4 + i);
-                    av[u] = __ldg(a4 + i);
-                    bv[u] = __ldg(b4 + i);
+                const int j = tid + u * nthr;
+                if (j < n4) {
+                    av[u] = __ldg(a4 + xi(j));
+                    bv[u] = __ldg(b4 + xi(j));
+                }
+            }
+            pdl_wait();  // projected and the residual are the previous kernels' outputs
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int j = tid + u * nthr;
+                if (j < n4) {
+                    pv[u] = __ldcg(p4 + xi(j));
+                    rv[u] = __ldcg(r4 + xi(j));
                 }
             }
             __syncwarp();
@@ -690,8 +773,9 @@ __global__ void __launch_bounds__(512, 1) mv1_kernel(const Mv1Args p) {
             const float inv2 = 1.0f / sqrtf(sh / n + p.eps2);
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
-                const int i = tid + u * nthr;
-                if (i < n4) {
+                const int j = tid + u * nthr;
+                if (j < n4) {
+                    const int i = xi(j);
                     const float4 xv = make_float4((rv[u].x * inv2) * bv[u].x, (rv[u].y * inv2) * bv[u].y,
                                                   (rv[u].z * inv2) * bv[u].z, (rv[u].w * inv2) * bv[u].w);
                     sts_float4(xslots + xslot_offset(i, QT == MUSER_Q4_K, parity_split, p.HP), xv);
@@ -702,27 +786,38 @@ __global__ void __launch_bounds__(512, 1) mv1_kernel(const Mv1Args p) {
                 }
             }
         } else {
-            // All of a thread's loads (at most 16: x holds 16 float4 per slice
+            // All of a thread's copies (at most 16: x holds 16 float4 per slice
             // and there are at least as many consumer threads as slices) are
             // in flight before the copy warp queues more weight requests.
+            // 16-byte asynchronous copies straight into the slots.
+            pdl_wait();  // x is the previous kernel's output
             const float4* x4 = reinterpret_cast<const float4*>(p.x);
-            const int n4 = nbc * 16, nthr = ncw * 32;
-            float4 v[16];
 #pragma unroll
             for (int u = 0; u < 16; ++u)
-                if (tid + u * nthr < n4) v[u] = __ldg(x4 + tid + u * nthr);
+                if (tid + u * nthr < n4) {
+                    const int i = xi(tid + u * nthr);
+                    cp_async16(xslots + xslot_offset(i, QT == MUSER_Q4_K, parity_split, p.HP), x4 + i);
+                }
+            cp_async_commit();
             __syncwarp();
             if (lane == 0) mbar_arrive(xissued);
-#pragma unroll
-            for (int u = 0; u < 16; ++u)
-                if (tid + u * nthr < n4)
-                    sts_float4(xslots + xslot_offset(tid + u * nthr, QT == MUSER_Q4_K, parity_split, p.HP), v[u]);
+            cp_async_wait_all();
         }
         named_barrier_sync(1, ncw * 32);  // the consumer warps only
-        if (active) {
-            const float* xs = reinterpret_cast<const float*>(xslots + idx * kXSlot);
-            if constexpr (QT == MUSER_Q4_K) load_slice_q4(sl, xs);
-            else load_slice_q6(sl, xs, parity_split && (b & 1));
+        if (QT == MUSER_Q4_K || G > 1) {
+            // Every slot converted once, a quarter per thread (the row groups
+            // share the slots), then each thread loads its own slot's record.
+            for (int q0 = 0; q0 < 4 * p.TG; q0 += nthr) {
+                const int q = q0 + tid, sq = q >> 2;
+                int bq = 0, cq = 0;
+                const bool valid = q < 4 * p.TG && slice_of(sq, nbc, parity_split, p.HP, bq, cq);
+                convert_quarter<QT>(xslots + (valid ? sq : 0) * kXSlot, q & 3, valid, parity_split && (bq & 1));
+            }
+            named_barrier_sync(1, ncw * 32);
+            if (active) load_record(sl, xslots + idx * kXSlot);
+        } else if constexpr (QT == MUSER_Q6_K) {
+            // one row group: each slot has one thread, which converts it
+            if (active) load_slice_q6(sl, reinterpret_cast<const float*>(xslots + idx * kXSlot), parity_split && (b & 1));
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(xready);
