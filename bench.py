@@ -45,9 +45,9 @@ METRIC = "weight-stream GB/s (% of GB300 HBM peak); decode FFN tokens/sec, 1 GPU
 
 # ncu DRAM traffic of the dominant kernel, per launch, with the source hash it
 # was captured on (profiles/ summary); reported as null once the kernel changed.
-NCU_TRAFFIC = {"kernel": "mv1_kernel<Q4_K,2,silu>", "bytes_per_launch": 152660480,
-               "source_sha256": "9f98676aa555252a8f6dc452556bb4317824063669020f834850e26f9060c4ce",
-               "profile": "profiles/mv1_gate_up_q4k_and_down_q6k_tail.md"}
+NCU_TRAFFIC = {"kernel": "mv1_kernel<Q4_K,2,silu,tail>", "bytes_per_launch": 152817408,
+               "source_sha256": "f088ecaebb34366d0e440b2926e6ec3bccb3abb30db6912f621577d32f656128",
+               "profile": "profiles/mv1_fused_gate_up_tail_q4k_and_down_q6k_m1.md"}
 
 
 def _env_int(k, d):
