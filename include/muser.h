@@ -180,7 +180,11 @@ int muser_ffn_gate_up_silu_tail(int qtype, const void* Wg, const void* Wu, int64
                                 const float* w1, const float* w2, float eps1, float eps2,
                                 float* x_out, int M, float* mid, void* stream);
 
-/* Scratch bytes muser_qmatvec_residual_dual_rmsnorm needs (a small constant). */
+/* Scratch bytes muser_qmatvec_residual_dual_rmsnorm should get: 1 KiB for the
+ * one-row kernel (its completion ticket, then one sum of projected^2 per
+ * block, which spares the tail one pass over the row) plus the tensor-core
+ * kernel's tickets and partial sums for several rows.  256 bytes (the ticket)
+ * is the minimum the call accepts. */
 size_t muser_scratch_bytes(int64_t hidden, int M);
 
 /*
