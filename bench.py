@@ -7,6 +7,8 @@ input RMSNorm (layer 0 only) -> Q4_K gate/up 19968x6656 with SiLU gating ->
 Q6_K down 6656x19968 with the dual-eps fused tail.  A step streams the 52
 layers' 13.44 GB of distinct weights (far larger than the 129 MB L2).
 `--workload stack52_m16` runs the same stack at M = 16 (speculative verify).
+`--workload attn52_m1` / `attn52_m16` run the attention side of the same
+layers (Q, K, V, gate projections; o_proj with the first dual-eps tail).
 
 Arms:
   --impl native     libmuser (CUDA, sm_103a) through its C ABI.
@@ -20,6 +22,7 @@ its own GPU; the value is the sum over ranks, timed by the slowest rank.
 from __future__ import annotations
 
 import argparse
+import ctypes
 import hashlib
 import json
 import os
@@ -460,6 +463,170 @@ def cpu_baseline(seconds: float, frac_rows: float = 0.125):
                       f"weights), {t_tot:.1f} s"}
 
 
+QD, KVD = synth.Q_DIM, synth.KV_DIM
+ATTN_W = (2 * QD + 2 * KVD) * (H // 256) * 144 + H * (QD // 256) * 144  # Q, K, V, gate, o_proj (Q4_K)
+
+
+def run_attn(args, rank, world):
+    """The attention-side weight stream of one decode token through the
+    layers (Ch 10 Figure 10.1 boxes 4, 9, 10): per layer the Q, K, V and gate
+    projections as one group (muser_qmatvec_group; from layer 1 with the
+    previous layer's post-attention tail fused in, muser_qmatvec_group_tail),
+    then o_proj (muser_qmatvec); the last tail once per step.  The tail's
+    output (the FFN input in the model) stands in for the next layer's normed
+    input.  Attention itself is outside the path: o_proj reads a seeded
+    stand-in for its output."""
+    import torch
+    import quantized_weight_streaming_q4_gb300 as mu
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(_env_int("LOCAL_RANK", 0))
+        dist.init_process_group("nccl")
+    mu.build()
+    L = mu.lib()
+    M = 16 if args.workload == "attn52_m16" else 1
+    nl, wl = args.layers, synth.ATTN_WORKLOAD
+    t0 = time.time()
+    layers = []
+    for l in range(nl):
+        A = synth.attn_layer(l, H)
+        d = {k: torch.from_numpy(v).cuda() for k, v in A.items()}
+        d["w_ffn"] = torch.from_numpy(synth.input_norm_weight(l + 1, H, workload=wl)).cuda()
+        layers.append(d)
+    gen_s = time.time() - t0
+    w_in = torch.from_numpy(synth.input_norm_weight(0, H, workload=wl)).cuda()
+    r0 = synth.residual_rows(M, H, workload=wl)
+    resid = torch.from_numpy(r0).cuda()
+    attn = torch.from_numpy(synth.attn_output(M)).cuda()
+    x = torch.empty(M, H, dtype=torch.float32, device="cuda")
+    q, g = (torch.empty(M, QD, dtype=torch.float32, device="cuda") for _ in range(2))
+    k, v = (torch.empty(M, KVD, dtype=torch.float32, device="cuda") for _ in range(2))
+    proj = torch.empty(M, H, dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream()
+    sh = stream.cuda_stream
+
+    def rc(name, r):
+        if r != 0:
+            raise RuntimeError(f"{name}: {mu.muser_last_error()}")
+
+    rows4 = (ctypes.c_int64 * 4)(QD, KVD, KVD, QD)
+    ys4 = (ctypes.c_void_p * 4)(q.data_ptr(), k.data_ptr(), v.data_ptr(), g.data_ptr())
+    w4 = [(ctypes.c_void_p * 4)(*[d[n].data_ptr() for n in ("Wq", "Wk", "Wv", "Wg")]) for d in layers]
+
+    def step(events=None):
+        rc("rms_norm", L.muser_rms_norm(resid.data_ptr(), w_in.data_ptr(), x.data_ptr(), H, M, 1e-5, sh))
+        prev = None
+        for l, d in enumerate(layers):
+            ev = events.get(l) if events is not None else None
+            if ev is not None:
+                ev[0].record(stream)
+            if prev is None:
+                rc("qkvg", L.muser_qmatvec_group(12, 4, w4[l], rows4, H, x.data_ptr(), M, ys4, sh))
+            else:
+                rc("qkvg_tail", L.muser_qmatvec_group_tail(
+                    12, 4, w4[l], rows4, H, proj.data_ptr(), resid.data_ptr(), prev["w_post"].data_ptr(),
+                    prev["w_ffn"].data_ptr(), 1e-8, 1e-5, x.data_ptr(), M, ys4, sh))
+            if ev is not None:
+                ev[1].record(stream)
+            rc("o_proj", L.muser_qmatvec(12, d["Wo"].data_ptr(), H, QD, attn.data_ptr(), M, proj.data_ptr(), sh))
+            if ev is not None:
+                ev[2].record(stream)
+            prev = d
+        rc("tail", L.muser_fused_residual_dual_rmsnorm(resid.data_ptr(), proj.data_ptr(), x.data_ptr(),
+                                                       prev["w_post"].data_ptr(), prev["w_ffn"].data_ptr(),
+                                                       H, M, 1e-8, 1e-5, sh))
+
+    def barrier():
+        torch.cuda.synchronize()
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    for _ in range(args.warmup):
+        step()
+    barrier()
+    uuid = None
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(torch.cuda.current_device()).uuid)
+    except Exception:
+        pass
+    clocks = ClockSampler(uuid)
+    clocks.start()
+    time.sleep(0.3)
+    probes = min(PROBES, nl)
+    events = []
+    for kk in range(args.steps):
+        ls = sorted({(kk + j * max(1, nl // probes)) % nl for j in range(probes)})
+        events.append({l: [torch.cuda.Event(enable_timing=True) for _ in range(3)] for l in ls})
+    barrier()
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for kk in range(args.steps):
+        step(events[kk])
+    t_end.record(stream)
+    barrier()
+    ms = t_start.elapsed_time(t_end) / args.steps
+    clock = clocks.stop()
+    q_ms = statistics.mean(t[0].elapsed_time(t[1]) for ev in events for t in ev.values())
+    o_ms = statistics.mean(t[1].elapsed_time(t[2]) for ev in events for t in ev.values())
+    if dist is not None:
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    # e2e: the same calls with the residual in from pinned host memory and x out
+    h_in = torch.from_numpy(r0.copy()).pin_memory()
+    h_out = torch.empty(M, H, dtype=torch.float32).pin_memory()
+    for _ in range(max(1, min(3, args.warmup))):
+        resid.copy_(h_in, non_blocking=True)
+        step()
+        h_out.copy_(x, non_blocking=True)
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        resid.copy_(h_in, non_blocking=True)
+        step()
+        h_out.copy_(x, non_blocking=True)
+    e1.record(stream)
+    barrier()
+    e2e_ms = e0.elapsed_time(e1) / args.steps
+    assert np.isfinite(h_out.numpy()).all()
+    peak, peak_kind = read_peaks()
+    weight_bytes = nl * ATTN_W
+    # the group with the previous tail: four matrices; p, r in/out, w1, w2, x out; four outputs
+    q_bytes = (2 * QD + 2 * KVD) * (H // 256) * 144 + 4 * M * H * 6 + 4 * M * (2 * QD + 2 * KVD)
+    o_bytes = H * (QD // 256) * 144 + 4 * M * QD + 4 * M * H
+    gbs = world * weight_bytes / (ms * 1e-3) / 1e9
+    achieved = q_bytes / (q_ms * 1e-3) / 1e9
+    return {
+        "metric": METRIC, "value": round(gbs, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded Q4_K fields per the workload recipe; a seeded stand-in for the attention output)",
+        "config": {"workload": f"attention-side weight stream: {nl} layers x [previous dual-eps tail -> Q {QD}x{H}, "
+                               f"K {KVD}x{H}, V {KVD}x{H}, gate {QD}x{H} (Q4_K) -> o_proj {H}x{QD} (Q4_K)], M={M}",
+                   "layers": nl, "hidden": H, "M": M, "weight_bytes_per_step": weight_bytes,
+                   "l2": f"inputs larger than L2: {weight_bytes / 1e9:.2f} GB of distinct weights per step vs 129 MB L2",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "tokens_per_s": round(world * M / (ms * 1e-3), 3),
+        "hbm_frac_of_" + peak_kind: round(gbs / world / peak, 4),
+        "roofline": {"bound": "hbm", "kernel": f"muser_qmatvec_group_tail (Q, K, V, gate Q4_K with the previous "
+                                               f"tail, M={M}; one launch at M = 1)",
+                     "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "traffic": None, "algorithmic_bytes_per_launch": q_bytes, "mean_launch_us": round(q_ms * 1e3, 2),
+                     "second_kernel": {"name": "muser_qmatvec (o_proj)",
+                                       "achieved_gbs": round(o_bytes / (o_ms * 1e-3) / 1e9, 1),
+                                       "mean_launch_us": round(o_ms * 1e3, 2),
+                                       "algorithmic_bytes_per_launch": o_bytes}},
+        "e2e": {"value": round(world * weight_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+                "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": 4 * M * H, "d2h_bytes_per_step": 4 * M * H,
+                "api": "per-layer muser_qmatvec_group[_tail] / muser_qmatvec calls, host residual in, x out"},
+        "gpu_launches": args.steps * (2 + 2 * nl) if M == 1 else None,
+        "clocks": clock, "device_status": mu.muser_device_status(), "weights_generation_s": round(gen_s, 1),
+    }
+
+
 def run_reference(args, rank, world):
     if rank != 0:
         return None
@@ -497,7 +664,8 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
-    ap.add_argument("--workload", choices=["stack52_m1", "stack52_m16"], default="stack52_m1")
+    ap.add_argument("--workload", choices=["stack52_m1", "stack52_m16", "attn52_m1", "attn52_m16"],
+                    default="stack52_m1")
     ap.add_argument("--layers", type=int, default=NL)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--ref-frac", type=float, default=0.0625)
@@ -508,6 +676,8 @@ def main():
     rank, world = _env_int("RANK", 0), _env_int("WORLD_SIZE", 1)
     if args.impl == "reference":
         res = run_reference(args, rank, world)
+    elif args.workload.startswith("attn"):
+        res = run_attn(args, rank, world)
     else:
         res = run_native(args, rank, world)
     if rank == 0 and res is not None:

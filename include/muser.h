@@ -156,6 +156,33 @@ int muser_fused_residual_dual_rmsnorm(float* residual, const float* src, float* 
                                       float eps2, void* stream);
 
 /*
+ * muser_qmatvec_group -- n (1..4) matvecs of one input, y_i = W_i . x, as the
+ *   book issues the attention projections Q, K, V and gate: one concurrent
+ *   group reading one shared normed input (Ch 10 Figure 10.1 box 4, §10.3
+ *   (e)).  W[i]: device matrices [rows[i] x cols] of `qtype`; x: device f32
+ *   [M*cols]; y[i]: device f32 [M*rows[i]].  W, rows and y are host arrays of
+ *   n entries.  For one row of x and Q4_K the n matrices stream in one launch,
+ *   their rows taken as one matrix; otherwise each runs as muser_qmatvec.
+ *   Results are those of n muser_qmatvec calls.  Fail-closed like
+ *   muser_qmatvec.
+ */
+int muser_qmatvec_group(int qtype, int n, const void* const* W, const int64_t* rows, int64_t cols,
+                        const float* x, int M, float* const* y, void* stream);
+
+/*
+ * muser_qmatvec_group_tail -- the previous sub-block's dual-eps tail, then
+ *   the group on its output: as muser_fused_residual_dual_rmsnorm (src =
+ *   projected, out = x_out, n = cols) followed by muser_qmatvec_group with
+ *   x = x_out.  With one row of x and Q4_K the tail runs inside the group's
+ *   launch, every block for itself.  projected, residual, x_out: device f32
+ *   [M*cols], distinct; w1, w2: device f32 [cols]; cols % 4 == 0;
+ *   eps1, eps2 > 0.
+ */
+int muser_qmatvec_group_tail(int qtype, int n, const void* const* W, const int64_t* rows, int64_t cols,
+                             const float* projected, float* residual, const float* w1, const float* w2,
+                             float eps1, float eps2, float* x_out, int M, float* const* y, void* stream);
+
+/*
  * muser_ffn_gate_up_silu_tail -- the boundary between two decode layers in
  *   one call: the previous layer's dual-eps tail (Ch 19 §19.4, as
  *   muser_fused_residual_dual_rmsnorm with src = projected, out = x_out),

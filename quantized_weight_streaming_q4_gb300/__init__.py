@@ -20,7 +20,7 @@ __all__ = [
     "muser_version", "muser_last_error", "muser_block_bytes", "muser_matrix_bytes",
     "muser_dequantize", "muser_qmatvec", "muser_rms_norm", "muser_silu_mul",
     "muser_ffn_gate_up_silu", "muser_gate_up_scratch_bytes", "muser_ffn_gate_up_silu_scratch",
-    "muser_ffn_gate_up_silu_tail",
+    "muser_ffn_gate_up_silu_tail", "muser_qmatvec_group", "muser_qmatvec_group_tail",
     "muser_fused_residual_dual_rmsnorm", "muser_scratch_bytes",
     "muser_qmatvec_residual_dual_rmsnorm", "muser_qmatvec_residual_dual_rmsnorm_static",
     "MUSER_STATIC_SCRATCH_BYTES", "FfnLayer", "muser_ffn_workspace_bytes",
@@ -96,6 +96,8 @@ def lib():
             "muser_gate_up_scratch_bytes": (SZ, [I, I64, I64, I]),
             "muser_ffn_gate_up_silu_scratch": (I, [I, P, P, I64, I64, P, I, P, P, SZ, P]),
             "muser_ffn_gate_up_silu_tail": (I, [I, P, P, I64, I64, P, P, P, P, F, F, P, I, P, P]),
+            "muser_qmatvec_group": (I, [I, I, P, P, I64, P, I, P, P]),
+            "muser_qmatvec_group_tail": (I, [I, I, P, P, I64, P, P, P, P, F, F, P, I, P, P]),
             "muser_fused_residual_dual_rmsnorm": (I, [P, P, P, P, P, I, I, F, F, P]),
             "muser_scratch_bytes": (SZ, [I64, I]),
             "muser_qmatvec_residual_dual_rmsnorm": (I, [I, P, I64, I64, P, I, P, P, P, P, P, F, F, P,
@@ -209,6 +211,28 @@ def muser_ffn_gate_up_silu_tail(qtype, Wg, Wu, ffn: int, hidden: int, projected,
            lib().muser_ffn_gate_up_silu_tail(_qt(qtype), _ptr(Wg), _ptr(Wu), ffn, hidden, _ptr(projected),
                                              _ptr(residual), _ptr(w1), _ptr(w2), eps1, eps2, _ptr(x_out), M,
                                              _ptr(mid), _stream(stream)))
+
+
+def _group_arrays(Ws, rows, ys):
+    n = len(Ws)
+    if not (len(rows) == n == len(ys)):
+        raise ValueError("one row count and one output per matrix")
+    return (n, (ctypes.c_void_p * n)(*[_ptr(w) for w in Ws]), (ctypes.c_int64 * n)(*rows),
+            (ctypes.c_void_p * n)(*[_ptr(y) for y in ys]))
+
+
+def muser_qmatvec_group(qtype, Ws, rows, cols: int, x, M: int, ys, stream=None) -> None:
+    n, wa, ra, ya = _group_arrays(Ws, rows, ys)
+    _check("muser_qmatvec_group",
+           lib().muser_qmatvec_group(_qt(qtype), n, wa, ra, cols, _ptr(x), M, ya, _stream(stream)))
+
+
+def muser_qmatvec_group_tail(qtype, Ws, rows, cols: int, projected, residual, w1, w2, eps1: float, eps2: float,
+                             x_out, M: int, ys, stream=None) -> None:
+    n, wa, ra, ya = _group_arrays(Ws, rows, ys)
+    _check("muser_qmatvec_group_tail",
+           lib().muser_qmatvec_group_tail(_qt(qtype), n, wa, ra, cols, _ptr(projected), _ptr(residual), _ptr(w1),
+                                          _ptr(w2), eps1, eps2, _ptr(x_out), M, ya, _stream(stream)))
 
 
 def muser_fused_residual_dual_rmsnorm(residual, src, out, w1, w2, n: int, M: int, eps1: float,

@@ -356,6 +356,18 @@ int muser_qmatvec(int qtype, const void* W, int64_t rows, int64_t cols, const fl
         a.y0 = y;
         return launch_mv1(qtype, 1, kEpiStore, a, as_stream(stream));
     }
+    if (mvt_supported(qtype, 1, rows, cols, M)) {
+        // several rows of x: the tensor-core kernel (whole row tiles per CTA)
+        MvtArgs t{};
+        t.W[0] = static_cast<const uint8_t*>(W);
+        t.W[1] = t.W[0];
+        t.rows = rows;
+        t.nsb = static_cast<int>(cols / kQK);
+        t.x = x;
+        t.M = M;
+        t.y = y;
+        return launch_mvt(qtype, kEpiStore, t, nullptr, as_stream(stream));
+    }
     MvMArgs a{};
     a.W[0] = static_cast<const uint8_t*>(W);
     a.W[1] = a.W[0];
@@ -448,6 +460,88 @@ int muser_ffn_gate_up_silu_tail(int qtype, const void* Wg, const void* Wu, int64
         return set_error(MUSER_ERR_INVALID_ARG, "%s: projected, residual and x_out must be distinct", fn);
     return gate_up_tail_launch(qtype, Wg, Wu, ffn, hidden, projected, residual, w1, w2, eps1, eps2,
                                x_out, M, mid, as_stream(stream));
+}
+
+// Validation shared by the two group calls.
+static int check_group(const char* fn, int qtype, int n, const void* const* W, const int64_t* rows, int64_t cols,
+                       const float* x, int M, float* const* y) {
+    if (n < 1 || n > kMv1MaxSeg || W == nullptr || rows == nullptr || y == nullptr)
+        return set_error(MUSER_ERR_INVALID_ARG, "%s: need 1..%d matrices with their rows and outputs", fn, kMv1MaxSeg);
+    for (int i = 0; i < n; ++i) {
+        MUSER_TRY(check_matrix(fn, qtype, W[i], rows[i], cols));
+        MUSER_TRY(check_f32(fn, "y", y[i]));
+    }
+    MUSER_TRY(check_M(fn, M));
+    MUSER_TRY(check_f32(fn, "x", x));
+    return MUSER_OK;
+}
+
+// One launch over the group's rows when one row of x, Q4_K (rows of whole
+// 16-byte units) and the one-token kernel fit; otherwise one call per matrix.
+static int group_launch(int qtype, int n, const void* const* W, const int64_t* rows, int64_t cols, const float* x,
+                        int M, float* const* y, const float* projected, float* residual, const float* w1,
+                        const float* w2, float eps1, float eps2, float* x_out, cudaStream_t s) {
+    const bool tail = projected != nullptr;
+    const bool fused = M == 1 && qtype == MUSER_Q4_K &&
+                       (tail ? mv1_tail_prologue_supported(qtype, cols) : mv1_supported(qtype, cols));
+    if (fused) {
+        Mv1Args a{};
+        a.nseg = n;
+        int64_t r = 0;
+        for (int i = 0; i < n; ++i) {
+            a.segW[i] = static_cast<const uint8_t*>(W[i]);
+            a.seg0[i] = r;
+            a.segY[i] = y[i];
+            r += rows[i];
+        }
+        a.seg0[n] = r;
+        a.rows = r;
+        a.nsb = static_cast<int>(cols / kQK);
+        a.x = tail ? projected : x;
+        if (tail) {
+            a.resid = residual;
+            a.out = x_out;
+            a.w1 = w1;
+            a.w2 = w2;
+            a.eps1 = eps1;
+            a.eps2 = eps2;
+        }
+        return launch_mv1(qtype, 1, kEpiStore, a, s, tail ? kXTail : kXMemory);
+    }
+    const float* xin = x;
+    if (tail) {
+        MUSER_TRY(launch_dual_tail(residual, projected, x_out, w1, w2, static_cast<int>(cols), M, eps1, eps2, s));
+        xin = x_out;
+    }
+    for (int i = 0; i < n; ++i) MUSER_TRY(muser_qmatvec(qtype, W[i], rows[i], cols, xin, M, y[i], s));
+    return MUSER_OK;
+}
+
+int muser_qmatvec_group(int qtype, int n, const void* const* W, const int64_t* rows, int64_t cols, const float* x,
+                        int M, float* const* y, void* stream) {
+    clear_error();
+    const char* fn = "muser_qmatvec_group";
+    MUSER_TRY(check_group(fn, qtype, n, W, rows, cols, x, M, y));
+    return group_launch(qtype, n, W, rows, cols, x, M, y, nullptr, nullptr, nullptr, nullptr, 0.f, 0.f, nullptr,
+                        as_stream(stream));
+}
+
+int muser_qmatvec_group_tail(int qtype, int n, const void* const* W, const int64_t* rows, int64_t cols,
+                             const float* projected, float* residual, const float* w1, const float* w2, float eps1,
+                             float eps2, float* x_out, int M, float* const* y, void* stream) {
+    clear_error();
+    const char* fn = "muser_qmatvec_group_tail";
+    MUSER_TRY(check_group(fn, qtype, n, W, rows, cols, x_out, M, y));
+    MUSER_TRY(check_f32(fn, "projected", projected));
+    MUSER_TRY(check_f32(fn, "residual", residual));
+    MUSER_TRY(check_f32(fn, "w1", w1));
+    MUSER_TRY(check_f32(fn, "w2", w2));
+    if (cols % 4) return set_error(MUSER_ERR_INVALID_ARG, "%s: cols must be a multiple of 4", fn);
+    if (!(eps1 > 0.0f) || !(eps2 > 0.0f)) return set_error(MUSER_ERR_INVALID_ARG, "%s: eps must be > 0", fn);
+    if (x_out == residual || x_out == projected || projected == residual)
+        return set_error(MUSER_ERR_INVALID_ARG, "%s: projected, residual and x_out must be distinct", fn);
+    return group_launch(qtype, n, W, rows, cols, nullptr, M, y, projected, residual, w1, w2, eps1, eps2, x_out,
+                        as_stream(stream));
 }
 
 int muser_fused_residual_dual_rmsnorm(float* residual, const float* src, float* out,

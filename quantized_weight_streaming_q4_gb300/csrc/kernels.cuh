@@ -11,6 +11,7 @@ enum EpiKind { kEpiStore = 0, kEpiSiluMul = 1, kEpiTail = 2 };
 enum XSource { kXMemory = 0, kXTail = 1 };
 
 // One-token matvec (mv1.cu).  W[0..NMAT-1] share rows x (nsb*256) and x.
+constexpr int kMv1MaxSeg = 4;
 struct Mv1Args {
     const uint8_t* W[2];
     int64_t rows;
@@ -26,6 +27,13 @@ struct Mv1Args {
     float eps1, eps2;
     unsigned* ticket;
     float* tail_part;  // per-block sums of projected^2 (kMv1TailParts floats), or null
+    // Row segments (Q4_K, one matrix, store epilogue; Q4_K rows are whole 16-byte units):
+    // rows [seg0[s], seg0[s+1]) of the virtual matrix are rows of segW[s],
+    // and their results go to segY[s].  nseg == 0: W[0] and y0 as usual.
+    int nseg;
+    const uint8_t* segW[kMv1MaxSeg];
+    int64_t seg0[kMv1MaxSeg + 1];
+    float* segY[kMv1MaxSeg];
     // geometry, filled by the launcher
     int G, RS, ns, nconsumer_warps;
     int TG;  // consumer threads per row group

@@ -559,6 +559,20 @@ __global__ void __launch_bounds__(512, 1) mv1_kernel(const Mv1Args p) {
         auto issue = [&](int k, int buf) {
             const int64_t lr0 = static_cast<int64_t>(k) * RS;
             const int64_t lr1 = min(static_cast<int64_t>(nloc), lr0 + RS);
+            if (QT == MUSER_Q4_K && NMAT == 1 && EPI == kEpiStore && p.nseg > 0) {
+                // Rows of several matrices (rows are whole 16-byte units): one
+                // copy per segment the stage touches, back to back in the buffer.
+                const int64_t v0 = r0 + lr0, v1 = r0 + lr1;
+                uint8_t* dst = stage_base + static_cast<size_t>(buf) * NMAT * stage_bytes;
+                mbar_arrive_expect_tx(&full[buf], static_cast<uint32_t>((v1 - v0) * rowbytes));
+                for (int sg = 0; sg < p.nseg; ++sg) {
+                    const int64_t a0 = max(v0, p.seg0[sg]), a1 = min(v1, p.seg0[sg + 1]);
+                    if (a1 > a0)
+                        tma_load_1d_hint(dst + (a0 - v0) * rowbytes, p.segW[sg] + (a0 - p.seg0[sg]) * rowbytes,
+                                         static_cast<uint32_t>((a1 - a0) * rowbytes), &full[buf], wpol);
+                }
+                return;
+            }
             uint32_t total = 0;
             uint32_t sizes[NMAT];
             const uint8_t* srcs[NMAT];
@@ -674,6 +688,10 @@ __global__ void __launch_bounds__(512, 1) mv1_kernel(const Mv1Args p) {
                     const int64_t row = r0 + lr0 + rs;
                     if constexpr (EPI == kEpiSiluMul) {
                         p.y0[row] = silu_mul_f(acc, other);
+                    } else if (QT == MUSER_Q4_K && NMAT == 1 && EPI == kEpiStore && p.nseg > 0) {
+                        int sg = 0;
+                        while (sg + 1 < p.nseg && row >= p.seg0[sg + 1]) ++sg;
+                        p.segY[sg][row - p.seg0[sg]] = acc;
                     } else {
                         p.y0[row] = acc;
                         if constexpr (NMAT == 2) p.y1[row] = other;
@@ -1038,6 +1056,12 @@ static int launch_mv1_t(Mv1Args a, cudaStream_t stream) {
     a.HP = geo.HP;
     a.G = geo.G;
     a.nconsumer_warps = geo.ncw;
+    if (a.nseg > 0) {
+        if (QT != MUSER_Q4_K || NMAT != 1 || EPI != kEpiStore || a.nseg > kMv1MaxSeg || a.seg0[0] != 0 ||
+            a.seg0[a.nseg] != a.rows)
+            return set_error(MUSER_ERR_UNSUPPORTED, "mv1: row segments need one 16-byte-row matrix, store epilogue");
+        a.W[0] = a.W[1] = a.segW[0];
+    }
     if (XS == kXTail && !(nbc * 16 <= 4 * 32 * geo.ncw))
         return set_error(MUSER_ERR_UNSUPPORTED, "mv1: %d inputs exceed the fused tail's registers", nbc * 64);
     const int threads = (a.nconsumer_warps + 3) * 32;
@@ -1095,6 +1119,8 @@ int launch_mv1(int qtype, int nmat, int epi, const Mv1Args& a, cudaStream_t s, i
     if (xs == kXTail) {
         if (qtype == MUSER_Q4_K && nmat == 2 && epi == kEpiSiluMul)
             return launch_mv1_t<MUSER_Q4_K, 2, kEpiSiluMul, kXTail>(a, s);
+        if (qtype == MUSER_Q4_K && nmat == 1 && epi == kEpiStore)
+            return launch_mv1_t<MUSER_Q4_K, 1, kEpiStore, kXTail>(a, s);
         if (qtype == MUSER_Q6_K && nmat == 2 && epi == kEpiSiluMul)
             return launch_mv1_t<MUSER_Q6_K, 2, kEpiSiluMul, kXTail>(a, s);
     } else if (qtype == MUSER_Q4_K) {

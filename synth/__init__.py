@@ -37,6 +37,9 @@ QK = 256  # weights per super-block
 # tensor ids inside one layer's stream family
 T_GATE, T_UP, T_DOWN = 0, 1, 2
 T_X, T_RESID, T_W_IN, T_W1, T_W2, T_A, T_B, T_K, T_V = 10, 11, 12, 13, 14, 15, 16, 17, 18
+# attention side of a layer: Q, K, V, gate and output projections, the
+# attention output fed to o_proj, and the post-attention norm weight
+T_WQ, T_WK, T_WV, T_WAG, T_WO, T_ATTN, T_W_POST_ATTN = 20, 21, 22, 23, 24, 25, 26
 
 
 def _bitgen(seed, workload: int, layer: int, tensor: int) -> np.random.PCG64:
@@ -141,6 +144,8 @@ WORKLOADS = {
     2: "q6k_down_6656x19968_tail",
     3: "ffn_block_m1",
     4: "ffn_stack52_m16",
+    5: "kv_ring_rows",
+    6: "attn_projections_m1_m16",
 }
 
 
@@ -170,6 +175,30 @@ def ffn_layer(layer: int, hidden=HIDDEN, ffn=FFN, *, seed=0, workload=3, down_qt
     Wd = qmatrix(down_qtype, hidden, ffn, seed=seed, workload=workload, layer=layer, tensor=T_DOWN)
     w1 = norm_weight(hidden, seed=seed, workload=workload, layer=layer, tensor=T_W1)
     return dict(Wg=Wg, Wu=Wu, Wd=Wd, w1=w1)
+
+
+# The attention-side projections of the Muser book's model (Ch 10 Figure 10.1
+# boxes 4 and 9): Q and gate [6656 -> 4096], K and V [6656 -> 256], o_proj
+# [4096 -> 6656].
+Q_DIM = 4096
+KV_DIM = 256
+ATTN_WORKLOAD = 6
+
+
+def attn_layer(layer: int, hidden=HIDDEN, *, seed=0, workload=ATTN_WORKLOAD):
+    """One layer's attention-side weights, all Q4_K with the Q4_K field recipe,
+    and its post-attention norm weight."""
+    kw = dict(seed=seed, workload=workload, layer=layer)
+    return dict(Wq=q4k_matrix(Q_DIM, hidden, tensor=T_WQ, **kw), Wk=q4k_matrix(KV_DIM, hidden, tensor=T_WK, **kw),
+                Wv=q4k_matrix(KV_DIM, hidden, tensor=T_WV, **kw), Wg=q4k_matrix(Q_DIM, hidden, tensor=T_WAG, **kw),
+                Wo=q4k_matrix(hidden, Q_DIM, tensor=T_WO, **kw),
+                w_post=norm_weight(hidden, tensor=T_W_POST_ATTN, **kw))
+
+
+def attn_output(M: int, layer: int = 0, *, seed=0, workload=ATTN_WORKLOAD):
+    """A stand-in for the gated attention output that o_proj reads: N(0,1)
+    f32 [M x 4096] (attention itself is outside this path)."""
+    return normal((M, Q_DIM), seed=seed, workload=workload, layer=layer, tensor=T_ATTN)
 
 
 def input_norm_weight(layer: int, hidden=HIDDEN, *, seed=0, workload=3):

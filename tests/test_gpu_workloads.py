@@ -10,7 +10,7 @@ import pytest
 
 import oracle
 import synth
-from tests.gpu_util import assert_close, dev, host, nan_like
+from tests.gpu_util import assert_close, check_canary, dev, host, nan_like
 
 pytestmark = pytest.mark.gpu
 
@@ -235,3 +235,68 @@ def test_workload4_52_layers_teacher_forced_and_end_to_end():
                 assert abs(g_rms - rms[row]) / rms[row] < CHAOTIC_RMS
     del keep
     torch.cuda.empty_cache()
+
+
+# ---------------------------------------------- attention-side projections
+@pytest.mark.parametrize("M", [1, 16])
+def test_attention_side_projections_and_first_tail(M):
+    """The rest of a layer's weight stream at the book's shapes (Ch 10 Figure
+    10.1 boxes 4, 9 and 10): Q, K, V and gate [6656 -> 4096/256/256/4096] on
+    the normed residual, then o_proj [4096 -> 6656] with the first dual-eps
+    tail (post-attention norm, then the FFN input norm).  Attention itself is
+    outside the path; o_proj reads a seeded stand-in for its output."""
+    A = synth.attn_layer(0, H)
+    r = synth.residual_rows(M, H, workload=synth.ATTN_WORKLOAD)
+    w_in = synth.input_norm_weight(0, H, workload=synth.ATTN_WORKLOAD)
+    w_ffn = synth.input_norm_weight(1, H, workload=synth.ATTN_WORKLOAD)
+    x = oracle.rms_norm(r, w_in, 1e-5)
+    xd = dev(x)
+    for name, rows in (("Wq", synth.Q_DIM), ("Wk", synth.KV_DIM), ("Wv", synth.KV_DIM), ("Wg", synth.Q_DIM)):
+        y = nan_like((M, rows), extra=16)
+        mu.muser_qmatvec("q4_k", dev(A[name]), rows, H, xd, M, y)
+        ref = oracle.qmatvec("q4_k", A[name], rows, H, x)
+        assert_close(host(y[:M * rows]).reshape(M, rows), ref, f"{name} M={M}", scaled=True)
+        check_canary(y, M * rows)
+    attn = synth.attn_output(M)
+    nscr = mu.muser_scratch_bytes(H, M)
+    scratch = torch.zeros(nscr // 4, dtype=torch.float32, device="cuda")
+    rd, proj, out = dev(r), nan_like((M, H)), nan_like((M, H))
+    mu.muser_qmatvec_residual_dual_rmsnorm("q4_k", dev(A["Wo"]), H, synth.Q_DIM, dev(attn), M, proj, rd, out,
+                                           dev(A["w_post"]), dev(w_ffn), 1e-8, 1e-5, scratch, nscr)
+    p_ref, r_ref, o_ref = oracle.down_tail("q4_k", A["Wo"], H, synth.Q_DIM, attn, r, A["w_post"], w_ffn)
+    assert_close(host(proj).reshape(M, H), p_ref, f"o_proj M={M}", scaled=True)
+    assert_close(host(rd), r_ref, f"post-attention residual M={M}")
+    assert_close(host(out).reshape(M, H), o_ref, f"FFN input M={M}")
+    assert not host(scratch).any()
+    assert mu.muser_device_status() == 0
+
+
+@pytest.mark.parametrize("M", [1, 3])
+@pytest.mark.parametrize("with_tail", [False, True])
+def test_attention_projection_group(M, with_tail):
+    """Q, K, V and gate as one group (one launch at M = 1), optionally after
+    the previous sub-block's tail: equal to the tail and four matvecs."""
+    A = synth.attn_layer(1, H)
+    names, rows = ("Wq", "Wk", "Wv", "Wg"), (synth.Q_DIM, synth.KV_DIM, synth.KV_DIM, synth.Q_DIM)
+    ys = [nan_like((M, n), extra=16) for n in rows]
+    if with_tail:
+        r = synth.residual_rows(M, H, workload=synth.ATTN_WORKLOAD)
+        p = synth.normal((M, H), seed=7, workload=synth.ATTN_WORKLOAD, tensor=synth.T_X) * np.float32(3e5)
+        w1 = synth.norm_weight(H, seed=7, workload=synth.ATTN_WORKLOAD, tensor=synth.T_W1)
+        w2 = synth.norm_weight(H, seed=7, workload=synth.ATTN_WORKLOAD, tensor=synth.T_W2)
+        rd, x_out = dev(r), nan_like((M, H), extra=16)
+        mu.muser_qmatvec_group_tail("q4_k", [dev(A[n]) for n in names], rows, H, dev(p), rd, dev(w1), dev(w2),
+                                    1e-8, 1e-5, x_out, M, ys)
+        r_ref, x = oracle.dual_tail(r, p, w1, w2, 1e-8, 1e-5)
+        assert_close(host(rd).reshape(M, H), r_ref, "tail residual")
+        assert_close(host(x_out[:M * H]).reshape(M, H), x, "tail x_out")
+        check_canary(x_out, M * H)
+    else:
+        x = oracle.rms_norm(synth.residual_rows(M, H, workload=synth.ATTN_WORKLOAD),
+                            synth.input_norm_weight(0, H, workload=synth.ATTN_WORKLOAD), 1e-5)
+        mu.muser_qmatvec_group("q4_k", [dev(A[n]) for n in names], rows, H, dev(x), M, ys)
+    for name, n, y in zip(names, rows, ys):
+        ref = oracle.qmatvec("q4_k", A[name], n, H, x)
+        assert_close(host(y[:M * n]).reshape(M, n), ref, f"{name} in the group M={M}", scaled=True)
+        check_canary(y, M * n)
+    assert mu.muser_device_status() == 0
