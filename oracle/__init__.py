@@ -78,6 +78,9 @@ def lib():
             L.orc_dual_tail.argtypes = [P, P, P, P, I64, I64, D, D, P, P]
             L.orc_silu.restype = D
             L.orc_silu.argtypes = [D]
+            L.orc_softcap.restype = D
+            L.orc_softcap.argtypes = [D, D, D]
+            L.orc_scale_softcap.argtypes = [P, I64, D, D, P]
             L.orc_silu_mul.argtypes = [P, P, I64, P]
             L.orc_gate_up_silu.argtypes = [I, P, P, I64, I64, P, I64, P]
             L.orc_ring_append.argtypes = [ctypes.POINTER(Ring), I64, ctypes.POINTER(I64)]
@@ -206,6 +209,29 @@ def dual_tail(resid: np.ndarray, src: np.ndarray, w1: np.ndarray, w2: np.ndarray
 
 
 # --------------------------------------------------------------------- SiLU
+# The LM head's logit scale and soft cap (Ch 10 Figure 10.1 box 15): x 0.196116
+# (1/sqrt(26)), then 20 * tanh(l / 20).
+LOGIT_SCALE = 0.196116
+SOFTCAP = 20.0
+
+
+def softcap(l: float, scale: float = LOGIT_SCALE, cap: float = SOFTCAP) -> float:
+    return lib().orc_softcap(float(l), float(scale), float(cap))
+
+
+def scale_softcap(logits: np.ndarray, scale: float = LOGIT_SCALE, cap: float = SOFTCAP) -> np.ndarray:
+    l = np.ascontiguousarray(logits, dtype=np.float32)
+    out = np.empty_like(l)
+    lib().orc_scale_softcap(_p(l), l.size, float(scale), float(cap), _p(out))
+    return out
+
+
+def lm_head(qtype, W: np.ndarray, vocab: int, hidden: int, x: np.ndarray, scale: float = LOGIT_SCALE,
+            cap: float = SOFTCAP) -> np.ndarray:
+    """Ch 10 Figure 10.1 boxes 14-15: binary32 logits W . x, then scale and cap."""
+    return scale_softcap(qmatvec(qtype, W, vocab, hidden, x), scale, cap)
+
+
 def silu(z: float) -> float:
     return lib().orc_silu(float(z))
 

@@ -294,6 +294,18 @@ void orc_silu_mul(const float* a, const float* b, int64_t n, float* out) {
     for (int64_t i = 0; i < n; ++i) out[i] = (float)(orc_silu((double)a[i]) * (double)b[i]);
 }
 
+/* ---------------------------------------------- LM head scale + soft cap */
+/* Ch 10 Figure 10.1 boxes 14 and 15: the LM head is a matvec of the final
+ * normed hidden row (its binary32 logits are written out), then
+ * muser_scale_softcap_inplace multiplies each logit by the logit scale and
+ * caps it as cap * tanh(l / cap).  Here the scaled and capped value is taken
+ * in fp64 from the binary32 logit and rounded once. */
+double orc_softcap(double l, double scale, double cap) { return cap * tanh(l * scale / cap); }
+
+void orc_scale_softcap(const float* logits, int64_t n, double scale, double cap, float* out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = (float)orc_softcap((double)logits[i], scale, cap);
+}
+
 /* FFN gate/up/SiLU (Ch 10 Figure 10.1 box 11): g = Wg.x and u = Wu.x are
  * binary32 activations (the book's default route writes both, then applies
  * SiLU in place), mid = silu(g) * u.  mid is [M][ffn]. */

@@ -247,3 +247,36 @@ def test_ffn_stack_rows_are_independent():
     rf, of = oracle.ffn_stack(r, w_in[0], layers, w_in[1:], hidden, ffn)
     rs, os_ = oracle.ffn_stack(r[2:3], w_in[0], layers, w_in[1:], hidden, ffn)
     assert np.array_equal(rf[2:3], rs) and np.array_equal(of[2:3], os_)
+
+
+# ------------------------------------------------- LM head scale + soft cap
+def test_softcap_constants_are_the_pages_values():
+    # Ch 10 Figure 10.1 box 15 prints "x 0.196116 (1/sqrt(26)), then 20 tanh(l/20)"
+    assert oracle.LOGIT_SCALE == 0.196116 and oracle.SOFTCAP == 20.0
+    assert abs(oracle.LOGIT_SCALE - 26 ** -0.5) < 5e-7
+
+
+def test_softcap_closed_forms():
+    s, c = oracle.LOGIT_SCALE, oracle.SOFTCAP
+    assert oracle.softcap(0.0) == 0.0
+    for l in (1e-3, 0.7, 13.0, 250.0, 4.0e3):
+        assert oracle.softcap(-l) == -oracle.softcap(l)                # odd
+        assert abs(oracle.softcap(l)) <= c and (l > 500 or abs(oracle.softcap(l)) < c)  # bounded by the cap
+        t = l * s / c                                                  # tanh through exp, another formula
+        assert abs(oracle.softcap(l) - c * np.expm1(2 * t) / (np.exp(2 * t) + 1)) <= 1e-12 * c
+    assert abs(oracle.softcap(1e-7) / 1e-7 - s) < 1e-9                # slope at 0 is the scale
+    assert oracle.softcap(1e5) == c and oracle.softcap(-1e5) == -c     # saturates at the cap
+    l = 37.25                                                          # inverse: atanh undoes it
+    assert abs(np.arctanh(oracle.softcap(l) / c) * c / s - l) < 1e-9
+
+
+def test_scale_softcap_rounds_once_and_lm_head_composes():
+    rng = np.random.default_rng(5)
+    logits = (rng.standard_normal(4099) * 60).astype(np.float32)
+    got = oracle.scale_softcap(logits)
+    ref = np.array([oracle.softcap(float(v)) for v in logits], np.float64).astype(np.float32)
+    assert np.array_equal(got, ref)
+    W = synth.q6k_matrix(300, 512, seed=3)
+    x = synth.normal((2, 512), seed=3)
+    assert np.array_equal(oracle.lm_head("q6_k", W, 300, 512, x),
+                          oracle.scale_softcap(oracle.qmatvec("q6_k", W, 300, 512, x)))
