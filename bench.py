@@ -9,6 +9,7 @@ layers' 13.44 GB of distinct weights (far larger than the 129 MB L2).
 `--workload stack52_m16` runs the same stack at M = 16 (speculative verify).
 `--workload attn52_m1` / `attn52_m16` run the attention side of the same
 layers (Q, K, V, gate projections; o_proj with the first dual-eps tail).
+`--workload lmhead_m1` runs the LM head (202,048 x 6,656 Q6_K, soft cap).
 
 Arms:
   --impl native     libmuser (CUDA, sm_103a) through its C ABI.
@@ -627,6 +628,105 @@ def run_attn(args, rank, world):
     }
 
 
+VOCAB = 202048
+LMHEAD_W = VOCAB * (H // 256) * 210  # Q6_K
+
+
+def run_lmhead(args, rank, world):
+    """The LM head of one decode token (Ch 10 Figure 10.1 boxes 14-15): the
+    202,048 x 6,656 Q6_K matvec of the final normed row with the logit scale
+    and soft cap as its epilogue (muser_lm_head), 1.09 GB per step."""
+    import torch
+    import quantized_weight_streaming_q4_gb300 as mu
+    import oracle
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(_env_int("LOCAL_RANK", 0))
+        dist.init_process_group("nccl")
+    mu.build()
+    L = mu.lib()
+    t0 = time.time()
+    W = torch.from_numpy(synth.q6k_matrix(VOCAB, H, seed=0, workload=7)).cuda()
+    gen_s = time.time() - t0
+    x = torch.from_numpy(synth.normal((1, H), seed=0, workload=7) * np.float32(0.02)).cuda()
+    logits = torch.empty(VOCAB, dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream()
+    sh = stream.cuda_stream
+    scale, cap = oracle.LOGIT_SCALE, oracle.SOFTCAP
+
+    def step():
+        r = L.muser_lm_head(14, W.data_ptr(), VOCAB, H, x.data_ptr(), 1, logits.data_ptr(), scale, cap, sh)
+        if r != 0:
+            raise RuntimeError(f"lm_head: {mu.muser_last_error()}")
+
+    def barrier():
+        torch.cuda.synchronize()
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    for _ in range(args.warmup):
+        step()
+    barrier()
+    uuid = None
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(torch.cuda.current_device()).uuid)
+    except Exception:
+        pass
+    clocks = ClockSampler(uuid)
+    clocks.start()
+    time.sleep(0.3)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    barrier()
+    for a, b in evs:
+        a.record(stream)
+        step()
+        b.record(stream)
+    barrier()
+    clock = clocks.stop()
+    ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    if dist is not None:
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    h_in = torch.from_numpy(x.cpu().numpy()).pin_memory()
+    h_out = torch.empty(VOCAB, dtype=torch.float32).pin_memory()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        x.copy_(h_in, non_blocking=True)
+        step()
+        h_out.copy_(logits, non_blocking=True)
+    e1.record(stream)
+    barrier()
+    e2e_ms = e0.elapsed_time(e1) / args.steps
+    assert np.isfinite(h_out.numpy()).all()
+    peak, peak_kind = read_peaks()
+    nbytes = LMHEAD_W + 4 * H + 4 * VOCAB
+    gbs = world * LMHEAD_W / (ms * 1e-3) / 1e9
+    achieved = nbytes / (ms * 1e-3) / 1e9
+    return {
+        "metric": METRIC, "value": round(gbs, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded Q6_K fields per the workload recipe)",
+        "config": {"workload": f"LM head: Q6_K {VOCAB}x{H} matvec with the logit scale and soft cap, M=1",
+                   "vocab": VOCAB, "hidden": H, "M": 1, "weight_bytes_per_step": LMHEAD_W,
+                   "l2": f"inputs larger than L2: {LMHEAD_W / 1e9:.2f} GB of weights per step vs 129 MB L2",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "tokens_per_s": round(world / (ms * 1e-3), 3),
+        "hbm_frac_of_" + peak_kind: round(gbs / world / peak, 4),
+        "roofline": {"bound": "hbm", "kernel": "muser_lm_head (mv1 Q6_K, soft-cap epilogue)",
+                     "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "traffic": None, "algorithmic_bytes_per_launch": nbytes, "mean_launch_us": round(ms * 1e3, 2)},
+        "e2e": {"value": round(world * LMHEAD_W / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+                "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": 4 * H, "d2h_bytes_per_step": 4 * VOCAB,
+                "api": "muser_lm_head with the hidden row in from pinned host memory and the logits out"},
+        "gpu_launches": args.steps, "clocks": clock, "device_status": mu.muser_device_status(),
+        "weights_generation_s": round(gen_s, 1),
+    }
+
+
 def run_reference(args, rank, world):
     if rank != 0:
         return None
@@ -664,7 +764,7 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
-    ap.add_argument("--workload", choices=["stack52_m1", "stack52_m16", "attn52_m1", "attn52_m16"],
+    ap.add_argument("--workload", choices=["stack52_m1", "stack52_m16", "attn52_m1", "attn52_m16", "lmhead_m1"],
                     default="stack52_m1")
     ap.add_argument("--layers", type=int, default=NL)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
@@ -678,6 +778,8 @@ def main():
         res = run_reference(args, rank, world)
     elif args.workload.startswith("attn"):
         res = run_attn(args, rank, world)
+    elif args.workload == "lmhead_m1":
+        res = run_lmhead(args, rank, world)
     else:
         res = run_native(args, rank, world)
     if rank == 0 and res is not None:

@@ -183,6 +183,26 @@ int muser_qmatvec_group_tail(int qtype, int n, const void* const* W, const int64
                              float eps1, float eps2, float* x_out, int M, float* const* y, void* stream);
 
 /*
+ * muser_scale_softcap -- logits[i] = cap * tanh(logits[i] * scale / cap), in
+ *   place (the book's muser_scale_softcap_inplace, Ch 10 Figure 10.1 box 15:
+ *   scale 0.196116 = 1/sqrt(26), cap 20).  logits: device f32 [n]; cap > 0
+ *   and finite; scale finite.
+ */
+int muser_scale_softcap(float* logits, int64_t n, float scale, float cap, void* stream);
+
+/*
+ * muser_lm_head -- the LM head (Ch 10 Figure 10.1 boxes 14 and 15): binary32
+ *   logits = W . x (the final normed hidden row), then the scale and soft cap
+ *   above.  W: device matrix [vocab x hidden] of `qtype` (the book's model:
+ *   202,048 x 6,656); x: device f32 [M*hidden]; logits: device f32
+ *   [M*vocab].  For one row of x the cap is the matvec kernel's epilogue;
+ *   otherwise the two run one after the other.  Fail-closed like
+ *   muser_qmatvec.
+ */
+int muser_lm_head(int qtype, const void* W, int64_t vocab, int64_t hidden, const float* x, int M,
+                  float* logits, float scale, float cap, void* stream);
+
+/*
  * muser_ffn_gate_up_silu_tail -- the boundary between two decode layers in
  *   one call: the previous layer's dual-eps tail (Ch 19 §19.4, as
  *   muser_fused_residual_dual_rmsnorm with src = projected, out = x_out),

@@ -20,7 +20,8 @@ __all__ = [
     "muser_version", "muser_last_error", "muser_block_bytes", "muser_matrix_bytes",
     "muser_dequantize", "muser_qmatvec", "muser_rms_norm", "muser_silu_mul",
     "muser_ffn_gate_up_silu", "muser_gate_up_scratch_bytes", "muser_ffn_gate_up_silu_scratch",
-    "muser_ffn_gate_up_silu_tail", "muser_qmatvec_group", "muser_qmatvec_group_tail",
+    "muser_ffn_gate_up_silu_tail", "muser_qmatvec_group", "muser_qmatvec_group_tail", "muser_scale_softcap",
+    "muser_lm_head",
     "muser_fused_residual_dual_rmsnorm", "muser_scratch_bytes",
     "muser_qmatvec_residual_dual_rmsnorm", "muser_qmatvec_residual_dual_rmsnorm_static",
     "MUSER_STATIC_SCRATCH_BYTES", "FfnLayer", "muser_ffn_workspace_bytes",
@@ -97,6 +98,8 @@ def lib():
             "muser_ffn_gate_up_silu_scratch": (I, [I, P, P, I64, I64, P, I, P, P, SZ, P]),
             "muser_ffn_gate_up_silu_tail": (I, [I, P, P, I64, I64, P, P, P, P, F, F, P, I, P, P]),
             "muser_qmatvec_group": (I, [I, I, P, P, I64, P, I, P, P]),
+            "muser_scale_softcap": (I, [P, I64, F, F, P]),
+            "muser_lm_head": (I, [I, P, I64, I64, P, I, P, F, F, P]),
             "muser_qmatvec_group_tail": (I, [I, I, P, P, I64, P, P, P, P, F, F, P, I, P, P]),
             "muser_fused_residual_dual_rmsnorm": (I, [P, P, P, P, P, I, I, F, F, P]),
             "muser_scratch_bytes": (SZ, [I64, I]),
@@ -211,6 +214,16 @@ def muser_ffn_gate_up_silu_tail(qtype, Wg, Wu, ffn: int, hidden: int, projected,
            lib().muser_ffn_gate_up_silu_tail(_qt(qtype), _ptr(Wg), _ptr(Wu), ffn, hidden, _ptr(projected),
                                              _ptr(residual), _ptr(w1), _ptr(w2), eps1, eps2, _ptr(x_out), M,
                                              _ptr(mid), _stream(stream)))
+
+
+def muser_scale_softcap(logits, n: int, scale: float, cap: float, stream=None) -> None:
+    _check("muser_scale_softcap", lib().muser_scale_softcap(_ptr(logits), n, scale, cap, _stream(stream)))
+
+
+def muser_lm_head(qtype, W, vocab: int, hidden: int, x, M: int, logits, scale: float, cap: float,
+                  stream=None) -> None:
+    _check("muser_lm_head", lib().muser_lm_head(_qt(qtype), _ptr(W), vocab, hidden, _ptr(x), M, _ptr(logits),
+                                                scale, cap, _stream(stream)))
 
 
 def _group_arrays(Ws, rows, ys):

@@ -6,6 +6,7 @@
 #include <algorithm>
 #include <cstdarg>
 #include <cstdio>
+#include <cmath>
 #include <mutex>
 
 #include "common.cuh"
@@ -542,6 +543,44 @@ int muser_qmatvec_group_tail(int qtype, int n, const void* const* W, const int64
         return set_error(MUSER_ERR_INVALID_ARG, "%s: projected, residual and x_out must be distinct", fn);
     return group_launch(qtype, n, W, rows, cols, nullptr, M, y, projected, residual, w1, w2, eps1, eps2, x_out,
                         as_stream(stream));
+}
+
+int muser_scale_softcap(float* logits, int64_t n, float scale, float cap, void* stream) {
+    clear_error();
+    const char* fn = "muser_scale_softcap";
+    MUSER_TRY(check_f32(fn, "logits", logits));
+    if (n < 0) return set_error(MUSER_ERR_INVALID_ARG, "%s: n must be >= 0", fn);
+    if (!(cap > 0.0f) || !std::isfinite(cap) || !std::isfinite(scale))
+        return set_error(MUSER_ERR_INVALID_ARG, "%s: cap must be > 0 and finite, scale finite", fn);
+    return launch_scale_softcap(logits, n, scale, cap, as_stream(stream));
+}
+
+int muser_lm_head(int qtype, const void* W, int64_t vocab, int64_t hidden, const float* x, int M, float* logits,
+                  float scale, float cap, void* stream) {
+    clear_error();
+    const char* fn = "muser_lm_head";
+    MUSER_TRY(check_matrix(fn, qtype, W, vocab, hidden));
+    MUSER_TRY(check_M(fn, M));
+    MUSER_TRY(check_f32(fn, "x", x));
+    MUSER_TRY(check_f32(fn, "logits", logits));
+    if (!(cap > 0.0f) || !std::isfinite(cap) || !std::isfinite(scale))
+        return set_error(MUSER_ERR_INVALID_ARG, "%s: cap must be > 0 and finite, scale finite", fn);
+    const cudaStream_t s = as_stream(stream);
+    if (M == 1 && mv1_supported(qtype, hidden)) {
+        // one row of x: the cap is the one-token kernel's epilogue
+        Mv1Args a{};
+        a.W[0] = static_cast<const uint8_t*>(W);
+        a.W[1] = a.W[0];
+        a.rows = vocab;
+        a.nsb = static_cast<int>(hidden / kQK);
+        a.x = x;
+        a.y0 = logits;
+        a.scale = scale;
+        a.cap = cap;
+        return launch_mv1(qtype, 1, kEpiSoftcap, a, s);
+    }
+    MUSER_TRY(muser_qmatvec(qtype, W, vocab, hidden, x, M, logits, stream));
+    return launch_scale_softcap(logits, vocab * M, scale, cap, s);
 }
 
 int muser_fused_residual_dual_rmsnorm(float* residual, const float* src, float* out,

@@ -357,6 +357,12 @@ __device__ __forceinline__ void block_dual_tail_row_parts(float* resid, const fl
     }
 }
 
+// The LM head's logit scale and soft cap in binary32 (Ch 10 Figure 10.1 box
+// 15): cap * tanh(l * scale / cap), with CUDA's tanhf.
+__device__ __forceinline__ float softcap_f(float l, float scale, float cap) {
+    return cap * tanhf((l * scale) / cap);
+}
+
 // SiLU(g) * u in binary32 (z/(1+exp(-z)) with CUDA's expf and IEEE division).
 __device__ __forceinline__ float silu_mul_f(float g, float u) {
     return (g / (1.0f + expf(-g))) * u;

@@ -5,7 +5,7 @@
 
 namespace muser {
 
-enum EpiKind { kEpiStore = 0, kEpiSiluMul = 1, kEpiTail = 2 };
+enum EpiKind { kEpiStore = 0, kEpiSiluMul = 1, kEpiTail = 2, kEpiSoftcap = 3 };
 // Where the one-token kernel's x comes from: memory, or the previous layer's
 // dual-eps tail computed in its prologue (x = p.x is then `projected`).
 enum XSource { kXMemory = 0, kXTail = 1 };
@@ -25,6 +25,7 @@ struct Mv1Args {
     const float* w1;
     const float* w2;
     float eps1, eps2;
+    float scale, cap;  // soft-cap epilogue: y = cap * tanh(y * scale / cap)
     unsigned* ticket;
     float* tail_part;  // per-block sums of projected^2 (kMv1TailParts floats), or null
     // Row segments (Q4_K, one matrix, store epilogue; Q4_K rows are whole 16-byte units):
@@ -99,6 +100,7 @@ int launch_dequantize(int qtype, const uint8_t* W, int64_t rows, int64_t cols, f
 int launch_rms_norm(const float* x, const float* w, float* out, int n, int M, float eps,
                     cudaStream_t s);
 int launch_silu_mul(const float* a, const float* b, float* out, int64_t n, cudaStream_t s);
+int launch_scale_softcap(float* logits, int64_t n, float scale, float cap, cudaStream_t s);
 int launch_dual_tail(float* resid, const float* src, float* out, const float* w1,
                      const float* w2, int n, int M, float eps1, float eps2, cudaStream_t s);
 int launch_kv_store(uint16_t* key, uint16_t* value, const float* k, const float* v,

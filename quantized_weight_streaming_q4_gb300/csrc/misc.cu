@@ -97,6 +97,12 @@ __global__ void rms_norm_kernel(const float* x, const float* __restrict__ w, flo
     }
 }
 
+__global__ void scale_softcap_kernel(float* l, int64_t n, float scale, float cap) {
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+        l[i] = softcap_f(l[i], scale, cap);
+}
+
 __global__ void silu_mul_kernel(const float* a, const float* b, float* out, int64_t n) {
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
          i += static_cast<int64_t>(gridDim.x) * blockDim.x)
@@ -161,6 +167,14 @@ int launch_rms_norm(const float* x, const float* w, float* out, int n, int M, fl
                     cudaStream_t s) {
     rms_norm_kernel<<<M, 1024, 0, s>>>(x, w, out, n, eps);
     return check_launch("rms_norm");
+}
+
+int launch_scale_softcap(float* logits, int64_t n, float scale, float cap, cudaStream_t s) {
+    if (n == 0) return MUSER_OK;
+    const int bs = 256;
+    const int64_t grid = std::min<int64_t>((n + bs - 1) / bs, static_cast<int64_t>(sm_count()) * 16);
+    scale_softcap_kernel<<<static_cast<unsigned>(grid), bs, 0, s>>>(logits, n, scale, cap);
+    return check_launch("scale_softcap");
 }
 
 int launch_silu_mul(const float* a, const float* b, float* out, int64_t n, cudaStream_t s) {

@@ -15,7 +15,8 @@
 //    per-digit sub-block sums.  Scales are applied once per sub-block.
 //  * Per stage, the slice partials of every row land in shared memory and
 //    one warp per row adds them in a fixed order (deterministic results).
-//  * Epilogues: store y; SiLU-gate two matrices (gate/up, Ch 10 §10.3 (d));
+//  * Epilogues: store y; scale and soft-cap logits (the LM head, Ch 10
+//    Figure 10.1 box 15); SiLU-gate two matrices (gate/up, Ch 10 §10.3 (d));
 //    or write `projected` and let the last CTA to finish run the dual-eps
 //    tail of Ch 19 §19.4 (atomic ticket, no spinning).
 #include <algorithm>
@@ -688,6 +689,8 @@ __global__ void __launch_bounds__(512, 1) mv1_kernel(const Mv1Args p) {
                     const int64_t row = r0 + lr0 + rs;
                     if constexpr (EPI == kEpiSiluMul) {
                         p.y0[row] = silu_mul_f(acc, other);
+                    } else if constexpr (EPI == kEpiSoftcap) {
+                        p.y0[row] = softcap_f(acc, p.scale, p.cap);
                     } else if (QT == MUSER_Q4_K && NMAT == 1 && EPI == kEpiStore && p.nseg > 0) {
                         int sg = 0;
                         while (sg + 1 < p.nseg && row >= p.seg0[sg + 1]) ++sg;
@@ -1127,10 +1130,12 @@ int launch_mv1(int qtype, int nmat, int epi, const Mv1Args& a, cudaStream_t s, i
         if (nmat == 1 && epi == kEpiStore) return launch_mv1_t<MUSER_Q4_K, 1, kEpiStore, kXMemory>(a, s);
         if (nmat == 1 && epi == kEpiTail) return launch_mv1_t<MUSER_Q4_K, 1, kEpiTail, kXMemory>(a, s);
         if (nmat == 2 && epi == kEpiSiluMul) return launch_mv1_t<MUSER_Q4_K, 2, kEpiSiluMul, kXMemory>(a, s);
+        if (nmat == 1 && epi == kEpiSoftcap) return launch_mv1_t<MUSER_Q4_K, 1, kEpiSoftcap, kXMemory>(a, s);
     } else if (qtype == MUSER_Q6_K) {
         if (nmat == 1 && epi == kEpiStore) return launch_mv1_t<MUSER_Q6_K, 1, kEpiStore, kXMemory>(a, s);
         if (nmat == 1 && epi == kEpiTail) return launch_mv1_t<MUSER_Q6_K, 1, kEpiTail, kXMemory>(a, s);
         if (nmat == 2 && epi == kEpiSiluMul) return launch_mv1_t<MUSER_Q6_K, 2, kEpiSiluMul, kXMemory>(a, s);
+        if (nmat == 1 && epi == kEpiSoftcap) return launch_mv1_t<MUSER_Q6_K, 1, kEpiSoftcap, kXMemory>(a, s);
     }
     return set_error(MUSER_ERR_UNSUPPORTED, "mv1: no kernel for qtype %d nmat %d epilogue %d", qtype, nmat, epi);
 }

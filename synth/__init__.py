@@ -146,6 +146,7 @@ WORKLOADS = {
     4: "ffn_stack52_m16",
     5: "kv_ring_rows",
     6: "attn_projections_m1_m16",
+    7: "lm_head_202048x6656",
 }
 
 

@@ -307,3 +307,46 @@ def test_sync_bounded_wait_times_out_then_completes():
 def test_device_status_clean():
     torch.cuda.synchronize()
     assert mu.muser_device_status() == 0
+
+
+# ------------------------------------------------ LM head scale + soft cap
+def test_scale_softcap_in_place():
+    rng = np.random.default_rng(11)
+    logits = (rng.standard_normal(70001) * np.float32(80)).astype(np.float32)
+    logits[:4] = [0.0, -0.0, 3.0e4, -3.0e4]
+    d = dev(logits)
+    mu.muser_scale_softcap(d, logits.size, oracle.LOGIT_SCALE, oracle.SOFTCAP)
+    assert_close(host(d), oracle.scale_softcap(logits), "scale_softcap")
+
+
+@pytest.mark.parametrize("qtype", ["q6_k", "q4_k"])
+@pytest.mark.parametrize("M,xscale", [(1, 0.02), (1, 1.0), (3, 0.02)])
+def test_lm_head(qtype, M, xscale):
+    """Logits in the cap's curved range (x scaled down) and saturated; one
+    row of x runs the cap as the matvec's epilogue, three rows separately."""
+    vocab, hidden = 20011, 6656
+    W = synth.qmatrix(qtype, vocab, hidden, seed=61)
+    x = (oracle.rms_norm(synth.normal((M, hidden), seed=62), synth.norm_weight(hidden, seed=62), 1e-5)
+         * np.float32(xscale)).astype(np.float32)
+    logits = nan_like((M, vocab), extra=32)
+    mu.muser_lm_head(qtype, dev(W), vocab, hidden, dev(x), M, logits, oracle.LOGIT_SCALE, oracle.SOFTCAP)
+    ref = oracle.lm_head(qtype, W, vocab, hidden, x)
+    assert_close(host(logits[:M * vocab]).reshape(M, vocab), ref, f"lm_head {qtype} M={M} x*{xscale}")
+    check_canary(logits, M * vocab)
+    assert mu.muser_device_status() == 0
+
+
+def test_lm_head_full_vocabulary():
+    """The book's LM head shape, 202,048 x 6,656 (Q6_K, 1.09 GB), every logit."""
+    vocab, hidden = 202048, 6656
+    W = synth.q6k_matrix(vocab, hidden, seed=63)
+    x = (oracle.rms_norm(synth.normal((1, hidden), seed=64), synth.norm_weight(hidden, seed=64), 1e-5)
+         * np.float32(0.02)).astype(np.float32)
+    logits = nan_like((1, vocab), extra=32)
+    Wd = dev(W)
+    mu.muser_lm_head("q6_k", Wd, vocab, hidden, dev(x), 1, logits, oracle.LOGIT_SCALE, oracle.SOFTCAP)
+    ref = oracle.lm_head("q6_k", W, vocab, hidden, x)
+    assert_close(host(logits[:vocab]).reshape(1, vocab), ref, "lm_head 202048 x 6656")
+    check_canary(logits, vocab)
+    del Wd
+    torch.cuda.empty_cache()
