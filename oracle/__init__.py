@@ -86,6 +86,8 @@ def lib():
             L.orc_ring_append.argtypes = [ctypes.POINTER(Ring), I64, ctypes.POINTER(I64)]
             L.orc_kv_write.argtypes = [ctypes.POINTER(Ring), P, P, I64, I64, I, P, P, I64, I64,
                                        ctypes.POINTER(I64)]
+            L.orc_kv_snapshot.argtypes = [ctypes.POINTER(Ring), P, P, I64, I64, I, I64, I64, P, P]
+            L.orc_kv_restore.argtypes = [ctypes.POINTER(Ring), P, P, I64, I64, I, P, P, I64, I64]
             L.orc_num_threads.restype = I
             L.orc_set_num_threads.argtypes = [I]
             _lib = L
@@ -332,3 +334,26 @@ def kv_write(ring: Ring, key: np.ndarray, value: np.ndarray, kv_dim: int, head_d
                             int(bool(head_major)), _p(k), _p(v), position, k.shape[0],
                             ctypes.byref(first))
     return rc, first.value
+
+
+def kv_snapshot(ring: Ring, key: np.ndarray, value: np.ndarray, kv_dim: int, head_dim: int,
+                head_major: bool, first: int, count: int):
+    """Ch 15 §15.6: live logical rows first..first+count-1 as token-major binary16
+    rows; returns (status, k_rows, v_rows)."""
+    assert key.dtype == np.uint16 and value.dtype == np.uint16
+    kr = np.zeros((count, kv_dim), np.uint16)
+    vr = np.zeros((count, kv_dim), np.uint16)
+    rc = lib().orc_kv_snapshot(ctypes.byref(ring), _p(key), _p(value), kv_dim, head_dim,
+                               int(bool(head_major)), first, count, _p(kr), _p(vr))
+    return rc, kr, vr
+
+
+def kv_restore(ring: Ring, key: np.ndarray, value: np.ndarray, kv_dim: int, head_dim: int,
+               head_major: bool, k_rows: np.ndarray, v_rows: np.ndarray, origin: int) -> int:
+    """Ch 15 §15.6: installs len(k_rows) logical rows from `origin` at rotation
+    origin % capacity; updates `ring` on success.  Returns the status."""
+    kr = np.ascontiguousarray(k_rows, dtype=np.uint16).reshape(-1, kv_dim)
+    vr = np.ascontiguousarray(v_rows, dtype=np.uint16).reshape(-1, kv_dim)
+    assert kr.shape == vr.shape
+    return lib().orc_kv_restore(ctypes.byref(ring), _p(key), _p(value), kv_dim, head_dim,
+                                int(bool(head_major)), _p(kr), _p(vr), origin, kr.shape[0])

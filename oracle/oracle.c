@@ -373,3 +373,59 @@ int orc_kv_write(orc_ring* r, uint16_t* key, uint16_t* value, int64_t kv_dim, in
     }
     return ORC_OK;
 }
+
+/* Element e of the token row held in physical slot p, in either layout
+ * (Ch 15 §15.3, Figure 15.1). */
+static int64_t orc_kv_index(int64_t p, int64_t e, int64_t kv_dim, int64_t head_dim, int head_major,
+                            int64_t capacity) {
+    return head_major ? ((e / head_dim) * capacity + p) * head_dim + e % head_dim : p * kv_dim + e;
+}
+
+/* Detached copy of live rows (Ch 15 §15.6): logical rows first..first+count-1,
+ * which must lie inside the live window [origin_logical, origin_logical+len),
+ * are written in logical order as token-major binary16 rows [count][kv_dim].
+ * The row of logical position q sits in slot
+ * (origin_physical + q - origin_logical) % capacity. */
+int orc_kv_snapshot(const orc_ring* r, const uint16_t* key, const uint16_t* value, int64_t kv_dim,
+                    int64_t head_dim, int head_major, int64_t first, int64_t count, uint16_t* k_rows,
+                    uint16_t* v_rows) {
+    if (count < 0 || kv_dim <= 0 || (head_major && (head_dim <= 0 || kv_dim % head_dim)))
+        return ORC_ERR_ARG;
+    if (first < r->origin_logical || first + count > r->origin_logical + r->len) return ORC_ERR_ARG;
+    for (int64_t j = 0; j < count; ++j) {
+        const int64_t p = (r->origin_physical + (first + j - r->origin_logical)) % r->capacity;
+        for (int64_t e = 0; e < kv_dim; ++e) {
+            const int64_t src = orc_kv_index(p, e, kv_dim, head_dim, head_major, r->capacity);
+            k_rows[j * kv_dim + e] = key[src];
+            v_rows[j * kv_dim + e] = value[src];
+        }
+    }
+    return ORC_OK;
+}
+
+/* Rotation-preserving restore (Ch 15 §15.6; Ch 10 §10.7): a detached window of
+ * `len` logical rows starting at logical position `origin` is installed at the
+ * rotation a ring built by sequential appends from position 0 holds there,
+ * origin % capacity.  Logical row j goes to slot (origin % capacity + j) %
+ * capacity, and the metadata becomes (len, origin, origin % capacity).  Slots
+ * outside the window are not written.  A NoPE plane (origin 0) reduces to the
+ * plain layout. */
+int orc_kv_restore(orc_ring* r, uint16_t* key, uint16_t* value, int64_t kv_dim, int64_t head_dim,
+                   int head_major, const uint16_t* k_rows, const uint16_t* v_rows, int64_t origin,
+                   int64_t len) {
+    if (kv_dim <= 0 || (head_major && (head_dim <= 0 || kv_dim % head_dim))) return ORC_ERR_ARG;
+    if (origin < 0 || len < 0 || len > r->capacity) return ORC_ERR_ARG;
+    const int64_t rotation = origin % r->capacity;
+    for (int64_t j = 0; j < len; ++j) {
+        const int64_t p = (rotation + j) % r->capacity;
+        for (int64_t e = 0; e < kv_dim; ++e) {
+            const int64_t dst = orc_kv_index(p, e, kv_dim, head_dim, head_major, r->capacity);
+            key[dst] = k_rows[j * kv_dim + e];
+            value[dst] = v_rows[j * kv_dim + e];
+        }
+    }
+    r->len = len;
+    r->origin_logical = origin;
+    r->origin_physical = rotation;
+    return ORC_OK;
+}

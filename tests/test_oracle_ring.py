@@ -4,6 +4,12 @@ Pinned against: the ring-wrap walk printed in the Muser book (Ch 15 §15.5,
 Figure 15.2), the boundary positions it names (§15.9), the fail-closed
 continuity rule, brute-force enumeration of the two index formulas (§15.3), and
 numpy's binary16 conversion.
+
+The snapshot and the rotation-preserving restore (§15.6; Ch 10 §10.7) are
+pinned by brute force on the rows they must hold, and by the book's own
+criterion: a window restored at origin o and then appended to holds exactly
+what a ring built by sequential appends holds (same metadata, same bytes in
+every live slot), while the slots outside the window stay untouched.
 """
 import json
 import os
@@ -106,3 +112,155 @@ def test_kv_write_discontinuity_leaves_planes_untouched():
     rc, _ = oracle.kv_write(ring, key, val, 2, 2, False, np.ones((1, 2), np.float32),
                             np.ones((1, 2), np.float32), 7)
     assert rc == -4 and np.all(key == 0xDEAD) and (ring.len, ring.origin_logical) == (1, 5)
+
+
+# ------------------------------------------------ snapshot and restore (§15.6)
+CASES = [(8, 6, 3, False), (8, 6, 3, True), (5, 4, 2, True), (16, 8, 8, False)]
+
+
+def _f16(a):
+    return np.asarray(a, np.float32).astype(np.float16).view(np.uint16)
+
+
+def _append_chunks(ring, key, val, kv_dim, head_dim, head_major, k, v, pos0, chunks):
+    t = 0
+    for c in chunks:
+        rc, _ = oracle.kv_write(ring, key, val, kv_dim, head_dim, head_major, k[t:t + c], v[t:t + c],
+                                pos0 + t)
+        assert rc == 0
+        t += c
+    assert t == k.shape[0]
+
+
+def _sequential_plane(cap, kv_dim, head_dim, head_major, ntok, seed=3, fill=0xDEAD):
+    key = np.full(cap * kv_dim, fill, np.uint16)
+    val = np.full(cap * kv_dim, fill, np.uint16)
+    ring = oracle.Ring(cap, 0, 0, 0)
+    k, v = synth.kv_rows(ntok, kv_dim, seed=seed)
+    chunks = [c for c in (1, 3, 2, 7, 1, 5, 11, 4) * 8]
+    out, t = [], 0
+    for c in chunks:
+        if t >= ntok:
+            break
+        out.append(min(c, ntok - t))
+        t += out[-1]
+    _append_chunks(ring, key, val, kv_dim, head_dim, head_major, k, v, 0, out)
+    return ring, key, val, k, v
+
+
+@pytest.mark.parametrize("cap,kv_dim,head_dim,head_major", CASES)
+@pytest.mark.parametrize("ntok", [0, 3, 8, 11, 29])
+def test_snapshot_rows_brute_force(cap, kv_dim, head_dim, head_major, ntok):
+    ntok = ntok * cap // 8
+    ring, key, val, k, v = _sequential_plane(cap, kv_dim, head_dim, head_major, ntok)
+    live0 = ring.origin_logical
+    assert live0 == max(0, ntok - cap) and ring.len == min(ntok, cap)
+    # every sub-range of the live window, logical position q holding token q
+    for first in range(live0, live0 + ring.len + 1):
+        for count in range(0, live0 + ring.len - first + 1):
+            rc, kr, vr = oracle.kv_snapshot(ring, key, val, kv_dim, head_dim, head_major, first, count)
+            assert rc == 0
+            assert np.array_equal(kr, _f16(k[first:first + count]))
+            assert np.array_equal(vr, _f16(v[first:first + count]))
+
+
+@pytest.mark.parametrize("head_major", [False, True])
+def test_snapshot_follows_origin_physical_not_position(head_major):
+    # a window whose physical origin is not its logical origin modulo capacity
+    cap, kv_dim, head_dim = 8, 4, 2
+    key = np.zeros(cap * kv_dim, np.uint16)
+    val = np.zeros(cap * kv_dim, np.uint16)
+    ring = oracle.Ring(cap, 0, 100, 5)
+    k, v = synth.kv_rows(6, kv_dim, seed=9)
+    _append_chunks(ring, key, val, kv_dim, head_dim, head_major, k, v, 100, [2, 4])
+    for j in range(6):
+        slot = (5 + j) % cap
+        for e in range(kv_dim):
+            dst = ((e // head_dim) * cap + slot) * head_dim + e % head_dim if head_major else slot * kv_dim + e
+            assert key[dst] == _f16(k[j, e])
+    rc, kr, vr = oracle.kv_snapshot(ring, key, val, kv_dim, head_dim, head_major, 100, 6)
+    assert rc == 0 and np.array_equal(kr, _f16(k)) and np.array_equal(vr, _f16(v))
+    rc, kr, _ = oracle.kv_snapshot(ring, key, val, kv_dim, head_dim, head_major, 102, 3)
+    assert rc == 0 and np.array_equal(kr, _f16(k[2:5]))
+
+
+@pytest.mark.parametrize("cap,kv_dim,head_dim,head_major", CASES)
+@pytest.mark.parametrize("ntok,more", [(0, 5), (3, 9), (8, 1), (11, 4), (29, 13), (64, 0)])
+def test_restore_then_append_equals_sequential_ring(cap, kv_dim, head_dim, head_major, ntok, more):
+    ntok = ntok * cap // 8
+    live, lkey, lval, k, v = _sequential_plane(cap, kv_dim, head_dim, head_major, ntok + more)
+    # the live ring as it stood after ntok tokens, and its detached window
+    a, akey, aval, _, _ = _sequential_plane(cap, kv_dim, head_dim, head_major, ntok)
+    rc, kr, vr = oracle.kv_snapshot(a, akey, aval, kv_dim, head_dim, head_major, a.origin_logical, a.len)
+    assert rc == 0
+    # restore into a fresh plane, then continue appending the same tokens
+    bkey = np.full(cap * kv_dim, 0xBEEF, np.uint16)
+    bval = np.full(cap * kv_dim, 0xBEEF, np.uint16)
+    b = oracle.Ring(cap, 0, 0, 0)
+    assert oracle.kv_restore(b, bkey, bval, kv_dim, head_dim, head_major, kr, vr, a.origin_logical) == 0
+    assert (b.len, b.origin_logical, b.origin_physical) == (a.len, a.origin_logical, a.origin_physical)
+    if more:
+        _append_chunks(b, bkey, bval, kv_dim, head_dim, head_major, k[ntok:], v[ntok:], ntok, [more])
+    assert (b.len, b.origin_logical, b.origin_physical) == (live.len, live.origin_logical,
+                                                             live.origin_physical)
+    written = np.zeros(cap, bool)
+    for j in range(live.len):
+        written[(live.origin_physical + j) % cap] = True
+    for slot in range(cap):
+        for e in range(kv_dim):
+            i = ((e // head_dim) * cap + slot) * head_dim + e % head_dim if head_major else slot * kv_dim + e
+            if written[slot]:
+                assert bkey[i] == lkey[i] and bval[i] == lval[i]
+            else:
+                assert bkey[i] == 0xBEEF and bval[i] == 0xBEEF
+
+
+@pytest.mark.parametrize("head_major", [False, True])
+def test_restore_rotation_is_origin_mod_capacity(head_major):
+    cap, kv_dim, head_dim = 8, 4, 2
+    rows = (np.arange(5 * kv_dim, dtype=np.uint16) + 1).reshape(5, kv_dim)
+    for origin, rot in [(0, 0), (3, 3), (8, 0), (100, 4), (101, 5)]:
+        key = np.zeros(cap * kv_dim, np.uint16)
+        val = np.zeros(cap * kv_dim, np.uint16)
+        ring = oracle.Ring(cap, 2, 7, 1)
+        assert oracle.kv_restore(ring, key, val, kv_dim, head_dim, head_major, rows, rows + 100, origin) == 0
+        assert (ring.len, ring.origin_logical, ring.origin_physical) == (5, origin, rot)
+        for j in range(5):
+            slot = (rot + j) % cap
+            for e in range(kv_dim):
+                i = ((e // head_dim) * cap + slot) * head_dim + e % head_dim if head_major else slot * kv_dim + e
+                assert key[i] == rows[j, e] and val[i] == rows[j, e] + 100
+        # a window packed at slot 0 is a different plane unless the rotation is 0
+        rc, kr, _ = oracle.kv_snapshot(ring, key, val, kv_dim, head_dim, head_major, origin, 5)
+        assert rc == 0 and np.array_equal(kr, rows)
+        packed = np.zeros_like(key)
+        for j in range(5):
+            for e in range(kv_dim):
+                i = ((e // head_dim) * cap + j) * head_dim + e % head_dim if head_major else j * kv_dim + e
+                packed[i] = rows[j, e]
+        assert np.array_equal(packed, key) == (rot == 0)
+
+
+def test_snapshot_and_restore_reject_bad_ranges_and_change_nothing():
+    cap, kv_dim, head_dim = 8, 4, 2
+    ring, key, val, _, _ = _sequential_plane(cap, kv_dim, head_dim, True, 11)
+    assert (ring.len, ring.origin_logical) == (8, 3)
+    for first, count in [(2, 1), (3, 9), (10, 2), (11, 1), (0, 0), (4, -1)]:
+        rc, kr, vr = oracle.kv_snapshot(ring, key, val, kv_dim, head_dim, True, first, max(count, 0))
+        if count < 0:
+            rc = oracle.lib().orc_kv_snapshot(oracle.ctypes.byref(ring), oracle._p(key), oracle._p(val),
+                                              kv_dim, head_dim, 1, first, count, oracle._p(kr),
+                                              oracle._p(vr))
+        assert rc == -1 and not kr.any() and not vr.any()
+    rc, _, _ = oracle.kv_snapshot(ring, key, val, kv_dim, 3, True, 3, 1)
+    assert rc == -1
+    before = (key.copy(), val.copy(), (ring.len, ring.origin_logical, ring.origin_physical))
+    rows = np.ones((9, kv_dim), np.uint16)
+    assert oracle.kv_restore(ring, key, val, kv_dim, head_dim, True, rows, rows, 0) == -1
+    assert oracle.kv_restore(ring, key, val, kv_dim, head_dim, True, rows[:2], rows[:2], -1) == -1
+    assert np.array_equal(key, before[0]) and np.array_equal(val, before[1])
+    assert (ring.len, ring.origin_logical, ring.origin_physical) == before[2]
+    # an empty window is a valid restore: it only resets the metadata
+    assert oracle.kv_restore(ring, key, val, kv_dim, head_dim, True, rows[:0], rows[:0], 20) == 0
+    assert (ring.len, ring.origin_logical, ring.origin_physical) == (0, 20, 4)
+    assert np.array_equal(key, before[0])
