@@ -24,9 +24,10 @@ import threading
 import numpy as np
 
 Q4_K = 12
+Q5_K = 13
 Q6_K = 14
-QTYPES = {"q4_k": Q4_K, "q6_k": Q6_K}
-BLOCK_BYTES = {Q4_K: 144, Q6_K: 210}
+QTYPES = {"q4_k": Q4_K, "q5_k": Q5_K, "q6_k": Q6_K}
+BLOCK_BYTES = {Q4_K: 144, Q5_K: 176, Q6_K: 210}
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "oracle.c")
@@ -70,6 +71,7 @@ def lib():
             L.orc_f32_to_f16_array.argtypes = [P, P, I64]
             L.orc_q4k_block.argtypes = [P, P]
             L.orc_q6k_block.argtypes = [P, P]
+            L.orc_q5k_block.argtypes = [P, P]
             L.orc_q4k_scale_min.argtypes = [P, I, P, P]
             L.orc_dequantize.argtypes = [I, P, I64, I64, P]
             L.orc_qmatvec.argtypes = [I, P, I64, I64, P, I64, P]
@@ -137,6 +139,14 @@ def q4k_block(blk: np.ndarray) -> np.ndarray:
     assert blk.size == 144
     out = np.empty(256, np.float32)
     lib().orc_q4k_block(_p(blk), _p(out))
+    return out
+
+
+def q5k_block(blk: np.ndarray) -> np.ndarray:
+    blk = np.ascontiguousarray(blk, dtype=np.uint8)
+    assert blk.size == 176
+    out = np.empty(256, np.float32)
+    lib().orc_q5k_block(_p(blk), _p(out))
     return out
 
 

@@ -15,7 +15,7 @@
  * is the same sequential fp64 loop whichever thread runs it.
  *
  * Readings of the pages (the pages are silent on these points; see DESIGN):
- *  - The Q4_K / Q6_K bit layouts are the ggml/GGUF super-block conventions that
+ *  - The Q4_K / Q5_K / Q6_K bit layouts are the ggml/GGUF super-block conventions that
  *    the book's "ggml-style" blocks name; the book gives only the block sizes
  *    (144 B and 210 B per 256 weights, Ch 19 §19.3) and field lists.
  *  - Q4_K value = d*scale*q - dmin*min (ggml form of the book's
@@ -32,6 +32,7 @@
 #endif
 
 #define ORC_Q4_K 12
+#define ORC_Q5_K 13
 #define ORC_Q6_K 14
 #define ORC_OK 0
 #define ORC_ERR_ARG -1
@@ -151,6 +152,37 @@ void orc_q4k_block(const uint8_t* blk, float* out) {
     }
 }
 
+/* ---------------------------------------------------------------- Q5_K block
+ * The third k-quant of the book's kernel registry (Ch 4 §4.4), which names the
+ * type but not its layout; the layout is the ggml/GGUF one.  256 weights in
+ * 176 bytes: f16 d, f16 dmin, the same 12 packed bytes of 6-bit scales and
+ * mins as Q4_K, 32 bytes of fifth code bits (qh), 128 bytes of 4-bit codes.
+ * Weight i = 64c + 32h + l (c = 0..3, h = 0/1, l = 0..31) belongs to sub-block
+ * 2c + h; its low four bits are the low (h = 0) or high (h = 1) nibble of code
+ * byte 32c + l, its fifth bit is bit 2c + h of qh[l], and its value is
+ * d*sc*q - dmin*min with q = 0..31. */
+void orc_q5k_block(const uint8_t* blk, float* out) {
+    const double d = orc_f16_to_f64(rd_u16(blk));
+    const double dmin = orc_f16_to_f64(rd_u16(blk + 2));
+    const uint8_t* s = blk + 4;
+    const uint8_t* qh = blk + 16;
+    const uint8_t* qs = blk + 48;
+    for (int i = 0; i < 256; ++i) {
+        const int c = i / 64;
+        const int h = (i % 64) >= 32;
+        const int l = i % 32;
+        const int byte = qs[32 * c + l];
+        const int low = h ? (byte >> 4) : (byte & 0x0f);
+        const int top = (qh[l] >> (2 * c + h)) & 1;
+        const int q = low | (top << 4);
+        int sc, mn;
+        orc_q4k_scale_min(s, i / 32, &sc, &mn);
+        /* as for Q4_K: both products are integer multiples of 2^-24 below
+         * 2^27, so the difference is exact in fp64 and the cast rounds once */
+        out[i] = (float)(d * sc * q - dmin * mn);
+    }
+}
+
 /* ---------------------------------------------------------------- Q6_K block
  * 256 weights in 210 bytes: 128 bytes of low 4-bit codes (ql), 64 bytes of
  * high 2-bit codes (qh), 16 int8 sub-block scales, f16 d.  Weight i: half
@@ -176,11 +208,12 @@ void orc_q6k_block(const uint8_t* blk, float* out) {
 }
 
 static int block_bytes(int qtype) {
-    return qtype == ORC_Q4_K ? 144 : (qtype == ORC_Q6_K ? 210 : 0);
+    return qtype == ORC_Q4_K ? 144 : (qtype == ORC_Q5_K ? 176 : (qtype == ORC_Q6_K ? 210 : 0));
 }
 
 static void decode_block(int qtype, const uint8_t* blk, float* out) {
     if (qtype == ORC_Q4_K) orc_q4k_block(blk, out);
+    else if (qtype == ORC_Q5_K) orc_q5k_block(blk, out);
     else orc_q6k_block(blk, out);
 }
 

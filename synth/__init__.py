@@ -32,6 +32,7 @@ import numpy as np
 
 Q4K_BLOCK_BYTES = 144
 Q6K_BLOCK_BYTES = 210
+Q5K_BLOCK_BYTES = 176
 QK = 256  # weights per super-block
 
 # tensor ids inside one layer's stream family
@@ -80,6 +81,24 @@ def q4k_matrix(rows: int, cols: int, *, seed=0, workload=0, layer=0, tensor=T_DO
     return blk.reshape(rows, (cols // QK) * Q4K_BLOCK_BYTES)
 
 
+def q5k_matrix(rows: int, cols: int, *, seed=0, workload=0, layer=0, tensor=T_DOWN,
+               d_range=(0.001, 0.01), dmin_range=(0.0, 0.005)) -> np.ndarray:
+    """A Q5_K matrix as uint8[rows, cols/256*176]: Q4_K's field distributions
+    (f16 d, dmin, uniform 6-bit scales and mins) with 5-bit codes uniform on
+    0..31 (uniform code and fifth-bit bytes)."""
+    if cols % QK:
+        raise ValueError("cols must be a multiple of 256")
+    nb = rows * (cols // QK)
+    bg = _bitgen(seed, workload, layer, tensor)
+    blk = _uniform_bytes(bg, nb * Q5K_BLOCK_BYTES).reshape(nb, Q5K_BLOCK_BYTES).copy()
+    g = np.random.Generator(bg)
+    d = _f16_bits(g.uniform(d_range[0], d_range[1], nb))
+    dmin = _f16_bits(g.uniform(dmin_range[0], dmin_range[1], nb))
+    blk[:, 0:2] = d.view(np.uint8).reshape(nb, 2)
+    blk[:, 2:4] = dmin.view(np.uint8).reshape(nb, 2)
+    return blk.reshape(rows, (cols // QK) * Q5K_BLOCK_BYTES)
+
+
 def q6k_matrix(rows: int, cols: int, *, seed=0, workload=0, layer=0, tensor=T_DOWN,
                d_range=(0.0005, 0.005), scale_range=(-32, 31)) -> np.ndarray:
     """A Q6_K matrix as uint8[rows, cols/256*210].
@@ -104,6 +123,8 @@ def q6k_matrix(rows: int, cols: int, *, seed=0, workload=0, layer=0, tensor=T_DO
 def qmatrix(qtype: str, rows: int, cols: int, **kw) -> np.ndarray:
     if qtype == "q4_k":
         return q4k_matrix(rows, cols, **kw)
+    if qtype == "q5_k":
+        return q5k_matrix(rows, cols, **kw)
     if qtype == "q6_k":
         return q6k_matrix(rows, cols, **kw)
     raise ValueError(qtype)

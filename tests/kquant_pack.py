@@ -1,6 +1,6 @@
 """Independent block ENCODERS used to pin the oracle's decoders.
 
-These pack field values (scales, mins, codes, d) into Q4_K / Q6_K super-block
+These pack field values (scales, mins, codes, d) into Q4_K / Q5_K / Q6_K super-block
 bytes.  They are the inverse map of the layout, written from its description
 (field lists in the Muser book Ch 19 §19.3; ggml/GGUF super-block conventions
 for the bit positions), so a decoder that reads a wrong bit, byte or nibble
@@ -55,6 +55,30 @@ def q4k_expected(d: float, dmin: float, sc, mn, q) -> np.ndarray:
         j = i // 32
         out[i] = d * sc[j] * q[i] - dmin * mn[j]
     return out.astype(np.float32)
+
+
+def pack_q5k(d: float, dmin: float, sc, mn, q) -> np.ndarray:
+    """Q5_K (ggml layout): sc, mn as for Q4_K; q: 256 ints in 0..31.  Bytes: d,
+    dmin, the Q4_K scale/min packing, 32 bytes of fifth bits, 128 code bytes."""
+    q = [int(v) for v in q]
+    assert len(q) == 256 and all(0 <= v < 32 for v in q)
+    # the header and scale packing are Q4_K's; the low four code bits too
+    q4 = pack_q4k(d, dmin, sc, mn, [v & 15 for v in q])
+    blk = np.zeros(176, np.uint8)
+    blk[0:16] = q4[0:16]
+    blk[48:176] = q4[16:144]
+    qh = [0] * 32
+    for i in range(256):
+        c, r = divmod(i, 64)
+        half, l = divmod(r, 32)
+        if q[i] >> 4:
+            qh[l] |= 1 << (2 * c + half)
+    blk[16:48] = np.array(qh, np.uint8)
+    return blk
+
+
+def q5k_expected(d: float, dmin: float, sc, mn, q) -> np.ndarray:
+    return q4k_expected(d, dmin, sc, mn, q)
 
 
 def pack_q6k(d: float, sc, q) -> np.ndarray:

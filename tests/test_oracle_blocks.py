@@ -1,4 +1,4 @@
-"""Pins for the oracle's binary16 conversions and Q4_K / Q6_K block decoders.
+"""Pins for the oracle's binary16 conversions and Q4_K / Q5_K / Q6_K block decoders.
 
 Pinned against: numpy's binary16 conversions (a library routine, exhaustive or
 dense samples), hand-worked single blocks, and round trips through the
@@ -8,7 +8,7 @@ import numpy as np
 import pytest
 
 import oracle
-from tests.kquant_pack import pack_q4k, pack_q6k, q4k_expected, q6k_expected
+from tests.kquant_pack import pack_q4k, pack_q5k, pack_q6k, q4k_expected, q5k_expected, q6k_expected
 
 
 def test_f16_decode_exhaustive_matches_numpy():
@@ -142,6 +142,91 @@ def test_q4k_zero_scales_give_zero():
     assert np.all(oracle.q4k_block(blk) == 0.0)
 
 
+# ------------------------------------------------------------------- Q5_K
+def test_q5k_hand_worked_block():
+    # d = 0.5, dmin = 0.25; sub-block 0: scale 3, min 1; sub-block 1: scale 2;
+    # sub-block 2: scale 1.
+    #   weight 0:  low nibble 5 of code byte 0, fifth bit (qh[0] bit 0) -> q 21:
+    #              0.5*3*21 - 0.25 = 31.25
+    #   weight 1:  fifth bit only (qh[1] bit 0) -> q 16: 24 - 0.25 = 23.75
+    #   weight 32: high nibble 7 of code byte 0, qh[0] bit 1 -> q 23: 0.5*2*23 = 23
+    #   weight 67: chunk 1, l = 3: qh[3] bit 2 -> q 16: 0.5*1*16 = 8
+    # the rest of sub-block 0 is -0.25, everything else 0.
+    blk = np.zeros(176, np.uint8)
+    blk[0:2] = [0x00, 0x38]      # d = 0.5
+    blk[2:4] = [0x00, 0x34]      # dmin = 0.25
+    blk[4 + 0] = 3
+    blk[4 + 1] = 2
+    blk[4 + 2] = 1
+    blk[4 + 4] = 1
+    blk[16 + 0] = 0b11
+    blk[16 + 1] = 0b01
+    blk[16 + 3] = 0b100
+    blk[48 + 0] = 0x75
+    w = oracle.q5k_block(blk)
+    ref = np.zeros(256, np.float32)
+    ref[0:32] = -0.25
+    ref[0], ref[1], ref[32], ref[67] = 31.25, 23.75, 23.0, 8.0
+    assert np.array_equal(w, ref)
+
+
+def test_q5k_without_fifth_bits_is_q4k():
+    # a Q5_K block whose qh is zero decodes as the Q4_K block with the same
+    # header and code bytes; with every fifth bit set each weight gains 16*d*sc
+    rng = np.random.default_rng(21)
+    for _ in range(50):
+        b4 = rng.integers(0, 256, 144).astype(np.uint8)
+        b4[0:2] = np.array([np.float16(rng.uniform(1e-3, 1.0))]).view(np.uint8)
+        b4[2:4] = np.array([np.float16(rng.uniform(0.0, 1.0))]).view(np.uint8)
+        b5 = np.concatenate([b4[:16], np.zeros(32, np.uint8), b4[16:]])
+        assert np.array_equal(oracle.q5k_block(b5), oracle.q4k_block(b4))
+        b5[16:48] = 0xFF
+        d = float(b4[0:2].view(np.float16)[0])
+        sc = [oracle.q4k_scale_min(b4[4:16], j)[0] for j in range(8)]
+        # d*sc*(q + 16) - dmin*m, exact in fp64 and rounded once
+        dmin = float(b4[2:4].view(np.float16)[0])
+        mn = [oracle.q4k_scale_min(b4[4:16], j)[1] for j in range(8)]
+        qs = b4[16:144]
+        low = [(int(qs[32 * (i // 64) + i % 32]) >> (4 * ((i % 64) >= 32))) & 15 for i in range(256)]
+        exact = np.array([d * sc[i // 32] * (low[i] + 16) - dmin * mn[i // 32] for i in range(256)])
+        assert np.array_equal(oracle.q5k_block(b5), exact.astype(np.float32))
+
+
+def test_q5k_one_hot_fifth_bit_positions():
+    for i in range(256):
+        q = [0] * 256
+        q[i] = 16
+        blk = pack_q5k(1.0, 0.0, [1] * 8, [0] * 8, q)
+        w = oracle.q5k_block(blk)
+        assert w[i] == 16.0 and np.count_nonzero(w) == 1, i
+
+
+@pytest.mark.parametrize("j", range(8))
+def test_q5k_one_hot_scale_selects_sub_block(j):
+    sc = [0] * 8
+    sc[j] = 1
+    blk = pack_q5k(1.0, 0.0, sc, [0] * 8, [31] * 256)
+    ref = np.zeros(256, np.float32)
+    ref[32 * j:32 * j + 32] = 31.0
+    assert np.array_equal(oracle.q5k_block(blk), ref)
+
+
+def test_q5k_encoder_round_trip_random_fields():
+    rng = np.random.default_rng(13)
+    for _ in range(300):
+        d = float(rng.uniform(1e-4, 2.0))
+        dmin = float(rng.uniform(0.0, 1.0))
+        sc = rng.integers(0, 64, 8)
+        mn = rng.integers(0, 64, 8)
+        q = rng.integers(0, 32, 256)
+        blk = pack_q5k(d, dmin, sc, mn, q)
+        assert np.array_equal(oracle.q5k_block(blk), q5k_expected(d, dmin, sc, mn, q))
+    for d, dmin in [(65504.0, 2.0 ** -24), (2.0 ** -24, 65504.0)]:
+        sc, mn, q = [63] * 8, [63] * 8, list(range(32)) * 8
+        blk = pack_q5k(d, dmin, sc, mn, q)
+        assert np.array_equal(oracle.q5k_block(blk), q5k_expected(d, dmin, sc, mn, q))
+
+
 # ------------------------------------------------------------------- Q6_K
 def test_q6k_hand_worked_block():
     # d = 1, scale[0] = 2, low nibble 1 and high bits 2 for weight 0 -> q = 33,
@@ -215,3 +300,9 @@ def test_dequantize_matrix_is_blockwise():
         for b in range(3):
             blk = W4[r, b * 144:(b + 1) * 144]
             assert np.array_equal(full4[r, b * 256:(b + 1) * 256], oracle.q4k_block(blk))
+    W5 = synth.q5k_matrix(2, 512, seed=7)
+    full5 = oracle.dequantize("q5_k", W5, 2, 512)
+    for r in range(2):
+        for b in range(2):
+            blk = W5[r, b * 176:(b + 1) * 176]
+            assert np.array_equal(full5[r, b * 256:(b + 1) * 256], oracle.q5k_block(blk))
