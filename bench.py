@@ -10,6 +10,11 @@ layers' 13.44 GB of distinct weights (far larger than the 129 MB L2).
 `--workload attn52_m1` / `attn52_m16` run the attention side of the same
 layers (Q, K, V, gate projections; o_proj with the first dual-eps tail).
 `--workload lmhead_m1` runs the LM head (202,048 x 6,656 Q6_K, soft cap).
+`--workload down_tail_q4k` / `down_tail_q6k` chain 52 instances of the
+standalone down projection + dual-eps tail (Q4_K or Q6_K W_down 6656x19968);
+`matvec_q5k` chains 52 plain Q5_K matvecs of the same shape.
+`--workload kv_restore` restores one session's K/V planes at 130,815 tokens
+(13 head-major NoPE planes, 39 wrapped 2,048-row SWA rings) from detached rows.
 
 Arms:
   --impl native     libmuser (CUDA, sm_103a) through its C ABI.
@@ -727,6 +732,305 @@ def run_lmhead(args, rank, world):
     }
 
 
+def run_down_tail(args, rank, world):
+    """The stand-alone down projection with the fused dual-eps tail at M = 1
+    (muser_qmatvec_residual_dual_rmsnorm; Ch 19 §19.4, §19.6), Q4_K or Q6_K
+    W_down 6656 x 19968: a chain of `--layers` calls on distinct seeded
+    weights, each one updating the residual in place, so a step streams more
+    than L2 holds.  `matvec_q5k`: the same chain of plain Q5_K matvecs
+    (muser_qmatvec), the k-quant the book's registry names beside Q4_K and
+    Q6_K (Ch 4 §4.4)."""
+    import torch
+    import quantized_weight_streaming_q4_gb300 as mu
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(_env_int("LOCAL_RANK", 0))
+        dist.init_process_group("nccl")
+    mu.build()
+    L = mu.lib()
+    q5 = args.workload == "matvec_q5k"
+    q4 = args.workload == "down_tail_q4k"
+    qname = "Q5_K" if q5 else ("Q4_K" if q4 else "Q6_K")
+    qt = {"Q4_K": 12, "Q5_K": 13, "Q6_K": 14}[qname]
+    wbytes = H * (F // 256) * {"Q4_K": 144, "Q5_K": 176, "Q6_K": 210}[qname]
+    nl = args.layers
+    t0 = time.time()
+    layers = []
+    for l in range(nl):
+        c = synth.down_tail_case(qname.lower(), H, F, 1, seed=0, workload=1 if q4 else 2, layer=l)
+        a, b = c["a"].astype(np.float32), c["b"].astype(np.float32)
+        mid = (a / (np.float32(1) + np.exp(-a)) * b).astype(np.float32)   # the FFN intermediate input
+        layers.append({k: torch.from_numpy(np.ascontiguousarray(v)).cuda()
+                       for k, v in (("W", c["W"]), ("mid", mid), ("w1", c["w1"]), ("w2", c["w2"]))})
+        if l == 0:
+            r0 = c["resid"].astype(np.float32)
+    gen_s = time.time() - t0
+    resid = torch.from_numpy(r0.copy()).cuda()
+    out = torch.empty(H, dtype=torch.float32, device="cuda")
+    proj = torch.empty(H, dtype=torch.float32, device="cuda")
+    nscr = mu.muser_scratch_bytes(H, 1)
+    scratch = torch.zeros(nscr // 4 + 64, dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream()
+    sh = stream.cuda_stream
+
+    def call(d):
+        if q5:
+            return L.muser_qmatvec(qt, d["W"].data_ptr(), H, F, d["mid"].data_ptr(), 1, out.data_ptr(), sh)
+        return L.muser_qmatvec_residual_dual_rmsnorm(
+            qt, d["W"].data_ptr(), H, F, d["mid"].data_ptr(), 1, proj.data_ptr(), resid.data_ptr(),
+            out.data_ptr(), d["w1"].data_ptr(), d["w2"].data_ptr(), 1e-8, 1e-5, scratch.data_ptr(), nscr, sh)
+
+    def step():
+        for d in layers:
+            r = call(d)
+            if r != 0:
+                raise RuntimeError(f"{args.workload}: {mu.muser_last_error()}")
+
+    def barrier():
+        torch.cuda.synchronize()
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    for _ in range(args.warmup):
+        resid.copy_(torch.from_numpy(r0))
+        step()
+    barrier()
+    uuid = None
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(torch.cuda.current_device()).uuid)
+    except Exception:
+        pass
+    clocks = ClockSampler(uuid)
+    clocks.start()
+    time.sleep(0.3)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    barrier()
+    clock = clocks.stop()
+    ms = e0.elapsed_time(e1) / args.steps
+    if dist is not None:
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    assert torch.isfinite(out).all() and torch.isfinite(resid).all()
+    # end to end: the residual row in from pinned host memory, the normed row out, every call
+    h_in = torch.from_numpy(r0.copy()).pin_memory()
+    h_x = [d["mid"].cpu().pin_memory() for d in layers] if q5 else None
+    h_out = torch.empty(H, dtype=torch.float32).pin_memory()
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    f0.record(stream)
+    for _ in range(args.steps):
+        for li, d in enumerate(layers):
+            if q5:
+                d["mid"].copy_(h_x[li], non_blocking=True)
+            else:
+                resid.copy_(h_in, non_blocking=True)
+            r = call(d)
+            if r != 0:
+                raise RuntimeError(f"{args.workload}: {mu.muser_last_error()}")
+            h_out.copy_(out, non_blocking=True)
+    f1.record(stream)
+    barrier()
+    e2e_ms = f0.elapsed_time(f1) / args.steps
+    peak, peak_kind = read_peaks()
+    # W, mid; p, r in/out, out; w1, w2 (a plain matvec: W, x, y)
+    per_launch = wbytes + 4 * F + (4 * H if q5 else 5 * 4 * H + 2 * 4 * H)
+    launch_ms = ms / nl
+    gbs = world * nl * wbytes / (ms * 1e-3) / 1e9
+    achieved = per_launch / (launch_ms * 1e-3) / 1e9
+    return {
+        "metric": METRIC, "value": round(gbs, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded; fields drawn per the workload recipe)",
+        "config": {"workload": (f"{nl} x [{qname} {H}x{F} matvec], M=1, distinct weights per call" if q5 else
+                                f"{nl} x [{qname} W_down {H}x{F} matvec + dual-eps fused tail], M=1, "
+                                "distinct weights per call"),
+                   "hidden": H, "ffn": F, "M": 1, "calls_per_step": nl, "weight_bytes_per_step": nl * wbytes,
+                   "l2": f"inputs larger than L2: {nl * wbytes / 1e9:.2f} GB of distinct weights per step "
+                         "vs 129 MB L2",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "matvec_tail_per_s": round(world * nl / (ms * 1e-3), 1),
+        "hbm_frac_of_" + peak_kind: round(gbs / world / peak, 4),
+        "roofline": {"bound": "hbm", "kernel": (f"muser_qmatvec (mv1 {qname}, store)" if q5 else
+                                                f"muser_qmatvec_residual_dual_rmsnorm (mv1 {qname}, one-pass "
+                                                "last-CTA tail)"),
+                     "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "traffic": None, "algorithmic_bytes_per_launch": per_launch,
+                     "mean_launch_us": round(launch_ms * 1e3, 2),
+                     "timing": "step time / calls per step (back-to-back launches)"},
+        "e2e": {"value": round(world * nl * wbytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+                "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": 4 * (F if q5 else H) * nl,
+                "d2h_bytes_per_step": 4 * H * nl,
+                "api": ("muser_qmatvec, the input row in and the output row out per call" if q5 else
+                        "muser_qmatvec_residual_dual_rmsnorm, residual in and normed row out per call")},
+        "gpu_launches": args.steps * nl, "clocks": clock, "device_status": mu.muser_device_status(),
+        "weights_generation_s": round(gen_s, 1),
+    }
+
+
+# One session slot's K/V planes (Ch 15 §15.7): 13 NoPE layers with head-major
+# planes of max_context rows, 39 sliding layers with 2,048-row token-major rings;
+# kv_dim 256 halves (2 KV heads x 128), K and V.
+KV_TOKENS = 130815          # the deep handoff's context depth (Ch 15 §15.7)
+KV_MAX_CONTEXT = 131072
+KV_SWA_CAP = 2048
+KV_DIM, KV_HEAD_DIM = 256, 128
+KV_NOPE, KV_SWA = 13, 39
+
+
+def run_kv_restore(args, rank, world):
+    """Rotation-preserving restore of one session slot (Ch 15 §15.6): every
+    layer's detached logical rows installed into its plane pair, the sliding
+    rings at rotation origin % 2,048.  The value counts the bytes each restore
+    reads and writes, 2 x 1.82 GB per step, against the measured copy
+    bandwidth (also read + write bytes)."""
+    import torch
+    import quantized_weight_streaming_q4_gb300 as mu
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(_env_int("LOCAL_RANK", 0))
+        dist.init_process_group("nccl")
+    mu.build()
+    L = mu.lib()
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(1234 + rank)
+    swa_len = min(KV_TOKENS, KV_SWA_CAP)
+    swa_origin = KV_TOKENS - swa_len
+    layers = []  # (plane, k_rows, v_rows, origin, len)
+    for layer in range(KV_NOPE + KV_SWA):
+        nope = layer < KV_NOPE
+        cap, n, origin = (KV_MAX_CONTEXT, KV_TOKENS, 0) if nope else (KV_SWA_CAP, swa_len, swa_origin)
+        key = torch.zeros(cap * KV_DIM, dtype=torch.int16, device="cuda")
+        val = torch.zeros_like(key)
+        kr = torch.randint(-32768, 32767, (n * KV_DIM,), dtype=torch.int16, device="cuda", generator=gen)
+        vr = torch.randint(-32768, 32767, (n * KV_DIM,), dtype=torch.int16, device="cuda", generator=gen)
+        plane = mu.KvPlane(key.data_ptr(), val.data_ptr(), cap, 0, 0, 0, KV_DIM, KV_HEAD_DIM,
+                           1 if nope else 0, 0)
+        layers.append((plane, key, val, kr, vr, origin, n, nope))
+    row_bytes = sum(2 * 2 * n * KV_DIM for (_, _, _, _, _, _, n, _) in layers)
+    stream = torch.cuda.current_stream()
+    sh = stream.cuda_stream
+
+    def restore(rows=None):
+        for i, (plane, _, _, kr, vr, origin, n, _) in enumerate(layers):
+            k_ptr, v_ptr = (kr.data_ptr(), vr.data_ptr()) if rows is None else rows[i]
+            r = L.muser_kv_restore(ctypes.byref(plane), k_ptr, v_ptr, origin, n, sh)
+            if r != 0:
+                raise RuntimeError(f"kv_restore: {mu.muser_last_error()}")
+
+    def snapshot():
+        for plane, _, _, kr, vr, origin, n, _ in layers:
+            r = L.muser_kv_snapshot(ctypes.byref(plane), origin, n, kr.data_ptr(), vr.data_ptr(), sh)
+            if r != 0:
+                raise RuntimeError(f"kv_snapshot: {mu.muser_last_error()}")
+
+    def barrier():
+        torch.cuda.synchronize()
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    for _ in range(args.warmup):
+        restore()
+        snapshot()
+    barrier()
+    # the restored planes hold the rows at their rotation (a sampled check; the
+    # bit-exact comparison against the oracle is in the GPU tests)
+    plane, key, _, kr, _, origin, n, _ = layers[-1]
+    rot = origin % plane.capacity
+    assert (plane.len, plane.origin_logical, plane.origin_physical) == (n, origin, rot)
+    assert torch.equal(key.view(-1, KV_DIM)[rot], kr.view(-1, KV_DIM)[0])
+    uuid = None
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(torch.cuda.current_device()).uuid)
+    except Exception:
+        pass
+    clocks = ClockSampler(uuid)
+    clocks.start()
+    time.sleep(0.3)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    barrier()
+    for a, b in evs:
+        a.record(stream)
+        restore()
+        b.record(stream)
+    barrier()
+    ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    sev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for a, b in sev:
+        a.record(stream)
+        snapshot()
+        b.record(stream)
+    barrier()
+    clock = clocks.stop()
+    snap_ms = statistics.mean(a.elapsed_time(b) for a, b in sev)
+    # one NoPE plane restore alone: the dominant launch
+    one = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    plane0, _, _, kr0, vr0, _, n0, _ = layers[0]
+    for a, b in one:
+        a.record(stream)
+        L.muser_kv_restore(ctypes.byref(plane0), kr0.data_ptr(), vr0.data_ptr(), 0, n0, sh)
+        b.record(stream)
+    barrier()
+    one_ms = statistics.mean(a.elapsed_time(b) for a, b in one)
+    if dist is not None:
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    # end to end: the detached rows arrive in pinned host memory (as from the wire)
+    host_rows = [(torch.empty(n * KV_DIM, dtype=torch.int16).pin_memory(),
+                  torch.empty(n * KV_DIM, dtype=torch.int16).pin_memory())
+                 for (_, _, _, _, _, _, n, _) in layers]
+    for (hk, hv), (_, _, _, kr, vr, _, _, _) in zip(host_rows, layers):
+        hk.copy_(kr)
+        hv.copy_(vr)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        for (hk, hv), (_, _, _, kr, vr, _, _, _) in zip(host_rows, layers):
+            kr.copy_(hk, non_blocking=True)
+            vr.copy_(hv, non_blocking=True)
+        restore()
+    e1.record(stream)
+    barrier()
+    e2e_ms = e0.elapsed_time(e1) / args.steps
+    peak, peak_kind = read_peaks()
+    moved = 2 * row_bytes
+    gbs = world * moved / (ms * 1e-3) / 1e9
+    one_bytes = 2 * 2 * 2 * n0 * KV_DIM
+    achieved = one_bytes / (one_ms * 1e-3) / 1e9
+    return {
+        "metric": "K/V bytes moved GB/s (read + write, % of GB300 HBM copy peak), 1 GPU", "value": round(gbs, 2),
+        "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u16",
+        "data": "synthetic (seeded random binary16 bit patterns)",
+        "config": {"workload": f"K/V restore of one session at {KV_TOKENS} tokens: {KV_NOPE} head-major NoPE planes "
+                               f"({KV_MAX_CONTEXT} rows) and {KV_SWA} token-major SWA rings ({KV_SWA_CAP} rows, "
+                               f"origin {swa_origin}, rotation {swa_origin % KV_SWA_CAP})",
+                   "kv_dim": KV_DIM, "head_dim": KV_HEAD_DIM, "row_bytes_per_step": row_bytes,
+                   "l2": f"inputs larger than L2: {row_bytes / 1e9:.2f} GB of rows per step vs 129 MB L2",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "hbm_frac_of_" + peak_kind: round(gbs / world / peak, 4),
+        "snapshot": {"ms_per_step": round(snap_ms, 4), "value": round(moved / (snap_ms * 1e-3) / 1e9, 2),
+                     "unit": "GB/s", "api": "muser_kv_snapshot of every layer's live window"},
+        "roofline": {"bound": "hbm", "kernel": "kv_window_kernel<8, restore> (one NoPE plane pair, 268 MB moved)",
+                     "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "traffic": None, "algorithmic_bytes_per_launch": one_bytes,
+                     "mean_launch_us": round(one_ms * 1e3, 2)},
+        "e2e": {"value": round(world * moved / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+                "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": row_bytes, "d2h_bytes_per_step": 0,
+                "api": "muser_kv_restore with the detached rows in from pinned host memory"},
+        "gpu_launches": args.steps * len(layers), "clocks": clock, "device_status": mu.muser_device_status(),
+    }
+
+
 def run_reference(args, rank, world):
     if rank != 0:
         return None
@@ -764,7 +1068,8 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
-    ap.add_argument("--workload", choices=["stack52_m1", "stack52_m16", "attn52_m1", "attn52_m16", "lmhead_m1"],
+    ap.add_argument("--workload", choices=["stack52_m1", "stack52_m16", "attn52_m1", "attn52_m16", "lmhead_m1",
+                                           "kv_restore", "down_tail_q4k", "down_tail_q6k", "matvec_q5k"],
                     default="stack52_m1")
     ap.add_argument("--layers", type=int, default=NL)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
@@ -780,6 +1085,10 @@ def main():
         res = run_attn(args, rank, world)
     elif args.workload == "lmhead_m1":
         res = run_lmhead(args, rank, world)
+    elif args.workload == "kv_restore":
+        res = run_kv_restore(args, rank, world)
+    elif args.workload.startswith("down_tail") or args.workload == "matvec_q5k":
+        res = run_down_tail(args, rank, world)
     else:
         res = run_native(args, rank, world)
     if rank == 0 and res is not None:

@@ -24,7 +24,12 @@
  *  - Types: activations and norm weights are binary32 ("f32"), row-major.
  *    A quantized matrix W with `rows` outputs and `cols` inputs is stored as
  *    rows of cols/256 consecutive super-blocks: rows*(cols/256)*block_bytes
- *    bytes, block_bytes = 144 (Q4_K) or 210 (Q6_K).
+ *    bytes, block_bytes = 144 (Q4_K), 176 (Q5_K) or 210 (Q6_K).
+ *  - Quant types: every matvec entry point takes Q4_K and Q6_K.
+ *    muser_dequantize and muser_qmatvec also take Q5_K, the third k-quant of
+ *    the book's kernel registry (Ch 4 §4.4; ggml layout: f16 d and dmin,
+ *    Q4_K's packed scales and mins, 32 bytes of fifth code bits, 128 code
+ *    bytes).  Any other type, or Q5_K elsewhere, is MUSER_ERR_UNSUPPORTED.
  *  - Alignment: f32 pointers and quantized matrices 16-byte aligned (any
  *    cudaMalloc/torch allocation is).  Misaligned pointers return
  *    MUSER_ERR_MISALIGNED.
@@ -46,7 +51,7 @@ extern "C" {
 #define MUSER_MAX_M 16
 
 /* ggml type ids, informational */
-typedef enum { MUSER_Q4_K = 12, MUSER_Q6_K = 14 } muser_qtype;
+typedef enum { MUSER_Q4_K = 12, MUSER_Q5_K = 13, MUSER_Q6_K = 14 } muser_qtype;
 
 typedef enum {
     MUSER_OK = 0,
@@ -65,7 +70,7 @@ int muser_version(void);
  * stays valid until the next failing call on the same thread. */
 const char* muser_last_error(void);
 
-/* Bytes of one super-block of `qtype` (144, 210; 0 if unknown). */
+/* Bytes of one super-block of `qtype` (144, 176, 210; 0 if unknown). */
 size_t muser_block_bytes(int qtype);
 
 /* Bytes of a rows x cols matrix of `qtype` (0 if cols % 256 != 0 or the type
@@ -74,7 +79,8 @@ size_t muser_matrix_bytes(int qtype, int64_t rows, int64_t cols);
 
 /*
  * muser_dequantize -- out[r*cols + k] = the binary32 value of weight (r, k).
- *   Q4_K: d*scale_j*q - dmin*min_j of sub-block j = k%256/32; Q6_K:
+ *   Q4_K: d*scale_j*q - dmin*min_j of sub-block j = k%256/32 (Q5_K the
+ *   same with q = 0..31, its fifth bit from qh); Q6_K:
  *   d*scale_s*(q-32) of sub-block s = k%256/16 (block layouts: Ch 19 §19.3,
  *   ggml super-block bit positions).  Each value is the exactly rounded
  *   binary32 of that expression; this is the bit-exact test hook of the
@@ -368,6 +374,40 @@ typedef struct {
  */
 int muser_kv_ring_write(muser_kv_plane* plane, const float* k, const float* v, int64_t position,
                         int64_t count, int64_t* first_physical, void* stream);
+
+/*
+ * muser_kv_snapshot -- copy the live logical rows first_logical ..
+ *   first_logical+count-1 out of a plane pair as a detached window (Ch 15
+ *   §15.6, the snapshot a restore replays).  The row of logical position q
+ *   sits in slot (origin_physical + q - origin_logical) % capacity.
+ *   plane: host struct, read only; k_rows, v_rows: device binary16
+ *   [count*kv_dim], token-major, in logical order, 2-byte aligned (16-byte
+ *   alignment with kv_dim, and head_dim for head-major planes, multiples of 8
+ *   takes 16-byte copies), not overlapping the planes.  count == 0 launches
+ *   nothing.  A range outside [origin_logical, origin_logical+len) returns
+ *   MUSER_ERR_INVALID_ARG and writes nothing.
+ */
+int muser_kv_snapshot(const muser_kv_plane* plane, int64_t first_logical, int64_t count,
+                      uint16_t* k_rows, uint16_t* v_rows, void* stream);
+
+/*
+ * muser_kv_restore -- install a detached window of `len` logical rows starting
+ *   at logical position origin_logical at the rotation a ring built by
+ *   sequential appends holds there (Ch 15 §15.6; Ch 10 §10.7): rotation =
+ *   origin_logical % capacity, logical row j goes to slot (rotation + j) %
+ *   capacity, and on success the metadata becomes len = len, origin_logical =
+ *   origin_logical, origin_physical = rotation.  Attention scans slots in
+ *   physical order, so this placement keeps a restored session's sums, and
+ *   their rounding, those of the live one.  Slots outside the window are not
+ *   written; a NoPE plane (origin 0) gets the plain layout.
+ *   plane: host struct (updated on success); k_rows, v_rows: device binary16
+ *   [len*kv_dim], token-major, as muser_kv_snapshot writes them, not
+ *   overlapping the planes.  origin_logical < 0, len < 0 or len > capacity
+ *   returns MUSER_ERR_INVALID_ARG and changes nothing.  len == 0 only sets the
+ *   metadata.
+ */
+int muser_kv_restore(muser_kv_plane* plane, const uint16_t* k_rows, const uint16_t* v_rows,
+                     int64_t origin_logical, int64_t len, void* stream);
 
 /*
  * muser_sync -- wait until all work enqueued on `stream` has finished, for at

@@ -16,7 +16,7 @@ import os
 import threading
 
 __all__ = [
-    "MUSER_Q4_K", "MUSER_Q6_K", "QTYPES", "MuserError", "build", "library_path", "lib",
+    "MUSER_Q4_K", "MUSER_Q5_K", "MUSER_Q6_K", "QTYPES", "MuserError", "build", "library_path", "lib",
     "muser_version", "muser_last_error", "muser_block_bytes", "muser_matrix_bytes",
     "muser_dequantize", "muser_qmatvec", "muser_rms_norm", "muser_silu_mul",
     "muser_ffn_gate_up_silu", "muser_gate_up_scratch_bytes", "muser_ffn_gate_up_silu_scratch",
@@ -25,15 +25,16 @@ __all__ = [
     "muser_fused_residual_dual_rmsnorm", "muser_scratch_bytes",
     "muser_qmatvec_residual_dual_rmsnorm", "muser_qmatvec_residual_dual_rmsnorm_static",
     "MUSER_STATIC_SCRATCH_BYTES", "FfnLayer", "muser_ffn_workspace_bytes",
-    "muser_ffn_stack", "KvPlane", "muser_kv_ring_write", "muser_sync", "muser_debug_spin",
+    "muser_ffn_stack", "KvPlane", "muser_kv_ring_write", "muser_kv_snapshot", "muser_kv_restore", "muser_sync", "muser_debug_spin",
     "muser_device_sm_count", "muser_device_status",
 ]
 
 MUSER_Q4_K = 12
+MUSER_Q5_K = 13
 MUSER_Q6_K = 14
-QTYPES = {"q4_k": MUSER_Q4_K, "q6_k": MUSER_Q6_K}
+QTYPES = {"q4_k": MUSER_Q4_K, "q5_k": MUSER_Q5_K, "q6_k": MUSER_Q6_K}
 MUSER_STATIC_SCRATCH_BYTES = 1 << 20
-BLOCK_BYTES = {MUSER_Q4_K: 144, MUSER_Q6_K: 210}
+BLOCK_BYTES = {MUSER_Q4_K: 144, MUSER_Q5_K: 176, MUSER_Q6_K: 210}
 STATUS = {0: "MUSER_OK", -1: "MUSER_ERR_INVALID_ARG", -2: "MUSER_ERR_UNSUPPORTED",
           -3: "MUSER_ERR_MISALIGNED", -4: "MUSER_ERR_CACHE_DISCONTINUITY", -5: "MUSER_ERR_CUDA",
           -6: "MUSER_ERR_TIMEOUT"}
@@ -112,6 +113,8 @@ def lib():
                                     P]),
             "muser_kv_ring_write": (I, [ctypes.POINTER(KvPlane), P, P, I64, I64,
                                         ctypes.POINTER(I64), P]),
+            "muser_kv_snapshot": (I, [ctypes.POINTER(KvPlane), I64, I64, P, P, P]),
+            "muser_kv_restore": (I, [ctypes.POINTER(KvPlane), P, P, I64, I64, P]),
             "muser_sync": (I, [P, I]),
             "muser_debug_spin": (I, [I64, P]),
             "muser_device_sm_count": (I, []),
@@ -304,6 +307,22 @@ def muser_kv_ring_write(plane: KvPlane, k, v, position: int, count: int, stream=
            lib().muser_kv_ring_write(ctypes.byref(plane), _ptr(k), _ptr(v), position, count,
                                      ctypes.byref(first), _stream(stream)))
     return first.value
+
+
+def muser_kv_snapshot(plane: KvPlane, first_logical: int, count: int, k_rows, v_rows,
+                      stream=None) -> None:
+    """Copies live logical rows first_logical..+count out as token-major binary16 rows."""
+    _check("muser_kv_snapshot",
+           lib().muser_kv_snapshot(ctypes.byref(plane), first_logical, count, _ptr(k_rows),
+                                   _ptr(v_rows), _stream(stream)))
+
+
+def muser_kv_restore(plane: KvPlane, k_rows, v_rows, origin_logical: int, length: int,
+                     stream=None) -> None:
+    """Installs `length` logical rows from origin_logical at rotation origin % capacity."""
+    _check("muser_kv_restore",
+           lib().muser_kv_restore(ctypes.byref(plane), _ptr(k_rows), _ptr(v_rows), origin_logical,
+                                  length, _stream(stream)))
 
 
 def muser_sync(stream=None, timeout_ms: int = -1) -> int:

@@ -50,16 +50,22 @@ int device_attr(int* cache, cudaDeviceAttr attr) {
     return cache[dev];
 }
 
+// The FFN, tail, group and LM-head calls take Q4_K and Q6_K; the plain
+// matvec and dequantisation take Q5_K as well.
 bool known_qtype(int q) { return q == MUSER_Q4_K || q == MUSER_Q6_K; }
+bool matvec_qtype(int q) { return known_qtype(q) || q == MUSER_Q5_K; }
 size_t block_bytes_of(int q) {
     return q == MUSER_Q4_K ? static_cast<size_t>(kQ4KBytes)
-                           : (q == MUSER_Q6_K ? static_cast<size_t>(kQ6KBytes) : 0);
+                           : q == MUSER_Q5_K ? static_cast<size_t>(kQ5KBytes)
+                                             : (q == MUSER_Q6_K ? static_cast<size_t>(kQ6KBytes) : 0);
 }
 
 // Shared checks of a quantized matrix operand.
-int check_matrix(const char* fn, int qtype, const void* W, int64_t rows, int64_t cols) {
-    if (!known_qtype(qtype))
-        return set_error(MUSER_ERR_UNSUPPORTED, "%s: unsupported quant type %d (Q4_K=12, Q6_K=14)", fn, qtype);
+int check_matrix(const char* fn, int qtype, const void* W, int64_t rows, int64_t cols,
+                 bool allow_q5 = false) {
+    if (!(allow_q5 ? matvec_qtype(qtype) : known_qtype(qtype)))
+        return set_error(MUSER_ERR_UNSUPPORTED, "%s: unsupported quant type %d (Q4_K=12, %sQ6_K=14)", fn,
+                         qtype, allow_q5 ? "Q5_K=13, " : "");
     if (W == nullptr) return set_error(MUSER_ERR_INVALID_ARG, "%s: weight pointer is NULL", fn);
     if (rows < 1 || rows > (int64_t{1} << 31))
         return set_error(MUSER_ERR_INVALID_ARG, "%s: rows = %lld out of range", fn, (long long)rows);
@@ -326,14 +332,14 @@ const char* muser_last_error(void) { return g_err; }
 size_t muser_block_bytes(int qtype) { return block_bytes_of(qtype); }
 
 size_t muser_matrix_bytes(int qtype, int64_t rows, int64_t cols) {
-    if (!known_qtype(qtype) || rows < 0 || cols < 0 || cols % kQK) return 0;
+    if (!matvec_qtype(qtype) || rows < 0 || cols < 0 || cols % kQK) return 0;
     return static_cast<size_t>(rows) * static_cast<size_t>(cols / kQK) * block_bytes_of(qtype);
 }
 
 int muser_dequantize(int qtype, const void* W, int64_t rows, int64_t cols, float* out,
                      void* stream) {
     clear_error();
-    MUSER_TRY(check_matrix("muser_dequantize", qtype, W, rows, cols));
+    MUSER_TRY(check_matrix("muser_dequantize", qtype, W, rows, cols, true));
     MUSER_TRY(check_f32("muser_dequantize", "out", out));
     return launch_dequantize(qtype, static_cast<const uint8_t*>(W), rows, cols, out,
                              as_stream(stream));
@@ -343,7 +349,7 @@ int muser_qmatvec(int qtype, const void* W, int64_t rows, int64_t cols, const fl
                   float* y, void* stream) {
     clear_error();
     const char* fn = "muser_qmatvec";
-    MUSER_TRY(check_matrix(fn, qtype, W, rows, cols));
+    MUSER_TRY(check_matrix(fn, qtype, W, rows, cols, true));
     MUSER_TRY(check_M(fn, M));
     MUSER_TRY(check_f32(fn, "x", x));
     MUSER_TRY(check_f32(fn, "y", y));
@@ -750,12 +756,10 @@ int muser_ffn_stack(const muser_ffn_layer* layers, int n_layers, const float* en
     return MUSER_OK;
 }
 
-int muser_kv_ring_write(muser_kv_plane* plane, const float* k, const float* v, int64_t position,
-                        int64_t count, int64_t* first_physical, void* stream) {
-    clear_error();
-    const char* fn = "muser_kv_ring_write";
+// The plane checks shared by the K/V calls (Ch 15 §15.2 metadata invariants).
+static int check_plane(const muser_kv_plane* plane, const char* fn) {
     if (plane == nullptr) return set_error(MUSER_ERR_INVALID_ARG, "%s: plane is NULL", fn);
-    muser_kv_plane& P = *plane;
+    const muser_kv_plane& P = *plane;
     if (P.key == nullptr || P.value == nullptr)
         return set_error(MUSER_ERR_INVALID_ARG, "%s: plane buffers are NULL", fn);
     if (!is_aligned(P.key, 2) || !is_aligned(P.value, 2))
@@ -765,6 +769,15 @@ int muser_kv_ring_write(muser_kv_plane* plane, const float* k, const float* v, i
         return set_error(MUSER_ERR_INVALID_ARG, "%s: inconsistent ring metadata", fn);
     if (P.kv_dim < 1 || (P.head_major && (P.head_dim < 1 || P.kv_dim % P.head_dim != 0)))
         return set_error(MUSER_ERR_INVALID_ARG, "%s: bad kv_dim/head_dim", fn);
+    return MUSER_OK;
+}
+
+int muser_kv_ring_write(muser_kv_plane* plane, const float* k, const float* v, int64_t position,
+                        int64_t count, int64_t* first_physical, void* stream) {
+    clear_error();
+    const char* fn = "muser_kv_ring_write";
+    MUSER_TRY(check_plane(plane, fn));
+    muser_kv_plane& P = *plane;
     if (count < 0) return set_error(MUSER_ERR_INVALID_ARG, "%s: count < 0", fn);
     const int64_t expected = P.origin_logical + P.len;
     if (position != expected)
@@ -794,6 +807,53 @@ int muser_kv_ring_write(muser_kv_plane* plane, const float* k, const float* v, i
         P.origin_physical = (P.origin_physical + advance) % P.capacity;
     }
     if (first_physical) *first_physical = phys_first;
+    return MUSER_OK;
+}
+
+int muser_kv_snapshot(const muser_kv_plane* plane, int64_t first_logical, int64_t count,
+                      uint16_t* k_rows, uint16_t* v_rows, void* stream) {
+    clear_error();
+    const char* fn = "muser_kv_snapshot";
+    MUSER_TRY(check_plane(plane, fn));
+    const muser_kv_plane& P = *plane;
+    if (count < 0 || count > P.len || first_logical < P.origin_logical ||
+        first_logical - P.origin_logical > P.len - count)
+        return set_error(MUSER_ERR_INVALID_ARG,
+                         "%s: rows %lld..+%lld are outside the live window %lld..+%lld", fn,
+                         (long long)first_logical, (long long)count, (long long)P.origin_logical,
+                         (long long)P.len);
+    if (count == 0) return MUSER_OK;
+    if (!k_rows || !v_rows) return set_error(MUSER_ERR_INVALID_ARG, "%s: k_rows/v_rows NULL", fn);
+    if (!is_aligned(k_rows, 2) || !is_aligned(v_rows, 2))
+        return set_error(MUSER_ERR_MISALIGNED, "%s: k_rows/v_rows must be 2-byte aligned", fn);
+    const int64_t phys0 = (P.origin_physical + (first_logical - P.origin_logical)) % P.capacity;
+    return launch_kv_window(P.key, P.value, k_rows, v_rows, P.kv_dim, P.head_dim, P.head_major,
+                            P.capacity, phys0, count, false, as_stream(stream));
+}
+
+int muser_kv_restore(muser_kv_plane* plane, const uint16_t* k_rows, const uint16_t* v_rows,
+                     int64_t origin_logical, int64_t len, void* stream) {
+    clear_error();
+    const char* fn = "muser_kv_restore";
+    MUSER_TRY(check_plane(plane, fn));
+    muser_kv_plane& P = *plane;
+    if (origin_logical < 0 || len < 0 || len > P.capacity)
+        return set_error(MUSER_ERR_INVALID_ARG,
+                         "%s: a window of %lld rows from origin %lld does not fit capacity %lld", fn,
+                         (long long)len, (long long)origin_logical, (long long)P.capacity);
+    const int64_t rotation = origin_logical % P.capacity;
+    if (len > 0) {
+        if (!k_rows || !v_rows) return set_error(MUSER_ERR_INVALID_ARG, "%s: k_rows/v_rows NULL", fn);
+        if (!is_aligned(k_rows, 2) || !is_aligned(v_rows, 2))
+            return set_error(MUSER_ERR_MISALIGNED, "%s: k_rows/v_rows must be 2-byte aligned", fn);
+        MUSER_TRY(launch_kv_window(P.key, P.value, const_cast<uint16_t*>(k_rows),
+                                   const_cast<uint16_t*>(v_rows), P.kv_dim, P.head_dim,
+                                   P.head_major, P.capacity, rotation, len, true,
+                                   as_stream(stream)));
+    }
+    P.len = len;
+    P.origin_logical = origin_logical;
+    P.origin_physical = rotation;
     return MUSER_OK;
 }
 

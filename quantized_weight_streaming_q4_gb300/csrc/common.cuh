@@ -47,6 +47,10 @@ unsigned read_device_status(bool reset);
 constexpr int kQK = 256;          // weights per super-block
 constexpr int kQ4KBytes = 144;    // Q4_K super-block bytes
 constexpr int kQ6KBytes = 210;    // Q6_K super-block bytes
+constexpr int kQ5KBytes = 176;    // Q5_K super-block bytes
+// Super-block bytes of a quant type known at compile time.
+template <int QT>
+constexpr int kBlockBytes = QT == MUSER_Q4_K ? kQ4KBytes : (QT == MUSER_Q5_K ? kQ5KBytes : kQ6KBytes);
 
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll

@@ -106,6 +106,11 @@ int launch_dual_tail(float* resid, const float* src, float* out, const float* w1
 int launch_kv_store(uint16_t* key, uint16_t* value, const float* k, const float* v,
                     int64_t kv_dim, int64_t head_dim, int head_major, int64_t capacity,
                     int64_t phys_of_first, int64_t src_first, int64_t nrows, cudaStream_t s);
+// Ch 15 §15.6: rows j < count of a window <-> plane slot (phys0 + j) % capacity;
+// to_plane restores detached rows into the plane, else snapshots them out.
+int launch_kv_window(uint16_t* key, uint16_t* value, uint16_t* k_rows, uint16_t* v_rows,
+                     int64_t kv_dim, int64_t head_dim, int head_major, int64_t capacity,
+                     int64_t phys0, int64_t count, bool to_plane, cudaStream_t s);
 int launch_spin(int64_t microseconds, cudaStream_t s);
 
 }  // namespace muser

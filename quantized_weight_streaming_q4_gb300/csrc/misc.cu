@@ -48,6 +48,49 @@ __global__ void dequant_q4k_kernel(const uint8_t* __restrict__ W, int64_t nblock
     }
 }
 
+// Q5_K: as Q4_K, with the codes at byte 48 and a fifth code bit, bit
+// 2c + (j & 1) of qh[l] (bytes 16..47), for weight l of sub-block j.
+__global__ void dequant_q5k_kernel(const uint8_t* __restrict__ W, int64_t nblocks,
+                                   float* __restrict__ out) {
+    const int64_t gid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (gid >= nblocks * 8) return;
+    const int64_t blkno = gid >> 3;
+    const int j = static_cast<int>(gid & 7);
+    const uint8_t* blk = W + blkno * kQ5KBytes;
+    const uint4 hd = *reinterpret_cast<const uint4*>(blk);
+    const int c = j >> 1;
+    const uint4 ha = *reinterpret_cast<const uint4*>(blk + 16);
+    const uint4 hb = *reinterpret_cast<const uint4*>(blk + 32);
+    const uint4 qa = *reinterpret_cast<const uint4*>(blk + 48 + 32 * c);
+    const uint4 qb = *reinterpret_cast<const uint4*>(blk + 64 + 32 * c);
+    uint32_t sc, mn;
+    if (j < 4) {
+        sc = (hd.y >> (8 * j)) & 63u;
+        mn = (hd.z >> (8 * j)) & 63u;
+    } else {
+        const int jj = j - 4;
+        sc = ((hd.w >> (8 * jj)) & 0x0Fu) | (((hd.y >> (8 * jj + 6)) & 3u) << 4);
+        mn = ((hd.w >> (8 * jj + 4)) & 0x0Fu) | (((hd.z >> (8 * jj + 6)) & 3u) << 4);
+    }
+    const float dsc = __fmul_rn(h2f(hd.x), static_cast<float>(sc));
+    const float ndm = -__fmul_rn(h2f(hd.x >> 16), static_cast<float>(mn));
+    const uint32_t words[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
+    const uint32_t hbits[8] = {ha.x, ha.y, ha.z, ha.w, hb.x, hb.y, hb.z, hb.w};
+    const int sh = (j & 1) ? 4 : 0;
+    const int hsh = 2 * c + (j & 1);
+    float* o = out + blkno * kQK + 32 * j;
+#pragma unroll
+    for (int t = 0; t < 8; ++t) {
+        const uint32_t q5 = ((words[t] >> sh) & 0x0F0F0F0Fu) | (((hbits[t] >> hsh) & 0x01010101u) << 4);
+        float4 v;
+        v.x = __fmaf_rn(dsc, static_cast<float>(q5 & 0xFFu), ndm);
+        v.y = __fmaf_rn(dsc, static_cast<float>((q5 >> 8) & 0xFFu), ndm);
+        v.z = __fmaf_rn(dsc, static_cast<float>((q5 >> 16) & 0xFFu), ndm);
+        v.w = __fmaf_rn(dsc, static_cast<float>(q5 >> 24), ndm);
+        reinterpret_cast<float4*>(o)[t] = v;
+    }
+}
+
 __global__ void dequant_q6k_kernel(const uint8_t* __restrict__ W, int64_t nblocks,
                                    float* __restrict__ out) {
     const int64_t gid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
@@ -139,6 +182,48 @@ __global__ void kv_store_kernel(uint16_t* key, uint16_t* value, const float* k, 
     }
 }
 
+// Muser book Ch 15 §15.6: moves `count` token rows between a K/V plane pair
+// and detached token-major rows.  Row j of the window <-> physical slot
+// (phys0 + j) % capacity, in either plane layout (§15.3 Figure 15.1).  Each
+// thread moves VW consecutive halves of one row: VW = 8 (16-byte vectors) when
+// every 8-half group stays inside one head row and all four buffers are
+// 16-byte aligned, else 1.  Consecutive threads cover one row, so the rows side
+// is read or written contiguously and the plane side in head-row runs.
+template <int VW, bool TO_PLANE>
+__global__ void kv_window_kernel(uint16_t* __restrict__ pk, uint16_t* __restrict__ pv,
+                                 uint16_t* __restrict__ rk, uint16_t* __restrict__ rv,
+                                 int64_t kv_dim, int64_t head_dim, int head_major,
+                                 int64_t capacity, int64_t phys0, int64_t count) {
+    const int64_t per_row = kv_dim / VW;
+    const int64_t total = count * per_row;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t j = i / per_row;
+        const int64_t e = (i - j * per_row) * VW;
+        const int64_t p = (phys0 + j) % capacity;
+        const int64_t pi =
+            head_major ? ((e / head_dim) * capacity + p) * head_dim + e % head_dim : p * kv_dim + e;
+        const int64_t ri = j * kv_dim + e;
+        if constexpr (VW == 8) {
+            if constexpr (TO_PLANE) {
+                *reinterpret_cast<uint4*>(pk + pi) = *reinterpret_cast<const uint4*>(rk + ri);
+                *reinterpret_cast<uint4*>(pv + pi) = *reinterpret_cast<const uint4*>(rv + ri);
+            } else {
+                *reinterpret_cast<uint4*>(rk + ri) = *reinterpret_cast<const uint4*>(pk + pi);
+                *reinterpret_cast<uint4*>(rv + ri) = *reinterpret_cast<const uint4*>(pv + pi);
+            }
+        } else {
+            if constexpr (TO_PLANE) {
+                pk[pi] = rk[ri];
+                pv[pi] = rv[ri];
+            } else {
+                rk[ri] = pk[pi];
+                rv[ri] = pv[pi];
+            }
+        }
+    }
+}
+
 // Busy-waits on the global nanosecond timer; returns after `ns` (bounded).
 __global__ void spin_kernel(uint64_t ns) {
     uint64_t t0, t;
@@ -159,6 +244,7 @@ int launch_dequantize(int qtype, const uint8_t* W, int64_t rows, int64_t cols, f
     const int bs = 256;
     const int64_t grid = (threads + bs - 1) / bs;
     if (qtype == MUSER_Q4_K) dequant_q4k_kernel<<<static_cast<unsigned>(grid), bs, 0, s>>>(W, nblocks, out);
+    else if (qtype == MUSER_Q5_K) dequant_q5k_kernel<<<static_cast<unsigned>(grid), bs, 0, s>>>(W, nblocks, out);
     else dequant_q6k_kernel<<<static_cast<unsigned>(grid), bs, 0, s>>>(W, nblocks, out);
     return check_launch("dequantize");
 }
@@ -201,6 +287,32 @@ int launch_kv_store(uint16_t* key, uint16_t* value, const float* k, const float*
     kv_store_kernel<<<static_cast<unsigned>(grid), bs, 0, s>>>(
         key, value, k, v, kv_dim, head_dim, head_major, capacity, phys_of_first, src_first, nrows);
     return check_launch("kv_store");
+}
+
+int launch_kv_window(uint16_t* key, uint16_t* value, uint16_t* k_rows, uint16_t* v_rows,
+                     int64_t kv_dim, int64_t head_dim, int head_major, int64_t capacity,
+                     int64_t phys0, int64_t count, bool to_plane, cudaStream_t s) {
+    if (count == 0) return MUSER_OK;
+    const auto a16 = [](const void* q) { return (reinterpret_cast<uintptr_t>(q) & 15u) == 0; };
+    const bool vec = kv_dim % 8 == 0 && (!head_major || head_dim % 8 == 0) && a16(key) &&
+                     a16(value) && a16(k_rows) && a16(v_rows);
+    const int64_t total = count * (vec ? kv_dim / 8 : kv_dim);
+    const int bs = 256;
+    const int64_t grid = std::min<int64_t>((total + bs - 1) / bs, static_cast<int64_t>(sm_count()) * 8);
+    const unsigned g = static_cast<unsigned>(grid);
+    if (vec && to_plane)
+        kv_window_kernel<8, true><<<g, bs, 0, s>>>(key, value, k_rows, v_rows, kv_dim, head_dim,
+                                                  head_major, capacity, phys0, count);
+    else if (vec)
+        kv_window_kernel<8, false><<<g, bs, 0, s>>>(key, value, k_rows, v_rows, kv_dim, head_dim,
+                                                   head_major, capacity, phys0, count);
+    else if (to_plane)
+        kv_window_kernel<1, true><<<g, bs, 0, s>>>(key, value, k_rows, v_rows, kv_dim, head_dim,
+                                                  head_major, capacity, phys0, count);
+    else
+        kv_window_kernel<1, false><<<g, bs, 0, s>>>(key, value, k_rows, v_rows, kv_dim, head_dim,
+                                                   head_major, capacity, phys0, count);
+    return check_launch("kv_window");
 }
 
 int launch_spin(int64_t microseconds, cudaStream_t s) {

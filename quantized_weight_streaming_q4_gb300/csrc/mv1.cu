@@ -118,13 +118,13 @@ struct SliceQ6 {
 // and the slice's digit words are rotated the same way.
 // ------------------------------------------------ slice conversion
 // The consumer threads convert the slices in quarters: quarter k of slot s
-// holds 16 of its 64 inputs (Q4_K: words 4(k&1)..4(k&1)+3 of the low half
+// holds 16 of its 64 inputs (Q4_K and Q5_K: words 4(k&1)..4(k&1)+3 of the low half
 // for k < 2, of the high half for k >= 2; Q6_K: group k).  The four quarters
 // of a slot sit in four neighbouring lanes, which agree on the slot's
 // exponent with two shuffles.  The digit words and the slot's scalars then
 // overwrite the slot's inputs, and every thread loads the record of its own
 // slot.  Record layouts (32-bit words):
-//   Q4_K: lo[d][t] at 8d + t, hi[d][t] at 24 + 8d + t; inv, s_lo, s_hi at 48..50.
+//   Q4_K, Q5_K: lo[d][t] at 8d + t, hi[d][t] at 24 + 8d + t; inv, s_lo, s_hi at 48..50.
 //   Q6_K: x[g][d][i] at 12g + 4d + i; neg32[g][d] at 48 + 3g + d; inv at 60.
 // All 32 lanes of a warp call it (shuffles); a lane with !valid converts
 // zeros and stores nothing.
@@ -154,7 +154,7 @@ __device__ __forceinline__ void convert_quarter(uint8_t* slot, int k, bool valid
         pack_digits(__float2int_rn(v[4 * i] * p2e), __float2int_rn(v[4 * i + 1] * p2e),
                     __float2int_rn(v[4 * i + 2] * p2e), __float2int_rn(v[4 * i + 3] * p2e), D[i]);
     uint32_t* rec = reinterpret_cast<uint32_t*>(slot);
-    if constexpr (QT == MUSER_Q4_K) {
+    if constexpr (QT != MUSER_Q6_K) {
         float sum = 0.0f;
 #pragma unroll
         for (int l = 0; l < 16; ++l) sum += v[l];
@@ -335,6 +335,64 @@ __device__ __forceinline__ void dot_q4(const SliceQ4& s, const uint8_t* const* b
     }
 }
 
+// Q5_K (Ch 4 §4.4's third k-quant; ggml layout): Q4_K's header and code
+// nibbles (code bytes at 48 + 32c) plus a fifth code bit, bit 2c (low half) or
+// 2c + 1 (high half) of qh[l] at byte 16 + l.  One rotation brings that bit of
+// every qh byte to bit 4, where it joins the nibble, so both halves' codes are
+// bytes q = 0..31 and both scales apply unscaled.
+template <int NR>
+__device__ __forceinline__ void dot_q5(const SliceQ4& s, const uint8_t* const* blk, int c,
+                                       uint32_t sel_lo, uint32_t sel_hi, float* out) {
+    const int rot_lo = (4 - 2 * c) & 31, rot_hi = (3 - 2 * c) & 31;
+    uint4 hd[NR];
+    uint32_t W[NR][8], Hb[NR][8];
+#pragma unroll
+    for (int r = 0; r < NR; ++r) {
+        hd[r] = *reinterpret_cast<const uint4*>(blk[r]);
+        const uint4 ha = *reinterpret_cast<const uint4*>(blk[r] + 16);
+        const uint4 hb = *reinterpret_cast<const uint4*>(blk[r] + 32);
+        const uint4 qa = *reinterpret_cast<const uint4*>(blk[r] + 48 + 32 * c);
+        const uint4 qb = *reinterpret_cast<const uint4*>(blk[r] + 64 + 32 * c);
+        W[r][0] = qa.x; W[r][1] = qa.y; W[r][2] = qa.z; W[r][3] = qa.w;
+        W[r][4] = qb.x; W[r][5] = qb.y; W[r][6] = qb.z; W[r][7] = qb.w;
+        Hb[r][0] = ha.x; Hb[r][1] = ha.y; Hb[r][2] = ha.z; Hb[r][3] = ha.w;
+        Hb[r][4] = hb.x; Hb[r][5] = hb.y; Hb[r][6] = hb.z; Hb[r][7] = hb.w;
+    }
+    int acc[NR][6];
+#pragma unroll
+    for (int r = 0; r < NR; ++r)
+#pragma unroll
+        for (int k = 0; k < 6; ++k) acc[r][k] = 0;
+#pragma unroll
+    for (int t = 0; t < 8; ++t) {
+#pragma unroll
+        for (int r = 0; r < NR; ++r) {
+            const uint32_t h = Hb[r][t];
+            const uint32_t ql = (W[r][t] & 0x0F0F0F0Fu) | (__funnelshift_l(h, h, rot_lo) & 0x10101010u);
+            const uint32_t qh = ((W[r][t] >> 4) & 0x0F0F0F0Fu) | (__funnelshift_l(h, h, rot_hi) & 0x10101010u);
+            acc[r][0] = dp4a_uu(ql, s.lo[0][t], acc[r][0]);
+            acc[r][1] = dp4a_uu(ql, s.lo[1][t], acc[r][1]);
+            acc[r][2] = dp4a_us(ql, s.lo[2][t], acc[r][2]);
+            acc[r][3] = dp4a_uu(qh, s.hi[0][t], acc[r][3]);
+            acc[r][4] = dp4a_uu(qh, s.hi[1][t], acc[r][4]);
+            acc[r][5] = dp4a_us(qh, s.hi[2][t], acc[r][5]);
+        }
+    }
+#pragma unroll
+    for (int r = 0; r < NR; ++r) {
+        const float flo = combine3(acc[r][0], acc[r][1], acc[r][2]);
+        const float fhi = combine3(acc[r][3], acc[r][4], acc[r][5]);
+        const uint32_t scw = (c < 2) ? (hd[r].y & 0x3F3F3F3Fu)
+                                     : ((hd[r].w & 0x0F0F0F0Fu) | ((hd[r].y >> 2) & 0x30303030u));
+        const uint32_t mnw = (c < 2) ? (hd[r].z & 0x3F3F3F3Fu)
+                                     : (((hd[r].w >> 4) & 0x0F0F0F0Fu) | ((hd[r].z >> 2) & 0x30303030u));
+        const float d = h2f(hd[r].x), dmin = h2f(hd[r].x >> 16);
+        const float dot = fmaf(byte_to_f(scw, sel_lo), flo, byte_to_f(scw, sel_hi) * fhi);
+        const float msum = fmaf(byte_to_f(mnw, sel_lo), s.s_lo, byte_to_f(mnw, sel_hi) * s.s_hi);
+        out[r] = fmaf(d * s.inv, dot, -(dmin * msum));
+    }
+}
+
 // Code-field loads.  kAlign: the field is 4-byte aligned.  kRotated: the
 // field sits 2 bytes past a word boundary and the thread's input slice is
 // rotated to match (convert_quarter): word 0 = (bytes 14,15,0,1), words 1..3 =
@@ -498,7 +556,7 @@ __device__ __forceinline__ float warps_sum(float v, float* red, int nwarps) {
 template <int QT, int NMAT, int EPI, int XS>
 __global__ void __launch_bounds__(512, 1) mv1_kernel(const Mv1Args p) {
     extern __shared__ __align__(128) uint8_t smem[];
-    constexpr int kBlk = (QT == MUSER_Q4_K) ? kQ4KBytes : kQ6KBytes;
+    constexpr int kBlk = kBlockBytes<QT>;
     const int nsb = p.nsb;
     const int nbc = nsb * 4;
     const int G = p.G, RS = p.RS, NS = p.ns;
@@ -727,7 +785,7 @@ __global__ void __launch_bounds__(512, 1) mv1_kernel(const Mv1Args p) {
         if (!active) b = c = 0;
         const int bc = b * 4 + c;  // partial slot of this slice
         pdl_launch_dependents();
-        using Slice = typename std::conditional<QT == MUSER_Q4_K, SliceQ4, SliceQ6>::type;
+        using Slice = typename std::conditional<QT != MUSER_Q6_K, SliceQ4, SliceQ6>::type;
         Slice sl;
         // Every block reads all of x: block b starts its loads at float4 number
         // b * n4 / grid (then wraps), so the blocks do not all ask for the
@@ -799,7 +857,7 @@ __global__ void __launch_bounds__(512, 1) mv1_kernel(const Mv1Args p) {
                     const int i = xi(j);
                     const float4 xv = make_float4((rv[u].x * inv2) * bv[u].x, (rv[u].y * inv2) * bv[u].y,
                                                   (rv[u].z * inv2) * bv[u].z, (rv[u].w * inv2) * bv[u].w);
-                    sts_float4(xslots + xslot_offset(i, QT == MUSER_Q4_K, parity_split, p.HP), xv);
+                    sts_float4(xslots + xslot_offset(i, QT != MUSER_Q6_K, parity_split, p.HP), xv);
                     if (blockIdx.x == 0) {
                         reinterpret_cast<float4*>(p.resid)[i] = rv[u];
                         if (p.out) reinterpret_cast<float4*>(p.out)[i] = xv;
@@ -817,7 +875,7 @@ __global__ void __launch_bounds__(512, 1) mv1_kernel(const Mv1Args p) {
             for (int u = 0; u < 16; ++u)
                 if (tid + u * nthr < n4) {
                     const int i = xi(tid + u * nthr);
-                    cp_async16(xslots + xslot_offset(i, QT == MUSER_Q4_K, parity_split, p.HP), x4 + i);
+                    cp_async16(xslots + xslot_offset(i, QT != MUSER_Q6_K, parity_split, p.HP), x4 + i);
                 }
             cp_async_commit();
             __syncwarp();
@@ -825,7 +883,7 @@ __global__ void __launch_bounds__(512, 1) mv1_kernel(const Mv1Args p) {
             cp_async_wait_all();
         }
         named_barrier_sync(1, ncw * 32);  // the consumer warps only
-        if (QT == MUSER_Q4_K || G > 1) {
+        if (QT != MUSER_Q6_K || G > 1) {
             // Every slot converted once, a quarter per thread (the row groups
             // share the slots), then each thread loads its own slot's record.
             for (int q0 = 0; q0 < 4 * p.TG; q0 += nthr) {
@@ -856,6 +914,7 @@ __global__ void __launch_bounds__(512, 1) mv1_kernel(const Mv1Args p) {
             auto dots = [&](auto nr_tag, const uint8_t* const* blk, float* out) {
                 constexpr int NR = decltype(nr_tag)::value;
                 if constexpr (QT == MUSER_Q4_K) dot_q4<NR>(sl, blk, c, sel_lo, sel_hi, out);
+                else if constexpr (QT == MUSER_Q5_K) dot_q5<NR>(sl, blk, c, sel_lo, sel_hi, out);
                 else dot_q6<NR, kAl ? kAlign : kRotated>(sl, blk, c, sel_sc, out);
             };
             using One = std::integral_constant<int, 1>;
@@ -894,6 +953,8 @@ __global__ void __launch_bounds__(512, 1) mv1_kernel(const Mv1Args p) {
                     float v[1];
                     if constexpr (QT == MUSER_Q4_K) {
                         dot_q4<1>(sl, blk, c, sel_lo, sel_hi, v);
+                    } else if constexpr (QT == MUSER_Q5_K) {
+                        dot_q5<1>(sl, blk, c, sel_lo, sel_hi, v);
                     } else {
                         if ((reinterpret_cast<uintptr_t>(blk[0]) & 2) == 0) dot_q6<1, kAlign>(sl, blk, c, sel_sc, v);
                         else dot_q6<1, kRealign>(sl, blk, c, sel_sc, v);
@@ -928,7 +989,7 @@ __global__ void __launch_bounds__(512, 1) mv1_kernel(const Mv1Args p) {
 #pragma unroll
                 for (int m = 0; m < NMAT; ++m) sb[m] = sbase[m] + buf * buf_stride + delta[m];
                 if (QT == MUSER_Q6_K && !rows4) stage_any(sb, rows_here, pk);
-                else if (QT == MUSER_Q4_K || aligned) stage(std::true_type{}, sb, rows_here, pk);
+                else if (QT != MUSER_Q6_K || aligned) stage(std::true_type{}, sb, rows_here, pk);
                 else stage(std::false_type{}, sb, rows_here, pk);
             }
             __syncwarp();
@@ -1045,7 +1106,7 @@ bool mv1_tail_prologue_supported(int qtype, int64_t cols) {
 
 template <int QT, int NMAT, int EPI, int XS>
 static int launch_mv1_t(Mv1Args a, cudaStream_t stream) {
-    constexpr int kBlk = (QT == MUSER_Q4_K) ? kQ4KBytes : kQ6KBytes;
+    constexpr int kBlk = kBlockBytes<QT>;
     const int nbc = a.nsb * 4;
     const int64_t rowbytes = static_cast<int64_t>(a.nsb) * kBlk;
     const int sms = sm_count();
@@ -1131,6 +1192,8 @@ int launch_mv1(int qtype, int nmat, int epi, const Mv1Args& a, cudaStream_t s, i
         if (nmat == 1 && epi == kEpiTail) return launch_mv1_t<MUSER_Q4_K, 1, kEpiTail, kXMemory>(a, s);
         if (nmat == 2 && epi == kEpiSiluMul) return launch_mv1_t<MUSER_Q4_K, 2, kEpiSiluMul, kXMemory>(a, s);
         if (nmat == 1 && epi == kEpiSoftcap) return launch_mv1_t<MUSER_Q4_K, 1, kEpiSoftcap, kXMemory>(a, s);
+    } else if (qtype == MUSER_Q5_K) {
+        if (nmat == 1 && epi == kEpiStore) return launch_mv1_t<MUSER_Q5_K, 1, kEpiStore, kXMemory>(a, s);
     } else if (qtype == MUSER_Q6_K) {
         if (nmat == 1 && epi == kEpiStore) return launch_mv1_t<MUSER_Q6_K, 1, kEpiStore, kXMemory>(a, s);
         if (nmat == 1 && epi == kEpiTail) return launch_mv1_t<MUSER_Q6_K, 1, kEpiTail, kXMemory>(a, s);

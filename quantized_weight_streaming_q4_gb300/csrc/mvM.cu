@@ -64,6 +64,43 @@ __device__ __forceinline__ void decode_slot_q4(const uint8_t* blk, int j8, float
     }
 }
 
+// Q5_K: slot j8 = sub-block j8, as Q4_K, with the codes at byte 48 and the
+// fifth code bit of weight l at bit 2*(j8 >> 1) + (j8 & 1) of qh[l] (byte 16 + l).
+__device__ __forceinline__ void decode_slot_q5(const uint8_t* blk, int j8, float w[32]) {
+    const uint4 hd = ldg_stream16(blk);
+    const int c = j8 >> 1;
+    const uint4 ha = ldg_stream16(blk + 16);
+    const uint4 hb = ldg_stream16(blk + 32);
+    const uint4 qa = ldg_stream16(blk + 48 + 32 * c);
+    const uint4 qb = ldg_stream16(blk + 64 + 32 * c);
+    const uint32_t s0 = hd.y, s1 = hd.z, s2 = hd.w;
+    uint32_t sc, mn;
+    if (j8 < 4) {
+        sc = (s0 >> (8 * j8)) & 63u;
+        mn = (s1 >> (8 * j8)) & 63u;
+    } else {
+        const int jj = j8 - 4;
+        sc = ((s2 >> (8 * jj)) & 0x0Fu) | (((s0 >> (8 * jj + 6)) & 3u) << 4);
+        mn = ((s2 >> (8 * jj + 4)) & 0x0Fu) | (((s1 >> (8 * jj + 6)) & 3u) << 4);
+    }
+    const float d = h2f(hd.x), dmin = h2f(hd.x >> 16);
+    const float dsc = __fmul_rn(d, static_cast<float>(sc));   // exact (<= 17 bits)
+    const float ndm = -__fmul_rn(dmin, static_cast<float>(mn));
+    const uint32_t words[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
+    const uint32_t hbits[8] = {ha.x, ha.y, ha.z, ha.w, hb.x, hb.y, hb.z, hb.w};
+    const int sh = (j8 & 1) ? 4 : 0;
+    const int hsh = 2 * c + (j8 & 1);
+#pragma unroll
+    for (int t = 0; t < 8; ++t) {
+        const uint32_t q5 = ((words[t] >> sh) & 0x0F0F0F0Fu) | (((hbits[t] >> hsh) & 0x01010101u) << 4);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float q = byte_to_f(q5, 0x7540u | e);
+            w[4 * t + e] = __fmaf_rn(dsc, q, ndm);  // d*sc*q - dmin*m, one rounding
+        }
+    }
+}
+
 // Q6_K: slot j8 = (h, g) = (j8 >> 2, j8 & 3): weights 128h + 32g + l.
 __device__ __forceinline__ void decode_slot_q6(const uint8_t* blk, int j8, float w[32]) {
     const int h = j8 >> 2, g = j8 & 3;
@@ -123,7 +160,7 @@ __device__ __forceinline__ void load_tile(float* xs, const float* x, int M, int6
 template <int QT, int NMAT, int MB, int EPI>
 __global__ void __launch_bounds__(kThreadsM) mvM_kernel(const MvMArgs p) {
     using T = Tile<MB>;
-    constexpr int kBlk = (QT == MUSER_Q4_K) ? kQ4KBytes : kQ6KBytes;
+    constexpr int kBlk = kBlockBytes<QT>;
     constexpr int kRowsPerCta = (NMAT == 1) ? 64 : 32;
     __shared__ __align__(16) float xs[2][T::kFloats];
 
@@ -165,6 +202,7 @@ __global__ void __launch_bounds__(kThreadsM) mvM_kernel(const MvMArgs p) {
             const uint8_t* blk = p.W[mat[r]] + row[r] * rowbytes + static_cast<int64_t>(b) * kBlk;
             float w[32];
             if constexpr (QT == MUSER_Q4_K) decode_slot_q4(blk, j8, w);
+            else if constexpr (QT == MUSER_Q5_K) decode_slot_q5(blk, j8, w);
             else decode_slot_q6(blk, j8, w);
 #pragma unroll
             for (int l = 0; l < 32; ++l) {
@@ -244,6 +282,8 @@ int launch_mvM(int qtype, int nmat, int epi, const MvMArgs& a, cudaStream_t s) {
         if (nmat == 1 && epi == kEpiStore) return launch_mb<MUSER_Q4_K, 1, kEpiStore>(a, s);
         if (nmat == 2 && epi == kEpiSiluMul) return launch_mb<MUSER_Q4_K, 2, kEpiSiluMul>(a, s);
         if (nmat == 2 && epi == kEpiStore) return launch_mb<MUSER_Q4_K, 2, kEpiStore>(a, s);
+    } else if (qtype == MUSER_Q5_K) {
+        if (nmat == 1 && epi == kEpiStore) return launch_mb<MUSER_Q5_K, 1, kEpiStore>(a, s);
     } else if (qtype == MUSER_Q6_K) {
         if (nmat == 1 && epi == kEpiStore) return launch_mb<MUSER_Q6_K, 1, kEpiStore>(a, s);
         if (nmat == 2 && epi == kEpiSiluMul) return launch_mb<MUSER_Q6_K, 2, kEpiSiluMul>(a, s);

@@ -41,6 +41,8 @@ def test_every_declared_symbol_is_exported(L):
 def test_sizes_and_version(L):
     assert mu.muser_version() == 1
     assert mu.muser_block_bytes("q4_k") == 144 and mu.muser_block_bytes("q6_k") == 210
+    assert mu.muser_block_bytes("q5_k") == 176 and mu.muser_block_bytes(13) == 176
+    assert mu.muser_matrix_bytes("q5_k", 6656, 19968) == 6656 * 78 * 176
     assert mu.muser_block_bytes(7) == 0
     assert mu.muser_matrix_bytes("q4_k", 6656, 19968) == 74760192
     assert mu.muser_matrix_bytes("q6_k", 6656, 19968) == 109025280
@@ -82,6 +84,18 @@ def test_tail_and_fused_reject_bad_arguments(L):
 
 
 @needs_nvcc
+def test_q5k_only_where_supported(L):
+    # Q5_K is taken by the plain matvec and dequantisation; the FFN, tail,
+    # group and LM-head calls reject it before any launch
+    assert L.muser_qmatvec(13, FAKE + 4, 8, 256, FAKE, 1, FAKE, None) == -3   # passes the type check
+    assert L.muser_ffn_gate_up_silu(13, FAKE, FAKE, 256, 256, FAKE, 1, FAKE, None) == -2
+    rc = L.muser_qmatvec_residual_dual_rmsnorm(13, FAKE, 256, 256, FAKE, 1, FAKE, FAKE + 4096, FAKE + 8192,
+                                               FAKE, FAKE, 1e-8, 1e-5, FAKE, 1024, None)
+    assert rc == -2 and "Q5_K" not in mu.muser_last_error().split("(")[1]
+    assert L.muser_lm_head(13, FAKE, 512, 256, FAKE, 1, FAKE, 0.2, 20.0, None) == -2
+
+
+@needs_nvcc
 def test_stack_rejects_bad_layers(L):
     layer = mu.FfnLayer(FAKE, FAKE, FAKE + 4, FAKE, FAKE, 12, 14)   # misaligned down matrix
     arr = (mu.FfnLayer * 1)(layer)
@@ -111,6 +125,29 @@ def test_kv_ring_discontinuity_fails_closed_without_touching_the_plane(L):
     # inconsistent metadata is rejected
     bad_plane = mu.KvPlane(FAKE, FAKE, 32, 40, 0, 0, 256, 128, 0, 0)
     assert L.muser_kv_ring_write(ctypes.byref(bad_plane), FAKE, FAKE, 40, 1, None, None) == -1
+
+
+@needs_nvcc
+def test_kv_snapshot_and_restore_fail_closed(L):
+    plane = mu.KvPlane(FAKE, FAKE * 2, 2048, 2048, 5000, 904, 256, 128, 1, 0)
+    # rows outside the live window 5000..7047
+    for first, count in ((4999, 1), (5000, 2049), (7047, 2), (7048, 1), (6000, -1)):
+        rc = L.muser_kv_snapshot(ctypes.byref(plane), first, count, FAKE, FAKE, None)
+        assert rc == -1 and "live window" in mu.muser_last_error()
+    # an empty range inside the window launches nothing
+    assert L.muser_kv_snapshot(ctypes.byref(plane), 7048, 0, None, None, None) == 0
+    for origin, n in ((-1, 1), (0, 2049), (10, -1)):
+        rc = L.muser_kv_restore(ctypes.byref(plane), FAKE, FAKE, origin, n, None)
+        assert rc == -1
+        assert (plane.len, plane.origin_logical, plane.origin_physical) == (2048, 5000, 904)
+    assert L.muser_kv_restore(ctypes.byref(plane), None, None, 0, 3, None) == -1
+    assert L.muser_kv_restore(ctypes.byref(plane), FAKE + 1, FAKE, 0, 3, None) == -3
+    assert (plane.len, plane.origin_logical, plane.origin_physical) == (2048, 5000, 904)
+    # an empty window sets only the metadata, at the rotation origin % capacity
+    assert L.muser_kv_restore(ctypes.byref(plane), None, None, 4100, 0, None) == 0
+    assert (plane.len, plane.origin_logical, plane.origin_physical) == (0, 4100, 4)
+    bad_plane = mu.KvPlane(FAKE, FAKE, 32, 40, 0, 0, 256, 128, 0, 0)
+    assert L.muser_kv_restore(ctypes.byref(bad_plane), FAKE, FAKE, 0, 1, None) == -1
 
 
 @needs_nvcc

@@ -11,7 +11,7 @@ import pytest
 import oracle
 import synth
 from tests.gpu_util import assert_close, check_canary, dev, host, nan_like
-from tests.kquant_pack import pack_q4k, pack_q6k
+from tests.kquant_pack import pack_q4k, pack_q5k, pack_q6k
 
 pytestmark = pytest.mark.gpu
 
@@ -39,7 +39,7 @@ def _qmatvec(qtype, W, rows, cols, x, canary=64):
 
 
 # ------------------------------------------------------------ dequantize
-@pytest.mark.parametrize("qtype", ["q4_k", "q6_k"])
+@pytest.mark.parametrize("qtype", ["q4_k", "q5_k", "q6_k"])
 @pytest.mark.parametrize("rows,cols", [(1, 256), (37, 768), (512, 2048), (300, 6656)])
 def test_dequantize_bit_exact(qtype, rows, cols):
     W = synth.qmatrix(qtype, rows, cols, seed=rows + cols)
@@ -68,10 +68,18 @@ def test_dequantize_extreme_blocks_bit_exact():
     out = nan_like((1, 1024))
     mu.muser_dequantize("q6_k", dev(W6), 1, 1024, out)
     assert np.array_equal(host(out).view(np.uint32), oracle.dequantize("q6_k", W6, 1, 1024).ravel().view(np.uint32))
+    blocks5 = [pack_q5k(65504.0, 2.0 ** -24, [63] * 8, [63] * 8, list(range(32)) * 8),
+               pack_q5k(2.0 ** -24, 65504.0, [63] * 8, [0] * 8, [31] * 256),
+               pack_q5k(6.1e-5, 3.0e-7, rng.integers(0, 64, 8), rng.integers(0, 64, 8), rng.integers(0, 32, 256)),
+               pack_q5k(0.0, 0.0, [5] * 8, [5] * 8, [17] * 256)]
+    W5 = np.concatenate(blocks5).reshape(1, -1)
+    out = nan_like((1, 1024))
+    mu.muser_dequantize("q5_k", dev(W5), 1, 1024, out)
+    assert np.array_equal(host(out).view(np.uint32), oracle.dequantize("q5_k", W5, 1, 1024).ravel().view(np.uint32))
 
 
 # ---------------------------------------------------------------- matvec
-@pytest.mark.parametrize("qtype", ["q4_k", "q6_k"])
+@pytest.mark.parametrize("qtype", ["q4_k", "q5_k", "q6_k"])
 @pytest.mark.parametrize("rows,cols", [(512, 2048), (37, 768), (5, 256), (1, 512), (997, 6656),
                                        (300, 19968)])
 def test_qmatvec_m1(qtype, rows, cols):
@@ -82,7 +90,19 @@ def test_qmatvec_m1(qtype, rows, cols):
     assert_close(got, ref, f"{qtype} {rows}x{cols} M=1", scaled=True)
 
 
-@pytest.mark.parametrize("qtype", ["q4_k", "q6_k"])
+def test_qmatvec_q5k_full_shape_sampled_rows():
+    # the bench's Q5_K launch: a 6656 x 19968 matrix at M = 1, every 23rd row
+    # and the last one against the oracle
+    rows, cols = 6656, 19968
+    W = synth.q5k_matrix(rows, cols, seed=0, workload=3, layer=0)
+    x = synth.normal((1, cols), seed=0, workload=3, tensor=synth.T_X)
+    got = _qmatvec("q5_k", W, rows, cols, x)
+    ridx = np.array(list(range(0, rows, 23)) + [rows - 1], np.int64)
+    ref = oracle.qmatvec_rows("q5_k", W, rows, cols, ridx, x)
+    assert_close(got[:, ridx], ref, "q5_k 6656x19968 sampled rows", scaled=True)
+
+
+@pytest.mark.parametrize("qtype", ["q4_k", "q5_k", "q6_k"])
 @pytest.mark.parametrize("M", [2, 3, 5, 8, 16])
 @pytest.mark.parametrize("rows,cols", [(100, 768), (37, 2048)])
 def test_qmatvec_multirow(qtype, M, rows, cols):
@@ -93,7 +113,7 @@ def test_qmatvec_multirow(qtype, M, rows, cols):
     assert_close(got, ref, f"{qtype} {rows}x{cols} M={M}", scaled=True)
 
 
-@pytest.mark.parametrize("qtype", ["q4_k", "q6_k"])
+@pytest.mark.parametrize("qtype", ["q4_k", "q5_k", "q6_k"])
 def test_qmatvec_one_hot_columns_bit_exact(qtype):
     # x = e_j picks column j of the dequantised matrix exactly (one product by
     # 1.0, every other term an exact zero), so every code and scale position
@@ -293,6 +313,94 @@ def test_kv_ring_discontinuity_leaves_planes_untouched():
     after = (host(key), host(val), plane.len, plane.origin_logical, plane.origin_physical)
     assert np.array_equal(before[0], after[0]) and np.array_equal(before[1], after[1])
     assert before[2:] == after[2:]
+
+
+def _u16(t):
+    return host(t).view(np.uint16)
+
+
+def _rows_buf(n, kv_dim, offset=0, canary=24):
+    """int16 device rows [n*kv_dim] starting `offset` halves into a buffer, canaries after."""
+    buf = torch.full((offset + n * kv_dim + canary,), 0x7777, dtype=torch.int16, device="cuda")
+    return buf, buf[offset:offset + n * kv_dim]
+
+
+def _check_rows_canary(buf, offset, n, kv_dim):
+    b = host(buf)
+    assert np.all(b[:offset] == 0x7777) and np.all(b[offset + n * kv_dim:] == 0x7777)
+
+
+@pytest.mark.parametrize("head_major", [False, True])
+@pytest.mark.parametrize("cap,kv_dim,head_dim,offset", [(2048, 256, 128, 0), (37, 256, 128, 0),
+                                                       (37, 256, 128, 1), (29, 6, 3, 0)])
+def test_kv_snapshot_and_restore_bit_exact(head_major, cap, kv_dim, head_dim, offset):
+    key, val, plane, ring, okey, oval = _plane_pair(cap, kv_dim, head_dim, head_major)
+    pos = 0
+    for step, count in enumerate([5, cap - 2, 3, cap // 3 + 1]):   # wraps, origins not 0
+        k, v = synth.kv_rows(count, kv_dim, seed=40 + step, step=step)
+        mu.muser_kv_ring_write(plane, dev(k), dev(v), pos, count)
+        assert oracle.kv_write(ring, okey, oval, kv_dim, head_dim, head_major, k, v, pos)[0] == 0
+        pos += count
+    assert np.array_equal(_u16(key), okey) and plane.origin_logical == ring.origin_logical > 0
+    o0, n = plane.origin_logical, plane.len
+    # the whole window, and a sub-range that crosses the physical end of the plane
+    split = (cap - plane.origin_physical) - 2
+    for first, count in [(o0, n), (o0 + split, min(7, n - split)), (o0 + n - 1, 1)]:
+        kb, kr = _rows_buf(count, kv_dim, offset)
+        vb, vr = _rows_buf(count, kv_dim, offset)
+        mu.muser_kv_snapshot(plane, first, count, kr, vr)
+        rc, ok, ov = oracle.kv_snapshot(ring, okey, oval, kv_dim, head_dim, head_major, first, count)
+        assert rc == 0
+        assert np.array_equal(_u16(kr).reshape(count, kv_dim), ok)
+        assert np.array_equal(_u16(vr).reshape(count, kv_dim), ov)
+        _check_rows_canary(kb, offset, count, kv_dim)
+        _check_rows_canary(vb, offset, count, kv_dim)
+    # restore the whole window into a fresh plane pair, at its own origin and at another one
+    kb, kr = _rows_buf(n, kv_dim, offset)
+    vb, vr = _rows_buf(n, kv_dim, offset)
+    mu.muser_kv_snapshot(plane, o0, n, kr, vr)
+    _, ok, ov = oracle.kv_snapshot(ring, okey, oval, kv_dim, head_dim, head_major, o0, n)
+    for origin in (o0, o0 + 5 * cap + 3, 0):
+        key2 = torch.full((cap * kv_dim,), 0x3C3C, dtype=torch.int16, device="cuda")
+        val2 = key2.clone()
+        plane2 = mu.KvPlane(key2.data_ptr(), val2.data_ptr(), cap, 1, 9, 9, kv_dim, head_dim,
+                            1 if head_major else 0, 0)
+        ring2 = oracle.Ring(cap, 1, 9, 9)
+        okey2 = np.full(cap * kv_dim, 0x3C3C, np.uint16)
+        oval2 = okey2.copy()
+        mu.muser_kv_restore(plane2, kr, vr, origin, n)
+        assert oracle.kv_restore(ring2, okey2, oval2, kv_dim, head_dim, head_major, ok, ov, origin) == 0
+        assert (plane2.len, plane2.origin_logical, plane2.origin_physical) == (
+            ring2.len, ring2.origin_logical, ring2.origin_physical) == (n, origin, origin % cap)
+        assert np.array_equal(_u16(key2), okey2) and np.array_equal(_u16(val2), oval2)
+        if origin == o0:
+            # restored at its own origin, the pair is the live one, slot for slot
+            assert np.array_equal(okey2, okey) and np.array_equal(oval2, oval)
+            # and it keeps appending as the live ring does
+            k, v = synth.kv_rows(4, kv_dim, seed=77)
+            mu.muser_kv_ring_write(plane2, dev(k), dev(v), o0 + n, 4)
+            mu.muser_kv_ring_write(plane, dev(k), dev(v), o0 + n, 4)
+            assert np.array_equal(_u16(key2), _u16(key)) and np.array_equal(_u16(val2), _u16(val))
+            assert (plane2.len, plane2.origin_logical, plane2.origin_physical) == (
+                plane.len, plane.origin_logical, plane.origin_physical)
+
+
+def test_kv_snapshot_and_restore_reject_without_writing():
+    key, val, plane, ring, okey, oval = _plane_pair(32, 256, 128, True)
+    k, v = synth.kv_rows(40, 256, seed=5)
+    mu.muser_kv_ring_write(plane, dev(k), dev(v), 0, 40)
+    kb, kr = _rows_buf(4, 256)
+    vb, vr = _rows_buf(4, 256)
+    for first in (7, 37, 100):
+        with pytest.raises(mu.MuserError) as ei:
+            mu.muser_kv_snapshot(plane, first, 4, kr, vr)
+        assert ei.value.status == -1
+    _check_rows_canary(kb, 0, 0, 256)
+    before = (_u16(key).copy(), plane.len, plane.origin_logical, plane.origin_physical)
+    with pytest.raises(mu.MuserError):
+        mu.muser_kv_restore(plane, kr, vr, 0, 33)
+    assert np.array_equal(_u16(key), before[0])
+    assert (plane.len, plane.origin_logical, plane.origin_physical) == before[1:]
 
 
 # ----------------------------------------------------------------- sync
