@@ -478,7 +478,9 @@ def run_attn(args, rank, world):
     layers (Ch 10 Figure 10.1 boxes 4, 9, 10): per layer the Q, K, V and gate
     projections as one group (muser_qmatvec_group; from layer 1 with the
     previous layer's post-attention tail fused in, muser_qmatvec_group_tail),
-    then o_proj (muser_qmatvec); the last tail once per step.  The tail's
+    then o_proj (muser_qmatvec); the last tail once per step.  With 16 rows
+    of x each projection is a muser_qmatvec_scratch call (the tensor-core
+    kernel split over every SM) after the stand-alone tail.  The tail's
     output (the FFN input in the model) stands in for the next layer's normed
     input.  Attention itself is outside the path: o_proj reads a seeded
     stand-in for its output."""
@@ -519,6 +521,13 @@ def run_attn(args, rank, world):
     rows4 = (ctypes.c_int64 * 4)(QD, KVD, KVD, QD)
     ys4 = (ctypes.c_void_p * 4)(q.data_ptr(), k.data_ptr(), v.data_ptr(), g.data_ptr())
     w4 = [(ctypes.c_void_p * 4)(*[d[n].data_ptr() for n in ("Wq", "Wk", "Wv", "Wg")]) for d in layers]
+    nscr = max(mu.muser_qmatvec_scratch_bytes(12, r, c, M) for r, c in ((QD, H), (KVD, H), (H, QD)))
+    scratch = torch.zeros(max(nscr, 16) // 4 + 64, dtype=torch.float32, device="cuda")
+    outs4 = (q, k, v, g)
+
+    def split_mv(W, rows, cols, xin, y):
+        rc("qmatvec_scratch", L.muser_qmatvec_scratch(12, W.data_ptr(), rows, cols, xin.data_ptr(), M, y.data_ptr(),
+                                                      scratch.data_ptr(), nscr, sh))
 
     def step(events=None):
         rc("rms_norm", L.muser_rms_norm(resid.data_ptr(), w_in.data_ptr(), x.data_ptr(), H, M, 1e-5, sh))
@@ -527,7 +536,14 @@ def run_attn(args, rank, world):
             ev = events.get(l) if events is not None else None
             if ev is not None:
                 ev[0].record(stream)
-            if prev is None:
+            if M > 1:
+                if prev is not None:
+                    rc("tail", L.muser_fused_residual_dual_rmsnorm(
+                        resid.data_ptr(), proj.data_ptr(), x.data_ptr(), prev["w_post"].data_ptr(),
+                        prev["w_ffn"].data_ptr(), H, M, 1e-8, 1e-5, sh))
+                for n, r, y in zip(("Wq", "Wk", "Wv", "Wg"), (QD, KVD, KVD, QD), outs4):
+                    split_mv(d[n], r, H, x, y)
+            elif prev is None:
                 rc("qkvg", L.muser_qmatvec_group(12, 4, w4[l], rows4, H, x.data_ptr(), M, ys4, sh))
             else:
                 rc("qkvg_tail", L.muser_qmatvec_group_tail(
@@ -535,7 +551,11 @@ def run_attn(args, rank, world):
                     prev["w_ffn"].data_ptr(), 1e-8, 1e-5, x.data_ptr(), M, ys4, sh))
             if ev is not None:
                 ev[1].record(stream)
-            rc("o_proj", L.muser_qmatvec(12, d["Wo"].data_ptr(), H, QD, attn.data_ptr(), M, proj.data_ptr(), sh))
+            if M > 1:
+                split_mv(d["Wo"], H, QD, attn, proj)
+            else:
+                rc("o_proj", L.muser_qmatvec(12, d["Wo"].data_ptr(), H, QD, attn.data_ptr(), M, proj.data_ptr(),
+                                             sh))
             if ev is not None:
                 ev[2].record(stream)
             prev = d
@@ -617,18 +637,23 @@ def run_attn(args, rank, world):
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "tokens_per_s": round(world * M / (ms * 1e-3), 3),
         "hbm_frac_of_" + peak_kind: round(gbs / world / peak, 4),
-        "roofline": {"bound": "hbm", "kernel": f"muser_qmatvec_group_tail (Q, K, V, gate Q4_K with the previous "
-                                               f"tail, M={M}; one launch at M = 1)",
+        "roofline": {"bound": "hbm", "kernel": ("muser_qmatvec_group_tail (Q, K, V, gate Q4_K with the previous "
+                                                "tail: one launch)" if M == 1 else
+                                                f"the previous tail, then Q, K, V, gate by muser_qmatvec_scratch "
+                                                f"(tensor cores split over the SMs), M={M}"),
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "traffic": None, "algorithmic_bytes_per_launch": q_bytes, "mean_launch_us": round(q_ms * 1e3, 2),
-                     "second_kernel": {"name": "muser_qmatvec (o_proj)",
+                     "second_kernel": {"name": "muser_qmatvec (o_proj)" if M == 1 else
+                                               "muser_qmatvec_scratch (o_proj)",
                                        "achieved_gbs": round(o_bytes / (o_ms * 1e-3) / 1e9, 1),
                                        "mean_launch_us": round(o_ms * 1e3, 2),
                                        "algorithmic_bytes_per_launch": o_bytes}},
         "e2e": {"value": round(world * weight_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
                 "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": 4 * M * H, "d2h_bytes_per_step": 4 * M * H,
-                "api": "per-layer muser_qmatvec_group[_tail] / muser_qmatvec calls, host residual in, x out"},
-        "gpu_launches": args.steps * (2 + 2 * nl) if M == 1 else None,
+                "api": ("per-layer muser_qmatvec_group[_tail] / muser_qmatvec calls" if M == 1 else
+                        "per-layer muser_fused_residual_dual_rmsnorm and muser_qmatvec_scratch calls") +
+                       ", host residual in, x out"},
+        "gpu_launches": args.steps * ((2 + 2 * nl) if M == 1 else (1 + 6 * nl)),
         "clocks": clock, "device_status": mu.muser_device_status(), "weights_generation_s": round(gen_s, 1),
     }
 

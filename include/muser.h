@@ -100,6 +100,26 @@ int muser_dequantize(int qtype, const void* W, int64_t rows, int64_t cols, float
 int muser_qmatvec(int qtype, const void* W, int64_t rows, int64_t cols, const float* x, int M,
                   float* y, void* stream);
 
+/* Scratch bytes muser_qmatvec_scratch needs (0: the call needs none, as for
+ * one row of x and for shapes the tensor-core kernel does not take). */
+size_t muser_qmatvec_scratch_bytes(int qtype, int64_t rows, int64_t cols, int M);
+
+/*
+ * muser_qmatvec_scratch -- the same result as muser_qmatvec.  With 2..16 rows
+ *   of x and caller scratch the tensor-core kernel spreads the (row tile,
+ *   super-block) units of the matrix evenly over the SMs and sums a tile's
+ *   parts in a fixed order; without it each SM takes whole 128-row tiles,
+ *   which leaves most SMs idle on matrices of few tiles (the attention-side
+ *   projections of the book's model are 2 to 52 tiles).
+ *   scratch: device memory of at least muser_qmatvec_scratch_bytes(...)
+ *   bytes, 16-byte aligned, owned by the caller, zero-filled before its first
+ *   use; every successful call leaves it zero-filled again.  Calls that can
+ *   run at the same time must not share it.  When the size is 0, scratch is
+ *   not used and may be NULL.  Other arguments as muser_qmatvec.
+ */
+int muser_qmatvec_scratch(int qtype, const void* W, int64_t rows, int64_t cols, const float* x, int M,
+                          float* y, void* scratch, size_t scratch_bytes, void* stream);
+
 /*
  * muser_rms_norm -- out[m*n+i] = w[i] * x[m*n+i] / sqrt(mean_i(x[m*n+i]^2) + eps)
  *   (Ch 2 §2.6 rms_norm_batch; the layer-0 input norm of Ch 10 Figure 10.1).

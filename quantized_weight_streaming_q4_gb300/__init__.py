@@ -20,6 +20,7 @@ __all__ = [
     "muser_version", "muser_last_error", "muser_block_bytes", "muser_matrix_bytes",
     "muser_dequantize", "muser_qmatvec", "muser_rms_norm", "muser_silu_mul",
     "muser_ffn_gate_up_silu", "muser_gate_up_scratch_bytes", "muser_ffn_gate_up_silu_scratch",
+    "muser_qmatvec_scratch_bytes", "muser_qmatvec_scratch",
     "muser_ffn_gate_up_silu_tail", "muser_qmatvec_group", "muser_qmatvec_group_tail", "muser_scale_softcap",
     "muser_lm_head",
     "muser_fused_residual_dual_rmsnorm", "muser_scratch_bytes",
@@ -92,6 +93,8 @@ def lib():
             "muser_matrix_bytes": (SZ, [I, I64, I64]),
             "muser_dequantize": (I, [I, P, I64, I64, P, P]),
             "muser_qmatvec": (I, [I, P, I64, I64, P, I, P, P]),
+            "muser_qmatvec_scratch_bytes": (SZ, [I, I64, I64, I]),
+            "muser_qmatvec_scratch": (I, [I, P, I64, I64, P, I, P, P, SZ, P]),
             "muser_rms_norm": (I, [P, P, P, I, I, F, P]),
             "muser_silu_mul": (I, [P, P, P, I64, P]),
             "muser_ffn_gate_up_silu": (I, [I, P, P, I64, I64, P, I, P, P]),
@@ -183,6 +186,17 @@ def muser_dequantize(qtype, W, rows: int, cols: int, out, stream=None) -> None:
 def muser_qmatvec(qtype, W, rows: int, cols: int, x, M: int, y, stream=None) -> None:
     _check("muser_qmatvec", lib().muser_qmatvec(_qt(qtype), _ptr(W), rows, cols, _ptr(x), M,
                                                 _ptr(y), _stream(stream)))
+
+
+def muser_qmatvec_scratch_bytes(qtype, rows: int, cols: int, M: int) -> int:
+    return lib().muser_qmatvec_scratch_bytes(_qt(qtype), rows, cols, M)
+
+
+def muser_qmatvec_scratch(qtype, W, rows: int, cols: int, x, M: int, y, scratch, scratch_bytes: int,
+                          stream=None) -> None:
+    _check("muser_qmatvec_scratch",
+           lib().muser_qmatvec_scratch(_qt(qtype), _ptr(W), rows, cols, _ptr(x), M, _ptr(y), _ptr(scratch),
+                                       scratch_bytes, _stream(stream)))
 
 
 def muser_rms_norm(x, w, out, n: int, M: int, eps: float, stream=None) -> None:

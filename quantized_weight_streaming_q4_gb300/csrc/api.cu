@@ -386,6 +386,38 @@ int muser_qmatvec(int qtype, const void* W, int64_t rows, int64_t cols, const fl
     return launch_mvM(qtype, 1, kEpiStore, a, as_stream(stream));
 }
 
+size_t muser_qmatvec_scratch_bytes(int qtype, int64_t rows, int64_t cols, int M) {
+    // one row of x runs on the one-token kernel, which needs none
+    if (M < 2 || M > MUSER_MAX_M || !mvt_supported(qtype, 1, rows, cols, M)) return 0;
+    return mvt_scratch_bytes(qtype, 1, rows, cols, M);
+}
+
+int muser_qmatvec_scratch(int qtype, const void* W, int64_t rows, int64_t cols, const float* x, int M,
+                          float* y, void* scratch, size_t scratch_bytes, void* stream) {
+    clear_error();
+    const char* fn = "muser_qmatvec_scratch";
+    MUSER_TRY(check_matrix(fn, qtype, W, rows, cols, true));
+    MUSER_TRY(check_M(fn, M));
+    MUSER_TRY(check_f32(fn, "x", x));
+    MUSER_TRY(check_f32(fn, "y", y));
+    const size_t need = muser_qmatvec_scratch_bytes(qtype, rows, cols, M);
+    if (need == 0) return muser_qmatvec(qtype, W, rows, cols, x, M, y, stream);
+    MUSER_TRY(check_f32(fn, "scratch", scratch));
+    if (scratch_bytes < need)
+        return set_error(MUSER_ERR_INVALID_ARG, "%s: scratch_bytes %zu < %zu", fn, scratch_bytes, need);
+    // several rows of x: the tensor-core kernel with the (tile, super-block)
+    // units spread evenly over the SMs
+    MvtArgs t{};
+    t.W[0] = static_cast<const uint8_t*>(W);
+    t.W[1] = t.W[0];
+    t.rows = rows;
+    t.nsb = static_cast<int>(cols / kQK);
+    t.x = x;
+    t.M = M;
+    t.y = y;
+    return launch_mvt(qtype, kEpiStore, t, scratch, as_stream(stream));
+}
+
 int muser_rms_norm(const float* x, const float* w, float* out, int n, int M, float eps,
                    void* stream) {
     clear_error();

@@ -84,6 +84,16 @@ def test_tail_and_fused_reject_bad_arguments(L):
 
 
 @needs_nvcc
+def test_qmatvec_scratch_host_checks(L):
+    # one row of x needs no scratch; checks run before any size query
+    assert mu.muser_qmatvec_scratch_bytes("q4_k", 4096, 6656, 1) == 0
+    assert mu.muser_qmatvec_scratch_bytes("q4_k", 4096, 6656, 17) == 0
+    assert L.muser_qmatvec_scratch(99, FAKE, 8, 256, FAKE, 3, FAKE, FAKE, 1 << 20, None) == -2
+    assert L.muser_qmatvec_scratch(12, FAKE, 8, 256, FAKE, 0, FAKE, FAKE, 1 << 20, None) == -1
+    assert L.muser_qmatvec_scratch(12, FAKE, 8, 256, FAKE + 4, 3, FAKE, FAKE, 1 << 20, None) == -3
+
+
+@needs_nvcc
 def test_q5k_only_where_supported(L):
     # Q5_K is taken by the plain matvec and dequantisation; the FFN, tail,
     # group and LM-head calls reject it before any launch

@@ -113,6 +113,33 @@ def test_qmatvec_multirow(qtype, M, rows, cols):
     assert_close(got, ref, f"{qtype} {rows}x{cols} M={M}", scaled=True)
 
 
+@pytest.mark.parametrize("qtype,rows,cols", [("q4_k", 4096, 6656), ("q4_k", 256, 6656), ("q4_k", 6656, 4096),
+                                            ("q4_k", 1000, 2048), ("q6_k", 6656, 19968), ("q6_k", 264, 1280)])
+@pytest.mark.parametrize("M", [3, 16])
+def test_qmatvec_scratch_split(qtype, rows, cols, M):
+    # the attention-side shapes at several rows of x, split over every SM with
+    # caller scratch; rows sampled against the oracle, the scratch left zeroed
+    W = synth.qmatrix(qtype, rows, cols, seed=rows + M)
+    x = synth.normal((M, cols), seed=M + 1, tensor=synth.T_X)
+    nscr = mu.muser_qmatvec_scratch_bytes(qtype, rows, cols, M)
+    assert nscr > 0
+    scratch = torch.zeros(nscr // 4 + 64, dtype=torch.float32, device="cuda")
+    scratch[nscr // 4:] = 777.0
+    y = nan_like((M, rows), extra=64)
+    Wd, xd = dev(W), dev(x)
+    for _ in range(2):  # the second call runs on the scratch the first one left
+        mu.muser_qmatvec_scratch(qtype, Wd, rows, cols, xd, M, y, scratch, nscr)
+        got = host(y[:M * rows]).reshape(M, rows)
+        check_canary(y, M * rows)
+        ridx = np.unique(np.r_[np.arange(0, rows, max(1, rows // 200)), rows - 1])
+        ref = oracle.qmatvec_rows(qtype, W, rows, cols, ridx, x)
+        assert_close(got[:, ridx], ref, f"{qtype} {rows}x{cols} M={M} split", scaled=True)
+        sc = host(scratch)
+        assert not np.any(sc[:nscr // 4]), "scratch not left zeroed"
+        assert np.all(sc[nscr // 4:] == 777.0), "write past the scratch"
+    assert mu.muser_device_status() == 0
+
+
 @pytest.mark.parametrize("qtype", ["q4_k", "q5_k", "q6_k"])
 def test_qmatvec_one_hot_columns_bit_exact(qtype):
     # x = e_j picks column j of the dequantised matrix exactly (one product by
