@@ -479,15 +479,20 @@ __device__ __forceinline__ void dot_q6(const SliceQ6& s, const uint8_t* const* b
     for (int r = 0; r < NR; ++r) {
         const uint2 sc8 = lds_w2<kMode == kAlign>(blk[r] + 192 + 8 * h);
         const uint32_t dbits = *reinterpret_cast<const uint16_t*>(blk[r] + 208);
-        // int8 scales of sub-blocks 8h + 2g + j -> floats (offset-binary via 2^23 magic)
-        const uint32_t sc4 = __byte_perm(sc8.x, sc8.y, sel_sc) ^ 0x80808080u;
-        float sum = 0.0f;
+        // int8 scales of sub-blocks 8h + 2g + j, byte g of sc4
+        const uint32_t sc4 = __byte_perm(sc8.x, sc8.y, sel_sc);
+        // Per digit k, sum over the four sub-blocks of scale * sum((q - 32) * D_k):
+        // |sum((q - 32) * D_k)| <= 16 * 32 * 255 < 2^17 and |scale| <= 128, so
+        // the four products and their sum stay below 2^26, exact in int32.
+        int T[3] = {0, 0, 0};
 #pragma unroll
         for (int g = 0; g < 4; ++g) {
-            const float scg = byte_to_f(sc4, 0x7540u | g) - 128.0f;
-            // sum((q - 32) * X) over the sub-block
-            sum = fmaf(scg, combine3(acc[r][g][0], acc[r][g][1], acc[r][g][2]), sum);
+            const int scg = static_cast<int8_t>((sc4 >> (8 * g)) & 0xFFu);
+#pragma unroll
+            for (int k = 0; k < 3; ++k) T[k] += scg * acc[r][g][k];
         }
+        const float sum = fmaf(static_cast<float>(T[2]), 65536.0f,
+                               fmaf(static_cast<float>(T[1]), 256.0f, static_cast<float>(T[0])));
         out[r] = (h2f(dbits) * s.inv) * sum;
     }
 }
