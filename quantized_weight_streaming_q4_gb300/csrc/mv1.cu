@@ -1134,10 +1134,17 @@ static int launch_mv1_t(Mv1Args a, cudaStream_t stream) {
     if (XS == kXTail && !(nbc * 16 <= 4 * 32 * geo.ncw))
         return set_error(MUSER_ERR_UNSUPPORTED, "mv1: %d inputs exceed the fused tail's registers", nbc * 64);
     const int threads = (a.nconsumer_warps + 3) * 32;
-    // rows per stage: a multiple of G, stage near 32 KB over all matrices
+    // Rows per stage: a multiple of G, the stage near 32 KB over all matrices,
+    // or near 64 KB for Q6_K and for rows that one row group spans.  There
+    // each thread has more work per stage and the per-stage cost (barrier
+    // waits, ring bookkeeping, one bulk copy) weighs more: on GB300 the
+    // larger stages took a 202,048 x 6,656 Q6_K matvec from 202 to 174 us and
+    // the 52-layer stack from 53.2 to 51.0 us per layer.  Gate/up (four row
+    // groups, two matrices) ran slower with them.
+    const bool big = QT == MUSER_Q6_K || geo.G == 1;
     const int64_t per_row = rowbytes * NMAT;
     const int64_t unit = static_cast<int64_t>(a.G) * (NMAT == 1 ? 2 : 1);  // one matrix: rows go in pairs
-    int64_t rs = std::max<int64_t>(1, (32 * 1024) / (per_row * unit)) * unit;
+    int64_t rs = std::max<int64_t>(1, (big ? 64 * 1024 : 32 * 1024) / (per_row * unit)) * unit;
     const int64_t rows_per_cta = (a.rows + grid - 1) / grid;
     rs = std::min<int64_t>(rs, ((rows_per_cta + unit - 1) / unit) * unit);
     a.RS = static_cast<int>(rs);
@@ -1164,7 +1171,7 @@ static int launch_mv1_t(Mv1Args a, cudaStream_t stream) {
     a.x_off = a.part_off;
     const int64_t over = a.part_off + xbytes - a.stage_off;
     a.rot = over > 0 ? static_cast<int>((over + per_stage - 1) / per_stage) : 0;
-    a.lead = 2;
+    a.lead = big ? 1 : 2;
     auto kern = mv1_kernel<QT, NMAT, EPI, XS>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
