@@ -96,6 +96,8 @@ int muser_dequantize(int qtype, const void* W, int64_t rows, int64_t cols, float
  *   dequantised in registers straight from HBM; sums are binary32.
  *   W: device matrix; x: device f32 [M*cols]; y: device f32 [M*rows].
  *   1 <= M <= 16, cols % 256 == 0, rows >= 1.  x and y must not overlap.
+ *   Intermediate sums are binary32: above |x| of about 1e34 the Q4_K/Q5_K
+ *   min terms (a 32-input sum of x times a min of up to 63) can overflow.
  */
 int muser_qmatvec(int qtype, const void* W, int64_t rows, int64_t cols, const float* x, int M,
                   float* y, void* stream);

@@ -90,6 +90,47 @@ def test_qmatvec_m1(qtype, rows, cols):
     assert_close(got, ref, f"{qtype} {rows}x{cols} M=1", scaled=True)
 
 
+@pytest.mark.parametrize("qtype", ["q4_k", "q5_k", "q6_k"])
+@pytest.mark.parametrize("cols", [26624, 26880])   # the one-token kernel's widest rows, and one block more
+@pytest.mark.parametrize("M", [1, 16])
+def test_qmatvec_width_limits(qtype, cols, M):
+    rows = 37 if M == 1 else 64
+    W = synth.qmatrix(qtype, rows, cols, seed=cols + M)
+    x = synth.normal((M, cols), seed=cols, tensor=synth.T_X)
+    got = _qmatvec(qtype, W, rows, cols, x)
+    ref = oracle.qmatvec(qtype, W, rows, cols, x)
+    assert_close(got, ref, f"{qtype} {rows}x{cols} M={M}", scaled=True)
+
+
+@pytest.mark.parametrize("qtype", ["q4_k", "q5_k", "q6_k"])
+def test_qmatvec_input_dynamic_range(qtype):
+    # every 64-input slice takes its own power-of-two scale: slices 1e-30 to
+    # 1e30 apart, all-zero slices, a slice with one nonzero input, binary32
+    # subnormal inputs, and inputs of magnitude 1e30 (the kernels keep the
+    # sums of each 32-input sub-block in binary32, times a 6-bit min)
+    rows, cols = 96, 2048
+    W = synth.qmatrix(qtype, rows, cols, seed=11)
+    base = synth.normal((3, cols), seed=12, tensor=synth.T_X)
+    x = base.copy()
+    scales = np.float32(10.0) ** np.arange(-30, 32, 2, dtype=np.float32)
+    for sl in range(cols // 64):
+        x[0, 64 * sl:64 * sl + 64] *= scales[sl % scales.size]
+    x[0, 0:64] = 0.0
+    x[0, 128:192] = 0.0
+    x[0, 130] = 3.0
+    x[1] *= np.float32(1e-41)   # subnormal binary32 inputs
+    x[2] *= np.float32(2e30)
+    for m in range(3):
+        got = _qmatvec(qtype, W, rows, cols, x[m:m + 1])
+        ref = oracle.qmatvec(qtype, W, rows, cols, x[m:m + 1])
+        assert np.isfinite(got).all()
+        if m == 1:
+            # the subnormal row: only the bound's absolute part is meaningful
+            assert np.max(np.abs(got - ref)) <= 1e-30
+        else:
+            assert_close(got, ref, f"{qtype} dynamic range row {m}", scaled=True)
+
+
 def test_qmatvec_q5k_full_shape_sampled_rows():
     # the bench's Q5_K launch: a 6656 x 19968 matrix at M = 1, every 23rd row
     # and the last one against the oracle
