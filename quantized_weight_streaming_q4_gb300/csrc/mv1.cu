@@ -903,6 +903,9 @@ __global__ void __launch_bounds__(512, 1) mv1_kernel(const Mv1Args p) {
             // one row group: each slot has one thread, which converts it
             if (active) load_slice_q6(sl, reinterpret_cast<const float*>(xslots + idx * kXSlot), parity_split && (b & 1));
         }
+        // the slots' generic writes come before the bulk copies that reuse
+        // the overlaid stage buffers
+        fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(xready);
         // the slots overlay the partial slots: every slice is read first
