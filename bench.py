@@ -55,7 +55,7 @@ METRIC = "weight-stream GB/s (% of GB300 HBM peak); decode FFN tokens/sec, 1 GPU
 # ncu DRAM traffic of the dominant kernel, per launch, with the source hash it
 # was captured on (profiles/ summary); reported as null once the kernel changed.
 NCU_TRAFFIC = {"kernel": "mv1_kernel<Q4_K,2,silu,tail>", "bytes_per_launch": 152691456,
-               "source_sha256": "2d3f0626dfc93f8f1ebb03614f49515ae4f0bd2d749cfd3536b87d420d30d980",
+               "source_sha256": "2a67001274fe7c932b82811640311065d1e3047683baa036bed341cbff17a349",
                "profile": "profiles/mv1_fused_gate_up_tail_q4k_and_down_q6k_m1.md"}
 
 

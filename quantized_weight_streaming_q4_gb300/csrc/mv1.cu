@@ -1,10 +1,11 @@
-// mv1.cu -- one-token (M = 1) quantized matvec over Q4_K / Q6_K super-blocks,
+// mv1.cu -- one-token (M = 1) quantized matvec over Q4_K / Q5_K / Q6_K super-blocks,
 // the decode projection of the Muser book (Ch 19 §19.1 operation 1, §19.3,
 // §19.5), re-designed for sm_103a:
 //
 //  * Each CTA owns a contiguous range of output rows (balanced over the SMs)
 //    and streams those rows' bytes HBM -> shared memory with 1-D TMA bulk
-//    copies (cp.async.bulk + mbarrier), NS stages deep.  Q6_K's 210-byte
+//    copies (cp.async.bulk + mbarrier), NS stages of about 32 KB (64 KB for
+//    Q6_K and for rows one row group spans) deep.  Q6_K's 210-byte
 //    blocks are only 2-byte aligned, so staging whole row spans is what keeps
 //    the global traffic in 16-byte-aligned bulk transfers.
 //  * Each thread owns a fixed 64-weight slice (super-block b, chunk c) of the
@@ -12,7 +13,8 @@
 //    the three bytes of a 24-bit fixed-point copy (one power of two per
 //    slice).  Codes are masked in place, four to a 32-bit word, and dp4a
 //    adds four code * digit products per instruction into exact int32
-//    per-digit sub-block sums.  Scales are applied once per sub-block.
+//    per-digit sub-block sums.  Q4_K/Q5_K scales are applied once per
+//    sub-block; Q6_K's int8 scales are folded into the integer digit sums.
 //  * Per stage, the slice partials of every row land in shared memory and
 //    one warp per row adds them in a fixed order (deterministic results).
 //  * Epilogues: store y; scale and soft-cap logits (the LM head, Ch 10
