@@ -66,6 +66,23 @@ def _env_int(k, d):
         return d
 
 
+def max_over_ranks(value: float, dist, device="cuda") -> float:
+    """The slowest rank's figure: with a process group every rank gets the
+    maximum over ranks (an all-reduce MAX); alone, the value itself."""
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gbs(world: int, bytes_per_rank: int, ms: float) -> float:
+    """Replicas: every rank streams `bytes_per_rank` per step; the job's rate
+    is all ranks' bytes over the slowest rank's step time."""
+    return world * bytes_per_rank / (ms * 1e-3) / 1e9
+
+
 def algorithmic_bytes(M: int):
     """Per layer and per kernel: weights read + activations read/written (f32).
 
@@ -330,10 +347,7 @@ def run_native(args, rank, world):
     gu_ms = [t[0].elapsed_time(t[1]) for ev in events for t in ev.values()]
     dt_ms = [t[1].elapsed_time(t[2]) for ev in events for t in ev.values()]
     ms = total_ms / args.steps
-    if dist is not None:
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, dist)
 
     # e2e: host residual in (pinned), the public call, host output out
     h_in = torch.from_numpy(S.r0.copy()).pin_memory()
@@ -354,10 +368,7 @@ def run_native(args, rank, world):
     e1.record(S.stream)
     barrier()
     e2e_ms = e0.elapsed_time(e1) / e_steps
-    if dist is not None:
-        t = torch.tensor([e2e_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e2e_ms, dist)
     assert np.isfinite(h_out.numpy()).all()
     status = mu.muser_device_status()
 
@@ -368,7 +379,7 @@ def run_native(args, rank, world):
     traffic = None
     if M == 1 and NCU_TRAFFIC["bytes_per_launch"] and NCU_TRAFFIC["source_sha256"] == source_sha():
         traffic = NCU_TRAFFIC["bytes_per_launch"]
-    gbs = world * weight_bytes / (ms * 1e-3) / 1e9
+    gbs = whole_job_gbs(world, weight_bytes, ms)
     kname = "mv1" if M == 1 else "mvt"
     result = {
         "metric": METRIC,
@@ -416,7 +427,7 @@ def run_native(args, rank, world):
                               "mean_launch_us": round(dt_mean * 1e3, 2),
                               "algorithmic_bytes_per_launch": dt_bytes},
         },
-        "e2e": {"value": round(world * weight_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+        "e2e": {"value": round(whole_job_gbs(world, weight_bytes, e2e_ms), 2), "unit": "GB/s",
                 "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": 4 * M * H,
                 "d2h_bytes_per_step": 4 * M * H,
                 "api": "muser_ffn_stack (one C call per token) with pinned host residual in / output out"},
@@ -596,10 +607,7 @@ def run_attn(args, rank, world):
     clock = clocks.stop()
     q_ms = statistics.mean(t[0].elapsed_time(t[1]) for ev in events for t in ev.values())
     o_ms = statistics.mean(t[1].elapsed_time(t[2]) for ev in events for t in ev.values())
-    if dist is not None:
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, dist)
     # e2e: the same calls with the residual in from pinned host memory and x out
     h_in = torch.from_numpy(r0.copy()).pin_memory()
     h_out = torch.empty(M, H, dtype=torch.float32).pin_memory()
@@ -623,7 +631,7 @@ def run_attn(args, rank, world):
     # the group with the previous tail: four matrices; p, r in/out, w1, w2, x out; four outputs
     q_bytes = (2 * QD + 2 * KVD) * (H // 256) * 144 + 4 * M * H * 6 + 4 * M * (2 * QD + 2 * KVD)
     o_bytes = H * (QD // 256) * 144 + 4 * M * QD + 4 * M * H
-    gbs = world * weight_bytes / (ms * 1e-3) / 1e9
+    gbs = whole_job_gbs(world, weight_bytes, ms)
     achieved = q_bytes / (q_ms * 1e-3) / 1e9
     return {
         "metric": METRIC, "value": round(gbs, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
@@ -648,7 +656,7 @@ def run_attn(args, rank, world):
                                        "achieved_gbs": round(o_bytes / (o_ms * 1e-3) / 1e9, 1),
                                        "mean_launch_us": round(o_ms * 1e3, 2),
                                        "algorithmic_bytes_per_launch": o_bytes}},
-        "e2e": {"value": round(world * weight_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+        "e2e": {"value": round(whole_job_gbs(world, weight_bytes, e2e_ms), 2), "unit": "GB/s",
                 "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": 4 * M * H, "d2h_bytes_per_step": 4 * M * H,
                 "api": ("per-layer muser_qmatvec_group[_tail] / muser_qmatvec calls" if M == 1 else
                         "per-layer muser_fused_residual_dual_rmsnorm and muser_qmatvec_scratch calls") +
@@ -716,10 +724,7 @@ def run_lmhead(args, rank, world):
     barrier()
     clock = clocks.stop()
     ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
-    if dist is not None:
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, dist)
     h_in = torch.from_numpy(x.cpu().numpy()).pin_memory()
     h_out = torch.empty(VOCAB, dtype=torch.float32).pin_memory()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -734,7 +739,7 @@ def run_lmhead(args, rank, world):
     assert np.isfinite(h_out.numpy()).all()
     peak, peak_kind = read_peaks()
     nbytes = LMHEAD_W + 4 * H + 4 * VOCAB
-    gbs = world * LMHEAD_W / (ms * 1e-3) / 1e9
+    gbs = whole_job_gbs(world, LMHEAD_W, ms)
     achieved = nbytes / (ms * 1e-3) / 1e9
     return {
         "metric": METRIC, "value": round(gbs, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
@@ -749,7 +754,7 @@ def run_lmhead(args, rank, world):
         "roofline": {"bound": "hbm", "kernel": "muser_lm_head (mv1 Q6_K, soft-cap epilogue)",
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "traffic": None, "algorithmic_bytes_per_launch": nbytes, "mean_launch_us": round(ms * 1e3, 2)},
-        "e2e": {"value": round(world * LMHEAD_W / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+        "e2e": {"value": round(whole_job_gbs(world, LMHEAD_W, e2e_ms), 2), "unit": "GB/s",
                 "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": 4 * H, "d2h_bytes_per_step": 4 * VOCAB,
                 "api": "muser_lm_head with the hidden row in from pinned host memory and the logits out"},
         "gpu_launches": args.steps, "clocks": clock, "device_status": mu.muser_device_status(),
@@ -839,10 +844,7 @@ def run_down_tail(args, rank, world):
     barrier()
     clock = clocks.stop()
     ms = e0.elapsed_time(e1) / args.steps
-    if dist is not None:
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, dist)
     assert torch.isfinite(out).all() and torch.isfinite(resid).all()
     # end to end: the residual row in from pinned host memory, the normed row out, every call
     h_in = torch.from_numpy(r0.copy()).pin_memory()
@@ -1005,10 +1007,7 @@ def run_kv_restore(args, rank, world):
         b.record(stream)
     barrier()
     one_ms = statistics.mean(a.elapsed_time(b) for a, b in one)
-    if dist is not None:
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, dist)
     # end to end: the detached rows arrive in pinned host memory (as from the wire)
     host_rows = [(torch.empty(n * KV_DIM, dtype=torch.int16).pin_memory(),
                   torch.empty(n * KV_DIM, dtype=torch.int16).pin_memory())
@@ -1028,7 +1027,7 @@ def run_kv_restore(args, rank, world):
     e2e_ms = e0.elapsed_time(e1) / args.steps
     peak, peak_kind = read_peaks()
     moved = 2 * row_bytes
-    gbs = world * moved / (ms * 1e-3) / 1e9
+    gbs = whole_job_gbs(world, moved, ms)
     one_bytes = 2 * 2 * 2 * n0 * KV_DIM
     achieved = one_bytes / (one_ms * 1e-3) / 1e9
     return {
@@ -1049,7 +1048,7 @@ def run_kv_restore(args, rank, world):
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "traffic": None, "algorithmic_bytes_per_launch": one_bytes,
                      "mean_launch_us": round(one_ms * 1e3, 2)},
-        "e2e": {"value": round(world * moved / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+        "e2e": {"value": round(whole_job_gbs(world, moved, e2e_ms), 2), "unit": "GB/s",
                 "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": row_bytes, "d2h_bytes_per_step": 0,
                 "api": "muser_kv_restore with the detached rows in from pinned host memory"},
         "gpu_launches": args.steps * len(layers), "clocks": clock, "device_status": mu.muser_device_status(),
