@@ -684,6 +684,8 @@ def run_lmhead(args, rank, world):
         dist.init_process_group("nccl")
     mu.build()
     L = mu.lib()
+    VOCAB = args.vocab                      # the model's 202,048 unless a smaller case is asked for
+    LMHEAD_W = VOCAB * (H // 256) * 210     # Q6_K
     t0 = time.time()
     W = torch.from_numpy(synth.q6k_matrix(VOCAB, H, seed=0, workload=7)).cuda()
     gen_s = time.time() - t0
@@ -1096,6 +1098,8 @@ def main():
                                            "kv_restore", "down_tail_q4k", "down_tail_q6k", "matvec_q5k"],
                     default="stack52_m1")
     ap.add_argument("--layers", type=int, default=NL)
+    ap.add_argument("--vocab", type=int, default=VOCAB,
+                    help="lmhead_m1: output rows (the model's 202,048; smaller for profiling)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--ref-frac", type=float, default=0.0625)
     ap.add_argument("--no-cpu-baseline", action="store_true")
