@@ -66,3 +66,24 @@ def test_reference_arm_does_no_work_off_rank_0():
     class Args:
         steps, warmup, ref_frac, workload, layers = 2, 3, 0.0625, "stack52_m1", 52
     assert bench.run_reference(Args(), 1, 2) is None
+
+
+def test_clock_sampler_parses_samples_and_cleans_up(tmp_path, monkeypatch):
+    # a stand-in for nvidia-smi that prints three samples in the queried CSV
+    # form (one of them with sw_power_cap active) and then waits to be stopped
+    fake = tmp_path / "nvidia-smi"
+    fake.write_text("#!/bin/sh\n"
+                    "echo '0, 2070, 2070, 900.1, 0x0, Not Active, Not Active, Not Active, Not Active'\n"
+                    "echo '0, 1950, 2070, 1399.0, 0x4, Not Active, Not Active, Not Active, Active'\n"
+                    "echo '0, 2070, 2070, 950.3, 0x0, Not Active, Not Active, Not Active, Not Active'\n"
+                    "exec sleep 30\n")
+    fake.chmod(0o755)
+    monkeypatch.setenv("PATH", f"{tmp_path}:{os.environ.get('PATH', '')}")
+    import time
+    s = bench.ClockSampler(None)
+    s.start()
+    path = s.path
+    time.sleep(0.5)
+    got = s.stop()
+    assert got == {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"], "samples": 3}
+    assert not os.path.exists(path)
