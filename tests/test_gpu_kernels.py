@@ -453,6 +453,34 @@ def test_kv_snapshot_and_restore_bit_exact(head_major, cap, kv_dim, head_dim, of
                 plane.len, plane.origin_logical, plane.origin_physical)
 
 
+@pytest.mark.parametrize("head_major,cap,n,origin", [(True, 131072, 130815, 0),        # a NoPE plane
+                                                     (False, 2048, 2048, 128767)])     # a wrapped SWA ring
+def test_kv_restore_full_session_plane(head_major, cap, n, origin):
+    # the bench's session shapes (kv_dim 256, two KV heads of 128): the whole
+    # plane pair against the oracle, byte for byte, and the snapshot back
+    kv_dim, head_dim = 256, 128
+    rng = np.random.default_rng(cap + n)
+    kr = rng.integers(0, 1 << 16, (n, kv_dim), dtype=np.uint16)
+    vr = rng.integers(0, 1 << 16, (n, kv_dim), dtype=np.uint16)
+    key = torch.full((cap * kv_dim,), 0x1234, dtype=torch.int16, device="cuda")
+    val = key.clone()
+    plane = mu.KvPlane(key.data_ptr(), val.data_ptr(), cap, 0, 0, 0, kv_dim, head_dim, 1 if head_major else 0, 0)
+    dk, dv = dev(kr.view(np.int16)), dev(vr.view(np.int16))
+    mu.muser_kv_restore(plane, dk, dv, origin, n)
+    ring = oracle.Ring(cap, 0, 0, 0)
+    okey = np.full(cap * kv_dim, 0x1234, np.uint16)
+    oval = okey.copy()
+    assert oracle.kv_restore(ring, okey, oval, kv_dim, head_dim, head_major, kr, vr, origin) == 0
+    assert (plane.len, plane.origin_logical, plane.origin_physical) == (
+        ring.len, ring.origin_logical, ring.origin_physical)
+    assert np.array_equal(_u16(key), okey) and np.array_equal(_u16(val), oval)
+    back_k = torch.empty(n * kv_dim, dtype=torch.int16, device="cuda")
+    back_v = torch.empty_like(back_k)
+    mu.muser_kv_snapshot(plane, origin, n, back_k, back_v)
+    assert np.array_equal(_u16(back_k).reshape(n, kv_dim), kr)
+    assert np.array_equal(_u16(back_v).reshape(n, kv_dim), vr)
+
+
 def test_kv_snapshot_and_restore_reject_without_writing():
     key, val, plane, ring, okey, oval = _plane_pair(32, 256, 128, True)
     k, v = synth.kv_rows(40, 256, seed=5)
