@@ -405,9 +405,10 @@ int muser_kv_ring_write(muser_kv_plane* plane, const float* k, const float* v, i
  *   plane: host struct, read only; k_rows, v_rows: device binary16
  *   [count*kv_dim], token-major, in logical order, 2-byte aligned (16-byte
  *   alignment with kv_dim, and head_dim for head-major planes, multiples of 8
- *   takes 16-byte copies), not overlapping the planes.  count == 0 launches
- *   nothing.  A range outside [origin_logical, origin_logical+len) returns
- *   MUSER_ERR_INVALID_ARG and writes nothing.
+ *   takes 16-byte copies), not overlapping the planes or each other
+ *   (MUSER_ERR_INVALID_ARG).  count == 0 launches nothing.  A range outside
+ *   [origin_logical, origin_logical+len) returns MUSER_ERR_INVALID_ARG and
+ *   writes nothing.
  */
 int muser_kv_snapshot(const muser_kv_plane* plane, int64_t first_logical, int64_t count,
                       uint16_t* k_rows, uint16_t* v_rows, void* stream);
@@ -424,7 +425,8 @@ int muser_kv_snapshot(const muser_kv_plane* plane, int64_t first_logical, int64_
  *   written; a NoPE plane (origin 0) gets the plain layout.
  *   plane: host struct (updated on success); k_rows, v_rows: device binary16
  *   [len*kv_dim], token-major, as muser_kv_snapshot writes them, not
- *   overlapping the planes.  origin_logical < 0, len < 0 or len > capacity
+ *   overlapping the planes or each other (MUSER_ERR_INVALID_ARG).
+ *   origin_logical < 0, len < 0 or len > capacity
  *   returns MUSER_ERR_INVALID_ARG and changes nothing.  len == 0 only sets the
  *   metadata.
  */

@@ -788,6 +788,22 @@ int muser_ffn_stack(const muser_ffn_layer* layers, int n_layers, const float* en
     return MUSER_OK;
 }
 
+// Whether the byte ranges [a, a + na) and [b, b + nb) share a byte.
+static bool ranges_overlap(const void* a, size_t na, const void* b, size_t nb) {
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return na > 0 && nb > 0 && x < y + nb && y < x + na;
+}
+
+// Detached rows (count rows of kv_dim halves each) must not overlap the planes.
+static bool rows_overlap_plane(const muser_kv_plane& P, const void* k_rows, const void* v_rows, int64_t count) {
+    const size_t nr = static_cast<size_t>(count) * static_cast<size_t>(P.kv_dim) * 2u;
+    const size_t np = static_cast<size_t>(P.capacity) * static_cast<size_t>(P.kv_dim) * 2u;
+    for (const void* r : {k_rows, v_rows})
+        for (const void* q : {static_cast<const void*>(P.key), static_cast<const void*>(P.value)})
+            if (ranges_overlap(r, nr, q, np)) return true;
+    return ranges_overlap(k_rows, nr, v_rows, nr);
+}
+
 // The plane checks shared by the K/V calls (Ch 15 §15.2 metadata invariants).
 static int check_plane(const muser_kv_plane* plane, const char* fn) {
     if (plane == nullptr) return set_error(MUSER_ERR_INVALID_ARG, "%s: plane is NULL", fn);
@@ -858,6 +874,8 @@ int muser_kv_snapshot(const muser_kv_plane* plane, int64_t first_logical, int64_
     if (!k_rows || !v_rows) return set_error(MUSER_ERR_INVALID_ARG, "%s: k_rows/v_rows NULL", fn);
     if (!is_aligned(k_rows, 2) || !is_aligned(v_rows, 2))
         return set_error(MUSER_ERR_MISALIGNED, "%s: k_rows/v_rows must be 2-byte aligned", fn);
+    if (rows_overlap_plane(P, k_rows, v_rows, count))
+        return set_error(MUSER_ERR_INVALID_ARG, "%s: k_rows, v_rows and the planes must not overlap", fn);
     const int64_t phys0 = (P.origin_physical + (first_logical - P.origin_logical)) % P.capacity;
     return launch_kv_window(P.key, P.value, k_rows, v_rows, P.kv_dim, P.head_dim, P.head_major,
                             P.capacity, phys0, count, false, as_stream(stream));
@@ -878,6 +896,8 @@ int muser_kv_restore(muser_kv_plane* plane, const uint16_t* k_rows, const uint16
         if (!k_rows || !v_rows) return set_error(MUSER_ERR_INVALID_ARG, "%s: k_rows/v_rows NULL", fn);
         if (!is_aligned(k_rows, 2) || !is_aligned(v_rows, 2))
             return set_error(MUSER_ERR_MISALIGNED, "%s: k_rows/v_rows must be 2-byte aligned", fn);
+        if (rows_overlap_plane(P, k_rows, v_rows, len))
+            return set_error(MUSER_ERR_INVALID_ARG, "%s: k_rows, v_rows and the planes must not overlap", fn);
         MUSER_TRY(launch_kv_window(P.key, P.value, const_cast<uint16_t*>(k_rows),
                                    const_cast<uint16_t*>(v_rows), P.kv_dim, P.head_dim,
                                    P.head_major, P.capacity, rotation, len, true,

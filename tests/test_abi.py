@@ -158,6 +158,14 @@ def test_kv_snapshot_and_restore_fail_closed(L):
     assert (plane.len, plane.origin_logical, plane.origin_physical) == (0, 4100, 4)
     bad_plane = mu.KvPlane(FAKE, FAKE, 32, 40, 0, 0, 256, 128, 0, 0)
     assert L.muser_kv_restore(ctypes.byref(bad_plane), FAKE, FAKE, 0, 1, None) == -1
+    # detached rows that overlap a plane, or each other, are rejected before any launch
+    plane = mu.KvPlane(FAKE, FAKE * 2, 64, 64, 0, 0, 256, 128, 0, 0)     # planes: 32 KB each
+    rows = FAKE * 4
+    for k_rows, v_rows in ((FAKE + 512, rows), (rows, FAKE * 2 + 32768 - 2), (rows, rows + 1024)):
+        assert L.muser_kv_restore(ctypes.byref(plane), k_rows, v_rows, 0, 8, None) == -1
+        assert "overlap" in mu.muser_last_error()
+        assert L.muser_kv_snapshot(ctypes.byref(plane), 0, 8, k_rows, v_rows, None) == -1
+    assert (plane.len, plane.origin_logical, plane.origin_physical) == (64, 0, 0)
 
 
 @needs_nvcc
