@@ -7,7 +7,12 @@
  * one-token quantized matvec over ggml-style Q4_K / Q6_K super-blocks
  * (Ch 19 §19.3, §19.5), the FFN gate/up/SiLU step (Ch 10 Figure 10.1 box 11,
  * §10.3 (d)), the dual-epsilon fused residual tail (Ch 19 §19.4; Ch 10 §10.4
- * Figure 10.2) and the f16 K/V ring store (Ch 15 §15.4-§15.5).
+ * Figure 10.2) and the f16 K/V ring store (Ch 15 §15.4-§15.5).  Around it:
+ * the attention-side projection group of the same layer (Ch 10 Figure 10.1
+ * box 4, §10.3 (e)), the LM head with its logit scale and soft cap (boxes 14
+ * and 15), Q5_K matrices (the third k-quant of the kernel registry, Ch 4
+ * §4.4), and the K/V window snapshot and rotation-preserving restore
+ * (Ch 15 §15.6).
  *
  * Conventions shared by every entry point:
  *  - Ownership: the caller owns every buffer.  No entry point allocates or
