@@ -184,41 +184,85 @@ __global__ void kv_store_kernel(uint16_t* key, uint16_t* value, const float* k, 
 
 // Muser book Ch 15 §15.6: moves `count` token rows between a K/V plane pair
 // and detached token-major rows.  Row j of the window <-> physical slot
-// (phys0 + j) % capacity, in either plane layout (§15.3 Figure 15.1).  Each
-// thread moves VW consecutive halves of one row: VW = 8 (16-byte vectors) when
-// every 8-half group stays inside one head row and all four buffers are
-// 16-byte aligned, else 1.  Consecutive threads cover one row, so the rows side
-// is read or written contiguously and the plane side in head-row runs.
-template <int VW, bool TO_PLANE>
+// (phys0 + j) % capacity, in either plane layout (§15.3 Figure 15.1).  This
+// is the element form, one half per thread, for shapes or buffers that the
+// 16-byte form below does not take.
+template <bool TO_PLANE>
 __global__ void kv_window_kernel(uint16_t* __restrict__ pk, uint16_t* __restrict__ pv,
                                  uint16_t* __restrict__ rk, uint16_t* __restrict__ rv,
                                  int64_t kv_dim, int64_t head_dim, int head_major,
                                  int64_t capacity, int64_t phys0, int64_t count) {
-    const int64_t per_row = kv_dim / VW;
-    const int64_t total = count * per_row;
+    const int64_t total = count * kv_dim;
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
          i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        const int64_t j = i / per_row;
-        const int64_t e = (i - j * per_row) * VW;
+        const int64_t j = i / kv_dim;
+        const int64_t e = i - j * kv_dim;
         const int64_t p = (phys0 + j) % capacity;
         const int64_t pi =
             head_major ? ((e / head_dim) * capacity + p) * head_dim + e % head_dim : p * kv_dim + e;
-        const int64_t ri = j * kv_dim + e;
-        if constexpr (VW == 8) {
-            if constexpr (TO_PLANE) {
-                *reinterpret_cast<uint4*>(pk + pi) = *reinterpret_cast<const uint4*>(rk + ri);
-                *reinterpret_cast<uint4*>(pv + pi) = *reinterpret_cast<const uint4*>(rv + ri);
-            } else {
-                *reinterpret_cast<uint4*>(rk + ri) = *reinterpret_cast<const uint4*>(pk + pi);
-                *reinterpret_cast<uint4*>(rv + ri) = *reinterpret_cast<const uint4*>(pv + pi);
-            }
+        if constexpr (TO_PLANE) {
+            pk[pi] = rk[i];
+            pv[pi] = rv[i];
         } else {
+            rk[i] = pk[pi];
+            rv[i] = pv[pi];
+        }
+    }
+}
+
+// The 16-byte form, one warp per token row: the row's slot is computed once
+// per row, the lanes take the row's 16-byte chunks (kv_dim / 8 of them), and
+// two rows are in flight per warp (both rows' loads before their stores).
+template <bool TO_PLANE>
+__global__ void kv_window_rows_kernel(uint16_t* __restrict__ pk, uint16_t* __restrict__ pv,
+                                      uint16_t* __restrict__ rk, uint16_t* __restrict__ rv,
+                                      int kv_dim, int head_dim, int head_major, int64_t capacity,
+                                      int64_t phys0, int64_t count) {
+    const int lane = threadIdx.x & 31;
+    const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+    const int nch = kv_dim >> 3;
+    auto plane_index = [&](int64_t p, int e) -> int64_t {
+        if (!head_major) return p * kv_dim + e;
+        const int h = e / head_dim;
+        return (static_cast<int64_t>(h) * capacity + p) * head_dim + (e - h * head_dim);
+    };
+    for (int64_t j0 = warp; j0 < count; j0 += 2 * nwarps) {
+        const int64_t j1 = j0 + nwarps;
+        const bool two = j1 < count;
+        const int64_t p0 = (phys0 + j0) % capacity;
+        const int64_t p1 = two ? (phys0 + j1) % capacity : 0;
+        for (int c = lane; c < nch; c += 32) {
+            const int e = c << 3;
+            const int64_t r0 = j0 * kv_dim + e, r1 = j1 * kv_dim + e;
+            const int64_t q0 = plane_index(p0, e), q1 = two ? plane_index(p1, e) : 0;
+            uint4 k0, v0, k1 = make_uint4(0, 0, 0, 0), v1 = k1;
             if constexpr (TO_PLANE) {
-                pk[pi] = rk[ri];
-                pv[pi] = rv[ri];
+                k0 = *reinterpret_cast<const uint4*>(rk + r0);
+                v0 = *reinterpret_cast<const uint4*>(rv + r0);
+                if (two) {
+                    k1 = *reinterpret_cast<const uint4*>(rk + r1);
+                    v1 = *reinterpret_cast<const uint4*>(rv + r1);
+                }
+                *reinterpret_cast<uint4*>(pk + q0) = k0;
+                *reinterpret_cast<uint4*>(pv + q0) = v0;
+                if (two) {
+                    *reinterpret_cast<uint4*>(pk + q1) = k1;
+                    *reinterpret_cast<uint4*>(pv + q1) = v1;
+                }
             } else {
-                rk[ri] = pk[pi];
-                rv[ri] = pv[pi];
+                k0 = *reinterpret_cast<const uint4*>(pk + q0);
+                v0 = *reinterpret_cast<const uint4*>(pv + q0);
+                if (two) {
+                    k1 = *reinterpret_cast<const uint4*>(pk + q1);
+                    v1 = *reinterpret_cast<const uint4*>(pv + q1);
+                }
+                *reinterpret_cast<uint4*>(rk + r0) = k0;
+                *reinterpret_cast<uint4*>(rv + r0) = v0;
+                if (two) {
+                    *reinterpret_cast<uint4*>(rk + r1) = k1;
+                    *reinterpret_cast<uint4*>(rv + r1) = v1;
+                }
             }
         }
     }
@@ -296,21 +340,29 @@ int launch_kv_window(uint16_t* key, uint16_t* value, uint16_t* k_rows, uint16_t*
     const auto a16 = [](const void* q) { return (reinterpret_cast<uintptr_t>(q) & 15u) == 0; };
     const bool vec = kv_dim % 8 == 0 && (!head_major || head_dim % 8 == 0) && a16(key) &&
                      a16(value) && a16(k_rows) && a16(v_rows);
-    const int64_t total = count * (vec ? kv_dim / 8 : kv_dim);
     const int bs = 256;
+    if (vec) {
+        // one warp per row, two rows per warp per pass
+        const int64_t warps = (count + 1) / 2;
+        const int64_t grid = std::min<int64_t>((warps * 32 + bs - 1) / bs, static_cast<int64_t>(sm_count()) * 8);
+        const unsigned g = static_cast<unsigned>(grid);
+        const int kd = static_cast<int>(kv_dim), hd = static_cast<int>(head_dim);
+        if (to_plane)
+            kv_window_rows_kernel<true><<<g, bs, 0, s>>>(key, value, k_rows, v_rows, kd, hd, head_major,
+                                                         capacity, phys0, count);
+        else
+            kv_window_rows_kernel<false><<<g, bs, 0, s>>>(key, value, k_rows, v_rows, kd, hd, head_major,
+                                                          capacity, phys0, count);
+        return check_launch("kv_window");
+    }
+    const int64_t total = count * kv_dim;
     const int64_t grid = std::min<int64_t>((total + bs - 1) / bs, static_cast<int64_t>(sm_count()) * 8);
     const unsigned g = static_cast<unsigned>(grid);
-    if (vec && to_plane)
-        kv_window_kernel<8, true><<<g, bs, 0, s>>>(key, value, k_rows, v_rows, kv_dim, head_dim,
-                                                  head_major, capacity, phys0, count);
-    else if (vec)
-        kv_window_kernel<8, false><<<g, bs, 0, s>>>(key, value, k_rows, v_rows, kv_dim, head_dim,
-                                                   head_major, capacity, phys0, count);
-    else if (to_plane)
-        kv_window_kernel<1, true><<<g, bs, 0, s>>>(key, value, k_rows, v_rows, kv_dim, head_dim,
+    if (to_plane)
+        kv_window_kernel<true><<<g, bs, 0, s>>>(key, value, k_rows, v_rows, kv_dim, head_dim,
                                                   head_major, capacity, phys0, count);
     else
-        kv_window_kernel<1, false><<<g, bs, 0, s>>>(key, value, k_rows, v_rows, kv_dim, head_dim,
+        kv_window_kernel<false><<<g, bs, 0, s>>>(key, value, k_rows, v_rows, kv_dim, head_dim,
                                                    head_major, capacity, phys0, count);
     return check_launch("kv_window");
 }
