@@ -169,6 +169,61 @@ def test_kv_snapshot_and_restore_fail_closed(L):
 
 
 @needs_nvcc
+def test_group_calls_fail_closed(L):
+    P3 = ctypes.c_void_p * 4
+    R4 = ctypes.c_int64 * 4
+    W = P3(FAKE, FAKE, FAKE, FAKE)
+    rows = R4(4096, 256, 256, 4096)
+    y = P3(FAKE * 2, FAKE * 3, FAKE * 4, FAKE * 5)
+    g = L.muser_qmatvec_group
+    assert g(12, 0, W, rows, 6656, FAKE * 6, 1, y, None) == -1          # no matrices
+    assert g(12, 5, W, rows, 6656, FAKE * 6, 1, y, None) == -1          # more than four
+    assert g(12, 4, None, rows, 6656, FAKE * 6, 1, y, None) == -1       # no weight array
+    assert g(13, 4, W, rows, 6656, FAKE * 6, 1, y, None) == -2          # Q5_K is not a group type
+    assert g(12, 4, W, rows, 6600, FAKE * 6, 1, y, None) == -1          # cols not a multiple of 256
+    assert g(12, 4, W, rows, 6656, FAKE * 6, 17, y, None) == -1         # M = 17
+    assert g(12, 4, P3(FAKE, FAKE + 8, FAKE, FAKE), rows, 6656, FAKE * 6, 1, y, None) == -3
+    assert g(12, 4, W, rows, 6656, FAKE * 6, 1, P3(FAKE * 2, FAKE * 3 + 4, FAKE * 4, FAKE * 5), None) == -3
+    t = L.muser_qmatvec_group_tail
+    args = (12, 4, W, rows, 6656)
+    assert t(*args, FAKE * 6, FAKE * 7, FAKE * 8, FAKE * 9, 1e-8, 1e-5, FAKE * 7, 1, y, None) == -1   # x_out == residual
+    assert t(*args, FAKE * 6, FAKE * 7, FAKE * 8, FAKE * 9, 0.0, 1e-5, FAKE * 10, 1, y, None) == -1   # eps1 = 0
+    assert t(*args, FAKE * 6, FAKE * 6, FAKE * 8, FAKE * 9, 1e-8, 1e-5, FAKE * 10, 1, y, None) == -1  # projected == residual
+
+
+@needs_nvcc
+def test_scale_softcap_and_lm_head_fail_closed(L):
+    sc = L.muser_scale_softcap
+    assert sc(FAKE, 8, 0.2, 0.0, None) == -1                 # cap must be > 0
+    assert sc(FAKE, 8, float("nan"), 20.0, None) == -1       # scale must be finite
+    assert sc(FAKE, 8, 0.2, float("inf"), None) == -1
+    assert sc(FAKE, -1, 0.2, 20.0, None) == -1
+    assert sc(FAKE + 4, 8, 0.2, 20.0, None) == -3
+    assert sc(FAKE, 0, 0.2, 20.0, None) == 0                 # nothing to do, nothing launched
+    lm = L.muser_lm_head
+    assert lm(14, FAKE, 202048, 6656, FAKE * 2, 1, FAKE * 3, 0.196116, -1.0, None) == -1
+    assert lm(14, FAKE, 202048, 6656, FAKE * 2, 0, FAKE * 3, 0.196116, 20.0, None) == -1
+    assert lm(14, FAKE, 202048, 6600, FAKE * 2, 1, FAKE * 3, 0.196116, 20.0, None) == -1
+    assert lm(99, FAKE, 202048, 6656, FAKE * 2, 1, FAKE * 3, 0.196116, 20.0, None) == -2
+
+
+@needs_nvcc
+def test_fused_layer_boundary_and_static_scratch_fail_closed(L):
+    f = L.muser_ffn_gate_up_silu_tail
+    base = (12, FAKE, FAKE * 2, 19968, 6656, FAKE * 3, FAKE * 4, FAKE * 5, FAKE * 6)
+    assert f(*base, 1e-8, 1e-5, FAKE * 4, 1, FAKE * 8, None) == -1   # x_out aliases the residual
+    assert f(*base, 1e-8, -1.0, FAKE * 7, 1, FAKE * 8, None) == -1   # eps2 < 0
+    assert f(*base, 1e-8, 1e-5, FAKE * 7, 0, FAKE * 8, None) == -1   # M = 0
+    assert f(14, FAKE, FAKE * 2, 19968, 6656, FAKE * 3, FAKE * 4, FAKE * 5, FAKE * 6, 1e-8, 1e-5,
+             FAKE * 7, 1, FAKE * 8 + 4, None) == -3                   # misaligned mid
+    st = L.muser_qmatvec_residual_dual_rmsnorm_static
+    # M * hidden above the static array's 262,080 floats
+    assert st(14, FAKE, 65536, 19968, FAKE * 2, 16, FAKE * 3, FAKE * 4, FAKE * 5, FAKE * 6, 1e-8, 1e-5,
+              None) == -1
+    assert "static" in mu.muser_last_error() or "scratch" in mu.muser_last_error()
+
+
+@needs_nvcc
 def test_debug_spin_bound(L):
     assert L.muser_debug_spin(11 * 1000 * 1000, None) == -1
 
