@@ -87,3 +87,22 @@ def test_clock_sampler_parses_samples_and_cleans_up(tmp_path, monkeypatch):
     got = s.stop()
     assert got == {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"], "samples": 3}
     assert not os.path.exists(path)
+
+
+def test_reference_arm_line_has_the_contract_keys():
+    # the reference arm times the fp64 oracle on a small row sample of one
+    # layer; its JSON line carries the keys and units of the native line
+    class Args:
+        steps, warmup, ref_frac, workload, layers = 1, 3, 0.002, "stack52_m1", 52
+    res = bench.run_reference(Args(), 0, 1)
+    for k in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+              "scaling", "vs_baseline", "dtype", "data", "config", "impl", "cpu_baseline", "e2e"):
+        assert k in res, k
+    assert res["impl"] == "reference" and res["unit"] == "GB/s" and res["higher_is_better"] is True
+    assert res["value"] > 0 and res["steps"] == 1 and res["n_gpus"] == 1
+    assert res["metric"] == bench.METRIC and res["config"]["workload"]
+    cb = res["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] == res["value"] and cb["cores"] >= 1 and cb["sample"]
+    assert res["e2e"] == {"value": res["value"], "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+    import json
+    json.dumps(res)
