@@ -183,35 +183,40 @@ class ClockSampler:
 
 
 # ----------------------------------------------------------------- native
+def make_layers(n_layers: int, seed: int = 0, workload: int = 4):
+    """The stack's seeded weights on the device: per layer Wg, Wu (Q4_K), Wd
+    (Q6_K), the post-FFN norm w1 and the next norm (the next layer's input
+    norm) w_next."""
+    import torch
+    layers = []
+    for l in range(n_layers):
+        Ld = synth.ffn_layer(l, H, F, seed=seed, workload=workload)
+        d = {k: torch.from_numpy(v).cuda() for k, v in Ld.items()}
+        d["w_next"] = torch.from_numpy(synth.input_norm_weight(l + 1, H, seed=seed, workload=workload)).cuda()
+        layers.append(d)
+    return layers
+
+
 class NativeStack:
     """The workload on the GPU, driven through libmuser's C ABI."""
 
-    def __init__(self, M: int, n_layers: int, seed: int = 0):
+    def __init__(self, M: int, layers, seed: int = 0, workload: int = 4):
         import torch
         import quantized_weight_streaming_q4_gb300 as mu
-        self.torch, self.mu, self.M, self.nl = torch, mu, M, n_layers
+        self.torch, self.mu, self.M, self.nl = torch, mu, M, len(layers)
         self.L = mu.lib()
-        wl = 4
-        self.layers = []
-        self.structs = []
-        t0 = time.time()
-        for l in range(n_layers):
-            Ld = synth.ffn_layer(l, H, F, seed=seed, workload=wl)
-            w_next = synth.input_norm_weight(l + 1, H, seed=seed, workload=wl)
-            d = {k: torch.from_numpy(v).cuda() for k, v in Ld.items()}
-            d["w_next"] = torch.from_numpy(w_next).cuda()
-            self.layers.append(d)
-            self.structs.append(mu.FfnLayer(d["Wg"].data_ptr(), d["Wu"].data_ptr(), d["Wd"].data_ptr(),
-                                            d["w1"].data_ptr(), d["w_next"].data_ptr(), mu.MUSER_Q4_K,
-                                            mu.MUSER_Q6_K))
-        self.gen_s = time.time() - t0
-        self.w_in = torch.from_numpy(synth.input_norm_weight(0, H, seed=seed, workload=wl)).cuda()
-        self.r0 = synth.residual_rows(M, H, seed=seed, workload=wl)
+        self.layers = layers
+        self.structs = [mu.FfnLayer(d["Wg"].data_ptr(), d["Wu"].data_ptr(), d["Wd"].data_ptr(),
+                                    d["w1"].data_ptr(), d["w_next"].data_ptr(), mu.MUSER_Q4_K, mu.MUSER_Q6_K)
+                        for d in layers]
+        self.w_in = torch.from_numpy(synth.input_norm_weight(0, H, seed=seed, workload=workload)).cuda()
+        self.r0 = synth.residual_rows(M, H, seed=seed, workload=workload)
         self.resid = torch.from_numpy(self.r0).cuda()
         self.out = torch.empty(M, H, dtype=torch.float32, device="cuda")
         self.x = [torch.empty(M, H, dtype=torch.float32, device="cuda") for _ in range(2)]
         self.mid = torch.empty(M, F, dtype=torch.float32, device="cuda")
         self.proj = torch.empty(M, H, dtype=torch.float32, device="cuda")
+        self.ticket = torch.zeros(mu.MUSER_BOUNDARY_SCRATCH_BYTES // 4, dtype=torch.int32, device="cuda")
         self.gu_scratch_bytes = mu.muser_gate_up_scratch_bytes(mu.MUSER_Q4_K, F, H, M)
         self.gu_scratch = torch.zeros(max(self.gu_scratch_bytes, 16) // 4, dtype=torch.float32, device="cuda")
         self.scratch_bytes = mu.muser_scratch_bytes(H, M)
@@ -221,19 +226,27 @@ class NativeStack:
         self.wsb = wsb
         self.stream = torch.cuda.current_stream()
         self.sh = self.stream.cuda_stream
-        self.arr = (mu.FfnLayer * n_layers)(*self.structs)
-        self.launches_per_step = 1 + 2 * n_layers + (1 if M == 1 else 0)
+        self.arr = (mu.FfnLayer * self.nl)(*self.structs)
+        # launches of one per-layer step: the entry norm, two per layer, and
+        # (M = 1) the last tail on its own
+        self.per_layer_launches = 1 + 2 * self.nl + (1 if M == 1 else 0)
 
     def _rc(self, name, rc):
         if rc != 0:
             raise RuntimeError(f"{name}: {self.mu.muser_last_error()}")
 
-    def step(self, events=None):
-        """One token (M rows) through every layer, per-layer calls.  `events`
-        maps a few layers to an event triple that brackets their gate/up and
-        down launches (the others run back to back, overlapped by PDL)."""
+    def step_public(self):
+        """One token (M rows) through every layer: the public one-call entry point."""
+        self._rc("ffn_stack", self.L.muser_ffn_stack(
+            self.arr, self.nl, self.w_in.data_ptr(), H, F, self.M, self.resid.data_ptr(),
+            self.out.data_ptr(), 1e-5, 1e-8, self.ws.data_ptr(), self.wsb, self.sh))
+
+    def step_layers(self, events=None):
+        """The same token as per-layer calls.  `events` maps a few layers to an
+        event triple that brackets their gate/up and down launches (the others
+        run back to back, overlapped by PDL)."""
         if self.M == 1:
-            return self._step_m1(events)
+            return self._layers_m1(events)
         L, M, sh = self.L, self.M, self.sh
         self._rc("rms_norm", L.muser_rms_norm(self.resid.data_ptr(), self.w_in.data_ptr(),
                                               self.x[0].data_ptr(), H, M, 1e-5, sh))
@@ -256,11 +269,10 @@ class NativeStack:
                 ev[2].record(self.stream)
             x, xn = xn, x
 
-    def _step_m1(self, events=None):
-        """One row of x, the composition muser_ffn_stack uses for it: the
-        entry norm, then per layer gate/up (with the previous layer's tail
-        fused in, from layer 1) and the plain down projection, then the last
-        layer's tail."""
+    def _layers_m1(self, events=None):
+        """One row of x as per-layer calls: the entry norm, then per layer
+        gate/up (with the previous layer's tail fused in, from layer 1) and the
+        plain down projection, then the last layer's tail."""
         L, M, sh = self.L, self.M, self.sh
         self._rc("rms_norm", L.muser_rms_norm(self.resid.data_ptr(), self.w_in.data_ptr(),
                                               self.x[0].data_ptr(), H, M, 1e-5, sh))
@@ -277,7 +289,8 @@ class NativeStack:
                 self._rc("gate_up_tail", L.muser_ffn_gate_up_silu_tail(
                     12, d["Wg"].data_ptr(), d["Wu"].data_ptr(), F, H, self.proj.data_ptr(),
                     self.resid.data_ptr(), prev["w1"].data_ptr(), prev["w_next"].data_ptr(), 1e-8, 1e-5,
-                    self.x[1].data_ptr(), M, self.mid.data_ptr(), sh))
+                    self.x[1].data_ptr(), M, self.mid.data_ptr(), self.ticket.data_ptr(),
+                    self.mu.MUSER_BOUNDARY_SCRATCH_BYTES, sh))
             if ev is not None:
                 ev[1].record(self.stream)
             self._rc("down", L.muser_qmatvec(14, d["Wd"].data_ptr(), H, F, self.mid.data_ptr(), M,
@@ -289,11 +302,104 @@ class NativeStack:
             self.resid.data_ptr(), self.proj.data_ptr(), self.out.data_ptr(), prev["w1"].data_ptr(),
             prev["w_next"].data_ptr(), H, M, 1e-8, 1e-5, sh))
 
-    def step_public(self):
-        """The same token through the one-call public entry point."""
-        self._rc("ffn_stack", self.L.muser_ffn_stack(
-            self.arr, self.nl, self.w_in.data_ptr(), H, F, self.M, self.resid.data_ptr(),
-            self.out.data_ptr(), 1e-5, 1e-8, self.ws.data_ptr(), self.wsb, self.sh))
+
+NOMINAL_HBM_GBS = 8000.0   # GB300 HBM3e, nominal (context beside the measured copy peak)
+REPS = 5                   # counted repetitions of the timed region (mean and coefficient of variation)
+
+
+def timed_reps(stream, steps: int, fn):
+    """Time exactly `steps` calls of fn() on `stream`, split into up to REPS
+    consecutive repetitions bracketed by CUDA events (no synchronisation
+    between them).  Returns (total ms, per-rep ms per step)."""
+    import torch
+    nrep = max(1, min(REPS, steps))
+    sizes = [steps // nrep + (1 if r < steps % nrep else 0) for r in range(nrep)]
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(nrep + 1)]
+    ev[0].record(stream)
+    for r, n in enumerate(sizes):
+        for _ in range(n):
+            fn()
+        ev[r + 1].record(stream)
+    torch.cuda.synchronize()
+    per = [ev[r].elapsed_time(ev[r + 1]) / n for r, n in enumerate(sizes)]
+    return ev[0].elapsed_time(ev[-1]), per
+
+
+def rep_stats(per):
+    m = statistics.mean(per)
+    cv = statistics.pstdev(per) / m if len(per) > 1 and m > 0 else 0.0
+    return {"reps": len(per), "ms_per_step_mean": round(m, 4), "cv": round(cv, 4),
+            "ms_per_step_each": [round(v, 4) for v in per]}
+
+
+def gpu_uuid():
+    import torch
+    try:
+        return "GPU-" + str(torch.cuda.get_device_properties(torch.cuda.current_device()).uuid)
+    except Exception:
+        return None
+
+
+def measure_stack(S, steps: int, warmup: int, barrier, with_probes: bool = True):
+    """The headline, probe-free: `steps` tokens through muser_ffn_stack after
+    `warmup`, then a separate probe pass (per-launch events, per-layer event
+    triples) and the end-to-end pass with host copies."""
+    import torch
+    M, nl = S.M, S.nl
+    for _ in range(warmup):
+        S.step_public()
+    barrier()
+    clocks = ClockSampler(gpu_uuid())
+    clocks.start()
+    time.sleep(0.3)
+    barrier()
+    total_ms, per = timed_reps(S.stream, steps, S.step_public)
+    barrier()
+    clock = clocks.stop()
+    res = {"ms": total_ms / steps, "reps": rep_stats(per), "clocks": clock}
+    if with_probes:
+        # one stack call per event pair: the duration of the whole call
+        pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                 for _ in range(max(3, min(steps, 10)))]
+        for a, b in pairs:
+            a.record(S.stream)
+            S.step_public()
+            b.record(S.stream)
+        barrier()
+        res["call_ms"] = statistics.mean(a.elapsed_time(b) for a, b in pairs)
+        # per-layer composition, PROBES layers per step bracketed by event triples
+        probes = min(PROBES, nl)
+        for _ in range(2):
+            S.step_layers()
+        evs = []
+        for k in range(max(3, min(steps, 10))):
+            ls = sorted({(k + j * max(1, nl // probes)) % nl for j in range(probes)})
+            evs.append({l: [torch.cuda.Event(enable_timing=True) for _ in range(3)] for l in ls})
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record(S.stream)
+        for e in evs:
+            S.step_layers(e)
+        t1.record(S.stream)
+        barrier()
+        res["layers_ms"] = t0.elapsed_time(t1) / len(evs)
+        res["gu_ms"] = statistics.mean(t[0].elapsed_time(t[1]) for e in evs for t in e.values())
+        res["dn_ms"] = statistics.mean(t[1].elapsed_time(t[2]) for e in evs for t in e.values())
+    # e2e: host residual in (pinned), the public call, host output out
+    h_in = torch.from_numpy(S.r0.copy()).pin_memory()
+    h_out = torch.empty(M, H, dtype=torch.float32).pin_memory()
+
+    def e2e_step():
+        S.resid.copy_(h_in, non_blocking=True)
+        S.step_public()
+        h_out.copy_(S.out, non_blocking=True)
+    for _ in range(max(1, min(3, warmup))):
+        e2e_step()
+    barrier()
+    e_total, _ = timed_reps(S.stream, steps, e2e_step)
+    barrier()
+    assert np.isfinite(h_out.numpy()).all()
+    res["e2e_ms"] = e_total / steps
+    return res
 
 
 def run_native(args, rank, world):
@@ -307,7 +413,10 @@ def run_native(args, rank, world):
     mu.build()
     M = 16 if args.workload == "stack52_m16" else 1
     nl = args.layers
-    S = NativeStack(M, nl)
+    t0 = time.time()
+    layers = make_layers(nl)
+    gen_s = time.time() - t0
+    S = NativeStack(M, layers)
     gu_bytes, dt_bytes, entry_bytes = algorithmic_bytes(M)
     step_bytes = nl * (gu_bytes + dt_bytes) + entry_bytes
     weight_bytes = nl * LAYER_W
@@ -318,74 +427,28 @@ def run_native(args, rank, world):
             dist.barrier()
         torch.cuda.synchronize()
 
-    # warm-up
-    for _ in range(args.warmup):
-        S.step()
-    barrier()
-
-    uuid = None
-    try:
-        uuid = "GPU-" + str(torch.cuda.get_device_properties(torch.cuda.current_device()).uuid)
-    except Exception:
-        pass
-    clocks = ClockSampler(uuid)
-    clocks.start()
-    time.sleep(0.3)
-    # Per-kernel durations: each step brackets PROBES layers spread over the
-    # stack (a different set every step) with event triples, read after the
-    # timed region.  Events stop PDL overlap only at the bracketed launches.
-    probes = min(PROBES, nl)
-    events = []
-    for k in range(args.steps):
-        ls = sorted({(k + j * max(1, nl // probes)) % nl for j in range(probes)})
-        events.append({l: [torch.cuda.Event(enable_timing=True) for _ in range(3)] for l in ls})
-    barrier()
-    t_start = torch.cuda.Event(enable_timing=True)
-    t_end = torch.cuda.Event(enable_timing=True)
-    t_start.record(S.stream)
-    for k in range(args.steps):
-        S.step(events[k])
-    t_end.record(S.stream)
-    barrier()
-    total_ms = t_start.elapsed_time(t_end)
-    clock = clocks.stop()
-    gu_ms = [t[0].elapsed_time(t[1]) for ev in events for t in ev.values()]
-    dt_ms = [t[1].elapsed_time(t[2]) for ev in events for t in ev.values()]
-    ms = total_ms / args.steps
-    ms = max_over_ranks(ms, dist)
-
-    # e2e: host residual in (pinned), the public call, host output out
-    h_in = torch.from_numpy(S.r0.copy()).pin_memory()
-    h_out = torch.empty(M, H, dtype=torch.float32).pin_memory()
-    for _ in range(max(1, min(3, args.warmup))):
-        S.resid.copy_(h_in, non_blocking=True)
-        S.step_public()
-        h_out.copy_(S.out, non_blocking=True)
-    barrier()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e_steps = args.steps
-    e0.record(S.stream)
-    for _ in range(e_steps):
-        S.resid.copy_(h_in, non_blocking=True)
-        S.step_public()
-        h_out.copy_(S.out, non_blocking=True)
-    e1.record(S.stream)
-    barrier()
-    e2e_ms = e0.elapsed_time(e1) / e_steps
-    e2e_ms = max_over_ranks(e2e_ms, dist)
-    assert np.isfinite(h_out.numpy()).all()
+    r = measure_stack(S, args.steps, args.warmup, barrier)
+    ms = max_over_ranks(r["ms"], dist)
+    e2e_ms = max_over_ranks(r["e2e_ms"], dist)
     status = mu.muser_device_status()
-
     peak, peak_kind = read_peaks()
-    gu_mean = statistics.mean(gu_ms)
-    dt_mean = statistics.mean(dt_ms)
-    achieved = gu_bytes / (gu_mean * 1e-3) / 1e9
+    one_launch = S.L.muser_ffn_stack_launches(S.arr, nl, H, F, M)
+    # the dominant kernel: the whole stack when one launch carries it, else the gate/up kernel
+    if M == 1 and one_launch == 1:
+        kname = "muser_ffn_stack (the persistent one-token stack kernel: every layer's gate/up, down and tail)"
+        k_bytes, k_ms = step_bytes, r["call_ms"]
+    elif M == 1:
+        kname = ("muser_ffn_gate_up_silu_tail (mv1 Q4_K gate+up, previous layer's dual-eps tail in the prologue, "
+                 "SiLU epilogue)")
+        k_bytes, k_ms = gu_bytes, r["gu_ms"]
+    else:
+        kname = "muser_ffn_gate_up_silu_scratch (mvt Q4_K gate+up, SiLU epilogue)"
+        k_bytes, k_ms = gu_bytes, r["gu_ms"]
+    achieved = k_bytes / (k_ms * 1e-3) / 1e9
     traffic = None
     if M == 1 and NCU_TRAFFIC["bytes_per_launch"] and NCU_TRAFFIC["source_sha256"] == source_sha():
         traffic = NCU_TRAFFIC["bytes_per_launch"]
     gbs = whole_job_gbs(world, weight_bytes, ms)
-    kname = "mv1" if M == 1 else "mvt"
     result = {
         "metric": METRIC,
         "value": round(gbs, 2),
@@ -397,14 +460,14 @@ def run_native(args, rank, world):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "f32",
+        "dtype": ("f32 activations in and out, exact f32 dequantised weights; inside the kernels x is held as "
+                  + ("24-bit block fixed point (dp4a digits, <= 2^-23 of each 64-input slice's max)" if M == 1 else
+                     "two binary16 parts per super-block (<= 2^-22 of the block max) for the tensor cores")),
         "data": "synthetic (seeded; Q4_K/Q6_K fields and activations drawn per the workload recipe)",
         "config": {
             "workload": f"decode-FFN stack: {nl} layers x [rms_norm(layer 0) -> Q4_K gate/up {F}x{H} + SiLU "
                         f"-> Q6_K down {H}x{F} + dual-eps tail], M={M}",
-            "composition": ("per layer: gate/up kernel with the previous layer's tail in its prologue, "
-                            "down projection; entry norm and last tail once per step" if M == 1 else
-                            "per layer: gate/up kernel, down projection + tail kernel"),
+            "api": "muser_ffn_stack, one C call per token (device-resident input)",
             "layers": nl, "hidden": H, "ffn": F, "M": M,
             "weight_bytes_per_step": weight_bytes,
             "algorithmic_bytes_per_step": step_bytes,
@@ -413,34 +476,66 @@ def run_native(args, rank, world):
         },
         "tokens_per_s": round(world * M / (ms * 1e-3), 3),
         "hbm_frac_of_" + peak_kind: round(gbs / world / peak, 4),
+        "hbm_frac_of_nominal_8000": round(gbs / world / NOMINAL_HBM_GBS, 4),
+        "repetitions": r["reps"],
         "roofline": {
             "bound": "hbm",
-            "kernel": (f"muser_ffn_gate_up_silu_tail ({kname} Q4_K gate+up, previous layer's dual-eps tail in "
-                       f"the prologue, SiLU epilogue)" if M == 1 else
-                       f"muser_ffn_gate_up_silu ({kname} Q4_K gate+up, SiLU epilogue)"),
+            "kernel": kname,
             "achieved": round(achieved, 1),
             "peak": peak,
-            "peak_kind": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else "fallback 6.8 TB/s",
+            "peak_kind": (f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
+                          else "fallback 6.8 TB/s"),
             "unit": "GB/s",
             "frac": round(achieved / peak, 4),
+            "frac_of_nominal_8000": round(achieved / NOMINAL_HBM_GBS, 4),
             "traffic": traffic,
-            "algorithmic_bytes_per_launch": gu_bytes,
-            "mean_launch_us": round(gu_mean * 1e3, 2),
-            "second_kernel": {"name": (f"muser_qmatvec ({kname} Q6_K down projection)" if M == 1 else
-                                       f"muser_qmatvec_residual_dual_rmsnorm ({kname} Q6_K + tail)"),
-                              "achieved_gbs": round(dt_bytes / (dt_mean * 1e-3) / 1e9, 1),
-                              "mean_launch_us": round(dt_mean * 1e3, 2),
-                              "algorithmic_bytes_per_launch": dt_bytes},
+            "algorithmic_bytes_per_launch": k_bytes,
+            "mean_launch_us": round(k_ms * 1e3, 2),
+            "timing": "CUDA events around each launch in a probe pass after the timed region",
+        },
+        "per_layer_calls": {
+            "ms_per_step": round(r["layers_ms"], 4),
+            "value": round(weight_bytes / (r["layers_ms"] * 1e-3) / 1e9, 2),
+            "gate_up": {"name": ("muser_ffn_gate_up_silu[_tail] (mv1)" if M == 1 else
+                                 "muser_ffn_gate_up_silu_scratch (mvt)"),
+                        "mean_launch_us": round(r["gu_ms"] * 1e3, 2),
+                        "achieved_gbs": round(gu_bytes / (r["gu_ms"] * 1e-3) / 1e9, 1),
+                        "algorithmic_bytes_per_launch": gu_bytes},
+            "down": {"name": ("muser_qmatvec (mv1 Q6_K)" if M == 1 else
+                              "muser_qmatvec_residual_dual_rmsnorm (mvt Q6_K + tail)"),
+                     "mean_launch_us": round(r["dn_ms"] * 1e3, 2),
+                     "achieved_gbs": round(dt_bytes / (r["dn_ms"] * 1e-3) / 1e9, 1),
+                     "algorithmic_bytes_per_launch": dt_bytes},
+            "timing": "probe pass: event triples around 4 layers per step (they stop PDL overlap there)",
         },
         "e2e": {"value": round(whole_job_gbs(world, weight_bytes, e2e_ms), 2), "unit": "GB/s",
                 "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": 4 * M * H,
                 "d2h_bytes_per_step": 4 * M * H,
-                "api": "muser_ffn_stack (one C call per token) with pinned host residual in / output out"},
-        "gpu_launches": args.steps * S.launches_per_step,
-        "clocks": clock,
+                "api": ("muser_ffn_stack, one C call per token on device buffers; the residual row is copied in "
+                        "from pinned host memory and the output row out (torch copies on the same stream)")},
+        "gpu_launches": args.steps * one_launch,
+        "clocks": r["clocks"],
         "device_status": status,
-        "weights_generation_s": round(S.gen_s, 1),
+        "weights_generation_s": round(gen_s, 1),
     }
+    if M == 1 and not args.no_sub and world == 1:
+        # config 4 (16 rows, speculative-verify shape) through the same weights
+        S16 = NativeStack(16, layers)
+        r16 = measure_stack(S16, max(3, min(args.steps, 8)), 3, barrier)
+        g16, d16, e16 = algorithmic_bytes(16)
+        result["sub_results"] = [{
+            "workload": f"decode-FFN stack: {nl} layers, M=16 (speculative-verify shape), same weights",
+            "value": round(weight_bytes / (r16["ms"] * 1e-3) / 1e9, 2), "unit": "GB/s",
+            "ms_per_step": round(r16["ms"], 4), "row_tokens_per_s": round(16 / (r16["ms"] * 1e-3), 1),
+            "hbm_frac_of_" + peak_kind: round(weight_bytes / (r16["ms"] * 1e-3) / 1e9 / peak, 4),
+            "repetitions": r16["reps"],
+            "gate_up": {"mean_launch_us": round(r16["gu_ms"] * 1e3, 2),
+                        "achieved_gbs": round(g16 / (r16["gu_ms"] * 1e-3) / 1e9, 1)},
+            "down_tail": {"mean_launch_us": round(r16["dn_ms"] * 1e3, 2),
+                          "achieved_gbs": round(d16 / (r16["dn_ms"] * 1e-3) / 1e9, 1)},
+            "e2e": {"value": round(weight_bytes / (r16["e2e_ms"] * 1e-3) / 1e9, 2), "unit": "GB/s",
+                    "ms_per_step": round(r16["e2e_ms"], 4)},
+            "clocks": r16["clocks"]}]
     if rank == 0 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
     return result
@@ -448,41 +543,67 @@ def run_native(args, rank, world):
 
 # ------------------------------------------------------------- CPU oracle
 def _oracle_layer_sample(frac_rows: float, seed=0):
-    """A bounded sample of one layer: the first rows of gate/up/down."""
+    """A bounded sample of one layer: the first rows of gate/up/down, the
+    norm vectors and a residual row."""
     wl = 4
     rg = max(8, int(F * frac_rows))
     rd = max(8, int(H * frac_rows))
     Wg = synth.q4k_matrix(F, H, seed=seed, workload=wl, layer=0, tensor=synth.T_GATE)[:rg]
     Wu = synth.q4k_matrix(F, H, seed=seed, workload=wl, layer=0, tensor=synth.T_UP)[:rg]
     Wd = synth.q6k_matrix(H, F, seed=seed, workload=wl, layer=0, tensor=synth.T_DOWN)[:rd]
-    return np.ascontiguousarray(Wg), np.ascontiguousarray(Wu), np.ascontiguousarray(Wd), rg, rd
+    return {"Wg": np.ascontiguousarray(Wg), "Wu": np.ascontiguousarray(Wu), "Wd": np.ascontiguousarray(Wd),
+            "rg": rg, "rd": rd, "r": synth.residual_rows(1, H, seed=seed, workload=wl),
+            "w_in": synth.input_norm_weight(0, H, seed=seed, workload=wl),
+            "w1": synth.norm_weight(H, seed=seed, workload=wl, tensor=synth.T_W1),
+            "w2": synth.input_norm_weight(1, H, seed=seed, workload=wl),
+            "p": synth.normal((1, H), seed=3) * np.float32(2.5e6), "mid": synth.normal((1, F), seed=2)}
 
 
-def _oracle_step(oracle, Wg, Wu, Wd, rg, rd, x, mid_full):
-    g = oracle.qmatvec("q4_k", Wg, rg, H, x)
-    u = oracle.qmatvec("q4_k", Wu, rg, H, x)
+def _oracle_step(oracle, s):
+    """One sampled pass of the whole path in the oracle: the input norm, the
+    sampled gate/up rows and SiLU, the sampled down rows (on a full-length
+    intermediate row) and the dual-eps tail.  Returns the weight bytes read."""
+    x = oracle.rms_norm(s["r"], s["w_in"], 1e-5)
+    g = oracle.qmatvec("q4_k", s["Wg"], s["rg"], H, x)
+    u = oracle.qmatvec("q4_k", s["Wu"], s["rg"], H, x)
     oracle.silu_mul(g, u)
-    oracle.qmatvec("q6_k", Wd, rd, F, mid_full)
-    return Wg.nbytes + Wu.nbytes + Wd.nbytes
+    oracle.qmatvec("q6_k", s["Wd"], s["rd"], F, s["mid"])
+    oracle.dual_tail(s["r"], s["p"], s["w1"], s["w2"], 1e-8, 1e-5)
+    return s["Wg"].nbytes + s["Wu"].nbytes + s["Wd"].nbytes
 
 
-def cpu_baseline(seconds: float, frac_rows: float = 0.125):
-    import oracle
-    Wg, Wu, Wd, rg, rd = _oracle_layer_sample(frac_rows)
-    x = synth.normal((1, H), seed=1)
-    mid = synth.normal((1, F), seed=2)
+def _time_oracle(oracle, s, seconds: float):
     nbytes, t_tot, reps = 0, 0.0, 0
     while t_tot < seconds or reps < 1:
         t0 = time.perf_counter()
-        nbytes += _oracle_step(oracle, Wg, Wu, Wd, rg, rd, x, mid)
+        nbytes += _oracle_step(oracle, s)
         t_tot += time.perf_counter() - t0
         reps += 1
-    gbs = nbytes / t_tot / 1e9
-    return {"value": round(gbs, 4), "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",
+    return nbytes / t_tot / 1e9, reps, t_tot
+
+
+def cpu_baseline(seconds: float, frac_rows: float = 0.125):
+    """The fp64 oracle on the host cores: all cores (OpenMP over output rows)
+    and one core, each about `seconds` of work on a bounded row sample of one
+    layer, scaled to GB/s of weights."""
+    import oracle
+    s = _oracle_layer_sample(frac_rows)
+    nthreads = oracle.num_threads()
+    gbs, reps, t_tot = _time_oracle(oracle, s, seconds)
+    oracle.set_num_threads(1)
+    try:
+        gbs1, reps1, t1 = _time_oracle(oracle, s, seconds / 2)
+    finally:
+        oracle.set_num_threads(nthreads)
+    wmb = (s["Wg"].nbytes + s["Wu"].nbytes + s["Wd"].nbytes) / 1e6
+    return {"value": round(gbs, 4), "unit": "GB/s", "cores": nthreads, "kind": "oracle",
             "tokens_per_s": round(gbs * 1e9 / (NL * LAYER_W), 6),
-            "sample": f"{reps} passes of the fp64 oracle over the first {frac_rows:.3f} of the rows of "
-                      f"one layer's gate/up/down ({(Wg.nbytes + Wu.nbytes + Wd.nbytes) / 1e6:.1f} MB of "
-                      f"weights), {t_tot:.1f} s"}
+            "sample": f"{reps} passes of the fp64 oracle over one layer's path: input rms_norm, the first "
+                      f"{frac_rows:.3f} of the gate/up rows + SiLU and of the down rows ({wmb:.1f} MB of weights), "
+                      f"the dual-eps tail; {t_tot:.1f} s",
+            "one_core": {"value": round(gbs1, 4), "unit": "GB/s", "cores": 1,
+                         "tokens_per_s": round(gbs1 * 1e9 / (NL * LAYER_W), 6),
+                         "sample": f"{reps1} passes of the same sample on one thread, {t1:.1f} s"}}
 
 
 QD, KVD = synth.Q_DIM, synth.KV_DIM
@@ -540,6 +661,7 @@ def run_attn(args, rank, world):
     nscr = max(mu.muser_qmatvec_scratch_bytes(12, r, c, M) for r, c in ((QD, H), (KVD, H), (H, QD)))
     scratch = torch.zeros(max(nscr, 16) // 4 + 64, dtype=torch.float32, device="cuda")
     outs4 = (q, k, v, g)
+    ticket = torch.zeros(mu.MUSER_BOUNDARY_SCRATCH_BYTES // 4, dtype=torch.int32, device="cuda")
 
     def split_mv(W, rows, cols, xin, y):
         rc("qmatvec_scratch", L.muser_qmatvec_scratch(12, W.data_ptr(), rows, cols, xin.data_ptr(), M, y.data_ptr(),
@@ -564,7 +686,8 @@ def run_attn(args, rank, world):
             else:
                 rc("qkvg_tail", L.muser_qmatvec_group_tail(
                     12, 4, w4[l], rows4, H, proj.data_ptr(), resid.data_ptr(), prev["w_post"].data_ptr(),
-                    prev["w_ffn"].data_ptr(), 1e-8, 1e-5, x.data_ptr(), M, ys4, sh))
+                    prev["w_ffn"].data_ptr(), 1e-8, 1e-5, x.data_ptr(), M, ys4, ticket.data_ptr(),
+                    mu.MUSER_BOUNDARY_SCRATCH_BYTES, sh))
             if ev is not None:
                 ev[1].record(stream)
             if M > 1:
@@ -673,6 +796,9 @@ def run_attn(args, rank, world):
 
 VOCAB = 202048
 LMHEAD_W = VOCAB * (H // 256) * 210  # Q6_K
+# The model's logit scale and soft cap as the book prints them (Ch 10 Figure
+# 10.1 box 15): logits = cap * tanh(l * scale / cap).
+LOGIT_SCALE, SOFTCAP = 0.196116, 20.0
 
 
 def run_lmhead(args, rank, world):
@@ -681,7 +807,6 @@ def run_lmhead(args, rank, world):
     and soft cap as its epilogue (muser_lm_head), 1.09 GB per step."""
     import torch
     import quantized_weight_streaming_q4_gb300 as mu
-    import oracle
     dist = None
     if world > 1:
         import torch.distributed as dist
@@ -698,7 +823,7 @@ def run_lmhead(args, rank, world):
     logits = torch.empty(VOCAB, dtype=torch.float32, device="cuda")
     stream = torch.cuda.current_stream()
     sh = stream.cuda_stream
-    scale, cap = oracle.LOGIT_SCALE, oracle.SOFTCAP
+    scale, cap = LOGIT_SCALE, SOFTCAP
 
     def step():
         r = L.muser_lm_head(14, W.data_ptr(), VOCAB, H, x.data_ptr(), 1, logits.data_ptr(), scale, cap, sh)
@@ -1066,20 +1191,19 @@ def run_reference(args, rank, world):
     if rank != 0:
         return None
     import oracle
-    Wg, Wu, Wd, rg, rd = _oracle_layer_sample(args.ref_frac)
-    x = synth.normal((1, H), seed=1)
-    mid = synth.normal((1, F), seed=2)
+    smp = _oracle_layer_sample(args.ref_frac)
     for _ in range(args.warmup):
-        _oracle_step(oracle, Wg, Wu, Wd, rg, rd, x, mid)
+        _oracle_step(oracle, smp)
     t0 = time.perf_counter()
     nbytes = 0
     for _ in range(args.steps):
-        nbytes += _oracle_step(oracle, Wg, Wu, Wd, rg, rd, x, mid)
+        nbytes += _oracle_step(oracle, smp)
     dt = time.perf_counter() - t0
     gbs = nbytes / dt / 1e9
     M = 16 if args.workload == "stack52_m16" else 1
-    sample = (f"each step: fp64 oracle over the first {args.ref_frac:.3f} of the rows of one layer's "
-              f"gate/up/down, {nbytes / args.steps / 1e6:.1f} MB of weights, M=1")
+    sample = (f"each step: the fp64 oracle over one layer's path (input rms_norm, the first {args.ref_frac:.3f} "
+              f"of the gate/up rows + SiLU and of the down rows, the dual-eps tail), "
+              f"{nbytes / args.steps / 1e6:.1f} MB of weights, M=1")
     return {
         "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3),
@@ -1108,6 +1232,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--ref-frac", type=float, default=0.0625)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-sub", action="store_true", help="skip the M = 16 sub-result of the default workload")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
