@@ -41,6 +41,10 @@
  *  - Activation rows: M is the number of activation rows (1 for one-token
  *    decode, up to MUSER_MAX_M = 16 for the speculative-verify shape,
  *    Ch 10 §10.1 MAX_DFLASH_BLOCK).
+ *  - Scratch: calls that take caller scratch want it zero-filled before its
+ *    first use and leave it zero-filled after every call that completes.  A
+ *    kernel that gives up a bounded wait (muser_device_status() non-zero)
+ *    may leave counters in it: zero-fill it again before reusing it.
  */
 #ifndef MUSER_H
 #define MUSER_H
@@ -52,8 +56,11 @@
 extern "C" {
 #endif
 
-#define MUSER_ABI_VERSION 1
+#define MUSER_ABI_VERSION 2
 #define MUSER_MAX_M 16
+/* Scratch of the fused layer-boundary calls (muser_ffn_gate_up_silu_tail,
+ * muser_qmatvec_group_tail): the blocks' completion ticket. */
+#define MUSER_BOUNDARY_SCRATCH_BYTES 256u
 
 /* ggml type ids, informational */
 typedef enum { MUSER_Q4_K = 12, MUSER_Q5_K = 13, MUSER_Q6_K = 14 } muser_qtype;
@@ -207,13 +214,17 @@ int muser_qmatvec_group(int qtype, int n, const void* const* W, const int64_t* r
  *   the group on its output: as muser_fused_residual_dual_rmsnorm (src =
  *   projected, out = x_out, n = cols) followed by muser_qmatvec_group with
  *   x = x_out.  With one row of x and Q4_K the tail runs inside the group's
- *   launch, every block for itself.  projected, residual, x_out: device f32
+ *   launch, every block for itself; the block that takes the last ticket in
+ *   `scratch` writes the updated residual and x_out, as in
+ *   muser_ffn_gate_up_silu_tail.  projected, residual, x_out: device f32
  *   [M*cols], distinct; w1, w2: device f32 [cols]; cols % 4 == 0;
- *   eps1, eps2 > 0.
+ *   eps1, eps2 > 0; scratch: MUSER_BOUNDARY_SCRATCH_BYTES or more of
+ *   zero-filled caller memory, as for muser_ffn_gate_up_silu_tail.
  */
 int muser_qmatvec_group_tail(int qtype, int n, const void* const* W, const int64_t* rows, int64_t cols,
                              const float* projected, float* residual, const float* w1, const float* w2,
-                             float eps1, float eps2, float* x_out, int M, float* const* y, void* stream);
+                             float eps1, float eps2, float* x_out, int M, float* const* y, void* scratch,
+                             size_t scratch_bytes, void* stream);
 
 /*
  * muser_scale_softcap -- logits[i] = cap * tanh(logits[i] * scale / cap), in
@@ -249,16 +260,25 @@ int muser_lm_head(int qtype, const void* W, int64_t vocab, int64_t hidden, const
  *   residual and x_out are binary32 values.  For one row of x with a short
  *   enough row (hidden <= 6656 for Q4_K gate/up) the tail runs inside the
  *   gate/up kernel, so the layer boundary costs no separate launch; other
- *   shapes run the two calls.
+ *   shapes run the two calls.  Inside the kernel every block computes the
+ *   tail for itself from the residual; the residual is updated in place, so
+ *   each block takes a ticket in `scratch` once it has read the row, and the
+ *   block that takes the last ticket writes the updated residual and x_out
+ *   (no block can overwrite the row while another still has to read it).
  *   projected, residual, x_out: device f32 [M*hidden] (residual in/out,
  *   x_out output; the three must be distinct); w1, w2: device f32 [hidden];
  *   Wg, Wu: device matrices [ffn x hidden]; mid: device f32 [M*ffn].
+ *   scratch: device memory of at least MUSER_BOUNDARY_SCRATCH_BYTES bytes,
+ *   16-byte aligned, owned by the caller, zero-filled before its first use
+ *   and left zero-filled by every call; calls that can run at the same time
+ *   must not share it.
  *   hidden % 4 == 0; eps1, eps2 > 0.  Fail-closed like the two calls.
  */
 int muser_ffn_gate_up_silu_tail(int qtype, const void* Wg, const void* Wu, int64_t ffn,
                                 int64_t hidden, const float* projected, float* residual,
                                 const float* w1, const float* w2, float eps1, float eps2,
-                                float* x_out, int M, float* mid, void* stream);
+                                float* x_out, int M, float* mid, void* scratch, size_t scratch_bytes,
+                                void* stream);
 
 /* Scratch bytes muser_qmatvec_residual_dual_rmsnorm should get: 1 KiB for the
  * one-row kernel (its completion ticket, then one sum of projected^2 per
@@ -320,6 +340,13 @@ int muser_qmatvec_residual_dual_rmsnorm(int qtype, const void* Wdown, int64_t hi
  *   on the GPU (on streams with no ordering between them) race on it and
  *   give wrong results: issue them on one stream, or order them with events.
  *
+ *   With one row of x the down projection and the tail run on the same
+ *   one-token kernel as muser_qmatvec_residual_dual_rmsnorm; the tail then
+ *   takes one more pass over the row, since the array has no room for the
+ *   blocks' partial sums.  With 2..16 rows the tensor-core kernel runs with
+ *   whole 128-row tiles per SM (its even split over every SM needs partial
+ *   sums the array has no room for), then the tail per row.
+ *
  *   Other arguments, alignment and errors as muser_qmatvec_residual_dual_rmsnorm.
  */
 int muser_qmatvec_residual_dual_rmsnorm_static(int qtype, const void* Wdown, int64_t hidden,
@@ -345,9 +372,16 @@ typedef struct {
     int32_t down_qtype;
 } muser_ffn_layer;
 
-/* Bytes of workspace muser_ffn_block / muser_ffn_stack need: two normed-input
- * buffers, the FFN intermediate, the projected buffer and the tail scratch. */
+/* Bytes of workspace muser_ffn_stack needs: two normed-input buffers, the
+ * FFN intermediate, the projected buffer, a second residual buffer, the
+ * one-launch stack's synchronisation words and input records, and the tail
+ * scratch. */
 size_t muser_ffn_workspace_bytes(int64_t hidden, int64_t ffn, int M);
+
+/* Number of kernel launches one muser_ffn_stack call with these arguments
+ * makes (1 when the whole stack runs as one persistent launch); -1 for
+ * arguments the call would reject outright. */
+int muser_ffn_stack_launches(const muser_ffn_layer* layers, int n_layers, int64_t hidden, int64_t ffn, int M);
 
 /*
  * muser_ffn_stack -- `n_layers` decode-FFN layers over M residual rows
@@ -360,6 +394,17 @@ size_t muser_ffn_workspace_bytes(int64_t hidden, int64_t ffn, int M);
  *   workspace: device memory of muser_ffn_workspace_bytes(hidden, ffn, M)
  *   bytes, 16-byte aligned, zero-filled before its first use.
  *   n_layers == 1 is one decode-FFN block.
+ *   One row of x with Q4_K gate/up and Q6_K down (up to 128 layers, hidden up
+ *   to 6656, ffn a multiple of 512 up to 24576) runs as one persistent
+ *   kernel: one block per SM, launched cooperatively so that every block is
+ *   resident; each block streams every layer's weights through one ring of
+ *   shared-memory stages, and its compute warps wait at grid barriers
+ *   (bounded in time) only for the activations each phase needs.  The
+ *   residual is relayed through a second buffer in the workspace, so no block
+ *   overwrites a row another block still reads; the result is left in
+ *   `residual`.  The call also clears a few synchronisation words of the
+ *   workspace on `stream` before the kernel.  Other shapes run one launch per
+ *   projection.
  */
 int muser_ffn_stack(const muser_ffn_layer* layers, int n_layers, const float* entry_norm,
                     int64_t hidden, int64_t ffn, int M, float* residual, float* out,
@@ -453,6 +498,17 @@ int muser_sync(void* stream, int timeout_ms);
  *   GPU.
  */
 int muser_debug_spin(int64_t microseconds, void* stream);
+
+/*
+ * muser_debug_occupy -- enqueue `ctas` (1..4096) blocks that each hold 160 KB
+ *   of shared memory, so that no block of this library's weight-streaming
+ *   kernels fits beside one on the same SM, and busy-wait `microseconds`
+ *   (0..10 s) on the GPU's global timer.  Bounded by construction.  Run on
+ *   another stream, it keeps SMs busy while a kernel under test starts, so
+ *   that some of that kernel's blocks start late: the tests use it to check
+ *   that no block depends on when the others start.
+ */
+int muser_debug_occupy(int ctas, int64_t microseconds, void* stream);
 
 /* Number of SMs of the current device (for reports); -1 on error. */
 int muser_device_sm_count(void);

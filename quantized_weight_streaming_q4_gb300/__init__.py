@@ -25,8 +25,8 @@ __all__ = [
     "muser_lm_head",
     "muser_fused_residual_dual_rmsnorm", "muser_scratch_bytes",
     "muser_qmatvec_residual_dual_rmsnorm", "muser_qmatvec_residual_dual_rmsnorm_static",
-    "MUSER_STATIC_SCRATCH_BYTES", "FfnLayer", "muser_ffn_workspace_bytes",
-    "muser_ffn_stack", "KvPlane", "muser_kv_ring_write", "muser_kv_snapshot", "muser_kv_restore", "muser_sync", "muser_debug_spin",
+    "MUSER_STATIC_SCRATCH_BYTES", "MUSER_BOUNDARY_SCRATCH_BYTES", "FfnLayer", "muser_ffn_workspace_bytes", "muser_ffn_stack_launches",
+    "muser_ffn_stack", "KvPlane", "muser_kv_ring_write", "muser_kv_snapshot", "muser_kv_restore", "muser_sync", "muser_debug_spin", "muser_debug_occupy",
     "muser_device_sm_count", "muser_device_status",
 ]
 
@@ -35,6 +35,7 @@ MUSER_Q5_K = 13
 MUSER_Q6_K = 14
 QTYPES = {"q4_k": MUSER_Q4_K, "q5_k": MUSER_Q5_K, "q6_k": MUSER_Q6_K}
 MUSER_STATIC_SCRATCH_BYTES = 1 << 20
+MUSER_BOUNDARY_SCRATCH_BYTES = 256
 BLOCK_BYTES = {MUSER_Q4_K: 144, MUSER_Q5_K: 176, MUSER_Q6_K: 210}
 STATUS = {0: "MUSER_OK", -1: "MUSER_ERR_INVALID_ARG", -2: "MUSER_ERR_UNSUPPORTED",
           -3: "MUSER_ERR_MISALIGNED", -4: "MUSER_ERR_CACHE_DISCONTINUITY", -5: "MUSER_ERR_CUDA",
@@ -100,11 +101,11 @@ def lib():
             "muser_ffn_gate_up_silu": (I, [I, P, P, I64, I64, P, I, P, P]),
             "muser_gate_up_scratch_bytes": (SZ, [I, I64, I64, I]),
             "muser_ffn_gate_up_silu_scratch": (I, [I, P, P, I64, I64, P, I, P, P, SZ, P]),
-            "muser_ffn_gate_up_silu_tail": (I, [I, P, P, I64, I64, P, P, P, P, F, F, P, I, P, P]),
+            "muser_ffn_gate_up_silu_tail": (I, [I, P, P, I64, I64, P, P, P, P, F, F, P, I, P, P, SZ, P]),
             "muser_qmatvec_group": (I, [I, I, P, P, I64, P, I, P, P]),
             "muser_scale_softcap": (I, [P, I64, F, F, P]),
             "muser_lm_head": (I, [I, P, I64, I64, P, I, P, F, F, P]),
-            "muser_qmatvec_group_tail": (I, [I, I, P, P, I64, P, P, P, P, F, F, P, I, P, P]),
+            "muser_qmatvec_group_tail": (I, [I, I, P, P, I64, P, P, P, P, F, F, P, I, P, P, SZ, P]),
             "muser_fused_residual_dual_rmsnorm": (I, [P, P, P, P, P, I, I, F, F, P]),
             "muser_scratch_bytes": (SZ, [I64, I]),
             "muser_qmatvec_residual_dual_rmsnorm": (I, [I, P, I64, I64, P, I, P, P, P, P, P, F, F, P,
@@ -112,6 +113,7 @@ def lib():
             "muser_qmatvec_residual_dual_rmsnorm_static": (I, [I, P, I64, I64, P, I, P, P, P, P, F,
                                                                F, P]),
             "muser_ffn_workspace_bytes": (SZ, [I64, I64, I]),
+            "muser_ffn_stack_launches": (I, [ctypes.POINTER(FfnLayer), I, I64, I64, I]),
             "muser_ffn_stack": (I, [ctypes.POINTER(FfnLayer), I, P, I64, I64, I, P, P, F, F, P, SZ,
                                     P]),
             "muser_kv_ring_write": (I, [ctypes.POINTER(KvPlane), P, P, I64, I64,
@@ -120,6 +122,7 @@ def lib():
             "muser_kv_restore": (I, [ctypes.POINTER(KvPlane), P, P, I64, I64, P]),
             "muser_sync": (I, [P, I]),
             "muser_debug_spin": (I, [I64, P]),
+            "muser_debug_occupy": (I, [I, I64, P]),
             "muser_device_sm_count": (I, []),
             "muser_device_status": (ctypes.c_uint, [I]),
         }
@@ -226,11 +229,12 @@ def muser_ffn_gate_up_silu_scratch(qtype, Wg, Wu, ffn: int, hidden: int, x, M: i
 
 
 def muser_ffn_gate_up_silu_tail(qtype, Wg, Wu, ffn: int, hidden: int, projected, residual, w1, w2,
-                                eps1: float, eps2: float, x_out, M: int, mid, stream=None) -> None:
+                                eps1: float, eps2: float, x_out, M: int, mid, scratch,
+                                scratch_bytes: int = MUSER_BOUNDARY_SCRATCH_BYTES, stream=None) -> None:
     _check("muser_ffn_gate_up_silu_tail",
            lib().muser_ffn_gate_up_silu_tail(_qt(qtype), _ptr(Wg), _ptr(Wu), ffn, hidden, _ptr(projected),
                                              _ptr(residual), _ptr(w1), _ptr(w2), eps1, eps2, _ptr(x_out), M,
-                                             _ptr(mid), _stream(stream)))
+                                             _ptr(mid), _ptr(scratch), scratch_bytes, _stream(stream)))
 
 
 def muser_scale_softcap(logits, n: int, scale: float, cap: float, stream=None) -> None:
@@ -258,11 +262,13 @@ def muser_qmatvec_group(qtype, Ws, rows, cols: int, x, M: int, ys, stream=None) 
 
 
 def muser_qmatvec_group_tail(qtype, Ws, rows, cols: int, projected, residual, w1, w2, eps1: float, eps2: float,
-                             x_out, M: int, ys, stream=None) -> None:
+                             x_out, M: int, ys, scratch, scratch_bytes: int = MUSER_BOUNDARY_SCRATCH_BYTES,
+                             stream=None) -> None:
     n, wa, ra, ya = _group_arrays(Ws, rows, ys)
     _check("muser_qmatvec_group_tail",
            lib().muser_qmatvec_group_tail(_qt(qtype), n, wa, ra, cols, _ptr(projected), _ptr(residual), _ptr(w1),
-                                          _ptr(w2), eps1, eps2, _ptr(x_out), M, ya, _stream(stream)))
+                                          _ptr(w2), eps1, eps2, _ptr(x_out), M, ya, _ptr(scratch), scratch_bytes,
+                                          _stream(stream)))
 
 
 def muser_fused_residual_dual_rmsnorm(residual, src, out, w1, w2, n: int, M: int, eps1: float,
@@ -300,6 +306,13 @@ def muser_qmatvec_residual_dual_rmsnorm_static(qtype, Wdown, hidden: int, ffn: i
 
 def muser_ffn_workspace_bytes(hidden: int, ffn: int, M: int) -> int:
     return lib().muser_ffn_workspace_bytes(hidden, ffn, M)
+
+
+def muser_ffn_stack_launches(layers, hidden: int, ffn: int, M: int) -> int:
+    """Kernel launches one muser_ffn_stack call makes for these arguments."""
+    if not isinstance(layers, ctypes.Array):
+        layers = (FfnLayer * len(layers))(*layers)
+    return lib().muser_ffn_stack_launches(layers, len(layers), hidden, ffn, M)
 
 
 def muser_ffn_stack(layers, entry_norm, hidden: int, ffn: int, M: int, residual, out,
@@ -349,6 +362,10 @@ def muser_sync(stream=None, timeout_ms: int = -1) -> int:
 
 def muser_debug_spin(microseconds: int, stream=None) -> None:
     _check("muser_debug_spin", lib().muser_debug_spin(microseconds, _stream(stream)))
+
+
+def muser_debug_occupy(ctas: int, microseconds: int, stream=None) -> None:
+    _check("muser_debug_occupy", lib().muser_debug_occupy(ctas, microseconds, _stream(stream)))
 
 
 def muser_device_sm_count() -> int:

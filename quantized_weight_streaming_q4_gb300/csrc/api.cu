@@ -82,6 +82,15 @@ int check_f32(const char* fn, const char* name, const void* p) {
     return MUSER_OK;
 }
 
+// The ticket scratch of the fused layer-boundary calls.
+int check_boundary_scratch(const char* fn, const void* scratch, size_t scratch_bytes) {
+    MUSER_TRY(check_f32(fn, "scratch", scratch));
+    if (scratch_bytes < MUSER_BOUNDARY_SCRATCH_BYTES)
+        return set_error(MUSER_ERR_INVALID_ARG, "%s: scratch_bytes %zu < %u", fn, scratch_bytes,
+                         static_cast<unsigned>(MUSER_BOUNDARY_SCRATCH_BYTES));
+    return MUSER_OK;
+}
+
 int check_M(const char* fn, int M) {
     if (M < 1 || M > MUSER_MAX_M)
         return set_error(MUSER_ERR_INVALID_ARG, "%s: M = %d outside 1..%d", fn, M, MUSER_MAX_M);
@@ -113,6 +122,9 @@ struct Workspace {
     float* xb;
     float* mid;
     float* proj;
+    unsigned* ticket;  // the fused layer boundary's ticket (MUSER_BOUNDARY_SCRATCH_BYTES)
+    float* resid_ws;   // the one-launch stack's second residual buffer
+    void* mvs;         // the one-launch stack's sync words and input records
     void* scratch;     // down + tail scratch, down_scratch_bytes(hidden)
     void* gu_scratch;  // gate/up tensor-core scratch (null if the shape has none)
     size_t scratch_bytes;
@@ -132,6 +144,12 @@ Workspace carve(void* base, int64_t hidden, int64_t ffn, int M) {
     off += fb;
     w.proj = reinterpret_cast<float*>(p + off);
     off += hb;
+    w.ticket = reinterpret_cast<unsigned*>(p + off);
+    off += MUSER_BOUNDARY_SCRATCH_BYTES;
+    w.resid_ws = reinterpret_cast<float*>(p + off);
+    off += hb;
+    w.mvs = p + off;
+    off += round_up(mvs_scratch_bytes(hidden, ffn), 256);
     w.scratch = p + off;
     w.scratch_bytes = round_up(down_scratch_bytes(hidden, M), 256);
     off += w.scratch_bytes;
@@ -149,10 +167,12 @@ int down_tail_launch(int qtype, const void* Wdown, int64_t hidden, int64_t ffn, 
                      cudaStream_t s) {
     // One token: the CUDA-core kernel mv1 is measured faster than the
     // tensor-core kernel on this shape, so it takes M = 1.
-    const bool tc_fits = mvt_supported(qtype, 1, hidden, ffn, M) &&
-                         scratch_bytes >= kScratchBytes + mvt_scratch_bytes(qtype, 1, hidden, ffn, M);
-    if (M > 1 && tc_fits) {
-        // several rows: the tensor-core matvec into `projected`, then the tail per row
+    const bool tc_ok = mvt_supported(qtype, 1, hidden, ffn, M);
+    const bool tc_fits = tc_ok && scratch_bytes >= kScratchBytes + mvt_scratch_bytes(qtype, 1, hidden, ffn, M);
+    if (M > 1 && tc_ok) {
+        // several rows: the tensor-core matvec into `projected`, then the tail
+        // per row.  With room for its partial sums the matvec spreads its
+        // units over every SM; otherwise each SM takes whole row tiles.
         MvtArgs a{};
         a.W[0] = static_cast<const uint8_t*>(Wdown);
         a.W[1] = a.W[0];
@@ -161,7 +181,8 @@ int down_tail_launch(int qtype, const void* Wdown, int64_t hidden, int64_t ffn, 
         a.x = mid;
         a.M = M;
         a.y = projected;
-        MUSER_TRY(launch_mvt(qtype, kEpiStore, a, static_cast<uint8_t*>(scratch) + kScratchBytes, s));
+        MUSER_TRY(launch_mvt(qtype, kEpiStore, a, tc_fits ? static_cast<uint8_t*>(scratch) + kScratchBytes : nullptr,
+                             s));
         return launch_dual_tail(residual, projected, out, w1, w2, static_cast<int>(hidden), M, eps1, eps2, s);
     }
     if (kTensorCoreM1 && M == 1 && tc_fits) {
@@ -215,6 +236,14 @@ int down_tail_launch(int qtype, const void* Wdown, int64_t hidden, int64_t ffn, 
                             eps2, s);
 }
 
+// Whether muser_ffn_stack runs the whole stack in one persistent launch.
+bool stack_one_launch(const muser_ffn_layer* layers, int n_layers, int64_t hidden, int64_t ffn, int M) {
+    if (M != 1 || n_layers < 1) return false;
+    for (int l = 0; l < n_layers; ++l)
+        if (layers[l].gate_up_qtype != MUSER_Q4_K || layers[l].down_qtype != MUSER_Q6_K) return false;
+    return mvs_supported(MUSER_Q4_K, MUSER_Q6_K, hidden, ffn, n_layers, M);
+}
+
 // The tail of the previous layer fused into this layer's gate/up kernel.
 bool gate_up_tail_fused(int qtype, int64_t hidden, int M) {
     return M == 1 && mv1_tail_prologue_supported(qtype, hidden);
@@ -224,9 +253,11 @@ int gate_up_launch(int qtype, const void* Wg, const void* Wu, int64_t ffn, int64
                    const float* x, int M, float* mid, void* scratch, cudaStream_t s);
 
 // The layer boundary (previous tail, then gate/up) on validated arguments.
+// ticket: MUSER_BOUNDARY_SCRATCH_BYTES of zero-filled caller scratch.
 int gate_up_tail_launch(int qtype, const void* Wg, const void* Wu, int64_t ffn, int64_t hidden,
                         const float* projected, float* residual, const float* w1, const float* w2,
-                        float eps1, float eps2, float* x_out, int M, float* mid, cudaStream_t s) {
+                        float eps1, float eps2, float* x_out, int M, float* mid, unsigned* ticket,
+                        cudaStream_t s) {
     if (gate_up_tail_fused(qtype, hidden, M)) {
         Mv1Args a{};
         a.W[0] = static_cast<const uint8_t*>(Wg);
@@ -241,6 +272,7 @@ int gate_up_tail_launch(int qtype, const void* Wg, const void* Wu, int64_t ffn, 
         a.w2 = w2;
         a.eps1 = eps1;
         a.eps2 = eps2;
+        a.xticket = ticket;
         return launch_mv1(qtype, 2, kEpiSiluMul, a, s, kXTail);
     }
     MUSER_TRY(launch_dual_tail(residual, projected, x_out, w1, w2, static_cast<int>(hidden), M, eps1, eps2, s));
@@ -481,7 +513,8 @@ int muser_ffn_gate_up_silu_scratch(int qtype, const void* Wg, const void* Wu, in
 int muser_ffn_gate_up_silu_tail(int qtype, const void* Wg, const void* Wu, int64_t ffn,
                                 int64_t hidden, const float* projected, float* residual,
                                 const float* w1, const float* w2, float eps1, float eps2,
-                                float* x_out, int M, float* mid, void* stream) {
+                                float* x_out, int M, float* mid, void* scratch, size_t scratch_bytes,
+                                void* stream) {
     clear_error();
     const char* fn = "muser_ffn_gate_up_silu_tail";
     MUSER_TRY(check_matrix(fn, qtype, Wg, ffn, hidden));
@@ -497,8 +530,9 @@ int muser_ffn_gate_up_silu_tail(int qtype, const void* Wg, const void* Wu, int64
     if (!(eps1 > 0.0f) || !(eps2 > 0.0f)) return set_error(MUSER_ERR_INVALID_ARG, "%s: eps must be > 0", fn);
     if (x_out == residual || x_out == projected || projected == residual)
         return set_error(MUSER_ERR_INVALID_ARG, "%s: projected, residual and x_out must be distinct", fn);
+    MUSER_TRY(check_boundary_scratch(fn, scratch, scratch_bytes));
     return gate_up_tail_launch(qtype, Wg, Wu, ffn, hidden, projected, residual, w1, w2, eps1, eps2,
-                               x_out, M, mid, as_stream(stream));
+                               x_out, M, mid, static_cast<unsigned*>(scratch), as_stream(stream));
 }
 
 // Validation shared by the two group calls.
@@ -519,7 +553,8 @@ static int check_group(const char* fn, int qtype, int n, const void* const* W, c
 // 16-byte units) and the one-token kernel fit; otherwise one call per matrix.
 static int group_launch(int qtype, int n, const void* const* W, const int64_t* rows, int64_t cols, const float* x,
                         int M, float* const* y, const float* projected, float* residual, const float* w1,
-                        const float* w2, float eps1, float eps2, float* x_out, cudaStream_t s) {
+                        const float* w2, float eps1, float eps2, float* x_out, unsigned* ticket,
+                        cudaStream_t s) {
     const bool tail = projected != nullptr;
     const bool fused = M == 1 && qtype == MUSER_Q4_K &&
                        (tail ? mv1_tail_prologue_supported(qtype, cols) : mv1_supported(qtype, cols));
@@ -544,6 +579,7 @@ static int group_launch(int qtype, int n, const void* const* W, const int64_t* r
             a.w2 = w2;
             a.eps1 = eps1;
             a.eps2 = eps2;
+            a.xticket = ticket;
         }
         return launch_mv1(qtype, 1, kEpiStore, a, s, tail ? kXTail : kXMemory);
     }
@@ -562,12 +598,13 @@ int muser_qmatvec_group(int qtype, int n, const void* const* W, const int64_t* r
     const char* fn = "muser_qmatvec_group";
     MUSER_TRY(check_group(fn, qtype, n, W, rows, cols, x, M, y));
     return group_launch(qtype, n, W, rows, cols, x, M, y, nullptr, nullptr, nullptr, nullptr, 0.f, 0.f, nullptr,
-                        as_stream(stream));
+                        nullptr, as_stream(stream));
 }
 
 int muser_qmatvec_group_tail(int qtype, int n, const void* const* W, const int64_t* rows, int64_t cols,
                              const float* projected, float* residual, const float* w1, const float* w2, float eps1,
-                             float eps2, float* x_out, int M, float* const* y, void* stream) {
+                             float eps2, float* x_out, int M, float* const* y, void* scratch, size_t scratch_bytes,
+                             void* stream) {
     clear_error();
     const char* fn = "muser_qmatvec_group_tail";
     MUSER_TRY(check_group(fn, qtype, n, W, rows, cols, x_out, M, y));
@@ -579,8 +616,9 @@ int muser_qmatvec_group_tail(int qtype, int n, const void* const* W, const int64
     if (!(eps1 > 0.0f) || !(eps2 > 0.0f)) return set_error(MUSER_ERR_INVALID_ARG, "%s: eps must be > 0", fn);
     if (x_out == residual || x_out == projected || projected == residual)
         return set_error(MUSER_ERR_INVALID_ARG, "%s: projected, residual and x_out must be distinct", fn);
+    MUSER_TRY(check_boundary_scratch(fn, scratch, scratch_bytes));
     return group_launch(qtype, n, W, rows, cols, nullptr, M, y, projected, residual, w1, w2, eps1, eps2, x_out,
-                        as_stream(stream));
+                        static_cast<unsigned*>(scratch), as_stream(stream));
 }
 
 int muser_scale_softcap(float* logits, int64_t n, float scale, float cap, void* stream) {
@@ -715,6 +753,19 @@ size_t muser_ffn_workspace_bytes(int64_t hidden, int64_t ffn, int M) {
     return carve(nullptr, hidden, ffn, M).total;
 }
 
+int muser_ffn_stack_launches(const muser_ffn_layer* layers, int n_layers, int64_t hidden, int64_t ffn, int M) {
+    clear_error();
+    if (layers == nullptr || n_layers < 1 || M < 1 || M > MUSER_MAX_M) return -1;
+    if (stack_one_launch(layers, n_layers, hidden, ffn, M)) return 1;
+    bool fused = true;
+    for (int l = 0; l < n_layers && fused; ++l)
+        fused = gate_up_tail_fused(layers[l].gate_up_qtype, hidden, M) && mv1_supported(layers[l].down_qtype, ffn);
+    // the entry norm, two kernels per layer, and (fused boundaries) the last tail;
+    // with several rows the down projection and its tail are two launches
+    if (fused) return 2 + 2 * n_layers;
+    return 1 + (M > 1 ? 3 : 2) * n_layers;
+}
+
 int muser_ffn_stack(const muser_ffn_layer* layers, int n_layers, const float* entry_norm,
                     int64_t hidden, int64_t ffn, int M, float* residual, float* out,
                     float eps_norm, float eps_post, void* workspace, size_t workspace_bytes,
@@ -744,6 +795,29 @@ int muser_ffn_stack(const muser_ffn_layer* layers, int n_layers, const float* en
         MUSER_TRY(check_f32(fn, "next_norm", L.next_norm));
     }
     cudaStream_t s = as_stream(stream);
+    if (stack_one_launch(layers, n_layers, hidden, ffn, M)) {
+        // One row of x, Q4_K gate/up and Q6_K down: the whole stack in one
+        // persistent launch (mvs.cu).
+        MvsArgs a{};
+        a.nl = n_layers;
+        a.hidden = static_cast<int>(hidden);
+        a.ffn = static_cast<int>(ffn);
+        a.eps_norm = eps_norm;
+        a.eps_post = eps_post;
+        a.w_in = entry_norm;
+        a.resid = residual;
+        a.resid_ws = ws.resid_ws;
+        a.out = out;
+        a.proj = ws.proj;
+        for (int l = 0; l < n_layers; ++l) {
+            a.layer[l].wg = static_cast<const uint8_t*>(layers[l].w_gate);
+            a.layer[l].wu = static_cast<const uint8_t*>(layers[l].w_up);
+            a.layer[l].wd = static_cast<const uint8_t*>(layers[l].w_down);
+            a.layer[l].w1 = layers[l].post_norm;
+            a.layer[l].w2 = layers[l].next_norm;
+        }
+        return launch_mvs(a, ws.mvs, s);
+    }
     MUSER_TRY(launch_rms_norm(residual, entry_norm, ws.xa, static_cast<int>(hidden), M, eps_norm, s));
     // One row of x: each layer's tail runs in the next layer's gate/up kernel
     // and the down projection only stores `projected`; the last tail runs on
@@ -759,7 +833,8 @@ int muser_ffn_stack(const muser_ffn_layer* layers, int n_layers, const float* en
             } else {
                 const muser_ffn_layer& P = layers[l - 1];
                 MUSER_TRY(gate_up_tail_launch(L.gate_up_qtype, L.w_gate, L.w_up, ffn, hidden, ws.proj, residual,
-                                              P.post_norm, P.next_norm, eps_post, eps_norm, ws.xb, M, ws.mid, s));
+                                              P.post_norm, P.next_norm, eps_post, eps_norm, ws.xb, M, ws.mid,
+                                              ws.ticket, s));
             }
             Mv1Args d{};
             d.W[0] = static_cast<const uint8_t*>(L.w_down);
@@ -950,6 +1025,13 @@ int muser_debug_spin(int64_t microseconds, void* stream) {
     if (microseconds < 0 || microseconds > 10 * 1000 * 1000)
         return set_error(MUSER_ERR_INVALID_ARG, "muser_debug_spin: 0..10 s only");
     return launch_spin(microseconds, as_stream(stream));
+}
+
+int muser_debug_occupy(int ctas, int64_t microseconds, void* stream) {
+    clear_error();
+    if (ctas < 1 || ctas > 4096 || microseconds < 0 || microseconds > 10 * 1000 * 1000)
+        return set_error(MUSER_ERR_INVALID_ARG, "muser_debug_occupy: 1..4096 blocks for 0..10 s only");
+    return launch_occupy(ctas, microseconds, as_stream(stream));
 }
 
 int muser_device_sm_count(void) { return sm_count(); }

@@ -242,6 +242,17 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
     return false;
 }
 
+// Atomic add at GPU scope with acquire-release semantics: the calling
+// thread's earlier accesses (and those ordered before them by a block or warp
+// barrier) are visible to a thread that later observes the result, and
+// accesses other threads released before the values this one observes are
+// visible to the caller afterwards.  Returns the old value.
+__device__ __forceinline__ unsigned atom_add_acq_rel_gpu(unsigned* p, unsigned v) {
+    unsigned old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+
 // Programmatic dependent launch controls (no-ops without the launch attribute).
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_launch_dependents() {

@@ -28,6 +28,9 @@ struct Mv1Args {
     float scale, cap;  // soft-cap epilogue: y = cap * tanh(y * scale / cap)
     unsigned* ticket;
     float* tail_part;  // per-block sums of projected^2 (kMv1TailParts floats), or null
+    // x from the previous layer's tail (kXTail): the blocks' tickets; the block
+    // that takes the last one writes the updated residual and re-zeroes it
+    unsigned* xticket;
     // Row segments (Q4_K, one matrix, store epilogue; Q4_K rows are whole 16-byte units):
     // rows [seg0[s], seg0[s+1]) of the virtual matrix are rows of segW[s],
     // and their results go to segY[s].  nseg == 0: W[0] and y0 as usual.
@@ -94,6 +97,38 @@ int launch_mvt(int qtype, int epi, MvtArgs a, void* scratch, cudaStream_t s);
 // Device address of the status word (mv1.cu), for kernels in other units.
 unsigned* device_status_word();
 
+// The one-token decode-FFN stack as one persistent kernel (mvs.cu): every
+// layer's gate/up (Q4_K), down (Q6_K) and dual-eps tail for one row of x.
+constexpr int kMvsMaxLayers = 128;
+struct MvsLayer {
+    const uint8_t* wg;
+    const uint8_t* wu;
+    const uint8_t* wd;
+    const float* w1;  // post-FFN norm
+    const float* w2;  // next norm (the next layer's input norm, or the output norm)
+};
+struct MvsArgs {
+    int nl;
+    int hidden, ffn;
+    float eps_norm, eps_post;
+    const float* w_in;  // entry norm
+    float* resid;       // caller's residual row (in/out)
+    float* resid_ws;    // the relay's other residual buffer
+    float* out;         // the last layer's next-norm output
+    float* proj;        // [hidden]
+    // filled by the launcher
+    unsigned* sync;     // grid barrier count, abort flag
+    float4* xperm;      // mid, slice-major for the down phase's threads
+    unsigned* status;   // device status word
+    int RSg, RSd, ns, np, part_stride, part_off, ring_off, HPd, TGd;
+    uint32_t sb, sbm_g;
+    MvsLayer layer[kMvsMaxLayers];
+};
+bool mvs_supported(int gu_qtype, int down_qtype, int64_t hidden, int64_t ffn, int n_layers, int M);
+// Scratch of launch_mvs: its synchronisation words and the slice-major mid.
+size_t mvs_scratch_bytes(int64_t hidden, int64_t ffn);
+int launch_mvs(MvsArgs a, void* scratch, cudaStream_t s);
+
 // misc.cu
 int launch_dequantize(int qtype, const uint8_t* W, int64_t rows, int64_t cols, float* out,
                       cudaStream_t s);
@@ -112,5 +147,9 @@ int launch_kv_window(uint16_t* key, uint16_t* value, uint16_t* k_rows, uint16_t*
                      int64_t kv_dim, int64_t head_dim, int head_major, int64_t capacity,
                      int64_t phys0, int64_t count, bool to_plane, cudaStream_t s);
 int launch_spin(int64_t microseconds, cudaStream_t s);
+// `ctas` blocks that each hold kOccupySmemBytes of shared memory (one block
+// per SM) and busy-wait `microseconds` on the global timer.
+constexpr int kOccupySmemBytes = 160 * 1024;
+int launch_occupy(int ctas, int64_t microseconds, cudaStream_t s);
 
 }  // namespace muser

@@ -278,6 +278,18 @@ __global__ void spin_kernel(uint64_t ns) {
     } while (t - t0 < ns);
 }
 
+// Holds its SM (through its shared memory) for `ns` of global time.
+__global__ void occupy_kernel(uint64_t ns) {
+    extern __shared__ uint8_t hold[];
+    uint64_t t0, t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
+    do {
+        __nanosleep(1000);
+        asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    } while (t - t0 < ns);
+    if (t == 0) hold[threadIdx.x] = 0;  // never true: keeps the allocation referenced
+}
+
 }  // namespace
 
 int launch_dequantize(int qtype, const uint8_t* W, int64_t rows, int64_t cols, float* out,
@@ -365,6 +377,14 @@ int launch_kv_window(uint16_t* key, uint16_t* value, uint16_t* k_rows, uint16_t*
         kv_window_kernel<false><<<g, bs, 0, s>>>(key, value, k_rows, v_rows, kv_dim, head_dim,
                                                    head_major, capacity, phys0, count);
     return check_launch("kv_window");
+}
+
+int launch_occupy(int ctas, int64_t microseconds, cudaStream_t s) {
+    cudaError_t e = cudaFuncSetAttribute(occupy_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kOccupySmemBytes);
+    if (e != cudaSuccess) return cuda_fail(e, "occupy: cudaFuncSetAttribute");
+    occupy_kernel<<<ctas, 32, kOccupySmemBytes, s>>>(static_cast<uint64_t>(microseconds) * 1000ull);
+    return check_launch("occupy");
 }
 
 int launch_spin(int64_t microseconds, cudaStream_t s) {

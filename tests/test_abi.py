@@ -39,7 +39,7 @@ def test_every_declared_symbol_is_exported(L):
 
 @needs_nvcc
 def test_sizes_and_version(L):
-    assert mu.muser_version() == 1
+    assert mu.muser_version() == 2
     assert mu.muser_block_bytes("q4_k") == 144 and mu.muser_block_bytes("q6_k") == 210
     assert mu.muser_block_bytes("q5_k") == 176 and mu.muser_block_bytes(13) == 176
     assert mu.muser_matrix_bytes("q5_k", 6656, 19968) == 6656 * 78 * 176
@@ -186,9 +186,14 @@ def test_group_calls_fail_closed(L):
     assert g(12, 4, W, rows, 6656, FAKE * 6, 1, P3(FAKE * 2, FAKE * 3 + 4, FAKE * 4, FAKE * 5), None) == -3
     t = L.muser_qmatvec_group_tail
     args = (12, 4, W, rows, 6656)
-    assert t(*args, FAKE * 6, FAKE * 7, FAKE * 8, FAKE * 9, 1e-8, 1e-5, FAKE * 7, 1, y, None) == -1   # x_out == residual
-    assert t(*args, FAKE * 6, FAKE * 7, FAKE * 8, FAKE * 9, 0.0, 1e-5, FAKE * 10, 1, y, None) == -1   # eps1 = 0
-    assert t(*args, FAKE * 6, FAKE * 6, FAKE * 8, FAKE * 9, 1e-8, 1e-5, FAKE * 10, 1, y, None) == -1  # projected == residual
+    S = (FAKE * 11, 256)                                                 # the ticket scratch
+    assert t(*args, FAKE * 6, FAKE * 7, FAKE * 8, FAKE * 9, 1e-8, 1e-5, FAKE * 7, 1, y, *S, None) == -1   # x_out == residual
+    assert t(*args, FAKE * 6, FAKE * 7, FAKE * 8, FAKE * 9, 0.0, 1e-5, FAKE * 10, 1, y, *S, None) == -1   # eps1 = 0
+    assert t(*args, FAKE * 6, FAKE * 6, FAKE * 8, FAKE * 9, 1e-8, 1e-5, FAKE * 10, 1, y, *S, None) == -1  # projected == residual
+    assert t(*args, FAKE * 6, FAKE * 7, FAKE * 8, FAKE * 9, 1e-8, 1e-5, FAKE * 10, 1, y, None, 256, None) == -1  # no scratch
+    assert t(*args, FAKE * 6, FAKE * 7, FAKE * 8, FAKE * 9, 1e-8, 1e-5, FAKE * 10, 1, y, FAKE * 11, 255, None) == -1
+    assert t(*args, FAKE * 6, FAKE * 7, FAKE * 8, FAKE * 9, 1e-8, 1e-5, FAKE * 10, 1, y, FAKE * 11 + 4, 256,
+             None) == -3                                                 # misaligned scratch
 
 
 @needs_nvcc
@@ -211,11 +216,15 @@ def test_scale_softcap_and_lm_head_fail_closed(L):
 def test_fused_layer_boundary_and_static_scratch_fail_closed(L):
     f = L.muser_ffn_gate_up_silu_tail
     base = (12, FAKE, FAKE * 2, 19968, 6656, FAKE * 3, FAKE * 4, FAKE * 5, FAKE * 6)
-    assert f(*base, 1e-8, 1e-5, FAKE * 4, 1, FAKE * 8, None) == -1   # x_out aliases the residual
-    assert f(*base, 1e-8, -1.0, FAKE * 7, 1, FAKE * 8, None) == -1   # eps2 < 0
-    assert f(*base, 1e-8, 1e-5, FAKE * 7, 0, FAKE * 8, None) == -1   # M = 0
+    S = (FAKE * 9, 256)                                              # the ticket scratch
+    assert f(*base, 1e-8, 1e-5, FAKE * 4, 1, FAKE * 8, *S, None) == -1   # x_out aliases the residual
+    assert f(*base, 1e-8, -1.0, FAKE * 7, 1, FAKE * 8, *S, None) == -1   # eps2 < 0
+    assert f(*base, 1e-8, 1e-5, FAKE * 7, 0, FAKE * 8, *S, None) == -1   # M = 0
     assert f(14, FAKE, FAKE * 2, 19968, 6656, FAKE * 3, FAKE * 4, FAKE * 5, FAKE * 6, 1e-8, 1e-5,
-             FAKE * 7, 1, FAKE * 8 + 4, None) == -3                   # misaligned mid
+             FAKE * 7, 1, FAKE * 8 + 4, *S, None) == -3                   # misaligned mid
+    assert f(*base, 1e-8, 1e-5, FAKE * 7, 1, FAKE * 8, None, 256, None) == -1        # no ticket scratch
+    assert f(*base, 1e-8, 1e-5, FAKE * 7, 1, FAKE * 8, FAKE * 9, 128, None) == -1    # too small
+    assert "scratch" in mu.muser_last_error()
     st = L.muser_qmatvec_residual_dual_rmsnorm_static
     # M * hidden above the static array's 262,080 floats
     assert st(14, FAKE, 65536, 19968, FAKE * 2, 16, FAKE * 3, FAKE * 4, FAKE * 5, FAKE * 6, 1e-8, 1e-5,
@@ -226,6 +235,9 @@ def test_fused_layer_boundary_and_static_scratch_fail_closed(L):
 @needs_nvcc
 def test_debug_spin_bound(L):
     assert L.muser_debug_spin(11 * 1000 * 1000, None) == -1
+    assert L.muser_debug_occupy(4, 11 * 1000 * 1000, None) == -1     # over 10 s
+    assert L.muser_debug_occupy(0, 1000, None) == -1                 # no blocks
+    assert L.muser_debug_occupy(5000, 1000, None) == -1              # too many blocks
 
 
 def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):

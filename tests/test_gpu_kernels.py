@@ -232,21 +232,35 @@ def test_ffn_gate_up_silu(M, with_scratch):
     assert_close(got, ref, f"gate_up_silu M={M}", scaled=True)
 
 
-@pytest.mark.parametrize("M,ffn", [(1, 19968), (1, 2001), (3, 2003)])
-def test_ffn_gate_up_silu_tail(M, ffn):
-    """The layer boundary: the previous tail then gate/up/SiLU.  One row of x
-    runs the tail inside the gate/up kernel (every block computes x, block 0
-    writes residual and x_out); M = 3 runs the two calls."""
-    hidden = 6656
+def boundary_case(M, ffn, hidden=6656):
+    """Inputs of the fused layer boundary: gate/up, a residual row, a large
+    projected row (as the down projection makes it) and the two norm weights."""
     Wg = synth.q4k_matrix(ffn, hidden, seed=40 + M, tensor=synth.T_GATE)
     Wu = synth.q4k_matrix(ffn, hidden, seed=40 + M, tensor=synth.T_UP)
     r = synth.normal((M, hidden), seed=41, tensor=synth.T_RESID)
     p = synth.normal((M, hidden), seed=41, tensor=synth.T_X) * np.float32(2.5e6)
     w1 = synth.norm_weight(hidden, seed=42, tensor=synth.T_W1)
     w2 = synth.norm_weight(hidden, seed=42, tensor=synth.T_W2)
+    return Wg, Wu, r, p, w1, w2
+
+
+def ticket_scratch():
+    return torch.zeros(mu.MUSER_BOUNDARY_SCRATCH_BYTES // 4, dtype=torch.int32, device="cuda")
+
+
+@pytest.mark.parametrize("M,ffn", [(1, 19968), (1, 2001), (3, 2003)])
+def test_ffn_gate_up_silu_tail(M, ffn):
+    """The layer boundary: the previous tail then gate/up/SiLU.  One row of x
+    runs the tail inside the gate/up kernel (every block computes x; the block
+    that takes the last ticket writes residual and x_out); M = 3 runs the two
+    calls."""
+    hidden = 6656
+    Wg, Wu, r, p, w1, w2 = boundary_case(M, ffn, hidden)
     rd, x_out, mid = dev(r), nan_like((M, hidden), extra=32), nan_like((M, ffn), extra=32)
+    tk = ticket_scratch()
     mu.muser_ffn_gate_up_silu_tail("q4_k", dev(Wg), dev(Wu), ffn, hidden, dev(p), rd, dev(w1), dev(w2),
-                                   1e-8, 1e-5, x_out, M, mid)
+                                   1e-8, 1e-5, x_out, M, mid, tk)
+    assert not host(tk).any(), "the ticket must be left zeroed"
     r_ref, x_ref = oracle.dual_tail(r, p, w1, w2, 1e-8, 1e-5)
     mid_ref = oracle.gate_up_silu("q4_k", Wg, Wu, ffn, hidden, x_ref)
     assert_close(host(rd).reshape(M, hidden), r_ref, "tail residual")
@@ -254,6 +268,79 @@ def test_ffn_gate_up_silu_tail(M, ffn):
     assert_close(host(mid[:M * ffn]).reshape(M, ffn), mid_ref, f"gate_up_silu after the tail M={M}", scaled=True)
     check_canary(x_out, M * hidden)
     check_canary(mid, M * ffn)
+    assert mu.muser_device_status() == 0
+
+
+def start_blocks_late(stream, ms=30):
+    """Keep all but 8 SMs busy for `ms` on another stream (bounded), then let
+    the host wait 5 ms so those blocks hold their SMs before anything else is
+    enqueued: a one-block-per-SM kernel enqueued next on `stream` starts 8
+    blocks at once and the rest about 25 ms later."""
+    import time
+    sms = mu.muser_device_sm_count()
+    busy = torch.cuda.Stream()
+    mu.muser_debug_occupy(1, 0, busy)       # loads the kernel before the timed use
+    busy.synchronize()
+    torch.cuda.synchronize()
+    mu.muser_debug_occupy(max(1, sms - 8), ms * 1000, busy)
+    time.sleep(0.005)
+    return busy
+
+
+@pytest.mark.parametrize("reps", [2])
+def test_ffn_gate_up_silu_tail_blocks_start_late(reps):
+    """The fused boundary updates the residual in place while every block reads
+    it.  With most blocks starting ~25 ms after the first ones, a block that
+    read the already-updated row would add the tail twice: residual, x_out and
+    mid must still equal the oracle's (Ch 19 §19.4: one update of `hidden`).
+    Two calls in a row check that the ticket is left at zero."""
+    M, ffn, hidden = 1, 19968, 6656
+    Wg, Wu, r, p, w1, w2 = boundary_case(M, ffn, hidden)
+    r_ref, x_ref = oracle.dual_tail(r, p, w1, w2, 1e-8, 1e-5)
+    mid_ref = oracle.gate_up_silu("q4_k", Wg, Wu, ffn, hidden, x_ref)
+    dWg, dWu, dp, dw1, dw2 = dev(Wg), dev(Wu), dev(p), dev(w1), dev(w2)
+    tk = ticket_scratch()
+    s = torch.cuda.current_stream()
+    for call in range(reps):
+        rd, x_out, mid = dev(r), nan_like((M, hidden)), nan_like((M, ffn))
+        busy = start_blocks_late(s)
+        mu.muser_ffn_gate_up_silu_tail("q4_k", dWg, dWu, ffn, hidden, dp, rd, dw1, dw2, 1e-8, 1e-5, x_out, M,
+                                       mid, tk, stream=s)
+        torch.cuda.synchronize()
+        busy.synchronize()
+        assert_close(host(rd).reshape(M, hidden), r_ref, f"residual with late blocks (call {call})")
+        assert_close(host(x_out).reshape(M, hidden), x_ref, f"x_out with late blocks (call {call})")
+        assert_close(host(mid).reshape(M, ffn), mid_ref, f"mid with late blocks (call {call})", scaled=True)
+        assert not host(tk).any(), "the ticket must be left zeroed"
+    assert mu.muser_device_status() == 0
+
+
+def test_group_tail_blocks_start_late():
+    """The attention-side group with the previous tail in its launch, under
+    the same late block starts: residual, x_out and the four projections."""
+    H = 6656
+    A = synth.attn_layer(2, H)
+    names, rows = ("Wq", "Wk", "Wv", "Wg"), (synth.Q_DIM, synth.KV_DIM, synth.KV_DIM, synth.Q_DIM)
+    r = synth.residual_rows(1, H, workload=synth.ATTN_WORKLOAD)
+    p = synth.normal((1, H), seed=8, workload=synth.ATTN_WORKLOAD, tensor=synth.T_X) * np.float32(3e5)
+    w1 = synth.norm_weight(H, seed=8, workload=synth.ATTN_WORKLOAD, tensor=synth.T_W1)
+    w2 = synth.norm_weight(H, seed=8, workload=synth.ATTN_WORKLOAD, tensor=synth.T_W2)
+    r_ref, x_ref = oracle.dual_tail(r, p, w1, w2, 1e-8, 1e-5)
+    rd, x_out = dev(r), nan_like((1, H))
+    ys = [nan_like((1, n)) for n in rows]
+    tk = ticket_scratch()
+    s = torch.cuda.current_stream()
+    busy = start_blocks_late(s)
+    mu.muser_qmatvec_group_tail("q4_k", [dev(A[n]) for n in names], rows, H, dev(p), rd, dev(w1), dev(w2),
+                                1e-8, 1e-5, x_out, 1, ys, tk, stream=s)
+    torch.cuda.synchronize()
+    busy.synchronize()
+    assert_close(host(rd).reshape(1, H), r_ref, "residual with late blocks")
+    assert_close(host(x_out).reshape(1, H), x_ref, "x_out with late blocks")
+    for name, n, y in zip(names, rows, ys):
+        assert_close(host(y).reshape(1, n), oracle.qmatvec("q4_k", A[name], n, H, x_ref),
+                     f"{name} with late blocks", scaled=True)
+    assert not host(tk).any()
     assert mu.muser_device_status() == 0
 
 

@@ -285,8 +285,10 @@ def test_attention_projection_group(M, with_tail):
         w1 = synth.norm_weight(H, seed=7, workload=synth.ATTN_WORKLOAD, tensor=synth.T_W1)
         w2 = synth.norm_weight(H, seed=7, workload=synth.ATTN_WORKLOAD, tensor=synth.T_W2)
         rd, x_out = dev(r), nan_like((M, H), extra=16)
+        tk = torch.zeros(mu.MUSER_BOUNDARY_SCRATCH_BYTES // 4, dtype=torch.int32, device="cuda")
         mu.muser_qmatvec_group_tail("q4_k", [dev(A[n]) for n in names], rows, H, dev(p), rd, dev(w1), dev(w2),
-                                    1e-8, 1e-5, x_out, M, ys)
+                                    1e-8, 1e-5, x_out, M, ys, tk)
+        assert not host(tk).any(), "the ticket must be left zeroed"
         r_ref, x = oracle.dual_tail(r, p, w1, w2, 1e-8, 1e-5)
         assert_close(host(rd).reshape(M, H), r_ref, "tail residual")
         assert_close(host(x_out[:M * H]).reshape(M, H), x, "tail x_out")
