@@ -54,9 +54,12 @@ METRIC = "weight-stream GB/s (% of GB300 HBM peak); decode FFN tokens/sec, 1 GPU
 
 # ncu DRAM traffic of the dominant kernel, per launch, with the source hash it
 # was captured on (profiles/ summary); reported as null once the kernel changed.
-NCU_TRAFFIC = {"kernel": "mv1_kernel<Q4_K,2,silu,tail>", "bytes_per_launch": 152691456,
-               "source_sha256": "2a67001274fe7c932b82811640311065d1e3047683baa036bed341cbff17a349",
-               "profile": "profiles/mv1_fused_gate_up_tail_q4k_and_down_q6k_m1.md"}
+# The capture ran 4 layers; the traffic per layer is the same, so the 52-layer
+# launch's figure is 13 x the captured launch's.
+NCU_TRAFFIC = {"kernel": "mvs_kernel<Q4_K,Q6_K>", "bytes_per_launch": 13 * 1038141088, "layers": 52,
+               "captured_layers": 4,
+               "source_sha256": "271e3a33d6eec3187f217ca15e32e10a376ee85ae6f84623f1ee544d39ef6b3d",
+               "profile": "profiles/mvs_stack_m1_4layers.md"}
 
 
 def _env_int(k, d):
@@ -111,14 +114,14 @@ def read_peaks():
         return 6800.0, "fallback"
 
 
-# Sources that define the one-token gate/up kernel (mv1): a change to any of
+# Sources that define the persistent stack kernel (mvs): a change to any of
 # them makes the recorded DRAM traffic stale.
-MV1_SOURCES = ("common.cuh", "kernels.cuh", "mv1.cu")
+MVS_SOURCES = ("common.cuh", "kernels.cuh", "mv1_core.cuh", "mvs.cu")
 
 
 def source_sha():
     h = hashlib.sha256()
-    for f in MV1_SOURCES:
+    for f in MVS_SOURCES:
         with open(os.path.join(ROOT, "quantized_weight_streaming_q4_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()
@@ -446,7 +449,8 @@ def run_native(args, rank, world):
         k_bytes, k_ms = gu_bytes, r["gu_ms"]
     achieved = k_bytes / (k_ms * 1e-3) / 1e9
     traffic = None
-    if M == 1 and NCU_TRAFFIC["bytes_per_launch"] and NCU_TRAFFIC["source_sha256"] == source_sha():
+    if (M == 1 and one_launch == 1 and nl == NCU_TRAFFIC["layers"] and
+            NCU_TRAFFIC["source_sha256"] == source_sha()):
         traffic = NCU_TRAFFIC["bytes_per_launch"]
     gbs = whole_job_gbs(world, weight_bytes, ms)
     result = {

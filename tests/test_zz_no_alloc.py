@@ -1,6 +1,7 @@
 """The down projection + dual-eps tail with the library's own fixed scratch
 (muser_qmatvec_residual_dual_rmsnorm_static) against the entry point that
-takes caller-owned scratch, through the C ABI, on two calls in a row.
+takes caller-owned scratch and against the oracle, through the C ABI, on two
+calls in a row.
 
 The file name sorts last, so in a full run these cases execute after every
 other GPU test has used the library in the same process; they also pass when
@@ -8,6 +9,7 @@ run alone in a fresh process."""
 import numpy as np
 import pytest
 
+import oracle
 import synth
 from tests.gpu_util import assert_close, dev, host, nan_like
 
@@ -49,6 +51,9 @@ def test_static_scratch_matches_caller_scratch(qtype, M, hidden, ffn):
                                            w1, w2, 1e-8, 1e-5, scratch, nscr)
     r_ref = host(r_ref).reshape(M, hidden).astype(np.float64)
     o_ref = host(o_ref).reshape(M, hidden).astype(np.float64)
+    # the oracle on the same intermediate row (Ch 19 §19.4-§19.5)
+    mid_h = host(mid).reshape(M, ffn)
+    _, r_orc, o_orc = oracle.down_tail(qtype, case["W"], hidden, ffn, mid_h, case["resid"], case["w1"], case["w2"])
 
     # two calls in a row on the same inputs: the second sees what the first
     # left in the shared array
@@ -58,6 +63,8 @@ def test_static_scratch_matches_caller_scratch(qtype, M, hidden, ffn):
                                                       1e-8, 1e-5)
         assert_close(host(r).reshape(M, hidden), r_ref, f"residual (call {call})")
         assert_close(host(o).reshape(M, hidden), o_ref, f"next-norm output (call {call})")
+        assert_close(host(r).reshape(M, hidden), r_orc, f"residual vs oracle (call {call})")
+        assert_close(host(o).reshape(M, hidden), o_orc, f"next-norm output vs oracle (call {call})")
     assert mu.muser_device_status() == 0
 
 
