@@ -219,7 +219,9 @@ class NativeStack:
         self.x = [torch.empty(M, H, dtype=torch.float32, device="cuda") for _ in range(2)]
         self.mid = torch.empty(M, F, dtype=torch.float32, device="cuda")
         self.proj = torch.empty(M, H, dtype=torch.float32, device="cuda")
-        self.ticket = torch.zeros(mu.MUSER_BOUNDARY_SCRATCH_BYTES // 4, dtype=torch.int32, device="cuda")
+        # the per-layer path relays the residual between two rows (each fused
+        # boundary reads one and writes the other through residual_out)
+        self.resid_b = torch.empty_like(self.resid)
         self.gu_scratch_bytes = mu.muser_gate_up_scratch_bytes(mu.MUSER_Q4_K, F, H, M)
         self.gu_scratch = torch.zeros(max(self.gu_scratch_bytes, 16) // 4, dtype=torch.float32, device="cuda")
         self.scratch_bytes = mu.muser_scratch_bytes(H, M)
@@ -274,11 +276,15 @@ class NativeStack:
 
     def _layers_m1(self, events=None):
         """One row of x as per-layer calls: the entry norm, then per layer
-        gate/up (with the previous layer's tail fused in, from layer 1) and the
-        plain down projection, then the last layer's tail."""
+        gate/up (with the previous layer's tail fused in, from layer 1, its
+        residual relayed to the other row) and the plain down projection, then
+        the last layer's tail, in place on the row the relay ended in, which it
+        copies back to self.resid when that is the other row."""
         L, M, sh = self.L, self.M, self.sh
         self._rc("rms_norm", L.muser_rms_norm(self.resid.data_ptr(), self.w_in.data_ptr(),
                                               self.x[0].data_ptr(), H, M, 1e-5, sh))
+        rows = (self.resid, self.resid_b)
+        cur = 0
         prev = None
         for l, d in enumerate(self.layers):
             ev = events.get(l) if events is not None else None
@@ -291,9 +297,10 @@ class NativeStack:
             else:
                 self._rc("gate_up_tail", L.muser_ffn_gate_up_silu_tail(
                     12, d["Wg"].data_ptr(), d["Wu"].data_ptr(), F, H, self.proj.data_ptr(),
-                    self.resid.data_ptr(), prev["w1"].data_ptr(), prev["w_next"].data_ptr(), 1e-8, 1e-5,
-                    self.x[1].data_ptr(), M, self.mid.data_ptr(), self.ticket.data_ptr(),
-                    self.mu.MUSER_BOUNDARY_SCRATCH_BYTES, sh))
+                    rows[cur].data_ptr(), rows[1 - cur].data_ptr(), prev["w1"].data_ptr(),
+                    prev["w_next"].data_ptr(), 1e-8, 1e-5, self.x[1].data_ptr(), M, self.mid.data_ptr(),
+                    None, 0, sh))
+                cur = 1 - cur
             if ev is not None:
                 ev[1].record(self.stream)
             self._rc("down", L.muser_qmatvec(14, d["Wd"].data_ptr(), H, F, self.mid.data_ptr(), M,
@@ -302,8 +309,10 @@ class NativeStack:
                 ev[2].record(self.stream)
             prev = d
         self._rc("tail", L.muser_fused_residual_dual_rmsnorm(
-            self.resid.data_ptr(), self.proj.data_ptr(), self.out.data_ptr(), prev["w1"].data_ptr(),
+            rows[cur].data_ptr(), self.proj.data_ptr(), self.out.data_ptr(), prev["w1"].data_ptr(),
             prev["w_next"].data_ptr(), H, M, 1e-8, 1e-5, sh))
+        if cur:
+            self.resid.copy_(self.resid_b)
 
 
 NOMINAL_HBM_GBS = 8000.0   # GB300 HBM3e, nominal (context beside the measured copy peak)
@@ -665,14 +674,19 @@ def run_attn(args, rank, world):
     nscr = max(mu.muser_qmatvec_scratch_bytes(12, r, c, M) for r, c in ((QD, H), (KVD, H), (H, QD)))
     scratch = torch.zeros(max(nscr, 16) // 4 + 64, dtype=torch.float32, device="cuda")
     outs4 = (q, k, v, g)
-    ticket = torch.zeros(mu.MUSER_BOUNDARY_SCRATCH_BYTES // 4, dtype=torch.int32, device="cuda")
+    # one row of x: each fused boundary reads the residual from one row and
+    # writes it to the other (residual_out); the step ends in the row it
+    # reached, which the next step starts from
+    rows_r = (resid, torch.empty_like(resid))
+    cur = [0]
 
     def split_mv(W, rows, cols, xin, y):
         rc("qmatvec_scratch", L.muser_qmatvec_scratch(12, W.data_ptr(), rows, cols, xin.data_ptr(), M, y.data_ptr(),
                                                       scratch.data_ptr(), nscr, sh))
 
     def step(events=None):
-        rc("rms_norm", L.muser_rms_norm(resid.data_ptr(), w_in.data_ptr(), x.data_ptr(), H, M, 1e-5, sh))
+        r = rows_r[cur[0]]
+        rc("rms_norm", L.muser_rms_norm(r.data_ptr(), w_in.data_ptr(), x.data_ptr(), H, M, 1e-5, sh))
         prev = None
         for l, d in enumerate(layers):
             ev = events.get(l) if events is not None else None
@@ -681,17 +695,20 @@ def run_attn(args, rank, world):
             if M > 1:
                 if prev is not None:
                     rc("tail", L.muser_fused_residual_dual_rmsnorm(
-                        resid.data_ptr(), proj.data_ptr(), x.data_ptr(), prev["w_post"].data_ptr(),
+                        r.data_ptr(), proj.data_ptr(), x.data_ptr(), prev["w_post"].data_ptr(),
                         prev["w_ffn"].data_ptr(), H, M, 1e-8, 1e-5, sh))
                 for n, r, y in zip(("Wq", "Wk", "Wv", "Wg"), (QD, KVD, KVD, QD), outs4):
                     split_mv(d[n], r, H, x, y)
             elif prev is None:
                 rc("qkvg", L.muser_qmatvec_group(12, 4, w4[l], rows4, H, x.data_ptr(), M, ys4, sh))
             else:
+                cur[0] = 1 - cur[0]
+                r_next = rows_r[cur[0]]
                 rc("qkvg_tail", L.muser_qmatvec_group_tail(
-                    12, 4, w4[l], rows4, H, proj.data_ptr(), resid.data_ptr(), prev["w_post"].data_ptr(),
-                    prev["w_ffn"].data_ptr(), 1e-8, 1e-5, x.data_ptr(), M, ys4, ticket.data_ptr(),
-                    mu.MUSER_BOUNDARY_SCRATCH_BYTES, sh))
+                    12, 4, w4[l], rows4, H, proj.data_ptr(), r.data_ptr(), r_next.data_ptr(),
+                    prev["w_post"].data_ptr(), prev["w_ffn"].data_ptr(), 1e-8, 1e-5, x.data_ptr(), M, ys4,
+                    None, 0, sh))
+                r = r_next
             if ev is not None:
                 ev[1].record(stream)
             if M > 1:
@@ -702,7 +719,7 @@ def run_attn(args, rank, world):
             if ev is not None:
                 ev[2].record(stream)
             prev = d
-        rc("tail", L.muser_fused_residual_dual_rmsnorm(resid.data_ptr(), proj.data_ptr(), x.data_ptr(),
+        rc("tail", L.muser_fused_residual_dual_rmsnorm(r.data_ptr(), proj.data_ptr(), x.data_ptr(),
                                                        prev["w_post"].data_ptr(), prev["w_ffn"].data_ptr(),
                                                        H, M, 1e-8, 1e-5, sh))
 
@@ -744,14 +761,14 @@ def run_attn(args, rank, world):
     h_in = torch.from_numpy(r0.copy()).pin_memory()
     h_out = torch.empty(M, H, dtype=torch.float32).pin_memory()
     for _ in range(max(1, min(3, args.warmup))):
-        resid.copy_(h_in, non_blocking=True)
+        rows_r[cur[0]].copy_(h_in, non_blocking=True)
         step()
         h_out.copy_(x, non_blocking=True)
     barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(args.steps):
-        resid.copy_(h_in, non_blocking=True)
+        rows_r[cur[0]].copy_(h_in, non_blocking=True)
         step()
         h_out.copy_(x, non_blocking=True)
     e1.record(stream)

@@ -59,7 +59,8 @@ extern "C" {
 #define MUSER_ABI_VERSION 2
 #define MUSER_MAX_M 16
 /* Scratch of the fused layer-boundary calls (muser_ffn_gate_up_silu_tail,
- * muser_qmatvec_group_tail): the blocks' completion ticket. */
+ * muser_qmatvec_group_tail) when they update the residual in place: the
+ * blocks' ticket. */
 #define MUSER_BOUNDARY_SCRATCH_BYTES 256u
 
 /* ggml type ids, informational */
@@ -214,17 +215,17 @@ int muser_qmatvec_group(int qtype, int n, const void* const* W, const int64_t* r
  *   the group on its output: as muser_fused_residual_dual_rmsnorm (src =
  *   projected, out = x_out, n = cols) followed by muser_qmatvec_group with
  *   x = x_out.  With one row of x and Q4_K the tail runs inside the group's
- *   launch, every block for itself; the block that takes the last ticket in
- *   `scratch` writes the updated residual and x_out, as in
- *   muser_ffn_gate_up_silu_tail.  projected, residual, x_out: device f32
+ *   launch, every block for itself.  residual_out, residual and scratch as
+ *   for muser_ffn_gate_up_silu_tail: a distinct residual_out takes the
+ *   updated residual; NULL updates `residual` in place through the ticket in
+ *   `scratch`.  projected, residual, x_out (and residual_out): device f32
  *   [M*cols], distinct; w1, w2: device f32 [cols]; cols % 4 == 0;
- *   eps1, eps2 > 0; scratch: MUSER_BOUNDARY_SCRATCH_BYTES or more of
- *   zero-filled caller memory, as for muser_ffn_gate_up_silu_tail.
+ *   eps1, eps2 > 0.
  */
 int muser_qmatvec_group_tail(int qtype, int n, const void* const* W, const int64_t* rows, int64_t cols,
-                             const float* projected, float* residual, const float* w1, const float* w2,
-                             float eps1, float eps2, float* x_out, int M, float* const* y, void* scratch,
-                             size_t scratch_bytes, void* stream);
+                             const float* projected, float* residual, float* residual_out, const float* w1,
+                             const float* w2, float eps1, float eps2, float* x_out, int M, float* const* y,
+                             void* scratch, size_t scratch_bytes, void* stream);
 
 /*
  * muser_scale_softcap -- logits[i] = cap * tanh(logits[i] * scale / cap), in
@@ -251,31 +252,38 @@ int muser_lm_head(int qtype, const void* W, int64_t vocab, int64_t hidden, const
  *   one call: the previous layer's dual-eps tail (Ch 19 §19.4, as
  *   muser_fused_residual_dual_rmsnorm with src = projected, out = x_out),
  *   then this layer's gate/up/SiLU on its output (Ch 10 §10.3 (d), as
- *   muser_ffn_gate_up_silu with x = x_out).  Per row m:
- *     residual += w1 * projected / sqrt(mean(projected^2) + eps1)  (in place)
- *     x_out     = w2 * residual / sqrt(mean(residual^2) + eps2)
- *     mid       = silu(Wg . x_out) * (Wu . x_out)
+ *   muser_ffn_gate_up_silu with x = x_out).  Per row m, with R the updated
+ *   residual (written to residual_out, or to residual when residual_out is
+ *   NULL):
+ *     R     = residual + w1 * projected / sqrt(mean(projected^2) + eps1)
+ *     x_out = w2 * R / sqrt(mean(R^2) + eps2)
+ *     mid   = silu(Wg . x_out) * (Wu . x_out)
  *   w2 is the next norm of the previous layer, i.e. this layer's input norm
  *   (Ch 10 §10.4).  The rounding points are those of the two calls: the
  *   residual and x_out are binary32 values.  For one row of x with a short
  *   enough row (hidden <= 6656 for Q4_K gate/up) the tail runs inside the
  *   gate/up kernel, so the layer boundary costs no separate launch; other
  *   shapes run the two calls.  Inside the kernel every block computes the
- *   tail for itself from the residual; the residual is updated in place, so
- *   each block takes a ticket in `scratch` once it has read the row, and the
- *   block that takes the last ticket writes the updated residual and x_out
- *   (no block can overwrite the row while another still has to read it).
- *   projected, residual, x_out: device f32 [M*hidden] (residual in/out,
- *   x_out output; the three must be distinct); w1, w2: device f32 [hidden];
- *   Wg, Wu: device matrices [ffn x hidden]; mid: device f32 [M*ffn].
- *   scratch: device memory of at least MUSER_BOUNDARY_SCRATCH_BYTES bytes,
- *   16-byte aligned, owned by the caller, zero-filled before its first use
- *   and left zero-filled by every call; calls that can run at the same time
- *   must not share it.
+ *   tail for itself from the whole residual row.
+ *   - residual_out != NULL (a row distinct from the others): the updated
+ *     residual goes there and `residual` is only read; no block can write a
+ *     row another block reads.  This is the fast form; a layer loop
+ *     alternates two residual buffers.  scratch is not used (may be NULL).
+ *   - residual_out == NULL: the residual is updated in place.  No block may
+ *     overwrite the row while another still has to read it, so each block
+ *     takes a ticket in `scratch` once it has read the row, and the block
+ *     that takes the last ticket writes the updated residual and x_out at its
+ *     end.  scratch: device memory of at least MUSER_BOUNDARY_SCRATCH_BYTES
+ *     bytes, 16-byte aligned, owned by the caller, zero-filled before its
+ *     first use and left zero-filled by every call; calls that can run at the
+ *     same time must not share it.
+ *   projected, residual, x_out (and residual_out): device f32 [M*hidden],
+ *   distinct; w1, w2: device f32 [hidden]; Wg, Wu: device matrices
+ *   [ffn x hidden]; mid: device f32 [M*ffn].
  *   hidden % 4 == 0; eps1, eps2 > 0.  Fail-closed like the two calls.
  */
 int muser_ffn_gate_up_silu_tail(int qtype, const void* Wg, const void* Wu, int64_t ffn,
-                                int64_t hidden, const float* projected, float* residual,
+                                int64_t hidden, const float* projected, float* residual, float* residual_out,
                                 const float* w1, const float* w2, float eps1, float eps2,
                                 float* x_out, int M, float* mid, void* scratch, size_t scratch_bytes,
                                 void* stream);

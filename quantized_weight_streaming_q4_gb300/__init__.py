@@ -101,11 +101,11 @@ def lib():
             "muser_ffn_gate_up_silu": (I, [I, P, P, I64, I64, P, I, P, P]),
             "muser_gate_up_scratch_bytes": (SZ, [I, I64, I64, I]),
             "muser_ffn_gate_up_silu_scratch": (I, [I, P, P, I64, I64, P, I, P, P, SZ, P]),
-            "muser_ffn_gate_up_silu_tail": (I, [I, P, P, I64, I64, P, P, P, P, F, F, P, I, P, P, SZ, P]),
+            "muser_ffn_gate_up_silu_tail": (I, [I, P, P, I64, I64, P, P, P, P, P, F, F, P, I, P, P, SZ, P]),
             "muser_qmatvec_group": (I, [I, I, P, P, I64, P, I, P, P]),
             "muser_scale_softcap": (I, [P, I64, F, F, P]),
             "muser_lm_head": (I, [I, P, I64, I64, P, I, P, F, F, P]),
-            "muser_qmatvec_group_tail": (I, [I, I, P, P, I64, P, P, P, P, F, F, P, I, P, P, SZ, P]),
+            "muser_qmatvec_group_tail": (I, [I, I, P, P, I64, P, P, P, P, P, F, F, P, I, P, P, SZ, P]),
             "muser_fused_residual_dual_rmsnorm": (I, [P, P, P, P, P, I, I, F, F, P]),
             "muser_scratch_bytes": (SZ, [I64, I]),
             "muser_qmatvec_residual_dual_rmsnorm": (I, [I, P, I64, I64, P, I, P, P, P, P, P, F, F, P,
@@ -229,12 +229,16 @@ def muser_ffn_gate_up_silu_scratch(qtype, Wg, Wu, ffn: int, hidden: int, x, M: i
 
 
 def muser_ffn_gate_up_silu_tail(qtype, Wg, Wu, ffn: int, hidden: int, projected, residual, w1, w2,
-                                eps1: float, eps2: float, x_out, M: int, mid, scratch,
-                                scratch_bytes: int = MUSER_BOUNDARY_SCRATCH_BYTES, stream=None) -> None:
+                                eps1: float, eps2: float, x_out, M: int, mid, scratch=None,
+                                scratch_bytes: int = MUSER_BOUNDARY_SCRATCH_BYTES, residual_out=None,
+                                stream=None) -> None:
+    """residual_out=None updates `residual` in place (scratch: the ticket);
+    otherwise the updated residual goes to residual_out."""
     _check("muser_ffn_gate_up_silu_tail",
            lib().muser_ffn_gate_up_silu_tail(_qt(qtype), _ptr(Wg), _ptr(Wu), ffn, hidden, _ptr(projected),
-                                             _ptr(residual), _ptr(w1), _ptr(w2), eps1, eps2, _ptr(x_out), M,
-                                             _ptr(mid), _ptr(scratch), scratch_bytes, _stream(stream)))
+                                             _ptr(residual), _ptr(residual_out), _ptr(w1), _ptr(w2), eps1, eps2,
+                                             _ptr(x_out), M, _ptr(mid), _ptr(scratch), scratch_bytes,
+                                             _stream(stream)))
 
 
 def muser_scale_softcap(logits, n: int, scale: float, cap: float, stream=None) -> None:
@@ -262,13 +266,13 @@ def muser_qmatvec_group(qtype, Ws, rows, cols: int, x, M: int, ys, stream=None) 
 
 
 def muser_qmatvec_group_tail(qtype, Ws, rows, cols: int, projected, residual, w1, w2, eps1: float, eps2: float,
-                             x_out, M: int, ys, scratch, scratch_bytes: int = MUSER_BOUNDARY_SCRATCH_BYTES,
-                             stream=None) -> None:
+                             x_out, M: int, ys, scratch=None, scratch_bytes: int = MUSER_BOUNDARY_SCRATCH_BYTES,
+                             residual_out=None, stream=None) -> None:
     n, wa, ra, ya = _group_arrays(Ws, rows, ys)
     _check("muser_qmatvec_group_tail",
-           lib().muser_qmatvec_group_tail(_qt(qtype), n, wa, ra, cols, _ptr(projected), _ptr(residual), _ptr(w1),
-                                          _ptr(w2), eps1, eps2, _ptr(x_out), M, ya, _ptr(scratch), scratch_bytes,
-                                          _stream(stream)))
+           lib().muser_qmatvec_group_tail(_qt(qtype), n, wa, ra, cols, _ptr(projected), _ptr(residual),
+                                          _ptr(residual_out), _ptr(w1), _ptr(w2), eps1, eps2, _ptr(x_out), M, ya,
+                                          _ptr(scratch), scratch_bytes, _stream(stream)))
 
 
 def muser_fused_residual_dual_rmsnorm(residual, src, out, w1, w2, n: int, M: int, eps1: float,

@@ -91,6 +91,18 @@ int check_boundary_scratch(const char* fn, const void* scratch, size_t scratch_b
     return MUSER_OK;
 }
 
+// The updated-residual output of the fused boundary calls: null (in place,
+// the ticket scratch required) or a row distinct from the other operands.
+int check_residual_out(const char* fn, const float* residual_out, const float* residual, const float* projected,
+                       const float* x_out, const void* scratch, size_t scratch_bytes) {
+    if (residual_out == nullptr) return check_boundary_scratch(fn, scratch, scratch_bytes);
+    MUSER_TRY(check_f32(fn, "residual_out", residual_out));
+    if (residual_out == residual || residual_out == projected || residual_out == x_out)
+        return set_error(MUSER_ERR_INVALID_ARG, "%s: residual_out must be distinct from residual, projected and x_out",
+                         fn);
+    return MUSER_OK;
+}
+
 int check_M(const char* fn, int M) {
     if (M < 1 || M > MUSER_MAX_M)
         return set_error(MUSER_ERR_INVALID_ARG, "%s: M = %d outside 1..%d", fn, M, MUSER_MAX_M);
@@ -122,8 +134,7 @@ struct Workspace {
     float* xb;
     float* mid;
     float* proj;
-    unsigned* ticket;  // the fused layer boundary's ticket (MUSER_BOUNDARY_SCRATCH_BYTES)
-    float* resid_ws;   // the one-launch stack's second residual buffer
+    float* resid_ws;   // the second buffer of the residual relay
     void* mvs;         // the one-launch stack's sync words and input records
     void* scratch;     // down + tail scratch, down_scratch_bytes(hidden)
     void* gu_scratch;  // gate/up tensor-core scratch (null if the shape has none)
@@ -144,8 +155,6 @@ Workspace carve(void* base, int64_t hidden, int64_t ffn, int M) {
     off += fb;
     w.proj = reinterpret_cast<float*>(p + off);
     off += hb;
-    w.ticket = reinterpret_cast<unsigned*>(p + off);
-    off += MUSER_BOUNDARY_SCRATCH_BYTES;
     w.resid_ws = reinterpret_cast<float*>(p + off);
     off += hb;
     w.mvs = p + off;
@@ -252,10 +261,24 @@ bool gate_up_tail_fused(int qtype, int64_t hidden, int M) {
 int gate_up_launch(int qtype, const void* Wg, const void* Wu, int64_t ffn, int64_t hidden,
                    const float* x, int M, float* mid, void* scratch, cudaStream_t s);
 
+// The tail with its residual going to resid_out (distinct) or, when that is
+// null, updated in place.
+int dual_tail_to(float* residual, float* resid_out, const float* src, float* out, const float* w1, const float* w2,
+                 int n, int M, float eps1, float eps2, cudaStream_t s) {
+    if (resid_out != nullptr) {
+        const cudaError_t e = cudaMemcpyAsync(resid_out, residual, sizeof(float) * static_cast<size_t>(n) * M,
+                                              cudaMemcpyDeviceToDevice, s);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyAsync(residual)");
+        residual = resid_out;
+    }
+    return launch_dual_tail(residual, src, out, w1, w2, n, M, eps1, eps2, s);
+}
+
 // The layer boundary (previous tail, then gate/up) on validated arguments.
-// ticket: MUSER_BOUNDARY_SCRATCH_BYTES of zero-filled caller scratch.
+// resid_out: a separate output row for the updated residual, or null (in
+// place; ticket: MUSER_BOUNDARY_SCRATCH_BYTES of zero-filled caller scratch).
 int gate_up_tail_launch(int qtype, const void* Wg, const void* Wu, int64_t ffn, int64_t hidden,
-                        const float* projected, float* residual, const float* w1, const float* w2,
+                        const float* projected, float* residual, float* resid_out, const float* w1, const float* w2,
                         float eps1, float eps2, float* x_out, int M, float* mid, unsigned* ticket,
                         cudaStream_t s) {
     if (gate_up_tail_fused(qtype, hidden, M)) {
@@ -272,10 +295,11 @@ int gate_up_tail_launch(int qtype, const void* Wg, const void* Wu, int64_t ffn, 
         a.w2 = w2;
         a.eps1 = eps1;
         a.eps2 = eps2;
+        a.resid_out = resid_out;
         a.xticket = ticket;
         return launch_mv1(qtype, 2, kEpiSiluMul, a, s, kXTail);
     }
-    MUSER_TRY(launch_dual_tail(residual, projected, x_out, w1, w2, static_cast<int>(hidden), M, eps1, eps2, s));
+    MUSER_TRY(dual_tail_to(residual, resid_out, projected, x_out, w1, w2, static_cast<int>(hidden), M, eps1, eps2, s));
     return gate_up_launch(qtype, Wg, Wu, ffn, hidden, x_out, M, mid, nullptr, s);
 }
 
@@ -511,7 +535,7 @@ int muser_ffn_gate_up_silu_scratch(int qtype, const void* Wg, const void* Wu, in
 }
 
 int muser_ffn_gate_up_silu_tail(int qtype, const void* Wg, const void* Wu, int64_t ffn,
-                                int64_t hidden, const float* projected, float* residual,
+                                int64_t hidden, const float* projected, float* residual, float* residual_out,
                                 const float* w1, const float* w2, float eps1, float eps2,
                                 float* x_out, int M, float* mid, void* scratch, size_t scratch_bytes,
                                 void* stream) {
@@ -530,8 +554,8 @@ int muser_ffn_gate_up_silu_tail(int qtype, const void* Wg, const void* Wu, int64
     if (!(eps1 > 0.0f) || !(eps2 > 0.0f)) return set_error(MUSER_ERR_INVALID_ARG, "%s: eps must be > 0", fn);
     if (x_out == residual || x_out == projected || projected == residual)
         return set_error(MUSER_ERR_INVALID_ARG, "%s: projected, residual and x_out must be distinct", fn);
-    MUSER_TRY(check_boundary_scratch(fn, scratch, scratch_bytes));
-    return gate_up_tail_launch(qtype, Wg, Wu, ffn, hidden, projected, residual, w1, w2, eps1, eps2,
+    MUSER_TRY(check_residual_out(fn, residual_out, residual, projected, x_out, scratch, scratch_bytes));
+    return gate_up_tail_launch(qtype, Wg, Wu, ffn, hidden, projected, residual, residual_out, w1, w2, eps1, eps2,
                                x_out, M, mid, static_cast<unsigned*>(scratch), as_stream(stream));
 }
 
@@ -552,8 +576,8 @@ static int check_group(const char* fn, int qtype, int n, const void* const* W, c
 // One launch over the group's rows when one row of x, Q4_K (rows of whole
 // 16-byte units) and the one-token kernel fit; otherwise one call per matrix.
 static int group_launch(int qtype, int n, const void* const* W, const int64_t* rows, int64_t cols, const float* x,
-                        int M, float* const* y, const float* projected, float* residual, const float* w1,
-                        const float* w2, float eps1, float eps2, float* x_out, unsigned* ticket,
+                        int M, float* const* y, const float* projected, float* residual, float* resid_out,
+                        const float* w1, const float* w2, float eps1, float eps2, float* x_out, unsigned* ticket,
                         cudaStream_t s) {
     const bool tail = projected != nullptr;
     const bool fused = M == 1 && qtype == MUSER_Q4_K &&
@@ -579,13 +603,14 @@ static int group_launch(int qtype, int n, const void* const* W, const int64_t* r
             a.w2 = w2;
             a.eps1 = eps1;
             a.eps2 = eps2;
+            a.resid_out = resid_out;
             a.xticket = ticket;
         }
         return launch_mv1(qtype, 1, kEpiStore, a, s, tail ? kXTail : kXMemory);
     }
     const float* xin = x;
     if (tail) {
-        MUSER_TRY(launch_dual_tail(residual, projected, x_out, w1, w2, static_cast<int>(cols), M, eps1, eps2, s));
+        MUSER_TRY(dual_tail_to(residual, resid_out, projected, x_out, w1, w2, static_cast<int>(cols), M, eps1, eps2, s));
         xin = x_out;
     }
     for (int i = 0; i < n; ++i) MUSER_TRY(muser_qmatvec(qtype, W[i], rows[i], cols, xin, M, y[i], s));
@@ -597,14 +622,14 @@ int muser_qmatvec_group(int qtype, int n, const void* const* W, const int64_t* r
     clear_error();
     const char* fn = "muser_qmatvec_group";
     MUSER_TRY(check_group(fn, qtype, n, W, rows, cols, x, M, y));
-    return group_launch(qtype, n, W, rows, cols, x, M, y, nullptr, nullptr, nullptr, nullptr, 0.f, 0.f, nullptr,
-                        nullptr, as_stream(stream));
+    return group_launch(qtype, n, W, rows, cols, x, M, y, nullptr, nullptr, nullptr, nullptr, nullptr, 0.f, 0.f,
+                        nullptr, nullptr, as_stream(stream));
 }
 
 int muser_qmatvec_group_tail(int qtype, int n, const void* const* W, const int64_t* rows, int64_t cols,
-                             const float* projected, float* residual, const float* w1, const float* w2, float eps1,
-                             float eps2, float* x_out, int M, float* const* y, void* scratch, size_t scratch_bytes,
-                             void* stream) {
+                             const float* projected, float* residual, float* residual_out, const float* w1,
+                             const float* w2, float eps1, float eps2, float* x_out, int M, float* const* y,
+                             void* scratch, size_t scratch_bytes, void* stream) {
     clear_error();
     const char* fn = "muser_qmatvec_group_tail";
     MUSER_TRY(check_group(fn, qtype, n, W, rows, cols, x_out, M, y));
@@ -616,9 +641,9 @@ int muser_qmatvec_group_tail(int qtype, int n, const void* const* W, const int64
     if (!(eps1 > 0.0f) || !(eps2 > 0.0f)) return set_error(MUSER_ERR_INVALID_ARG, "%s: eps must be > 0", fn);
     if (x_out == residual || x_out == projected || projected == residual)
         return set_error(MUSER_ERR_INVALID_ARG, "%s: projected, residual and x_out must be distinct", fn);
-    MUSER_TRY(check_boundary_scratch(fn, scratch, scratch_bytes));
-    return group_launch(qtype, n, W, rows, cols, nullptr, M, y, projected, residual, w1, w2, eps1, eps2, x_out,
-                        static_cast<unsigned*>(scratch), as_stream(stream));
+    MUSER_TRY(check_residual_out(fn, residual_out, residual, projected, x_out, scratch, scratch_bytes));
+    return group_launch(qtype, n, W, rows, cols, nullptr, M, y, projected, residual, residual_out, w1, w2, eps1, eps2,
+                        x_out, static_cast<unsigned*>(scratch), as_stream(stream));
 }
 
 int muser_scale_softcap(float* logits, int64_t n, float scale, float cap, void* stream) {
@@ -831,10 +856,15 @@ int muser_ffn_stack(const muser_ffn_layer* layers, int n_layers, const float* en
             if (l == 0) {
                 MUSER_TRY(gate_up_launch(L.gate_up_qtype, L.w_gate, L.w_up, ffn, hidden, ws.xa, M, ws.mid, nullptr, s));
             } else {
+                // the residual relays between the caller's buffer and the
+                // workspace (tail t reads buffer t % 2, writes the other), so
+                // no block overwrites the row the others still read
                 const muser_ffn_layer& P = layers[l - 1];
-                MUSER_TRY(gate_up_tail_launch(L.gate_up_qtype, L.w_gate, L.w_up, ffn, hidden, ws.proj, residual,
+                float* r_in = (l - 1) % 2 == 0 ? residual : ws.resid_ws;
+                float* r_out = (l - 1) % 2 == 0 ? ws.resid_ws : residual;
+                MUSER_TRY(gate_up_tail_launch(L.gate_up_qtype, L.w_gate, L.w_up, ffn, hidden, ws.proj, r_in, r_out,
                                               P.post_norm, P.next_norm, eps_post, eps_norm, ws.xb, M, ws.mid,
-                                              ws.ticket, s));
+                                              nullptr, s));
             }
             Mv1Args d{};
             d.W[0] = static_cast<const uint8_t*>(L.w_down);
@@ -845,9 +875,11 @@ int muser_ffn_stack(const muser_ffn_layer* layers, int n_layers, const float* en
             d.y0 = ws.proj;
             MUSER_TRY(launch_mv1(L.down_qtype, 1, kEpiStore, d, s));
         }
+        // the last tail reads buffer (n_layers - 1) % 2 and ends in the caller's
         const muser_ffn_layer& Z = layers[n_layers - 1];
-        return launch_dual_tail(residual, ws.proj, out, Z.post_norm, Z.next_norm, static_cast<int>(hidden), M,
-                                eps_post, eps_norm, s);
+        float* r_last = (n_layers - 1) % 2 == 0 ? residual : ws.resid_ws;
+        return dual_tail_to(r_last, r_last == residual ? nullptr : residual, ws.proj, out, Z.post_norm, Z.next_norm,
+                            static_cast<int>(hidden), M, eps_post, eps_norm, s);
     }
     float* x = ws.xa;
     float* xnext = ws.xb;

@@ -28,8 +28,11 @@ struct Mv1Args {
     float scale, cap;  // soft-cap epilogue: y = cap * tanh(y * scale / cap)
     unsigned* ticket;
     float* tail_part;  // per-block sums of projected^2 (kMv1TailParts floats), or null
-    // x from the previous layer's tail (kXTail): the blocks' tickets; the block
-    // that takes the last one writes the updated residual and re-zeroes it
+    // x from the previous layer's tail (kXTail): the updated residual goes to
+    // resid_out when that is set (a row distinct from resid); otherwise it
+    // replaces resid, written by the block that takes the last ticket in
+    // xticket, which it re-zeroes
+    float* resid_out;
     unsigned* xticket;
     // Row segments (Q4_K, one matrix, store epilogue; Q4_K rows are whole 16-byte units):
     // rows [seg0[s], seg0[s+1]) of the virtual matrix are rows of segW[s],

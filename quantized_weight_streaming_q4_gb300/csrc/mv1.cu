@@ -46,11 +46,16 @@ namespace {
 // runs per stage.
 // XS: where x comes from.  kXMemory: x is p.x.  kXTail: x is the next-norm
 // output of the previous layer's dual-eps tail (Ch 19 §19.4), computed here
-// by every block from p.x (= projected), p.resid, p.w1, p.w2.  The residual
-// is updated in place, so no block may write it before every block has read
-// it: each block takes a ticket (p.xticket) once its consumers hold the row,
-// and the block that takes the last one writes the updated residual (and x to
-// p.out when that is set), then re-zeroes the ticket.
+// by every block from p.x (= projected), p.resid, p.w1, p.w2.  With a
+// separate output row (p.resid_out) block 0 writes the updated row there (and
+// x to p.out) as soon as it has it.  In place, no block may write the
+// residual before every block has read it: once its consumers hold their
+// slices (they read the row before), each block's copy warp takes a ticket
+// (p.xticket) and looks at the answer only after its last copy request, so
+// the ticket's round trip (many blocks update one counter) stays off the
+// stream; at its end the block that took the last ticket recomputes the
+// updated row with the consumers' 1/rms values (the same operations, so the
+// same bits), writes it (and x to p.out) and re-zeroes the ticket.
 template <int QT, int NMAT, int EPI, int XS>
 __global__ void __launch_bounds__(512, 1) mv1_kernel(const Mv1Args p) {
     extern __shared__ __align__(128) uint8_t smem[];
@@ -77,6 +82,7 @@ __global__ void __launch_bounds__(512, 1) mv1_kernel(const Mv1Args p) {
     uint64_t* reduced = full + 32;
     uint64_t* xissued = full + 48;  // every consumer warp has issued its loads of x
     uint64_t* xready = full + 49;   // every consumer warp holds its slice
+    // kXTail: consumer thread 0 leaves inv1, inv2 of the tail in red[60..61]
     float* red = reinterpret_cast<float*>(smem + 512);
     int* flag = reinterpret_cast<int*>(smem + 512 + 64 * 4);
     float* part = reinterpret_cast<float*>(smem + p.part_off);
@@ -178,6 +184,11 @@ __global__ void __launch_bounds__(512, 1) mv1_kernel(const Mv1Args p) {
         __syncwarp();
         // The rest of the first NS stages once the slots are free again.
         if (ok) ok = mbar_wait_bounded(xready, 0, &g_device_status, kDevStatusWaitTimeout);
+        // kXTail: every consumer has read the residual; take the ticket now
+        // (release: this block's reads; acquire: the others'), look at the
+        // answer after the last copy request.
+        unsigned tk = 0u;
+        if (XS == kXTail && p.resid_out == nullptr && ok && lane == 0) tk = atom_add_acq_rel_gpu(p.xticket, 1u);
         if (ok && lane == 0)
             for (int k = early; k < nfirst; ++k) issue(k, k + rot - NS);
         __syncwarp();
@@ -201,6 +212,7 @@ __global__ void __launch_bounds__(512, 1) mv1_kernel(const Mv1Args p) {
             if (++rslot == NP) rslot = 0;
             if (kp >= NP && rslot == 0) rphase ^= 1u;
         }
+        if (XS == kXTail && lane == 0) *flag = (ok && tk == gridDim.x - 1) ? 1 : 0;
     } else if (warp > ncw) {
         // ----------------------------------------------------- reducer warps
         // Two warps take alternate stages (the 2*NS partial slots alternate
@@ -291,10 +303,6 @@ __global__ void __launch_bounds__(512, 1) mv1_kernel(const Mv1Args p) {
         const int n4 = nbc * 16, nthr = ncw * 32;
         const int x0 = static_cast<int>((static_cast<int64_t>(blockIdx.x) * n4) / gridDim.x);
         auto xi = [&](int j) { return j + x0 < n4 ? j + x0 : j + x0 - n4; };
-        // the previous layer's tail: the updated residual row (this thread's
-        // share), the next norm's weights and 1/rms of the updated row
-        float4 rv[4], bv[4];
-        float inv2 = 0.0f;
         if constexpr (XS == kXTail) {
             // The tail of the previous layer, at most 4 float4 of each vector
             // per thread (the launcher checks), in registers.  The norm
@@ -304,7 +312,8 @@ __global__ void __launch_bounds__(512, 1) mv1_kernel(const Mv1Args p) {
             const float4* r4 = reinterpret_cast<const float4*>(p.resid);
             const float4* a4 = reinterpret_cast<const float4*>(p.w1);
             const float4* b4 = reinterpret_cast<const float4*>(p.w2);
-            float4 pv[4], av[4];
+            float4 pv[4], rv[4], av[4], bv[4];
+            float inv2;
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
                 const int j = tid + u * nthr;
@@ -351,12 +360,11 @@ __global__ void __launch_bounds__(512, 1) mv1_kernel(const Mv1Args p) {
                     rv[u] = h;
                 }
             sh = warps_sum(sh, red, ncw);
-            // Every consumer thread of this block has read its share of the
-            // residual (the sum above used it): the block takes its ticket.
-            // The result is needed only after the slots are written.
-            unsigned tk = 0u;
-            if (tid == 0) tk = atom_add_acq_rel_gpu(p.xticket, 1u);  // release: the block's reads first
             inv2 = 1.0f / sqrtf(sh / n + p.eps2);
+            if (tid == 0) {  // for the block that writes the updated row (kernel end)
+                red[60] = inv1;
+                red[61] = inv2;
+            }
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
                 const int j = tid + u * nthr;
@@ -365,9 +373,13 @@ __global__ void __launch_bounds__(512, 1) mv1_kernel(const Mv1Args p) {
                     const float4 xv = make_float4((rv[u].x * inv2) * bv[u].x, (rv[u].y * inv2) * bv[u].y,
                                                   (rv[u].z * inv2) * bv[u].z, (rv[u].w * inv2) * bv[u].w);
                     sts_float4(xslots + xslot_offset(i, QT != MUSER_Q6_K, parity_split, p.HP), xv);
+                    // a separate output row: nobody reads it here, block 0 writes it now
+                    if (p.resid_out != nullptr && blockIdx.x == 0) {
+                        reinterpret_cast<float4*>(p.resid_out)[i] = rv[u];
+                        if (p.out) reinterpret_cast<float4*>(p.out)[i] = xv;
+                    }
                 }
             }
-            if (tid == 0) *flag = (tk == gridDim.x - 1) ? 1 : 0;  // acquire: the other blocks' reads precede
         } else {
             // All of a thread's copies (at most 16: x holds 16 float4 per slice
             // and there are at least as many consumer threads as slices) are
@@ -387,25 +399,6 @@ __global__ void __launch_bounds__(512, 1) mv1_kernel(const Mv1Args p) {
             cp_async_wait_all();
         }
         named_barrier_sync(1, ncw * 32);  // the consumer warps only
-        if constexpr (XS == kXTail) {
-            // The block with the last ticket: every block has read the
-            // residual, so the updated row can replace it.
-            if (*flag) {
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const int j = tid + u * nthr;
-                    if (j < n4) {
-                        const int i = xi(j);
-                        reinterpret_cast<float4*>(p.resid)[i] = rv[u];
-                        if (p.out)
-                            reinterpret_cast<float4*>(p.out)[i] =
-                                make_float4((rv[u].x * inv2) * bv[u].x, (rv[u].y * inv2) * bv[u].y,
-                                            (rv[u].z * inv2) * bv[u].z, (rv[u].w * inv2) * bv[u].w);
-                    }
-                }
-                if (tid == 0) *p.xticket = 0u;
-            }
-        }
         if (QT != MUSER_Q6_K || G > 1) {
             // Every slot converted once, a quarter per thread (the row groups
             // share the slots), then each thread loads its own slot's record.
@@ -535,6 +528,33 @@ __global__ void __launch_bounds__(512, 1) mv1_kernel(const Mv1Args p) {
         }
     }
     ok = __syncthreads_and(ok);
+    if constexpr (XS == kXTail) {
+        // In place (no p.resid_out): the block that took the last ticket.
+        // Every block has read the residual, so the updated row replaces it
+        // (h = r + p * inv1 * w1 as in the prologue, bit for bit) and x goes
+        // to p.out.
+        if (ok && p.resid_out == nullptr && *flag) {
+            const float inv1 = red[60], inv2 = red[61];
+            const int n4 = nbc * 16;
+            const float4* p4 = reinterpret_cast<const float4*>(p.x);
+            float4* r4 = reinterpret_cast<float4*>(p.resid);
+            const float4* a4 = reinterpret_cast<const float4*>(p.w1);
+            const float4* b4 = reinterpret_cast<const float4*>(p.w2);
+            for (int i = tid; i < n4; i += blockDim.x) {
+                const float4 pv = __ldcg(p4 + i), rv = __ldcg(r4 + i), av = __ldg(a4 + i), bv = __ldg(b4 + i);
+                float4 h;
+                h.x = fmaf(pv.x * inv1, av.x, rv.x);
+                h.y = fmaf(pv.y * inv1, av.y, rv.y);
+                h.z = fmaf(pv.z * inv1, av.z, rv.z);
+                h.w = fmaf(pv.w * inv1, av.w, rv.w);
+                r4[i] = h;
+                if (p.out)
+                    reinterpret_cast<float4*>(p.out)[i] =
+                        make_float4((h.x * inv2) * bv.x, (h.y * inv2) * bv.y, (h.z * inv2) * bv.z, (h.w * inv2) * bv.w);
+            }
+            if (tid == 0) *p.xticket = 0u;
+        }
+    }
     if (!ok) {
         // A bounded wait gave up (status word set).  Give the copies still in
         // flight a bounded chance to land before the block's shared memory is
@@ -654,8 +674,8 @@ static int launch_mv1_t(Mv1Args a, cudaStream_t stream) {
     }
     if (XS == kXTail && !(nbc * 16 <= 4 * 32 * geo.ncw))
         return set_error(MUSER_ERR_UNSUPPORTED, "mv1: %d inputs exceed the fused tail's registers", nbc * 64);
-    if (XS == kXTail && a.xticket == nullptr)
-        return set_error(MUSER_ERR_INVALID_ARG, "mv1: the fused tail needs its ticket");
+    if (XS == kXTail && a.resid_out == nullptr && a.xticket == nullptr)
+        return set_error(MUSER_ERR_INVALID_ARG, "mv1: the fused tail in place needs its ticket");
     const int threads = (a.nconsumer_warps + 3) * 32;
     // Rows per stage: a multiple of G, the stage near 32 KB over all matrices,
     // or near 64 KB for Q6_K and for rows that one row group spans.  There

@@ -33,8 +33,10 @@
 // share of the residual and of `out`.
 //
 // Warp roles (480 threads): 13 consumer warps (gate/up uses all of them in
-// four row groups; down uses 10, one row group split by block parity); one
-// copy warp; one reducer warp.  (With 480 threads a thread may hold 136
+// four row groups; down uses 12: one row group of 320 threads split by block
+// parity, and two warps that mirror the first two warps' slices and take half
+// their rows, so the four schedulers carry equal work); one copy warp; one
+// reducer warp.  (With 480 threads a thread may hold 136
 // registers: the two phases' slices and dot products fit without spills.)  Barriers: full/empty
 // per stage buffer, pfull/reduced per partial slot, as in the one-token
 // kernel, with ring positions counted across phases.  Every wait is bounded
@@ -418,14 +420,24 @@ __device__ __forceinline__ uint32_t d_phase(const MvsArgs& p, int l, uint32_t st
     uint32_t phase = ring_phase(st);
     bool ok = ring_ok(st);
 
+                // Scheduler balance at the model's shape (320 slice threads,
+                // 4 rows a stage): the 10 busy warps would put 3/3/2/2 on the
+                // schedulers.  Warps 10 and 11 (idle otherwise, on schedulers
+                // 2 and 3) hold copies of warps 0 and 1's slices and take the
+                // second row pair of each stage from them: 5/5/5/5 row pairs.
+                const bool bal = p.TGd == 320 && RSd == 4;
+                const bool helper = bal && tid >= 320 && tid < 384;
+                const int t = helper ? tid - 320 : tid;   // the slice this thread holds
+                const int pair0 = helper ? 2 : 0;                    // first row of the thread's pairs
+                const int pair_end = (bal && tid < 64) ? 2 : RSd;    // warps 0, 1: first pair only
                 int b = 0, c = 0;
-                const bool active = tid < p.TGd && slice_of(tid, nbc_d, true, p.HPd, b, c);
+                const bool active = t < p.TGd && slice_of(t, nbc_d, true, p.HPd, b, c);
                 if (!active) b = c = 0;
                 const int bc = b * 4 + c;
                 ok = consumers_grid_wait(p, gridDim.x * static_cast<unsigned>(2 * l + 1), abort_s, flag) && ok;
                 // every thread converts a slice (inactive ones block 0's, unused)
                 SliceQ6 sl;
-                load_slice_q6_mem(sl, p.xperm, active ? tid : 0, p.TGd, (b & 1) != 0);
+                load_slice_q6_mem(sl, p.xperm, active ? t : 0, p.TGd, (b & 1) != 0);
                 const uint32_t jq = static_cast<uint32_t>(c & 1);
                 const uint32_t sel_sc = jq | ((jq + 2) << 4) | ((jq + 4) << 8) | ((jq + 6) << 12);
                 const bool aligned = (b % 2) == 0;
@@ -441,7 +453,7 @@ __device__ __forceinline__ uint32_t d_phase(const MvsArgs& p, int l, uint32_t st
                         const uint32_t delta = static_cast<uint32_t>(
                             (wbase + static_cast<uint64_t>(d0 + static_cast<int64_t>(s) * RSd) * rb_d) & 15u);
                         const uint8_t* sb = rb + static_cast<size_t>(buf) * p.sb + delta;
-                        for (int rs = 0; rs < rows_here; rs += 2) {
+                        for (int rs = pair0; rs < min(rows_here, pair_end); rs += 2) {
                             const uint8_t* blk[2] = {sb + rs * rb_d, sb + (rs + 1) * rb_d};
                             float v[2];
                             if (rs + 1 < rows_here) {

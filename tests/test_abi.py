@@ -187,13 +187,20 @@ def test_group_calls_fail_closed(L):
     t = L.muser_qmatvec_group_tail
     args = (12, 4, W, rows, 6656)
     S = (FAKE * 11, 256)                                                 # the ticket scratch
-    assert t(*args, FAKE * 6, FAKE * 7, FAKE * 8, FAKE * 9, 1e-8, 1e-5, FAKE * 7, 1, y, *S, None) == -1   # x_out == residual
-    assert t(*args, FAKE * 6, FAKE * 7, FAKE * 8, FAKE * 9, 0.0, 1e-5, FAKE * 10, 1, y, *S, None) == -1   # eps1 = 0
-    assert t(*args, FAKE * 6, FAKE * 6, FAKE * 8, FAKE * 9, 1e-8, 1e-5, FAKE * 10, 1, y, *S, None) == -1  # projected == residual
-    assert t(*args, FAKE * 6, FAKE * 7, FAKE * 8, FAKE * 9, 1e-8, 1e-5, FAKE * 10, 1, y, None, 256, None) == -1  # no scratch
-    assert t(*args, FAKE * 6, FAKE * 7, FAKE * 8, FAKE * 9, 1e-8, 1e-5, FAKE * 10, 1, y, FAKE * 11, 255, None) == -1
-    assert t(*args, FAKE * 6, FAKE * 7, FAKE * 8, FAKE * 9, 1e-8, 1e-5, FAKE * 10, 1, y, FAKE * 11 + 4, 256,
-             None) == -3                                                 # misaligned scratch
+    pr = (FAKE * 6, FAKE * 7, None, FAKE * 8, FAKE * 9)                  # projected, residual, residual_out, w1, w2
+    assert t(*args, *pr, 1e-8, 1e-5, FAKE * 7, 1, y, *S, None) == -1     # x_out == residual
+    assert t(*args, *pr, 0.0, 1e-5, FAKE * 10, 1, y, *S, None) == -1     # eps1 = 0
+    assert t(*args, FAKE * 6, FAKE * 6, None, FAKE * 8, FAKE * 9, 1e-8, 1e-5, FAKE * 10, 1, y, *S,
+             None) == -1                                                 # projected == residual
+    assert t(*args, *pr, 1e-8, 1e-5, FAKE * 10, 1, y, None, 256, None) == -1   # in place without scratch
+    assert t(*args, *pr, 1e-8, 1e-5, FAKE * 10, 1, y, FAKE * 11, 255, None) == -1
+    assert t(*args, *pr, 1e-8, 1e-5, FAKE * 10, 1, y, FAKE * 11 + 4, 256, None) == -3   # misaligned scratch
+    assert t(*args, FAKE * 6, FAKE * 7, FAKE * 7, FAKE * 8, FAKE * 9, 1e-8, 1e-5, FAKE * 10, 1, y, None, 0,
+             None) == -1                                                 # residual_out == residual
+    assert t(*args, FAKE * 6, FAKE * 7, FAKE * 10, FAKE * 8, FAKE * 9, 1e-8, 1e-5, FAKE * 10, 1, y, None, 0,
+             None) == -1                                                 # residual_out == x_out
+    assert t(*args, FAKE * 6, FAKE * 7, FAKE * 12 + 4, FAKE * 8, FAKE * 9, 1e-8, 1e-5, FAKE * 10, 1, y, None, 0,
+             None) == -3                                                 # misaligned residual_out
 
 
 @needs_nvcc
@@ -215,16 +222,22 @@ def test_scale_softcap_and_lm_head_fail_closed(L):
 @needs_nvcc
 def test_fused_layer_boundary_and_static_scratch_fail_closed(L):
     f = L.muser_ffn_gate_up_silu_tail
-    base = (12, FAKE, FAKE * 2, 19968, 6656, FAKE * 3, FAKE * 4, FAKE * 5, FAKE * 6)
+    base = (12, FAKE, FAKE * 2, 19968, 6656, FAKE * 3, FAKE * 4, None, FAKE * 5, FAKE * 6)
     S = (FAKE * 9, 256)                                              # the ticket scratch
     assert f(*base, 1e-8, 1e-5, FAKE * 4, 1, FAKE * 8, *S, None) == -1   # x_out aliases the residual
     assert f(*base, 1e-8, -1.0, FAKE * 7, 1, FAKE * 8, *S, None) == -1   # eps2 < 0
     assert f(*base, 1e-8, 1e-5, FAKE * 7, 0, FAKE * 8, *S, None) == -1   # M = 0
-    assert f(14, FAKE, FAKE * 2, 19968, 6656, FAKE * 3, FAKE * 4, FAKE * 5, FAKE * 6, 1e-8, 1e-5,
+    assert f(14, FAKE, FAKE * 2, 19968, 6656, FAKE * 3, FAKE * 4, None, FAKE * 5, FAKE * 6, 1e-8, 1e-5,
              FAKE * 7, 1, FAKE * 8 + 4, *S, None) == -3                   # misaligned mid
-    assert f(*base, 1e-8, 1e-5, FAKE * 7, 1, FAKE * 8, None, 256, None) == -1        # no ticket scratch
+    assert f(*base, 1e-8, 1e-5, FAKE * 7, 1, FAKE * 8, None, 256, None) == -1        # in place without scratch
     assert f(*base, 1e-8, 1e-5, FAKE * 7, 1, FAKE * 8, FAKE * 9, 128, None) == -1    # too small
     assert "scratch" in mu.muser_last_error()
+    out = (12, FAKE, FAKE * 2, 19968, 6656, FAKE * 3, FAKE * 4)
+    assert f(*out, FAKE * 3, FAKE * 5, FAKE * 6, 1e-8, 1e-5, FAKE * 7, 1, FAKE * 8, None, 0,
+             None) == -1                                             # residual_out == projected
+    assert "residual_out" in mu.muser_last_error()
+    assert f(*out, FAKE * 10 + 8, FAKE * 5, FAKE * 6, 1e-8, 1e-5, FAKE * 7, 1, FAKE * 8, None, 0,
+             None) == -3                                             # misaligned residual_out
     st = L.muser_qmatvec_residual_dual_rmsnorm_static
     # M * hidden above the static array's 262,080 floats
     assert st(14, FAKE, 65536, 19968, FAKE * 2, 16, FAKE * 3, FAKE * 4, FAKE * 5, FAKE * 6, 1e-8, 1e-5,

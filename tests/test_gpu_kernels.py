@@ -249,20 +249,27 @@ def ticket_scratch():
 
 
 @pytest.mark.parametrize("M,ffn", [(1, 19968), (1, 2001), (3, 2003)])
-def test_ffn_gate_up_silu_tail(M, ffn):
+@pytest.mark.parametrize("form", ["in_place", "residual_out"])
+def test_ffn_gate_up_silu_tail(M, ffn, form):
     """The layer boundary: the previous tail then gate/up/SiLU.  One row of x
-    runs the tail inside the gate/up kernel (every block computes x; the block
-    that takes the last ticket writes residual and x_out); M = 3 runs the two
-    calls."""
+    runs the tail inside the gate/up kernel (every block computes x; in place,
+    the block that takes the last ticket writes residual and x_out); M = 3
+    runs the two calls.  With residual_out the input residual is left as it
+    was."""
     hidden = 6656
     Wg, Wu, r, p, w1, w2 = boundary_case(M, ffn, hidden)
     rd, x_out, mid = dev(r), nan_like((M, hidden), extra=32), nan_like((M, ffn), extra=32)
     tk = ticket_scratch()
+    r_out = nan_like((M, hidden), extra=32) if form == "residual_out" else None
     mu.muser_ffn_gate_up_silu_tail("q4_k", dev(Wg), dev(Wu), ffn, hidden, dev(p), rd, dev(w1), dev(w2),
-                                   1e-8, 1e-5, x_out, M, mid, tk)
+                                   1e-8, 1e-5, x_out, M, mid, tk if r_out is None else None, residual_out=r_out)
     assert not host(tk).any(), "the ticket must be left zeroed"
     r_ref, x_ref = oracle.dual_tail(r, p, w1, w2, 1e-8, 1e-5)
     mid_ref = oracle.gate_up_silu("q4_k", Wg, Wu, ffn, hidden, x_ref)
+    if r_out is not None:
+        assert np.array_equal(host(rd).reshape(M, hidden), r), "residual_out form: the input row is read only"
+        check_canary(r_out, M * hidden)
+        rd = r_out[:M * hidden]
     assert_close(host(rd).reshape(M, hidden), r_ref, "tail residual")
     assert_close(host(x_out[:M * hidden]).reshape(M, hidden), x_ref, "tail x_out")
     assert_close(host(mid[:M * ffn]).reshape(M, ffn), mid_ref, f"gate_up_silu after the tail M={M}", scaled=True)
@@ -288,7 +295,8 @@ def start_blocks_late(stream, ms=30):
 
 
 @pytest.mark.parametrize("reps", [2])
-def test_ffn_gate_up_silu_tail_blocks_start_late(reps):
+@pytest.mark.parametrize("form", ["in_place", "residual_out"])
+def test_ffn_gate_up_silu_tail_blocks_start_late(reps, form):
     """The fused boundary updates the residual in place while every block reads
     it.  With most blocks starting ~25 ms after the first ones, a block that
     read the already-updated row would add the tail twice: residual, x_out and
@@ -303,11 +311,15 @@ def test_ffn_gate_up_silu_tail_blocks_start_late(reps):
     s = torch.cuda.current_stream()
     for call in range(reps):
         rd, x_out, mid = dev(r), nan_like((M, hidden)), nan_like((M, ffn))
+        r_out = nan_like((M, hidden)) if form == "residual_out" else None
         busy = start_blocks_late(s)
         mu.muser_ffn_gate_up_silu_tail("q4_k", dWg, dWu, ffn, hidden, dp, rd, dw1, dw2, 1e-8, 1e-5, x_out, M,
-                                       mid, tk, stream=s)
+                                       mid, tk, residual_out=r_out, stream=s)
         torch.cuda.synchronize()
         busy.synchronize()
+        if r_out is not None:
+            assert np.array_equal(host(rd).reshape(M, hidden), r)
+            rd = r_out
         assert_close(host(rd).reshape(M, hidden), r_ref, f"residual with late blocks (call {call})")
         assert_close(host(x_out).reshape(M, hidden), x_ref, f"x_out with late blocks (call {call})")
         assert_close(host(mid).reshape(M, ffn), mid_ref, f"mid with late blocks (call {call})", scaled=True)
@@ -315,7 +327,8 @@ def test_ffn_gate_up_silu_tail_blocks_start_late(reps):
     assert mu.muser_device_status() == 0
 
 
-def test_group_tail_blocks_start_late():
+@pytest.mark.parametrize("form", ["in_place", "residual_out"])
+def test_group_tail_blocks_start_late(form):
     """The attention-side group with the previous tail in its launch, under
     the same late block starts: residual, x_out and the four projections."""
     H = 6656
@@ -330,11 +343,15 @@ def test_group_tail_blocks_start_late():
     ys = [nan_like((1, n)) for n in rows]
     tk = ticket_scratch()
     s = torch.cuda.current_stream()
+    r_out = nan_like((1, H)) if form == "residual_out" else None
     busy = start_blocks_late(s)
     mu.muser_qmatvec_group_tail("q4_k", [dev(A[n]) for n in names], rows, H, dev(p), rd, dev(w1), dev(w2),
-                                1e-8, 1e-5, x_out, 1, ys, tk, stream=s)
+                                1e-8, 1e-5, x_out, 1, ys, tk, residual_out=r_out, stream=s)
     torch.cuda.synchronize()
     busy.synchronize()
+    if r_out is not None:
+        assert np.array_equal(host(rd).reshape(1, H), r)
+        rd = r_out
     assert_close(host(rd).reshape(1, H), r_ref, "residual with late blocks")
     assert_close(host(x_out).reshape(1, H), x_ref, "x_out with late blocks")
     for name, n, y in zip(names, rows, ys):

@@ -272,7 +272,7 @@ def test_attention_side_projections_and_first_tail(M):
 
 
 @pytest.mark.parametrize("M", [1, 3])
-@pytest.mark.parametrize("with_tail", [False, True])
+@pytest.mark.parametrize("with_tail", [False, "in_place", "residual_out"])
 def test_attention_projection_group(M, with_tail):
     """Q, K, V and gate as one group (one launch at M = 1), optionally after
     the previous sub-block's tail: equal to the tail and four matvecs."""
@@ -286,10 +286,15 @@ def test_attention_projection_group(M, with_tail):
         w2 = synth.norm_weight(H, seed=7, workload=synth.ATTN_WORKLOAD, tensor=synth.T_W2)
         rd, x_out = dev(r), nan_like((M, H), extra=16)
         tk = torch.zeros(mu.MUSER_BOUNDARY_SCRATCH_BYTES // 4, dtype=torch.int32, device="cuda")
+        r_out = nan_like((M, H), extra=16) if with_tail == "residual_out" else None
         mu.muser_qmatvec_group_tail("q4_k", [dev(A[n]) for n in names], rows, H, dev(p), rd, dev(w1), dev(w2),
-                                    1e-8, 1e-5, x_out, M, ys, tk)
+                                    1e-8, 1e-5, x_out, M, ys, tk, residual_out=r_out)
         assert not host(tk).any(), "the ticket must be left zeroed"
         r_ref, x = oracle.dual_tail(r, p, w1, w2, 1e-8, 1e-5)
+        if r_out is not None:
+            assert np.array_equal(host(rd).reshape(M, H), r), "residual_out form: the input row is read only"
+            check_canary(r_out, M * H)
+            rd = r_out[:M * H]
         assert_close(host(rd).reshape(M, H), r_ref, "tail residual")
         assert_close(host(x_out[:M * H]).reshape(M, H), x, "tail x_out")
         check_canary(x_out, M * H)
