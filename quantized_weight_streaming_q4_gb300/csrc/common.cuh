@@ -136,6 +136,10 @@ __device__ __forceinline__ void sts_float4(void* p, float4 v) {
                  "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w)
                  : "memory");
 }
+// Bring the 128-byte line holding p into L2 (no register result).
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
 // 16-byte asynchronous copy global -> shared (both 16-byte aligned), and
 // the waits on this thread's copies.
 __device__ __forceinline__ void cp_async16(void* dst, const void* src) {

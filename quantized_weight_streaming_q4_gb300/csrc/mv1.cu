@@ -220,6 +220,18 @@ __global__ void __launch_bounds__(512, 1) mv1_kernel(const Mv1Args p) {
         pdl_launch_dependents();
         pdl_wait();  // outputs of the previous kernel are complete before ours are written
         const int n4 = nbc / 4;
+        if constexpr (EPI == kEpiTail) {
+            // the last block reads this block's rows of the residual and both
+            // norm weights: bring them to L2 while the stream runs
+            if (warp == ncw + 1) {
+                const char* vecs[3] = {reinterpret_cast<const char*>(p.resid), reinterpret_cast<const char*>(p.w1),
+                                       reinterpret_cast<const char*>(p.w2)};
+                const int64_t lo = (r0 * 4) & ~int64_t{127}, hi = (r0 + nloc) * 4;
+                for (int64_t o = lo + 128 * lane; o < hi; o += 32 * 128)
+#pragma unroll
+                    for (int v = 0; v < 3; ++v) prefetch_l2(vecs[v] + o);
+            }
+        }
         int slot = warp - ncw - 1;  // k % NP (NP is even)
         uint32_t sphase = 0;        // (k / NP) & 1
         float tss = 0.0f;           // tail: sum of this warp's projected^2
@@ -267,10 +279,7 @@ __global__ void __launch_bounds__(512, 1) mv1_kernel(const Mv1Args p) {
                         p.y0[row] = acc;
                         if constexpr (NMAT == 2) p.y1[row] = other;
                     }
-                    if constexpr (EPI == kEpiTail) {
-                        tss = fmaf(acc, acc, tss);
-                        __threadfence();
-                    }
+                    if constexpr (EPI == kEpiTail) tss = fmaf(acc, acc, tss);
                 }
             }
             __syncwarp();
@@ -380,6 +389,36 @@ __global__ void __launch_bounds__(512, 1) mv1_kernel(const Mv1Args p) {
                     }
                 }
             }
+        } else if (G == 1) {
+            // One row group: thread tid owns slot tid, and warp w's 32 slots
+            // are the four slices of eight super-blocks.  Each warp copies
+            // those blocks' inputs (coalesced, 1 KB per block) and converts
+            // its own slots, so no warp waits for another before its loop.
+            pdl_wait();  // x is the previous kernel's output
+            const float4* x4 = reinterpret_cast<const float4*>(p.x);
+#pragma unroll
+            for (int k0 = 0; k0 < 8; ++k0) {
+                const int k = (k0 + blockIdx.x) & 7;  // blocks start at different lines
+                int bk, ck;
+                if (slice_of(warp * 32 + 4 * k, nbc, parity_split, p.HP, bk, ck)) {
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int i = bk * 64 + lane + 32 * h;
+                        cp_async16(xslots + xslot_offset(i, QT != MUSER_Q6_K, parity_split, p.HP), x4 + i);
+                    }
+                }
+            }
+            cp_async_commit();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(xissued);
+            cp_async_wait_all();
+            __syncwarp();
+            if (active) {
+                if constexpr (QT == MUSER_Q6_K)
+                    load_slice_q6(sl, reinterpret_cast<const float*>(xslots + idx * kXSlot), parity_split && (b & 1));
+                else
+                    load_slice_q4(sl, reinterpret_cast<const float*>(xslots + idx * kXSlot));
+            }
         } else {
             // All of a thread's copies (at most 16: x holds 16 float4 per slice
             // and there are at least as many consumer threads as slices) are
@@ -398,8 +437,10 @@ __global__ void __launch_bounds__(512, 1) mv1_kernel(const Mv1Args p) {
             if (lane == 0) mbar_arrive(xissued);
             cp_async_wait_all();
         }
-        named_barrier_sync(1, ncw * 32);  // the consumer warps only
-        if (QT != MUSER_Q6_K || G > 1) {
+        if (XS == kXTail || G > 1) named_barrier_sync(1, ncw * 32);  // the consumer warps only
+        if (G == 1 && XS == kXMemory) {
+            // converted above, each thread its own slot
+        } else if (QT != MUSER_Q6_K || G > 1) {
             // Every slot converted once, a quarter per thread (the row groups
             // share the slots), then each thread loads its own slot's record.
             for (int q0 = 0; q0 < 4 * p.TG; q0 += nthr) {
@@ -571,15 +612,16 @@ __global__ void __launch_bounds__(512, 1) mv1_kernel(const Mv1Args p) {
         // Last CTA to finish runs the dual-eps tail over the whole row.  With
         // p.tail_part, every CTA first leaves the sum of its rows' squares
         // there (its two reducers' sums, in order).
+        // The ticket is taken after a block barrier with acquire-release
+        // semantics: it releases every write of this block (projected, the
+        // partial) and the last block acquires all the others'.
         if (tid == 0) {
             if (p.tail_part) p.tail_part[blockIdx.x] = red[40] + red[41];
-            __threadfence();
-            const unsigned t = atomicAdd(p.ticket, 1u);
+            const unsigned t = atom_add_acq_rel_gpu(p.ticket, 1u);
             *flag = (t == gridDim.x - 1) ? 1 : 0;
         }
         __syncthreads();
         if (*flag) {
-            __threadfence();
             const int n = static_cast<int>(p.rows);
             if (p.tail_part && (n >> 2) <= 4 * static_cast<int>(blockDim.x))
                 block_dual_tail_row_parts(p.resid, p.y0, p.out, p.w1, p.w2, n, p.eps1, p.eps2, p.tail_part,

@@ -174,6 +174,49 @@ __device__ __forceinline__ void convert_quarter(uint8_t* slot, int k, bool valid
     }
 }
 
+// One thread converts a whole Q4_K / Q5_K slot (its 64 inputs in order at xs)
+// into its own slice: the arithmetic of convert_quarter's four quarters (the
+// same exponent, digits and half sums, each half summed as two sequential
+// 16-input sums) without the shared-memory record.
+__device__ __forceinline__ void load_slice_q4(SliceQ4& s, const float* xs) {
+    float v[64];
+#pragma unroll
+    for (int q = 0; q < 16; ++q) {
+        const float4 f = lds_float4(xs + 4 * q);
+        v[4 * q + 0] = f.x;
+        v[4 * q + 1] = f.y;
+        v[4 * q + 2] = f.z;
+        v[4 * q + 3] = f.w;
+    }
+    float m = 0.0f;
+#pragma unroll
+    for (int l = 0; l < 64; ++l) m = fmaxf(m, fabsf(v[l]));
+    const int e = slice_exponent(m);
+    const float p2e = pow2f(e);
+    s.inv = pow2f(-e);
+    float qs[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        float sum = 0.0f;
+#pragma unroll
+        for (int l = 0; l < 16; ++l) sum += v[16 * k + l];
+        qs[k] = sum;
+    }
+    s.s_lo = qs[0] + qs[1];
+    s.s_hi = qs[2] + qs[3];
+#pragma unroll
+    for (int t = 0; t < 16; ++t) {
+        uint32_t D[3];
+        pack_digits(__float2int_rn(v[4 * t] * p2e), __float2int_rn(v[4 * t + 1] * p2e),
+                    __float2int_rn(v[4 * t + 2] * p2e), __float2int_rn(v[4 * t + 3] * p2e), D);
+#pragma unroll
+        for (int d = 0; d < 3; ++d) {
+            if (t < 8) s.lo[d][t] = D[d];
+            else s.hi[d][t - 8] = D[d];
+        }
+    }
+}
+
 // One thread converts a whole Q6_K slot (four 16-input groups, group g at xs
 // + 16g) into its own slice.
 __device__ __forceinline__ void load_slice_q6(SliceQ6& s, const float* xs, bool rot) {
