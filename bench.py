@@ -697,8 +697,8 @@ def run_attn(args, rank, world):
                     rc("tail", L.muser_fused_residual_dual_rmsnorm(
                         r.data_ptr(), proj.data_ptr(), x.data_ptr(), prev["w_post"].data_ptr(),
                         prev["w_ffn"].data_ptr(), H, M, 1e-8, 1e-5, sh))
-                for n, r, y in zip(("Wq", "Wk", "Wv", "Wg"), (QD, KVD, KVD, QD), outs4):
-                    split_mv(d[n], r, H, x, y)
+                for n, nrows, y in zip(("Wq", "Wk", "Wv", "Wg"), (QD, KVD, KVD, QD), outs4):
+                    split_mv(d[n], nrows, H, x, y)
             elif prev is None:
                 rc("qkvg", L.muser_qmatvec_group(12, 4, w4[l], rows4, H, x.data_ptr(), M, ys4, sh))
             else:
@@ -810,6 +810,8 @@ def run_attn(args, rank, world):
                 "api": ("per-layer muser_qmatvec_group[_tail] / muser_qmatvec calls" if M == 1 else
                         "per-layer muser_fused_residual_dual_rmsnorm and muser_qmatvec_scratch calls") +
                        ", host residual in, x out"},
+        # M = 16: per layer the tail (after the first) and five tensor-core matvecs (too few units per CTA
+        # for the prebuilt B image: one launch each)
         "gpu_launches": args.steps * ((2 + 2 * nl) if M == 1 else (1 + 6 * nl)),
         "clocks": clock, "device_status": mu.muser_device_status(), "weights_generation_s": round(gen_s, 1),
     }

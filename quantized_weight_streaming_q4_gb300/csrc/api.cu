@@ -124,7 +124,7 @@ constexpr bool kTensorCoreM1 = false;
 // The bound holds for every row length (a one-block Q6_K row has the most
 // tiles).
 size_t down_scratch_bytes(int64_t hidden, int M) {
-    return kScratchBytes + mvt_scratch_bytes(MUSER_Q6_K, 1, hidden, kQK, M);
+    return kScratchBytes + mvt_split_scratch_bytes(MUSER_Q6_K, 1, hidden, kQK, M);
 }
 
 size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
@@ -160,7 +160,13 @@ Workspace carve(void* base, int64_t hidden, int64_t ffn, int M) {
     w.mvs = p + off;
     off += round_up(mvs_scratch_bytes(hidden, ffn), 256);
     w.scratch = p + off;
-    w.scratch_bytes = round_up(down_scratch_bytes(hidden, M), 256);
+    // with several rows of x, also room for the tensor-core kernel's B image
+    // of a down projection over ffn inputs
+    size_t down = down_scratch_bytes(hidden, M);
+    if (M > 1)
+        for (int qt : {MUSER_Q4_K, MUSER_Q6_K})
+            down = std::max(down, kScratchBytes + mvt_scratch_bytes(qt, 1, hidden, ffn, M));
+    w.scratch_bytes = round_up(down, 256);
     off += w.scratch_bytes;
     const size_t gu = mvt_scratch_bytes(MUSER_Q4_K, 2, ffn, hidden, M);
     w.gu_scratch = gu ? p + off : nullptr;
@@ -177,7 +183,7 @@ int down_tail_launch(int qtype, const void* Wdown, int64_t hidden, int64_t ffn, 
     // One token: the CUDA-core kernel mv1 is measured faster than the
     // tensor-core kernel on this shape, so it takes M = 1.
     const bool tc_ok = mvt_supported(qtype, 1, hidden, ffn, M);
-    const bool tc_fits = tc_ok && scratch_bytes >= kScratchBytes + mvt_scratch_bytes(qtype, 1, hidden, ffn, M);
+    const bool tc_fits = tc_ok && scratch_bytes >= kScratchBytes + mvt_split_scratch_bytes(qtype, 1, hidden, ffn, M);
     if (M > 1 && tc_ok) {
         // several rows: the tensor-core matvec into `projected`, then the tail
         // per row.  With room for its partial sums the matvec spreads its
@@ -191,7 +197,7 @@ int down_tail_launch(int qtype, const void* Wdown, int64_t hidden, int64_t ffn, 
         a.M = M;
         a.y = projected;
         MUSER_TRY(launch_mvt(qtype, kEpiStore, a, tc_fits ? static_cast<uint8_t*>(scratch) + kScratchBytes : nullptr,
-                             s));
+                             tc_fits ? scratch_bytes - kScratchBytes : 0, s));
         return launch_dual_tail(residual, projected, out, w1, w2, static_cast<int>(hidden), M, eps1, eps2, s);
     }
     if (kTensorCoreM1 && M == 1 && tc_fits) {
@@ -209,7 +215,8 @@ int down_tail_launch(int qtype, const void* Wdown, int64_t hidden, int64_t ffn, 
         a.eps1 = eps1;
         a.eps2 = eps2;
         a.M = 1;
-        return launch_mvt(qtype, kEpiTail, a, static_cast<uint8_t*>(scratch) + kScratchBytes, s);
+        return launch_mvt(qtype, kEpiTail, a, static_cast<uint8_t*>(scratch) + kScratchBytes, scratch_bytes - kScratchBytes,
+                          s);
     }
     if (M == 1 && mv1_supported(qtype, ffn)) {
         Mv1Args a{};
@@ -315,7 +322,7 @@ int gate_up_launch(int qtype, const void* Wg, const void* Wu, int64_t ffn, int64
         a.x = x;
         a.M = M;
         a.y = mid;
-        return launch_mvt(qtype, kEpiSiluMul, a, scratch, s);
+        return launch_mvt(qtype, kEpiSiluMul, a, scratch, scratch ? mvt_scratch_bytes(qtype, 2, ffn, hidden, M) : 0, s);
     }
     if (M == 1 && mv1_supported(qtype, hidden)) {
         Mv1Args a{};
@@ -429,7 +436,7 @@ int muser_qmatvec(int qtype, const void* W, int64_t rows, int64_t cols, const fl
         t.x = x;
         t.M = M;
         t.y = y;
-        return launch_mvt(qtype, kEpiStore, t, nullptr, as_stream(stream));
+        return launch_mvt(qtype, kEpiStore, t, nullptr, 0, as_stream(stream));
     }
     MvMArgs a{};
     a.W[0] = static_cast<const uint8_t*>(W);
@@ -471,7 +478,7 @@ int muser_qmatvec_scratch(int qtype, const void* W, int64_t rows, int64_t cols, 
     t.x = x;
     t.M = M;
     t.y = y;
-    return launch_mvt(qtype, kEpiStore, t, scratch, as_stream(stream));
+    return launch_mvt(qtype, kEpiStore, t, scratch, scratch_bytes, as_stream(stream));
 }
 
 int muser_rms_norm(const float* x, const float* w, float* out, int n, int M, float eps,
@@ -785,10 +792,18 @@ int muser_ffn_stack_launches(const muser_ffn_layer* layers, int n_layers, int64_
     bool fused = true;
     for (int l = 0; l < n_layers && fused; ++l)
         fused = gate_up_tail_fused(layers[l].gate_up_qtype, hidden, M) && mv1_supported(layers[l].down_qtype, ffn);
-    // the entry norm, two kernels per layer, and (fused boundaries) the last tail;
-    // with several rows the down projection and its tail are two launches
+    // the entry norm, two kernels per layer, and (fused boundaries) the last tail
     if (fused) return 2 + 2 * n_layers;
-    return 1 + (M > 1 ? 3 : 2) * n_layers;
+    if (M == 1) return 1 + 2 * n_layers;
+    // several rows: gate/up, the down projection and its tail; a tensor-core
+    // matvec with its B image is three launches (built before, cleared after)
+    int n = 1;
+    for (int l = 0; l < n_layers; ++l) {
+        const int gu = mvt_launches(layers[l].gate_up_qtype, 2, ffn, hidden, M);
+        const int dn = mvt_launches(layers[l].down_qtype, 1, hidden, ffn, M);
+        n += (gu > 0 ? gu : 1) + (dn > 0 ? dn : 1) + 1;
+    }
+    return n;
 }
 
 int muser_ffn_stack(const muser_ffn_layer* layers, int n_layers, const float* entry_norm,

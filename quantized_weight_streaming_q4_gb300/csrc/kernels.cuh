@@ -88,15 +88,25 @@ struct MvtArgs {
     float* part;      // scratch: partial sums, 128 floats per slot; tile t from CTA c in slot t + c
     unsigned* tick;   // scratch: per-tile tickets [ntiles], then the tail counter
     unsigned* status; // device status word
+    // several rows of x with scratch: the B operand of every super-block,
+    // built once per call by a prep kernel (slab, then the x sums and scales)
+    const uint8_t* bimg;
     // geometry, filled by the launcher
     int ntiles, P, maxparts, ns, tiles_per_cta;
     uint32_t x_off, b_off, stage_off, xch_off;
 };
 bool mvt_supported(int qtype, int nmat, int64_t rows, int64_t cols, int M);
+// Scratch of the even split: tickets and partial sums, and for several rows
+// of x the B image after them (mvt_split_scratch_bytes: without the image).
 size_t mvt_scratch_bytes(int qtype, int nmat, int64_t rows, int64_t cols, int M);
+size_t mvt_split_scratch_bytes(int qtype, int nmat, int64_t rows, int64_t cols, int M);
 // scratch == nullptr: whole tiles per CTA; else the even split over all SMs
-// with `scratch` of mvt_scratch_bytes() (zero-filled, left zeroed).
-int launch_mvt(int qtype, int epi, MvtArgs a, void* scratch, cudaStream_t s);
+// with `scratch` (zero-filled, left zeroed) of scratch_bytes >=
+// mvt_split_scratch_bytes(); from mvt_scratch_bytes() on, several rows of x
+// take the prebuilt B image.
+int launch_mvt(int qtype, int epi, MvtArgs a, void* scratch, size_t scratch_bytes, cudaStream_t s);
+// Launches one launch_mvt call makes with scratch of mvt_scratch_bytes() (0: unsupported).
+int mvt_launches(int qtype, int nmat, int64_t rows, int64_t cols, int M);
 // Device address of the status word (mv1.cu), for kernels in other units.
 unsigned* device_status_word();
 

@@ -68,6 +68,12 @@ __host__ __device__ constexpr int mvt_threads(bool multi) { return (kDeqWarps + 
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kDCol0 = kNA * 128;        // first D column
 constexpr int kMaxStages = 12;
+// Several rows of x: one super-block's B image, as the builders leave it in
+// shared memory: the 16 KB slab, then 8 sub-block sums of x per row (Q4_K)
+// and the 16 rows' scales 2^e.
+constexpr uint32_t kSlabBytes = 16384;
+constexpr uint32_t kXrBytes = (16 * 8 + 16) * 4;
+constexpr uint32_t kBImg = kSlabBytes + kXrBytes;
 constexpr uint32_t kMagic2 = 0x64006400u;     // binary16 1024.0 in both halves
 
 // ------------------------------------------------------- tcgen05 helpers
@@ -866,6 +872,32 @@ __global__ void __launch_bounds__(mvt_threads(MULTI), 1)
                     if (lane == 0) mbar_arrive(&sfull[db]);
                 }
             }
+        } else if (MULTI && warp >= kBldWarp0 && p.bimg != nullptr) {
+            // -------- several rows of x, B image prebuilt: per unit, one
+            // bulk copy of the super-block's slab and of its sums and scales
+            // (the image is the previous kernel's output: read after the PDL
+            // wait above).  Warp kBldWarp0 copies, the other only arrives.
+            const int bw = warp - kBldWarp0;
+            UnitIter<QT> it(u0, nsb);
+            Ring rb, rd;
+            for (int i = 0; i < nunits; ++i, it.next(), rb.next(kNB), rd.next(kND)) {
+                if (ok && i >= kNB) ok = mbar_wait_bounded(&dfull[rb.slot], rb.phase ^ 1u, p.status, kDevStatusWaitTimeout);
+                if (ok && i >= kND) ok = mbar_wait_bounded(&dempty[rd.slot], rd.phase ^ 1u, p.status, kDevStatusWaitTimeout);
+                if (bw == 0) {
+                    if (ok && lane == 0) {
+                        const uint8_t* src = p.bimg + static_cast<size_t>(it.sb) * kBImg;
+                        mbar_arrive_expect_tx(&xfull[rb.slot], kBImg);
+                        tma_load_1d(B + kSlab * rb.slot, src, kSlabBytes, &xfull[rb.slot]);
+                        tma_load_1d(xr + kXr * rd.slot, src + kSlabBytes, kXrBytes, &xfull[rb.slot]);
+                    }
+                    if (ok) ok = mbar_wait_bounded(&xfull[rb.slot], rb.phase, p.status, kDevStatusWaitTimeout);
+                }
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(&bfull[rb.slot]);
+                    mbar_arrive(&sfull[rd.slot]);
+                }
+            }
         } else if (MULTI && warp >= kBldWarp0) {
             // -------- several rows of x: per-unit B slabs, scales and sums
             // Builder warp bw owns rows 8bw..8bw+7 of x; its slots of x are
@@ -1072,12 +1104,57 @@ __global__ void __launch_bounds__(mvt_threads(MULTI), 1)
     }
 }
 
+// Several rows of x: the B image of super-block blockIdx.x (its slab, the
+// rows' sub-block sums of x and scales), built by two warps exactly as the
+// builder warps of mvt_kernel build it per unit.  Rows past M convert zeros.
+template <int QT>
+__global__ void __launch_bounds__(64) mvt_prep_kernel(const float* __restrict__ x, int M, int nsb, uint8_t* img) {
+    __shared__ __align__(16) float xs[16 * 256];
+    const int sb = blockIdx.x, tid = threadIdx.x;
+    pdl_launch_dependents();
+    pdl_wait();  // x is the previous kernel's output
+    const int64_t K = static_cast<int64_t>(nsb) * kQK;
+    for (int i = tid; i < 16 * 64; i += 64) {
+        const int m = i >> 6;
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (m < M) v = __ldg(reinterpret_cast<const float4*>(x + m * K + static_cast<int64_t>(sb) * kQK) + (i & 63));
+        reinterpret_cast<float4*>(xs)[i] = v;
+    }
+    __syncthreads();
+    const int lane = tid & 31, m = 8 * (tid >> 5) + (lane >> 2), q = lane & 3;
+    uint8_t* base = img + static_cast<size_t>(sb) * kBImg;
+    float* xr = reinterpret_cast<float*>(base + kSlabBytes);
+    float xs8[8];
+    const float e2 = build_row_quarter<QT>(xs + m * 256, q, base, (m >> 2) * 128 + (2 * m & 7) * 16, xs8);
+    if (q == 0) {
+        xr[8 * 16 + m] = e2;
+        if constexpr (QT == MUSER_Q4_K) {
+            *reinterpret_cast<float4*>(xr + 8 * m) = make_float4(xs8[0], xs8[1], xs8[2], xs8[3]);
+            *reinterpret_cast<float4*>(xr + 8 * m + 4) = make_float4(xs8[4], xs8[5], xs8[6], xs8[7]);
+        }
+    }
+}
+
+// Zeroes the B image after the matvec has read it (the caller's scratch is
+// left zero-filled).
+__global__ void __launch_bounds__(256) mvt_clear_kernel(uint8_t* img, int nsb) {
+    pdl_launch_dependents();
+    pdl_wait();  // the matvec that reads the image is complete
+    uint4* p = reinterpret_cast<uint4*>(img + static_cast<size_t>(blockIdx.x) * kBImg);
+    for (int i = threadIdx.x; i < static_cast<int>(kBImg / 16); i += blockDim.x) p[i] = make_uint4(0u, 0u, 0u, 0u);
+}
+
 }  // namespace
 
 // ------------------------------------------------------------------ host
 namespace {
 
 constexpr int kMaxGrid = 256;  // bound on the grid, so scratch sizes need no device query
+// The B image costs two small launches; it pays when every CTA has enough
+// units to amortise them (measured: the 19968 x 6656 gate/up, 53 units per
+// CTA, and the 6656 x 19968 down projection, 27; not the 1-15 MB attention
+// projections, 1-6).
+constexpr int64_t kImgMinUnitsPerCta = 8;
 
 struct MvtGeo {
     int P = 1, ntiles = 0, grid = 0, maxparts = 1, ns = 0, tiles_per_cta = 0;
@@ -1098,7 +1175,10 @@ int tile_count(int nmat, int64_t rows, int P) {
 }
 
 // Geometry of one launch; false if the shape does not fit this kernel.
-bool mvt_geometry(int qtype, int nmat, int64_t rows, int64_t cols, int M, MvtGeo& g, bool whole_tiles) {
+// img: several rows of x with the B image built once per call (the builders
+// need no ring of x).
+bool mvt_geometry(int qtype, int nmat, int64_t rows, int64_t cols, int M, MvtGeo& g, bool whole_tiles,
+                  bool img = false) {
     if (qtype != MUSER_Q4_K && qtype != MUSER_Q6_K) return false;
     if (nmat == 2 && qtype != MUSER_Q4_K) return false;
     if (cols % kQK != 0 || rows < 1 || M < 1 || M > 16) return false;
@@ -1134,7 +1214,7 @@ bool mvt_geometry(int qtype, int nmat, int64_t rows, int64_t cols, int M, MvtGeo
                                   : static_cast<uint32_t>(((nsb + 3) & ~3) * 4 + (qtype == MUSER_Q4_K ? nsb * 8 * 4 : 0));
     g.b_off = (g.x_off + xbytes + 127) / 128 * 128;
     // several rows: kNB B slabs, then two builder warps' kNB slots of 8 rows of x
-    const uint32_t bbytes = multi ? static_cast<uint32_t>(kNB * 16384 + 2 * kNB * 8192)
+    const uint32_t bbytes = multi ? static_cast<uint32_t>(kNB * 16384 + (img ? 0 : 2 * kNB * 8192))
                                   : static_cast<uint32_t>(nsb * 1024 + 512);
     g.stage_off = (g.b_off + bbytes + 1023) / 1024 * 1024;
     const uint32_t stage = 128u * (qtype == MUSER_Q4_K ? 144u : 240u);
@@ -1193,6 +1273,24 @@ int encode_map_f32(CUtensorMap* m, const void* base, uint64_t inner, uint64_t ou
     return MUSER_OK;
 }
 
+// A small kernel launched with programmatic stream serialization.
+template <typename... KArgs, typename... Args>
+int launch_pdl(void (*kern)(KArgs...), int grid, int threads, cudaStream_t stream, Args... args) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(threads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+    if (e != cudaSuccess) return cuda_fail(e, "mvt: cudaLaunchKernelEx (B image)");
+    return check_launch("mvt B image");
+}
+
 template <int QT, int EPI, bool MULTI>
 int launch_mvt_t(MvtArgs a, const MvtGeo& g, cudaStream_t stream) {
     constexpr int NMAT = (EPI == kEpiSiluMul) ? 2 : 1;
@@ -1239,10 +1337,23 @@ bool mvt_supported(int qtype, int nmat, int64_t rows, int64_t cols, int M) {
     return mvt_geometry(qtype, nmat, rows, cols, M, g, true);
 }
 
+// Launches of one launch_mvt call with scratch of mvt_scratch_bytes(): three
+// with the B image (built before, cleared after), else one; 0 if unsupported.
+int mvt_launches(int qtype, int nmat, int64_t rows, int64_t cols, int M) {
+    MvtGeo g;
+    if (!mvt_geometry(qtype, nmat, rows, cols, M, g, false)) return 0;
+    return M > 1 && static_cast<int64_t>(g.ntiles) * (cols / kQK) >= kImgMinUnitsPerCta * g.grid ? 3 : 1;
+}
+
 // Scratch of the even split: per-tile tickets and the tail counter, then
 // ntiles + grid - 1 partial slots of 128 floats per row of x.  Depends only
 // on the tile count and the grid bound, not on the device.
 size_t mvt_scratch_bytes(int qtype, int nmat, int64_t rows, int64_t cols, int M) {
+    const size_t split = mvt_split_scratch_bytes(qtype, nmat, rows, cols, M);
+    return split && M > 1 ? split + static_cast<size_t>(cols / kQK) * kBImg : split;
+}
+
+size_t mvt_split_scratch_bytes(int qtype, int nmat, int64_t rows, int64_t cols, int M) {
     if (qtype != MUSER_Q4_K && qtype != MUSER_Q6_K) return 0;
     if (cols % kQK != 0 || rows < 1 || M < 1 || M > 16) return 0;
     const int64_t rowbytes = (cols / kQK) * (qtype == MUSER_Q4_K ? kQ4KBytes : kQ6KBytes);
@@ -1256,11 +1367,16 @@ size_t mvt_scratch_bytes(int qtype, int nmat, int64_t rows, int64_t cols, int M)
 // scratch == nullptr: whole tiles per CTA (no partial sums).  Otherwise the
 // even split, with `scratch` of mvt_scratch_bytes(), zero-filled, left zeroed.
 // The tail epilogue is for one row of x and needs scratch.
-int launch_mvt(int qtype, int epi, MvtArgs a, void* scratch, cudaStream_t s) {
+int launch_mvt(int qtype, int epi, MvtArgs a, void* scratch, size_t scratch_bytes, cudaStream_t s) {
     const int nmat = epi == kEpiSiluMul ? 2 : 1;
     const int64_t cols = static_cast<int64_t>(a.nsb) * kQK;
     MvtGeo g;
     if (!mvt_geometry(qtype, nmat, a.rows, cols, a.M, g, scratch == nullptr))
+        return set_error(MUSER_ERR_UNSUPPORTED, "mvt: shape not supported");
+    const bool img = scratch != nullptr && a.M > 1 &&
+                     scratch_bytes >= mvt_scratch_bytes(qtype, nmat, a.rows, cols, a.M) &&
+                     static_cast<int64_t>(g.ntiles) * a.nsb >= kImgMinUnitsPerCta * g.grid;
+    if (img && !mvt_geometry(qtype, nmat, a.rows, cols, a.M, g, false, true))
         return set_error(MUSER_ERR_UNSUPPORTED, "mvt: shape not supported");
     if (epi == kEpiTail && (scratch == nullptr || a.M != 1))
         return set_error(MUSER_ERR_UNSUPPORTED, "mvt: the tail epilogue needs scratch and one row of x");
@@ -1273,14 +1389,31 @@ int launch_mvt(int qtype, int epi, MvtArgs a, void* scratch, cudaStream_t s) {
     a.b_off = g.b_off;
     a.stage_off = g.stage_off;
     a.xch_off = g.xch_off;
+    a.bimg = nullptr;
     if (scratch != nullptr) {
         const size_t ticks = (static_cast<size_t>(g.ntiles) + 1) * sizeof(unsigned);
         a.tick = static_cast<unsigned*>(scratch);
         a.part = reinterpret_cast<float*>(static_cast<uint8_t*>(scratch) + (ticks + 255) / 256 * 256);
+        if (img)
+            a.bimg = reinterpret_cast<const uint8_t*>(a.part) +
+                     static_cast<size_t>(g.ntiles + kMaxGrid) * 16 * 128 * sizeof(float);
     }
     if (a.status == nullptr) a.status = device_status_word();
     if (a.status == nullptr) return set_error(MUSER_ERR_CUDA, "mvt: no device status word");
     const bool multi = a.M > 1;
+    if (a.bimg != nullptr) {
+        // the B image: built before the matvec, zeroed after it
+        uint8_t* img = const_cast<uint8_t*>(a.bimg);
+        MUSER_TRY(qtype == MUSER_Q4_K ? launch_pdl(mvt_prep_kernel<MUSER_Q4_K>, a.nsb, 64, s, a.x, a.M, a.nsb, img)
+                                      : launch_pdl(mvt_prep_kernel<MUSER_Q6_K>, a.nsb, 64, s, a.x, a.M, a.nsb, img));
+        int r = MUSER_ERR_UNSUPPORTED;
+        if (qtype == MUSER_Q4_K && epi == kEpiSiluMul) r = launch_mvt_t<MUSER_Q4_K, kEpiSiluMul, true>(a, g, s);
+        else if (qtype == MUSER_Q4_K && epi == kEpiStore) r = launch_mvt_t<MUSER_Q4_K, kEpiStore, true>(a, g, s);
+        else if (qtype == MUSER_Q6_K && epi == kEpiStore) r = launch_mvt_t<MUSER_Q6_K, kEpiStore, true>(a, g, s);
+        else return set_error(MUSER_ERR_UNSUPPORTED, "mvt: no kernel for qtype %d epilogue %d", qtype, epi);
+        MUSER_TRY(r);
+        return launch_pdl(mvt_clear_kernel, a.nsb, 256, s, img, a.nsb);
+    }
     if (qtype == MUSER_Q4_K) {
         if (epi == kEpiSiluMul)
             return multi ? launch_mvt_t<MUSER_Q4_K, kEpiSiluMul, true>(a, g, s) : launch_mvt_t<MUSER_Q4_K, kEpiSiluMul, false>(a, g, s);

@@ -92,7 +92,9 @@ def test_stack_launch_counts():
     fake = mu.FfnLayer(16, 32, 48, 64, 80, mu.MUSER_Q4_K, mu.MUSER_Q6_K)
     arr = (mu.FfnLayer * 52)(*([fake] * 52))
     assert mu.muser_ffn_stack_launches(arr, 6656, 19968, 1) == 1
-    assert mu.muser_ffn_stack_launches(arr, 6656, 19968, 16) == 1 + 3 * 52
+    # several rows: per layer gate/up and down as tensor-core matvecs (each
+    # with its B image built before and cleared after: three launches) and the tail
+    assert mu.muser_ffn_stack_launches(arr, 6656, 19968, 16) == 1 + 7 * 52
     q4down = mu.FfnLayer(16, 32, 48, 64, 80, mu.MUSER_Q4_K, mu.MUSER_Q4_K)
     arr2 = (mu.FfnLayer * 2)(q4down, q4down)
     assert mu.muser_ffn_stack_launches(arr2, 6656, 19968, 1) == 2 + 2 * 2
