@@ -56,9 +56,9 @@ METRIC = "weight-stream GB/s (% of GB300 HBM peak); decode FFN tokens/sec, 1 GPU
 # was captured on (profiles/ summary); reported as null once the kernel changed.
 # The capture ran 4 layers; the traffic per layer is the same, so the 52-layer
 # launch's figure is 13 x the captured launch's.
-NCU_TRAFFIC = {"kernel": "mvs_kernel<Q4_K,Q6_K>", "bytes_per_launch": 13 * 1038141088, "layers": 52,
+NCU_TRAFFIC = {"kernel": "mvs_kernel<Q4_K,Q6_K>", "bytes_per_launch": 13 * 1038038000, "layers": 52,
                "captured_layers": 4,
-               "source_sha256": "271e3a33d6eec3187f217ca15e32e10a376ee85ae6f84623f1ee544d39ef6b3d",
+               "source_sha256": "a0cd17b5ff439f8e94622ccd1a7db00a478785165544911c3192a06c3df23453",
                "profile": "profiles/mvs_stack_m1_4layers.md"}
 
 

@@ -116,7 +116,11 @@ int muser_qmatvec(int qtype, const void* W, int64_t rows, int64_t cols, const fl
                   float* y, void* stream);
 
 /* Scratch bytes muser_qmatvec_scratch needs (0: the call needs none, as for
- * one row of x and for shapes the tensor-core kernel does not take). */
+ * one row of x and for shapes the tensor-core kernel does not take).  It
+ * covers the tile tickets, the partial sums and, for 2..16 rows of x, the
+ * call's B operand image (x split into binary16 parts once per call, about
+ * 17 KB per 256 inputs, when every SM has enough units to amortise building
+ * it). */
 size_t muser_qmatvec_scratch_bytes(int qtype, int64_t rows, int64_t cols, int M);
 
 /*
@@ -162,7 +166,8 @@ int muser_silu_mul(const float* a, const float* b, float* out, int64_t n, void* 
 int muser_ffn_gate_up_silu(int qtype, const void* Wg, const void* Wu, int64_t ffn,
                            int64_t hidden, const float* x, int M, float* mid, void* stream);
 
-/* Scratch bytes muser_ffn_gate_up_silu_scratch needs (0: the call needs none). */
+/* Scratch bytes muser_ffn_gate_up_silu_scratch needs (0: the call needs
+ * none); as for muser_qmatvec_scratch_bytes, including the B operand image. */
 size_t muser_gate_up_scratch_bytes(int qtype, int64_t ffn, int64_t hidden, int M);
 
 /*
@@ -292,7 +297,9 @@ int muser_ffn_gate_up_silu_tail(int qtype, const void* Wg, const void* Wu, int64
  * one-row kernel (its completion ticket, then one sum of projected^2 per
  * block, which spares the tail one pass over the row) plus the tensor-core
  * kernel's tickets and partial sums for several rows.  256 bytes (the ticket)
- * is the minimum the call accepts. */
+ * is the minimum the call accepts.  With 1 KiB more than
+ * muser_qmatvec_scratch_bytes(qtype, hidden, ffn, M), several rows of x also
+ * take the B operand image described there. */
 size_t muser_scratch_bytes(int64_t hidden, int M);
 
 /*
