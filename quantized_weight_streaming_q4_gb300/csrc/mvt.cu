@@ -1040,14 +1040,16 @@ __global__ void __launch_bounds__(mvt_threads(MULTI), 1)
 #pragma unroll
                     for (int m = 0; m < MB; ++m)
                         if (m < M) own[m * 128 + l] = val[m];
-                    __threadfence();
+                    // the ticket after the readback warps' barrier, with
+                    // acquire-release semantics: it releases their part and
+                    // the last CTA's acquire covers every other part
                     named_sync(kBarReadback, 128);
-                    if (l == 0) flags[1] = (atomicAdd(&p.tick[t], 1u) == static_cast<unsigned>(c1 - c0)) ? 1 : 0;
+                    if (l == 0)
+                        flags[1] = (atom_add_acq_rel_gpu(&p.tick[t], 1u) == static_cast<unsigned>(c1 - c0)) ? 1 : 0;
                     named_sync(kBarReadback, 128);
                     const bool last = flags[1] != 0;
                     named_sync(kBarReadback, 128);
                     if (!last) continue;
-                    __threadfence();
 #pragma unroll
                     for (int m = 0; m < MB; ++m) val[m] = 0.0f;
                     for (int pp = 0; pp <= c1 - c0; ++pp) {
@@ -1080,9 +1082,8 @@ __global__ void __launch_bounds__(mvt_threads(MULTI), 1)
                             if (m < M) p.y[static_cast<int64_t>(m) * p.rows + row] = val[m];
                     }
                     if constexpr (EPI == kEpiTail) {
-                        __threadfence();
                         named_sync(kBarReadback, 128);
-                        if (l == 0 && atomicAdd(&p.tick[p.ntiles], 1u) == static_cast<unsigned>(p.ntiles - 1))
+                        if (l == 0 && atom_add_acq_rel_gpu(&p.tick[p.ntiles], 1u) == static_cast<unsigned>(p.ntiles - 1))
                             flags[0] = 1;
                     }
                 }
@@ -1097,7 +1098,6 @@ __global__ void __launch_bounds__(mvt_threads(MULTI), 1)
     }
     if constexpr (EPI == kEpiTail && !MULTI) {
         if (ok && flags[0]) {
-            __threadfence();
             block_dual_tail_row(p.resid, p.y, p.out, p.w1, p.w2, static_cast<int>(p.rows), p.eps1, p.eps2, red);
             if (tid == 0) p.tick[p.ntiles] = 0u;
         }
