@@ -671,7 +671,8 @@ def run_attn(args, rank, world):
     rows4 = (ctypes.c_int64 * 4)(QD, KVD, KVD, QD)
     ys4 = (ctypes.c_void_p * 4)(q.data_ptr(), k.data_ptr(), v.data_ptr(), g.data_ptr())
     w4 = [(ctypes.c_void_p * 4)(*[d[n].data_ptr() for n in ("Wq", "Wk", "Wv", "Wg")]) for d in layers]
-    nscr = max(mu.muser_qmatvec_scratch_bytes(12, r, c, M) for r, c in ((QD, H), (KVD, H), (H, QD)))
+    nscr = max([mu.muser_qmatvec_scratch_bytes(12, r, c, M) for r, c in ((QD, H), (KVD, H), (H, QD))] +
+               [L.muser_qmatvec_group_scratch_bytes(12, 4, rows4, H, M)])
     scratch = torch.zeros(max(nscr, 16) // 4 + 64, dtype=torch.float32, device="cuda")
     outs4 = (q, k, v, g)
     # one row of x: each fused boundary reads the residual from one row and
@@ -693,12 +694,14 @@ def run_attn(args, rank, world):
             if ev is not None:
                 ev[0].record(stream)
             if M > 1:
+                # the previous tail (in place), then Q, K, V and gate as one
+                # tensor-core launch on the shared x
                 if prev is not None:
                     rc("tail", L.muser_fused_residual_dual_rmsnorm(
                         r.data_ptr(), proj.data_ptr(), x.data_ptr(), prev["w_post"].data_ptr(),
                         prev["w_ffn"].data_ptr(), H, M, 1e-8, 1e-5, sh))
-                for n, nrows, y in zip(("Wq", "Wk", "Wv", "Wg"), (QD, KVD, KVD, QD), outs4):
-                    split_mv(d[n], nrows, H, x, y)
+                rc("qkvg", L.muser_qmatvec_group_scratch(12, 4, w4[l], rows4, H, x.data_ptr(), M, ys4,
+                                                         scratch.data_ptr(), nscr, sh))
             elif prev is None:
                 rc("qkvg", L.muser_qmatvec_group(12, 4, w4[l], rows4, H, x.data_ptr(), M, ys4, sh))
             else:
@@ -796,8 +799,8 @@ def run_attn(args, rank, world):
         "hbm_frac_of_" + peak_kind: round(gbs / world / peak, 4),
         "roofline": {"bound": "hbm", "kernel": ("muser_qmatvec_group_tail (Q, K, V, gate Q4_K with the previous "
                                                 "tail: one launch)" if M == 1 else
-                                                f"the previous tail, then Q, K, V, gate by muser_qmatvec_scratch "
-                                                f"(tensor cores split over the SMs), M={M}"),
+                                                f"the previous tail, then Q, K, V, gate by muser_qmatvec_group_scratch "
+                                                f"(one tensor-core launch, units split over the SMs), M={M}"),
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "traffic": None, "algorithmic_bytes_per_launch": q_bytes, "mean_launch_us": round(q_ms * 1e3, 2),
                      "second_kernel": {"name": "muser_qmatvec (o_proj)" if M == 1 else
@@ -810,9 +813,10 @@ def run_attn(args, rank, world):
                 "api": ("per-layer muser_qmatvec_group[_tail] / muser_qmatvec calls" if M == 1 else
                         "per-layer muser_fused_residual_dual_rmsnorm and muser_qmatvec_scratch calls") +
                        ", host residual in, x out"},
-        # M = 16: per layer the tail (after the first) and five tensor-core matvecs (too few units per CTA
-        # for the prebuilt B image: one launch each)
-        "gpu_launches": args.steps * ((2 + 2 * nl) if M == 1 else (1 + 6 * nl)),
+        # M = 16: the entry norm; per layer the tail (after the first), the grouped Q/K/V/gate launch (1,768
+        # units, above 8 per CTA: its B image is built before it and cleared after, three launches) and o_proj
+        # (832 units, one launch); the last tail
+        "gpu_launches": args.steps * ((2 + 2 * nl) if M == 1 else (1 + 5 * nl)),
         "clocks": clock, "device_status": mu.muser_device_status(), "weights_generation_s": round(gen_s, 1),
     }
 

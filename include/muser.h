@@ -215,6 +215,28 @@ int muser_fused_residual_dual_rmsnorm(float* residual, const float* src, float* 
 int muser_qmatvec_group(int qtype, int n, const void* const* W, const int64_t* rows, int64_t cols,
                         const float* x, int M, float* const* y, void* stream);
 
+/* Scratch bytes muser_qmatvec_group_scratch needs for one tensor-core launch
+ * over the whole group (0: the group runs as muser_qmatvec_group: one row of
+ * x, a type other than Q4_K, or a shape the tensor-core kernel does not take).
+ * rows: host array of n entries. */
+size_t muser_qmatvec_group_scratch_bytes(int qtype, int n, const int64_t* rows, int64_t cols, int M);
+
+/*
+ * muser_qmatvec_group_scratch -- the same results as muser_qmatvec_group.
+ *   With 2..16 rows of x, Q4_K and caller scratch of at least
+ *   muser_qmatvec_group_scratch_bytes(...) bytes, the n matrices run as one
+ *   tensor-core launch: each matrix's rows start a 128-row tile of one
+ *   virtual matrix, the (tile, super-block) units spread over every SM and x
+ *   is converted once for all of them (Ch 10 Figure 10.1 box 4: one group on
+ *   one input).  Otherwise as muser_qmatvec_group (scratch unused, may be
+ *   NULL).  scratch: 16-byte aligned, owned by the caller, zero-filled before
+ *   its first use and left zero-filled by every call; calls that can run at
+ *   the same time must not share it.
+ */
+int muser_qmatvec_group_scratch(int qtype, int n, const void* const* W, const int64_t* rows, int64_t cols,
+                                const float* x, int M, float* const* y, void* scratch, size_t scratch_bytes,
+                                void* stream);
+
 /*
  * muser_qmatvec_group_tail -- the previous sub-block's dual-eps tail, then
  *   the group on its output: as muser_fused_residual_dual_rmsnorm (src =
@@ -223,9 +245,11 @@ int muser_qmatvec_group(int qtype, int n, const void* const* W, const int64_t* r
  *   launch, every block for itself.  residual_out, residual and scratch as
  *   for muser_ffn_gate_up_silu_tail: a distinct residual_out takes the
  *   updated residual; NULL updates `residual` in place through the ticket in
- *   `scratch`.  projected, residual, x_out (and residual_out): device f32
- *   [M*cols], distinct; w1, w2: device f32 [cols]; cols % 4 == 0;
- *   eps1, eps2 > 0.
+ *   `scratch`.  With 2..16 rows of x the tail runs on its own, and scratch of
+ *   at least muser_qmatvec_group_scratch_bytes(...) bytes takes the group's
+ *   one tensor-core launch (as muser_qmatvec_group_scratch).
+ *   projected, residual, x_out (and residual_out): device f32 [M*cols],
+ *   distinct; w1, w2: device f32 [cols]; cols % 4 == 0; eps1, eps2 > 0.
  */
 int muser_qmatvec_group_tail(int qtype, int n, const void* const* W, const int64_t* rows, int64_t cols,
                              const float* projected, float* residual, float* residual_out, const float* w1,

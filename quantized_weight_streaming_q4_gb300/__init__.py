@@ -106,6 +106,8 @@ def lib():
             "muser_scale_softcap": (I, [P, I64, F, F, P]),
             "muser_lm_head": (I, [I, P, I64, I64, P, I, P, F, F, P]),
             "muser_qmatvec_group_tail": (I, [I, I, P, P, I64, P, P, P, P, P, F, F, P, I, P, P, SZ, P]),
+    "muser_qmatvec_group_scratch_bytes": (SZ, [I, I, P, I64, I]),
+    "muser_qmatvec_group_scratch": (I, [I, I, P, P, I64, P, I, P, P, SZ, P]),
             "muser_fused_residual_dual_rmsnorm": (I, [P, P, P, P, P, I, I, F, F, P]),
             "muser_scratch_bytes": (SZ, [I64, I]),
             "muser_qmatvec_residual_dual_rmsnorm": (I, [I, P, I64, I64, P, I, P, P, P, P, P, F, F, P,
@@ -263,6 +265,19 @@ def muser_qmatvec_group(qtype, Ws, rows, cols: int, x, M: int, ys, stream=None) 
     n, wa, ra, ya = _group_arrays(Ws, rows, ys)
     _check("muser_qmatvec_group",
            lib().muser_qmatvec_group(_qt(qtype), n, wa, ra, cols, _ptr(x), M, ya, _stream(stream)))
+
+
+def muser_qmatvec_group_scratch_bytes(qtype, rows, cols: int, M: int) -> int:
+    n = len(rows)
+    return int(lib().muser_qmatvec_group_scratch_bytes(_qt(qtype), n, (ctypes.c_int64 * n)(*rows), cols, M))
+
+
+def muser_qmatvec_group_scratch(qtype, Ws, rows, cols: int, x, M: int, ys, scratch, scratch_bytes: int,
+                                stream=None) -> None:
+    n, wa, ra, ya = _group_arrays(Ws, rows, ys)
+    _check("muser_qmatvec_group_scratch",
+           lib().muser_qmatvec_group_scratch(_qt(qtype), n, wa, ra, cols, _ptr(x), M, ya, _ptr(scratch),
+                                             scratch_bytes, _stream(stream)))
 
 
 def muser_qmatvec_group_tail(qtype, Ws, rows, cols: int, projected, residual, w1, w2, eps1: float, eps2: float,

@@ -580,12 +580,24 @@ static int check_group(const char* fn, int qtype, int n, const void* const* W, c
     return MUSER_OK;
 }
 
+// Scratch of the grouped tensor-core launch (0: the group does not take it).
+static size_t group_scratch_bytes(int qtype, int n, const int64_t* rows, int64_t cols, int M) {
+    if (qtype != MUSER_Q4_K || M < 2 || M > MUSER_MAX_M || n < 1 || n > kMvtMaxSeg || rows == nullptr) return 0;
+    for (int i = 0; i < n; ++i)
+        if (rows[i] < 1) return 0;
+    const int64_t vrows = mvt_group_rows(n, rows);
+    if (!mvt_supported(qtype, 1, vrows, cols, M)) return 0;
+    return mvt_scratch_bytes(qtype, 1, vrows, cols, M);
+}
+
 // One launch over the group's rows when one row of x, Q4_K (rows of whole
-// 16-byte units) and the one-token kernel fit; otherwise one call per matrix.
+// 16-byte units) and the one-token kernel fit; with 2..16 rows of x, Q4_K and
+// enough scratch, one tensor-core launch over the group's row tiles;
+// otherwise one call per matrix.
 static int group_launch(int qtype, int n, const void* const* W, const int64_t* rows, int64_t cols, const float* x,
                         int M, float* const* y, const float* projected, float* residual, float* resid_out,
                         const float* w1, const float* w2, float eps1, float eps2, float* x_out, unsigned* ticket,
-                        cudaStream_t s) {
+                        cudaStream_t s, void* gscratch = nullptr, size_t gscratch_bytes = 0) {
     const bool tail = projected != nullptr;
     const bool fused = M == 1 && qtype == MUSER_Q4_K &&
                        (tail ? mv1_tail_prologue_supported(qtype, cols) : mv1_supported(qtype, cols));
@@ -620,8 +632,44 @@ static int group_launch(int qtype, int n, const void* const* W, const int64_t* r
         MUSER_TRY(dual_tail_to(residual, resid_out, projected, x_out, w1, w2, static_cast<int>(cols), M, eps1, eps2, s));
         xin = x_out;
     }
+    const size_t gneed = group_scratch_bytes(qtype, n, rows, cols, M);
+    if (gneed > 0 && gscratch != nullptr && gscratch_bytes >= gneed) {
+        MvtArgs t{};
+        t.nseg = n;
+        for (int i = 0; i < n; ++i) {
+            t.seg_W[i] = static_cast<const uint8_t*>(W[i]);
+            t.seg_rows[i] = rows[i];
+            t.seg_y[i] = y[i];
+        }
+        t.W[0] = t.W[1] = t.seg_W[0];
+        t.rows = mvt_group_rows(n, rows);
+        t.nsb = static_cast<int>(cols / kQK);
+        t.x = xin;
+        t.M = M;
+        return launch_mvt(qtype, kEpiStore, t, gscratch, gscratch_bytes, s);
+    }
     for (int i = 0; i < n; ++i) MUSER_TRY(muser_qmatvec(qtype, W[i], rows[i], cols, xin, M, y[i], s));
     return MUSER_OK;
+}
+
+size_t muser_qmatvec_group_scratch_bytes(int qtype, int n, const int64_t* rows, int64_t cols, int M) {
+    return group_scratch_bytes(qtype, n, rows, cols, M);
+}
+
+int muser_qmatvec_group_scratch(int qtype, int n, const void* const* W, const int64_t* rows, int64_t cols,
+                                const float* x, int M, float* const* y, void* scratch, size_t scratch_bytes,
+                                void* stream) {
+    clear_error();
+    const char* fn = "muser_qmatvec_group_scratch";
+    MUSER_TRY(check_group(fn, qtype, n, W, rows, cols, x, M, y));
+    const size_t need = group_scratch_bytes(qtype, n, rows, cols, M);
+    if (need > 0) {
+        MUSER_TRY(check_f32(fn, "scratch", scratch));
+        if (scratch_bytes < need)
+            return set_error(MUSER_ERR_INVALID_ARG, "%s: scratch_bytes %zu < %zu", fn, scratch_bytes, need);
+    }
+    return group_launch(qtype, n, W, rows, cols, x, M, y, nullptr, nullptr, nullptr, nullptr, nullptr, 0.f, 0.f,
+                        nullptr, nullptr, as_stream(stream), scratch, scratch_bytes);
 }
 
 int muser_qmatvec_group(int qtype, int n, const void* const* W, const int64_t* rows, int64_t cols, const float* x,
@@ -649,8 +697,11 @@ int muser_qmatvec_group_tail(int qtype, int n, const void* const* W, const int64
     if (x_out == residual || x_out == projected || projected == residual)
         return set_error(MUSER_ERR_INVALID_ARG, "%s: projected, residual and x_out must be distinct", fn);
     MUSER_TRY(check_residual_out(fn, residual_out, residual, projected, x_out, scratch, scratch_bytes));
+    // several rows of x: the tail runs on its own, and scratch of
+    // muser_qmatvec_group_scratch_bytes() or more takes the grouped launch
     return group_launch(qtype, n, W, rows, cols, nullptr, M, y, projected, residual, residual_out, w1, w2, eps1, eps2,
-                        x_out, static_cast<unsigned*>(scratch), as_stream(stream));
+                        x_out, static_cast<unsigned*>(scratch), as_stream(stream), M > 1 ? scratch : nullptr,
+                        M > 1 ? scratch_bytes : 0);
 }
 
 int muser_scale_softcap(float* logits, int64_t n, float scale, float cap, void* stream) {

@@ -69,6 +69,7 @@ struct MvMArgs {
 };
 int launch_mvM(int qtype, int nmat, int epi, const MvMArgs& a, cudaStream_t s);
 
+constexpr int kMvtMaxSeg = 4;
 // One-token matvec on the tensor cores (mvt.cu).  Gate+up Q4_K with the SiLU
 // epilogue (two matrices), or one Q4_K/Q6_K matrix with the store or tail
 // epilogue.  Work is split into (row tile, super-block) units over all SMs;
@@ -91,6 +92,14 @@ struct MvtArgs {
     // several rows of x with scratch: the B operand of every super-block,
     // built once per call by a prep kernel (slab, then the x sums and scales)
     const uint8_t* bimg;
+    // A group of Q4_K matrices on one x (store epilogue; nseg > 0): segment s
+    // has seg_rows[s] rows (weights seg_W[s], results seg_y[s]) and owns tiles
+    // [seg_t0[s], seg_t0[s+1]) of 128 rows; `rows` is then the tile total * 128.
+    int nseg;
+    const uint8_t* seg_W[kMvtMaxSeg];
+    int64_t seg_rows[kMvtMaxSeg];
+    float* seg_y[kMvtMaxSeg];
+    int seg_t0[kMvtMaxSeg + 1];
     // geometry, filled by the launcher
     int ntiles, P, maxparts, ns, tiles_per_cta;
     uint32_t x_off, b_off, stage_off, xch_off;
@@ -107,6 +116,9 @@ size_t mvt_split_scratch_bytes(int qtype, int nmat, int64_t rows, int64_t cols, 
 int launch_mvt(int qtype, int epi, MvtArgs a, void* scratch, size_t scratch_bytes, cudaStream_t s);
 // Launches one launch_mvt call makes with scratch of mvt_scratch_bytes() (0: unsupported).
 int mvt_launches(int qtype, int nmat, int64_t rows, int64_t cols, int M);
+// Rows of the tile-aligned matrix a group of Q4_K matrices forms in one
+// launch (each matrix starts a 128-row tile).
+int64_t mvt_group_rows(int n, const int64_t* rows);
 // Device address of the status word (mv1.cu), for kernels in other units.
 unsigned* device_status_word();
 

@@ -630,7 +630,8 @@ __device__ __forceinline__ float build_row_quarter(const float* xrow, int q, uin
 template <int QT, int EPI, bool MULTI>
 __global__ void __launch_bounds__(mvt_threads(MULTI), 1)
     mvt_kernel(const MvtArgs p, const __grid_constant__ CUtensorMap map0, const __grid_constant__ CUtensorMap map1,
-               const __grid_constant__ CUtensorMap mapx) {
+               const __grid_constant__ CUtensorMap mapx, const __grid_constant__ CUtensorMap map2,
+               const __grid_constant__ CUtensorMap map3) {
     constexpr int NMAT = (EPI == kEpiSiluMul) ? 2 : 1;
     constexpr int kBlk = (QT == MUSER_Q4_K) ? kQ4KBytes : kQ6KBytes;
     constexpr int RS = (QT == MUSER_Q4_K) ? 144 : 240;  // row slot of a stage (odd multiple of 16 B)
@@ -737,7 +738,15 @@ __global__ void __launch_bounds__(mvt_threads(MULTI), 1)
                     tma_load_2d_hint(dst, &map0, sb * kBlk, t * 64, &full[s], wpol);
                     tma_load_2d_hint(dst + 64 * RS, &map1, sb * kBlk, t * 64, &full[s], wpol);
                 } else if constexpr (QT == MUSER_Q4_K) {
-                    tma_load_2d_hint(dst, &map0, sb * kBlk, t * 128, &full[s], wpol);
+                    if (p.nseg > 0) {
+                        // a group: the segment's own map, its own tile rows
+                        int sg = 0;
+                        while (sg + 1 < p.nseg && t >= p.seg_t0[sg + 1]) ++sg;
+                        const CUtensorMap* mp = sg == 0 ? &map0 : sg == 1 ? &map1 : sg == 2 ? &map2 : &map3;
+                        tma_load_2d_hint(dst, mp, sb * kBlk, (t - p.seg_t0[sg]) * 128, &full[s], wpol);
+                    } else {
+                        tma_load_2d_hint(dst, &map0, sb * kBlk, t * 128, &full[s], wpol);
+                    }
                 } else {
                     // class t % P of block t / P: box from the 16-byte boundary below the block
                     const int64_t off = static_cast<int64_t>(t % p.P) * rowbytes + static_cast<int64_t>(sb) * kBlk;
@@ -1075,6 +1084,15 @@ __global__ void __launch_bounds__(mvt_threads(MULTI), 1)
                             p.y[static_cast<int64_t>(m) * p.rows + row] = silu_mul_f(xch[m * 128 + l], xch[m * 128 + l + 64]);
                     }
                     named_sync(kBarReadback, 128);
+                } else if (EPI == kEpiStore && p.nseg > 0) {
+                    int sg = 0;
+                    while (sg + 1 < p.nseg && t >= p.seg_t0[sg + 1]) ++sg;
+                    const int64_t srow = static_cast<int64_t>(t - p.seg_t0[sg]) * 128 + l, nrows = p.seg_rows[sg];
+                    if (srow < nrows) {
+#pragma unroll
+                        for (int m = 0; m < MB; ++m)
+                            if (m < M) p.seg_y[sg][static_cast<int64_t>(m) * nrows + srow] = val[m];
+                    }
                 } else {
                     if (row < p.rows) {
 #pragma unroll
@@ -1296,15 +1314,25 @@ int launch_mvt_t(MvtArgs a, const MvtGeo& g, cudaStream_t stream) {
     constexpr int NMAT = (EPI == kEpiSiluMul) ? 2 : 1;
     const uint64_t rowbytes = static_cast<uint64_t>(a.nsb) * (QT == MUSER_Q4_K ? kQ4KBytes : kQ6KBytes);
     const uint64_t rows = static_cast<uint64_t>(a.rows);
-    CUtensorMap m0, m1;
+    CUtensorMap m0, m1, m2, m3;
     if constexpr (QT == MUSER_Q4_K) {
         const uint32_t box_y = NMAT == 2 ? 64u : 128u;
-        MUSER_TRY(encode_map(&m0, a.W[0], rowbytes, rows, rowbytes, kQ4KBytes, box_y));
-        MUSER_TRY(encode_map(&m1, a.W[NMAT - 1], rowbytes, rows, rowbytes, kQ4KBytes, box_y));
+        if (a.nseg > 0) {
+            CUtensorMap* ms[kMvtMaxSeg] = {&m0, &m1, &m2, &m3};
+            for (int i = 0; i < kMvtMaxSeg; ++i) {
+                const int j = i < a.nseg ? i : 0;
+                MUSER_TRY(encode_map(ms[i], a.seg_W[j], rowbytes, static_cast<uint64_t>(a.seg_rows[j]), rowbytes,
+                                     kQ4KBytes, 128u));
+            }
+        } else {
+            MUSER_TRY(encode_map(&m0, a.W[0], rowbytes, rows, rowbytes, kQ4KBytes, box_y));
+            MUSER_TRY(encode_map(&m1, a.W[NMAT - 1], rowbytes, rows, rowbytes, kQ4KBytes, box_y));
+            m2 = m3 = m0;
+        }
     } else {
         const uint64_t P = static_cast<uint64_t>(g.P);
         MUSER_TRY(encode_map(&m0, a.W[0], P * rowbytes, rows / P, P * rowbytes, 240u, 128u));
-        m1 = m0;
+        m1 = m2 = m3 = m0;
     }
     CUtensorMap mx = m0;
     if constexpr (MULTI) {
@@ -1325,7 +1353,7 @@ int launch_mvt_t(MvtArgs a, const MvtGeo& g, cudaStream_t stream) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, kern, a, m0, m1, mx);
+    e = cudaLaunchKernelEx(&cfg, kern, a, m0, m1, mx, m2, m3);
     if (e != cudaSuccess) return cuda_fail(e, "mvt: cudaLaunchKernelEx");
     return check_launch("mvt_kernel");
 }
@@ -1335,6 +1363,12 @@ int launch_mvt_t(MvtArgs a, const MvtGeo& g, cudaStream_t stream) {
 bool mvt_supported(int qtype, int nmat, int64_t rows, int64_t cols, int M) {
     MvtGeo g;
     return mvt_geometry(qtype, nmat, rows, cols, M, g, true);
+}
+
+int64_t mvt_group_rows(int n, const int64_t* rows) {
+    int64_t t = 0;
+    for (int i = 0; i < n; ++i) t += (rows[i] + 127) / 128;
+    return t * 128;
 }
 
 // Launches of one launch_mvt call with scratch of mvt_scratch_bytes(): three
@@ -1389,6 +1423,14 @@ int launch_mvt(int qtype, int epi, MvtArgs a, void* scratch, size_t scratch_byte
     a.b_off = g.b_off;
     a.stage_off = g.stage_off;
     a.xch_off = g.xch_off;
+    if (a.nseg > 0) {
+        if (qtype != MUSER_Q4_K || epi != kEpiStore || a.M < 2 || a.nseg > kMvtMaxSeg)
+            return set_error(MUSER_ERR_UNSUPPORTED, "mvt: a group needs Q4_K, the store epilogue and 2..16 rows of x");
+        a.seg_t0[0] = 0;
+        for (int i = 0; i < a.nseg; ++i) a.seg_t0[i + 1] = a.seg_t0[i] + static_cast<int>((a.seg_rows[i] + 127) / 128);
+        if (static_cast<int64_t>(a.seg_t0[a.nseg]) * 128 != a.rows)
+            return set_error(MUSER_ERR_INVALID_ARG, "mvt: group rows must be the tile-aligned total");
+    }
     a.bimg = nullptr;
     if (scratch != nullptr) {
         const size_t ticks = (static_cast<size_t>(g.ntiles) + 1) * sizeof(unsigned);

@@ -184,6 +184,12 @@ def test_group_calls_fail_closed(L):
     assert g(12, 4, W, rows, 6656, FAKE * 6, 17, y, None) == -1         # M = 17
     assert g(12, 4, P3(FAKE, FAKE + 8, FAKE, FAKE), rows, 6656, FAKE * 6, 1, y, None) == -3
     assert g(12, 4, W, rows, 6656, FAKE * 6, 1, P3(FAKE * 2, FAKE * 3 + 4, FAKE * 4, FAKE * 5), None) == -3
+    gs = L.muser_qmatvec_group_scratch
+    assert gs(12, 0, W, rows, 6656, FAKE * 6, 16, y, FAKE * 11, 1 << 20, None) == -1   # no matrices
+    assert gs(12, 4, W, rows, 6656, FAKE * 6, 17, y, FAKE * 11, 1 << 20, None) == -1   # M = 17
+    assert gs(12, 4, W, rows, 6656, FAKE * 6 + 4, 16, y, FAKE * 11, 1 << 20, None) == -3   # misaligned x
+    assert L.muser_qmatvec_group_scratch_bytes(14, 4, rows, 6656, 16) == 0   # Q6_K: per matrix
+    assert L.muser_qmatvec_group_scratch_bytes(12, 4, rows, 6656, 1) == 0    # one row: the one-token kernel
     t = L.muser_qmatvec_group_tail
     args = (12, 4, W, rows, 6656)
     S = (FAKE * 11, 256)                                                 # the ticket scratch

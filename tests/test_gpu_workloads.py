@@ -307,3 +307,44 @@ def test_attention_projection_group(M, with_tail):
         assert_close(host(y[:M * n]).reshape(M, n), ref, f"{name} in the group M={M}", scaled=True)
         check_canary(y, M * n)
     assert mu.muser_device_status() == 0
+
+
+@pytest.mark.parametrize("M", [3, 16])
+@pytest.mark.parametrize("case", ["attention", "ragged", "tail"])
+def test_group_scratch_one_tensor_core_launch(M, case):
+    """Several rows of x with group scratch: the group's matrices run as one
+    tensor-core launch, each matrix starting a 128-row tile (ragged row counts
+    leave partial tiles inside the virtual matrix); every output equals the
+    oracle's matvec, canaries stay, the scratch is left zeroed."""
+    if case == "ragged":
+        rows = (200, 72, 328, 136)
+        mats = [synth.q4k_matrix(r, H, seed=M, layer=i, tensor=synth.T_GATE) for i, r in enumerate(rows)]
+    else:
+        A = synth.attn_layer(2, H)
+        rows = (synth.Q_DIM, synth.KV_DIM, synth.KV_DIM, synth.Q_DIM)
+        mats = [A[n] for n in ("Wq", "Wk", "Wv", "Wg")]
+    nscr = mu.muser_qmatvec_group_scratch_bytes("q4_k", rows, H, M)
+    assert nscr > 0, "the group takes the one-launch tensor-core path"
+    scratch = torch.zeros(nscr // 4 + 4, dtype=torch.float32, device="cuda")
+    ys = [nan_like((M, n), extra=16) for n in rows]
+    if case == "tail":
+        r = synth.residual_rows(M, H, workload=synth.ATTN_WORKLOAD)
+        p = synth.normal((M, H), seed=9, workload=synth.ATTN_WORKLOAD, tensor=synth.T_X) * np.float32(3e5)
+        w1 = synth.norm_weight(H, seed=9, workload=synth.ATTN_WORKLOAD, tensor=synth.T_W1)
+        w2 = synth.norm_weight(H, seed=9, workload=synth.ATTN_WORKLOAD, tensor=synth.T_W2)
+        rd, r_out, x_out = dev(r), nan_like((M, H), extra=16), nan_like((M, H), extra=16)
+        mu.muser_qmatvec_group_tail("q4_k", [dev(m) for m in mats], rows, H, dev(p), rd, dev(w1), dev(w2), 1e-8,
+                                    1e-5, x_out, M, ys, scratch, nscr, residual_out=r_out)
+        r_ref, x = oracle.dual_tail(r, p, w1, w2, 1e-8, 1e-5)
+        assert_close(host(r_out[:M * H]).reshape(M, H), r_ref, "tail residual")
+        assert_close(host(x_out[:M * H]).reshape(M, H), x, "tail x_out")
+        assert np.array_equal(host(rd).reshape(M, H), r)
+    else:
+        x = oracle.rms_norm(synth.normal((M, H), seed=M + 1), synth.norm_weight(H, seed=M + 1), 1e-5)
+        mu.muser_qmatvec_group_scratch("q4_k", [dev(m) for m in mats], rows, H, dev(x), M, ys, scratch, nscr)
+    for i, (m, n, y) in enumerate(zip(mats, rows, ys)):
+        ref = oracle.qmatvec("q4_k", m, n, H, x)
+        assert_close(host(y[:M * n]).reshape(M, n), ref, f"matrix {i} of the group ({case}) M={M}", scaled=True)
+        check_canary(y, M * n)
+    assert not host(scratch).any(), "scratch must be left zeroed"
+    assert mu.muser_device_status() == 0
