@@ -332,8 +332,7 @@ __device__ __forceinline__ void block_dual_tail_row_parts(float* resid, const fl
     float4* o4 = reinterpret_cast<float4*>(out);
     const float4* a4 = reinterpret_cast<const float4*>(w1);
     const float4* b4 = reinterpret_cast<const float4*>(w2);
-    float ss = 0.0f;
-    for (int i = threadIdx.x; i < nparts; i += blockDim.x) ss += __ldcg(parts + i);
+    // the row's loads go out first: the partials' sum waits on its own loads
     float4 pv[V], rv[V], av[V], bv[V];
 #pragma unroll
     for (int u = 0; u < V; ++u) {
@@ -345,6 +344,8 @@ __device__ __forceinline__ void block_dual_tail_row_parts(float* resid, const fl
             bv[u] = __ldg(b4 + i);
         }
     }
+    float ss = 0.0f;
+    for (int i = threadIdx.x; i < nparts; i += blockDim.x) ss += __ldcg(parts + i);
     ss = block_sum(ss, red);
     const float inv1 = 1.0f / sqrtf(ss / static_cast<float>(n) + eps1);
     float sh = 0.0f;
