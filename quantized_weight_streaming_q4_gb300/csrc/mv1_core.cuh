@@ -302,6 +302,19 @@ __device__ __forceinline__ void load_record(SliceQ6& s, const uint8_t* slot) {
 // same input slice, interleaved so each warp has several independent dp4a
 // chains in flight.
 
+// The packed six-bit scales and mins of a Q4_K / Q5_K header (words y, z, w
+// after d, dmin): sub-blocks 0..3 are the low six bits of bytes y (scales)
+// and z (mins); sub-blocks 4..7 take their low four bits from w and their top
+// two bits from the top of y and z.  A slice c uses sub-blocks 2c and 2c+1,
+// so one shift and two masks select its bytes for either half:
+//   scales = ((y >> sh) & m1) | (w & m2),  mins = ((z >> sh) & m1) | ((w >> 4) & m2).
+struct ScaleSel {
+    uint32_t sh, m1, m2;
+};
+__device__ __forceinline__ ScaleSel scale_sel(int c) {
+    return c < 2 ? ScaleSel{0u, 0x3F3F3F3Fu, 0u} : ScaleSel{2u, 0x30303030u, 0x0F0F0F0Fu};
+}
+
 // Q4_K: out[r] = sum over the slice's 64 weights of w * x, with
 // w = d*sc_j*q - dmin*m_j (j = 2c, 2c+1).  Low nibbles are masked in place
 // as the bytes q; high nibbles are masked in place too, as the bytes 16q,
@@ -338,16 +351,15 @@ __device__ __forceinline__ void dot_q4(const SliceQ4& s, const uint8_t* const* b
             acc[r][5] = dp4a_us(qh, s.hi[2][t], acc[r][5]);
         }
     }
+    const ScaleSel k = scale_sel(c);
 #pragma unroll
     for (int r = 0; r < NR; ++r) {
         // sum(q * X) over sub-block 2c, and 16 * sum(q * X) over sub-block 2c+1
         const float flo = combine3(acc[r][0], acc[r][1], acc[r][2]);
         const float fhi = combine3(acc[r][3], acc[r][4], acc[r][5]);
         // six-bit scales/mins of sub-blocks 0..3 (low bits) and 4..7 (split)
-        const uint32_t scw = (c < 2) ? (hd[r].y & 0x3F3F3F3Fu)
-                                     : ((hd[r].w & 0x0F0F0F0Fu) | ((hd[r].y >> 2) & 0x30303030u));
-        const uint32_t mnw = (c < 2) ? (hd[r].z & 0x3F3F3F3Fu)
-                                     : (((hd[r].w >> 4) & 0x0F0F0F0Fu) | ((hd[r].z >> 2) & 0x30303030u));
+        const uint32_t scw = ((hd[r].y >> k.sh) & k.m1) | (hd[r].w & k.m2);
+        const uint32_t mnw = ((hd[r].z >> k.sh) & k.m1) | ((hd[r].w >> 4) & k.m2);
         const float sc_lo = byte_to_f(scw, sel_lo);
         const float sc_hi = byte_to_f16th(scw, sel_hi);  // sc / 16
         const float2 mins = make_float2(byte_to_f(mnw, sel_lo), byte_to_f(mnw, sel_hi));
@@ -401,14 +413,13 @@ __device__ __forceinline__ void dot_q5(const SliceQ4& s, const uint8_t* const* b
             acc[r][5] = dp4a_us(qh, s.hi[2][t], acc[r][5]);
         }
     }
+    const ScaleSel k = scale_sel(c);
 #pragma unroll
     for (int r = 0; r < NR; ++r) {
         const float flo = combine3(acc[r][0], acc[r][1], acc[r][2]);
         const float fhi = combine3(acc[r][3], acc[r][4], acc[r][5]);
-        const uint32_t scw = (c < 2) ? (hd[r].y & 0x3F3F3F3Fu)
-                                     : ((hd[r].w & 0x0F0F0F0Fu) | ((hd[r].y >> 2) & 0x30303030u));
-        const uint32_t mnw = (c < 2) ? (hd[r].z & 0x3F3F3F3Fu)
-                                     : (((hd[r].w >> 4) & 0x0F0F0F0Fu) | ((hd[r].z >> 2) & 0x30303030u));
+        const uint32_t scw = ((hd[r].y >> k.sh) & k.m1) | (hd[r].w & k.m2);
+        const uint32_t mnw = ((hd[r].z >> k.sh) & k.m1) | ((hd[r].w >> 4) & k.m2);
         const float d = h2f(hd[r].x), dmin = h2f(hd[r].x >> 16);
         const float dot = fmaf(byte_to_f(scw, sel_lo), flo, byte_to_f(scw, sel_hi) * fhi);
         const float msum = fmaf(byte_to_f(mnw, sel_lo), s.s_lo, byte_to_f(mnw, sel_hi) * s.s_hi);
