@@ -56,7 +56,10 @@ namespace {
 // stream; at its end the block that took the last ticket recomputes the
 // updated row with the consumers' 1/rms values (the same operations, so the
 // same bits), writes it (and x to p.out) and re-zeroes the ticket.
-template <int QT, int NMAT, int EPI, int XS>
+// ONEG: one row group spans the row (G == 1; the down projections): each
+// warp copies and converts its own input slots.  A separate instantiation,
+// so the other shapes' code is not touched by that path.
+template <int QT, int NMAT, int EPI, int XS, bool ONEG>
 __global__ void __launch_bounds__(512, 1) mv1_kernel(const Mv1Args p) {
     extern __shared__ __align__(128) uint8_t smem[];
     constexpr int kBlk = kBlockBytes<QT>;
@@ -389,7 +392,7 @@ __global__ void __launch_bounds__(512, 1) mv1_kernel(const Mv1Args p) {
                     }
                 }
             }
-        } else if (G == 1) {
+        } else if constexpr (ONEG) {
             // One row group: thread tid owns slot tid, and warp w's 32 slots
             // are the four slices of eight super-blocks.  Each warp copies
             // those blocks' inputs (coalesced, 1 KB per block) and converts
@@ -437,8 +440,8 @@ __global__ void __launch_bounds__(512, 1) mv1_kernel(const Mv1Args p) {
             if (lane == 0) mbar_arrive(xissued);
             cp_async_wait_all();
         }
-        if (XS == kXTail || G > 1) named_barrier_sync(1, ncw * 32);  // the consumer warps only
-        if (G == 1 && XS == kXMemory) {
+        if constexpr (!ONEG) named_barrier_sync(1, ncw * 32);  // the consumer warps only
+        if constexpr (ONEG) {
             // converted above, each thread its own slot
         } else if (QT != MUSER_Q6_K || G > 1) {
             // Every slot converted once, a quarter per thread (the row groups
@@ -692,7 +695,7 @@ bool mv1_tail_prologue_supported(int qtype, int64_t cols) {
     return nsb * 4 * 16 <= 4 * 32 * mv1_geom(qtype, nsb).ncw;
 }
 
-template <int QT, int NMAT, int EPI, int XS>
+template <int QT, int NMAT, int EPI, int XS, bool ONEG = false>
 static int launch_mv1_t(Mv1Args a, cudaStream_t stream) {
     constexpr int kBlk = kBlockBytes<QT>;
     const int nbc = a.nsb * 4;
@@ -757,7 +760,9 @@ static int launch_mv1_t(Mv1Args a, cudaStream_t stream) {
     const int64_t over = a.part_off + xbytes - a.stage_off;
     a.rot = over > 0 ? static_cast<int>((over + per_stage - 1) / per_stage) : 0;
     a.lead = big ? 1 : 2;
-    auto kern = mv1_kernel<QT, NMAT, EPI, XS>;
+    if (ONEG != (geo.G == 1 && XS == kXMemory && NMAT == 1))
+        return set_error(MUSER_ERR_UNSUPPORTED, "mv1: one-row-group instantiation for the wrong geometry");
+    auto kern = mv1_kernel<QT, NMAT, EPI, XS, ONEG>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return cuda_fail(e, "mv1: cudaFuncSetAttribute");
@@ -784,14 +789,27 @@ int launch_mv1(int qtype, int nmat, int epi, const Mv1Args& a, cudaStream_t s, i
             return launch_mv1_t<MUSER_Q4_K, 1, kEpiStore, kXTail>(a, s);
         if (qtype == MUSER_Q6_K && nmat == 2 && epi == kEpiSiluMul)
             return launch_mv1_t<MUSER_Q6_K, 2, kEpiSiluMul, kXTail>(a, s);
-    } else if (qtype == MUSER_Q4_K) {
+    }
+    // one row group (the down projections' rows): the ONEG instantiations
+    const bool oneg = xs == kXMemory && nmat == 1 && mv1_geom(qtype, a.nsb).G == 1;
+    if (oneg) {
+        if (qtype == MUSER_Q4_K && epi == kEpiStore) return launch_mv1_t<MUSER_Q4_K, 1, kEpiStore, kXMemory, true>(a, s);
+        if (qtype == MUSER_Q4_K && epi == kEpiTail) return launch_mv1_t<MUSER_Q4_K, 1, kEpiTail, kXMemory, true>(a, s);
+        if (qtype == MUSER_Q5_K && epi == kEpiStore) return launch_mv1_t<MUSER_Q5_K, 1, kEpiStore, kXMemory, true>(a, s);
+        if (qtype == MUSER_Q6_K && epi == kEpiStore) return launch_mv1_t<MUSER_Q6_K, 1, kEpiStore, kXMemory, true>(a, s);
+        if (qtype == MUSER_Q6_K && epi == kEpiTail) return launch_mv1_t<MUSER_Q6_K, 1, kEpiTail, kXMemory, true>(a, s);
+        if (qtype == MUSER_Q6_K && epi == kEpiSoftcap)
+            return launch_mv1_t<MUSER_Q6_K, 1, kEpiSoftcap, kXMemory, true>(a, s);
+        if (qtype == MUSER_Q4_K && epi == kEpiSoftcap)
+            return launch_mv1_t<MUSER_Q4_K, 1, kEpiSoftcap, kXMemory, true>(a, s);
+    } else if (xs == kXMemory && qtype == MUSER_Q4_K) {
         if (nmat == 1 && epi == kEpiStore) return launch_mv1_t<MUSER_Q4_K, 1, kEpiStore, kXMemory>(a, s);
         if (nmat == 1 && epi == kEpiTail) return launch_mv1_t<MUSER_Q4_K, 1, kEpiTail, kXMemory>(a, s);
         if (nmat == 2 && epi == kEpiSiluMul) return launch_mv1_t<MUSER_Q4_K, 2, kEpiSiluMul, kXMemory>(a, s);
         if (nmat == 1 && epi == kEpiSoftcap) return launch_mv1_t<MUSER_Q4_K, 1, kEpiSoftcap, kXMemory>(a, s);
-    } else if (qtype == MUSER_Q5_K) {
+    } else if (xs == kXMemory && qtype == MUSER_Q5_K) {
         if (nmat == 1 && epi == kEpiStore) return launch_mv1_t<MUSER_Q5_K, 1, kEpiStore, kXMemory>(a, s);
-    } else if (qtype == MUSER_Q6_K) {
+    } else if (xs == kXMemory && qtype == MUSER_Q6_K) {
         if (nmat == 1 && epi == kEpiStore) return launch_mv1_t<MUSER_Q6_K, 1, kEpiStore, kXMemory>(a, s);
         if (nmat == 1 && epi == kEpiTail) return launch_mv1_t<MUSER_Q6_K, 1, kEpiTail, kXMemory>(a, s);
         if (nmat == 2 && epi == kEpiSiluMul) return launch_mv1_t<MUSER_Q6_K, 2, kEpiSiluMul, kXMemory>(a, s);
