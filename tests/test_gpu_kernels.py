@@ -155,7 +155,9 @@ def test_qmatvec_multirow(qtype, M, rows, cols):
 
 
 @pytest.mark.parametrize("qtype,rows,cols", [("q4_k", 4096, 6656), ("q4_k", 256, 6656), ("q4_k", 6656, 4096),
-                                            ("q4_k", 1000, 2048), ("q6_k", 6656, 19968), ("q6_k", 264, 1280)])
+                                            ("q4_k", 1000, 2048), ("q6_k", 6656, 19968), ("q6_k", 264, 1280),
+                                            # enough units per SM for the prebuilt B image, with a partial last tile
+                                            ("q4_k", 9999, 6656), ("q6_k", 6600, 19968)])
 @pytest.mark.parametrize("M", [3, 16])
 def test_qmatvec_scratch_split(qtype, rows, cols, M):
     # the attention-side shapes at several rows of x, split over every SM with
@@ -275,6 +277,29 @@ def test_ffn_gate_up_silu_tail(M, ffn, form):
     assert_close(host(mid[:M * ffn]).reshape(M, ffn), mid_ref, f"gate_up_silu after the tail M={M}", scaled=True)
     check_canary(x_out, M * hidden)
     check_canary(mid, M * ffn)
+    assert mu.muser_device_status() == 0
+
+
+@pytest.mark.parametrize("M", [3, 16])
+def test_ffn_gate_up_silu_scratch_b_image_ragged(M):
+    """Gate/up with caller scratch at a row count whose units exceed 8 per SM
+    (the B operand image path) and whose last tile is partial: equal to the
+    oracle; the scratch (image region included) left zeroed and not overrun."""
+    ffn, hidden = 9999, 6656
+    Wg = synth.q4k_matrix(ffn, hidden, seed=M, tensor=synth.T_GATE)
+    Wu = synth.q4k_matrix(ffn, hidden, seed=M, tensor=synth.T_UP)
+    x = oracle.rms_norm(synth.normal((M, hidden), seed=M + 3), synth.norm_weight(hidden, seed=M + 3), 1e-5)
+    nscr = mu.muser_gate_up_scratch_bytes("q4_k", ffn, hidden, M)
+    scratch = torch.zeros(nscr // 4 + 64, dtype=torch.float32, device="cuda")
+    scratch[nscr // 4:] = 777.0
+    mid = nan_like((M, ffn), extra=32)
+    mu.muser_ffn_gate_up_silu_scratch("q4_k", dev(Wg), dev(Wu), ffn, hidden, dev(x), M, mid, scratch, nscr)
+    ref = oracle.gate_up_silu("q4_k", Wg, Wu, ffn, hidden, x)
+    assert_close(host(mid[:M * ffn]).reshape(M, ffn), ref, f"gate_up_silu image path M={M}", scaled=True)
+    check_canary(mid, M * ffn)
+    sc = host(scratch)
+    assert not np.any(sc[:nscr // 4]), "scratch not left zeroed"
+    assert np.all(sc[nscr // 4:] == 777.0), "write past the scratch"
     assert mu.muser_device_status() == 0
 
 
