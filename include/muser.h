@@ -109,6 +109,10 @@ int muser_dequantize(int qtype, const void* W, int64_t rows, int64_t cols, float
  *   dequantised in registers straight from HBM; sums are binary32.
  *   W: device matrix; x: device f32 [M*cols]; y: device f32 [M*rows].
  *   1 <= M <= 16, cols % 256 == 0, rows >= 1.  x and y must not overlap.
+ *   Q6_K with 2..16 rows of x runs on the tensor cores with the products
+ *   sc * (q - 32) in binary16, exact for sub-block scales in [-62, 62] (the
+ *   book's workloads draw them on [-32, 31]); a scale outside that range sets
+ *   bit 4 of muser_device_status().  One row of x takes any int8 scale.
  *   Intermediate sums are binary32: above |x| of about 1e34 the Q4_K/Q5_K
  *   min terms (a 32-input sum of x times a min of up to 63) can overflow.
  */
@@ -555,7 +559,9 @@ int muser_device_sm_count(void);
 /*
  * muser_device_status -- the library's device status word (0 = clean).  Bit 1:
  *   a kernel gave up a bounded wait on a weight-tile transfer and returned
- *   without finishing its outputs; bit 2: its clean-up wait also gave up.
+ *   without finishing its outputs; bit 2: its clean-up wait also gave up;
+ *   bit 4: a Q6_K sub-block scale outside [-62, 62] reached the tensor-core
+ *   kernel (2..16 rows of x), whose results are then not exact.
  *   Synchronous (reads device memory); reset != 0 clears the word afterwards.
  *   Returns 0xFFFFFFFF if the word cannot be read.
  */

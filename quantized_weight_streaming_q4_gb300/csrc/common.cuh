@@ -40,7 +40,9 @@ inline cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
 
 // Device-side status word: kernels that give up a bounded wait set a bit
 // here instead of hanging; the host can read and clear it.
-enum : unsigned { kDevStatusWaitTimeout = 1u, kDevStatusTxTimeout = 2u };
+// kDevStatusQ6kScale: a Q6_K sub-block scale outside [-62, 62] reached the
+// tensor-core kernel, whose binary16 products are exact only inside it.
+enum : unsigned { kDevStatusWaitTimeout = 1u, kDevStatusTxTimeout = 2u, kDevStatusQ6kScale = 4u };
 unsigned read_device_status(bool reset);
 
 // ------------------------------------------------------------------ device

@@ -683,3 +683,31 @@ def test_lm_head_full_vocabulary():
     check_canary(logits, vocab)
     del Wd
     torch.cuda.empty_cache()
+
+
+def test_q6k_scale_outside_the_tensor_core_range_is_flagged():
+    """Q6_K scales are exact in the tensor-core kernel's binary16 products only
+    on [-62, 62].  A matrix with one scale of 100: one row of x takes it exactly
+    (the oracle's result, no flag); 16 rows through the tensor-core kernel set
+    bit 4 of the device status instead of failing silently."""
+    rows, cols = 1024, 2048
+    W = synth.q6k_matrix(rows, cols, seed=5)
+    Wbig = W.copy()
+    Wbig[37, 192 + 3] = np.uint8(100)       # row 37, super-block 0, sub-block 3: scale 100
+    x1 = synth.normal((1, cols), seed=6, tensor=synth.T_X)
+    assert mu.muser_device_status(1) == 0
+    y1 = nan_like((1, rows))
+    mu.muser_qmatvec("q6_k", dev(Wbig), rows, cols, dev(x1), 1, y1)
+    assert_close(host(y1).reshape(1, rows), oracle.qmatvec("q6_k", Wbig, rows, cols, x1), "M=1 scale 100",
+                 scaled=True)
+    assert mu.muser_device_status() == 0, "the one-token kernel takes any int8 scale"
+    x16 = synth.normal((16, cols), seed=7, tensor=synth.T_X)
+    nscr = mu.muser_qmatvec_scratch_bytes("q6_k", rows, cols, 16)
+    scratch = torch.zeros(max(nscr, 16) // 4 + 4, dtype=torch.float32, device="cuda")
+    y16 = nan_like((16, rows))
+    mu.muser_qmatvec_scratch("q6_k", dev(W), rows, cols, dev(x16), 16, y16, scratch, nscr)
+    assert mu.muser_device_status() == 0, "in-range scales leave the status clean"
+    mu.muser_qmatvec_scratch("q6_k", dev(Wbig), rows, cols, dev(x16), 16, y16, scratch, nscr)
+    torch.cuda.synchronize()
+    assert mu.muser_device_status(1) == 4, "an out-of-range scale on the tensor-core path is flagged"
+    assert mu.muser_device_status() == 0
