@@ -163,10 +163,12 @@ __device__ __forceinline__ uint32_t hfma2u(uint32_t a, uint32_t b, uint32_t c) {
     asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
     return d;
 }
-// Both halves = the binary16 value of f (f exactly representable).
+// Both halves = the binary16 value of f (f exactly representable): one
+// packed conversion.
 __device__ __forceinline__ uint32_t h2rep(float f) {
-    const uint32_t h = __half_as_ushort(__float2half_rn(f));
-    return h | (h << 16);
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %1;" : "=r"(r) : "f"(f));
+    return r;
 }
 
 // Shared-memory loads through the shared window (the pointers are generic).
