@@ -348,3 +348,39 @@ def test_group_scratch_one_tensor_core_launch(M, case):
         check_canary(y, M * n)
     assert not host(scratch).any(), "scratch must be left zeroed"
     assert mu.muser_device_status() == 0
+
+
+def test_group_scratch_edges():
+    """muser_qmatvec_group_scratch refuses scratch below its size before any
+    launch; the group tail at several rows with only the 256-byte ticket scratch
+    runs one launch per matrix and still equals the oracle; one row of x needs
+    no group scratch (size 0) and takes the one-token kernel."""
+    M = 4
+    A = synth.attn_layer(3, H)
+    names, rows = ("Wq", "Wk", "Wv", "Wg"), (synth.Q_DIM, synth.KV_DIM, synth.KV_DIM, synth.Q_DIM)
+    mats = [dev(A[n]) for n in names]
+    x = oracle.rms_norm(synth.normal((M, H), seed=11), synth.norm_weight(H, seed=11), 1e-5)
+    nscr = mu.muser_qmatvec_group_scratch_bytes("q4_k", rows, H, M)
+    assert nscr > 0 and mu.muser_qmatvec_group_scratch_bytes("q4_k", rows, H, 1) == 0
+    small = torch.zeros(nscr // 8, dtype=torch.float32, device="cuda")
+    ys = [nan_like((M, n), extra=16) for n in rows]
+    with pytest.raises(RuntimeError, match="scratch"):
+        mu.muser_qmatvec_group_scratch("q4_k", mats, rows, H, dev(x), M, ys, small, nscr // 2)
+    for n, y in zip(rows, ys):
+        assert torch.isnan(y[:M * n]).all(), "nothing launched"
+    # the tail at several rows with the ticket scratch only: one launch per matrix
+    r = synth.residual_rows(M, H, workload=synth.ATTN_WORKLOAD)
+    p = synth.normal((M, H), seed=12, workload=synth.ATTN_WORKLOAD, tensor=synth.T_X) * np.float32(3e5)
+    w1 = synth.norm_weight(H, seed=12, workload=synth.ATTN_WORKLOAD, tensor=synth.T_W1)
+    w2 = synth.norm_weight(H, seed=12, workload=synth.ATTN_WORKLOAD, tensor=synth.T_W2)
+    tk = torch.zeros(mu.MUSER_BOUNDARY_SCRATCH_BYTES // 4, dtype=torch.int32, device="cuda")
+    rd, x_out = dev(r), nan_like((M, H), extra=16)
+    mu.muser_qmatvec_group_tail("q4_k", mats, rows, H, dev(p), rd, dev(w1), dev(w2), 1e-8, 1e-5, x_out, M, ys, tk)
+    r_ref, xr = oracle.dual_tail(r, p, w1, w2, 1e-8, 1e-5)
+    assert_close(host(rd).reshape(M, H), r_ref, "tail residual (per-matrix path)")
+    for name, n, y in zip(names, rows, ys):
+        assert_close(host(y[:M * n]).reshape(M, n), oracle.qmatvec("q4_k", A[name], n, H, xr),
+                     f"{name} per-matrix path", scaled=True)
+        check_canary(y, M * n)
+    assert not host(tk).any()
+    assert mu.muser_device_status() == 0
