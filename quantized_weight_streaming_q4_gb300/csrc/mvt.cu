@@ -1071,14 +1071,36 @@ __global__ void __launch_bounds__(mvt_threads(MULTI), 1)
                     if (!last) continue;
 #pragma unroll
                     for (int m = 0; m < MB; ++m) val[m] = 0.0f;
-                    for (int pp = 0; pp <= c1 - c0; ++pp) {
-                        float* slot = p.part + static_cast<size_t>(t + c0 + pp) * MB * 128;
+                    // The parts in order (the sum does not depend on timing),
+                    // two at a time and loads only, so their L2 round trips
+                    // overlap; the zeroing stores follow in a pass of their own.
+                    const int np = c1 - c0 + 1;
+                    const float* part0 = p.part + static_cast<size_t>(t + c0) * MB * 128 + l;
+                    int pp = 0;
+                    for (; pp + 1 < np; pp += 2) {
+                        const float* s0 = part0 + static_cast<size_t>(pp) * MB * 128;
+                        const float* s1 = s0 + MB * 128;
+                        float a0[MB], a1[MB];
+#pragma unroll
+                        for (int m = 0; m < MB; ++m) {
+                            a0[m] = m < M ? __ldcg(s0 + m * 128) : 0.0f;
+                            a1[m] = m < M ? __ldcg(s1 + m * 128) : 0.0f;
+                        }
+#pragma unroll
+                        for (int m = 0; m < MB; ++m) val[m] = (val[m] + a0[m]) + a1[m];
+                    }
+                    if (pp < np) {
+                        const float* s0 = part0 + static_cast<size_t>(pp) * MB * 128;
 #pragma unroll
                         for (int m = 0; m < MB; ++m)
-                            if (m < M) {
-                                val[m] += __ldcg(slot + m * 128 + l);
-                                slot[m * 128 + l] = 0.0f;  // leave the scratch zeroed
-                            }
+                            if (m < M) val[m] += __ldcg(s0 + m * 128);
+                    }
+                    // leave the scratch zeroed
+                    for (int q = 0; q < np; ++q) {
+                        float* s0 = p.part + static_cast<size_t>(t + c0 + q) * MB * 128 + l;
+#pragma unroll
+                        for (int m = 0; m < MB; ++m)
+                            if (m < M) s0[m * 128] = 0.0f;
                     }
                     if (l == 0) p.tick[t] = 0u;
                 }
