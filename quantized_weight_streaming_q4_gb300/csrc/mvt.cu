@@ -492,17 +492,18 @@ struct BlockX {
     float esc, sa, sb;
 };
 // The lane's x values of a block: Q4_K v[0] = x[64c + 4t ..], v[1] = x[64c +
-// 32 + 4t ..]; Q6_K v[g] = x[128h + 32g + 4i ..] (g = 0..3).
+// 32 + 4t ..]; Q6_K v[g] = x[128h + 32g + 4i ..] (g = 0..3).  Read through L2:
+// x may be the output of the kernel this one waits for.
 template <int QT>
 __device__ __forceinline__ void block_x_load(const float* xb, int lane, float4* v) {
     if constexpr (QT == MUSER_Q4_K) {
         const int c = lane >> 3, t = lane & 7;
-        v[0] = __ldg(reinterpret_cast<const float4*>(xb + 64 * c + 4 * t));
-        v[1] = __ldg(reinterpret_cast<const float4*>(xb + 64 * c + 32 + 4 * t));
+        v[0] = __ldcg(reinterpret_cast<const float4*>(xb + 64 * c + 4 * t));
+        v[1] = __ldcg(reinterpret_cast<const float4*>(xb + 64 * c + 32 + 4 * t));
     } else {
         const int item = lane & 15, h = item >> 3, i = item & 7;
 #pragma unroll
-        for (int g = 0; g < 4; ++g) v[g] = __ldg(reinterpret_cast<const float4*>(xb + 128 * h + 32 * g + 4 * i));
+        for (int g = 0; g < 4; ++g) v[g] = __ldcg(reinterpret_cast<const float4*>(xb + 128 * h + 32 * g + 4 * i));
     }
 }
 template <int QT>
@@ -1164,12 +1165,18 @@ __global__ void __launch_bounds__(64) mvt_prep_kernel(const float* __restrict__ 
     pdl_launch_dependents();
     pdl_wait();  // x is the previous kernel's output
     const int64_t K = static_cast<int64_t>(nsb) * kQK;
-    for (int i = tid; i < 16 * 64; i += 64) {
-        const int m = i >> 6;
-        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (m < M) v = __ldg(reinterpret_cast<const float4*>(x + m * K + static_cast<int64_t>(sb) * kQK) + (i & 63));
-        reinterpret_cast<float4*>(xs)[i] = v;
+    // all sixteen loads of a thread in flight at once, then the stores; x is
+    // read through L2 (a non-coherent load counts as invariant and may be
+    // moved above the wait for the kernel that writes x)
+    float4 v[16];
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+        const int i = tid + 64 * k, m = i >> 6;
+        v[k] = m < M ? __ldcg(reinterpret_cast<const float4*>(x + m * K + static_cast<int64_t>(sb) * kQK) + (i & 63))
+                     : make_float4(0.f, 0.f, 0.f, 0.f);
     }
+#pragma unroll
+    for (int k = 0; k < 16; ++k) reinterpret_cast<float4*>(xs)[tid + 64 * k] = v[k];
     __syncthreads();
     const int lane = tid & 31, m = 8 * (tid >> 5) + (lane >> 2), q = lane & 3;
     uint8_t* base = img + static_cast<size_t>(sb) * kBImg;
