@@ -766,7 +766,11 @@ __global__ void __launch_bounds__(mvt_threads(MULTI), 1)
             __syncwarp();
         }
     } else {
-        pdl_wait();  // x is the previous kernel's output; outputs are written after it
+        // x is the previous kernel's output, and outputs are written after
+        // it.  With several rows of x the dequantisation and MMA warps read
+        // neither (weights, shared and tensor memory only): they fill the A
+        // stages while the previous kernel finishes.
+        if (!MULTI || !(warp == kMmaWarp || warp < kDeqWarps)) pdl_wait();
         if constexpr (!MULTI) {
             // ---------- one row of x: the whole B operand, one warp per block
             const int bw = warp < kTmaWarp ? warp : warp - 1;
