@@ -175,11 +175,21 @@ Workspace carve(void* base, int64_t hidden, int64_t ffn, int M) {
     return w;
 }
 
+// The gate/up launch that follows a multi-row down projection + tail in a
+// stack: its tail can also write that launch's B image.
+struct NextImage {
+    int qtype;
+    void* scratch;
+    size_t scratch_bytes;
+    bool* built;  // set when the tail wrote it
+};
+
 // Launch the matvec + tail on validated arguments.
 int down_tail_launch(int qtype, const void* Wdown, int64_t hidden, int64_t ffn, const float* mid,
                      int M, float* projected, float* residual, float* out, const float* w1,
                      const float* w2, float eps1, float eps2, void* scratch, size_t scratch_bytes,
-                     cudaStream_t s) {
+                     cudaStream_t s, const NextImage* next = nullptr) {
+    if (next != nullptr) *next->built = false;
     // One token: the CUDA-core kernel mv1 is measured faster than the
     // tensor-core kernel on this shape, so it takes M = 1.
     const bool tc_ok = mvt_supported(qtype, 1, hidden, ffn, M);
@@ -198,6 +208,14 @@ int down_tail_launch(int qtype, const void* Wdown, int64_t hidden, int64_t ffn, 
         a.y = projected;
         MUSER_TRY(launch_mvt(qtype, kEpiStore, a, tc_fits ? static_cast<uint8_t*>(scratch) + kScratchBytes : nullptr,
                              tc_fits ? scratch_bytes - kScratchBytes : 0, s));
+        if (next != nullptr) {
+            const int r = launch_mvt_tail_image(next->qtype, 2, ffn, hidden, M, residual, projected, out, w1, w2, eps1,
+                                                eps2, next->scratch, next->scratch_bytes, s);
+            if (r != MUSER_ERR_UNSUPPORTED) {
+                *next->built = r == MUSER_OK;
+                return r;
+            }
+        }
         return launch_dual_tail(residual, projected, out, w1, w2, static_cast<int>(hidden), M, eps1, eps2, s);
     }
     if (kTensorCoreM1 && M == 1 && tc_fits) {
@@ -266,7 +284,7 @@ bool gate_up_tail_fused(int qtype, int64_t hidden, int M) {
 }
 
 int gate_up_launch(int qtype, const void* Wg, const void* Wu, int64_t ffn, int64_t hidden,
-                   const float* x, int M, float* mid, void* scratch, cudaStream_t s);
+                   const float* x, int M, float* mid, void* scratch, cudaStream_t s, bool image_ready = false);
 
 // The tail with its residual going to resid_out (distinct) or, when that is
 // null, updated in place.
@@ -312,7 +330,7 @@ int gate_up_tail_launch(int qtype, const void* Wg, const void* Wu, int64_t ffn, 
 
 // scratch: the tensor-core kernel's even-split scratch, or null (whole tiles).
 int gate_up_launch(int qtype, const void* Wg, const void* Wu, int64_t ffn, int64_t hidden,
-                   const float* x, int M, float* mid, void* scratch, cudaStream_t s) {
+                   const float* x, int M, float* mid, void* scratch, cudaStream_t s, bool image_ready) {
     if ((M > 1 || kTensorCoreM1) && mvt_supported(qtype, 2, ffn, hidden, M)) {
         MvtArgs a{};
         a.W[0] = static_cast<const uint8_t*>(Wg);
@@ -322,6 +340,7 @@ int gate_up_launch(int qtype, const void* Wg, const void* Wu, int64_t ffn, int64
         a.x = x;
         a.M = M;
         a.y = mid;
+        a.image_ready = image_ready ? 1 : 0;  // written by the previous layer's tail
         return launch_mvt(qtype, kEpiSiluMul, a, scratch, scratch ? mvt_scratch_bytes(qtype, 2, ffn, hidden, M) : 0, s);
     }
     if (M == 1 && mv1_supported(qtype, hidden)) {
@@ -628,12 +647,35 @@ static int group_launch(int qtype, int n, const void* const* W, const int64_t* r
         return launch_mv1(qtype, 1, kEpiStore, a, s, tail ? kXTail : kXMemory);
     }
     const float* xin = x;
+    const size_t gneed = group_scratch_bytes(qtype, n, rows, cols, M);
+    const bool grouped = gneed > 0 && gscratch != nullptr && gscratch_bytes >= gneed;
+    bool image_ready = false;
     if (tail) {
-        MUSER_TRY(dual_tail_to(residual, resid_out, projected, x_out, w1, w2, static_cast<int>(cols), M, eps1, eps2, s));
+        // several rows: the tail, which also builds the grouped launch's B
+        // image of its output when that launch takes one
+        int r = MUSER_ERR_UNSUPPORTED;
+        if (grouped) {
+            float* res = residual;
+            if (resid_out != nullptr) {
+                const cudaError_t e = cudaMemcpyAsync(resid_out, residual, sizeof(float) * static_cast<size_t>(cols) * M,
+                                                      cudaMemcpyDeviceToDevice, s);
+                if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyAsync(residual)");
+                res = resid_out;
+            }
+            r = launch_mvt_tail_image(qtype, 1, mvt_group_rows(n, rows), cols, M, res, projected, x_out, w1, w2, eps1,
+                                      eps2, gscratch, gscratch_bytes, s);
+            if (r != MUSER_OK && r != MUSER_ERR_UNSUPPORTED) return r;
+            if (r == MUSER_ERR_UNSUPPORTED) r = launch_dual_tail(res, projected, x_out, w1, w2, static_cast<int>(cols),
+                                                                 M, eps1, eps2, s);
+            else image_ready = true;
+            MUSER_TRY(r);
+        } else {
+            MUSER_TRY(dual_tail_to(residual, resid_out, projected, x_out, w1, w2, static_cast<int>(cols), M, eps1, eps2,
+                                   s));
+        }
         xin = x_out;
     }
-    const size_t gneed = group_scratch_bytes(qtype, n, rows, cols, M);
-    if (gneed > 0 && gscratch != nullptr && gscratch_bytes >= gneed) {
+    if (grouped) {
         MvtArgs t{};
         t.nseg = n;
         for (int i = 0; i < n; ++i) {
@@ -646,6 +688,7 @@ static int group_launch(int qtype, int n, const void* const* W, const int64_t* r
         t.nsb = static_cast<int>(cols / kQK);
         t.x = xin;
         t.M = M;
+        t.image_ready = image_ready ? 1 : 0;
         return launch_mvt(qtype, kEpiStore, t, gscratch, gscratch_bytes, s);
     }
     for (int i = 0; i < n; ++i) MUSER_TRY(muser_qmatvec(qtype, W[i], rows[i], cols, xin, M, y[i], s));
@@ -847,12 +890,18 @@ int muser_ffn_stack_launches(const muser_ffn_layer* layers, int n_layers, int64_
     if (fused) return 2 + 2 * n_layers;
     if (M == 1) return 1 + 2 * n_layers;
     // several rows: gate/up, the down projection and its tail; a tensor-core
-    // matvec with its B image is three launches (built before, cleared after)
+    // matvec with its B image is three launches (built before, cleared
+    // after), or two when the previous layer's tail built the image
     int n = 1;
+    const size_t gu_bytes = mvt_scratch_bytes(MUSER_Q4_K, 2, ffn, hidden, M);
+    bool image_ready = false;
     for (int l = 0; l < n_layers; ++l) {
         const int gu = mvt_launches(layers[l].gate_up_qtype, 2, ffn, hidden, M);
         const int dn = mvt_launches(layers[l].down_qtype, 1, hidden, ffn, M);
-        n += (gu > 0 ? gu : 1) + (dn > 0 ? dn : 1) + 1;
+        n += (gu > 0 ? gu - (image_ready ? 1 : 0) : 1) + (dn > 0 ? dn : 1) + 1;
+        image_ready = l + 1 < n_layers && M > 1 && mvt_supported(layers[l].down_qtype, 1, hidden, ffn, M) &&
+                      gu_bytes > 0 &&
+                      mvt_tail_image_fits(layers[l + 1].gate_up_qtype, 2, ffn, hidden, M, gu_bytes);
     }
     return n;
 }
@@ -947,15 +996,22 @@ int muser_ffn_stack(const muser_ffn_layer* layers, int n_layers, const float* en
         return dual_tail_to(r_last, r_last == residual ? nullptr : residual, ws.proj, out, Z.post_norm, Z.next_norm,
                             static_cast<int>(hidden), M, eps_post, eps_norm, s);
     }
+    // Several rows: each layer's tail also writes the next gate/up launch's B
+    // image of its output, where that launch takes one.
     float* x = ws.xa;
     float* xnext = ws.xb;
+    bool image_ready = false;
+    const size_t gu_bytes = ws.gu_scratch ? mvt_scratch_bytes(MUSER_Q4_K, 2, ffn, hidden, M) : 0;
     for (int l = 0; l < n_layers; ++l) {
         const muser_ffn_layer& L = layers[l];
-        MUSER_TRY(gate_up_launch(L.gate_up_qtype, L.w_gate, L.w_up, ffn, hidden, x, M, ws.mid, ws.gu_scratch, s));
+        MUSER_TRY(gate_up_launch(L.gate_up_qtype, L.w_gate, L.w_up, ffn, hidden, x, M, ws.mid, ws.gu_scratch, s,
+                                 image_ready));
         float* dst = (l == n_layers - 1) ? out : xnext;
+        NextImage next{l + 1 < n_layers ? layers[l + 1].gate_up_qtype : 0, ws.gu_scratch, gu_bytes, &image_ready};
         MUSER_TRY(down_tail_launch(L.down_qtype, L.w_down, hidden, ffn, ws.mid, M, ws.proj,
                                    residual, dst, L.post_norm, L.next_norm, eps_post, eps_norm,
-                                   ws.scratch, ws.scratch_bytes, s));
+                                   ws.scratch, ws.scratch_bytes, s,
+                                   l + 1 < n_layers && ws.gu_scratch ? &next : nullptr));
         std::swap(x, xnext);
     }
     return MUSER_OK;

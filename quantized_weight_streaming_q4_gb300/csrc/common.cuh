@@ -318,6 +318,80 @@ __device__ __forceinline__ void block_dual_tail_row(float* resid, const float* s
     }
 }
 
+// The same row with the vectors in registers, for a kernel whose one
+// block per row starts before the previous kernel ends (programmatic
+// launch): w1 is read before the wait on it, src and the residual after it,
+// w2 while the second sum is reduced.  Thread t holds float4 t + u * nt (u
+// < V; n / 4 <= V * nt); the per-thread partial sums take its elements in
+// the same order as block_dual_tail_row and the block sums are the same, so
+// the results are equal.  x = w2 * h * inv2 also comes back in xv (zero past
+// the row).
+template <int V>
+__device__ __forceinline__ void dual_tail_row_reg(float* resid, const float* src, float* out, const float* w1,
+                                                  const float* w2, int n, float eps1, float eps2, float* red,
+                                                  float4* xv) {
+    const int n4 = n >> 2, tid = threadIdx.x, nt = blockDim.x;
+    const float4* s4 = reinterpret_cast<const float4*>(src);
+    float4* r4 = reinterpret_cast<float4*>(resid);
+    float4* o4 = reinterpret_cast<float4*>(out);
+    const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+    float4 pv[V], rv[V], av[V], bv[V];
+#pragma unroll
+    for (int u = 0; u < V; ++u) {
+        const int i = tid + u * nt;
+        av[u] = i < n4 ? __ldg(reinterpret_cast<const float4*>(w1) + i) : z;
+    }
+    pdl_launch_dependents();
+    pdl_wait();  // src and the residual are the previous kernels' outputs
+#pragma unroll
+    for (int u = 0; u < V; ++u) {
+        const int i = tid + u * nt;
+        pv[u] = i < n4 ? __ldcg(s4 + i) : z;
+        rv[u] = i < n4 ? __ldcg(r4 + i) : z;
+    }
+    float ss = 0.0f;
+#pragma unroll
+    for (int u = 0; u < V; ++u) {
+        ss = fmaf(pv[u].x, pv[u].x, ss);
+        ss = fmaf(pv[u].y, pv[u].y, ss);
+        ss = fmaf(pv[u].z, pv[u].z, ss);
+        ss = fmaf(pv[u].w, pv[u].w, ss);
+    }
+    ss = block_sum(ss, red);
+    const float inv1 = 1.0f / sqrtf(ss / static_cast<float>(n) + eps1);
+    float sh = 0.0f;
+#pragma unroll
+    for (int u = 0; u < V; ++u) {
+        float4 h;  // zero past the row
+        h.x = fmaf(pv[u].x * inv1, av[u].x, rv[u].x);
+        h.y = fmaf(pv[u].y * inv1, av[u].y, rv[u].y);
+        h.z = fmaf(pv[u].z * inv1, av[u].z, rv[u].z);
+        h.w = fmaf(pv[u].w * inv1, av[u].w, rv[u].w);
+        sh = fmaf(h.x, h.x, sh);
+        sh = fmaf(h.y, h.y, sh);
+        sh = fmaf(h.z, h.z, sh);
+        sh = fmaf(h.w, h.w, sh);
+        rv[u] = h;
+    }
+#pragma unroll
+    for (int u = 0; u < V; ++u) {
+        const int i = tid + u * nt;
+        bv[u] = i < n4 ? __ldg(reinterpret_cast<const float4*>(w2) + i) : z;
+    }
+    sh = block_sum(sh, red);
+    const float inv2 = 1.0f / sqrtf(sh / static_cast<float>(n) + eps2);
+#pragma unroll
+    for (int u = 0; u < V; ++u) {
+        const int i = tid + u * nt;
+        xv[u] = make_float4((rv[u].x * inv2) * bv[u].x, (rv[u].y * inv2) * bv[u].y, (rv[u].z * inv2) * bv[u].z,
+                            (rv[u].w * inv2) * bv[u].w);
+        if (i < n4) {
+            r4[i] = rv[u];
+            o4[i] = xv[u];
+        }
+    }
+}
+
 // The same row of the dual-eps tail when every block of the grid has left
 // its share of sum(src^2) in parts[0..nparts) (the block that wrote those
 // rows of src summed their squares): the first pass is a sum of nparts

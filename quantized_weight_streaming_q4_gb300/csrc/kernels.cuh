@@ -92,6 +92,9 @@ struct MvtArgs {
     // several rows of x with scratch: the B operand of every super-block,
     // built once per call by a prep kernel (slab, then the x sums and scales)
     const uint8_t* bimg;
+    // the image is already in the scratch (launch_mvt_tail_image wrote it
+    // for this x): no prep launch
+    int image_ready;
     // A group of Q4_K matrices on one x (store epilogue; nseg > 0): segment s
     // has seg_rows[s] rows (weights seg_W[s], results seg_y[s]) and owns tiles
     // [seg_t0[s], seg_t0[s+1]) of 128 rows; `rows` is then the tile total * 128.
@@ -114,6 +117,16 @@ size_t mvt_split_scratch_bytes(int qtype, int nmat, int64_t rows, int64_t cols, 
 // mvt_split_scratch_bytes(); from mvt_scratch_bytes() on, several rows of x
 // take the prebuilt B image.
 int launch_mvt(int qtype, int epi, MvtArgs a, void* scratch, size_t scratch_bytes, cudaStream_t s);
+// The dual-eps tail of M rows (as launch_dual_tail, cols inputs) that also
+// writes the B image of its output `out` into `scratch` for a launch_mvt of
+// (qtype, nmat, rows, cols, M) with that scratch, which then takes
+// image_ready.  MUSER_ERR_UNSUPPORTED, with nothing launched, when that
+// launch builds no image or the row is longer than 8,192.
+int launch_mvt_tail_image(int qtype, int nmat, int64_t rows, int64_t cols, int M, float* resid, const float* src,
+                          float* out, const float* w1, const float* w2, float eps1, float eps2, void* scratch,
+                          size_t scratch_bytes, cudaStream_t s);
+// Whether launch_mvt_tail_image takes that shape (with scratch_bytes of scratch).
+bool mvt_tail_image_fits(int qtype, int nmat, int64_t rows, int64_t cols, int M, size_t scratch_bytes);
 // Launches one launch_mvt call makes with scratch of mvt_scratch_bytes() (0: unsupported).
 int mvt_launches(int qtype, int nmat, int64_t rows, int64_t cols, int M);
 // Rows of the tile-aligned matrix a group of Q4_K matrices forms in one

@@ -162,77 +162,17 @@ __global__ void dual_tail_kernel(float* resid, const float* src, float* out, con
     block_dual_tail_row(resid + off, src + off, out + off, w1, w2, n, eps1, eps2, red);
 }
 
-// The same row with the vectors in registers (n / 4 <= V * 1024, V <= 3;
-// longer rows take dual_tail_kernel): one round
-// of loads instead of three passes, the same per-thread partial sums (a
-// thread's elements in the same order) and block reductions, so the results
-// are those of dual_tail_kernel.  w1 is read before the wait on the previous
-// kernel, w2 while the second sum is reduced.
+// The same row with the vectors in registers (dual_tail_row_reg; n / 4 <=
+// V * 1024, V <= 3; longer rows take dual_tail_kernel): one round of loads
+// instead of three passes, with the results of dual_tail_kernel.
 template <int V>  // float4 of each vector per thread: n / 4 <= V * 1024
 __global__ void __launch_bounds__(1024) dual_tail_reg_kernel(float* resid, const float* src, float* out,
                                                               const float* w1, const float* w2, int n, float eps1,
                                                               float eps2) {
     __shared__ float red[33];
-    const int n4 = n >> 2, tid = threadIdx.x, nt = blockDim.x;
     const int64_t off = static_cast<int64_t>(blockIdx.x) * n;
-    const float4* s4 = reinterpret_cast<const float4*>(src + off);
-    float4* r4 = reinterpret_cast<float4*>(resid + off);
-    float4* o4 = reinterpret_cast<float4*>(out + off);
-    const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-    float4 pv[V], rv[V], av[V], bv[V];
-#pragma unroll
-    for (int u = 0; u < V; ++u) {
-        const int i = tid + u * nt;
-        av[u] = i < n4 ? __ldg(reinterpret_cast<const float4*>(w1) + i) : z;
-    }
-    pdl_launch_dependents();
-    pdl_wait();  // src and the residual are the previous kernels' outputs
-#pragma unroll
-    for (int u = 0; u < V; ++u) {
-        const int i = tid + u * nt;
-        pv[u] = i < n4 ? __ldcg(s4 + i) : z;
-        rv[u] = i < n4 ? __ldcg(r4 + i) : z;
-    }
-    float ss = 0.0f;
-#pragma unroll
-    for (int u = 0; u < V; ++u) {
-        ss = fmaf(pv[u].x, pv[u].x, ss);
-        ss = fmaf(pv[u].y, pv[u].y, ss);
-        ss = fmaf(pv[u].z, pv[u].z, ss);
-        ss = fmaf(pv[u].w, pv[u].w, ss);
-    }
-    ss = block_sum(ss, red);
-    const float inv1 = 1.0f / sqrtf(ss / static_cast<float>(n) + eps1);
-    float sh = 0.0f;
-#pragma unroll
-    for (int u = 0; u < V; ++u) {
-        float4 h;  // zero past the row
-        h.x = fmaf(pv[u].x * inv1, av[u].x, rv[u].x);
-        h.y = fmaf(pv[u].y * inv1, av[u].y, rv[u].y);
-        h.z = fmaf(pv[u].z * inv1, av[u].z, rv[u].z);
-        h.w = fmaf(pv[u].w * inv1, av[u].w, rv[u].w);
-        sh = fmaf(h.x, h.x, sh);
-        sh = fmaf(h.y, h.y, sh);
-        sh = fmaf(h.z, h.z, sh);
-        sh = fmaf(h.w, h.w, sh);
-        rv[u] = h;
-    }
-#pragma unroll
-    for (int u = 0; u < V; ++u) {
-        const int i = tid + u * nt;
-        bv[u] = i < n4 ? __ldg(reinterpret_cast<const float4*>(w2) + i) : z;
-    }
-    sh = block_sum(sh, red);
-    const float inv2 = 1.0f / sqrtf(sh / static_cast<float>(n) + eps2);
-#pragma unroll
-    for (int u = 0; u < V; ++u) {
-        const int i = tid + u * nt;
-        if (i < n4) {
-            r4[i] = rv[u];
-            o4[i] = make_float4((rv[u].x * inv2) * bv[u].x, (rv[u].y * inv2) * bv[u].y, (rv[u].z * inv2) * bv[u].z,
-                                (rv[u].w * inv2) * bv[u].w);
-        }
-    }
+    float4 xv[V];
+    dual_tail_row_reg<V>(resid + off, src + off, out + off, w1, w2, n, eps1, eps2, red, xv);
 }
 
 // -------------------------------------------------------------- KV store

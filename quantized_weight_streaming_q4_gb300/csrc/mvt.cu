@@ -561,9 +561,10 @@ __device__ __forceinline__ BlockX<QT> block_x(const float4* pv, int lane) {
 // reads of a warp at most 2-way conflicted; the row's block maximum and the
 // Q4_K sub-block sums need only the 4 lanes of the row.  Returns 2^e, the
 // row's block scale; the sums of sub-blocks 0..7 are valid in lane q == 0.
+// store == false: the lanes only take part in the shuffles.
 template <int QT>
 __device__ __forceinline__ float build_row_quarter(const float* xrow, int q, uint8_t* slab, uint32_t rowoff,
-                                                   float* xsum8) {
+                                                   float* xsum8, bool store_slab = true) {
     float4 v[16];
     if constexpr (QT == MUSER_Q4_K) {
         // B chunk 8c + t (t = q, q + 4): x chunks 16c + t and 16c + 8 + t
@@ -601,6 +602,7 @@ __device__ __forceinline__ float build_row_quarter(const float* xrow, int q, uin
         pack_hl(__fmul2_rn(make_float2(a.y, a.w), d2), hi.y, lo.y);
         pack_hl(__fmul2_rn(make_float2(b.x, b.z), d2), hi.z, lo.z);
         pack_hl(__fmul2_rn(make_float2(b.y, b.w), d2), hi.w, lo.w);
+        if (!store_slab) return;
         uint8_t* ch = slab + chunk * 512 + rowoff;
         *reinterpret_cast<uint4*>(ch) = hi;
         *reinterpret_cast<uint4*>(ch + 16) = lo;
@@ -1196,6 +1198,48 @@ __global__ void __launch_bounds__(64) mvt_prep_kernel(const float* __restrict__ 
     }
 }
 
+// The dual-eps tail of row m = blockIdx.x (dual_tail_row_reg) that also
+// writes row m of every super-block's B image from the row's x, held in
+// shared memory: quad (sb, q) of the first four warps converts quarter q of
+// block sb as the prep kernel does.  Rows of the image past M stay as the
+// zero-filled scratch has them, which the matvec reads as rows of zeros.
+template <int QT, int V>
+__global__ void __launch_bounds__(1024) mvt_tail_image_kernel(float* resid, const float* src, float* out,
+                                                              const float* w1, const float* w2, int n, float eps1,
+                                                              float eps2, uint8_t* img) {
+    extern __shared__ __align__(16) float xrow[];  // n floats
+    __shared__ float red[33];
+    const int m = blockIdx.x, tid = threadIdx.x, n4 = n >> 2, nsb = n / kQK;
+    const int64_t off = static_cast<int64_t>(m) * n;
+    float4 xv[V];
+    dual_tail_row_reg<V>(resid + off, src + off, out + off, w1, w2, n, eps1, eps2, red, xv);
+#pragma unroll
+    for (int u = 0; u < V; ++u) {
+        const int i = tid + u * 1024;
+        if (i < n4) reinterpret_cast<float4*>(xrow)[i] = xv[u];
+    }
+    __syncthreads();
+    if (tid < 128) {
+        const uint32_t rowoff = static_cast<uint32_t>((m >> 2) * 128 + (2 * m & 7) * 16);
+        for (int sb0 = 0; sb0 < nsb; sb0 += 32) {
+            const int sbq = sb0 + (tid >> 2), q = tid & 3;
+            const bool valid = sbq < nsb;
+            const int sb = valid ? sbq : nsb - 1;  // past the row: shuffles only
+            uint8_t* base = img + static_cast<size_t>(sb) * kBImg;
+            float xs8[8];
+            const float e2 = build_row_quarter<QT>(xrow + sb * kQK, q, base, rowoff, xs8, valid);
+            if (valid && q == 0) {
+                float* xr = reinterpret_cast<float*>(base + kSlabBytes);
+                xr[8 * 16 + m] = e2;
+                if constexpr (QT == MUSER_Q4_K) {
+                    *reinterpret_cast<float4*>(xr + 8 * m) = make_float4(xs8[0], xs8[1], xs8[2], xs8[3]);
+                    *reinterpret_cast<float4*>(xr + 8 * m + 4) = make_float4(xs8[4], xs8[5], xs8[6], xs8[7]);
+                }
+            }
+        }
+    }
+}
+
 // Zeroes the B image after the matvec has read it (the caller's scratch is
 // left zero-filled).
 __global__ void __launch_bounds__(256) mvt_clear_kernel(uint8_t* img, int nsb) {
@@ -1441,6 +1485,14 @@ size_t mvt_split_scratch_bytes(int qtype, int nmat, int64_t rows, int64_t cols, 
     return (ticks + 255) / 256 * 256 + static_cast<size_t>(ntiles + kMaxGrid) * MB * 128 * sizeof(float);
 }
 
+// Where the B image sits in the even split's scratch: after the tile
+// tickets and the partial slots.
+uint8_t* image_of(void* scratch, int ntiles) {
+    const size_t ticks = (static_cast<size_t>(ntiles) + 1) * sizeof(unsigned);
+    return static_cast<uint8_t*>(scratch) + (ticks + 255) / 256 * 256 +
+           static_cast<size_t>(ntiles + kMaxGrid) * 16 * 128 * sizeof(float);
+}
+
 // scratch == nullptr: whole tiles per CTA (no partial sums).  Otherwise the
 // even split, with `scratch` of mvt_scratch_bytes(), zero-filled, left zeroed.
 // The tail epilogue is for one row of x and needs scratch.
@@ -1479,18 +1531,19 @@ int launch_mvt(int qtype, int epi, MvtArgs a, void* scratch, size_t scratch_byte
         const size_t ticks = (static_cast<size_t>(g.ntiles) + 1) * sizeof(unsigned);
         a.tick = static_cast<unsigned*>(scratch);
         a.part = reinterpret_cast<float*>(static_cast<uint8_t*>(scratch) + (ticks + 255) / 256 * 256);
-        if (img)
-            a.bimg = reinterpret_cast<const uint8_t*>(a.part) +
-                     static_cast<size_t>(g.ntiles + kMaxGrid) * 16 * 128 * sizeof(float);
+        if (img) a.bimg = image_of(scratch, g.ntiles);
     }
+    if (a.image_ready && a.bimg == nullptr)
+        return set_error(MUSER_ERR_INVALID_ARG, "mvt: a prebuilt B image for a launch that reads none");
     if (a.status == nullptr) a.status = device_status_word();
     if (a.status == nullptr) return set_error(MUSER_ERR_CUDA, "mvt: no device status word");
     const bool multi = a.M > 1;
     if (a.bimg != nullptr) {
         // the B image: built before the matvec, zeroed after it
         uint8_t* img = const_cast<uint8_t*>(a.bimg);
-        MUSER_TRY(qtype == MUSER_Q4_K ? launch_pdl(mvt_prep_kernel<MUSER_Q4_K>, a.nsb, 64, s, a.x, a.M, a.nsb, img)
-                                      : launch_pdl(mvt_prep_kernel<MUSER_Q6_K>, a.nsb, 64, s, a.x, a.M, a.nsb, img));
+        if (!a.image_ready)
+            MUSER_TRY(qtype == MUSER_Q4_K ? launch_pdl(mvt_prep_kernel<MUSER_Q4_K>, a.nsb, 64, s, a.x, a.M, a.nsb, img)
+                                          : launch_pdl(mvt_prep_kernel<MUSER_Q6_K>, a.nsb, 64, s, a.x, a.M, a.nsb, img));
         int r = MUSER_ERR_UNSUPPORTED;
         if (qtype == MUSER_Q4_K && epi == kEpiSiluMul) r = launch_mvt_t<MUSER_Q4_K, kEpiSiluMul, true>(a, g, s);
         else if (qtype == MUSER_Q4_K && epi == kEpiStore) r = launch_mvt_t<MUSER_Q4_K, kEpiStore, true>(a, g, s);
@@ -1511,6 +1564,50 @@ int launch_mvt(int qtype, int epi, MvtArgs a, void* scratch, size_t scratch_byte
         if (epi == kEpiTail) return launch_mvt_t<MUSER_Q6_K, kEpiTail, false>(a, g, s);
     }
     return set_error(MUSER_ERR_UNSUPPORTED, "mvt: no kernel for qtype %d epilogue %d", qtype, epi);
+}
+
+bool mvt_tail_image_fits(int qtype, int nmat, int64_t rows, int64_t cols, int M, size_t scratch_bytes) {
+    MvtGeo g;
+    return M >= 2 && M <= 16 && cols % kQK == 0 && cols <= 8192 && (qtype == MUSER_Q4_K || qtype == MUSER_Q6_K) &&
+           mvt_supported(qtype, nmat, rows, cols, M) && mvt_geometry(qtype, nmat, rows, cols, M, g, false) &&
+           scratch_bytes >= mvt_scratch_bytes(qtype, nmat, rows, cols, M) &&
+           static_cast<int64_t>(g.ntiles) * (cols / kQK) >= kImgMinUnitsPerCta * g.grid &&
+           mvt_geometry(qtype, nmat, rows, cols, M, g, false, true);
+}
+
+int launch_mvt_tail_image(int qtype, int nmat, int64_t rows, int64_t cols, int M, float* resid, const float* src,
+                          float* out, const float* w1, const float* w2, float eps1, float eps2, void* scratch,
+                          size_t scratch_bytes, cudaStream_t s) {
+    if (scratch == nullptr || !mvt_tail_image_fits(qtype, nmat, rows, cols, M, scratch_bytes))
+        return MUSER_ERR_UNSUPPORTED;  // no image for this launch: the caller runs the plain tail
+    MvtGeo g;
+    (void)mvt_geometry(qtype, nmat, rows, cols, M, g, false, true);
+    uint8_t* img = image_of(scratch, g.ntiles);
+    const int n = static_cast<int>(cols), v = (n / 4 + 1023) / 1024;
+    const size_t smem = sizeof(float) * static_cast<size_t>(n);
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(static_cast<unsigned>(M));
+    cfg.blockDim = dim3(1024);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e;
+    if (qtype == MUSER_Q4_K)
+        e = v <= 1 ? cudaLaunchKernelEx(&cfg, mvt_tail_image_kernel<MUSER_Q4_K, 1>, resid, src, out, w1, w2, n, eps1,
+                                        eps2, img)
+                   : cudaLaunchKernelEx(&cfg, mvt_tail_image_kernel<MUSER_Q4_K, 2>, resid, src, out, w1, w2, n, eps1,
+                                        eps2, img);
+    else
+        e = v <= 1 ? cudaLaunchKernelEx(&cfg, mvt_tail_image_kernel<MUSER_Q6_K, 1>, resid, src, out, w1, w2, n, eps1,
+                                        eps2, img)
+                   : cudaLaunchKernelEx(&cfg, mvt_tail_image_kernel<MUSER_Q6_K, 2>, resid, src, out, w1, w2, n, eps1,
+                                        eps2, img);
+    if (e != cudaSuccess) return cuda_fail(e, "mvt_tail_image: cudaLaunchKernelEx");
+    return check_launch("mvt_tail_image");
 }
 
 }  // namespace muser

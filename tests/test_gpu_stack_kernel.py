@@ -93,8 +93,10 @@ def test_stack_launch_counts():
     arr = (mu.FfnLayer * 52)(*([fake] * 52))
     assert mu.muser_ffn_stack_launches(arr, 6656, 19968, 1) == 1
     # several rows: per layer gate/up and down as tensor-core matvecs (each
-    # with its B image built before and cleared after: three launches) and the tail
-    assert mu.muser_ffn_stack_launches(arr, 6656, 19968, 16) == 1 + 7 * 52
+    # with its B image built before and cleared after: three launches) and the
+    # tail, which from layer 0 on also builds the next gate/up's image (one
+    # launch fewer per later layer)
+    assert mu.muser_ffn_stack_launches(arr, 6656, 19968, 16) == 1 + 7 + 6 * 51
     q4down = mu.FfnLayer(16, 32, 48, 64, 80, mu.MUSER_Q4_K, mu.MUSER_Q4_K)
     arr2 = (mu.FfnLayer * 2)(q4down, q4down)
     assert mu.muser_ffn_stack_launches(arr2, 6656, 19968, 1) == 2 + 2 * 2

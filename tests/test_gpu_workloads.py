@@ -310,12 +310,14 @@ def test_attention_projection_group(M, with_tail):
 
 
 @pytest.mark.parametrize("M", [3, 16])
-@pytest.mark.parametrize("case", ["attention", "ragged", "tail"])
+@pytest.mark.parametrize("case", ["attention", "ragged", "tail", "tail_in_place"])
 def test_group_scratch_one_tensor_core_launch(M, case):
     """Several rows of x with group scratch: the group's matrices run as one
     tensor-core launch, each matrix starting a 128-row tile (ragged row counts
     leave partial tiles inside the virtual matrix); every output equals the
-    oracle's matvec, canaries stay, the scratch is left zeroed."""
+    oracle's matvec, canaries stay, the scratch is left zeroed.  With the
+    tail (residual_out or in place), the tail kernel also writes the launch's
+    B image of its output (rows of the image past M stay zero)."""
     if case == "ragged":
         rows = (200, 72, 328, 136)
         mats = [synth.q4k_matrix(r, H, seed=M, layer=i, tensor=synth.T_GATE) for i, r in enumerate(rows)]
@@ -327,18 +329,25 @@ def test_group_scratch_one_tensor_core_launch(M, case):
     assert nscr > 0, "the group takes the one-launch tensor-core path"
     scratch = torch.zeros(nscr // 4 + 4, dtype=torch.float32, device="cuda")
     ys = [nan_like((M, n), extra=16) for n in rows]
-    if case == "tail":
+    if case.startswith("tail"):
         r = synth.residual_rows(M, H, workload=synth.ATTN_WORKLOAD)
         p = synth.normal((M, H), seed=9, workload=synth.ATTN_WORKLOAD, tensor=synth.T_X) * np.float32(3e5)
         w1 = synth.norm_weight(H, seed=9, workload=synth.ATTN_WORKLOAD, tensor=synth.T_W1)
         w2 = synth.norm_weight(H, seed=9, workload=synth.ATTN_WORKLOAD, tensor=synth.T_W2)
-        rd, r_out, x_out = dev(r), nan_like((M, H), extra=16), nan_like((M, H), extra=16)
+        in_place = case == "tail_in_place"
+        rd, x_out = dev(r), nan_like((M, H), extra=16)
+        r_out = None if in_place else nan_like((M, H), extra=16)
         mu.muser_qmatvec_group_tail("q4_k", [dev(m) for m in mats], rows, H, dev(p), rd, dev(w1), dev(w2), 1e-8,
                                     1e-5, x_out, M, ys, scratch, nscr, residual_out=r_out)
         r_ref, x = oracle.dual_tail(r, p, w1, w2, 1e-8, 1e-5)
-        assert_close(host(r_out[:M * H]).reshape(M, H), r_ref, "tail residual")
+        if in_place:
+            assert_close(host(rd).reshape(M, H), r_ref, "tail residual (in place)")
+        else:
+            assert_close(host(r_out[:M * H]).reshape(M, H), r_ref, "tail residual")
+            check_canary(r_out, M * H)
+            assert np.array_equal(host(rd).reshape(M, H), r)
         assert_close(host(x_out[:M * H]).reshape(M, H), x, "tail x_out")
-        assert np.array_equal(host(rd).reshape(M, H), r)
+        check_canary(x_out, M * H)
     else:
         x = oracle.rms_norm(synth.normal((M, H), seed=M + 1), synth.norm_weight(H, seed=M + 1), 1e-5)
         mu.muser_qmatvec_group_scratch("q4_k", [dev(m) for m in mats], rows, H, dev(x), M, ys, scratch, nscr)
