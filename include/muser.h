@@ -249,9 +249,13 @@ int muser_qmatvec_group_scratch(int qtype, int n, const void* const* W, const in
  *   launch, every block for itself.  residual_out, residual and scratch as
  *   for muser_ffn_gate_up_silu_tail: a distinct residual_out takes the
  *   updated residual; NULL updates `residual` in place through the ticket in
- *   `scratch`.  With 2..16 rows of x the tail runs on its own, and scratch of
- *   at least muser_qmatvec_group_scratch_bytes(...) bytes takes the group's
- *   one tensor-core launch (as muser_qmatvec_group_scratch).
+ *   `scratch`.  With 2..16 rows of x the tail runs as a kernel of its own,
+ *   and scratch of at least muser_qmatvec_group_scratch_bytes(...) bytes
+ *   takes the group's one tensor-core launch (as
+ *   muser_qmatvec_group_scratch); when that launch reads its B operand from
+ *   an image in the scratch (Q4_K groups large enough to give every SM at
+ *   least 8 units of 128 rows x 256 inputs, cols <= 8192), the tail kernel
+ *   writes the image of x_out itself, saving the kernel that would build it.
  *   projected, residual, x_out (and residual_out): device f32 [M*cols],
  *   distinct; w1, w2: device f32 [cols]; cols % 4 == 0; eps1, eps2 > 0.
  */
