@@ -56,9 +56,9 @@ METRIC = "weight-stream GB/s (% of GB300 HBM peak); decode FFN tokens/sec, 1 GPU
 # was captured on (profiles/ summary); reported as null once the kernel changed.
 # The capture ran 4 layers; the traffic per layer is the same, so the 52-layer
 # launch's figure is 13 x the captured launch's.
-NCU_TRAFFIC = {"kernel": "mvs_kernel<Q4_K,Q6_K>", "bytes_per_launch": 13 * 1038113168, "layers": 52,
+NCU_TRAFFIC = {"kernel": "mvs_kernel<Q4_K,Q6_K>", "bytes_per_launch": 13 * 1038162688, "layers": 52,
                "captured_layers": 4,
-               "source_sha256": "ef3ed21e263bfc8d93a18ae77a54ffd47eabd21bd468d3863188bb0aa6ebd5aa",
+               "source_sha256": "064b9000264b591a7c1ed77c6aad4184a76070b4220ccd0c527787d0430ed589",
                "profile": "profiles/mvs_stack_m1_4layers.md"}
 
 
