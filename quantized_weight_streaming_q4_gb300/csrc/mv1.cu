@@ -181,9 +181,28 @@ __global__ void __launch_bounds__(512, 1) mv1_kernel(const Mv1Args p) {
             for (int k = 0; k < lead; ++k) issue(k, k + rot);
         __syncwarp();
         pdl_launch_dependents();
+        // One row group (the long rows of a down projection): while the
+        // consumers still wait for the previous kernel (x not yet requested),
+        // the stream need not idle, so each time the last request has landed
+        // the next free buffer is requested (bounded in time).  Measured
+        // faster for the stand-alone 6656 x 19968 down projections, slower
+        // for the shorter attention projections, which keep `lead`.
+        int issued = lead;
+        if (ONEG && lane == 0 && issued > 0) {
+            const uint64_t t0 = global_ns();
+            while (issued < early && !mbar_try_wait(xissued, 0, 0u)) {
+                if (mbar_try_wait(&full[issued - 1 + rot], 0, 200u)) {
+                    issue(issued, issued + rot);
+                    ++issued;
+                } else if (global_ns() - t0 > 1000000000ull) {
+                    break;
+                }
+            }
+        }
+        issued = __shfl_sync(0xffffffffu, issued, 0);
         ok = mbar_wait_bounded(xissued, 0, &g_device_status, kDevStatusWaitTimeout);
         if (ok && lane == 0)
-            for (int k = lead; k < early; ++k) issue(k, k + rot);
+            for (int k = issued; k < early; ++k) issue(k, k + rot);
         __syncwarp();
         // The rest of the first NS stages once the slots are free again.
         if (ok) ok = mbar_wait_bounded(xready, 0, &g_device_status, kDevStatusWaitTimeout);

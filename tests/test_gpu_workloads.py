@@ -359,6 +359,42 @@ def test_group_scratch_one_tensor_core_launch(M, case):
     assert mu.muser_device_status() == 0
 
 
+@pytest.mark.parametrize("form", ["residual_out", "in_place"])
+def test_group_tail_image_short_row_two_rows(form):
+    """The tail that writes the grouped launch's B image, at a row of 2,048
+    (one float4 per thread of its block) and the fewest rows of x (M = 2, so
+    14 of the image's 16 rows stay as the zero-filled scratch has them), on a
+    group of ragged Q4_K matrices large enough to take the image (8 units of
+    128 rows x 256 inputs per SM): residual, x_out and every output equal the
+    oracle's tail and matvecs; canaries stay; the scratch is left zeroed."""
+    M, cols = 2, 2048
+    rows = (9000, 4040, 5000, 1480)  # 155 tiles of 128 rows: 1,240 units over 8 super-blocks
+    mats = [synth.q4k_matrix(r, cols, seed=21, layer=i, tensor=synth.T_GATE) for i, r in enumerate(rows)]
+    nscr = mu.muser_qmatvec_group_scratch_bytes("q4_k", rows, cols, M)
+    assert nscr > 0
+    scratch = torch.zeros(nscr // 4 + 4, dtype=torch.float32, device="cuda")
+    r = synth.normal((M, cols), seed=22, workload=synth.ATTN_WORKLOAD, tensor=synth.T_X)
+    p = synth.normal((M, cols), seed=23, workload=synth.ATTN_WORKLOAD, tensor=synth.T_X) * np.float32(40.0)
+    w1 = synth.norm_weight(cols, seed=24, workload=synth.ATTN_WORKLOAD, tensor=synth.T_W1)
+    w2 = synth.norm_weight(cols, seed=24, workload=synth.ATTN_WORKLOAD, tensor=synth.T_W2)
+    rd, x_out = dev(r), nan_like((M, cols), extra=16)
+    r_out = nan_like((M, cols), extra=16) if form == "residual_out" else None
+    ys = [nan_like((M, n), extra=16) for n in rows]
+    mu.muser_qmatvec_group_tail("q4_k", [dev(m) for m in mats], rows, cols, dev(p), rd, dev(w1), dev(w2), 1e-8,
+                                1e-5, x_out, M, ys, scratch, nscr, residual_out=r_out)
+    r_ref, x = oracle.dual_tail(r, p, w1, w2, 1e-8, 1e-5)
+    got_r = host(rd).reshape(M, cols) if r_out is None else host(r_out[:M * cols]).reshape(M, cols)
+    assert_close(got_r, r_ref, "tail residual")
+    assert_close(host(x_out[:M * cols]).reshape(M, cols), x, "tail x_out")
+    check_canary(x_out, M * cols)
+    for i, (m, n, y) in enumerate(zip(mats, rows, ys)):
+        assert_close(host(y[:M * n]).reshape(M, n), oracle.qmatvec("q4_k", m, n, cols, x),
+                     f"matrix {i} after the image-writing tail", scaled=True)
+        check_canary(y, M * n)
+    assert not host(scratch).any(), "scratch must be left zeroed"
+    assert mu.muser_device_status() == 0
+
+
 def test_group_scratch_edges():
     """muser_qmatvec_group_scratch refuses scratch below its size before any
     launch; the group tail at several rows with only the 256-byte ticket scratch
