@@ -185,8 +185,9 @@ __global__ void __launch_bounds__(512, 1) mv1_kernel(const Mv1Args p) {
         // consumers still wait for the previous kernel (x not yet requested),
         // the stream need not idle, so each time the last request has landed
         // the next free buffer is requested (bounded in time).  Measured
-        // faster for the stand-alone 6656 x 19968 down projections, slower
-        // for the shorter attention projections, which keep `lead`.
+        // faster for the stand-alone 6656 x 19968 down projections; with the
+        // previous tail in the prologue the extra requests delay the tail's
+        // loads (slower), and the shorter plain projections gain nothing.
         int issued = lead;
         if (ONEG && lane == 0 && issued > 0) {
             const uint64_t t0 = global_ns();
