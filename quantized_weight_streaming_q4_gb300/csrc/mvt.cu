@@ -1203,8 +1203,11 @@ __global__ void __launch_bounds__(64) mvt_prep_kernel(const float* __restrict__ 
 // shared memory: quad (sb, q) of the first four warps converts quarter q of
 // block sb as the prep kernel does.  Rows of the image past M stay as the
 // zero-filled scratch has them, which the matvec reads as rows of zeros.
+// 512 threads, so that a thread may hold the conversion's 64 inputs in
+// registers (with 1,024 it spilled).
+constexpr int kTailImageThreads = 512;
 template <int QT, int V>
-__global__ void __launch_bounds__(1024) mvt_tail_image_kernel(float* resid, const float* src, float* out,
+__global__ void __launch_bounds__(kTailImageThreads) mvt_tail_image_kernel(float* resid, const float* src, float* out,
                                                               const float* w1, const float* w2, int n, float eps1,
                                                               float eps2, uint8_t* img) {
     extern __shared__ __align__(16) float xrow[];  // n floats
@@ -1215,7 +1218,7 @@ __global__ void __launch_bounds__(1024) mvt_tail_image_kernel(float* resid, cons
     dual_tail_row_reg<V>(resid + off, src + off, out + off, w1, w2, n, eps1, eps2, red, xv);
 #pragma unroll
     for (int u = 0; u < V; ++u) {
-        const int i = tid + u * 1024;
+        const int i = tid + u * kTailImageThreads;
         if (i < n4) reinterpret_cast<float4*>(xrow)[i] = xv[u];
     }
     __syncthreads();
@@ -1583,11 +1586,11 @@ int launch_mvt_tail_image(int qtype, int nmat, int64_t rows, int64_t cols, int M
     MvtGeo g;
     (void)mvt_geometry(qtype, nmat, rows, cols, M, g, false, true);
     uint8_t* img = image_of(scratch, g.ntiles);
-    const int n = static_cast<int>(cols), v = (n / 4 + 1023) / 1024;
+    const int n = static_cast<int>(cols), v = (n / 4 + kTailImageThreads - 1) / kTailImageThreads;
     const size_t smem = sizeof(float) * static_cast<size_t>(n);
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(static_cast<unsigned>(M));
-    cfg.blockDim = dim3(1024);
+    cfg.blockDim = dim3(kTailImageThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
@@ -1596,16 +1599,11 @@ int launch_mvt_tail_image(int qtype, int nmat, int64_t rows, int64_t cols, int M
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     cudaError_t e;
+    auto kern = [&](auto k) { return cudaLaunchKernelEx(&cfg, k, resid, src, out, w1, w2, n, eps1, eps2, img); };
     if (qtype == MUSER_Q4_K)
-        e = v <= 1 ? cudaLaunchKernelEx(&cfg, mvt_tail_image_kernel<MUSER_Q4_K, 1>, resid, src, out, w1, w2, n, eps1,
-                                        eps2, img)
-                   : cudaLaunchKernelEx(&cfg, mvt_tail_image_kernel<MUSER_Q4_K, 2>, resid, src, out, w1, w2, n, eps1,
-                                        eps2, img);
+        e = v <= 2 ? kern(mvt_tail_image_kernel<MUSER_Q4_K, 2>) : kern(mvt_tail_image_kernel<MUSER_Q4_K, 4>);
     else
-        e = v <= 1 ? cudaLaunchKernelEx(&cfg, mvt_tail_image_kernel<MUSER_Q6_K, 1>, resid, src, out, w1, w2, n, eps1,
-                                        eps2, img)
-                   : cudaLaunchKernelEx(&cfg, mvt_tail_image_kernel<MUSER_Q6_K, 2>, resid, src, out, w1, w2, n, eps1,
-                                        eps2, img);
+        e = v <= 2 ? kern(mvt_tail_image_kernel<MUSER_Q6_K, 2>) : kern(mvt_tail_image_kernel<MUSER_Q6_K, 4>);
     if (e != cudaSuccess) return cuda_fail(e, "mvt_tail_image: cudaLaunchKernelEx");
     return check_launch("mvt_tail_image");
 }
