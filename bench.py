@@ -1052,7 +1052,7 @@ def run_down_tail(args, rank, world):
                    "l2": f"inputs larger than L2: {nl * wbytes / 1e9:.2f} GB of distinct weights per step "
                          "vs 129 MB L2",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
-        "matvec_tail_per_s": round(world * nl / (ms * 1e-3), 1),
+        ("matvecs_per_s" if q5 else "matvec_tail_per_s"): round(world * nl / (ms * 1e-3), 1),
         "hbm_frac_of_" + peak_kind: round(gbs / world / peak, 4),
         "roofline": {"bound": "hbm", "kernel": (f"muser_qmatvec (mv1 {qname}, store)" if q5 else
                                                 f"muser_qmatvec_residual_dual_rmsnorm (mv1 {qname}, one-pass "
